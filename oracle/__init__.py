@@ -1,0 +1,192 @@
+"""CPU oracle for the DSA decode path -- TEST INFRASTRUCTURE ONLY.
+
+Python marshalling for ``dsa_oracle.c`` (plain single-threaded fp64 C).  Only
+the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline /
+reference leg may import this package; the product path never does.
+
+Functions take numpy arrays (or CPU torch tensors) and return numpy arrays.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dsa_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+KEYS_BF16, KEYS_E4M3_ROW = 0, 1
+LATENT_BF16, LATENT_DS_MLA = 0, 2
+ERRORS = {-1: "bad argument", -2: "query position outside the context", -3: "page or row outside the cache",
+          -4: "selected index outside the context", -5: "out of memory"}
+
+
+def compile_oracle(src: str, out: str) -> str:
+    """gcc, fp64, no FMA contraction (so x86 and Arm round the same way)."""
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-Wall", "-ffp-contract=off", "-shared", "-fPIC",
+                           "-I", _HERE, "-o", tmp, src, "-lm"])
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < max(
+            os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "dsa_oracle.h"))):
+        compile_oracle(_SRC, _LIB)
+    return _LIB
+
+
+def load(path: str):
+    """A handle on another build of the oracle (e.g. a deliberately broken
+    copy in a test); pass it as ``L=`` to the functions below."""
+    return _bind(path)
+
+
+class Seqs(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("ctx_len", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
+                ("page_size", ctypes.c_int32), ("max_pages", ctypes.c_int32), ("seq_base", ctypes.c_void_p),
+                ("num_rows", ctypes.c_int64)]
+
+
+def _bind(path: str):
+    L = ctypes.CDLL(path)
+    P, I32, I64, D = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+    L.oracle_bf16_value.argtypes, L.oracle_bf16_value.restype = [ctypes.c_uint16], D
+    L.oracle_e4m3_value.argtypes, L.oracle_e4m3_value.restype = [ctypes.c_uint8], D
+    L.oracle_ds_mla_row.argtypes, L.oracle_ds_mla_row.restype = [P, P], ctypes.c_int
+    L.oracle_index_scores.argtypes = [I32, P, P, P, P, P, P, P, I32, P, P, ctypes.POINTER(Seqs), P, I64]
+    L.oracle_index_scores.restype = ctypes.c_int
+    L.oracle_topk.argtypes, L.oracle_topk.restype = [P, I32, I32, P, ctypes.POINTER(I32)], ctypes.c_int
+    L.oracle_sparse_mla.argtypes = [P, I32, P, ctypes.POINTER(Seqs), I32, P, I32, D, P, P, P]
+    L.oracle_sparse_mla.restype = ctypes.c_int
+    L.oracle_latent_row_bytes.argtypes, L.oracle_latent_row_bytes.restype = [I32], I64
+    L.oracle_index_row_bytes.argtypes, L.oracle_index_row_bytes.restype = [I32], I64
+    return L
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = _bind(_LIB)
+    return _lib
+
+
+def _np(x, dtype=None):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor
+        import torch
+        x = x.detach().cpu()
+        if x.dtype == torch.bfloat16:
+            x = x.view(torch.int16)
+        x = x.numpy()
+    a = np.ascontiguousarray(x)
+    if dtype is not None:
+        a = a.view(dtype) if a.dtype.itemsize == np.dtype(dtype).itemsize and a.dtype != dtype else a.astype(dtype, copy=False)
+    return a
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _check(rc):
+    if rc != 0:
+        raise ValueError(f"oracle: {ERRORS.get(rc, rc)}")
+
+
+class Layout:
+    """Host copy of where tokens live; keeps the arrays alive for the call."""
+
+    def __init__(self, ctx_len, num_rows, page_table=None, page_size=0, seq_base=None):
+        self.ctx_len = _np(ctx_len, np.int32)
+        self.page_table = None if page_table is None else _np(page_table, np.int32)
+        self.seq_base = None if seq_base is None else _np(seq_base, np.int64)
+        self.page_size = int(page_size)
+        self.max_pages = 0 if self.page_table is None else int(self.page_table.shape[-1])
+        self.num_rows = int(num_rows)
+        if self.page_table is None and self.seq_base is None:
+            raise ValueError("need page_table or seq_base")
+
+    def struct(self):
+        return Seqs(len(self.ctx_len), _ptr(self.ctx_len), _ptr(self.page_table), self.page_size, self.max_pages,
+                    _ptr(self.seq_base), self.num_rows)
+
+
+def bf16_value(bits: int, L=None) -> float:
+    return (L or lib()).oracle_bf16_value(bits & 0xFFFF)
+
+
+def e4m3_value(code: int, L=None) -> float:
+    return (L or lib()).oracle_e4m3_value(code & 0xFF)
+
+
+def ds_mla_row(row656, L=None) -> np.ndarray:
+    r = _np(row656, np.uint8)
+    assert r.size == 656
+    out = np.empty(576, np.float64)
+    _check((L or lib()).oracle_ds_mla_row(_ptr(r), _ptr(out)))
+    return out
+
+
+def latent_row_bytes(kind: int, L=None) -> int:
+    return (L or lib()).oracle_latent_row_bytes(kind)
+
+
+def index_row_bytes(kind: int, L=None) -> int:
+    return (L or lib()).oracle_index_row_bytes(kind)
+
+
+def index_scores(q, w, ssmax_s, ssmax_b, inv_freq, q_seq, q_pos, keys, layout: Layout, key_scale=None,
+                 ld=None, L=None) -> np.ndarray:
+    """fp64 scores [nq, ld]; -inf after each query's position."""
+    q = _np(q, np.uint16)
+    w = _np(w, np.float32)
+    ss, sb = _np(ssmax_s, np.float32), _np(ssmax_b, np.float32)
+    fr = None if inv_freq is None else _np(inv_freq, np.float32)
+    qs, qp = _np(q_seq, np.int32), _np(q_pos, np.int32)
+    if key_scale is None:
+        k, kind, ks = _np(keys, np.uint16), KEYS_BF16, None
+    else:
+        k, kind, ks = _np(keys, np.uint8), KEYS_E4M3_ROW, _np(key_scale, np.float32)
+    nq = qp.shape[0]
+    ld = int(layout.ctx_len.max()) if ld is None else int(ld)
+    out = np.full((nq, ld), -np.inf, np.float64)
+    st = layout.struct()
+    _check((L or lib()).oracle_index_scores(nq, _ptr(q), _ptr(w), _ptr(ss), _ptr(sb), _ptr(fr), _ptr(qs), _ptr(qp), kind,
+                                     _ptr(k), _ptr(ks), ctypes.byref(st), _ptr(out), ld))
+    return out
+
+
+def topk(scores, k: int, L=None):
+    """(idx int32 [k] in selection order, -1 padded; length)."""
+    s = _np(scores, np.float64)
+    idx = np.empty(k, np.int32)
+    n = ctypes.c_int32()
+    _check((L or lib()).oracle_topk(_ptr(s), s.shape[0], k, _ptr(idx), ctypes.byref(n)))
+    return idx, int(n.value)
+
+
+def sparse_mla(q, latent, layout: Layout, seq: int, idx, topk_len: int, sm_scale: float, fp8: bool = False,
+               want_probs: bool = False, L=None):
+    """(out fp64 [64,512], lse fp64 [64], probs [64, topk_len] or None)."""
+    qq = _np(q, np.uint16)
+    lat = _np(latent, np.uint8 if fp8 else np.uint16)
+    ii = _np(idx, np.int32)
+    out = np.empty((64, 512), np.float64)
+    lse = np.empty(64, np.float64)
+    probs = np.empty((64, max(topk_len, 1)), np.float64) if want_probs else None
+    st = layout.struct()
+    _check((L or lib()).oracle_sparse_mla(_ptr(qq), LATENT_DS_MLA if fp8 else LATENT_BF16, _ptr(lat), ctypes.byref(st),
+                                   seq, _ptr(ii), topk_len, sm_scale, _ptr(out), _ptr(lse), _ptr(probs)))
+    return out, lse, (probs[:, :topk_len] if want_probs else None)

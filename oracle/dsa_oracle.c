@@ -1,0 +1,284 @@
+/* dsa_oracle.c -- CPU oracle for the DSA decode path (TEST INFRASTRUCTURE ONLY).
+ *
+ * Plain fp64, single-threaded, no blocking, fusion or reordering beyond the
+ * definitions on the pages.  Only the tests, the package smoke check and the
+ * benchmark's CPU-baseline leg use it.  See dsa_oracle.h for the sources.
+ *
+ * Parity pins live in tests/test_oracle.py (closed forms, invariants, special
+ * cases, brute force on tiny inputs).
+ */
+#include "dsa_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { IH = 32, ID = 128, RP = 32, MH = 64, MD = 576, MV = 512 };
+
+/* bf16 is the upper 16 bits of an IEEE-754 binary32. */
+double oracle_bf16_value(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* OCP 8-bit floating point, E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa
+ * bits; exponent 0 is subnormal (2^-6 * m/8); no infinities; S.1111.111 is
+ * NaN; largest finite 448.  The fp8 caches store this format
+ * ([vLLM-ML4] Sparse MLA + DSA indexer; FP8 latent cache). */
+double oracle_e4m3_value(uint8_t code) {
+    int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, 1 - 7);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* fp8_ds_mla row, 656 bytes per token per layer ([vLLM-ML4] Sparse MLA + DSA
+ * indexer: 41,328 latent bytes per token = 63 cache-owning layers x 656; FP8
+ * latent cache: 656 for fp8_ds_mla).  Byte order taken here: [0,512) e4m3
+ * latent codes, [512,528) four little-endian fp32 scales, one per 128 latent
+ * dims, [528,656) the 64 RoPE dims as bf16. */
+int oracle_ds_mla_row(const uint8_t* row, double* out) {
+    float scale[4];
+    for (int g = 0; g < 4; ++g) memcpy(&scale[g], row + MV + 4 * g, 4);
+    for (int d = 0; d < MV; ++d) out[d] = oracle_e4m3_value(row[d]) * (double)scale[d / 128];
+    for (int r = 0; r < MD - MV; ++r) {
+        uint16_t b;
+        memcpy(&b, row + MV + 16 + 2 * r, 2);
+        out[MV + r] = oracle_bf16_value(b);
+    }
+    return 0;
+}
+
+int64_t oracle_latent_row_bytes(int32_t kind) {
+    if (kind == ORACLE_LATENT_BF16) return 2 * MD; /* 1,152 */
+    if (kind == ORACLE_LATENT_DS_MLA) return MV + 4 * 4 + 2 * (MD - MV); /* 656 */
+    return -1;
+}
+
+int64_t oracle_index_row_bytes(int32_t kind) {
+    if (kind == ORACLE_KEYS_BF16) return 2 * ID;        /* 256 */
+    if (kind == ORACLE_KEYS_E4M3_ROW) return ID + 4;    /* 132 */
+    return -1;
+}
+
+/* Physical row of token j of sequence b, or -1. */
+static int64_t phys_row(const oracle_seqs* s, int32_t b, int64_t j) {
+    int64_t row;
+    if (s->page_table) {
+        int64_t p = j / s->page_size;
+        if (p >= s->max_pages) return -1;
+        int64_t page = s->page_table[(int64_t)b * s->max_pages + p];
+        if (page < 0) return -1;
+        row = page * s->page_size + j % s->page_size;
+    } else {
+        row = s->seq_base[b] + j;
+    }
+    if (row < 0 || row >= s->num_rows) return -1;
+    return row;
+}
+
+static void decode_key(int32_t kind, const void* keys, const float* key_scale, int64_t row, double* k) {
+    if (kind == ORACLE_KEYS_BF16) {
+        const uint16_t* p = (const uint16_t*)keys + row * ID;
+        for (int d = 0; d < ID; ++d) k[d] = oracle_bf16_value(p[d]);
+    } else {
+        const uint8_t* p = (const uint8_t*)keys + row * ID;
+        double sc = (double)key_scale[row];
+        for (int d = 0; d < ID; ++d) k[d] = oracle_e4m3_value(p[d]) * sc;
+    }
+}
+
+/* Lightning-indexer score of one query against every causal key.
+ *
+ * [colibri] What differs from GLM-5.2 -- SSMax: every head's query is
+ * multiplied by s*log(position+1)+b with the head's own s and b, in the
+ * indexer too (natural log, 0-based absolute position).  The indexer: q and k
+ * are rotated on their first 64 dims on RoPE layers (the cached keys are
+ * stored already rotated at their own positions, so only q rotates here); the
+ * score is relu(q.k/sqrt(128)) weighted by w/sqrt(32), summed over the 32
+ * index heads ([vLLM-ML4] Model architecture: 32 index heads).  RoPE and the
+ * rest: interleaved pairs (2i, 2i+1), i < 32, rotated by pos*inv_freq_i where
+ * inv_freq already holds the YaRN frequency divided by the pair's learned
+ * LeRoPE factor ([vLLM-ML4] NoPE, SSMax and LeRoPE: LeRoPE is folded into the
+ * YaRN frequencies).  NoPE layers: no rotation (inv_freq == NULL). */
+static int score_query(const uint16_t* q, const float* w, const float* ss, const float* sb,
+                       const float* inv_freq, int32_t b, int32_t pos, int32_t kind, const void* keys,
+                       const float* key_scale, const oracle_seqs* seqs, double* out) {
+    double qh[IH][ID];
+    double k[ID];
+    for (int h = 0; h < IH; ++h) {
+        double f = (double)ss[h] * log((double)pos + 1.0) + (double)sb[h];
+        for (int d = 0; d < ID; ++d) qh[h][d] = f * oracle_bf16_value(q[h * ID + d]);
+        if (inv_freq) {
+            for (int i = 0; i < RP; ++i) {
+                double th = (double)pos * (double)inv_freq[i];
+                double c = cos(th), s = sin(th);
+                double x0 = qh[h][2 * i], x1 = qh[h][2 * i + 1];
+                qh[h][2 * i] = x0 * c - x1 * s;
+                qh[h][2 * i + 1] = x0 * s + x1 * c;
+            }
+        }
+    }
+    for (int64_t j = 0; j <= pos; ++j) {
+        int64_t row = phys_row(seqs, b, j);
+        if (row < 0) return ORACLE_ERR_PAGE;
+        decode_key(kind, keys, key_scale, row, k);
+        double total = 0.0;
+        for (int h = 0; h < IH; ++h) {
+            double dot = 0.0;
+            for (int d = 0; d < ID; ++d) dot += qh[h][d] * k[d];
+            double r = dot / sqrt(128.0);
+            if (r < 0.0) r = 0.0;
+            total += (double)w[h] * r / sqrt(32.0);
+        }
+        out[j] = total;
+    }
+    return 0;
+}
+
+int oracle_index_scores(int32_t nq, const uint16_t* q, const float* w, const float* ssmax_s,
+                        const float* ssmax_b, const float* inv_freq, const int32_t* q_seq,
+                        const int32_t* q_pos, int32_t key_kind, const void* keys, const float* key_scale,
+                        const oracle_seqs* seqs, double* scores, int64_t ld) {
+    if (nq < 0 || !q || !w || !ssmax_s || !ssmax_b || !q_seq || !q_pos || !keys || !seqs || !scores)
+        return ORACLE_ERR_ARG;
+    if (key_kind != ORACLE_KEYS_BF16 && key_kind != ORACLE_KEYS_E4M3_ROW) return ORACLE_ERR_ARG;
+    if (key_kind == ORACLE_KEYS_E4M3_ROW && !key_scale) return ORACLE_ERR_ARG;
+    for (int32_t t = 0; t < nq; ++t) {
+        int32_t b = q_seq[t], pos = q_pos[t];
+        if (b < 0 || b >= seqs->num_seqs) return ORACLE_ERR_ARG;
+        if (pos < 0 || pos >= seqs->ctx_len[b] || seqs->ctx_len[b] > ld) return ORACLE_ERR_POS;
+    }
+    for (int32_t t = 0; t < nq; ++t) {
+        int32_t b = q_seq[t], pos = q_pos[t];
+        double* row = scores + (int64_t)t * ld;
+        int rc = score_query(q + (int64_t)t * IH * ID, w + (int64_t)t * IH, ssmax_s, ssmax_b, inv_freq, b, pos,
+                             key_kind, keys, key_scale, seqs, row);
+        if (rc) return rc;
+        for (int64_t j = (int64_t)pos + 1; j < seqs->ctx_len[b]; ++j) row[j] = -INFINITY;
+    }
+    return 0;
+}
+
+typedef struct {
+    double s;
+    int32_t j;
+} scored;
+
+/* score descending, then index ascending */
+static int by_score(const void* a, const void* b) {
+    const scored* x = (const scored*)a;
+    const scored* y = (const scored*)b;
+    if (x->s > y->s) return -1;
+    if (x->s < y->s) return 1;
+    return (x->j > y->j) - (x->j < y->j);
+}
+
+/* Exact top-k: the keys with the k largest scores ([vLLM-ML4] Highlights and
+ * Model architecture: top-k 2048 keys per query; Specialized decode: an exact
+ * top-2048).  Ties at the boundary go to the smaller index (a reading; the
+ * pages name no rule).  Fewer than k causal keys: all of them, the rest of
+ * the slots -1 ([vLLM-ML4] DCP: top-k compaction, topk_length and slots full
+ * of -1). */
+int oracle_topk(const double* scores, int32_t n, int32_t k, int32_t* idx, int32_t* len) {
+    if (n < 0 || k < 0 || (!scores && n) || (!idx && k) || !len) return ORACLE_ERR_ARG;
+    scored* v = (scored*)malloc(sizeof(scored) * (size_t)(n ? n : 1));
+    if (!v) return ORACLE_ERR_NOMEM;
+    for (int32_t j = 0; j < n; ++j) {
+        v[j].s = scores[j];
+        v[j].j = j;
+    }
+    qsort(v, (size_t)n, sizeof(scored), by_score);
+    int32_t m = n < k ? n : k;
+    for (int32_t i = 0; i < k; ++i) idx[i] = i < m ? v[i].j : -1;
+    *len = m;
+    free(v);
+    return 0;
+}
+
+/* Absorbed-MLA attention over the selected latent rows.
+ *
+ * [vLLM-ML4] Model architecture: 64 heads, MLA with KV LoRA rank 512 and RoPE
+ * dim 64, so each token holds one shared 576-dim latent row (512 latent + 64
+ * RoPE) that serves as the key of every head; in absorbed form the value is
+ * the 512 latent dims and the output stays in latent space.  Sparse MLA + DSA
+ * indexer: attention reads only the indexer's selected tokens.  For head h:
+ * s_j = sm_scale * q_h . c_j over the 576 dims, p = softmax(s) over the
+ * selected j, O_h = sum_j p_j c_j[0:512], LSE_h = log sum_j exp(s_j).  An
+ * empty selection gives O = 0 and LSE = -inf ([vLLM-ML4] DCP: a fused kernel
+ * neutralises empty rows).  NoPE layers are MLA with zero RoPE dims ([vLLM-ML4]
+ * NoPE, SSMax and LeRoPE): their inputs carry zeros in dims 512..575. */
+int oracle_sparse_mla(const uint16_t* q, int32_t latent_kind, const void* latent, const oracle_seqs* seqs,
+                      int32_t seq, const int32_t* idx, int32_t topk_len, double sm_scale, double* out,
+                      double* lse, double* probs) {
+    if (!q || !latent || !seqs || !out || !lse || topk_len < 0 || (topk_len && !idx)) return ORACLE_ERR_ARG;
+    if (latent_kind != ORACLE_LATENT_BF16 && latent_kind != ORACLE_LATENT_DS_MLA) return ORACLE_ERR_ARG;
+    if (seq < 0 || seq >= seqs->num_seqs) return ORACLE_ERR_ARG;
+    int64_t row_bytes = oracle_latent_row_bytes(latent_kind);
+    double* c = (double*)malloc(sizeof(double) * MD * (size_t)(topk_len ? topk_len : 1));
+    int32_t* slot = (int32_t*)malloc(sizeof(int32_t) * (size_t)(topk_len ? topk_len : 1));
+    double* s = (double*)malloc(sizeof(double) * (size_t)(topk_len ? topk_len : 1));
+    if (!c || !slot || !s) {
+        free(c); free(slot); free(s);
+        return ORACLE_ERR_NOMEM;
+    }
+    int32_t n = 0;
+    for (int32_t i = 0; i < topk_len; ++i) {
+        int32_t j = idx[i];
+        if (j < 0) continue;
+        if (j >= seqs->ctx_len[seq]) {
+            free(c); free(slot); free(s);
+            return ORACLE_ERR_INDEX;
+        }
+        int64_t row = phys_row(seqs, seq, j);
+        if (row < 0) {
+            free(c); free(slot); free(s);
+            return ORACLE_ERR_PAGE;
+        }
+        double* cj = c + (int64_t)n * MD;
+        if (latent_kind == ORACLE_LATENT_BF16) {
+            const uint16_t* p = (const uint16_t*)latent + row * MD;
+            for (int d = 0; d < MD; ++d) cj[d] = oracle_bf16_value(p[d]);
+        } else {
+            oracle_ds_mla_row((const uint8_t*)latent + row * row_bytes, cj);
+        }
+        slot[n++] = i;
+    }
+    double qd[MD];
+    if (probs) memset(probs, 0, sizeof(double) * (size_t)MH * (size_t)topk_len);
+    for (int h = 0; h < MH; ++h) {
+        for (int d = 0; d < MD; ++d) qd[d] = oracle_bf16_value(q[h * MD + d]);
+        double* oh = out + (int64_t)h * MV;
+        for (int d = 0; d < MV; ++d) oh[d] = 0.0;
+        if (n == 0) {
+            lse[h] = -INFINITY;
+            continue;
+        }
+        double mx = -INFINITY;
+        for (int32_t j = 0; j < n; ++j) {
+            double dot = 0.0;
+            for (int d = 0; d < MD; ++d) dot += qd[d] * c[(int64_t)j * MD + d];
+            s[j] = sm_scale * dot;
+            if (s[j] > mx) mx = s[j];
+        }
+        double l = 0.0;
+        for (int32_t j = 0; j < n; ++j) l += exp(s[j] - mx);
+        for (int32_t j = 0; j < n; ++j) {
+            double p = exp(s[j] - mx) / l;
+            if (probs) probs[(int64_t)h * topk_len + slot[j]] = p;
+            const double* cj = c + (int64_t)j * MD;
+            for (int d = 0; d < MV; ++d) oh[d] += p * cj[d];
+        }
+        lse[h] = mx + log(l);
+    }
+    free(c);
+    free(slot);
+    free(s);
+    return 0;
+}

@@ -1,0 +1,89 @@
+/* dsa_oracle.h -- CPU oracle for the DSA decode path (TEST INFRASTRUCTURE ONLY).
+ *
+ * A plain, slow, single-threaded fp64 statement of what one decode layer of a
+ * Mistral-Large-4-style DeepSeek Sparse Attention stack computes: the
+ * lightning-indexer scores, the exact top-k selection and absorbed-MLA
+ * attention over the selected latent rows.  Only the test suite, the package
+ * smoke check and the CPU-baseline leg of the benchmark may load it.  It shares
+ * no code, header, table or helper with the CUDA library.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [vLLM-ML4]  "Day 0 support for Mistral Large 4" (vLLM blog),
+ *               Implementation details: Model architecture table; Sparse MLA +
+ *               DSA indexer; NoPE, SSMax and LeRoPE; DCP (top-k compaction);
+ *               ROCm implementation details: FP8 latent cache.
+ *   [colibri]   "Mistral-Large-4 (c/colibri.c)" (colibri docs,
+ *               mistral-large4.md), What differs from GLM-5.2: NoPE layers;
+ *               SSMax; The indexer; RoPE and the rest.
+ *
+ * Every pointer is host memory owned by the caller.  Functions return 0 on
+ * success and a negative code on a bad argument (nothing is written then).
+ */
+#ifndef DSA_ORACLE_H
+#define DSA_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* key storage kinds */
+#define ORACLE_KEYS_BF16 0        /* [rows,128] bf16 bits                          */
+#define ORACLE_KEYS_E4M3_ROW 1    /* [rows,128] e4m3 codes + [rows] fp32 scale      */
+/* latent storage kinds */
+#define ORACLE_LATENT_BF16 0      /* [rows,576] bf16 bits                           */
+#define ORACLE_LATENT_DS_MLA 2    /* [rows,656] bytes: 512 e4m3, 4 fp32, 64 bf16    */
+
+#define ORACLE_ERR_ARG (-1)
+#define ORACLE_ERR_POS (-2)       /* query position outside [0, ctx_len)            */
+#define ORACLE_ERR_PAGE (-3)      /* page id / row outside the cache                */
+#define ORACLE_ERR_INDEX (-4)     /* selected index outside [0, ctx_len)            */
+#define ORACLE_ERR_NOMEM (-5)
+
+/* Where each sequence's tokens live.  Token j of sequence b is physical row
+ * page_table[b*max_pages + j/page_size]*page_size + j%page_size when
+ * page_table is non-NULL, else seq_base[b] + j. */
+typedef struct {
+    int32_t num_seqs;
+    const int32_t* ctx_len;     /* [num_seqs] */
+    const int32_t* page_table;  /* [num_seqs*max_pages] or NULL */
+    int32_t page_size;
+    int32_t max_pages;
+    const int64_t* seq_base;    /* [num_seqs], used when page_table == NULL */
+    int64_t num_rows;           /* rows in every cache, for bounds checks */
+} oracle_seqs;
+
+double oracle_bf16_value(uint16_t bits);
+double oracle_e4m3_value(uint8_t code);
+int oracle_ds_mla_row(const uint8_t* row656, double* out576);
+
+/* Indexer scores of nq queries.  scores[t*ld + j] for j <= q_pos[t]; the rest
+ * of the row up to ctx_len is set to -INFINITY. */
+int oracle_index_scores(int32_t nq, const uint16_t* q /*[nq,32,128]*/, const float* w /*[nq,32]*/,
+                        const float* ssmax_s, const float* ssmax_b /*[32]*/,
+                        const float* inv_freq /*[32] or NULL = NoPE*/,
+                        const int32_t* q_seq, const int32_t* q_pos /*[nq]*/,
+                        int32_t key_kind, const void* keys, const float* key_scale,
+                        const oracle_seqs* seqs, double* scores, int64_t ld);
+
+/* Exact top-k of n scores: the min(k, n) largest, ties to the smaller index.
+ * idx[0..len) in selection order (score descending, index ascending), the
+ * rest of idx[0..k) set to -1. */
+int oracle_topk(const double* scores, int32_t n, int32_t k, int32_t* idx, int32_t* len);
+
+/* Absorbed-MLA attention of one query over the selected tokens of its
+ * sequence: slots idx[0..topk_len) that are >= 0.  out [64,512], lse [64]
+ * (natural log); probs [64, topk_len] (per slot, 0 for skipped slots) or NULL. */
+int oracle_sparse_mla(const uint16_t* q /*[64,576]*/, int32_t latent_kind, const void* latent,
+                      const oracle_seqs* seqs, int32_t seq, const int32_t* idx, int32_t topk_len,
+                      double sm_scale, double* out, double* lse, double* probs);
+
+/* Row sizes in bytes of the stored formats, per token per layer. */
+int64_t oracle_latent_row_bytes(int32_t latent_kind);
+int64_t oracle_index_row_bytes(int32_t key_kind);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,520 @@
+"""Pins of the CPU oracle to facts other than itself.
+
+Each ``pin_*`` takes a handle on a build of the oracle (``oracle.lib()`` or a
+deliberately broken copy) and raises AssertionError when the build disagrees
+with a closed form, an invariant, a library routine on a special case, or a
+byte count printed on the pages.  ``tests/test_oracle.py`` runs them on the
+real oracle; ``tests/test_oracle_mutants.py`` checks that every planted
+mistake fails at least one of them.
+
+Sources: "Day 0 support for Mistral Large 4" (vLLM blog) and the colibri
+"Mistral-Large-4" doc (What differs from GLM-5.2).
+"""
+
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------------------
+# helpers
+def bf16_bits(x) -> np.ndarray:
+    """Round fp64/fp32 values to bf16 bit patterns (nearest even) with numpy."""
+    f = np.asarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    return r
+
+
+def contiguous(ctx_len, rows):
+    base = np.concatenate([[0], np.cumsum(ctx_len)[:-1]]).astype(np.int64)
+    return oracle.Layout(np.asarray(ctx_len, np.int32), rows, seq_base=base)
+
+
+def index_case(n=16, pos=None, rope=False, seed=1):
+    """Random small indexer inputs: one query in one sequence of n keys."""
+    rng = np.random.default_rng(seed)
+    q = bf16_bits(rng.standard_normal((1, 32, 128)))
+    w = rng.standard_normal((1, 32)).astype(np.float32)
+    s = np.full(32, 0.0, np.float32)
+    b = np.full(32, 1.0, np.float32)
+    inv = (0.5 ** np.arange(32)).astype(np.float32) if rope else None
+    keys = bf16_bits(rng.standard_normal((n, 128)))
+    pos = n - 1 if pos is None else pos
+    return dict(q=q, w=w, ssmax_s=s, ssmax_b=b, inv_freq=inv, q_seq=np.array([0], np.int32),
+                q_pos=np.array([pos], np.int32), keys=keys)
+
+
+def scores_of(L, c, layout=None, **over):
+    d = dict(c)
+    d.update(over)
+    lay = layout or contiguous([d["keys"].shape[0]], d["keys"].shape[0])
+    return oracle.index_scores(d["q"], d["w"], d["ssmax_s"], d["ssmax_b"], d["inv_freq"], d["q_seq"], d["q_pos"],
+                               d["keys"], lay, key_scale=d.get("key_scale"), L=L)[0]
+
+
+def close(a, b, tol=1e-12):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    assert a.shape == b.shape, (a.shape, b.shape)
+    fin = np.isfinite(b)
+    assert np.array_equal(np.isfinite(a), fin), "finite pattern differs"
+    assert np.array_equal(a[~fin], b[~fin]), "non-finite values differ"
+    err = np.max(np.abs(a[fin] - b[fin]), initial=0.0)
+    assert err <= tol * max(1.0, np.max(np.abs(b[fin]), initial=0.0)), f"max err {err}"
+
+
+# ---------------------------------------------------------------------------
+# formats
+def pin_bf16_decode(L):
+    """bf16 = top half of binary32: every 16-bit pattern against torch."""
+    import torch
+    codes = np.arange(1 << 16, dtype=np.uint16)
+    ref = torch.from_numpy(codes.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([oracle.bf16_value(int(c), L=L) for c in codes[::97]] + [oracle.bf16_value(0x3F80, L=L)])
+    want = np.concatenate([ref[::97], [1.0]])
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    m = ~np.isnan(want)
+    assert np.array_equal(got[m], want[m])
+
+
+def pin_e4m3_decode(L):
+    """OCP E4M3: all 256 codes against torch.float8_e4m3fn, plus the format's
+    landmarks (1.0 = 0x38, max 448 = 0x7E, min subnormal 2^-9 = 0x01, NaN = 0x7F)."""
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_value(int(c), L=L) for c in codes])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    m = ~np.isnan(ref)
+    assert np.array_equal(got[m], ref[m])
+    assert oracle.e4m3_value(0x38, L=L) == 1.0 and oracle.e4m3_value(0x7E, L=L) == 448.0
+    assert oracle.e4m3_value(0x01, L=L) == 2.0 ** -9 and oracle.e4m3_value(0x80 | 0x38, L=L) == -1.0
+    assert math.isnan(oracle.e4m3_value(0x7F, L=L)) and math.isnan(oracle.e4m3_value(0xFF, L=L))
+
+
+def pin_kv_bytes(L):
+    """Per-token cache bytes printed on the pages (tests/golden/kv_bytes.json)."""
+    with open(os.path.join(GOLDEN, "kv_bytes.json")) as f:
+        g = json.load(f)
+    lat8 = oracle.latent_row_bytes(oracle.LATENT_DS_MLA, L=L)
+    lat16 = oracle.latent_row_bytes(oracle.LATENT_BF16, L=L)
+    idx8 = oracle.index_row_bytes(oracle.KEYS_E4M3_ROW, L=L)
+    n_lat, n_idx = g["cache_owning_layers"], g["indexer_layers"]
+    assert n_lat * lat8 == g["latent_bytes_fp8_ds_mla"]
+    assert n_idx * idx8 == g["indexer_bytes_fp8"]
+    assert n_lat * lat8 + n_idx * idx8 == g["total_bytes_fp8"]
+    assert lat8 == g["fp8_ds_mla_row"] and lat16 == g["bf16_row"] and idx8 == g["indexer_row"]
+    assert n_lat * lat16 + n_idx * idx8 == g["total_bytes_bf16"]
+    assert n_lat * g["plain_e4m3_row"] + n_idx * idx8 == g["total_bytes_plain_e4m3"]
+
+
+def pin_ds_mla_row(L):
+    """fp8_ds_mla row decode: group g of 128 latent dims uses scale g; RoPE
+    dims are bf16 after the 16 scale bytes."""
+    row = np.zeros(656, np.uint8)
+    row[:512] = 0x38                                   # e4m3 1.0 everywhere
+    row[5] = 0xB8                                      # -1.0
+    row[300] = 0x40                                    # 2.0
+    scales = np.array([1.0, 2.0, 4.0, 0.5], np.float32)
+    row[512:528] = np.frombuffer(scales.tobytes(), np.uint8)
+    rope = np.arange(64, dtype=np.float32) - 31.5      # exact in bf16
+    row[528:656] = np.frombuffer(bf16_bits(rope).tobytes(), np.uint8)
+    got = oracle.ds_mla_row(row, L=L)
+    want = np.concatenate([np.repeat(scales.astype(np.float64), 128), rope.astype(np.float64)])
+    want[5] = -1.0
+    want[300] = 2.0 * 4.0
+    assert np.array_equal(got, want)
+
+
+# ---------------------------------------------------------------------------
+# indexer score
+def _one_head_case(n=8, head=3, weight=2.0, pos=None):
+    rng = np.random.default_rng(7)
+    c = index_case(n=n, pos=pos)
+    q = bf16_bits(rng.standard_normal((1, 32, 128)))
+    q[0, head, :] = 0
+    q[0, head, :8] = bf16_bits(np.ones(8))            # q_h = 1 on dims 0..7
+    w = np.zeros((1, 32), np.float32)
+    w[0, head] = weight
+    keys = np.zeros((n, 128), np.float32)
+    keys[:, :8] = (np.arange(n) - 2.0)[:, None]        # k_j = j-2 on dims 0..7
+    keys[:, 8:] = rng.standard_normal((n, 120))        # q_h is 0 there
+    c.update(q=q, w=w, keys=bf16_bits(keys))
+    return c
+
+
+def pin_score_single_head(L):
+    """One head weighted 2, f = 1, q.k = 8(j-2): score = 2 relu(8(j-2)/sqrt(128))/sqrt(32) = max(j-2,0)/4."""
+    c = _one_head_case()
+    got = scores_of(L, c)
+    want = np.maximum(np.arange(8) - 2.0, 0.0) / 4.0
+    close(got, want, 1e-14)
+
+
+def pin_score_negative_weight(L):
+    """The weight multiplies relu(...), it is not inside it: w = -2 gives -max(j-2,0)/4."""
+    c = _one_head_case(weight=-2.0)
+    close(scores_of(L, c), -np.maximum(np.arange(8) - 2.0, 0.0) / 4.0, 1e-14)
+
+
+def pin_ssmax_scale(L):
+    """SSMax f = s*ln(pos+1) + b multiplies the query before relu:
+    f > 0 scales the score, f < 0 mirrors the relu."""
+    c = _one_head_case(pos=7)
+    s = np.zeros(32, np.float32)
+    b = np.zeros(32, np.float32)
+    s[3], b[3] = 0.5, -0.25
+    f = float(np.float32(0.5)) * math.log(8.0) + float(np.float32(-0.25))
+    base = np.maximum(np.arange(8) - 2.0, 0.0) / 4.0
+    close(scores_of(L, c, ssmax_s=s, ssmax_b=b), f * base, 1e-13)
+    # negative f: relu(f x) = |f| relu(-x): keys 0,1 (q.k < 0) now count
+    s[3], b[3] = 0.0, -1.0
+    close(scores_of(L, c, ssmax_s=s, ssmax_b=b), np.maximum(2.0 - np.arange(8), 0.0) / 4.0, 1e-14)
+    # position 0: ln 1 = 0 so f = b whatever s is
+    c0 = _one_head_case(pos=0)
+    s[3], b[3] = 100.0, 3.0
+    got = scores_of(L, c0, ssmax_s=s, ssmax_b=b)
+    assert got[0] == 0.0 and np.all(np.isneginf(got[1:]))
+
+
+def pin_causal_mask(L):
+    """Keys after the query position are -inf; the position itself scores."""
+    c = _one_head_case(n=8, pos=4)
+    got = scores_of(L, c)
+    assert np.all(np.isneginf(got[5:])) and np.all(np.isfinite(got[:5]))
+    assert abs(got[4] - 0.5) < 1e-14
+
+
+def pin_rope_interleaved(L):
+    """Interleaved pairs: q with pair i = (1, 0) rotated by theta = pos*inv_freq_i
+    becomes (cos, sin); against a key (0, 1) on that pair the dot is sin(theta).
+    A half-split rotation or the opposite direction gives 0 here."""
+    n, pos, pair, head = 6, 3, 5, 0
+    c = index_case(n=n, pos=pos, rope=True)
+    inv = (0.1 * (np.arange(32) + 1)).astype(np.float32)
+    inv[pair] = 0.5
+    q = np.zeros((1, 32, 128), np.uint16)
+    q[0, head, 2 * pair] = bf16_bits(1.0)
+    w = np.zeros((1, 32), np.float32)
+    w[0, head] = 64.0                                  # cancels 1/(sqrt(128) sqrt(32))
+    keys = np.zeros((n, 128), np.float32)
+    keys[:, 2 * pair + 1] = 1.0
+    got = scores_of(L, c, q=q, w=w, keys=bf16_bits(keys), inv_freq=inv)
+    th = pos * float(inv[pair])
+    want = np.full(n, -np.inf)
+    want[:pos + 1] = max(math.sin(th), 0.0)
+    assert math.sin(th) > 0.5
+    close(got, want, 1e-14)
+    # the cosine component lands on dim 2*pair
+    keys = np.zeros((n, 128), np.float32)
+    keys[:, 2 * pair] = 1.0
+    got = scores_of(L, c, q=q, w=w, keys=bf16_bits(keys), inv_freq=inv)
+    want[:pos + 1] = max(math.cos(th), 0.0)
+    close(got, want, 1e-14)
+
+
+def pin_rope_first_64_only(L):
+    """Dims 64..127 are never rotated: a query and key on dim 100 only give
+    the same score at any position and frequency."""
+    n = 5
+    q = np.zeros((1, 32, 128), np.uint16)
+    q[0, 9, 100] = bf16_bits(1.5)
+    w = np.zeros((1, 32), np.float32)
+    w[0, 9] = 64.0
+    keys = np.zeros((n, 128), np.float32)
+    keys[:, 100] = np.arange(n) + 1.0
+    inv = np.full(32, 0.7, np.float32)
+    for pos in (0, 4):
+        c = index_case(n=n, pos=pos, rope=True)
+        got = scores_of(L, c, q=q, w=w, keys=bf16_bits(keys), inv_freq=inv)
+        want = np.full(n, -np.inf)
+        want[:pos + 1] = 1.5 * (np.arange(pos + 1) + 1.0)
+        close(got, want, 1e-14)
+
+
+def pin_nope_is_zero_frequency(L):
+    """NoPE equals RoPE with every frequency 0 (angle 0), on random data."""
+    c = index_case(n=40, rope=True, seed=3)
+    a = scores_of(L, c, inv_freq=None)
+    b = scores_of(L, c, inv_freq=np.zeros(32, np.float32))
+    close(a, b, 0.0)
+
+
+def pin_rope_rotation_invariance(L):
+    """Rotating the key by the query's own angles (same pairs) leaves the
+    unrotated score: R(theta) q . R(theta) k = q . k.  Checked with exact
+    rotations by multiples of pi/2 (cos, sin in {0, +-1})."""
+    c = index_case(n=12, pos=11, rope=False, seed=5)
+    base = scores_of(L, c)
+    # theta_i = pos * inv_freq_i = 11 * (pi/2 * m_i / 11) -> quarter turns m_i
+    m = np.arange(32) % 4
+    inv = (np.pi / 2 * m / 11.0).astype(np.float32)
+    th = 11.0 * inv.astype(np.float64)
+    cs, sn = np.round(np.cos(th)), np.round(np.sin(th))
+    assert np.allclose(np.cos(th), cs, atol=1e-6)
+    k = np.array([oracle.bf16_value(int(v), L=L) for v in c["keys"].ravel()]).reshape(12, 128)
+    kr = k.copy()
+    kr[:, 0:64:2] = k[:, 0:64:2] * cs - k[:, 1:64:2] * sn
+    kr[:, 1:64:2] = k[:, 0:64:2] * sn + k[:, 1:64:2] * cs
+    got = scores_of(L, c, inv_freq=inv, keys=bf16_bits(kr))
+    # the fp32 angle is not exactly a quarter turn: allow its tiny residue
+    close(got, base, 1e-5)
+
+
+def pin_linear_in_weights(L):
+    """The score is linear in the head weights."""
+    c = index_case(n=30, rope=True, seed=11)
+    rng = np.random.default_rng(2)
+    w1 = rng.standard_normal((1, 32)).astype(np.float32)
+    w2 = rng.standard_normal((1, 32)).astype(np.float32)
+    a = scores_of(L, c, w=w1)
+    b = scores_of(L, c, w=w2)
+    ab = scores_of(L, c, w=(w1.astype(np.float64) + w2).astype(np.float32))
+    close(ab[np.isfinite(ab)], (a + b)[np.isfinite(ab)], 1e-6)
+
+
+def pin_paged_equals_contiguous(L):
+    """A page table gives the same scores as the rows gathered in order."""
+    rng = np.random.default_rng(4)
+    ps, n = 4, 22
+    pages = (n + ps - 1) // ps
+    perm = rng.permutation(pages + 3)[:pages].astype(np.int32)
+    phys = rng.standard_normal(((pages + 3) * ps, 128))
+    keys_phys = bf16_bits(phys)
+    logical = np.concatenate([keys_phys[p * ps:(p + 1) * ps] for p in perm])[:n]
+    c = index_case(n=n, rope=True, seed=9)
+    paged = oracle.Layout(np.array([n], np.int32), keys_phys.shape[0], page_table=perm[None, :], page_size=ps)
+    a = scores_of(L, c, keys=keys_phys, layout=paged)
+    b = scores_of(L, c, keys=logical)
+    close(a, b, 0.0)
+
+
+def pin_fp8_keys_equal_their_values(L):
+    """e4m3 keys times a power-of-two row scale score like bf16 keys holding
+    the same values (all exact in bf16)."""
+    rng = np.random.default_rng(6)
+    n = 17
+    codes = rng.integers(0, 256, (n, 128)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3C               # no NaN codes
+    scale = (2.0 ** rng.integers(-6, 3, n)).astype(np.float32)
+    vals = np.array([[oracle.e4m3_value(int(x), L=L) for x in r] for r in codes]) * scale[:, None]
+    c = index_case(n=n, rope=True, seed=12)
+    a = scores_of(L, c, keys=codes, key_scale=scale)
+    b = scores_of(L, c, keys=bf16_bits(vals))
+    close(a, b, 0.0)
+
+
+def pin_multi_query_sequences(L):
+    """Two sequences, two queries each: each query reads only its own
+    sequence's keys up to its own position."""
+    rng = np.random.default_rng(13)
+    ctx = [9, 6]
+    keys = bf16_bits(rng.standard_normal((15, 128)))
+    lay = contiguous(ctx, 15)
+    q = bf16_bits(rng.standard_normal((4, 32, 128)))
+    w = rng.standard_normal((4, 32)).astype(np.float32)
+    s = (0.1 * np.ones(32)).astype(np.float32)
+    b = np.ones(32, np.float32)
+    inv = (0.3 ** np.arange(32)).astype(np.float32)
+    qseq = np.array([0, 0, 1, 1], np.int32)
+    qpos = np.array([7, 8, 4, 5], np.int32)
+    allq = oracle.index_scores(q, w, s, b, inv, qseq, qpos, keys, lay, L=L)
+    for t in range(4):
+        bb = int(qseq[t])
+        sub = keys[sum(ctx[:bb]):sum(ctx[:bb]) + ctx[bb]]
+        one = oracle.index_scores(q[t:t + 1], w[t:t + 1], s, b, inv, np.array([0], np.int32), qpos[t:t + 1], sub,
+                                  contiguous([ctx[bb]], ctx[bb]), ld=9, L=L)[0]
+        close(allq[t], one, 0.0)
+
+
+# ---------------------------------------------------------------------------
+# top-k
+def pin_topk_library(L):
+    """Exact top-k against numpy's lexsort (score descending, index
+    ascending) on scores with many ties."""
+    rng = np.random.default_rng(21)
+    for n, k in ((50, 8), (300, 64), (64, 64), (10, 30), (1, 1), (5, 0)):
+        s = rng.integers(-5, 6, n).astype(np.float64) * 0.25
+        idx, m = oracle.topk(s, k, L=L)
+        order = np.lexsort((np.arange(n), -s))
+        assert m == min(n, k)
+        assert np.array_equal(idx[:m], order[:m].astype(np.int32))
+        assert np.all(idx[m:] == -1)
+
+
+def pin_topk_properties(L):
+    """Every selected score >= every unselected one; among scores equal to
+    the k-th, the selected indices are the smallest."""
+    rng = np.random.default_rng(22)
+    n, k = 1000, 100
+    s = np.round(rng.standard_normal(n), 1)
+    idx, m = oracle.topk(s, k, L=L)
+    sel = np.zeros(n, bool)
+    sel[idx[:m]] = True
+    assert sel.sum() == k
+    assert s[sel].min() >= s[~sel].max()
+    kth = s[sel].min()
+    eq = np.flatnonzero(s == kth)
+    assert np.array_equal(np.flatnonzero(sel & (s == kth)), eq[:np.count_nonzero(sel & (s == kth))])
+
+
+def pin_topk_short_context(L):
+    """Context <= k: the selection is every causal key; the other slots -1."""
+    s = np.random.default_rng(23).standard_normal(37)
+    idx, m = oracle.topk(s, 2048, L=L)
+    assert m == 37 and sorted(idx[:m].tolist()) == list(range(37)) and np.all(idx[m:] == -1)
+
+
+# ---------------------------------------------------------------------------
+# sparse MLA
+def mla_case(n=12, seed=31):
+    rng = np.random.default_rng(seed)
+    q = bf16_bits(rng.standard_normal((64, 576)))
+    lat = bf16_bits(rng.standard_normal((n, 576)))
+    return q, lat, contiguous([n], n)
+
+
+def _vals(L, bits):
+    return np.array([oracle.bf16_value(int(v), L=L) for v in np.asarray(bits).ravel()]).reshape(np.shape(bits))
+
+
+def pin_mla_one_key(L):
+    """One selected key: every head outputs that key's 512 latent dims and
+    LSE = sm_scale * q_h . c_j over all 576 dims."""
+    q, lat, lay = mla_case()
+    qv, lv = _vals(L, q), _vals(L, lat)
+    idx = np.array([7, -1, -1], np.int32)
+    out, lse, _ = oracle.sparse_mla(q, lat, lay, 0, idx, 3, 0.125, L=L)
+    close(out, np.tile(lv[7, :512], (64, 1)), 0.0)
+    close(lse, 0.125 * (qv @ lv[7]), 1e-12)
+
+
+def pin_mla_two_keys_rope_dims(L):
+    """Two keys that differ only in the 64 RoPE dims: the score uses all 576
+    dims, softmax is over keys, LSE = log(e^s1 + e^s2) (natural log)."""
+    q = np.zeros((64, 576), np.uint16)
+    lat = np.zeros((2, 576), np.float32)
+    lat[0, :512] = 1.0
+    lat[1, :512] = -1.0
+    lat[0, 512:] = 0.25
+    lat[1, 512:] = -0.5
+    h = np.arange(64)
+    qf = np.zeros((64, 576), np.float32)
+    qf[:, 512:] = ((h % 7) - 3.0)[:, None] / 8.0
+    q = bf16_bits(qf)
+    lay = contiguous([2], 2)
+    out, lse, p = oracle.sparse_mla(q, bf16_bits(lat), lay, 0, np.array([0, 1], np.int32), 2, 0.5,
+                                    want_probs=True, L=L)
+    a = 0.5 * 64 * 0.25 * ((h % 7) - 3.0) / 8.0
+    b = 0.5 * 64 * -0.5 * ((h % 7) - 3.0) / 8.0
+    p0 = 1.0 / (1.0 + np.exp(b - a))
+    close(out, np.repeat((p0 * 1.0 + (1 - p0) * -1.0)[:, None], 512, 1), 1e-13)
+    close(lse, np.logaddexp(a, b), 1e-13)
+    close(p[:, 0], p0, 1e-13)
+
+
+def pin_mla_uniform_scores(L):
+    """q = 0: equal weights, O = mean of the selected rows, LSE = ln n."""
+    _, lat, lay = mla_case(n=20)
+    lv = _vals(L, lat)
+    idx = np.array([3, 9, 4, 17, -1, 0], np.int32)
+    out, lse, p = oracle.sparse_mla(np.zeros((64, 576), np.uint16), lat, lay, 0, idx, 6, 1.0, want_probs=True, L=L)
+    sel = [3, 9, 4, 17, 0]
+    close(out, np.tile(lv[sel, :512].mean(0), (64, 1)), 1e-14)
+    close(lse, np.full(64, math.log(5.0)), 1e-14)
+    assert np.all(p[:, 4] == 0.0)
+
+
+def pin_mla_softmax_sums_to_one(L):
+    """Softmax weights of every head sum to 1 (|sum - 1| <= 1e-12)."""
+    q, lat, lay = mla_case(n=300, seed=33)
+    idx = np.random.default_rng(1).permutation(300)[:257].astype(np.int32)
+    _, _, p = oracle.sparse_mla(q, lat, lay, 0, idx, 257, 1.0 / math.sqrt(192), want_probs=True, L=L)
+    assert np.max(np.abs(p.sum(1) - 1.0)) <= 1e-12
+    assert np.all(p >= 0)
+
+
+def pin_mla_empty(L):
+    """No selected key: O = 0, LSE = -inf (an empty row is neutral)."""
+    q, lat, lay = mla_case()
+    out, lse, _ = oracle.sparse_mla(q, lat, lay, 0, np.full(4, -1, np.int32), 4, 1.0, L=L)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+    out, lse, _ = oracle.sparse_mla(q, lat, lay, 0, np.full(4, 2, np.int32), 0, 1.0, L=L)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+def pin_mla_library_softmax(L):
+    """Against scipy.special.softmax/logsumexp with numpy matmuls (library
+    routines on a small random case)."""
+    from scipy.special import logsumexp, softmax
+    q, lat, lay = mla_case(n=40, seed=34)
+    qv, lv = _vals(L, q), _vals(L, lat)
+    idx = np.arange(0, 40, 3, dtype=np.int32)
+    sc = 1.0 / math.sqrt(192)
+    out, lse, _ = oracle.sparse_mla(q, lat, lay, 0, idx, len(idx), sc, L=L)
+    s = sc * qv @ lv[idx].T
+    close(out, softmax(s, axis=1) @ lv[idx, :512], 1e-12)
+    close(lse, logsumexp(s, axis=1), 1e-12)
+
+
+def pin_mla_sparse_equals_dense(L):
+    """Context <= k: top-k selects every causal key, so sparse attention over
+    the selection equals dense attention over all keys (order-free)."""
+    q, lat, lay = mla_case(n=50, seed=35)
+    s = np.random.default_rng(3).standard_normal(50)
+    idx, m = oracle.topk(s, 2048, L=L)
+    a, la, _ = oracle.sparse_mla(q, lat, lay, 0, idx, 2048, 0.07, L=L)
+    b, lb, _ = oracle.sparse_mla(q, lat, lay, 0, np.arange(50, dtype=np.int32), 50, 0.07, L=L)
+    close(a, b, 1e-12)
+    close(la, lb, 1e-12)
+
+
+def pin_mla_fp8_equals_values(L):
+    """fp8_ds_mla rows score and average like bf16 rows holding the same
+    dequantised values (power-of-two scales keep them exact)."""
+    rng = np.random.default_rng(36)
+    n = 24
+    rows = np.zeros((n, 656), np.uint8)
+    codes = rng.integers(0, 256, (n, 512)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x30
+    rows[:, :512] = codes
+    sc = (2.0 ** rng.integers(-4, 2, (n, 4))).astype(np.float32)
+    rows[:, 512:528] = np.frombuffer(sc.tobytes(), np.uint8).reshape(n, 16)
+    rope = bf16_bits(rng.standard_normal((n, 64)))
+    rows[:, 528:] = np.frombuffer(rope.tobytes(), np.uint8).reshape(n, 128)
+    vals = np.stack([oracle.ds_mla_row(r, L=L) for r in rows])
+    q = bf16_bits(rng.standard_normal((64, 576)))
+    lay = contiguous([n], n)
+    idx = rng.permutation(n)[:15].astype(np.int32)
+    a, la, _ = oracle.sparse_mla(q, rows, lay, 0, idx, 15, 0.1, fp8=True, L=L)
+    b, lb, _ = oracle.sparse_mla(q, bf16_bits(vals), lay, 0, idx, 15, 0.1, L=L)
+    close(a, b, 0.0)
+    close(la, lb, 0.0)
+
+
+def pin_mla_paged(L):
+    """Selected tokens go through the page table."""
+    rng = np.random.default_rng(37)
+    ps, n = 8, 30
+    pages = 4
+    perm = np.array([5, 0, 3, 1], np.int32)
+    phys = bf16_bits(rng.standard_normal((6 * ps, 576)))
+    logical = np.concatenate([phys[p * ps:(p + 1) * ps] for p in perm])[:n]
+    q = bf16_bits(rng.standard_normal((64, 576)))
+    idx = np.array([29, 0, 8, 17, 25, 3], np.int32)
+    paged = oracle.Layout(np.array([n], np.int32), phys.shape[0], page_table=perm[None, :pages], page_size=ps)
+    a, la, _ = oracle.sparse_mla(q, phys, paged, 0, idx, 6, 0.1, L=L)
+    b, lb, _ = oracle.sparse_mla(q, logical, contiguous([n], n), 0, idx, 6, 0.1, L=L)
+    close(a, b, 0.0)
+    close(la, lb, 0.0)
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
