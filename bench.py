@@ -1,0 +1,416 @@
+#!/usr/bin/env python3
+"""Benchmark of one DSA decode layer (indexer -> exact top-2048 -> sparse MLA).
+
+Prints ONE JSON line.  A step is one pass of the whole layer (query prep,
+indexer scan, top-k, sparse absorbed-MLA attention, LSE combine; plus the
+shared-indexer layer where the workload has one) over one batch of synthetic
+decode queries, with the caches resident in HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload paged]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+metric: decode queries/s per layer (whole job over all ranks); the dominant
+kernel's HBM roofline fraction is reported beside it.  Under torchrun (N > 1)
+every rank runs its own full copy of the workload (independent sequences, no
+data-path collective): weak scaling.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from dsa_sparse_mla_query_gb300 import inputs as I  # noqa: E402
+
+METRIC = "decode queries/s per layer (indexer+top-k+sparse MLA)"
+UNIT = "queries/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="paged", choices=sorted(I.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak-s", type=float, default=1.0, help="untimed load before the timed region (clocks)")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (per launch / per step), see DESIGN.md "Roofline"
+def index_row_bytes(wl):
+    return 132 if wl.index_fp8 else 256
+
+
+def latent_row_bytes(wl):
+    return 656 if wl.latent_fp8 else 1152
+
+
+def algorithmic_bytes(wl, lay):
+    ctx = lay.ctx_len
+    Q = wl.num_queries
+    keys = sum(ctx) * index_row_bytes(wl)
+    scores = sum(lay.ctx_len[b] for b in lay.q_seq) * 4
+    qside = Q * (32 * 128 * 2 + 32 * 4)
+    indexer = keys + scores + qside
+    sel = sum(min(p + 1, wl.topk) for p in lay.q_pos)
+    layers = 2 if wl.shared_layer else 1
+    gather = sel * latent_row_bytes(wl) * layers
+    mla_small = layers * Q * (64 * 576 * 2 + 64 * 512 * 2 + 64 * 4) + Q * wl.topk * 4
+    return dict(indexer=indexer, gather=gather, step=keys + qside + gather + mla_small)
+
+
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(gpu_index), "-lms", "50"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        mhz, max_mhz, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1 + 0.1):
+                continue
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                mhz.append(float(f[2]))
+                max_mhz = float(f[3])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[6:10]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": max_mhz, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max_mhz, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def indexer_traffic(wl_name: str):
+    """dram bytes per launch of the indexer kernel from the committed ncu
+    summary, if the kernel sources still hash the same; else None."""
+    p = os.path.join(ROOT, "profiles", "indexer_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        j = json.load(f)
+    if j.get("source_sha256") != kernel_source_hash() or wl_name not in j.get("per_launch_bytes", {}):
+        return None
+    return j["per_launch_bytes"][wl_name]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("indexer.cu", "dsa_internal.cuh"):
+        with open(os.path.join(ROOT, "dsa_sparse_mla_query_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline / reference arm)
+def oracle_sample(wl, n_queries: int):
+    """Per sampled query: host inputs for the oracle, generated on the CPU by
+    the seeded generator (same values as the device copy).  The latent rows
+    are generated for the oracle's own selection only."""
+    import numpy as np
+    import oracle
+    lay = I.make_layout(wl)
+    s, b, inv = I.params(wl)
+    Q = wl.num_queries
+    picks = [int(x) for x in np.linspace(0, Q - 1, n_queries)]
+    jobs = []
+    for t in picks:
+        bq = lay.q_seq[t]
+        rows = lay.phys_rows(bq)
+        cache = I.make_cache_rows(wl, rows, "cpu", which="index")
+        q = I.make_queries(wl, "cpu", t, 1)
+        jobs.append(dict(t=t, pos=lay.q_pos[t], ctx=lay.ctx_len[bq], rows=rows, keys=cache["k_idx"],
+                         k_scale=cache.get("k_scale"), q=q, s=s, b=b, inv=inv))
+    # the latent rows the oracle will select: run its indexer once here
+    for j in jobs:
+        olay = oracle.Layout(np.array([j["ctx"]], np.int32), j["ctx"], seq_base=np.zeros(1, np.int64))
+        sc = oracle.index_scores(j["q"]["q_idx"], j["q"]["w"], j["s"], j["b"], j["inv"], np.zeros(1, np.int32),
+                                 np.array([j["pos"]], np.int32), j["keys"], olay, key_scale=j["k_scale"])[0]
+        sel, m = oracle.topk(sc[:j["pos"] + 1], wl.topk)
+        j["lat"] = I.make_cache_rows(wl, j["rows"][torch.from_numpy(sel[:m].astype(np.int64))], "cpu",
+                                     which="latent")
+        j["m"] = m
+        j["olay"] = olay
+    return jobs
+
+
+def oracle_run(wl, job):
+    """The oracle's whole layer for one query (indexer, top-k, attention)."""
+    import numpy as np
+    import oracle
+    sc = oracle.index_scores(job["q"]["q_idx"], job["q"]["w"], job["s"], job["b"], job["inv"], np.zeros(1, np.int32),
+                             np.array([job["pos"]], np.int32), job["keys"], job["olay"], key_scale=job["k_scale"])[0]
+    sel, m = oracle.topk(sc[:job["pos"] + 1], wl.topk)
+    m = job["m"]
+    mlay = oracle.Layout(np.array([m], np.int32), m, seq_base=np.zeros(1, np.int64))
+    oracle.sparse_mla(job["q"]["q_mla"][0], job["lat"]["latent"], mlay, 0, np.arange(m, dtype=np.int32), m,
+                      1.0 / math.sqrt(192.0), fp8=wl.latent_fp8)
+    if wl.shared_layer:
+        oracle.sparse_mla(job["q"]["q_mla2"][0], job["lat"]["latent2"], mlay, 0, np.arange(m, dtype=np.int32), m,
+                          1.0 / math.sqrt(192.0), fp8=wl.latent_fp8)
+
+
+def oracle_timed(wl, jobs, threads: int) -> float:
+    from concurrent.futures import ThreadPoolExecutor
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(lambda j: oracle_run(wl, j), jobs))
+    return time.perf_counter() - t0
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, wl, ws, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    threads = cpu_threads()
+    jobs = oracle_sample(wl, threads)
+    for _ in range(max(args.warmup, 0)):
+        oracle_timed(wl, jobs[:1], 1)
+    times = [oracle_timed(wl, jobs, threads) for _ in range(args.steps)]
+    total = sum(times)
+    value = len(jobs) * args.steps / total
+    sample = (f"{len(jobs)} queries per step (one per host thread), each the whole layer for one query of "
+              f"{wl.name}: indexer over its full causal context, top-{wl.topk}, attention")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.describe(), "queries_per_step": len(jobs)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def run_ours(args, wl, ws, rank, local):
+    from dsa_sparse_mla_query_gb300.runner import DecodeStep
+    import dsa_sparse_mla_query_gb300 as dsa
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dsa.load()
+    d = I.make_inputs(wl, dev)
+    lay = d["layout"]
+    step = DecodeStep(d, wl.queries_per_seq, wl.topk, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    K, W = args.steps, args.warmup
+
+    def events(n):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in ev:
+            e.record(stream)  # creates the underlying CUDA event
+        return ev
+
+    ev = [events(4) for _ in range(K)]
+    ev2 = [events(4) for _ in range(K)] if step.shared else [None] * K
+    for _ in range(W):
+        step.run(stream)
+    torch.cuda.synchronize(dev)
+    if step.device_status() != 0:
+        raise RuntimeError(f"device status {step.device_status()} after warm-up")
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    sampler = ClockSampler(local)
+    t_soak = time.time()
+    t_end_soak = t_soak + args.soak_s
+    while time.time() < t_end_soak:  # untimed load, so the clock samples see the timed region's state
+        for _ in range(20):
+            step.run(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(K):
+        step.run(stream, events=ev[i], events2=ev2[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t_done = time.time()
+    ms = start.elapsed_time(end)
+    clocks = sampler.stop(t_soak, t_done)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / K
+    value = ws * wl.num_queries / (ms_step / 1000.0)
+
+    stage = lambda i, a, b: ev[i][a].elapsed_time(ev[i][b])  # noqa: E731
+    idx_ms = statistics.mean(stage(i, 0, 1) for i in range(K))
+    topk_ms = statistics.mean(stage(i, 1, 2) for i in range(K))
+    mla_ms = statistics.mean(stage(i, 2, 3) for i in range(K))
+    mla2_ms = statistics.mean(ev2[i][2].elapsed_time(ev2[i][3]) for i in range(K)) if step.shared else 0.0
+
+    ab = algorithmic_bytes(wl, lay)
+    peak, peak_kind = measured_peaks()
+    achieved = ab["indexer"] / (idx_ms / 1000.0) / 1e9
+    traffic = indexer_traffic(wl.name)
+
+    # ---- end to end through the C ABI with host buffers
+    keys = ["q_idx", "w", "q_mla"] + (["q_mla2"] if step.shared else [])
+    host_in = {k: d[k].cpu().pin_memory() for k in keys}
+    host_pos = d["q_pos"].cpu().pin_memory()
+    outs = [step.out, step.lse, step.idx, step.topk_len] + ([step.out2, step.lse2] if step.shared else [])
+    host_out = [o.cpu().pin_memory() for o in outs]
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values()) + host_pos.numel() * 4
+    d2h = sum(o.numel() * o.element_size() for o in host_out)
+    Ke = max(1, K)
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        for k, v in host_in.items():
+            d[k].copy_(v, non_blocking=True)
+        d["q_pos"].copy_(host_pos, non_blocking=True)
+        step.run(stream)
+        for o, h in zip(outs, host_out):
+            h.copy_(o, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if step.device_status() != 0:
+        raise RuntimeError(f"device status {step.device_status()}")
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        threads = cpu_threads()
+        jobs = oracle_sample(wl, 2 * threads)
+        secs = oracle_timed(wl, jobs, threads)
+        cpu = {"value": len(jobs) / secs, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{len(jobs)} queries of {wl.name} spread over the batch, each the whole layer "
+                         f"(indexer over the full causal context, top-{wl.topk}, attention), "
+                         f"{threads} threads of the single-threaded fp64 oracle, {secs:.1f} s wall"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": W,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if not wl.index_fp8 else "e4m3/bf16", "data": "synthetic",
+            "config": {"workload": wl.describe(), "queries": wl.num_queries, "global_batch": ws * wl.num_queries,
+                       "l2": "inputs larger than L2 (index keys %.0f MB, latent cache %.0f MB per step window)"
+                             % (sum(lay.ctx_len) * index_row_bytes(wl) / 1e6,
+                                lay.num_rows * latent_row_bytes(wl) / 1e6),
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic, "kernel": "indexer (query prep + key scan)",
+                         "algorithmic_bytes_per_launch": ab["indexer"], "ms_per_launch": idx_ms,
+                         "peak_kind": f"{peak_kind} HBM copy"},
+            "layer": {"algorithmic_bytes_per_step": ab["step"],
+                      "achieved_gbs": ab["step"] / (ms_step / 1000.0) / 1e9,
+                      "frac_of_peak": ab["step"] / (ms_step / 1000.0) / 1e9 / peak,
+                      "stage_ms": {"indexer": idx_ms, "topk": topk_ms, "mla": mla_ms, "mla_shared_layer": mla2_ms},
+                      "keys_scanned_per_s": ws * sum(lay.ctx_len) / (ms_step / 1000.0)},
+            "e2e": {"value": ws * wl.num_queries / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": K * step.launches_per_step(),
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    wl = I.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if ws > 1 and rank != 0:
+            return
+        run_reference(args, wl, ws, rank)
+        return
+    if ws > 1:
+        torch.distributed.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+    try:
+        run_ours(args, wl, ws, rank, local)
+    finally:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

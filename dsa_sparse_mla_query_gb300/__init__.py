@@ -1,0 +1,26 @@
+"""GB300 (sm_103a) DSA decode path: lightning indexer -> exact top-k -> sparse
+absorbed-MLA attention, as hand-written CUDA behind a C ABI (include/dsa.h).
+
+The Python names mirror the C entry points; they only marshal arguments.
+Importing the package loads nothing; the first call loads ``libdsa.so`` and
+raises if it is not built.
+"""
+
+from ._binding import (  # noqa: F401
+    DSA_BF16,
+    DSA_FP8_DS_MLA,
+    DSA_FP8_E4M3_ROWSCALE,
+    DsaError,
+    Seqs,
+    dsa_decode_layer,
+    dsa_decode_layer_launches,
+    dsa_index_scores,
+    dsa_topk,
+    dsa_workspace_size,
+    load,
+    sparse_mla_decode,
+    version,
+)
+
+__all__ = ["Seqs", "DsaError", "dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode",
+           "dsa_decode_layer", "dsa_decode_layer_launches", "load", "version", "DSA_BF16", "DSA_FP8_E4M3_ROWSCALE", "DSA_FP8_DS_MLA"]

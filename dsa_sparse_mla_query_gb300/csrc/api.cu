@@ -1,0 +1,285 @@
+// api.cu -- the C ABI of include/dsa.h: host-side validation (default-deny,
+// every reason listed), workspace carving and the launch sequence.  No entry
+// point allocates, synchronises or reads device memory on the host.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <string>
+
+#include "dsa_internal.cuh"
+
+namespace dsa {
+namespace {
+
+thread_local char g_err[1024] = "";
+
+dsa_status fail(dsa_status st, const std::string& why) {
+    snprintf(g_err, sizeof g_err, "%s", why.c_str());
+    return st;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Collects every reason a call is refused, so one message lists them all.
+struct Check {
+    std::string why;
+    dsa_status st = DSA_OK;
+    void need(bool ok, dsa_status code, const char* fmt, ...) {
+        if (ok) return;
+        char buf[256];
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(buf, sizeof buf, fmt, ap);
+        va_end(ap);
+        if (!why.empty()) why += "; ";
+        why += buf;
+        if (st == DSA_OK || (st == DSA_ERR_UNSUPPORTED && code == DSA_ERR_INVALID_ARG)) st = code;
+    }
+    void ptr(const void* p, const char* name, size_t align = 16) {
+        need(p != nullptr, DSA_ERR_INVALID_ARG, "%s is NULL", name);
+        if (p) need(aligned(p, align), DSA_ERR_INVALID_ARG, "%s is not %zu-byte aligned", name, align);
+    }
+    dsa_status done() {
+        if (st != DSA_OK) return fail(st, why);
+        g_err[0] = 0;
+        return DSA_OK;
+    }
+};
+
+void check_seqs(Check& c, const dsa_seqs* s, int32_t num_q) {
+    c.need(s != nullptr, DSA_ERR_INVALID_ARG, "seqs is NULL");
+    if (!s) return;
+    c.need(s->num_seqs >= 1, DSA_ERR_INVALID_ARG, "num_seqs %d < 1", s->num_seqs);
+    c.need(s->max_ctx >= 1 && s->max_ctx <= (1 << 30), DSA_ERR_INVALID_ARG, "max_ctx %d outside [1, 2^30]",
+           s->max_ctx);
+    c.need(s->max_q_per_seq >= 1, DSA_ERR_INVALID_ARG, "max_q_per_seq %d < 1", s->max_q_per_seq);
+    c.need(num_q >= 0, DSA_ERR_INVALID_ARG, "num_q %d < 0", num_q);
+    c.need(s->num_rows >= 1, DSA_ERR_INVALID_ARG, "num_rows %lld < 1", (long long)s->num_rows);
+    c.ptr(s->ctx_len, "seqs.ctx_len", 4);
+    c.ptr(s->q_start, "seqs.q_start", 4);
+    c.ptr(s->q_pos, "seqs.q_pos", 4);
+    if (s->page_table) {
+        c.ptr(s->page_table, "seqs.page_table", 4);
+        c.need(s->page_size >= 16 && s->page_size % 16 == 0, DSA_ERR_UNSUPPORTED,
+               "page_size %d is not a positive multiple of 16", s->page_size);
+        c.need(s->max_pages >= 1, DSA_ERR_INVALID_ARG, "max_pages %d < 1", s->max_pages);
+    } else {
+        c.ptr(s->seq_base, "seqs.seq_base (page_table is NULL)", 8);
+    }
+}
+
+void check_workspace(Check& c, const dsa_seqs* s, int32_t num_q, int32_t k, const void* ws, size_t bytes) {
+    if (!s || c.st != DSA_OK) return;
+    int64_t ld;
+    const size_t need = workspace_bytes(*s, num_q, k, &ld);
+    c.need(ws != nullptr || need == 0, DSA_ERR_WORKSPACE, "workspace is NULL");
+    c.need(ws == nullptr || aligned(ws, 256), DSA_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+    c.need(bytes >= need, DSA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", bytes, need);
+}
+
+dsa_status cuda_status(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) {
+        g_err[0] = 0;
+        return DSA_OK;
+    }
+    return fail(DSA_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+}  // namespace
+
+size_t workspace_bytes(const dsa_seqs& s, int num_q, int k, int64_t* scores_ld) {
+    const int64_t ld = ((int64_t)s.max_ctx + 3) / 4 * 4;
+    if (scores_ld) *scores_ld = ld;
+    const int kk = k < 1 ? 1 : (k > DSA_MAX_TOPK ? DSA_MAX_TOPK : k);
+    const int splits = mla_splits(num_q > 0 ? num_q : 1, kk);
+    size_t b = 0;
+    b += up256((size_t)num_q * kIH * 192 * 2);                       // q'
+    b += up256((size_t)num_q * kIH * 4);                             // w'
+    b += up256((size_t)num_q * splits * kMH * kMV * 4);              // partial outputs
+    b += up256((size_t)num_q * splits * kMH * 2 * 4);                // partial (max, sum)
+    b += up256((size_t)num_q * ld * 4);                              // scores (fused layer)
+    return b;
+}
+
+Workspace carve_workspace(void* base, const dsa_seqs& s, int num_q, int k) {
+    Workspace w{};
+    int64_t ld;
+    workspace_bytes(s, num_q, k, &ld);
+    const int kk = k < 1 ? 1 : (k > DSA_MAX_TOPK ? DSA_MAX_TOPK : k);
+    const int splits = mla_splits(num_q > 0 ? num_q : 1, kk);
+    uint8_t* p = reinterpret_cast<uint8_t*>(base);
+    w.qprep = p;
+    p += up256((size_t)num_q * kIH * 192 * 2);
+    w.wprep = reinterpret_cast<float*>(p);
+    p += up256((size_t)num_q * kIH * 4);
+    w.mla_part = reinterpret_cast<float*>(p);
+    p += up256((size_t)num_q * splits * kMH * kMV * 4);
+    w.mla_ml = reinterpret_cast<float*>(p);
+    p += up256((size_t)num_q * splits * kMH * 2 * 4);
+    w.scores = reinterpret_cast<float*>(p);
+    w.scores_ld = ld;
+    return w;
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+const char* dsa_last_error_string(void) { return g_err; }
+
+const char* dsa_status_string(dsa_status s) {
+    switch (s) {
+        case DSA_OK: return "DSA_OK";
+        case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG";
+        case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED";
+        case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+        case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE";
+        case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT";
+        case DSA_ERR_BAD_INPUT: return "DSA_ERR_BAD_INPUT";
+    }
+    return "unknown dsa_status";
+}
+
+const char* dsa_version(void) { return "0.1.0"; }
+
+dsa_status dsa_workspace_size(const dsa_seqs* seqs, int32_t num_q, int32_t k, size_t* bytes) {
+    Check c;
+    check_seqs(c, seqs, num_q);
+    c.need(bytes != nullptr, DSA_ERR_INVALID_ARG, "bytes is NULL");
+    c.need(k >= 1 && k <= DSA_MAX_TOPK, DSA_ERR_UNSUPPORTED, "k %d outside [1, %d]", k, DSA_MAX_TOPK);
+    dsa_status st = c.done();
+    if (st != DSA_OK) return st;
+    *bytes = workspace_bytes(*seqs, num_q, k, nullptr);
+    return DSA_OK;
+}
+
+static void check_index_args(Check& c, const void* q_idx, const float* w, const float* ssmax_s, const float* ssmax_b,
+                             const float* inv_freq, const void* k_idx, const float* k_scale, dsa_dtype k_dtype) {
+    c.ptr(q_idx, "q_idx");
+    c.ptr(w, "w", 4);
+    c.ptr(ssmax_s, "ssmax_s", 4);
+    c.ptr(ssmax_b, "ssmax_b", 4);
+    if (inv_freq) c.ptr(inv_freq, "inv_freq", 4);
+    c.ptr(k_idx, "k_idx");
+    c.need(k_dtype == DSA_BF16 || k_dtype == DSA_FP8_E4M3_ROWSCALE, DSA_ERR_UNSUPPORTED,
+           "index key dtype %d is neither DSA_BF16 nor DSA_FP8_E4M3_ROWSCALE", (int)k_dtype);
+    if (k_dtype == DSA_FP8_E4M3_ROWSCALE) c.ptr(k_scale, "k_scale", 4);
+}
+
+dsa_status dsa_index_scores(const void* q_idx, const float* w, const float* ssmax_s, const float* ssmax_b,
+                            const float* inv_freq, const void* k_idx, const float* k_scale, dsa_dtype k_dtype,
+                            const dsa_seqs* seqs, int32_t num_q, float* scores, int64_t ld, void* workspace,
+                            size_t workspace_bytes, int32_t* d_status, cudaStream_t stream) {
+    Check c;
+    check_seqs(c, seqs, num_q);
+    check_index_args(c, q_idx, w, ssmax_s, ssmax_b, inv_freq, k_idx, k_scale, k_dtype);
+    c.ptr(scores, "scores");
+    if (seqs) c.need(ld >= seqs->max_ctx && ld % 4 == 0, DSA_ERR_INVALID_ARG, "ld %lld must be >= max_ctx and a multiple of 4", (long long)ld);
+    check_workspace(c, seqs, num_q, 1, workspace, workspace_bytes);
+    dsa_status st = c.done();
+    if (st != DSA_OK || num_q == 0) return st;
+    Workspace ws = carve_workspace(workspace, *seqs, num_q, 1);
+    return cuda_status(launch_index_scores(q_idx, w, ssmax_s, ssmax_b, inv_freq, k_idx, k_scale, k_dtype, *seqs,
+                                           num_q, scores, ld, ws, d_status, stream),
+                       "dsa_index_scores launch");
+}
+
+dsa_status dsa_topk(const float* scores, int64_t ld, const dsa_seqs* seqs, int32_t num_q, int32_t k, int32_t* idx,
+                    int32_t* topk_len, void* workspace, size_t workspace_bytes, int32_t* d_status,
+                    cudaStream_t stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    Check c;
+    check_seqs(c, seqs, num_q);
+    c.ptr(scores, "scores");
+    c.ptr(idx, "idx", 4);
+    c.ptr(topk_len, "topk_len", 4);
+    c.need(k >= 1 && k <= DSA_MAX_TOPK, DSA_ERR_UNSUPPORTED, "k %d outside [1, %d]", k, DSA_MAX_TOPK);
+    if (seqs) c.need(ld >= seqs->max_ctx && ld % 4 == 0, DSA_ERR_INVALID_ARG, "ld %lld must be >= max_ctx and a multiple of 4", (long long)ld);
+    dsa_status st = c.done();
+    if (st != DSA_OK || num_q == 0) return st;
+    return cuda_status(launch_topk(scores, ld, *seqs, num_q, k, idx, topk_len, d_status, stream), "dsa_topk launch");
+}
+
+static void check_mla_args(Check& c, const void* q, const void* latent, dsa_dtype latent_dtype, const int32_t* idx,
+                           const int32_t* topk_len, int32_t k, float sm_scale, const void* out, const float* lse) {
+    c.ptr(q, "q");
+    c.ptr(latent, "latent");
+    c.need(latent_dtype == DSA_BF16 || latent_dtype == DSA_FP8_DS_MLA, DSA_ERR_UNSUPPORTED,
+           "latent dtype %d is neither DSA_BF16 nor DSA_FP8_DS_MLA", (int)latent_dtype);
+    c.ptr(idx, "idx", 4);
+    c.ptr(topk_len, "topk_len", 4);
+    c.need(k >= 1 && k <= DSA_MAX_TOPK, DSA_ERR_UNSUPPORTED, "k %d outside [1, %d]", k, DSA_MAX_TOPK);
+    c.need(sm_scale > 0.f && sm_scale < 1e30f, DSA_ERR_INVALID_ARG, "sm_scale must be positive and finite");
+    c.ptr(out, "out");
+    if (lse) c.ptr(lse, "lse", 4);
+}
+
+dsa_status sparse_mla_decode(const void* q, const void* latent, dsa_dtype latent_dtype, const dsa_seqs* seqs,
+                             int32_t num_q, const int32_t* idx, const int32_t* topk_len, int32_t k, float sm_scale,
+                             void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* d_status,
+                             cudaStream_t stream) {
+    Check c;
+    check_seqs(c, seqs, num_q);
+    check_mla_args(c, q, latent, latent_dtype, idx, topk_len, k, sm_scale, out, lse);
+    check_workspace(c, seqs, num_q, k, workspace, workspace_bytes);
+    dsa_status st = c.done();
+    if (st != DSA_OK || num_q == 0) return st;
+    Workspace ws = carve_workspace(workspace, *seqs, num_q, k);
+    return cuda_status(launch_sparse_mla(q, latent, latent_dtype, *seqs, num_q, idx, topk_len, k, sm_scale, out, lse,
+                                         ws, d_status, stream),
+                       "sparse_mla_decode launch");
+}
+
+dsa_status dsa_decode_layer(const dsa_layer_args* a, const dsa_seqs* seqs, int32_t num_q, void* workspace,
+                            size_t workspace_bytes, int32_t* d_status, cudaStream_t stream) {
+    Check c;
+    c.need(a != nullptr, DSA_ERR_INVALID_ARG, "args is NULL");
+    if (!a) return c.done();
+    check_seqs(c, seqs, num_q);
+    if (!a->reuse_idx)
+        check_index_args(c, a->q_idx, a->w, a->ssmax_s, a->ssmax_b, a->inv_freq, a->k_idx, a->k_scale, a->k_dtype);
+    check_mla_args(c, a->q_mla, a->latent, a->latent_dtype, a->idx, a->topk_len, a->k, a->sm_scale, a->out, a->lse);
+    check_workspace(c, seqs, num_q, a->k, workspace, workspace_bytes);
+    dsa_status st = c.done();
+    if (st != DSA_OK || num_q == 0) return st;
+    Workspace ws = carve_workspace(workspace, *seqs, num_q, a->k);
+    cudaError_t e = cudaSuccess;
+    auto mark = [&](int i) {
+        if (a->events && e == cudaSuccess) e = cudaEventRecord(a->events[i], stream);
+    };
+    mark(0);
+    if (!a->reuse_idx) {
+        if (e == cudaSuccess)
+            e = launch_index_scores(a->q_idx, a->w, a->ssmax_s, a->ssmax_b, a->inv_freq, a->k_idx, a->k_scale,
+                                    a->k_dtype, *seqs, num_q, ws.scores, ws.scores_ld, ws, d_status, stream);
+        mark(1);
+        if (e == cudaSuccess)
+            e = launch_topk(ws.scores, ws.scores_ld, *seqs, num_q, a->k, a->idx, a->topk_len, d_status, stream);
+        mark(2);
+    } else {
+        mark(1);
+        mark(2);
+    }
+    if (e == cudaSuccess)
+        e = launch_sparse_mla(a->q_mla, a->latent, a->latent_dtype, *seqs, num_q, a->idx, a->topk_len, a->k,
+                              a->sm_scale, a->out, a->lse, ws, d_status, stream);
+    mark(3);
+    return cuda_status(e, "dsa_decode_layer launch");
+}
+
+int32_t dsa_decode_layer_launches(const dsa_seqs* seqs, int32_t num_q, int32_t k, int32_t reuse_idx) {
+    Check c;
+    check_seqs(c, seqs, num_q);
+    c.need(k >= 1 && k <= DSA_MAX_TOPK, DSA_ERR_UNSUPPORTED, "k %d outside [1, %d]", k, DSA_MAX_TOPK);
+    if (c.done() != DSA_OK || num_q == 0) return 0;
+    const int mla = mla_splits(num_q, k) > 1 ? 2 : 1;  // attention (+ LSE combine)
+    return (reuse_idx ? 0 : 3) + mla;                  // query prep, scores, top-k
+}
+
+}  // extern "C"

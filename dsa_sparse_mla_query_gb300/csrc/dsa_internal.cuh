@@ -1,0 +1,135 @@
+// dsa_internal.cuh -- shared device helpers and launcher declarations of the
+// sm_103a DSA decode library.  Not part of the public ABI (include/dsa.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+constexpr int kIH = DSA_INDEX_HEADS;   // 32
+constexpr int kID = DSA_INDEX_DIM;     // 128
+constexpr int kRopeDims = 64;          // rotated dims of an index head
+constexpr int kMH = DSA_MLA_HEADS;     // 64
+constexpr int kMD = DSA_MLA_DIM;       // 576
+constexpr int kMV = DSA_MLA_VDIM;      // 512
+constexpr int kDsRow = DSA_DS_MLA_ROW; // 656
+
+// ---------------------------------------------------------------------------
+// device-side error reporting: first error wins, never traps
+__device__ __forceinline__ void report(int32_t* d_status, int32_t code) {
+    if (d_status) atomicCAS(d_status, 0, code);
+}
+
+// sequence of query row t (q_start is a CSR offset array of B+1 entries)
+__device__ __forceinline__ int seq_of(const int32_t* q_start, int B, int t) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (__ldg(q_start + mid) <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// physical row of token j of sequence b; -1 when the page table or base
+// points outside the cache
+__device__ __forceinline__ int64_t phys_row(const dsa_seqs& s, int b, int64_t j) {
+    int64_t row;
+    if (s.page_table) {
+        int64_t p = j / s.page_size;
+        if (p >= s.max_pages) return -1;
+        int64_t page = __ldg(s.page_table + (int64_t)b * s.max_pages + p);
+        row = page * s.page_size + (j - p * s.page_size);
+        if (page < 0) return -1;
+    } else {
+        row = __ldg(s.seq_base + b) + j;
+    }
+    return (row >= 0 && row < s.num_rows) ? row : -1;
+}
+
+// ---------------------------------------------------------------------------
+// warp-level tensor-core and async-copy primitives (inline PTX)
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+    // 16-byte async copy; zero-fills when !valid (src-size 0)
+    uint32_t s = smem_u32(smem);
+    int n = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(n));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(p)));
+}
+
+// D = A(16x16, row) * B(16x8, col) + D, fp32 accumulate
+__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// two OCP e4m3 codes (low byte first) -> f16x2, exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// ---------------------------------------------------------------------------
+// launchers (host)
+struct Workspace {
+    // carved from the caller's workspace, 256-byte aligned pieces
+    void* qprep;      // q' [Q, 32, KP] 16-bit
+    float* wprep;     // w' [Q, 32]
+    float* mla_part;  // O partials [Q, splits, 64, 512]
+    float* mla_ml;    // (m, l) partials [Q, splits, 64, 2]
+    float* scores;    // [Q, ld] for dsa_decode_layer
+    int64_t scores_ld;
+};
+
+int mla_splits(int num_q, int k);
+size_t workspace_bytes(const dsa_seqs& s, int num_q, int k, int64_t* scores_ld);
+Workspace carve_workspace(void* base, const dsa_seqs& s, int num_q, int k);
+
+cudaError_t launch_index_scores(const void* q_idx, const float* w, const float* ssmax_s, const float* ssmax_b,
+                                const float* inv_freq, const void* k_idx, const float* k_scale, dsa_dtype k_dtype,
+                                const dsa_seqs& s, int num_q, float* scores, int64_t ld, const Workspace& ws,
+                                int32_t* d_status, cudaStream_t stream);
+cudaError_t launch_topk(const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int k, int32_t* idx,
+                        int32_t* topk_len, int32_t* d_status, cudaStream_t stream);
+cudaError_t launch_sparse_mla(const void* q, const void* latent, dsa_dtype latent_dtype, const dsa_seqs& s,
+                              int num_q, const int32_t* idx, const int32_t* topk_len, int k, float sm_scale,
+                              void* out, float* lse, const Workspace& ws, int32_t* d_status, cudaStream_t stream);
+
+}  // namespace dsa

@@ -149,6 +149,7 @@ class Workload:
     queries_per_seq: int
     ctx: Optional[int] = None              # fixed context per sequence
     ctx_range: Optional[tuple] = None      # (lo, hi) inclusive, uniform integer
+    ctx_list: Optional[tuple] = None       # explicit context per sequence
     rope: bool = True
     alpha_range: Optional[tuple] = None    # LeRoPE alpha ~ U(lo, hi) per pair
     page_size: int = 0                     # 0 = contiguous rows per sequence
@@ -163,7 +164,8 @@ class Workload:
         return self.num_seqs * self.queries_per_seq
 
     def describe(self) -> str:
-        c = f"{self.ctx}" if self.ctx else f"U{{{self.ctx_range[0]}..{self.ctx_range[1]}}}"
+        c = (f"{self.ctx}" if self.ctx else f"U{{{self.ctx_range[0]}..{self.ctx_range[1]}}}" if self.ctx_range
+             else f"{list(self.ctx_list)}")
         return (f"{self.name}: {self.num_seqs} seq x ctx {c}, {self.queries_per_seq} q/seq, "
                 f"{'RoPE' if self.rope else 'NoPE'}, index {'e4m3+rowscale' if self.index_fp8 else 'bf16'}, "
                 f"latent {'fp8_ds_mla' if self.latent_fp8 else 'bf16'}"
@@ -181,6 +183,9 @@ WORKLOADS: Dict[str, Workload] = {
 
 
 def context_lengths(wl: Workload) -> List[int]:
+    if wl.ctx_list is not None:
+        assert len(wl.ctx_list) == wl.num_seqs
+        return [int(c) for c in wl.ctx_list]
     if wl.ctx is not None:
         return [wl.ctx] * wl.num_seqs
     lo, hi = wl.ctx_range

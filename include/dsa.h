@@ -1,0 +1,205 @@
+/* dsa.h -- C ABI of the GB300 (sm_103a) DSA decode path.
+ *
+ * One decode layer of a Mistral-Large-4-style DeepSeek Sparse Attention stack:
+ *   1. lightning indexer: SSMax-scaled, interleaved-RoPE index queries scored
+ *      against every causal key (dsa_index_scores),
+ *   2. exact top-k selection per query (dsa_topk),
+ *   3. absorbed-MLA attention of 64 heads over only the selected latent rows
+ *      (sparse_mla_decode),
+ * and the three chained on one stream (dsa_decode_layer), including the
+ * shared-indexer variant that reuses an earlier layer's selection.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [vLLM-ML4] "Day 0 support for Mistral Large 4" (vLLM blog), Implementation
+ *              details: Model architecture; Sparse MLA + DSA indexer; NoPE,
+ *              SSMax and LeRoPE; Long context: DCP (LSE combine, top-k
+ *              compaction with topk_length, slots of -1); ROCm implementation
+ *              details: Sparse MLA on AITER (top-k positions mapped to cache
+ *              slots), DSA indexer on AITER (132-byte FP8 indexer rows), FP8
+ *              latent cache (656-byte fp8_ds_mla rows, 1,152-byte bf16 rows).
+ *   [colibri]  "Mistral-Large-4 (c/colibri.c)", What differs from GLM-5.2:
+ *              NoPE layers; SSMax; The indexer; RoPE and the rest.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE memory owned by the caller unless marked "host".  The
+ *     library never allocates; scratch comes from a caller workspace sized by
+ *     dsa_workspace_size.
+ *   - Work is enqueued on `stream` and returns without synchronising.  Calls are
+ *     deterministic: the same inputs give the same bits.
+ *   - The return value reports what the host can see: a NULL or misaligned
+ *     pointer, an unsupported size or dtype, a too-small workspace, a launch
+ *     error.  Nothing is enqueued when it is not DSA_OK.  dsa_last_error_string()
+ *     gives the reason (thread-local).
+ *   - What only the device can see (a position outside its context, a page or
+ *     row outside the cache, an out-of-range selected index, a malformed
+ *     q_start) is written to *d_status (device int32; first error wins, the
+ *     caller clears it) and the affected work item is skipped.  No kernel traps
+ *     or asserts.
+ *   - Indices are logical token positions within a sequence.  The page table or
+ *     seq_base maps them to physical cache rows.
+ */
+#ifndef DSA_H
+#define DSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_INDEX_HEADS 32   /* index heads ([vLLM-ML4] Model architecture: 32 index heads) */
+#define DSA_INDEX_DIM 128    /* per index head; first 64 dims rotate on RoPE layers ([colibri] The indexer) */
+#define DSA_MLA_HEADS 64     /* attention heads ([vLLM-ML4] Model architecture) */
+#define DSA_MLA_DIM 576      /* latent row: 512 KV-LoRA dims + 64 RoPE dims */
+#define DSA_MLA_VDIM 512     /* value / output width in latent space */
+#define DSA_DS_MLA_ROW 656   /* fp8_ds_mla bytes per token */
+#define DSA_MAX_TOPK 2048    /* largest k served ([vLLM-ML4] top-k 2048) */
+
+typedef enum {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1,  /* NULL/misaligned pointer, bad size or stride */
+    DSA_ERR_UNSUPPORTED = 2,  /* valid but not served (dtype, k, shape) */
+    DSA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    DSA_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than dsa_workspace_size */
+    DSA_ERR_TIMEOUT = 5,      /* device: a bounded wait gave up */
+    DSA_ERR_BAD_INPUT = 6     /* device: position, page, row or index out of range */
+} dsa_status;
+
+typedef enum {
+    DSA_BF16 = 0,               /* bf16 rows: index keys [rows,128], latent [rows,576] */
+    DSA_FP8_E4M3_ROWSCALE = 1,  /* index keys: [rows,128] OCP e4m3 codes + k_scale fp32 [rows]
+                                   (132 B/token, [vLLM-ML4] DSA indexer on AITER) */
+    DSA_FP8_DS_MLA = 2          /* latent: [rows,656] bytes = [0,512) e4m3 latent codes,
+                                   [512,528) 4 fp32 scales (one per 128 latent dims),
+                                   [528,656) 64 bf16 RoPE dims ([vLLM-ML4] FP8 latent cache) */
+} dsa_dtype;
+
+/* Where tokens live.  Sequence b holds ctx_len[b] tokens; its queries are rows
+ * q_start[b] .. q_start[b+1]-1 of every per-query tensor, at absolute
+ * positions q_pos[row] < ctx_len[b] (a query sees keys 0..q_pos).  Token j of
+ * sequence b is physical row page_table[b*max_pages + j/page_size]*page_size +
+ * j%page_size when page_table is non-NULL, else seq_base[b] + j. */
+typedef struct {
+    int32_t num_seqs;         /* host: B >= 1 */
+    int32_t max_ctx;          /* host: >= every ctx_len[b]; sizes the grids */
+    int32_t max_q_per_seq;    /* host: >= every q_start[b+1]-q_start[b] */
+    int32_t page_size;        /* host: tokens per page (page_table only), multiple of 16 */
+    int32_t max_pages;        /* host: columns of page_table */
+    int32_t reserved;
+    int64_t num_rows;         /* host: physical rows in every cache, for bounds checks */
+    const int32_t* ctx_len;   /* [B] */
+    const int32_t* q_start;   /* [B+1], q_start[0] = 0, q_start[B] = num_q */
+    const int32_t* q_pos;     /* [num_q] */
+    const int32_t* page_table;/* [B, max_pages] or NULL */
+    const int64_t* seq_base;  /* [B] when page_table is NULL */
+} dsa_seqs;
+
+/* Bytes of workspace the calls below need for these sizes (host only; no
+ * device access).  One workspace sized for the largest call serves all. */
+dsa_status dsa_workspace_size(const dsa_seqs* seqs, int32_t num_q, int32_t k, size_t* bytes);
+
+/* Lightning-indexer scores ([colibri] SSMax, The indexer, RoPE and the rest;
+ * [vLLM-ML4] Model architecture, NoPE, SSMax and LeRoPE):
+ *   f_h = ssmax_s[h]*ln(pos+1) + ssmax_b[h];  q_h <- f_h * q_h;
+ *   RoPE layers (inv_freq != NULL): pairs (2i, 2i+1), i < 32, of q_h rotated by
+ *   pos*inv_freq[i] (inv_freq already holds the YaRN frequency divided by the
+ *   LeRoPE factor exp(alpha_i)); NoPE layers (inv_freq == NULL): no rotation;
+ *   score[t][j] = sum_h w[t][h] * relu(q_h . k_j / sqrt(128)) / sqrt(32)
+ *   for 0 <= j <= pos_t, and -inf for pos_t < j < ctx_len.  Entries at
+ *   j >= ctx_len are not written.  Cached keys are stored already rotated.
+ *   q_idx   bf16 [num_q, 32, 128]          w        fp32 [num_q, 32]
+ *   ssmax_s, ssmax_b fp32 [32]              inv_freq fp32 [32] or NULL
+ *   k_idx   k_dtype DSA_BF16 ([rows,128] bf16) or DSA_FP8_E4M3_ROWSCALE
+ *           ([rows,128] e4m3 + k_scale fp32 [rows]; k_scale NULL for bf16)
+ *   scores  fp32 [num_q, ld], ld >= max_ctx, ld % 4 == 0
+ * Alignment: every pointer 16-byte aligned. */
+dsa_status dsa_index_scores(const void* q_idx, const float* w, const float* ssmax_s, const float* ssmax_b,
+                            const float* inv_freq, const void* k_idx, const float* k_scale, dsa_dtype k_dtype,
+                            const dsa_seqs* seqs, int32_t num_q, float* scores, int64_t ld, void* workspace,
+                            size_t workspace_bytes, int32_t* d_status, cudaStream_t stream);
+
+/* Exact top-k per query ([vLLM-ML4] Model architecture: top-k 2048; DCP: an
+ * exact top-k, top-k compaction with topk_length, unused slots -1):
+ * the min(k, pos+1) keys j <= pos_t with the largest scores; at the boundary
+ * equal scores go to the smaller index (-0.0 counts as +0.0).
+ *   scores   fp32 [num_q, ld] (as written by dsa_index_scores)
+ *   idx      int32 [num_q, k]: selected positions in ascending order, then -1
+ *   topk_len int32 [num_q]: number of selected positions
+ * 1 <= k <= 2048. */
+dsa_status dsa_topk(const float* scores, int64_t ld, const dsa_seqs* seqs, int32_t num_q, int32_t k, int32_t* idx,
+                    int32_t* topk_len, void* workspace, size_t workspace_bytes, int32_t* d_status,
+                    cudaStream_t stream);
+
+/* Absorbed-MLA attention over selected latent rows ([vLLM-ML4] Model
+ * architecture: 64 heads, KV LoRA rank 512, RoPE dim 64; Sparse MLA + DSA
+ * indexer; NoPE, SSMax and LeRoPE: NoPE layers are MLA with zero RoPE dims):
+ *   for query t, head h, over slots i < topk_len[t] with idx[t][i] >= 0:
+ *   s_i = sm_scale * q[t][h] . c_{idx[t][i]} (576 dims), p = softmax(s),
+ *   out[t][h] = sum_i p_i c_{idx[t][i]}[0:512],  lse[t][h] = ln sum_i exp(s_i).
+ *   An empty selection gives out = 0 and lse = -inf.
+ *   q      bf16 [num_q, 64, 576] (SSMax and RoPE already applied)
+ *   latent DSA_BF16 [rows, 576] bf16 or DSA_FP8_DS_MLA [rows, 656] bytes
+ *   idx    int32 [num_q, k], topk_len int32 [num_q] (0..k)
+ *   out    bf16 [num_q, 64, 512]; lse fp32 [num_q, 64] or NULL
+ * 1 <= k <= 2048. */
+dsa_status sparse_mla_decode(const void* q, const void* latent, dsa_dtype latent_dtype, const dsa_seqs* seqs,
+                             int32_t num_q, const int32_t* idx, const int32_t* topk_len, int32_t k, float sm_scale,
+                             void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* d_status,
+                             cudaStream_t stream);
+
+/* One decode layer: dsa_index_scores -> dsa_topk -> sparse_mla_decode on one
+ * stream, with the scores kept in the workspace.  reuse_idx != 0 is a
+ * shared-indexer layer ([vLLM-ML4] Model architecture: 28 layers reuse the
+ * top-k of the nearest earlier indexer layer; [colibri] The indexer): idx and
+ * topk_len are inputs and only the attention runs; otherwise they are outputs. */
+typedef struct {
+    /* indexer (ignored when reuse_idx != 0) */
+    const void* q_idx;
+    const float* w;
+    const float* ssmax_s;
+    const float* ssmax_b;
+    const float* inv_freq;
+    const void* k_idx;
+    const float* k_scale;
+    dsa_dtype k_dtype;
+    int32_t reuse_idx;
+    /* selection */
+    int32_t k;
+    int32_t reserved;
+    int32_t* idx;
+    int32_t* topk_len;
+    /* attention */
+    const void* q_mla;
+    const void* latent;
+    dsa_dtype latent_dtype;
+    float sm_scale;
+    void* out;
+    float* lse;
+    /* optional: NULL, or 4 events recorded on `stream` before the indexer and
+       after the indexer, the top-k and the attention (a shared-indexer layer
+       records the first three back to back), for per-stage timing */
+    cudaEvent_t* events;
+} dsa_layer_args;
+
+dsa_status dsa_decode_layer(const dsa_layer_args* args, const dsa_seqs* seqs, int32_t num_q, void* workspace,
+                            size_t workspace_bytes, int32_t* d_status, cudaStream_t stream);
+
+/* Number of kernels dsa_decode_layer enqueues for these sizes (reuse_idx as
+ * in dsa_layer_args); 0 when the sizes are refused.  For callers that count
+ * or capture launches. */
+int32_t dsa_decode_layer_launches(const dsa_seqs* seqs, int32_t num_q, int32_t k, int32_t reuse_idx);
+
+/* Text of the last non-OK status returned on this thread ("" if none). */
+const char* dsa_last_error_string(void);
+/* Name of a status code. */
+const char* dsa_status_string(dsa_status s);
+/* Library version, "major.minor.patch". */
+const char* dsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_H */

@@ -37,8 +37,16 @@ def compile_oracle(src: str, out: str) -> str:
     return out
 
 
+def _foreign(path: str) -> bool:
+    import platform
+    want = {"x86_64": 0x3E, "AMD64": 0x3E, "aarch64": 0xB7, "arm64": 0xB7}.get(platform.machine())
+    with open(path, "rb") as f:
+        head = f.read(20)
+    return len(head) < 20 or head[:4] != b"\x7fELF" or int.from_bytes(head[18:20], "little") != want
+
+
 def build(force: bool = False) -> str:
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < max(
+    if force or not os.path.exists(_LIB) or _foreign(_LIB) or os.path.getmtime(_LIB) < max(
             os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "dsa_oracle.h"))):
         compile_oracle(_SRC, _LIB)
     return _LIB

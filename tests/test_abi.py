@@ -1,0 +1,104 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/dsa.h declares, and refuses bad arguments on the host (before any
+CUDA call) with a status and a message listing every reason."""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while", "for", "sizeof")))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dsa_sparse_mla_query_gb300 import _binding as B
+    from dsa_sparse_mla_query_gb300 import build
+    build.build()
+    return B.load()
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for n in ("dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode", "dsa_decode_layer",
+              "dsa_last_error_string", "dsa_status_string", "dsa_version"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"libdsa.so does not export {n}"
+
+
+def test_version_and_status_names(lib):
+    assert lib.dsa_version().decode().count(".") == 2
+    assert lib.dsa_status_string(0) == b"DSA_OK"
+    assert lib.dsa_status_string(6) == b"DSA_ERR_BAD_INPUT"
+
+
+def _seqs(B, **kw):
+    base = dict(num_seqs=1, max_ctx=4096, max_q_per_seq=1, page_size=0, max_pages=0, reserved=0, num_rows=4096,
+                ctx_len=0x1000, q_start=0x2000, q_pos=0x3000, page_table=None, seq_base=0x4000)
+    base.update(kw)
+    return B.DsaSeqsC(**base)
+
+
+def test_host_validation_lists_every_reason(lib):
+    from dsa_sparse_mla_query_gb300 import _binding as B
+    s = _seqs(B, num_seqs=0, q_pos=None)
+    rc = lib.dsa_index_scores(None, None, 0x10, 0x10, None, 0x10, None, 7, ctypes.byref(s), 1, 0x10, 3, None, 0,
+                              None, None)
+    assert rc == B.DSA_ERR_INVALID_ARG
+    msg = lib.dsa_last_error_string().decode()
+    for part in ("num_seqs 0", "seqs.q_pos is NULL", "q_idx is NULL", "w is NULL", "dtype 7", "ld 3"):
+        assert part in msg, (part, msg)
+
+
+def test_workspace_size_and_refusals(lib):
+    from dsa_sparse_mla_query_gb300 import _binding as B
+    s = _seqs(B)
+    n = ctypes.c_size_t()
+    assert lib.dsa_workspace_size(ctypes.byref(s), 4, 2048, ctypes.byref(n)) == 0
+    assert n.value > 4 * 4096 * 4
+    assert lib.dsa_workspace_size(ctypes.byref(s), 4, 4096, ctypes.byref(n)) == B.DSA_ERR_UNSUPPORTED
+    assert "k 4096" in lib.dsa_last_error_string().decode()
+    # too-small workspace is refused before anything is enqueued
+    rc = lib.sparse_mla_decode(0x100, 0x100, 0, ctypes.byref(s), 4, 0x100, 0x100, 2048, ctypes.c_float(0.07), 0x100,
+                               None, 0x100, 16, None, None)
+    assert rc == B.DSA_ERR_WORKSPACE
+    assert "workspace has 16 bytes" in lib.dsa_last_error_string().decode()
+    # misaligned pointer and bad page size
+    s2 = _seqs(B, page_table=0x5000, page_size=10, max_pages=4)
+    rc = lib.dsa_topk(0x104, 4096, ctypes.byref(s2), 1, 2048, 0x200, 0x300, None, 0, None, None)
+    assert rc != 0
+    msg = lib.dsa_last_error_string().decode()
+    assert "scores is not 16-byte aligned" in msg and "page_size 10" in msg
+
+
+def test_zero_queries_is_a_no_op(lib):
+    from dsa_sparse_mla_query_gb300 import _binding as B
+    s = _seqs(B)
+    rc = lib.dsa_topk(0x100, 4096, ctypes.byref(s), 0, 2048, 0x200, 0x300, None, 0, None, None)
+    assert rc == 0
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from dsa_sparse_mla_query_gb300 import _binding as B
+    with pytest.raises(RuntimeError, match="not built"):
+        B._lib_saved = B._lib
+        try:
+            B._lib = None
+            B.load(str(tmp_path / "missing.so"))
+        finally:
+            B._lib = B._lib_saved

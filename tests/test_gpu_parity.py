@@ -1,0 +1,230 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle on a GB300.
+
+Small workloads span several key tiles, ragged tails, pages, several queries
+per sequence, NoPE + a shared-indexer layer, fp8 caches and a prefill chunk;
+every query is checked.  The full-size workloads run in the launch
+configuration the benchmark times and are checked on sampled queries.
+Tolerances are in tests/parity.py.
+"""
+
+from __future__ import annotations
+
+import math
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import pytest
+import torch
+
+import dsa_sparse_mla_query_gb300 as dsa
+from dsa_sparse_mla_query_gb300 import inputs as I
+from dsa_sparse_mla_query_gb300.runner import DecodeStep
+import parity as P
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+W = I.WORKLOADS
+SMALL = {
+    "tiny": W["tiny"],
+    "paged_small": I.scaled(W["paged"], num_seqs=3, ctx=None, ctx_list=(1500, 4163, 130)),
+    "specv_small": I.scaled(W["specv"], num_seqs=4, ctx_range=(2100, 6000)),
+    "fp8_small": I.scaled(W["long_fp8"], num_seqs=3, ctx=None, ctx_list=(2000, 9000, 2049)),
+    "prefill_small": I.scaled(W["prefill"], ctx=3000, queries_per_seq=40),
+}
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    dsa.load()
+    yield
+    torch.cuda.synchronize()
+
+
+def _inputs_cpu_then_gpu(wl):
+    d = I.make_inputs(wl, "cpu")
+    return P.to_device(d, DEV), d
+
+
+def _separate_scores(d, wl, step):
+    """dsa_index_scores into a [Q, ld] buffer (NaN-poisoned, so unwritten
+    entries inside the context would show)."""
+    ld = P.ld_of(step.seqs.max_ctx)
+    scores = torch.full((step.num_q, ld), float("nan"), dtype=torch.float32, device=DEV)
+    dsa.dsa_index_scores(d["q_idx"], d["w"], d["ssmax_s"], d["ssmax_b"], d["inv_freq"], d["k_idx"], d.get("k_scale"),
+                         dsa.DSA_FP8_E4M3_ROWSCALE if step.k_fp8 else dsa.DSA_BF16, step.seqs, step.num_q, scores,
+                         ld, step.ws, step.ws_bytes, step.status)
+    return scores, ld
+
+
+def _check_workload(d, wl, queries, threads=8):
+    """Runs the separate calls and the fused layer; checks queries against the
+    oracle.  Returns a small report."""
+    step = DecodeStep(d, wl.queries_per_seq, wl.topk)
+    k = wl.topk
+    scores, ld = _separate_scores(d, wl, step)
+    idx = torch.empty(step.num_q, k, dtype=torch.int32, device=DEV)
+    tlen = torch.empty(step.num_q, dtype=torch.int32, device=DEV)
+    dsa.dsa_topk(scores, ld, step.seqs, step.num_q, k, idx, tlen, step.ws, step.ws_bytes, step.status)
+    step.run()  # fused layer(s), the launch configuration the benchmark times
+    torch.cuda.synchronize()
+    assert step.device_status() == 0, f"device status {step.device_status()}"
+    lay = d["layout"]
+    sc_h, idx_h, len_h = scores.cpu().numpy(), idx.cpu().numpy(), tlen.cpu().numpy()
+    fidx_h, flen_h = step.idx.cpu().numpy(), step.topk_len.cpu().numpy()
+    assert np.array_equal(fidx_h, idx_h) and np.array_equal(flen_h, len_h), "fused and separate selections differ"
+
+    def one(t):
+        b = lay.q_seq[t]
+        pos, ctx = lay.q_pos[t], lay.ctx_len[b]
+        ref = P.oracle_scores_for_query(d, t)
+        rep = {"t": t}
+        rep["score_rel_err"] = P.check_scores(sc_h[t], ref, pos, ctx)
+        rep["boundary_diff"] = P.check_topk(idx_h[t], int(len_h[t]), ref[:pos + 1], k)
+        ref_idx, m = __import__("oracle").topk(ref[:pos + 1], k)
+        rep["oracle_sel"] = np.sort(ref_idx[:m])
+        return rep
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        reps = list(ex.map(one, queries))
+
+    # attention on the oracle's own selection through sparse_mla_decode
+    oidx = torch.full((step.num_q, k), -1, dtype=torch.int32)
+    olen = torch.zeros(step.num_q, dtype=torch.int32)
+    for r in reps:
+        oidx[r["t"], :len(r["oracle_sel"])] = torch.from_numpy(r["oracle_sel"].astype(np.int32))
+        olen[r["t"]] = len(r["oracle_sel"])
+    oidx_d, olen_d = oidx.to(DEV), olen.to(DEV)
+    layers = [("latent", "q_mla", False)] + ([("latent2", "q_mla2", True)] if step.shared else [])
+    for lat_key, q_key, shared in layers:
+        out = torch.empty(step.num_q, 64, 512, dtype=torch.bfloat16, device=DEV)
+        lse = torch.empty(step.num_q, 64, dtype=torch.float32, device=DEV)
+        dsa.sparse_mla_decode(d[q_key], d[lat_key], dsa.DSA_FP8_DS_MLA if step.lat_fp8 else dsa.DSA_BF16, step.seqs,
+                              step.num_q, oidx_d, olen_d, k, d["sm_scale"], out, lse, step.ws, step.ws_bytes,
+                              step.status)
+        torch.cuda.synchronize()
+        assert step.device_status() == 0
+        out_h, lse_h = out.float().cpu().numpy(), lse.cpu().numpy()
+        fout = (step.out2 if shared else step.out).float().cpu().numpy()
+        flse = (step.lse2 if shared else step.lse).cpu().numpy()
+
+        def att(r):
+            t = r["t"]
+            ro, rl = P.oracle_mla_for_query(d, t, r["oracle_sel"], shared)
+            e = P.check_mla(out_h[t], lse_h[t], ro, rl)
+            # fused layer: its own selection; where it equals the oracle's the
+            # output must match; where boundary ties were resolved the other
+            # way the output must be attention over the selection it made
+            fsel = fidx_h[t][:flen_h[t]]
+            if np.array_equal(np.sort(fsel), r["oracle_sel"]):
+                P.check_mla(fout[t], flse[t], ro, rl)
+            else:
+                vo, vl = P.oracle_mla_for_query(d, t, fsel, shared)
+                P.check_mla(fout[t], flse[t], vo, vl)
+            return e
+
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            errs = list(ex.map(att, reps))
+        for r, e in zip(reps, errs):
+            r["out_rel_err_" + lat_key] = e
+    return reps
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_workload_all_queries(name):
+    wl = SMALL[name]
+    d, _ = _inputs_cpu_then_gpu(wl)
+    reps = _check_workload(d, wl, list(range(wl.num_queries)))
+    worst = max(r["score_rel_err"] for r in reps)
+    assert worst < 1e-4, f"scores should be near fp32 accuracy, got {worst:.2e}"
+
+
+@pytest.mark.parametrize("ctx_list", [(1,), (2047,), (2048,), (2049,), (4096 + 37,)])
+def test_context_around_k(ctx_list):
+    """Context shorter than, equal to and just above k; one key; a ragged tail."""
+    wl = I.scaled(W["tiny"], num_seqs=len(ctx_list), ctx=None, ctx_list=ctx_list, queries_per_seq=1)
+    d, _ = _inputs_cpu_then_gpu(wl)
+    _check_workload(d, wl, list(range(wl.num_queries)))
+
+
+@pytest.mark.parametrize("k", [1, 7, 100, 2047])
+def test_small_k(k):
+    wl = I.scaled(W["paged"], num_seqs=2, ctx=None, ctx_list=(3000, 777), topk=k)
+    d, _ = _inputs_cpu_then_gpu(wl)
+    _check_workload(d, wl, list(range(wl.num_queries)))
+
+
+def test_all_equal_scores_take_smallest_indices():
+    """w = 0 makes every score 0: the selection is positions 0..k-1."""
+    wl = I.scaled(W["tiny"], num_seqs=1, ctx=5000, queries_per_seq=2)
+    d, _ = _inputs_cpu_then_gpu(wl)
+    d["w"].zero_()
+    step = DecodeStep(d, wl.queries_per_seq, wl.topk)
+    step.run()
+    torch.cuda.synchronize()
+    idx = step.idx.cpu().numpy()
+    for t in range(2):
+        assert np.array_equal(idx[t], np.arange(2048))
+    _check_workload(d, wl, [0, 1])
+
+
+def test_empty_selection_and_holes():
+    """topk_len = 0 gives zeros and -inf; -1 slots inside the selection are skipped."""
+    wl = I.scaled(W["tiny"], num_seqs=1, ctx=3000, queries_per_seq=3)
+    d, _ = _inputs_cpu_then_gpu(wl)
+    step = DecodeStep(d, wl.queries_per_seq, wl.topk)
+    k = wl.topk
+    idx = torch.full((3, k), -1, dtype=torch.int32)
+    sel = np.array([5, 17, 2999, 0, 1024, 1500], np.int32)
+    idx[1, :6] = torch.from_numpy(sel)
+    idx[1, 2] = -1                     # a hole
+    idx[2, :6] = torch.from_numpy(sel)
+    tlen = torch.tensor([0, 6, 6], dtype=torch.int32)
+    out = torch.empty(3, 64, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(3, 64, dtype=torch.float32, device=DEV)
+    dsa.sparse_mla_decode(d["q_mla"], d["latent"], dsa.DSA_BF16, step.seqs, 3, idx.to(DEV), tlen.to(DEV), k,
+                          d["sm_scale"], out, lse, step.ws, step.ws_bytes, step.status)
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+    o, l = out.float().cpu().numpy(), lse.cpu().numpy()
+    assert np.all(o[0] == 0) and np.all(np.isneginf(l[0]))
+    r1 = P.oracle_mla_for_query(d, 1, np.delete(sel, 2))
+    P.check_mla(o[1], l[1], *r1)
+    r2 = P.oracle_mla_for_query(d, 2, sel)
+    P.check_mla(o[2], l[2], *r2)
+
+
+def test_bad_position_sets_device_status():
+    """A query position outside its context is reported in d_status and its
+    row is skipped; the other queries are unaffected; nothing traps."""
+    wl = I.scaled(W["tiny"], num_seqs=2, ctx=None, ctx_list=(3000, 2500), queries_per_seq=1)
+    d, _ = _inputs_cpu_then_gpu(wl)
+    d["q_pos"][1] = 2500  # == ctx_len[1]
+    step = DecodeStep(d, 1, wl.topk)
+    step.run()
+    torch.cuda.synchronize()
+    assert step.device_status() == 6  # DSA_ERR_BAD_INPUT
+    assert int(step.topk_len[1].item()) == 0
+    assert int(step.topk_len[0].item()) == 2048
+    torch.cuda.synchronize()
+
+
+FULL = ["paged", "specv", "long_fp8", "prefill"]
+SAMPLES = {"paged": 6, "specv": 6, "long_fp8": 3, "prefill": 4}
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    """Full-size workload in the benchmark's launch configuration; sampled
+    queries against the oracle."""
+    wl = W[name]
+    d = I.make_inputs(wl, DEV)
+    try:
+        qs = P.sample_queries(wl.num_queries, SAMPLES[name])
+        reps = _check_workload(d, wl, qs, threads=8)
+        print(name, [(r["t"], round(r["score_rel_err"], 9), r["boundary_diff"]) for r in reps])
+    finally:
+        del d
+        torch.cuda.empty_cache()
