@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--workload", default="paged", choices=sorted(I.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak-s", type=float, default=1.0, help="untimed load before the timed region (clocks)")
+    ap.add_argument("--seqs", type=int, default=0, help="override the number of sequences (small profiling cases)")
     return ap.parse_args()
 
 
@@ -359,7 +360,7 @@ def run_ours(args, wl, ws, rank, local):
         import oracle
         oracle.build()
         threads = cpu_threads()
-        jobs = oracle_sample(wl, 2 * threads)
+        jobs = oracle_sample(wl, 6 * threads)
         secs = oracle_timed(wl, jobs, threads)
         cpu = {"value": len(jobs) / secs, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{len(jobs)} queries of {wl.name} spread over the batch, each the whole layer "
@@ -398,6 +399,8 @@ def main():
     args = parse()
     ws, rank, local = dist_env()
     wl = I.WORKLOADS[args.workload]
+    if args.seqs:
+        wl = I.scaled(wl, num_seqs=args.seqs)
     if args.impl == "reference":
         if ws > 1 and rank != 0:
             return
