@@ -19,8 +19,9 @@ from ._binding import (  # noqa: F401
     dsa_workspace_size,
     load,
     sparse_mla_decode,
+    sparse_mla_decode_noalloc,
     version,
 )
 
-__all__ = ["Seqs", "DsaError", "dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode",
+__all__ = ["Seqs", "DsaError", "dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode", "sparse_mla_decode_noalloc",
            "dsa_decode_layer", "dsa_decode_layer_launches", "load", "version", "DSA_BF16", "DSA_FP8_E4M3_ROWSCALE", "DSA_FP8_DS_MLA"]

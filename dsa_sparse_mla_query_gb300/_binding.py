@@ -20,7 +20,8 @@ DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA = 0, 1, 2, 3
 DSA_ERR_WORKSPACE, DSA_ERR_TIMEOUT, DSA_ERR_BAD_INPUT = 4, 5, 6
 DSA_BF16, DSA_FP8_E4M3_ROWSCALE, DSA_FP8_DS_MLA = 0, 1, 2
 EXPORTS = ("dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode", "dsa_decode_layer",
-           "dsa_decode_layer_launches", "dsa_last_error_string", "dsa_status_string", "dsa_version")
+           "dsa_decode_layer_launches", "sparse_mla_decode_noalloc", "dsa_last_error_string", "dsa_status_string",
+           "dsa_version")
 
 
 class DsaError(RuntimeError):
@@ -67,6 +68,8 @@ def load(path: str = LIB_PATH):
         L.dsa_topk.argtypes = [P, I64, S, I32, I32, P, P, P, SZ, P, P]
         L.sparse_mla_decode.argtypes = [P, P, ctypes.c_int, S, I32, P, P, I32, ctypes.c_float, P, P, P, SZ, P, P]
         L.dsa_decode_layer.argtypes = [ctypes.POINTER(DsaLayerArgsC), S, I32, P, SZ, P, P]
+        L.sparse_mla_decode_noalloc.argtypes = [P, P, ctypes.c_int, S, I32, P, P, I32, ctypes.c_float, P, P, P, P]
+        L.sparse_mla_decode_noalloc.restype = ctypes.c_int
         L.dsa_decode_layer_launches.argtypes = [S, I32, I32, I32]
         L.dsa_decode_layer_launches.restype = ctypes.c_int32
         for f in ("dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode", "dsa_decode_layer"):
@@ -149,6 +152,16 @@ def sparse_mla_decode(q, latent, latent_dtype: int, seqs: Seqs, num_q: int, idx,
     _check(load().sparse_mla_decode(_p(q), _p(latent), latent_dtype, ctypes.byref(sc), num_q, _p(idx), _p(topk_len),
                                     k, float(sm_scale), _p(out), _p(lse), _p(workspace), workspace_bytes,
                                     _p(d_status), _stream(stream)))
+
+
+def sparse_mla_decode_noalloc(q, latent, latent_dtype: int, seqs: Seqs, num_q: int, idx, topk_len, k: int,
+                              sm_scale: float, out, lse, d_status=None, stream=None):
+    """sparse_mla_decode for callers that cannot allocate: no workspace, the
+    partials live in the library's static device scratch (see include/dsa.h)."""
+    sc = seqs.c()
+    _check(load().sparse_mla_decode_noalloc(_p(q), _p(latent), latent_dtype, ctypes.byref(sc), num_q, _p(idx),
+                                            _p(topk_len), k, float(sm_scale), _p(out), _p(lse), _p(d_status),
+                                            _stream(stream)))
 
 
 def dsa_decode_layer_launches(seqs: Seqs, num_q: int, k: int, reuse_idx: int = 0) -> int:

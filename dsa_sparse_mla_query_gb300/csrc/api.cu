@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
 #include <string>
 
 #include "dsa_internal.cuh"
@@ -283,3 +284,67 @@ int32_t dsa_decode_layer_launches(const dsa_seqs* seqs, int32_t num_q, int32_t k
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// sparse_mla_decode_noalloc: the attention's split-K partials in a
+// library-owned static device array instead of a caller workspace.
+namespace dsa {
+namespace {
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[DSA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the static array on the current device, looked up once
+// per device with that device current.
+cudaError_t noalloc_scratch(void** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" dsa_status sparse_mla_decode_noalloc(const void* q, const void* latent, dsa_dtype latent_dtype,
+                                                const dsa_seqs* seqs, int32_t num_q, const int32_t* idx,
+                                                const int32_t* topk_len, int32_t k, float sm_scale, void* out,
+                                                float* lse, int32_t* d_status, cudaStream_t stream) {
+    Check c;
+    check_seqs(c, seqs, num_q);
+    check_mla_args(c, q, latent, latent_dtype, idx, topk_len, k, sm_scale, out, lse);
+    size_t part_bytes = 0, ml_bytes = 0;
+    if (c.st == DSA_OK && num_q > 0) {
+        const int splits = mla_splits(num_q, k);
+        if (splits > 1) {
+            part_bytes = up256((size_t)num_q * splits * kMH * kMV * 4);
+            ml_bytes = up256((size_t)num_q * splits * kMH * 2 * 4);
+        }
+        c.need(part_bytes + ml_bytes <= (size_t)DSA_NOALLOC_SCRATCH_BYTES, DSA_ERR_UNSUPPORTED,
+               "%d queries x %d splits need %zu bytes of scratch; the static scratch holds %zu", num_q, splits,
+               part_bytes + ml_bytes, (size_t)DSA_NOALLOC_SCRATCH_BYTES);
+    }
+    dsa_status st = c.done();
+    if (st != DSA_OK || num_q == 0) return st;
+    void* base = nullptr;
+    cudaError_t e = noalloc_scratch(&base);
+    if (e != cudaSuccess) return cuda_status(e, "sparse_mla_decode_noalloc scratch address");
+    Workspace ws{};
+    ws.mla_part = reinterpret_cast<float*>(base);
+    ws.mla_ml = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(base) + part_bytes);
+    return cuda_status(launch_sparse_mla(q, latent, latent_dtype, *seqs, num_q, idx, topk_len, k, sm_scale, out, lse,
+                                         ws, d_status, stream),
+                       "sparse_mla_decode_noalloc launch");
+}

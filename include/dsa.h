@@ -187,6 +187,31 @@ typedef struct {
 dsa_status dsa_decode_layer(const dsa_layer_args* args, const dsa_seqs* seqs, int32_t num_q, void* workspace,
                             size_t workspace_bytes, int32_t* d_status, cudaStream_t stream);
 
+/* sparse_mla_decode without a workspace, for callers that cannot allocate
+ * device memory at all: code embedded in a host process whose GPU memory is
+ * owned by another allocator (a serving engine that reserves the whole pool at
+ * start-up, a plugin ABI that hands over only input and output buffers), so it
+ * has no way to provide the workspace the other entry points take.  The pages
+ * have no counterpart of this call; it is a deployment convenience.
+ *   Same arguments, semantics and results as sparse_mla_decode, minus the
+ *   workspace.  The split-K partial results go to a static device array of
+ *   DSA_NOALLOC_SCRATCH_BYTES owned by the library: every GPU that loads the
+ *   library holds it until the process exits.  Sizes whose partials do not fit
+ *   (num_q x splits x 131,584 bytes, rounded up) are refused with
+ *   DSA_ERR_UNSUPPORTED and a message giving both sizes; nothing is enqueued.
+ *   The first call on each device looks up the array's device address with
+ *   that device current (a runtime query, no allocation); make that first call
+ *   before any stream capture on the device.  Every call shares the one array
+ *   and each call writes every partial it later reads, so nothing needs
+ *   clearing between calls; calls that overlap on the GPU (other streams, other
+ *   host threads) race on it and must be serialised by the caller.  No call
+ *   allocates or frees memory. */
+#define DSA_NOALLOC_SCRATCH_BYTES (32u << 20)
+dsa_status sparse_mla_decode_noalloc(const void* q, const void* latent, dsa_dtype latent_dtype,
+                                     const dsa_seqs* seqs, int32_t num_q, const int32_t* idx,
+                                     const int32_t* topk_len, int32_t k, float sm_scale, void* out, float* lse,
+                                     int32_t* d_status, cudaStream_t stream);
+
 /* Number of kernels dsa_decode_layer enqueues for these sizes (reuse_idx as
  * in dsa_layer_args); 0 when the sizes are refused.  For callers that count
  * or capture launches. */
