@@ -11,31 +11,42 @@
 //   relu(f x) = |f| relu(sgn(f) x), and sqrt(128) sqrt(32) = 64, so
 //   score = sum_h w'_h relu(q'_h . k_j) with w'_h = w_h |f_h| / 64 and
 //   q'_h = sgn(f_h) rot(q_h).  The unrotated dims of q' stay exact bf16; the 64
-//   rotated dims (angle and rotation in fp64) are split into hi + lo 16-bit
+//   rotated dims (fp64 angle, fp32 rotation) are split into hi + lo 16-bit
 //   parts, so the contraction runs over K = 192 columns [hi | lo | unrotated]
 //   against key dims [0..63 | 0..63 | 64..127] and reproduces the fp64 query to
 //   ~2^-17 relative.  That keeps the top-k boundary exact (see dsa_topk).
 //   e4m3 keys decode exactly to f16, so the fp8 path runs the same contraction
 //   in f16 and multiplies the per-row scale after the relu-weighted sum
 //   (scale >= 0).
-#include "dsa_internal.cuh"
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "tc_ptx.cuh"
 
 namespace dsa {
 
 // ---------------------------------------------------------------------------
 // query preparation: q' [Q, 32, KP] (KP = 192 RoPE, 128 NoPE), w' [Q, 32]
+//
+// The 32 SSMax factors and the 32 rotation angles of a query are computed in
+// fp64 (the angle pos*inv_freq reaches ~5e5 rad at 512K context, where fp32
+// would lose the phase); cos and sin of the fp64 angle are then rounded to
+// fp32 and the rotation of the exact bf16 inputs runs in fp32 with fused
+// multiply-adds (relative error ~2^-23, below the 2^-17 of the hi + lo split).
 template <typename T>
-__device__ __forceinline__ T from_double(double x);
+__device__ __forceinline__ T from_float(float x);
 template <>
-__device__ __forceinline__ __nv_bfloat16 from_double<__nv_bfloat16>(double x) { return __double2bfloat16(x); }
+__device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 template <>
-__device__ __forceinline__ __half from_double<__half>(double x) { return __double2half(x); }
+__device__ __forceinline__ __half from_float<__half>(float x) { return __float2half_rn(x); }
 template <typename T>
-__device__ __forceinline__ double to_double(T x);
+__device__ __forceinline__ float to_float(T x);
 template <>
-__device__ __forceinline__ double to_double<__nv_bfloat16>(__nv_bfloat16 x) { return (double)__bfloat162float(x); }
+__device__ __forceinline__ float to_float<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
 template <>
-__device__ __forceinline__ double to_double<__half>(__half x) { return (double)__half2float(x); }
+__device__ __forceinline__ float to_float<__half>(__half x) { return __half2float(x); }
 
 template <typename T>
 __global__ void __launch_bounds__(128) qprep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ w,
@@ -46,8 +57,7 @@ __global__ void __launch_bounds__(128) qprep_kernel(const __nv_bfloat16* __restr
     const int t = blockIdx.x;
     const bool rope = inv_freq != nullptr;
     const int KP = rope ? 192 : 128;
-    __shared__ double cs[32], sn[32];
-    __shared__ double sgn[32];
+    __shared__ float cs[32], sn[32], sgn[32];
     __shared__ int ok;
     const int b = seq_of(s.q_start, s.num_seqs, t);
     const int pos = __ldg(s.q_pos + t);
@@ -58,257 +68,494 @@ __global__ void __launch_bounds__(128) qprep_kernel(const __nv_bfloat16* __restr
     }
     if (threadIdx.x < 32) {
         const int h = threadIdx.x;
-        double f = (double)__ldg(ss + h) * log((double)pos + 1.0) + (double)__ldg(sb + h);
-        sgn[h] = f < 0.0 ? -1.0 : 1.0;
+        const double f = (double)__ldg(ss + h) * log((double)pos + 1.0) + (double)__ldg(sb + h);
+        sgn[h] = f < 0.0 ? -1.f : 1.f;
         wp[(int64_t)t * kIH + h] = (float)((double)__ldg(w + (int64_t)t * kIH + h) * fabs(f) / 64.0);
-        if (rope) {
-            double th = (double)pos * (double)__ldg(inv_freq + h);
-            sincos(th, &sn[h], &cs[h]);
-        }
+    } else if (threadIdx.x < 64 && rope) {
+        const int i = threadIdx.x - 32;  // rotation pair
+        double sd, cd;
+        sincos((double)pos * (double)__ldg(inv_freq + i), &sd, &cd);
+        cs[i] = (float)cd;
+        sn[i] = (float)sd;
     }
     __syncthreads();
+    // one work item = 4 consecutive pairs (8 dims) of one head
     const __nv_bfloat16* qt = q + (int64_t)t * kIH * kID;
     T* out = qp + (int64_t)t * kIH * KP;
-    for (int e = threadIdx.x; e < kIH * 64; e += blockDim.x) {
-        const int h = e >> 6, p = e & 63;  // pair p = dims (2p, 2p+1)
-        double x0 = (double)__bfloat162float(qt[h * kID + 2 * p]);
-        double x1 = (double)__bfloat162float(qt[h * kID + 2 * p + 1]);
-        const double g = ok ? sgn[h] : 0.0;
+    for (int e = threadIdx.x; e < kIH * 16; e += blockDim.x) {
+        const int h = e >> 4, c8 = e & 15;  // dims 8*c8 .. 8*c8+7
+        const uint4 raw = *reinterpret_cast<const uint4*>(qt + h * kID + c8 * 8);
+        const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&raw);
+        const float g = ok ? sgn[h] : 0.f;
         T* o = out + h * KP;
-        if (rope && p < 32) {
-            double y0 = g * (x0 * cs[p] - x1 * sn[p]);
-            double y1 = g * (x0 * sn[p] + x1 * cs[p]);
-            T h0 = from_double<T>(y0), h1 = from_double<T>(y1);
-            o[2 * p] = h0;
-            o[2 * p + 1] = h1;
-            o[64 + 2 * p] = from_double<T>(y0 - to_double<T>(h0));
-            o[64 + 2 * p + 1] = from_double<T>(y1 - to_double<T>(h1));
+        alignas(16) T hi[8];
+        alignas(16) T lo[8];
+        if (rope && c8 < 8) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int p = c8 * 4 + u;
+                const float x0 = __bfloat162float(x[2 * u]), x1 = __bfloat162float(x[2 * u + 1]);
+                const float y0 = g * fmaf(x0, cs[p], -x1 * sn[p]);
+                const float y1 = g * fmaf(x0, sn[p], x1 * cs[p]);
+                hi[2 * u] = from_float<T>(y0);
+                hi[2 * u + 1] = from_float<T>(y1);
+                lo[2 * u] = from_float<T>(y0 - to_float<T>(hi[2 * u]));
+                lo[2 * u + 1] = from_float<T>(y1 - to_float<T>(hi[2 * u + 1]));
+            }
+            *reinterpret_cast<uint4*>(o + c8 * 8) = *reinterpret_cast<const uint4*>(hi);
+            *reinterpret_cast<uint4*>(o + 64 + c8 * 8) = *reinterpret_cast<const uint4*>(lo);
         } else {
-            const int col = rope ? 64 + 2 * p : 2 * p;
-            o[col] = from_double<T>(g * x0);
-            o[col + 1] = from_double<T>(g * x1);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) hi[u] = from_float<T>(g * __bfloat162float(x[u]));
+            *reinterpret_cast<uint4*>(o + (rope ? 64 : 0) + c8 * 8) = *reinterpret_cast<const uint4*>(hi);
         }
     }
 }
 
 // ---------------------------------------------------------------------------
-// scores: one CTA = 128 keys of one sequence x NQ queries of that sequence.
-// 8 warps, warp w owns keys 16w..16w+15 (the MMA M rows); N = NQ*32 heads.
+// scores on the 5th-generation tensor cores.
+//
+// Work: tiles of 128 keys of one sequence x one chunk of NQ <= 8 queries of
+// that sequence (N = NQ*32 accumulator columns).  The tile space
+// (sequence, chunk, tile) is cut into one contiguous range per CTA; CTAs are
+// persistent (one per SM) and stream their range through a ring of shared-
+// memory stages:
+//   warp 0     TMA producer: key tiles (128-byte swizzled, K-major) and, at
+//              each new (sequence, chunk), the chunk's q' (same layout);
+//   warp 1     allocates TMEM and issues tcgen05.mma: M = 128 keys, N = NQ*32
+//              heads, K = 192 (hi | lo | unrotated) or 128 (NoPE), fp32
+//              accumulators double-buffered in TMEM;
+//   warps 2-5  epilogue: one key row per thread straight from TMEM, relu and
+//              head weights, causal mask, fp8 row scale, coalesced stores;
+//   warps 6-9  (e4m3 keys only) decode the staged codes to f16 in the
+//              swizzled layout the MMA reads.
+// Keys past the context are never stored; pages are read through the page
+// table one TMA box (R rows, R | page size) at a time.
 constexpr int kTileKeys = 128;
-constexpr int kKeyStride = kID + 8;  // 16-bit elements per key row in smem (pad: no ldmatrix bank conflicts)
 
-template <int NQ, int KP>
-struct IdxSmem {
-    static constexpr int kQStride = KP + 8;
-    static constexpr size_t q_bytes = (size_t)NQ * kIH * kQStride * 2;
-    static constexpr size_t k_bytes = (size_t)kTileKeys * kKeyStride * 2;
-    static constexpr size_t raw_bytes = (size_t)kTileKeys * kID;  // e4m3 staging
-    static constexpr size_t out_bytes = (size_t)NQ * kTileKeys * 4;
-    static constexpr size_t total = q_bytes + k_bytes + raw_bytes + out_bytes + NQ * kIH * 4 + kTileKeys * 4 + 64;
+template <bool FP8>
+struct StageBytes {
+    static constexpr int raw = FP8 ? kTileKeys * kID : 0;   // e4m3 codes, unswizzled
+    static constexpr int mma = kTileKeys * kID * 2;         // 16-bit, two swizzled 64-dim blocks
+    static constexpr int total = raw + mma;
+};
+
+struct IdxSeg {
+    int b, ctx, q0, nq, maxpos;
+    bool ok;
+};
+
+template <int NQ>
+__device__ __forceinline__ IdxSeg load_seg(const dsa_seqs& s, int seg, int chunks, int32_t* d_status,
+                                           bool report_errors) {
+    IdxSeg g;
+    g.b = seg / chunks;
+    const int c = seg - g.b * chunks;
+    g.ctx = __ldg(s.ctx_len + g.b);
+    const int qs = __ldg(s.q_start + g.b), qe = __ldg(s.q_start + g.b + 1);
+    g.ok = g.ctx >= 0 && g.ctx <= s.max_ctx && qe >= qs && qe - qs <= s.max_q_per_seq;
+    g.q0 = qs + c * NQ;
+    g.nq = g.ok ? max(0, min(NQ, qe - g.q0)) : 0;
+    g.maxpos = -1;
+    if (!g.ok && report_errors && c == 0) report(d_status, DSA_ERR_BAD_INPUT);
+    for (int i = 0; i < g.nq; ++i) {
+        const int p = __ldg(s.q_pos + g.q0 + i);
+        if (p >= 0 && p < g.ctx) g.maxpos = max(g.maxpos, p);
+    }
+    return g;
+}
+
+// 0 = nothing to do, 1 = only -inf to write (after every query position), 2 = contract
+__device__ __forceinline__ int tile_kind(const IdxSeg& g, int j0) {
+    if (!g.ok || g.nq == 0 || j0 >= g.ctx) return 0;
+    return j0 > g.maxpos ? 1 : 2;
+}
+
+// Walks the CTA's tile range; next() returns the next tile of kind >= min_kind.
+template <int NQ>
+struct TileWalker {
+    int64_t t, t_end;
+    int tiles_per_seq, chunks, cur_seg;
+    IdxSeg g;
+    __device__ TileWalker(int64_t t0, int64_t t1, int tps, int ch) : t(t0 - 1), t_end(t1), tiles_per_seq(tps),
+                                                                     chunks(ch), cur_seg(-1) {}
+    __device__ bool next(const dsa_seqs& s, int min_kind, int32_t* d_status, bool report_errors, int& seg_out,
+                         int& j0_out, int& kind_out) {
+        while (++t < t_end) {
+            const int seg = (int)(t / tiles_per_seq);
+            const int tile = (int)(t - (int64_t)seg * tiles_per_seq);
+            if (seg != cur_seg) {
+                g = load_seg<NQ>(s, seg, chunks, d_status, report_errors);
+                cur_seg = seg;
+            }
+            const int j0 = tile * kTileKeys;
+            const int kind = tile_kind(g, j0);
+            if (kind >= min_kind) {
+                seg_out = seg;
+                j0_out = j0;
+                kind_out = kind;
+                return true;
+            }
+            if (kind < min_kind) {  // every later tile of this segment is of a lower kind too
+                const int64_t seg_end = (int64_t)(seg + 1) * tiles_per_seq;
+                if (kind == 0 || min_kind == 2) t = min(seg_end, t_end) - 1;
+            }
+        }
+        return false;
+    }
 };
 
 template <int NQ, int KP, bool FP8>
-__global__ void __launch_bounds__(256) index_scores_kernel(const uint16_t* __restrict__ qp,
-                                                           const float* __restrict__ wp,
-                                                           const void* __restrict__ k_idx,
-                                                           const float* __restrict__ k_scale, dsa_seqs s,
-                                                           float* __restrict__ scores, int64_t ld,
-                                                           int32_t* d_status) {
-    using L = IdxSmem<NQ, KP>;
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint16_t* sq = reinterpret_cast<uint16_t*>(smem);
-    uint16_t* sk = reinterpret_cast<uint16_t*>(smem + L::q_bytes);
-    uint8_t* sraw = smem + L::q_bytes + L::k_bytes;
-    float* sout = reinterpret_cast<float*>(smem + L::q_bytes + L::k_bytes + L::raw_bytes);
-    float* sw = sout + NQ * kTileKeys;
-    float* sscale = sw + NQ * kIH;
-    int* spos = reinterpret_cast<int*>(sscale + kTileKeys);
+struct IdxCfg {
+    static constexpr int N = NQ * kIH;
+    static constexpr int q_bytes = N * KP * 2;                         // KP/64 blocks of N x 128 B
+    static constexpr int stage_bytes = StageBytes<FP8>::total;
+    static constexpr int budget = 220 * 1024;
+    static constexpr int tail = 5120;  // barriers, TMEM slot, per-warp head weights and positions
+    static constexpr int stages_fit = (budget - q_bytes - 1024 - tail) / stage_bytes;
+    static constexpr int S = stages_fit > 8 ? 8 : stages_fit;
+    static constexpr int threads = FP8 ? 320 : 192;
+    static constexpr int tmem_cols = 2 * N < 32 ? 32 : 2 * N;
+    static constexpr size_t smem = 1024 + (size_t)S * stage_bytes + q_bytes + tail;  // + alignment slack
+    static_assert(S >= 2, "too little shared memory for two stages");
+};
 
-    const int b = blockIdx.y;
-    const int ctx = __ldg(s.ctx_len + b);
-    const int j0 = blockIdx.x * kTileKeys;
-    if (ctx > s.max_ctx || ctx < 0) {
-        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0) report(d_status, DSA_ERR_BAD_INPUT);
-        return;
-    }
-    if (j0 >= ctx) return;
-    const int qs = __ldg(s.q_start + b), qe = __ldg(s.q_start + b + 1);
-    if (qe - qs > s.max_q_per_seq || qe < qs) {
-        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0) report(d_status, DSA_ERR_BAD_INPUT);
-        return;
-    }
-    const int q0 = qs + blockIdx.z * NQ;
-    if (q0 >= qe) return;
-    const int nq = min(NQ, qe - q0);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+template <int NQ, int KP, bool FP8>
+__global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, 1)
+    index_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                    const float* __restrict__ wp, const float* __restrict__ k_scale, dsa_seqs s,
+                    float* __restrict__ scores, int64_t ld, int tiles_per_seq, int chunks, int64_t total_tiles,
+                    int box_rows, int32_t* d_status) {
+    using C = IdxCfg<NQ, KP, FP8>;
+    constexpr int S = C::S, N = C::N;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* stages = base;
+    uint8_t* qs = base + S * C::stage_bytes;  // 1024-aligned (stage bytes are multiples of 1024)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(qs + C::q_bytes);
+    uint64_t* full = bars;               // [S] TMA landed
+    uint64_t* empty = bars + S;          // [S] MMA done reading
+    uint64_t* conv = bars + 2 * S;       // [S] e4m3 decoded (fp8)
+    uint64_t* tfull = bars + 3 * S;      // [2] accumulator ready
+    uint64_t* tempty = bars + 3 * S + 2; // [2] accumulator drained
+    uint64_t* qfull = bars + 3 * S + 4;
+    uint64_t* qempty = bars + 3 * S + 5;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 6);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* sw_all = reinterpret_cast<float*>(tmem_slot + 2);  // [4][NQ*32] head weights, one copy per epilogue warp
+    int* spos_all = reinterpret_cast<int*>(sw_all + 4 * NQ * kIH);  // [4][NQ] query positions
 
-    int maxpos = -1;
-    if (tid < NQ) {
-        int p = tid < nq ? __ldg(s.q_pos + q0 + tid) : -1;
-        if (tid < nq && (p < 0 || p >= ctx)) {
-            report(d_status, DSA_ERR_BAD_INPUT);
-            p = -1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t_begin = total_tiles * blockIdx.x / gridDim.x;
+    const int64_t t_end = total_tiles * (blockIdx.x + 1) / gridDim.x;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            ptx::mbar_init(full + i, 1);
+            ptx::mbar_init(empty + i, 1);
+            ptx::mbar_init(conv + i, 4);
         }
-        spos[tid] = p;
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(tfull + i, 1);
+            ptx::mbar_init(tempty + i, 4);
+        }
+        ptx::mbar_init(qfull, 1);
+        ptx::mbar_init(qempty, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
     }
+    if (warp == 1) {
+        ptx::tmem_alloc(tmem_slot, C::tmem_cols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
     __syncthreads();
-#pragma unroll
-    for (int i = 0; i < NQ; ++i) maxpos = max(maxpos, spos[i]);
-    const int jn = min(kTileKeys, ctx - j0);
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
 
-    if (j0 > maxpos) {  // fully masked tile: -inf only
-        for (int e = tid; e < nq * jn; e += blockDim.x) {
-            const int qi = e / jn, jj = e % jn;
-            scores[(int64_t)(q0 + qi) * ld + j0 + jj] = -INFINITY;
-        }
-        return;
-    }
-
-    // ---- stage q' rows and w'
-    {
-        const int chunks_per_row = KP / 8;  // 16-byte chunks
-        for (int e = tid; e < NQ * kIH * chunks_per_row; e += blockDim.x) {
-            const int r = e / chunks_per_row, c = e % chunks_per_row;
-            const int qi = r / kIH;
-            const bool v = qi < nq;
-            const uint16_t* src = qp + ((int64_t)(q0 + (v ? qi : 0)) * kIH + (r % kIH)) * KP + c * 8;
-            cp_async16(sq + r * L::kQStride + c * 8, src, v);
-        }
-        for (int e = tid; e < NQ * kIH; e += blockDim.x) {
-            const int qi = e / kIH;
-            sw[e] = qi < nq ? __ldg(wp + (int64_t)(q0 + qi) * kIH + (e % kIH)) : 0.f;
-        }
-    }
-    // ---- stage the key tile
-    bool bad_row = false;
-    if (!FP8) {
-        const uint16_t* kb = reinterpret_cast<const uint16_t*>(k_idx);
-        for (int e = tid; e < kTileKeys * 16; e += blockDim.x) {
-            const int r = e >> 4, c = e & 15;
-            int64_t row = r < jn ? phys_row(s, b, j0 + r) : -1;
-            if (r < jn && row < 0) bad_row = true;
-            cp_async16(sk + r * kKeyStride + c * 8, kb + (row < 0 ? 0 : row) * kID + c * 8, row >= 0);
-        }
-        cp_async_commit();
-        if (tid < kTileKeys) sscale[tid] = 1.f;
-        cp_async_wait<0>();
-    } else {
-        const uint8_t* kb = reinterpret_cast<const uint8_t*>(k_idx);
-        for (int e = tid; e < kTileKeys * 8; e += blockDim.x) {
-            const int r = e >> 3, c = e & 7;
-            int64_t row = r < jn ? phys_row(s, b, j0 + r) : -1;
-            if (r < jn && row < 0) bad_row = true;
-            cp_async16(sraw + r * kID + c * 16, kb + (row < 0 ? 0 : row) * kID + c * 16, row >= 0);
-        }
-        cp_async_commit();
-        if (tid < kTileKeys) {
-            int64_t row = tid < jn ? phys_row(s, b, j0 + tid) : -1;
-            float sc = row >= 0 ? __ldg(k_scale + row) : 0.f;
-            if (sc < 0.f) {
-                report(d_status, DSA_ERR_BAD_INPUT);
-                sc = 0.f;
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------ producer
+        ptx::prefetch_tmap(&kmap);
+        ptx::prefetch_tmap(&qmap);
+        TileWalker<NQ> wk(t_begin, t_end, tiles_per_seq, chunks);
+        int seg, j0, kind, q_seg = -1, qloads = 0;
+        int64_t issued = 0;
+        bool alive = true;
+        while (alive && wk.next(s, 2, d_status, false, seg, j0, kind)) {
+            const IdxSeg& g = wk.g;
+            if (seg != q_seg) {
+                if (qloads > 0 && !ptx::mbar_wait(qempty, (qloads - 1) & 1, abort_flag, d_status)) break;
+                ptx::mbar_expect_tx(qfull, C::q_bytes);
+                for (int kb = 0; kb < KP / 64; ++kb)
+                    ptx::tma_load_2d(qs + kb * N * 128, &qmap, kb * 64, g.q0 * kIH, qfull);
+                q_seg = seg;
+                ++qloads;
             }
-            sscale[tid] = sc;
+            const int st = (int)(issued % S);
+            const uint32_t use = (uint32_t)(issued / S);
+            if (issued >= S && !ptx::mbar_wait(empty + st, (use - 1) & 1, abort_flag, d_status)) break;
+            uint8_t* dst = stages + st * C::stage_bytes;
+            const int nb = kTileKeys / box_rows;
+            uint32_t bytes = 0;
+            for (int rb = 0; rb < nb; ++rb) {
+                const int j = j0 + rb * box_rows;
+                if (j >= g.ctx) break;
+                if (phys_row(s, g.b, j) >= 0) bytes += (FP8 ? 1 : 2) * box_rows * 128;
+            }
+            ptx::mbar_expect_tx(full + st, bytes);
+            for (int rb = 0; rb < nb; ++rb) {
+                const int j = j0 + rb * box_rows;
+                if (j >= g.ctx) break;
+                const int64_t row = phys_row(s, g.b, j);
+                if (row < 0) continue;
+                if (FP8) {
+                    ptx::tma_load_2d(dst + rb * box_rows * 128, &kmap, 0, (int)row, full + st);
+                } else {
+                    ptx::tma_load_2d(dst + rb * box_rows * 128, &kmap, 0, (int)row, full + st);
+                    ptx::tma_load_2d(dst + kTileKeys * 128 + rb * box_rows * 128, &kmap, 64, (int)row, full + st);
+                }
+            }
+            ++issued;
         }
-        cp_async_wait<0>();
-        __syncthreads();
-        // e4m3 -> f16 (exact), 8 codes per step
-        for (int e = tid; e < kTileKeys * 16; e += blockDim.x) {
-            const int r = e >> 4, c = e & 15;
-            uint2 raw = *reinterpret_cast<const uint2*>(sraw + r * kID + c * 8);
-            uint4 o;
-            o.x = e4m3x2_to_f16x2((uint16_t)(raw.x & 0xFFFF));
-            o.y = e4m3x2_to_f16x2((uint16_t)(raw.x >> 16));
-            o.z = e4m3x2_to_f16x2((uint16_t)(raw.y & 0xFFFF));
-            o.w = e4m3x2_to_f16x2((uint16_t)(raw.y >> 16));
-            *reinterpret_cast<uint4*>(sk + r * kKeyStride + c * 8) = o;
+        // drain: every issued copy has landed and every MMA reading a stage is done
+        for (int64_t i = issued > S ? issued - S : 0; i < issued; ++i) {
+            const int st = (int)(i % S);
+            const uint32_t ph = (uint32_t)(i / S) & 1;
+            if (!ptx::mbar_drain(empty + st, ph)) ptx::mbar_drain(full + st, ph);
         }
-    }
-    if (bad_row) report(d_status, DSA_ERR_BAD_INPUT);
-    __syncthreads();
-
-    // ---- contraction on the tensor cores
-    constexpr int NT = NQ * 4;  // n-tiles of 8 heads
-    float acc[NT][4];
+        if (qloads > 0) ptx::mbar_drain(qempty, (qloads - 1) & 1);
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = ptx::idesc_f16_m128(N, !FP8);
+        TileWalker<NQ> wk(t_begin, t_end, tiles_per_seq, chunks);
+        int seg, j0, kind, nseg, nj0, nkind;
+        bool have = wk.next(s, 2, d_status, false, seg, j0, kind);
+        int q_seg = -1, qloads = 0;
+        int64_t consumed = 0;
+        while (have) {
+            const bool have_next = wk.next(s, 2, d_status, false, nseg, nj0, nkind);
+            if (seg != q_seg) {
+                if (!ptx::mbar_wait(qfull, qloads & 1, abort_flag, d_status)) break;
+                ++qloads;
+                q_seg = seg;
+            }
+            const int st = (int)(consumed % S);
+            const uint32_t use = (uint32_t)(consumed / S);
+            if (!ptx::mbar_wait(FP8 ? conv + st : full + st, use & 1, abort_flag, d_status)) break;
+            const int a = (int)(consumed & 1);
+            const uint32_t au = (uint32_t)(consumed >> 1);
+            if (consumed >= 2 && !ptx::mbar_wait(tempty + a, (au - 1) & 1, abort_flag, d_status)) break;
+            ptx::tc_fence_after();
+            const uint32_t kbase = smem_u32(stages + st * C::stage_bytes + StageBytes<FP8>::raw);
+            const uint32_t qbase = smem_u32(qs);
 #pragma unroll
-    for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    const uint16_t* arow = sk + (warp * 16 + (lane & 15)) * kKeyStride + (lane >> 4) * 8;
-    const int bl = lane & 7, bm = lane >> 3;
-#pragma unroll
-    for (int ks = 0; ks < KP / 16; ++ks) {
-        int kd;  // key dim of this k-step
-        if (KP == 192) kd = ks < 4 ? ks * 16 : (ks < 8 ? (ks - 4) * 16 : 64 + (ks - 8) * 16);
-        else kd = ks * 16;
-        uint32_t a[4];
-        ldsm_x4(a[0], a[1], a[2], a[3], arow + kd);
-#pragma unroll
-        for (int nt = 0; nt < NT; nt += 2) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(b0, b1, b2, b3, sq + ((nt + (bm >> 1)) * 8 + bl) * L::kQStride + ks * 16 + (bm & 1) * 8);
+            for (int ks = 0; ks < KP / 16; ++ks) {
+                int kd;  // key dim of this k-step: [hi | lo | unrotated] all read dims 0..63, 0..63, 64..127
+                if (KP == 192) kd = ks < 4 ? ks * 16 : (ks < 8 ? (ks - 4) * 16 : 64 + (ks - 8) * 16);
+                else kd = ks * 16;
+                const uint64_t ad = ptx::sdesc_sw128(kbase + (kd >> 6) * (kTileKeys * 128) + (kd & 63) * 2);
+                const uint64_t bd = ptx::sdesc_sw128(qbase + ((ks * 16) >> 6) * (N * 128) + ((ks * 16) & 63) * 2);
+                ptx::mma_ss(tmem_base + a * N, ad, bd, idesc, ks > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(empty + st);
+            ptx::mma_commit(tfull + a);
+            if (!have_next || nseg != seg) ptx::mma_commit(qempty);
+            ++consumed;
+            have = have_next;
+            seg = nseg;
+            j0 = nj0;
+            kind = nkind;
+        }
+    } else if (warp >= 2 && warp < 6) {
+        // ------------------------------------------------------------ epilogue
+        // each epilogue warp keeps its own copy of the chunk's weights and
+        // positions, so the warps never wait on each other
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        float* sw = sw_all + (warp - 2) * NQ * kIH;
+        int* spos = spos_all + (warp - 2) * NQ;
+        TileWalker<NQ> wk(t_begin, t_end, tiles_per_seq, chunks);
+        int seg, j0, kind, cur = -1;
+        int64_t consumed = 0;
+        while (wk.next(s, 1, d_status, true, seg, j0, kind)) {
+            const IdxSeg& g = wk.g;
+            if (seg != cur) {
+                __syncwarp();
+                for (int e = lane; e < NQ * kIH; e += 32)
+                    sw[e] = (e / kIH) < g.nq ? __ldg(wp + (int64_t)g.q0 * kIH + e) : 0.f;
+                if (lane < NQ) {
+                    int p = lane < g.nq ? __ldg(s.q_pos + g.q0 + lane) : -1;
+                    if (lane < g.nq && (p < 0 || p >= g.ctx)) {
+                        report(d_status, DSA_ERR_BAD_INPUT);
+                        p = -1;
+                    }
+                    spos[lane] = p;
+                }
+                __syncwarp();
+                cur = seg;
+            }
+            const int j = j0 + row;
+            const bool in_ctx = j < g.ctx;
+            if (kind == 1) {
+                if (in_ctx)
+                    for (int q = 0; q < g.nq; ++q) scores[(int64_t)(g.q0 + q) * ld + j] = -INFINITY;
+                continue;
+            }
+            const int a = (int)(consumed & 1);
+            const uint32_t au = (uint32_t)(consumed >> 1);
+            // warp-uniform outcome: a lane that sees an abort takes the whole warp out
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(tfull + a, au & 1, abort_flag, d_status))) break;
+            ptx::tc_fence_after();
+            const int64_t prow = in_ctx ? phys_row(s, g.b, j) : -1;
+            if (in_ctx && prow < 0) report(d_status, DSA_ERR_BAD_INPUT);
+            float sigma = 1.f;
             if (FP8) {
-                mma_f16(acc[nt], a, b0, b1);
-                mma_f16(acc[nt + 1], a, b2, b3);
-            } else {
-                mma_bf16(acc[nt], a, b0, b1);
-                mma_bf16(acc[nt + 1], a, b2, b3);
+                sigma = prow >= 0 ? __ldg(k_scale + prow) : 0.f;
+                if (sigma < 0.f) {
+                    report(d_status, DSA_ERR_BAD_INPUT);
+                    sigma = 0.f;
+                }
             }
+#pragma unroll 1
+            for (int q = 0; q < NQ; ++q) {
+                float v[32];
+                ptx::tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + a * N + q * 32, v);
+                float acc = 0.f;
+#pragma unroll
+                for (int h = 0; h < 32; ++h) acc = fmaf(sw[q * kIH + h], fmaxf(v[h], 0.f), acc);
+                if (in_ctx && q < g.nq)
+                    scores[(int64_t)(g.q0 + q) * ld + j] = (prow >= 0 && j <= spos[q]) ? acc * sigma : -INFINITY;
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(tempty + a);
+            ++consumed;
+        }
+    } else if (FP8 && warp >= 6) {
+        // ------------------------------------------------------------ e4m3 -> f16 (exact)
+        const int r = threadIdx.x - 192;  // key row of the tile
+        TileWalker<NQ> wk(t_begin, t_end, tiles_per_seq, chunks);
+        int seg, j0, kind;
+        int64_t n = 0;
+        while (wk.next(s, 2, d_status, false, seg, j0, kind)) {
+            const int st = (int)(n % S);
+            const uint32_t use = (uint32_t)(n / S);
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(full + st, use & 1, abort_flag, d_status))) break;
+            const uint8_t* raw = stages + st * C::stage_bytes + r * kID;
+            uint8_t* out = stages + st * C::stage_bytes + StageBytes<FP8>::raw;
+#pragma unroll
+            for (int step = 0; step < 8; ++step) {
+                const int i = (step + r) & 7;  // 16 codes -> dims 16i .. 16i+15
+                const uint4 c = *reinterpret_cast<const uint4*>(raw + i * 16);
+                const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+                uint32_t h[8];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    h[2 * u] = e4m3x2_to_f16x2((uint16_t)(w4[u] & 0xFFFF));
+                    h[2 * u + 1] = e4m3x2_to_f16x2((uint16_t)(w4[u] >> 16));
+                }
+                const int kb = i >> 2, c0 = (i & 3) * 2;
+                uint8_t* rowp = out + kb * (kTileKeys * 128) + r * 128;
+                *reinterpret_cast<uint4*>(rowp + ((c0 ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(conv + st);
+            ++n;
         }
     }
-    // ---- epilogue: relu, head weights, sum over 32 heads
-    const int g = lane >> 2, c = lane & 3;
-#pragma unroll
-    for (int qi = 0; qi < NQ; ++qi) {
-        float p0 = 0.f, p1 = 0.f;  // keys g and g+8 of this warp
-#pragma unroll
-        for (int n4 = 0; n4 < 4; ++n4) {
-            const int nt = qi * 4 + n4;
-            const int h = n4 * 8 + 2 * c;
-            const float w0 = sw[qi * kIH + h], w1 = sw[qi * kIH + h + 1];
-            p0 += w0 * fmaxf(acc[nt][0], 0.f) + w1 * fmaxf(acc[nt][1], 0.f);
-            p1 += w0 * fmaxf(acc[nt][2], 0.f) + w1 * fmaxf(acc[nt][3], 0.f);
-        }
-        p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
-        p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
-        p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
-        p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
-        if (c == 0) {
-            const int r0 = warp * 16 + g, r1 = r0 + 8;
-            const int pos = spos[qi];
-            sout[qi * kTileKeys + r0] = (j0 + r0 <= pos) ? p0 * sscale[r0] : -INFINITY;
-            sout[qi * kTileKeys + r1] = (j0 + r1 <= pos) ? p1 * sscale[r1] : -INFINITY;
-        }
-    }
+    ptx::tc_fence_before();
     __syncthreads();
-    for (int e = tid; e < nq * jn; e += blockDim.x) {
-        const int qi = e / jn, jj = e % jn;
-        scores[(int64_t)(q0 + qi) * ld + j0 + jj] = sout[qi * kTileKeys + jj];
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, C::tmem_cols);
     }
 }
 
+// ---------------------------------------------------------------------------
+// host side
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+cudaError_t make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    auto enc = tmap_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    return n;
+}
+
 template <int NQ, int KP, bool FP8>
-static cudaError_t launch_scores_t(const void* qp, const float* wp, const void* k_idx, const float* k_scale,
-                                   const dsa_seqs& s, float* scores, int64_t ld, int32_t* d_status,
-                                   cudaStream_t stream) {
-    using L = IdxSmem<NQ, KP>;
-    auto kern = index_scores_kernel<NQ, KP, FP8>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::total);
+cudaError_t launch_tc(const void* qp, int num_q, const float* wp, const void* k_idx, const float* k_scale,
+                      const dsa_seqs& s, float* scores, int64_t ld, int32_t* d_status, cudaStream_t stream) {
+    using C = IdxCfg<NQ, KP, FP8>;
+    const int box_rows = s.page_table ? std::min(64, s.page_size & -s.page_size) : kTileKeys;
+    CUtensorMap kmap, qmap;
+    cudaError_t e;
+    if (FP8)
+        e = make_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, k_idx, kID, (uint64_t)s.num_rows, kID, kID, box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
+    else
+        e = make_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_idx, kID, (uint64_t)s.num_rows, kID * 2, 64,
+                     box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
-    dim3 grid((s.max_ctx + kTileKeys - 1) / kTileKeys, s.num_seqs, (s.max_q_per_seq + NQ - 1) / NQ);
-    kern<<<grid, 256, L::total, stream>>>(reinterpret_cast<const uint16_t*>(qp), wp, k_idx, k_scale, s, scores, ld,
-                                          d_status);
+    e = make_map(&qmap, FP8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qp, KP,
+                 (uint64_t)num_q * kIH, KP * 2, 64, C::N, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+    auto kern = index_tc_kernel<NQ, KP, FP8>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int tiles_per_seq = (s.max_ctx + kTileKeys - 1) / kTileKeys;
+    const int chunks = (s.max_q_per_seq + NQ - 1) / NQ;
+    const int64_t total = (int64_t)s.num_seqs * chunks * tiles_per_seq;
+    const int grid = (int)std::min<int64_t>(num_sms(), total);
+    kern<<<grid, C::threads, C::smem, stream>>>(kmap, qmap, wp, k_scale, s, scores, ld, tiles_per_seq, chunks, total,
+                                                box_rows, d_status);
     return cudaGetLastError();
 }
 
 template <int NQ>
-static cudaError_t launch_scores_nq(bool rope, bool fp8, const void* qp, const float* wp, const void* k_idx,
-                                    const float* k_scale, const dsa_seqs& s, float* scores, int64_t ld,
-                                    int32_t* d_status, cudaStream_t stream) {
+cudaError_t launch_tc_nq(bool rope, bool fp8, const void* qp, int num_q, const float* wp, const void* k_idx,
+                         const float* k_scale, const dsa_seqs& s, float* scores, int64_t ld, int32_t* d_status,
+                         cudaStream_t stream) {
     if (rope)
-        return fp8 ? launch_scores_t<NQ, 192, true>(qp, wp, k_idx, k_scale, s, scores, ld, d_status, stream)
-                   : launch_scores_t<NQ, 192, false>(qp, wp, k_idx, k_scale, s, scores, ld, d_status, stream);
-    return fp8 ? launch_scores_t<NQ, 128, true>(qp, wp, k_idx, k_scale, s, scores, ld, d_status, stream)
-               : launch_scores_t<NQ, 128, false>(qp, wp, k_idx, k_scale, s, scores, ld, d_status, stream);
+        return fp8 ? launch_tc<NQ, 192, true>(qp, num_q, wp, k_idx, k_scale, s, scores, ld, d_status, stream)
+                   : launch_tc<NQ, 192, false>(qp, num_q, wp, k_idx, k_scale, s, scores, ld, d_status, stream);
+    return fp8 ? launch_tc<NQ, 128, true>(qp, num_q, wp, k_idx, k_scale, s, scores, ld, d_status, stream)
+               : launch_tc<NQ, 128, false>(qp, num_q, wp, k_idx, k_scale, s, scores, ld, d_status, stream);
 }
+
+}  // namespace
 
 cudaError_t launch_index_scores(const void* q_idx, const float* w, const float* ssmax_s, const float* ssmax_b,
                                 const float* inv_freq, const void* k_idx, const float* k_scale, dsa_dtype k_dtype,
@@ -327,10 +574,10 @@ cudaError_t launch_index_scores(const void* q_idx, const float* w, const float* 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int mq = s.max_q_per_seq;
-    if (mq <= 1) return launch_scores_nq<1>(rope, fp8, ws.qprep, ws.wprep, k_idx, k_scale, s, scores, ld, d_status, stream);
-    if (mq <= 2) return launch_scores_nq<2>(rope, fp8, ws.qprep, ws.wprep, k_idx, k_scale, s, scores, ld, d_status, stream);
-    if (mq <= 4) return launch_scores_nq<4>(rope, fp8, ws.qprep, ws.wprep, k_idx, k_scale, s, scores, ld, d_status, stream);
-    return launch_scores_nq<8>(rope, fp8, ws.qprep, ws.wprep, k_idx, k_scale, s, scores, ld, d_status, stream);
+    if (mq <= 1) return launch_tc_nq<1>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, d_status, stream);
+    if (mq <= 2) return launch_tc_nq<2>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, d_status, stream);
+    if (mq <= 4) return launch_tc_nq<4>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, d_status, stream);
+    return launch_tc_nq<8>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, d_status, stream);
 }
 
 }  // namespace dsa

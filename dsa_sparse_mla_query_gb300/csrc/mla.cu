@@ -383,42 +383,44 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
 
 // LSE combine of the splits of one query ([vLLM-ML4] DCP: LSE combine):
 //   M = max_s m_s, out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
-__global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restrict__ part_o,
+// One block per (query, 4 heads).
+constexpr int kCombineHeads = 4;
+__global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restrict__ part_o,
                                                           const float* __restrict__ part_ml, int splits,
                                                           __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
-    __shared__ float wgt[kMH * 16];
-    __shared__ float inv_l[kMH];
-    const int t = blockIdx.x;
+    __shared__ float wgt[kCombineHeads * 16];
+    __shared__ float inv_l[kCombineHeads];
+    const int t = blockIdx.x, h0 = blockIdx.y * kCombineHeads;
     const float* ml = part_ml + (int64_t)t * splits * kMH * 2;
-    if (threadIdx.x < kMH) {
-        const int h = threadIdx.x;
+    if (threadIdx.x < kCombineHeads) {
+        const int h = h0 + threadIdx.x;
         float M = -INFINITY;
         for (int sp = 0; sp < splits; ++sp) M = fmaxf(M, ml[(sp * kMH + h) * 2]);
         float L = 0.f;
         for (int sp = 0; sp < splits; ++sp) {
             const float m = ml[(sp * kMH + h) * 2];
             const float wv = (M == -INFINITY) ? 0.f : exp2f(m - M);
-            wgt[h * 16 + sp] = wv;
+            wgt[threadIdx.x * 16 + sp] = wv;
             L += wv * ml[(sp * kMH + h) * 2 + 1];
         }
-        inv_l[h] = L > 0.f ? 1.f / L : 0.f;
+        inv_l[threadIdx.x] = L > 0.f ? 1.f / L : 0.f;
         if (lse) lse[(int64_t)t * kMH + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
     }
     __syncthreads();
-    const float* po = part_o + (int64_t)t * splits * kMH * kMV;
-    __nv_bfloat16* ot = out + (int64_t)t * kMH * kMV;
-    for (int e = threadIdx.x; e < kMH * kMV / 4; e += blockDim.x) {
-        const int h = (e * 4) / kMV;
+    const float* po = part_o + (int64_t)t * splits * kMH * kMV + (int64_t)h0 * kMV;
+    __nv_bfloat16* ot = out + (int64_t)t * kMH * kMV + (int64_t)h0 * kMV;
+    for (int e = threadIdx.x; e < kCombineHeads * kMV / 4; e += blockDim.x) {
+        const int hh = (e * 4) / kMV;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int sp = 0; sp < splits; ++sp) {
-            const float wv = wgt[h * 16 + sp];
+            const float wv = wgt[hh * 16 + sp];
             const float4 v = *reinterpret_cast<const float4*>(po + (int64_t)sp * kMH * kMV + e * 4);
             acc.x += wv * v.x;
             acc.y += wv * v.y;
             acc.z += wv * v.z;
             acc.w += wv * v.w;
         }
-        const float il = inv_l[h];
+        const float il = inv_l[hh];
         uint2 o;
         o.x = pack_bf16(acc.x * il, acc.y * il);
         o.y = pack_bf16(acc.z * il, acc.w * il);
@@ -441,7 +443,7 @@ cudaError_t launch_sparse_mla(const void* q, const void* latent, dsa_dtype laten
         scale_log2, splits, reinterpret_cast<__nv_bfloat16*>(out), lse, ws.mla_part, ws.mla_ml, d_status);
     e = cudaGetLastError();
     if (e != cudaSuccess || splits == 1) return e;
-    mla_combine_kernel<<<num_q, 256, 0, stream>>>(ws.mla_part, ws.mla_ml, splits,
+    mla_combine_kernel<<<dim3(num_q, kMH / kCombineHeads), 128, 0, stream>>>(ws.mla_part, ws.mla_ml, splits,
                                                    reinterpret_cast<__nv_bfloat16*>(out), lse);
     return cudaGetLastError();
 }
