@@ -64,8 +64,8 @@ void check_seqs(Check& c, const dsa_seqs* s, int32_t num_q) {
     c.ptr(s->q_pos, "seqs.q_pos", 4);
     if (s->page_table) {
         c.ptr(s->page_table, "seqs.page_table", 4);
-        c.need(s->page_size >= 16 && s->page_size % 16 == 0, DSA_ERR_UNSUPPORTED,
-               "page_size %d is not a positive multiple of 16", s->page_size);
+        c.need(s->page_size >= 16 && (s->page_size & (s->page_size - 1)) == 0, DSA_ERR_UNSUPPORTED,
+               "page_size %d is not a power of two >= 16", s->page_size);
         c.need(s->max_pages >= 1, DSA_ERR_INVALID_ARG, "max_pages %d < 1", s->max_pages);
     } else {
         c.ptr(s->seq_base, "seqs.seq_base (page_table is NULL)", 8);

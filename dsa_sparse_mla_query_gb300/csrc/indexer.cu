@@ -143,6 +143,7 @@ struct StageBytes {
 struct IdxSeg {
     int b, ctx, q0, nq, maxpos;
     bool ok;
+    int64_t base;  // first physical row (contiguous caches)
 };
 
 template <int NQ>
@@ -157,6 +158,7 @@ __device__ __forceinline__ IdxSeg load_seg(const dsa_seqs& s, int seg, int chunk
     g.q0 = qs + c * NQ;
     g.nq = g.ok ? max(0, min(NQ, qe - g.q0)) : 0;
     g.maxpos = -1;
+    g.base = s.page_table ? 0 : __ldg(s.seq_base + g.b);
     if (!g.ok && report_errors && c == 0) report(d_status, DSA_ERR_BAD_INPUT);
     for (int i = 0; i < g.nq; ++i) {
         const int p = __ldg(s.q_pos + g.q0 + i);
@@ -171,19 +173,20 @@ __device__ __forceinline__ int tile_kind(const IdxSeg& g, int j0) {
     return j0 > g.maxpos ? 1 : 2;
 }
 
-// Walks the CTA's tile range; next() returns the next tile of kind >= min_kind.
+// Walks the CTA's tile range in order (no division per tile); next() returns
+// the next tile of kind >= min_kind and skips the rest of a segment once no
+// later tile of it can qualify.
 template <int NQ>
 struct TileWalker {
     int64_t t, t_end;
-    int tiles_per_seq, chunks, cur_seg;
+    int seg, tile, tiles_per_seq, chunks, cur_seg;
     IdxSeg g;
-    __device__ TileWalker(int64_t t0, int64_t t1, int tps, int ch) : t(t0 - 1), t_end(t1), tiles_per_seq(tps),
-                                                                     chunks(ch), cur_seg(-1) {}
+    __device__ TileWalker(int64_t t0, int64_t t1, int tps, int ch)
+        : t(t0), t_end(t1), seg((int)(t0 / tps)), tile((int)(t0 - (t0 / tps) * tps)), tiles_per_seq(tps), chunks(ch),
+          cur_seg(-1) {}
     __device__ bool next(const dsa_seqs& s, int min_kind, int32_t* d_status, bool report_errors, int& seg_out,
                          int& j0_out, int& kind_out) {
-        while (++t < t_end) {
-            const int seg = (int)(t / tiles_per_seq);
-            const int tile = (int)(t - (int64_t)seg * tiles_per_seq);
+        while (t < t_end) {
             if (seg != cur_seg) {
                 g = load_seg<NQ>(s, seg, chunks, d_status, report_errors);
                 cur_seg = seg;
@@ -194,12 +197,17 @@ struct TileWalker {
                 seg_out = seg;
                 j0_out = j0;
                 kind_out = kind;
+                ++t;
+                if (++tile == tiles_per_seq) {
+                    tile = 0;
+                    ++seg;
+                }
                 return true;
             }
-            if (kind < min_kind) {  // every later tile of this segment is of a lower kind too
-                const int64_t seg_end = (int64_t)(seg + 1) * tiles_per_seq;
-                if (kind == 0 || min_kind == 2) t = min(seg_end, t_end) - 1;
-            }
+            // every later tile of this segment is of this kind or lower
+            t += tiles_per_seq - tile;
+            tile = 0;
+            ++seg;
         }
         return false;
     }
@@ -273,57 +281,96 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 0 && lane == 0) {
+    if (warp == 0) {
         // ------------------------------------------------------------ producer
-        ptx::prefetch_tmap(&kmap);
-        ptx::prefetch_tmap(&qmap);
+        // The whole warp walks the tiles; lanes fetch 32 page-table entries at
+        // a time, lane 0 waits on the ring and issues the TMA copies.
+        if (lane == 0) {
+            ptx::prefetch_tmap(&kmap);
+            ptx::prefetch_tmap(&qmap);
+        }
         TileWalker<NQ> wk(t_begin, t_end, tiles_per_seq, chunks);
         int seg, j0, kind, q_seg = -1, qloads = 0;
         int64_t issued = 0;
-        bool alive = true;
-        while (alive && wk.next(s, 2, d_status, false, seg, j0, kind)) {
+        int win_b = -1, win_p0 = 0, win_entry = -1;
+        const int ps_log2 = s.page_table ? __ffs(s.page_size) - 1 : 7;  // page size is a power of two
+        const int ps_mask = (1 << ps_log2) - 1;
+        const int nb = kTileKeys / box_rows;
+        while (wk.next(s, 2, d_status, false, seg, j0, kind)) {
             const IdxSeg& g = wk.g;
+            bool ok = true;
             if (seg != q_seg) {
-                if (qloads > 0 && !ptx::mbar_wait(qempty, (qloads - 1) & 1, abort_flag, d_status)) break;
-                ptx::mbar_expect_tx(qfull, C::q_bytes);
-                for (int kb = 0; kb < KP / 64; ++kb)
-                    ptx::tma_load_2d(qs + kb * N * 128, &qmap, kb * 64, g.q0 * kIH, qfull);
+                if (lane == 0) {
+                    ok = qloads == 0 || ptx::mbar_wait(qempty, (qloads - 1) & 1, abort_flag, d_status);
+                    if (ok) {
+                        ptx::mbar_expect_tx(qfull, C::q_bytes);
+                        for (int kb = 0; kb < KP / 64; ++kb)
+                            ptx::tma_load_2d(qs + kb * N * 128, &qmap, kb * 64, g.q0 * kIH, qfull);
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
                 q_seg = seg;
                 ++qloads;
             }
-            const int st = (int)(issued % S);
-            const uint32_t use = (uint32_t)(issued / S);
-            if (issued >= S && !ptx::mbar_wait(empty + st, (use - 1) & 1, abort_flag, d_status)) break;
-            uint8_t* dst = stages + st * C::stage_bytes;
-            const int nb = kTileKeys / box_rows;
-            uint32_t bytes = 0;
-            for (int rb = 0; rb < nb; ++rb) {
-                const int j = j0 + rb * box_rows;
-                if (j >= g.ctx) break;
-                if (phys_row(s, g.b, j) >= 0) bytes += (FP8 ? 1 : 2) * box_rows * 128;
-            }
-            ptx::mbar_expect_tx(full + st, bytes);
-            for (int rb = 0; rb < nb; ++rb) {
-                const int j = j0 + rb * box_rows;
-                if (j >= g.ctx) break;
-                const int64_t row = phys_row(s, g.b, j);
-                if (row < 0) continue;
-                if (FP8) {
-                    ptx::tma_load_2d(dst + rb * box_rows * 128, &kmap, 0, (int)row, full + st);
-                } else {
-                    ptx::tma_load_2d(dst + rb * box_rows * 128, &kmap, 0, (int)row, full + st);
-                    ptx::tma_load_2d(dst + kTileKeys * 128 + rb * box_rows * 128, &kmap, 64, (int)row, full + st);
+            // physical rows of the tile's row blocks (-1: past the context or invalid)
+            const int jn = min(kTileKeys, g.ctx - j0);
+            int64_t rows[kTileKeys / 16];
+            if (s.page_table) {
+                const int p_first = j0 >> ps_log2, p_last = (j0 + jn - 1) >> ps_log2;
+                if (g.b != win_b || p_first < win_p0 || p_last >= win_p0 + 32) {
+                    win_b = g.b;
+                    win_p0 = p_first;
+                    const int p = win_p0 + lane;
+                    win_entry = p < s.max_pages ? __ldg(s.page_table + (int64_t)g.b * s.max_pages + p) : -1;
+                }
+#pragma unroll
+                for (int rb = 0; rb < kTileKeys / 16; ++rb) {
+                    const int j = j0 + rb * box_rows;
+                    const int entry = __shfl_sync(0xffffffffu, win_entry, ((j >> ps_log2) - win_p0) & 31);
+                    const int64_t row = ((int64_t)entry << ps_log2) + (j & ps_mask);
+                    rows[rb] = (rb < nb && rb * box_rows < jn && entry >= 0 && row + box_rows <= s.num_rows)
+                                   ? row : -1;
+                }
+            } else {
+#pragma unroll
+                for (int rb = 0; rb < kTileKeys / 16; ++rb) {
+                    const int64_t row = g.base + j0 + rb * box_rows;
+                    rows[rb] = (rb < nb && rb * box_rows < jn && row >= 0 && row < s.num_rows) ? row : -1;
                 }
             }
+            if (lane == 0) {
+                const int st = (int)(issued % S);
+                const uint32_t use = (uint32_t)(issued / S);
+                ok = issued < S || ptx::mbar_wait(empty + st, (use - 1) & 1, abort_flag, d_status);
+                if (ok) {
+                    uint8_t* dst = stages + st * C::stage_bytes;
+                    uint32_t bytes = 0;
+#pragma unroll
+                    for (int rb = 0; rb < kTileKeys / 16; ++rb)
+                        if (rows[rb] >= 0) bytes += (FP8 ? 1 : 2) * box_rows * 128;
+                    ptx::mbar_expect_tx(full + st, bytes);
+#pragma unroll
+                    for (int rb = 0; rb < kTileKeys / 16; ++rb) {
+                        if (rows[rb] < 0) continue;
+                        ptx::tma_load_2d(dst + rb * box_rows * 128, &kmap, 0, (int)rows[rb], full + st);
+                        if (!FP8)
+                            ptx::tma_load_2d(dst + kTileKeys * 128 + rb * box_rows * 128, &kmap, 64, (int)rows[rb],
+                                             full + st);
+                    }
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             ++issued;
         }
         // drain: every issued copy has landed and every MMA reading a stage is done
-        for (int64_t i = issued > S ? issued - S : 0; i < issued; ++i) {
-            const int st = (int)(i % S);
-            const uint32_t ph = (uint32_t)(i / S) & 1;
-            if (!ptx::mbar_drain(empty + st, ph)) ptx::mbar_drain(full + st, ph);
+        if (lane == 0) {
+            for (int64_t i = issued > S ? issued - S : 0; i < issued; ++i) {
+                const int st = (int)(i % S);
+                const uint32_t ph = (uint32_t)(i / S) & 1;
+                if (!ptx::mbar_drain(empty + st, ph)) ptx::mbar_drain(full + st, ph);
+            }
+            if (qloads > 0) ptx::mbar_drain(qempty, (qloads - 1) & 1);
         }
-        if (qloads > 0) ptx::mbar_drain(qempty, (qloads - 1) & 1);
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------------ MMA issuer
         constexpr uint32_t idesc = ptx::idesc_f16_m128(N, !FP8);
@@ -401,20 +448,30 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, 1)
                     for (int q = 0; q < g.nq; ++q) scores[(int64_t)(g.q0 + q) * ld + j] = -INFINITY;
                 continue;
             }
+            // the row's physical location and scale load while the MMA runs
+            int64_t prow = -1;
+            if (in_ctx) {
+                if (s.page_table) {
+                    const int ps_log2 = __ffs(s.page_size) - 1;
+                    const int p = j >> ps_log2;
+                    const int64_t page = p < s.max_pages ? __ldg(s.page_table + (int64_t)g.b * s.max_pages + p) : -1;
+                    prow = page >= 0 ? (page << ps_log2) + (j & ((1 << ps_log2) - 1)) : -1;
+                } else {
+                    prow = g.base + j;
+                }
+                if (prow >= s.num_rows) prow = -1;
+            }
+            float sigma = 1.f;
+            if (FP8) sigma = prow >= 0 ? __ldg(k_scale + prow) : 0.f;
             const int a = (int)(consumed & 1);
             const uint32_t au = (uint32_t)(consumed >> 1);
             // warp-uniform outcome: a lane that sees an abort takes the whole warp out
             if (!__all_sync(0xffffffffu, ptx::mbar_wait(tfull + a, au & 1, abort_flag, d_status))) break;
             ptx::tc_fence_after();
-            const int64_t prow = in_ctx ? phys_row(s, g.b, j) : -1;
             if (in_ctx && prow < 0) report(d_status, DSA_ERR_BAD_INPUT);
-            float sigma = 1.f;
-            if (FP8) {
-                sigma = prow >= 0 ? __ldg(k_scale + prow) : 0.f;
-                if (sigma < 0.f) {
-                    report(d_status, DSA_ERR_BAD_INPUT);
-                    sigma = 0.f;
-                }
+            if (FP8 && sigma < 0.f) {
+                report(d_status, DSA_ERR_BAD_INPUT);
+                sigma = 0.f;
             }
 #pragma unroll 1
             for (int q = 0; q < NQ; ++q) {

@@ -47,6 +47,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// As above, but the thread may sleep in hardware until the phase completes or
+// about `ns` nanoseconds pass, instead of spinning on the issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
 
 // Waits for the phase with this parity to complete.  Returns false when the
 // CTA aborts (another role timed out) or this wait times out (then it raises
@@ -56,7 +67,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000)) return true;
         if (*abort_flag) return false;
         if (globaltimer() - t0 > kWaitTimeoutNs) {
             *abort_flag = 1;
@@ -69,7 +80,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // Short bounded wait that ignores the abort flag (draining after an abort).
 __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
     const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity))
+    while (!mbar_try_wait_sleep(bar, parity, 20000))
         if (globaltimer() - t0 > kDrainTimeoutNs) return false;
     return true;
 }

@@ -86,7 +86,7 @@ typedef struct {
     int32_t num_seqs;         /* host: B >= 1 */
     int32_t max_ctx;          /* host: >= every ctx_len[b]; sizes the grids */
     int32_t max_q_per_seq;    /* host: >= every q_start[b+1]-q_start[b] */
-    int32_t page_size;        /* host: tokens per page (page_table only), multiple of 16 */
+    int32_t page_size;        /* host: tokens per page (page_table only), a power of two >= 16 */
     int32_t max_pages;        /* host: columns of page_table */
     int32_t reserved;
     int64_t num_rows;         /* host: physical rows in every cache, for bounds checks */

@@ -83,7 +83,7 @@ def test_workspace_size_and_refusals(lib):
     rc = lib.dsa_topk(0x104, 4096, ctypes.byref(s2), 1, 2048, 0x200, 0x300, None, 0, None, None)
     assert rc != 0
     msg = lib.dsa_last_error_string().decode()
-    assert "scores is not 16-byte aligned" in msg and "page_size 10" in msg
+    assert "scores is not 16-byte aligned" in msg and "page_size 10 is not a power of two" in msg
 
 
 def test_zero_queries_is_a_no_op(lib):
