@@ -218,8 +218,12 @@ struct IdxCfg {
     static constexpr int N = NQ * kIH;
     static constexpr int q_bytes = N * KP * 2;                         // KP/64 blocks of N x 128 B
     static constexpr int stage_bytes = StageBytes<FP8>::total;
-    static constexpr int budget = 220 * 1024;
-    static constexpr int tail = 5120;  // barriers, TMEM slot, per-warp head weights and positions
+    // Decode shapes (small q') run two persistent CTAs per SM, so two
+    // producer / MMA-issuer pairs overlap their per-tile issue work.
+    static constexpr int tail_raw = (3 * 8 + 6) * 8 + 8 + 4 * NQ * kIH * 4 + 4 * NQ * 4;
+    static constexpr int tail = (tail_raw + 1023) / 1024 * 1024;  // barriers, TMEM slot, per-warp weights
+    static constexpr int ctas_per_sm = (110 * 1024 - q_bytes - 1024 - tail) / stage_bytes >= 2 ? 2 : 1;
+    static constexpr int budget = (ctas_per_sm == 2 ? 110 : 220) * 1024;
     static constexpr int stages_fit = (budget - q_bytes - 1024 - tail) / stage_bytes;
     static constexpr int S = stages_fit > 8 ? 8 : stages_fit;
     static constexpr int threads = FP8 ? 320 : 192;
@@ -229,7 +233,7 @@ struct IdxCfg {
 };
 
 template <int NQ, int KP, bool FP8>
-__global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, 1)
+__global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, FP8>::ctas_per_sm)
     index_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                     const float* __restrict__ wp, const float* __restrict__ k_scale, dsa_seqs s,
                     float* __restrict__ scores, int64_t ld, int tiles_per_seq, int chunks, int64_t total_tiles,
@@ -295,7 +299,7 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, 1)
         int win_b = -1, win_p0 = 0, win_entry = -1;
         const int ps_log2 = s.page_table ? __ffs(s.page_size) - 1 : 7;  // page size is a power of two
         const int ps_mask = (1 << ps_log2) - 1;
-        const int nb = kTileKeys / box_rows;
+        const int nb = kTileKeys / box_rows;  // row blocks per tile (<= 8, so <= 16 boxes <= 32 lanes)
         while (wk.next(s, 2, d_status, false, seg, j0, kind)) {
             const IdxSeg& g = wk.g;
             bool ok = true;
@@ -312,9 +316,13 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, 1)
                 q_seg = seg;
                 ++qloads;
             }
-            // physical rows of the tile's row blocks (-1: past the context or invalid)
+            // One TMA box per lane: lane L takes row block L >> 1 (L for e4m3)
+            // and, for bf16, K-half L & 1.  Rows past the context or behind an
+            // invalid page are not loaded (the epilogue masks and reports them).
             const int jn = min(kTileKeys, g.ctx - j0);
-            int64_t rows[kTileKeys / 16];
+            const int rb = FP8 ? lane : (lane >> 1), half = FP8 ? 0 : (lane & 1);
+            const int j = j0 + rb * box_rows;
+            int64_t row = -1;
             if (s.page_table) {
                 const int p_first = j0 >> ps_log2, p_last = (j0 + jn - 1) >> ps_log2;
                 if (g.b != win_b || p_first < win_p0 || p_last >= win_p0 + 32) {
@@ -323,41 +331,24 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, 1)
                     const int p = win_p0 + lane;
                     win_entry = p < s.max_pages ? __ldg(s.page_table + (int64_t)g.b * s.max_pages + p) : -1;
                 }
-#pragma unroll
-                for (int rb = 0; rb < kTileKeys / 16; ++rb) {
-                    const int j = j0 + rb * box_rows;
-                    const int entry = __shfl_sync(0xffffffffu, win_entry, ((j >> ps_log2) - win_p0) & 31);
-                    const int64_t row = ((int64_t)entry << ps_log2) + (j & ps_mask);
-                    rows[rb] = (rb < nb && rb * box_rows < jn && entry >= 0 && row + box_rows <= s.num_rows)
-                                   ? row : -1;
-                }
+                const int entry = __shfl_sync(0xffffffffu, win_entry, ((j >> ps_log2) - win_p0) & 31);
+                const int64_t r = ((int64_t)entry << ps_log2) + (j & ps_mask);
+                if (rb < nb && rb * box_rows < jn && entry >= 0 && r + box_rows <= s.num_rows) row = r;
             } else {
-#pragma unroll
-                for (int rb = 0; rb < kTileKeys / 16; ++rb) {
-                    const int64_t row = g.base + j0 + rb * box_rows;
-                    rows[rb] = (rb < nb && rb * box_rows < jn && row >= 0 && row < s.num_rows) ? row : -1;
-                }
+                const int64_t r = g.base + j;
+                if (rb < nb && rb * box_rows < jn && r >= 0 && r < s.num_rows) row = r;
             }
+            const uint32_t loads = __ballot_sync(0xffffffffu, row >= 0);
+            const int st = (int)(issued % S);
             if (lane == 0) {
-                const int st = (int)(issued % S);
                 const uint32_t use = (uint32_t)(issued / S);
                 ok = issued < S || ptx::mbar_wait(empty + st, (use - 1) & 1, abort_flag, d_status);
-                if (ok) {
-                    uint8_t* dst = stages + st * C::stage_bytes;
-                    uint32_t bytes = 0;
-#pragma unroll
-                    for (int rb = 0; rb < kTileKeys / 16; ++rb)
-                        if (rows[rb] >= 0) bytes += (FP8 ? 1 : 2) * box_rows * 128;
-                    ptx::mbar_expect_tx(full + st, bytes);
-#pragma unroll
-                    for (int rb = 0; rb < kTileKeys / 16; ++rb) {
-                        if (rows[rb] < 0) continue;
-                        ptx::tma_load_2d(dst + rb * box_rows * 128, &kmap, 0, (int)rows[rb], full + st);
-                        if (!FP8)
-                            ptx::tma_load_2d(dst + kTileKeys * 128 + rb * box_rows * 128, &kmap, 64, (int)rows[rb],
-                                             full + st);
-                    }
-                }
+                if (ok) ptx::mbar_expect_tx(full + st, (uint32_t)__popc(loads) * box_rows * 128);
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (ok && row >= 0) {
+                uint8_t* dst = stages + st * C::stage_bytes + half * (kTileKeys * 128) + rb * box_rows * 128;
+                ptx::tma_load_2d(dst, &kmap, half * 64, (int)row, full + st);
             }
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             ++issued;
@@ -595,7 +586,7 @@ cudaError_t launch_tc(const void* qp, int num_q, const float* wp, const void* k_
     const int tiles_per_seq = (s.max_ctx + kTileKeys - 1) / kTileKeys;
     const int chunks = (s.max_q_per_seq + NQ - 1) / NQ;
     const int64_t total = (int64_t)s.num_seqs * chunks * tiles_per_seq;
-    const int grid = (int)std::min<int64_t>(num_sms(), total);
+    const int grid = (int)std::min<int64_t>((int64_t)C::ctas_per_sm * num_sms(), total);
     kern<<<grid, C::threads, C::smem, stream>>>(kmap, qmap, wp, k_scale, s, scores, ld, tiles_per_seq, chunks, total,
                                                 box_rows, d_status);
     return cudaGetLastError();
