@@ -19,7 +19,11 @@
 // fp8_ds_mla rows are dequantised in-kernel: e4m3 codes decode exactly to
 // bf16, the four per-group scales multiply the per-group partial scores and
 // fold into the probabilities of the value product.
-#include "dsa_internal.cuh"
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "tc_ptx.cuh"
 
 namespace dsa {
 
@@ -428,16 +432,482 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restric
     }
 }
 
+// ---------------------------------------------------------------------------
+// bf16 latent cache on the 5th-generation tensor cores.
+//
+// One CTA = one query x one split of its selected slots, tiles of 64 rows:
+//   warp 0     gathers the tile's 64 selected rows with TMA gather4 (4 rows per
+//              copy, one 64-dim block per copy, 128-byte swizzle), two stages;
+//              the 64 query heads are loaded once by TMA;
+//   warp 1     issues tcgen05.mma: S^T = K Q^T (M = 128 rows of which the 64
+//              gathered keys are used, N = 64 heads, K = 576) into TMEM, then
+//              O^T += V^T P^T (M = 128 value dims per block, N = 64 heads,
+//              K = 64 keys; V^T is the same gathered tile read MN-major);
+//   warps 4-5  softmax, one key per thread straight from TMEM: per-head tile
+//              max (warp max + exchange), exp2, row sums, P^T to shared memory;
+//              the running max is raised only when a head's tile max exceeds
+//              it by more than 2^8 (then O^T is rescaled in TMEM);
+//   warps 2-5  rescale O^T (rare) and write the output or the split partial.
+namespace tcmla {
+constexpr int TK = 64;                     // selected rows per tile
+constexpr int KB = kMD / 64;               // 9 blocks of 64 dims
+constexpr int kKBlock = TK * 128;          // bytes of one 64-dim block of a tile
+constexpr int kStage = KB * kKBlock;       // 73728
+constexpr int kQBytes = KB * kMH * 128;    // 73728
+constexpr int kPBytes = TK * 128;          // P^T: 64 keys x 64 heads, bf16
+constexpr int kMisc = 3072;
+constexpr size_t kSmem = 2 * (size_t)kStage + kQBytes + kPBytes + kMisc;
+constexpr float kRescale = 8.f;            // log2 headroom before O^T is rescaled
+constexpr uint32_t kOCol = 0;              // O^T: 4 blocks x 64 heads
+constexpr uint32_t kSCol = 256;            // S^T: 2 buffers x 64 heads
+constexpr uint32_t kTmemCols = 512;
+}  // namespace tcmla
+
+__global__ void __launch_bounds__(192, 1)
+    mla_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap lmap, dsa_seqs s,
+                  const int32_t* __restrict__ idx, const int32_t* __restrict__ topk_len, int k, float scale_log2,
+                  int splits, __nv_bfloat16* __restrict__ out, float* __restrict__ lse, float* __restrict__ part_o,
+                  float* __restrict__ part_ml, int32_t* d_status) {
+    using namespace tcmla;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint8_t* stage = smem;                                  // [2][KB][TK rows x 128 B]
+    uint8_t* qs = smem + 2 * kStage;                        // [KB][64 heads x 128 B]
+    uint8_t* ps = qs + kQBytes;                             // [TK keys x 128 B]
+    uint8_t* misc = ps + kPBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
+    uint64_t* qfull = bars + 0;
+    uint64_t* kfull = bars + 1;   // [2] gathered tile landed
+    uint64_t* kempty = bars + 3;  // [2] tile no longer read by the MMA
+    uint64_t* sfull = bars + 5;   // [2] S^T ready
+    uint64_t* sempty = bars + 7;  // [2] S^T read by the softmax warps
+    uint64_t* xch = bars + 9;     // [2] tile maxima of both softmax warps written
+    uint64_t* dec = bars + 11;    // rescale decision of the tile written
+    uint64_t* pfull = bars + 12;  // P^T written and O^T rescaled (4 warps)
+    uint64_t* pvdone = bars + 13; // O^T += V^T P^T of the tile complete
+    uint64_t* ofull = bars + 14;  // last product complete
+    uint64_t* lready = bars + 15; // row sums of both softmax warps written
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* srow = reinterpret_cast<int*>(misc + 160);          // [2][TK] gathered row (-1 = masked)
+    float* wmax = reinterpret_cast<float*>(misc + 672);      // [2 parity][2 warps][64]
+    float* mu = reinterpret_cast<float*>(misc + 1696);       // [2 warps][64] running max (log2 units)
+    float* alpha = reinterpret_cast<float*>(misc + 2208);    // [2 parity][64] rescale factors (warp 4's copy)
+    int* need = reinterpret_cast<int*>(misc + 2720);         // [2 parity]
+    // row sums [2 warps][64] reuse srow: after the last tile's max exchange no
+    // thread reads srow again
+    float* lsum = reinterpret_cast<float*>(srow);
+
+    const int t = blockIdx.y, sp = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = seq_of(s.q_start, s.num_seqs, t);
+    const int ctx = __ldg(s.ctx_len + b);
+    int len = __ldg(topk_len + t);
+    if (len < 0 || len > k || ctx > s.max_ctx) {
+        if (threadIdx.x == 0 && sp == 0) report(d_status, DSA_ERR_BAD_INPUT);
+        len = 0;
+    }
+    const int per = ((k + splits - 1) / splits + TK - 1) / TK * TK;
+    const int slot0 = sp * per;
+    const int slot1 = min(slot0 + per, len);
+    const int ntiles = slot1 > slot0 ? (slot1 - slot0 + TK - 1) / TK : 0;
+    const int32_t* tidx = idx + (int64_t)t * k;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(qfull, 1);
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(kfull + i, 1);
+            ptx::mbar_init(kempty + i, 1);
+            ptx::mbar_init(sfull + i, 1);
+            ptx::mbar_init(sempty + i, 2);
+            ptx::mbar_init(xch + i, 2);
+        }
+        ptx::mbar_init(dec, 1);
+        ptx::mbar_init(pfull, 4);
+        ptx::mbar_init(pvdone, 1);
+        ptx::mbar_init(ofull, 1);
+        ptx::mbar_init(lready, 2);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(tmem_slot, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ gather
+        if (lane == 0 && ntiles > 0) {
+            ptx::prefetch_tmap(&qmap);
+            ptx::prefetch_tmap(&lmap);
+            ptx::mbar_expect_tx(qfull, kQBytes);
+            for (int kb = 0; kb < KB; ++kb) ptx::tma_load_2d(qs + kb * kMH * 128, &qmap, kb * 64, t * kMH, qfull);
+        }
+        int issued = 0;
+        for (int i = 0; i < ntiles; ++i) {
+            const int st = i & 1;
+            // the tile's 64 rows: lane l resolves slots 2l and 2l+1
+            int rows2[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int slot = slot0 + i * TK + 2 * lane + u;
+                int row = -1;
+                if (slot < slot1) {
+                    const int j = __ldg(tidx + slot);
+                    if (j >= ctx || j < -1) {
+                        report(d_status, DSA_ERR_BAD_INPUT);
+                    } else if (j >= 0) {
+                        const int64_t r = phys_row(s, b, j);
+                        if (r < 0) report(d_status, DSA_ERR_BAD_INPUT);
+                        else row = (int)r;
+                    }
+                }
+                rows2[u] = row;
+            }
+            bool ok = true;
+            if (lane == 0 && i >= 2) ok = ptx::mbar_wait(kempty + st, ((i >> 1) - 1) & 1, abort_flag, d_status);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            srow[st * TK + 2 * lane] = rows2[0];
+            srow[st * TK + 2 * lane + 1] = rows2[1];
+            // rows 4g..4g+3 come from lanes 2g and 2g+1; masked rows read row 0
+            const int g = lane & 15;
+            const int r0 = __shfl_sync(0xffffffffu, rows2[0], 2 * g), r1 = __shfl_sync(0xffffffffu, rows2[1], 2 * g);
+            const int r2 = __shfl_sync(0xffffffffu, rows2[0], 2 * g + 1), r3 = __shfl_sync(0xffffffffu, rows2[1], 2 * g + 1);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_expect_tx(kfull + st, kStage);
+            __syncwarp();
+            if (lane < 16) {
+                uint8_t* dst = stage + st * kStage + g * 512;
+#pragma unroll
+                for (int kb = 0; kb < KB; ++kb)
+                    ptx::tma_gather4(dst + kb * kKBlock, &lmap, kb * 64, max(r0, 0), max(r1, 0), max(r2, 0),
+                                     max(r3, 0), kfull + st);
+            }
+            issued = i + 1;
+        }
+        // drain: the last copies have landed and the MMA no longer reads them
+        if (lane == 0) {
+            for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
+                if (!ptx::mbar_drain(kempty + (i & 1), (i >> 1) & 1)) ptx::mbar_drain(kfull + (i & 1), (i >> 1) & 1);
+            if (ntiles > 0) ptx::mbar_drain(qfull, 0);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && ntiles > 0) {
+            constexpr uint32_t idesc_s = ptx::idesc_f16_m128(kMH, true);
+            constexpr uint32_t idesc_pv = ptx::idesc_f16_m128(kMH, true, true, true);
+            const uint32_t qb = smem_u32(qs), pb = smem_u32(ps);
+            bool ok = ptx::mbar_wait(qfull, 0, abort_flag, d_status);
+            auto issue_pv = [&](int i) -> bool {  // O^T += V^T P^T for tile i
+                if (!ptx::mbar_wait(pfull, i & 1, abort_flag, d_status)) return false;
+                ptx::tc_fence_after();
+                const uint32_t kbase = smem_u32(stage + (i & 1) * kStage);
+#pragma unroll
+                for (int db = 0; db < 4; ++db)
+#pragma unroll
+                    for (int kk = 0; kk < TK / 16; ++kk) {
+                        const uint64_t ad = ptx::sdesc_sw128_mn(kbase + 2 * db * kKBlock + kk * 2048, kKBlock, 1024);
+                        const uint64_t bd = ptx::sdesc_sw128_mn(pb + kk * 2048, kKBlock, 1024);
+                        ptx::mma_ss(tmem + kOCol + db * kMH, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+                    }
+                ptx::mma_commit(kempty + (i & 1));
+                ptx::mma_commit(pvdone);
+                return true;
+            };
+            for (int i = 0; ok && i < ntiles; ++i) {
+                const int st = i & 1;
+                if (!ptx::mbar_wait(kfull + st, (i >> 1) & 1, abort_flag, d_status)) break;
+                if (i >= 2 && !ptx::mbar_wait(sempty + st, ((i >> 1) - 1) & 1, abort_flag, d_status)) break;
+                ptx::tc_fence_after();
+                const uint32_t kbase = smem_u32(stage + st * kStage);
+#pragma unroll
+                for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t ad = ptx::sdesc_sw128(kbase + kb * kKBlock + ks * 32);
+                        const uint64_t bd = ptx::sdesc_sw128(qb + kb * kMH * 128 + ks * 32);
+                        ptx::mma_ss(tmem + kSCol + st * kMH, ad, bd, idesc_s, (kb > 0 || ks > 0) ? 1u : 0u);
+                    }
+                ptx::mma_commit(sfull + st);
+                if (i >= 1 && !issue_pv(i - 1)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (ok && issue_pv(ntiles - 1)) ptx::mma_commit(ofull);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax (4,5) and output (2..5)
+        const bool sm = warp >= 4;
+        const int quarter = warp & 3;                       // TMEM lanes 32*quarter ..
+        const int sw = warp - 4;                            // softmax warp index
+        const int key = quarter * 32 + lane;                // softmax: key row of the tile (< 64)
+        float l[kMH];
+#pragma unroll
+        for (int h = 0; h < kMH; ++h) l[h] = 0.f;
+        float* my_mu = mu + (sm ? sw : 0) * kMH;
+        if (sm) {
+            my_mu[lane] = -INFINITY;
+            my_mu[lane + 32] = -INFINITY;
+            __syncwarp();
+        }
+        bool alive = true;
+        for (int i = 0; alive && i < ntiles; ++i) {
+            const int st = i & 1;
+            if (sm) {
+                float sv[kMH];
+                // the producer's row list of this stage, then the scores
+                if (!__all_sync(0xffffffffu, ptx::mbar_wait(kfull + st, (i >> 1) & 1, abort_flag, d_status) &&
+                                                 ptx::mbar_wait(sfull + st, (i >> 1) & 1, abort_flag, d_status))) {
+                    alive = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + kSCol + st * kMH, sv);
+                ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + kSCol + st * kMH + 32, sv + 32);
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(sempty + st);
+                const bool valid = srow[st * TK + key] >= 0;
+#pragma unroll
+                for (int h = 0; h < kMH; ++h) sv[h] = valid ? sv[h] * scale_log2 : -INFINITY;
+                // tile maxima of this warp's 32 keys, then of both warps
+                float* wm = wmax + (st * 2 + sw) * kMH;
+#pragma unroll
+                for (int h = 0; h < kMH; ++h) {
+                    const float m = ptx::warp_max(sv[h]);
+                    if (lane == (h & 31)) wm[h] = m;
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(xch + st);
+                if (!__all_sync(0xffffffffu, ptx::mbar_wait(xch + st, (i >> 1) & 1, abort_flag, d_status))) {
+                    alive = false;
+                    break;
+                }
+                // new running max for heads lane and lane+32 (both warps compute the same)
+                const float* w0 = wmax + (st * 2) * kMH;
+                const float* w1 = w0 + kMH;
+                float a_lo = 1.f, a_hi = 1.f;
+                bool grow = false;
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int h = lane + 32 * u;
+                    const float mt = fmaxf(w0[h], w1[h]);
+                    const float mo = my_mu[h];
+                    float mn = mo;
+                    if (i == 0) mn = mt;
+                    else if (mt > mo + kRescale) { mn = mt; grow = true; }
+                    const float a = (mo == -INFINITY || mn == mo) ? (mo == mn ? 1.f : 0.f) : exp2f(mo - mn);
+                    if (u == 0) a_lo = a; else a_hi = a;
+                    my_mu[h] = mn;
+                }
+                const bool rescale = __any_sync(0xffffffffu, grow);
+                if (sw == 0) {
+                    alpha[st * kMH + lane] = a_lo;
+                    alpha[st * kMH + lane + 32] = a_hi;
+                    if (lane == 0) need[st] = rescale ? 1 : 0;
+                }
+                __syncwarp();
+                if (sw == 0 && lane == 0) ptx::mbar_arrive(dec);
+                // P^T buffer and O^T are free once the previous product completes
+                if (i >= 1 && !__all_sync(0xffffffffu, ptx::mbar_wait(pvdone, (i - 1) & 1, abort_flag, d_status))) {
+                    alive = false;
+                    break;
+                }
+                if (rescale) {
+                    // O^T lanes of this warp: value dims 32*quarter.. of each block; columns = heads
+                    ptx::tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < 8; ++c) {
+                        float o[32];
+                        const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + kOCol + c * 32;
+                        ptx::tmem_ld32(ta, o);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] *= __shfl_sync(0xffffffffu, (c & 1) ? a_hi : a_lo, j);
+                        ptx::tmem_st32(ta, o);
+                    }
+#pragma unroll
+                    for (int h = 0; h < kMH; ++h) l[h] *= __shfl_sync(0xffffffffu, h < 32 ? a_lo : a_hi, h & 31);
+                }
+                // probabilities of this key, row sums, P^T row (128 bytes, swizzled)
+                uint32_t pk[kMH / 2];
+#pragma unroll
+                for (int h = 0; h < kMH; h += 2) {
+                    const float m0 = my_mu[h], m1 = my_mu[h + 1];
+                    const float p0 = m0 == -INFINITY ? 0.f : exp2f(sv[h] - m0);
+                    const float p1 = m1 == -INFINITY ? 0.f : exp2f(sv[h + 1] - m1);
+                    l[h] += p0;
+                    l[h + 1] += p1;
+                    pk[h / 2] = pack_bf16(p0, p1);
+                }
+                uint8_t* prow = ps + key * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4*>(prow + ((c ^ (key & 7)) << 4)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                ptx::fence_proxy_async_smem();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(pfull);
+            } else {
+                // helpers: rescale the O^T lanes 64..127 when the softmax asks for it
+                if (!__all_sync(0xffffffffu, ptx::mbar_wait(dec, i & 1, abort_flag, d_status))) {
+                    alive = false;
+                    break;
+                }
+                if (need[st]) {
+                    if (i >= 1 && !__all_sync(0xffffffffu, ptx::mbar_wait(pvdone, (i - 1) & 1, abort_flag, d_status))) {
+                        alive = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < 8; ++c) {
+                        float o[32];
+                        const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + kOCol + c * 32;
+                        ptx::tmem_ld32(ta, o);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] *= alpha[st * kMH + ((c & 1) * 32 + j)];
+                        ptx::tmem_st32(ta, o);
+                    }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(pfull);
+            }
+        }
+        // ---- row sums of the softmax warps -> lsum[64]; running max -> mu (warp 4's copy)
+        float* ml_m = mu;  // warp 4's running max
+        if (sm && alive && ntiles > 0) {
+#pragma unroll
+            for (int h = 0; h < kMH; ++h) {
+                float v = l[h];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (lane == (h & 31)) lsum[sw * kMH + h] = v;
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(lready);
+        }
+        // ---- output: all four warps, one value dim per thread of each 128-dim block
+        const int dim = quarter * 32 + lane;
+        bool have = alive && ntiles > 0;
+        if (have) have = __all_sync(0xffffffffu, ptx::mbar_wait(lready, 0, abort_flag, d_status));
+        if (have) have = __all_sync(0xffffffffu, ptx::mbar_wait(ofull, 0, abort_flag, d_status));
+        if (have) ptx::tc_fence_after();
+        if (splits == 1) {
+            __nv_bfloat16* ot = out + (int64_t)t * kMH * kMV;
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {  // 32 columns = 32 heads of one 128-dim block
+                float o[32];
+                const int db = c >> 1, h0 = (c & 1) * 32;
+                if (have) ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + kOCol + c * 32, o);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int h = h0 + j;
+                    const float L = have ? lsum[h] + lsum[kMH + h] : 0.f;
+                    const float v = L > 0.f ? o[j] / L : 0.f;
+                    ot[(int64_t)h * kMV + db * 128 + dim] = __float2bfloat16_rn(v);
+                }
+            }
+            if (lse && warp == 2) {
+                for (int h = lane; h < kMH; h += 32) {
+                    const float L = have ? lsum[h] + lsum[kMH + h] : 0.f;
+                    lse[(int64_t)t * kMH + h] = L > 0.f ? (ml_m[h] + log2f(L)) * 0.69314718055994531f : -INFINITY;
+                }
+            }
+        } else {
+            float* po = part_o + ((int64_t)t * splits + sp) * kMH * kMV;
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+                float o[32];
+                const int db = c >> 1, h0 = (c & 1) * 32;
+                if (have) ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + kOCol + c * 32, o);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) po[(int64_t)(h0 + j) * kMV + db * 128 + dim] = have ? o[j] : 0.f;
+            }
+            if (warp == 2) {
+                for (int h = lane; h < kMH; h += 32) {
+                    float* ml = part_ml + (((int64_t)t * splits + sp) * kMH + h) * 2;
+                    const float L = have ? lsum[h] + lsum[kMH + h] : 0.f;
+                    ml[0] = L > 0.f ? ml_m[h] : -INFINITY;
+                    ml[1] = L;
+                }
+            }
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 mla_tmap_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+cudaError_t bf16_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+    auto enc = mla_tmap_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)kMD, rows};
+    cuuint64_t strides[1] = {(cuuint64_t)kMD * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
 cudaError_t launch_sparse_mla(const void* q, const void* latent, dsa_dtype latent_dtype, const dsa_seqs& s,
                               int num_q, const int32_t* idx, const int32_t* topk_len, int k, float sm_scale,
                               void* out, float* lse, const Workspace& ws, int32_t* d_status, cudaStream_t stream) {
     const bool fp8 = latent_dtype == DSA_FP8_DS_MLA;
     const int splits = mla_splits(num_q, k);
+    const float scale_log2 = sm_scale * 1.4426950408889634f;
+    cudaError_t e;
+    if (!fp8) {
+        CUtensorMap qmap, lmap;
+        if ((e = bf16_map(&qmap, q, (uint64_t)num_q * kMH, 64)) != cudaSuccess) return e;
+        if ((e = bf16_map(&lmap, latent, (uint64_t)s.num_rows, 1)) != cudaSuccess) return e;
+        static bool attr = false;
+        if (!attr) {
+            e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcmla::kSmem);
+            if (e != cudaSuccess) return e;
+            attr = true;
+        }
+        mla_tc_kernel<<<dim3(splits, num_q), 192, tcmla::kSmem, stream>>>(
+            qmap, lmap, s, idx, topk_len, k, scale_log2, splits, reinterpret_cast<__nv_bfloat16*>(out), lse,
+            ws.mla_part, ws.mla_ml, d_status);
+        e = cudaGetLastError();
+        if (e != cudaSuccess || splits == 1) return e;
+        mla_combine_kernel<<<dim3(num_q, kMH / kCombineHeads), 128, 0, stream>>>(
+            ws.mla_part, ws.mla_ml, splits, reinterpret_cast<__nv_bfloat16*>(out), lse);
+        return cudaGetLastError();
+    }
     const size_t smem = MlaSmem::total(fp8);
     auto kern = fp8 ? mla_kernel<true> : mla_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const float scale_log2 = sm_scale * 1.4426950408889634f;
     kern<<<dim3(splits, num_q), kMlaThreads, smem, stream>>>(
         reinterpret_cast<const uint16_t*>(q), reinterpret_cast<const uint8_t*>(latent), s, idx, topk_len, k,
         scale_log2, splits, reinterpret_cast<__nv_bfloat16*>(out), lse, ws.mla_part, ws.mla_ml, d_status);
