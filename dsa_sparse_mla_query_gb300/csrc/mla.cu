@@ -43,10 +43,11 @@ struct MlaSmem {
 };
 
 int mla_splits(int num_q, int k) {
-    const int tiles = (k + kBN - 1) / kBN;
-    int sp = (152 + num_q - 1) / num_q;
+    // one resident CTA per SM: as many splits as fill one wave of 152 SMs
+    const int tiles = (k + 63) / 64;
+    int sp = 152 / (num_q > 0 ? num_q : 1);
     sp = sp < 1 ? 1 : sp;
-    int max_sp = tiles / 2 > 0 ? tiles / 2 : 1;  // at least two tiles per split
+    int max_sp = tiles / 2 > 0 ? tiles / 2 : 1;  // at least two 64-row tiles per split
     if (max_sp > 16) max_sp = 16;                  // the combine holds 16 weights per head
     return sp > max_sp ? max_sp : sp;
 }
@@ -436,18 +437,20 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restric
 // bf16 latent cache on the 5th-generation tensor cores.
 //
 // One CTA = one query x one split of its selected slots, tiles of 64 rows:
-//   warp 0     gathers the tile's 64 selected rows with TMA gather4 (4 rows per
-//              copy, one 64-dim block per copy, 128-byte swizzle), two stages;
-//              the 64 query heads are loaded once by TMA;
-//   warp 1     issues tcgen05.mma: S^T = K Q^T (M = 128 rows of which the 64
-//              gathered keys are used, N = 64 heads, K = 576) into TMEM, then
-//              O^T += V^T P^T (M = 128 value dims per block, N = 64 heads,
-//              K = 64 keys; V^T is the same gathered tile read MN-major);
-//   warps 4-5  softmax, one key per thread straight from TMEM: per-head tile
-//              max (warp max + exchange), exp2, row sums, P^T to shared memory;
-//              the running max is raised only when a head's tile max exceeds
-//              it by more than 2^8 (then O^T is rescaled in TMEM);
-//   warps 2-5  rescale O^T (rare) and write the output or the split partial.
+//   warp 0      loads the 64 query heads (TMA) and resolves each tile's slots
+//               to physical rows (page table) up to three tiles ahead;
+//   warps 6-13  gather the tile's rows: 16-byte loads, 18 per thread in flight,
+//               stored into the 128-byte-swizzled K-major layout (two stages);
+//               random 1,152-byte rows stream fastest this way on GB300;
+//   warp 1      issues tcgen05.mma: S^T = K Q^T (M = 128 rows of which the 64
+//               gathered keys are used, N = 64 heads, K = 576) into TMEM, then
+//               O^T += V^T P^T (M = 128 value dims per block, N = 64 heads,
+//               K = 64 keys; V^T is the same gathered tile read MN-major);
+//   warps 4-5   softmax, one key per thread straight from TMEM: per-head tile
+//               max (warp max + exchange), exp2, row sums kept in TMEM, P^T to
+//               shared memory; the running max is raised only when a head's
+//               tile max exceeds it by more than 2^8 (then O^T is rescaled);
+//   warps 2-5   rescale O^T (rare) and write the output or the split partial.
 namespace tcmla {
 constexpr int TK = 64;                     // selected rows per tile
 constexpr int KB = kMD / 64;               // 9 blocks of 64 dims
@@ -460,11 +463,15 @@ constexpr size_t kSmem = 2 * (size_t)kStage + kQBytes + kPBytes + kMisc;
 constexpr float kRescale = 8.f;            // log2 headroom before O^T is rescaled
 constexpr uint32_t kOCol = 0;              // O^T: 4 blocks x 64 heads
 constexpr uint32_t kSCol = 256;            // S^T: 2 buffers x 64 heads
+constexpr uint32_t kLCol = 384;            // row sums: lanes = keys, columns = heads
 constexpr uint32_t kTmemCols = 512;
+constexpr int kThreads = 448;              // 14 warps
+constexpr int kGatherWarps = 8;
+constexpr int kRing = 3;                   // resolved-row ring depth
 }  // namespace tcmla
 
-__global__ void __launch_bounds__(192, 1)
-    mla_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap lmap, dsa_seqs s,
+__global__ void __launch_bounds__(tcmla::kThreads, 1)
+    mla_tc_kernel(const __grid_constant__ CUtensorMap qmap, const uint8_t* __restrict__ latent, dsa_seqs s,
                   const int32_t* __restrict__ idx, const int32_t* __restrict__ topk_len, int k, float scale_log2,
                   int splits, __nv_bfloat16* __restrict__ out, float* __restrict__ lse, float* __restrict__ part_o,
                   float* __restrict__ part_ml, int32_t* d_status) {
@@ -476,7 +483,7 @@ __global__ void __launch_bounds__(192, 1)
     uint8_t* misc = ps + kPBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
     uint64_t* qfull = bars + 0;
-    uint64_t* kfull = bars + 1;   // [2] gathered tile landed
+    uint64_t* kfull = bars + 1;   // [2] gathered tile stored (8 gather warps)
     uint64_t* kempty = bars + 3;  // [2] tile no longer read by the MMA
     uint64_t* sfull = bars + 5;   // [2] S^T ready
     uint64_t* sempty = bars + 7;  // [2] S^T read by the softmax warps
@@ -486,15 +493,16 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t* pvdone = bars + 13; // O^T += V^T P^T of the tile complete
     uint64_t* ofull = bars + 14;  // last product complete
     uint64_t* lready = bars + 15; // row sums of both softmax warps written
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* srow = reinterpret_cast<int*>(misc + 160);          // [2][TK] gathered row (-1 = masked)
-    float* wmax = reinterpret_cast<float*>(misc + 672);      // [2 parity][2 warps][64]
-    float* mu = reinterpret_cast<float*>(misc + 1696);       // [2 warps][64] running max (log2 units)
-    float* alpha = reinterpret_cast<float*>(misc + 2208);    // [2 parity][64] rescale factors (warp 4's copy)
-    int* need = reinterpret_cast<int*>(misc + 2720);         // [2 parity]
-    // row sums [2 warps][64] reuse srow: after the last tile's max exchange no
-    // thread reads srow again
+    uint64_t* rfull = bars + 16;  // [3] rows of a tile resolved
+    uint64_t* rfree = bars + 19;  // [3] rows of a tile no longer read (8 gather + 2 softmax warps)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 176);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 180);
+    int* srow = reinterpret_cast<int*>(misc + 192);          // [3][TK] physical row (-1 = masked)
+    float* wmax = reinterpret_cast<float*>(misc + 960);      // [2 parity][2 warps][64]
+    float* mu = reinterpret_cast<float*>(misc + 1984);       // [2 warps][64] running max (log2 units)
+    float* alpha = reinterpret_cast<float*>(misc + 2496);    // [2 parity][64] rescale factors (warp 4's copy)
+    int* need = reinterpret_cast<int*>(misc + 3008);         // [2 parity]
+    // row sums [2 warps][64] reuse srow once every tile has been resolved and read
     float* lsum = reinterpret_cast<float*>(srow);
 
     const int t = blockIdx.y, sp = blockIdx.x;
@@ -515,11 +523,15 @@ __global__ void __launch_bounds__(192, 1)
     if (threadIdx.x == 0) {
         ptx::mbar_init(qfull, 1);
         for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(kfull + i, 1);
+            ptx::mbar_init(kfull + i, kGatherWarps);
             ptx::mbar_init(kempty + i, 1);
             ptx::mbar_init(sfull + i, 1);
             ptx::mbar_init(sempty + i, 2);
             ptx::mbar_init(xch + i, 2);
+        }
+        for (int i = 0; i < kRing; ++i) {
+            ptx::mbar_init(rfull + i, 1);
+            ptx::mbar_init(rfree + i, kGatherWarps + 2);
         }
         ptx::mbar_init(dec, 1);
         ptx::mbar_init(pfull, 4);
@@ -539,17 +551,14 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ gather
+        // ------------------------------------------------------------ query load, row resolution
         if (lane == 0 && ntiles > 0) {
             ptx::prefetch_tmap(&qmap);
-            ptx::prefetch_tmap(&lmap);
             ptx::mbar_expect_tx(qfull, kQBytes);
             for (int kb = 0; kb < KB; ++kb) ptx::tma_load_2d(qs + kb * kMH * 128, &qmap, kb * 64, t * kMH, qfull);
         }
-        int issued = 0;
         for (int i = 0; i < ntiles; ++i) {
-            const int st = i & 1;
-            // the tile's 64 rows: lane l resolves slots 2l and 2l+1
+            const int r = i % kRing;
             int rows2[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -560,39 +569,20 @@ __global__ void __launch_bounds__(192, 1)
                     if (j >= ctx || j < -1) {
                         report(d_status, DSA_ERR_BAD_INPUT);
                     } else if (j >= 0) {
-                        const int64_t r = phys_row(s, b, j);
-                        if (r < 0) report(d_status, DSA_ERR_BAD_INPUT);
-                        else row = (int)r;
+                        const int64_t pr = phys_row(s, b, j);
+                        if (pr < 0) report(d_status, DSA_ERR_BAD_INPUT);
+                        else row = (int)pr;
                     }
                 }
                 rows2[u] = row;
             }
             bool ok = true;
-            if (lane == 0 && i >= 2) ok = ptx::mbar_wait(kempty + st, ((i >> 1) - 1) & 1, abort_flag, d_status);
+            if (lane == 0 && i >= kRing) ok = ptx::mbar_wait(rfree + r, ((i / kRing) - 1) & 1, abort_flag, d_status);
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-            srow[st * TK + 2 * lane] = rows2[0];
-            srow[st * TK + 2 * lane + 1] = rows2[1];
-            // rows 4g..4g+3 come from lanes 2g and 2g+1; masked rows read row 0
-            const int g = lane & 15;
-            const int r0 = __shfl_sync(0xffffffffu, rows2[0], 2 * g), r1 = __shfl_sync(0xffffffffu, rows2[1], 2 * g);
-            const int r2 = __shfl_sync(0xffffffffu, rows2[0], 2 * g + 1), r3 = __shfl_sync(0xffffffffu, rows2[1], 2 * g + 1);
+            srow[r * TK + 2 * lane] = rows2[0];
+            srow[r * TK + 2 * lane + 1] = rows2[1];
             __syncwarp();
-            if (lane == 0) ptx::mbar_expect_tx(kfull + st, kStage);
-            __syncwarp();
-            if (lane < 16) {
-                uint8_t* dst = stage + st * kStage + g * 512;
-#pragma unroll
-                for (int kb = 0; kb < KB; ++kb)
-                    ptx::tma_gather4(dst + kb * kKBlock, &lmap, kb * 64, max(r0, 0), max(r1, 0), max(r2, 0),
-                                     max(r3, 0), kfull + st);
-            }
-            issued = i + 1;
-        }
-        // drain: the last copies have landed and the MMA no longer reads them
-        if (lane == 0) {
-            for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
-                if (!ptx::mbar_drain(kempty + (i & 1), (i >> 1) & 1)) ptx::mbar_drain(kfull + (i & 1), (i >> 1) & 1);
-            if (ntiles > 0) ptx::mbar_drain(qfull, 0);
+            if (lane == 0) ptx::mbar_arrive(rfull + r);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -639,47 +629,77 @@ __global__ void __launch_bounds__(192, 1)
             }
             if (ok && issue_pv(ntiles - 1)) ptx::mma_commit(ofull);
         }
+    } else if (warp >= 6) {
+        // ------------------------------------------------------------ gather
+        const int gt = threadIdx.x - 6 * 32;  // 0..255
+        for (int i = 0; i < ntiles; ++i) {
+            const int st = i & 1, r = i % kRing;
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(rfull + r, (i / kRing) & 1, abort_flag, d_status))) break;
+            uint4 v[18];
+#pragma unroll
+            for (int u = 0; u < 18; ++u) {
+                const int e = gt + u * 256;
+                const int row = e / 72, c = e - row * 72;
+                const int pr = srow[r * TK + row];
+                v[u] = __ldg(reinterpret_cast<const uint4*>(latent + (size_t)max(pr, 0) * (kMD * 2)) + c);
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(rfree + r);
+            if (i >= 2 && !__all_sync(0xffffffffu, ptx::mbar_wait(kempty + st, ((i >> 1) - 1) & 1, abort_flag, d_status)))
+                break;
+            uint8_t* dst = stage + st * kStage;
+#pragma unroll
+            for (int u = 0; u < 18; ++u) {
+                const int e = gt + u * 256;
+                const int row = e / 72, c = e - row * 72;
+                *reinterpret_cast<uint4*>(dst + (c >> 3) * kKBlock + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = v[u];
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(kfull + st);
+        }
     } else {
         // ------------------------------------------------------------ softmax (4,5) and output (2..5)
         const bool sm = warp >= 4;
         const int quarter = warp & 3;                       // TMEM lanes 32*quarter ..
         const int sw = warp - 4;                            // softmax warp index
         const int key = quarter * 32 + lane;                // softmax: key row of the tile (< 64)
-        float l[kMH];
-#pragma unroll
-        for (int h = 0; h < kMH; ++h) l[h] = 0.f;
+        const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's TMEM lanes
         float* my_mu = mu + (sm ? sw : 0) * kMH;
         if (sm) {
             my_mu[lane] = -INFINITY;
             my_mu[lane + 32] = -INFINITY;
+            float z[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) z[j] = 0.f;
+            ptx::tmem_st32(tl + kLCol, z);
+            ptx::tmem_st32(tl + kLCol + 32, z);
             __syncwarp();
         }
         bool alive = true;
         for (int i = 0; alive && i < ntiles; ++i) {
-            const int st = i & 1;
+            const int st = i & 1, r = i % kRing;
             if (sm) {
-                float sv[kMH];
-                // the producer's row list of this stage, then the scores
-                if (!__all_sync(0xffffffffu, ptx::mbar_wait(kfull + st, (i >> 1) & 1, abort_flag, d_status) &&
+                if (!__all_sync(0xffffffffu, ptx::mbar_wait(rfull + r, (i / kRing) & 1, abort_flag, d_status) &&
                                                  ptx::mbar_wait(sfull + st, (i >> 1) & 1, abort_flag, d_status))) {
                     alive = false;
                     break;
                 }
-                ptx::tc_fence_after();
-                ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + kSCol + st * kMH, sv);
-                ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + kSCol + st * kMH + 32, sv + 32);
-                ptx::tc_fence_before();
+                const bool valid = srow[r * TK + key] >= 0;
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(sempty + st);
-                const bool valid = srow[st * TK + key] >= 0;
-#pragma unroll
-                for (int h = 0; h < kMH; ++h) sv[h] = valid ? sv[h] * scale_log2 : -INFINITY;
-                // tile maxima of this warp's 32 keys, then of both warps
+                if (lane == 0) ptx::mbar_arrive(rfree + r);
+                ptx::tc_fence_after();
+                // pass 1: this warp's per-head maxima over its 32 keys
                 float* wm = wmax + (st * 2 + sw) * kMH;
 #pragma unroll
-                for (int h = 0; h < kMH; ++h) {
-                    const float m = ptx::warp_max(sv[h]);
-                    if (lane == (h & 31)) wm[h] = m;
+                for (int half = 0; half < 2; ++half) {
+                    float sv[32];
+                    ptx::tmem_ld32(tl + kSCol + st * kMH + half * 32, sv);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float m = ptx::warp_max(valid ? sv[j] * scale_log2 : -INFINITY);
+                        if (lane == j) wm[half * 32 + j] = m;
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(xch + st);
@@ -718,38 +738,48 @@ __global__ void __launch_bounds__(192, 1)
                     break;
                 }
                 if (rescale) {
-                    // O^T lanes of this warp: value dims 32*quarter.. of each block; columns = heads
                     ptx::tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < 8; ++c) {
                         float o[32];
-                        const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + kOCol + c * 32;
-                        ptx::tmem_ld32(ta, o);
+                        ptx::tmem_ld32(tl + kOCol + c * 32, o);
 #pragma unroll
                         for (int j = 0; j < 32; ++j) o[j] *= __shfl_sync(0xffffffffu, (c & 1) ? a_hi : a_lo, j);
-                        ptx::tmem_st32(ta, o);
+                        ptx::tmem_st32(tl + kOCol + c * 32, o);
                     }
-#pragma unroll
-                    for (int h = 0; h < kMH; ++h) l[h] *= __shfl_sync(0xffffffffu, h < 32 ? a_lo : a_hi, h & 31);
                 }
-                // probabilities of this key, row sums, P^T row (128 bytes, swizzled)
-                uint32_t pk[kMH / 2];
-#pragma unroll
-                for (int h = 0; h < kMH; h += 2) {
-                    const float m0 = my_mu[h], m1 = my_mu[h + 1];
-                    const float p0 = m0 == -INFINITY ? 0.f : exp2f(sv[h] - m0);
-                    const float p1 = m1 == -INFINITY ? 0.f : exp2f(sv[h + 1] - m1);
-                    l[h] += p0;
-                    l[h + 1] += p1;
-                    pk[h / 2] = pack_bf16(p0, p1);
-                }
+                // pass 2: probabilities, row sums (TMEM), P^T row (128 bytes, swizzled)
                 uint8_t* prow = ps + key * 128;
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4*>(prow + ((c ^ (key & 7)) << 4)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                ptx::fence_proxy_async_smem();
+                for (int half = 0; half < 2; ++half) {
+                    float sv[32], lv[32];
+                    ptx::tmem_ld32(tl + kSCol + st * kMH + half * 32, sv);
+                    ptx::tmem_ld32(tl + kLCol + half * 32, lv);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const int h = half * 32 + j;
+                        const float m0 = my_mu[h], m1 = my_mu[h + 1];
+                        const float p0 = (!valid || m0 == -INFINITY) ? 0.f : exp2f(sv[j] * scale_log2 - m0);
+                        const float p1 = (!valid || m1 == -INFINITY) ? 0.f : exp2f(sv[j + 1] * scale_log2 - m1);
+                        const float s0 = rescale ? __shfl_sync(0xffffffffu, half ? a_hi : a_lo, j) : 1.f;
+                        const float s1 = rescale ? __shfl_sync(0xffffffffu, half ? a_hi : a_lo, j + 1) : 1.f;
+                        lv[j] = lv[j] * s0 + p0;
+                        lv[j + 1] = lv[j + 1] * s1 + p1;
+                        pk[j / 2] = pack_bf16(p0, p1);
+                    }
+                    ptx::tmem_st32(tl + kLCol + half * 32, lv);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int cc = half * 4 + c;
+                        *reinterpret_cast<uint4*>(prow + ((cc ^ (key & 7)) << 4)) =
+                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    }
+                }
                 ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(sempty + st);
+                ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(pfull);
             } else {
@@ -767,11 +797,10 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll 1
                     for (int c = 0; c < 8; ++c) {
                         float o[32];
-                        const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + kOCol + c * 32;
-                        ptx::tmem_ld32(ta, o);
+                        ptx::tmem_ld32(tl + kOCol + c * 32, o);
 #pragma unroll
                         for (int j = 0; j < 32; ++j) o[j] *= alpha[st * kMH + ((c & 1) * 32 + j)];
-                        ptx::tmem_st32(ta, o);
+                        ptx::tmem_st32(tl + kOCol + c * 32, o);
                     }
                 }
                 ptx::tc_fence_before();
@@ -779,15 +808,21 @@ __global__ void __launch_bounds__(192, 1)
                 if (lane == 0) ptx::mbar_arrive(pfull);
             }
         }
-        // ---- row sums of the softmax warps -> lsum[64]; running max -> mu (warp 4's copy)
+        // ---- row sums of the softmax warps -> lsum[2][64]
         float* ml_m = mu;  // warp 4's running max
         if (sm && alive && ntiles > 0) {
+            ptx::tc_fence_after();
 #pragma unroll
-            for (int h = 0; h < kMH; ++h) {
-                float v = l[h];
+            for (int half = 0; half < 2; ++half) {
+                float lv[32];
+                ptx::tmem_ld32(tl + kLCol + half * 32, lv);
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane == (h & 31)) lsum[sw * kMH + h] = v;
+                for (int j = 0; j < 32; ++j) {
+                    float v = lv[j];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == j) lsum[sw * kMH + half * 32 + j] = v;
+                }
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(lready);
@@ -804,7 +839,7 @@ __global__ void __launch_bounds__(192, 1)
             for (int c = 0; c < 8; ++c) {  // 32 columns = 32 heads of one 128-dim block
                 float o[32];
                 const int db = c >> 1, h0 = (c & 1) * 32;
-                if (have) ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + kOCol + c * 32, o);
+                if (have) ptx::tmem_ld32(tl + kOCol + c * 32, o);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int h = h0 + j;
@@ -825,7 +860,7 @@ __global__ void __launch_bounds__(192, 1)
             for (int c = 0; c < 8; ++c) {
                 float o[32];
                 const int db = c >> 1, h0 = (c & 1) * 32;
-                if (have) ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + kOCol + c * 32, o);
+                if (have) ptx::tmem_ld32(tl + kOCol + c * 32, o);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) po[(int64_t)(h0 + j) * kMV + db * 128 + dim] = have ? o[j] : 0.f;
             }
@@ -886,18 +921,17 @@ cudaError_t launch_sparse_mla(const void* q, const void* latent, dsa_dtype laten
     const float scale_log2 = sm_scale * 1.4426950408889634f;
     cudaError_t e;
     if (!fp8) {
-        CUtensorMap qmap, lmap;
+        CUtensorMap qmap;
         if ((e = bf16_map(&qmap, q, (uint64_t)num_q * kMH, 64)) != cudaSuccess) return e;
-        if ((e = bf16_map(&lmap, latent, (uint64_t)s.num_rows, 1)) != cudaSuccess) return e;
         static bool attr = false;
         if (!attr) {
             e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcmla::kSmem);
             if (e != cudaSuccess) return e;
             attr = true;
         }
-        mla_tc_kernel<<<dim3(splits, num_q), 192, tcmla::kSmem, stream>>>(
-            qmap, lmap, s, idx, topk_len, k, scale_log2, splits, reinterpret_cast<__nv_bfloat16*>(out), lse,
-            ws.mla_part, ws.mla_ml, d_status);
+        mla_tc_kernel<<<dim3(splits, num_q), tcmla::kThreads, tcmla::kSmem, stream>>>(
+            qmap, reinterpret_cast<const uint8_t*>(latent), s, idx, topk_len, k, scale_log2, splits,
+            reinterpret_cast<__nv_bfloat16*>(out), lse, ws.mla_part, ws.mla_ml, d_status);
         e = cudaGetLastError();
         if (e != cudaSuccess || splits == 1) return e;
         mla_combine_kernel<<<dim3(num_q, kMH / kCombineHeads), 128, 0, stream>>>(

@@ -206,7 +206,7 @@ dsa_status dsa_decode_layer(const dsa_layer_args* args, const dsa_seqs* seqs, in
  *   clearing between calls; calls that overlap on the GPU (other streams, other
  *   host threads) race on it and must be serialised by the caller.  No call
  *   allocates or frees memory. */
-#define DSA_NOALLOC_SCRATCH_BYTES (32u << 20)
+#define DSA_NOALLOC_SCRATCH_BYTES (16u << 20)
 dsa_status sparse_mla_decode_noalloc(const void* q, const void* latent, dsa_dtype latent_dtype,
                                      const dsa_seqs* seqs, int32_t num_q, const int32_t* idx,
                                      const int32_t* topk_len, int32_t k, float sm_scale, void* out, float* lse,

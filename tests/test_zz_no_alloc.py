@@ -66,18 +66,18 @@ def test_noalloc_matches_workspace_entry_point(name, fp8):
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch():
-    """140 queries need 2 splits x 140 x 131,584 bytes > 32 MiB: refused on
+    """64 queries take 2 splits, 2 x 64 x 131,584 bytes > 16 MiB: refused on
     the host with both sizes in the message, nothing enqueued."""
     lib = B.load() if B._lib is not None else None
     if lib is None:
         from dsa_sparse_mla_query_gb300 import build
         build.build()
         lib = B.load()
-    s = B.DsaSeqsC(num_seqs=140, max_ctx=4096, max_q_per_seq=1, page_size=0, max_pages=0, reserved=0,
-                   num_rows=140 * 4096, ctx_len=0x1000, q_start=0x2000, q_pos=0x3000, page_table=None,
+    s = B.DsaSeqsC(num_seqs=64, max_ctx=4096, max_q_per_seq=1, page_size=0, max_pages=0, reserved=0,
+                   num_rows=64 * 4096, ctx_len=0x1000, q_start=0x2000, q_pos=0x3000, page_table=None,
                    seq_base=0x4000)
-    rc = lib.sparse_mla_decode_noalloc(0x100, 0x100, 0, ctypes.byref(s), 140, 0x100, 0x100, 2048,
+    rc = lib.sparse_mla_decode_noalloc(0x100, 0x100, 0, ctypes.byref(s), 64, 0x100, 0x100, 2048,
                                        ctypes.c_float(0.07), 0x100, None, None, None)
     assert rc == B.DSA_ERR_UNSUPPORTED
     msg = lib.dsa_last_error_string().decode()
-    assert "140 queries x 2 splits need" in msg and str(32 << 20) in msg, msg
+    assert "64 queries x 2 splits need" in msg and str(16 << 20) in msg, msg
