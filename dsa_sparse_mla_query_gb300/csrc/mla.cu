@@ -446,10 +446,12 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restric
 //               gathered keys are used, N = 64 heads, K = 576) into TMEM, then
 //               O^T += V^T P^T (M = 128 value dims per block, N = 64 heads,
 //               K = 64 keys; V^T is the same gathered tile read MN-major);
-//   warps 4-5   softmax, one key per thread straight from TMEM: per-head tile
-//               max (warp max + exchange), exp2, row sums kept in TMEM, P^T to
-//               shared memory; the running max is raised only when a head's
-//               tile max exceeds it by more than 2^8 (then O^T is rescaled);
+//   warps 4-5   softmax, one key per thread straight from TMEM: exact per-head
+//               maxima of the first tile set the running max; later tiles only
+//               check that no score exceeds it by more than 2^64 (one flag
+//               exchanged between the two warps) and raise it, rescaling O^T,
+//               only when one does; exp2, row sums kept in TMEM, P^T to shared
+//               memory;
 //   warps 2-5   rescale O^T (rare) and write the output or the split partial.
 namespace tcmla {
 constexpr int TK = 64;                     // selected rows per tile
@@ -460,7 +462,7 @@ constexpr int kQBytes = KB * kMH * 128;    // 73728
 constexpr int kPBytes = TK * 128;          // P^T: 64 keys x 64 heads, bf16
 constexpr int kMisc = 3072;
 constexpr size_t kSmem = 2 * (size_t)kStage + kQBytes + kPBytes + kMisc;
-constexpr float kRescale = 8.f;            // log2 headroom before O^T is rescaled
+constexpr float kRescale = 64.f;           // log2 headroom before O^T is rescaled (bf16 P, fp32 O)
 constexpr uint32_t kOCol = 0;              // O^T: 4 blocks x 64 heads
 constexpr uint32_t kSCol = 256;            // S^T: 2 buffers x 64 heads
 constexpr uint32_t kLCol = 384;            // row sums: lanes = keys, columns = heads
@@ -495,13 +497,15 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
     uint64_t* lready = bars + 15; // row sums of both softmax warps written
     uint64_t* rfull = bars + 16;  // [3] rows of a tile resolved
     uint64_t* rfree = bars + 19;  // [3] rows of a tile no longer read (8 gather + 2 softmax warps)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 176);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 180);
-    int* srow = reinterpret_cast<int*>(misc + 192);          // [3][TK] physical row (-1 = masked)
-    float* wmax = reinterpret_cast<float*>(misc + 960);      // [2 parity][2 warps][64]
-    float* mu = reinterpret_cast<float*>(misc + 1984);       // [2 warps][64] running max (log2 units)
-    float* alpha = reinterpret_cast<float*>(misc + 2496);    // [2 parity][64] rescale factors (warp 4's copy)
-    int* need = reinterpret_cast<int*>(misc + 3008);         // [2 parity]
+    uint64_t* xmax = bars + 22;   // per-head maxima of both softmax warps written (first tile, growth)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 192);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 196);
+    int* need = reinterpret_cast<int*>(misc + 200);          // [2 parity]
+    int* wflag = reinterpret_cast<int*>(misc + 208);         // [2 parity][2 warps] growth flags
+    int* srow = reinterpret_cast<int*>(misc + 256);          // [3][TK] physical row (-1 = masked)
+    float* wmax = reinterpret_cast<float*>(misc + 1024);     // [2 warps][64] per-head maxima
+    float* mu = reinterpret_cast<float*>(misc + 1536);       // [2 warps][64] running max (log2 units)
+    float* alpha = reinterpret_cast<float*>(misc + 2048);    // [2 parity][64] rescale factors (warp 4's copy)
     // row sums [2 warps][64] reuse srow once every tile has been resolved and read
     float* lsum = reinterpret_cast<float*>(srow);
 
@@ -538,6 +542,7 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
         ptx::mbar_init(pvdone, 1);
         ptx::mbar_init(ofull, 1);
         ptx::mbar_init(lready, 2);
+        ptx::mbar_init(xmax, 2);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -607,27 +612,58 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                 ptx::mma_commit(pvdone);
                 return true;
             };
-            for (int i = 0; ok && i < ntiles; ++i) {
-                const int st = i & 1;
-                if (!ptx::mbar_wait(kfull + st, (i >> 1) & 1, abort_flag, d_status)) break;
-                if (i >= 2 && !ptx::mbar_wait(sempty + st, ((i >> 1) - 1) & 1, abort_flag, d_status)) break;
-                ptx::tc_fence_after();
-                const uint32_t kbase = smem_u32(stage + st * kStage);
+            // S^T of a tile is issued as soon as its rows are stored and its TMEM
+            // buffer is free; O^T += V^T P^T as soon as its P^T is written.  The
+            // two streams interleave, so the scores of tile i+1 are computed
+            // while the softmax of tile i runs.
+            int s_next = 0, pv_next = 0;
+            uint64_t t_idle = 0;
+            while (ok && pv_next < ntiles) {
+                bool progressed = false;
+                if (s_next < ntiles) {
+                    const int st = s_next & 1;
+                    if (ptx::mbar_try_wait(kfull + st, (s_next >> 1) & 1) &&
+                        (s_next < 2 || ptx::mbar_try_wait(sempty + st, ((s_next >> 1) - 1) & 1))) {
+                        ptx::tc_fence_after();
+                        const uint32_t kbase = smem_u32(stage + st * kStage);
 #pragma unroll
-                for (int kb = 0; kb < KB; ++kb)
+                        for (int kb = 0; kb < KB; ++kb)
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t ad = ptx::sdesc_sw128(kbase + kb * kKBlock + ks * 32);
-                        const uint64_t bd = ptx::sdesc_sw128(qb + kb * kMH * 128 + ks * 32);
-                        ptx::mma_ss(tmem + kSCol + st * kMH, ad, bd, idesc_s, (kb > 0 || ks > 0) ? 1u : 0u);
+                            for (int ks = 0; ks < 4; ++ks) {
+                                const uint64_t ad = ptx::sdesc_sw128(kbase + kb * kKBlock + ks * 32);
+                                const uint64_t bd = ptx::sdesc_sw128(qb + kb * kMH * 128 + ks * 32);
+                                ptx::mma_ss(tmem + kSCol + st * kMH, ad, bd, idesc_s, (kb > 0 || ks > 0) ? 1u : 0u);
+                            }
+                        ptx::mma_commit(sfull + st);
+                        ++s_next;
+                        progressed = true;
                     }
-                ptx::mma_commit(sfull + st);
-                if (i >= 1 && !issue_pv(i - 1)) {
-                    ok = false;
-                    break;
+                }
+                if (pv_next < s_next && ptx::mbar_try_wait(pfull, pv_next & 1)) {
+                    if (!issue_pv(pv_next)) {
+                        ok = false;
+                        break;
+                    }
+                    ++pv_next;
+                    progressed = true;
+                }
+                if (progressed) {
+                    t_idle = 0;
+                } else {
+                    // bounded idle: give up after the wait limit like every other wait
+                    const uint64_t now = ptx::globaltimer();
+                    if (t_idle == 0) t_idle = now;
+                    else if (now - t_idle > ptx::kWaitTimeoutNs || *abort_flag) {
+                        if (!*abort_flag) {
+                            *abort_flag = 1;
+                            report(d_status, DSA_ERR_TIMEOUT);
+                        }
+                        ok = false;
+                    }
+                    __nanosleep(32);
                 }
             }
-            if (ok && issue_pv(ntiles - 1)) ptx::mma_commit(ofull);
+            if (ok) ptx::mma_commit(ofull);
         }
     } else if (warp >= 6) {
         // ------------------------------------------------------------ gather
@@ -677,6 +713,7 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
             __syncwarp();
         }
         bool alive = true;
+        int n_grow = 0;  // exact-maxima exchanges so far (same count in both softmax warps)
         for (int i = 0; alive && i < ntiles; ++i) {
             const int st = i & 1, r = i % kRing;
             if (sm) {
@@ -689,42 +726,61 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(rfree + r);
                 ptx::tc_fence_after();
-                // pass 1: this warp's per-head maxima over its 32 keys
-                float* wm = wmax + (st * 2 + sw) * kMH;
+                // does any score of this tile rise more than 2^64 above the running max?
+                bool grow = i == 0;
+                if (i > 0) {
+                    float over = -INFINITY;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float sv[32];
-                    ptx::tmem_ld32(tl + kSCol + st * kMH + half * 32, sv);
+                    for (int half = 0; half < 2; ++half) {
+                        float sv[32];
+                        ptx::tmem_ld32(tl + kSCol + st * kMH + half * 32, sv);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float m = ptx::warp_max(valid ? sv[j] * scale_log2 : -INFINITY);
-                        if (lane == j) wm[half * 32 + j] = m;
+                        for (int j = 0; j < 32; ++j) over = fmaxf(over, sv[j] * scale_log2 - my_mu[half * 32 + j]);
                     }
+                    const bool g = __any_sync(0xffffffffu, valid && over > kRescale);
+                    if (lane == 0) wflag[st * 2 + sw] = g ? 1 : 0;
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(xch + st);
+                    // xch[st] serves tiles 1, 2, 3, ... (not 0): use u of it is tile 2u+1 or 2u+2
+                    if (!__all_sync(0xffffffffu, ptx::mbar_wait(xch + st, ((i - 1) >> 1) & 1, abort_flag, d_status))) {
+                        alive = false;
+                        break;
+                    }
+                    grow = wflag[st * 2] || wflag[st * 2 + 1];
                 }
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(xch + st);
-                if (!__all_sync(0xffffffffu, ptx::mbar_wait(xch + st, (i >> 1) & 1, abort_flag, d_status))) {
-                    alive = false;
-                    break;
-                }
-                // new running max for heads lane and lane+32 (both warps compute the same)
-                const float* w0 = wmax + (st * 2) * kMH;
-                const float* w1 = w0 + kMH;
                 float a_lo = 1.f, a_hi = 1.f;
-                bool grow = false;
+                if (grow) {
+                    // exact per-head maxima of this tile (first tile, or a growth)
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int h = lane + 32 * u;
-                    const float mt = fmaxf(w0[h], w1[h]);
-                    const float mo = my_mu[h];
-                    float mn = mo;
-                    if (i == 0) mn = mt;
-                    else if (mt > mo + kRescale) { mn = mt; grow = true; }
-                    const float a = (mo == -INFINITY || mn == mo) ? (mo == mn ? 1.f : 0.f) : exp2f(mo - mn);
-                    if (u == 0) a_lo = a; else a_hi = a;
-                    my_mu[h] = mn;
+                    for (int half = 0; half < 2; ++half) {
+                        float sv[32];
+                        ptx::tmem_ld32(tl + kSCol + st * kMH + half * 32, sv);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float m = ptx::warp_max(valid ? sv[j] * scale_log2 : -INFINITY);
+                            if (lane == j) wmax[sw * kMH + half * 32 + j] = m;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(xmax);
+                    if (!__all_sync(0xffffffffu, ptx::mbar_wait(xmax, n_grow & 1, abort_flag, d_status))) {
+                        alive = false;
+                        break;
+                    }
+                    ++n_grow;
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int h = lane + 32 * u;
+                        const float mt = fmaxf(wmax[h], wmax[kMH + h]);
+                        const float mo = my_mu[h];
+                        const float mn = fmaxf(mo, mt);
+                        const float a = (mo == -INFINITY || mn == mo) ? (mo == mn ? 1.f : 0.f) : exp2f(mo - mn);
+                        if (u == 0) a_lo = a; else a_hi = a;
+                        my_mu[h] = mn;
+                    }
+                    __syncwarp();
                 }
-                const bool rescale = __any_sync(0xffffffffu, grow);
+                const bool rescale = grow && i > 0;
                 if (sw == 0) {
                     alpha[st * kMH + lane] = a_lo;
                     alpha[st * kMH + lane + 32] = a_hi;

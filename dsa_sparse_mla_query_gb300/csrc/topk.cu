@@ -11,7 +11,13 @@
 // pass in index order writes every key > T and the first needed keys == T
 // (ties to the smaller index) with block-wide prefix sums, so the output is
 // the selected positions in ascending order: deterministic and compacted.
+#include <cooperative_groups.h>
+
+#include <mutex>
+
 #include "dsa_internal.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace dsa {
 
@@ -146,8 +152,308 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
     if (tid == 0) topk_len[t] = min(base_out, k);
 }
 
+// ---------------------------------------------------------------------------
+// Register-resident variant: a thread-block cluster of CL CTAs per query row,
+// each CTA holding 512 x EPT scores in registers, so the row is read from
+// memory exactly once.  Three digit passes (11 + 11 + 10 bits): each CTA
+// histograms its keys in shared memory (lanes of a warp that hit the same bin
+// add with one atomic), CTA r of the cluster sums slice r of the CL histograms
+// through distributed shared memory, and every CTA reads the merged slices
+// and finds the same digit.  After the first pass only the keys of the chosen
+// bin take part, compacted into shared memory when they fit.  The compaction
+// ranks ties and positions across the cluster with prefix sums of per-CTA
+// counts, so the output is the same as the one-CTA kernel's.
+constexpr int kCT = 512;                 // threads per CTA
+constexpr int kCBins = 2048;
+constexpr int kCandCap = 4096;           // keys of the chosen bin kept in shared memory
+
+// exclusive prefix sum over the kCT threads of a CTA
+__device__ __forceinline__ int cta_exclusive_scan(int v, int* buf, int* total) {
+    constexpr int W = kCT / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) buf[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < W ? buf[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        buf[32 + lane] = w;
+    }
+    __syncthreads();
+    const int before = (warp ? buf[32 + warp - 1] : 0) + x - v;
+    *total = buf[32 + W - 1];
+    __syncthreads();
+    return before;
+}
+
+__device__ __forceinline__ void hist_add(int* hist, bool act, int bin) {
+    const unsigned am = __ballot_sync(0xffffffffu, act);
+    if (act) {
+        const unsigned peers = __match_any_sync(am, bin);
+        if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(hist + bin, __popc(peers));
+    }
+}
+
+template <int EPT>
+__global__ void __launch_bounds__(kCT, EPT <= 16 ? 2 : 1)
+    topk_cluster_kernel(const float* __restrict__ scores, int64_t ld, dsa_seqs s, int k, int32_t* __restrict__ idx,
+                        int32_t* __restrict__ topk_len, int32_t* d_status) {
+    constexpr int kChunk = kCT * EPT;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int CL = (int)cluster.num_blocks();
+    __shared__ int hist[kCBins];     // this CTA's histogram
+    __shared__ int mhist[kCBins];    // merged counts of the bins this CTA owns
+    __shared__ uint32_t cand[kCandCap];
+    __shared__ int scan_buf[64];
+    __shared__ int sel_digit, sel_above, ncand;
+    __shared__ int cnt[2];
+    const int t = blockIdx.y;
+    const int tid = threadIdx.x;
+    const int b = seq_of(s.q_start, s.num_seqs, t);
+    const int pos = __ldg(s.q_pos + t);
+    const int ctx = __ldg(s.ctx_len + b);
+    int32_t* out = idx + (int64_t)t * k;
+    // uniform per row: every CTA of the cluster takes the same branch
+    if (pos < 0 || pos >= ctx || ctx > s.max_ctx || pos + 1 > CL * kChunk) {
+        if (rank == 0) {
+            if (tid == 0) {
+                report(d_status, DSA_ERR_BAD_INPUT);
+                topk_len[t] = 0;
+            }
+            for (int i = tid; i < k; i += kCT) out[i] = -1;
+        }
+        return;
+    }
+    const int n = pos + 1;
+    if (n <= k) {
+        if (rank == 0) {
+            for (int i = tid; i < k; i += kCT) out[i] = i < n ? i : -1;
+            if (tid == 0) topk_len[t] = n;
+        }
+        return;
+    }
+    // ---- this thread's EPT consecutive keys
+    const float* row = scores + (int64_t)t * ld;
+    const int base = rank * kChunk + tid * EPT;
+    uint32_t u[EPT];
+    uint64_t valid = 0;
+#pragma unroll
+    for (int v = 0; v < EPT / 4; ++v) {
+        const int i0 = base + 4 * v;
+        float4 f;
+        if (i0 + 3 < n) {
+            f = __ldg(reinterpret_cast<const float4*>(row + i0));
+        } else {
+            f.x = i0 < n ? __ldg(row + i0) : 0.f;
+            f.y = i0 + 1 < n ? __ldg(row + i0 + 1) : 0.f;
+            f.z = i0 + 2 < n ? __ldg(row + i0 + 2) : 0.f;
+            f.w = i0 + 3 < n ? __ldg(row + i0 + 3) : 0.f;
+        }
+        u[4 * v] = order_key(f.x);
+        u[4 * v + 1] = order_key(f.y);
+        u[4 * v + 2] = order_key(f.z);
+        u[4 * v + 3] = order_key(f.w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (i0 + e < n) valid |= 1ull << (4 * v + e);
+    }
+    // ---- three digit passes
+    uint32_t prefix = 0, mask = 0;
+    int remaining = k;
+    bool use_cand = false;
+    if (tid == 0) ncand = 0;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int nb = pass == 2 ? 1024 : 2048;
+        for (int i = tid; i < kCBins; i += kCT) hist[i] = 0;
+        __syncthreads();
+        if (use_cand) {
+            const int nc = ncand, nc_r = (nc + 31) & ~31;  // whole warps take part in hist_add
+            for (int i = tid; i < nc_r; i += kCT) {
+                const bool act = i < nc && (cand[i < nc ? i : 0] & mask) == prefix;
+                hist_add(hist, act, act ? (cand[i] >> shift) & (nb - 1) : 0);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < EPT; ++e) {
+                const bool act = ((valid >> e) & 1) && (u[e] & mask) == prefix;
+                hist_add(hist, act, (u[e] >> shift) & (nb - 1));
+            }
+        }
+        cluster.sync();  // A: every CTA's histogram is final
+        // merge slice `rank` of the bins over the cluster
+        const int slice = nb / CL;
+        for (int i = tid; i < slice; i += kCT) {
+            const int bin = rank * slice + i;
+            int v = 0;
+            for (int r = 0; r < CL; ++r) v += cluster.map_shared_rank(hist, r)[bin];
+            mhist[bin] = v;
+        }
+        cluster.sync();  // B: merged slices final
+        // digits in descending order, 4 per thread, read from their owners
+        int c[4], csum = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int d = nb - 1 - 4 * tid - q;
+            const int v = d >= 0 ? cluster.map_shared_rank(mhist, d / slice)[d] : 0;
+            c[q] = v;
+            csum += v;
+        }
+        int tot;
+        int before = cta_exclusive_scan(csum, scan_buf, &tot);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (before < remaining && before + c[q] >= remaining) {
+                sel_digit = nb - 1 - 4 * tid - q;
+                sel_above = before;
+            }
+            before += c[q];
+        }
+        cluster.sync();  // C: every CTA is done reading histograms; the digit is visible
+        prefix |= (uint32_t)sel_digit << shift;
+        mask |= (uint32_t)(nb - 1) << shift;
+        remaining -= sel_above;
+        if (pass == 0) {
+            // keep the keys of the chosen bin for the next two passes
+            const int lane = tid & 31;
+#pragma unroll
+            for (int e = 0; e < EPT; ++e) {
+                const bool act = ((valid >> e) & 1) && (u[e] & mask) == prefix;
+                const unsigned am = __ballot_sync(0xffffffffu, act);
+                int slot0 = 0;
+                if (lane == 0 && am) slot0 = atomicAdd(&ncand, __popc(am));
+                slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+                const int sl = slot0 + __popc(am & ((1u << lane) - 1));
+                if (act && sl < kCandCap) cand[sl] = u[e];
+            }
+            __syncthreads();
+            use_cand = ncand <= kCandCap;
+        }
+    }
+    const uint32_t T = prefix;
+    const int need_eq = remaining;
+    // ---- cluster-wide ranks: keys > T and keys == T, in index order
+    int n_gt = 0, n_eq = 0;
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+        const bool vld = (valid >> e) & 1;
+        n_gt += vld && u[e] > T;
+        n_eq += vld && u[e] == T;
+    }
+    int gt_cta, eq_cta;
+    cta_exclusive_scan(n_gt, scan_buf, &gt_cta);
+    const int eq_before = cta_exclusive_scan(n_eq, scan_buf, &eq_cta);
+    if (tid == 0) {
+        cnt[0] = gt_cta;
+        cnt[1] = eq_cta;
+    }
+    cluster.sync();
+    int gt_prefix = 0, eq_prefix = 0;
+    for (int r = 0; r < rank; ++r) {
+        const int* rc = cluster.map_shared_rank(cnt, r);
+        gt_prefix += rc[0];
+        eq_prefix += rc[1];
+    }
+    int eq_rank = eq_prefix + eq_before;
+    const int n_sel = n_gt + max(0, min(need_eq - eq_rank, n_eq));
+    int sel_cta;
+    int o = gt_prefix + min(need_eq, eq_prefix) + cta_exclusive_scan(n_sel, scan_buf, &sel_cta);
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+        if (!((valid >> e) & 1)) continue;
+        bool take = u[e] > T;
+        if (u[e] == T) take = eq_rank++ < need_eq;
+        if (take && o < k) out[o++] = base + e;
+    }
+    if (rank == 0 && tid == 0) topk_len[t] = k;
+    cluster.sync();  // no CTA leaves while another may still read its counts
+}
+
+namespace {
+
+struct ClusterPlan {
+    int cl, ept;
+};
+
+// CTAs per row and keys per thread: enough capacity for the longest row, then
+// more CTAs per row (down to 16 keys per thread) until the launch fills the GPU.
+ClusterPlan topk_plan(int max_ctx, int num_q) {
+    ClusterPlan p{1, 64};
+    while (p.cl * kCT * 64 < max_ctx) p.cl *= 2;
+    while (p.cl < 16 && p.cl * num_q < 256 && (p.cl * 2) * kCT * 16 <= max_ctx * 2) p.cl *= 2;
+    p.ept = 16;
+    while (p.cl * kCT * p.ept < max_ctx) p.ept *= 2;
+    return p;
+}
+
+template <int EPT>
+int max_cluster() {
+    static std::once_flag once;
+    static int max_ok = 0;
+    std::call_once(once, [] {
+        cudaFuncSetAttribute(topk_cluster_kernel<EPT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        for (int c = 1; c <= 16; c *= 2) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(c, 1, 1);
+            cfg.blockDim = dim3(kCT, 1, 1);
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = c;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel<EPT>, &cfg) == cudaSuccess && n > 0) max_ok = c;
+            else break;
+        }
+        cudaGetLastError();
+    });
+    return max_ok;
+}
+
+template <int EPT>
+cudaError_t launch_cluster(int cl, const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int k,
+                           int32_t* idx, int32_t* topk_len, int32_t* d_status, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cl, num_q, 1);
+    cfg.blockDim = dim3(kCT, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<EPT>, scores, ld, s, k, idx, topk_len, d_status);
+}
+
+}  // namespace
+
 cudaError_t launch_topk(const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int k, int32_t* idx,
                         int32_t* topk_len, int32_t* d_status, cudaStream_t stream) {
+    const ClusterPlan p = topk_plan(s.max_ctx, num_q);
+    if (p.cl <= 16 && p.ept <= 64) {
+        if (p.ept == 16 && p.cl <= max_cluster<16>())
+            return launch_cluster<16>(p.cl, scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
+        if (p.ept == 32 && p.cl <= max_cluster<32>())
+            return launch_cluster<32>(p.cl, scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
+        if (p.ept == 64 && p.cl <= max_cluster<64>())
+            return launch_cluster<64>(p.cl, scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
+    }
+    // rows longer than 16 x 32,768 keys: one CTA per row, passes over memory
     topk_kernel<<<num_q, kTopkThreads, 0, stream>>>(scores, ld, s, k, idx, topk_len, d_status);
     return cudaGetLastError();
 }
