@@ -95,6 +95,15 @@ __device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32): relative error
+// near 2^-22, subnormal results flushed to zero, 2^-inf = 0.  Ample for
+// softmax probabilities, which are rounded to bf16 right after.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);

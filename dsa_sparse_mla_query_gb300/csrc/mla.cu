@@ -272,10 +272,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 8; ++i) pr[hr][i] = 0.f;
                 } else {
-                    alpha = exp2f(m_run[hr] - m_new);
+                    alpha = fast_exp2(m_run[hr] - m_new);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        pr[hr][i] = exp2f(pr[hr][i] - m_new);
+                        pr[hr][i] = fast_exp2(pr[hr][i] - m_new);
                         sum += pr[hr][i];
                     }
                 }
@@ -442,26 +442,26 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restric
 //   warps 6-13  gather the tile's rows: 16-byte loads, 18 per thread in flight,
 //               stored into the 128-byte-swizzled K-major layout (two stages);
 //               random 1,152-byte rows stream fastest this way on GB300;
-//   warp 1      issues tcgen05.mma: S^T = K Q^T (M = 128 rows of which the 64
-//               gathered keys are used, N = 64 heads, K = 576) into TMEM, then
+//   warp 1      issues tcgen05.mma: S^T = K Q^T (M = 64 keys, N = 64 heads,
+//               K = 576; key r lands in TMEM lane 32 (r / 16) + r % 16) and
 //               O^T += V^T P^T (M = 128 value dims per block, N = 64 heads,
 //               K = 64 keys; V^T is the same gathered tile read MN-major);
-//   warps 4-5   softmax, one key per thread straight from TMEM: exact per-head
+//   warps 2-5   softmax, 16 keys per warp straight from TMEM: exact per-head
 //               maxima of the first tile set the running max; later tiles only
-//               check that no score exceeds it by more than 2^64 (one flag
-//               exchanged between the two warps) and raise it, rescaling O^T,
-//               only when one does; exp2, row sums kept in TMEM, P^T to shared
-//               memory;
-//   warps 2-5   rescale O^T (rare) and write the output or the split partial.
+//               check that no score exceeds it by more than 2^64 (one flag per
+//               warp exchanged) and raise it, each warp rescaling its own lanes
+//               of O^T, only when one does; exp2, row sums kept in TMEM, P^T
+//               written over the tile's rope block (64 keys x 64 heads, bf16,
+//               exactly its size), which the scores no longer need; then the
+//               output or the split partial.
 namespace tcmla {
 constexpr int TK = 64;                     // selected rows per tile
 constexpr int KB = kMD / 64;               // 9 blocks of 64 dims
 constexpr int kKBlock = TK * 128;          // bytes of one 64-dim block of a tile
 constexpr int kStage = KB * kKBlock;       // 73728
 constexpr int kQBytes = KB * kMH * 128;    // 73728
-constexpr int kPBytes = TK * 128;          // P^T: 64 keys x 64 heads, bf16
-constexpr int kMisc = 3072;
-constexpr size_t kSmem = 2 * (size_t)kStage + kQBytes + kPBytes + kMisc;
+constexpr int kMisc = 4096;
+constexpr size_t kSmem = 2 * (size_t)kStage + kQBytes + kMisc;
 constexpr float kRescale = 64.f;           // log2 headroom before O^T is rescaled (bf16 P, fp32 O)
 constexpr uint32_t kOCol = 0;              // O^T: 4 blocks x 64 heads
 constexpr uint32_t kSCol = 256;            // S^T: 2 buffers x 64 heads
@@ -469,7 +469,9 @@ constexpr uint32_t kLCol = 384;            // row sums: lanes = keys, columns = 
 constexpr uint32_t kTmemCols = 512;
 constexpr int kThreads = 448;              // 14 warps
 constexpr int kGatherWarps = 8;
+constexpr int kSoftWarps = 4;
 constexpr int kRing = 3;                   // resolved-row ring depth
+static_assert(kKBlock == TK * kMH * 2, "P^T must fit the rope block of its tile");
 }  // namespace tcmla
 
 __global__ void __launch_bounds__(tcmla::kThreads, 1)
@@ -479,35 +481,30 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                   float* __restrict__ part_ml, int32_t* d_status) {
     using namespace tcmla;
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t* stage = smem;                                  // [2][KB][TK rows x 128 B]
+    uint8_t* stage = smem;                                  // [2][KB][TK rows x 128 B]; block 8 later holds P^T
     uint8_t* qs = smem + 2 * kStage;                        // [KB][64 heads x 128 B]
-    uint8_t* ps = qs + kQBytes;                             // [TK keys x 128 B]
-    uint8_t* misc = ps + kPBytes;
+    uint8_t* misc = qs + kQBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
     uint64_t* qfull = bars + 0;
     uint64_t* kfull = bars + 1;   // [2] gathered tile stored (8 gather warps)
     uint64_t* kempty = bars + 3;  // [2] tile no longer read by the MMA
     uint64_t* sfull = bars + 5;   // [2] S^T ready
     uint64_t* sempty = bars + 7;  // [2] S^T read by the softmax warps
-    uint64_t* xch = bars + 9;     // [2] tile maxima of both softmax warps written
-    uint64_t* dec = bars + 11;    // rescale decision of the tile written
-    uint64_t* pfull = bars + 12;  // P^T written and O^T rescaled (4 warps)
-    uint64_t* pvdone = bars + 13; // O^T += V^T P^T of the tile complete
-    uint64_t* ofull = bars + 14;  // last product complete
-    uint64_t* lready = bars + 15; // row sums of both softmax warps written
-    uint64_t* rfull = bars + 16;  // [3] rows of a tile resolved
-    uint64_t* rfree = bars + 19;  // [3] rows of a tile no longer read (8 gather + 2 softmax warps)
-    uint64_t* xmax = bars + 22;   // per-head maxima of both softmax warps written (first tile, growth)
+    uint64_t* xch = bars + 9;     // [2] growth flags of the softmax warps written
+    uint64_t* pfull = bars + 11;  // P^T written (and O^T rescaled) by the softmax warps
+    uint64_t* pvdone = bars + 12; // O^T += V^T P^T of the tile complete
+    uint64_t* ofull = bars + 13;  // last product complete
+    uint64_t* lready = bars + 14; // row sums of the softmax warps written
+    uint64_t* rfull = bars + 15;  // [3] rows of a tile resolved
+    uint64_t* rfree = bars + 18;  // [3] rows of a tile no longer read (gather + softmax warps)
+    uint64_t* xmax = bars + 21;   // per-head maxima of the softmax warps written (first tile, growth)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 192);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 196);
-    int* need = reinterpret_cast<int*>(misc + 200);          // [2 parity]
-    int* wflag = reinterpret_cast<int*>(misc + 208);         // [2 parity][2 warps] growth flags
+    int* wflag = reinterpret_cast<int*>(misc + 208);         // [2 parity][4 warps] growth flags
     int* srow = reinterpret_cast<int*>(misc + 256);          // [3][TK] physical row (-1 = masked)
-    float* wmax = reinterpret_cast<float*>(misc + 1024);     // [2 warps][64] per-head maxima
-    float* mu = reinterpret_cast<float*>(misc + 1536);       // [2 warps][64] running max (log2 units)
-    float* alpha = reinterpret_cast<float*>(misc + 2048);    // [2 parity][64] rescale factors (warp 4's copy)
-    // row sums [2 warps][64] reuse srow once every tile has been resolved and read
-    float* lsum = reinterpret_cast<float*>(srow);
+    float* wmax = reinterpret_cast<float*>(misc + 1024);     // [4 warps][64] per-head maxima
+    float* mu = reinterpret_cast<float*>(misc + 2048);       // [4 warps][64] running max (log2 units)
+    float* lsum = reinterpret_cast<float*>(misc + 3072);     // [4 warps][64] row sums
 
     const int t = blockIdx.y, sp = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -530,19 +527,18 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
             ptx::mbar_init(kfull + i, kGatherWarps);
             ptx::mbar_init(kempty + i, 1);
             ptx::mbar_init(sfull + i, 1);
-            ptx::mbar_init(sempty + i, 2);
-            ptx::mbar_init(xch + i, 2);
+            ptx::mbar_init(sempty + i, kSoftWarps);
+            ptx::mbar_init(xch + i, kSoftWarps);
         }
         for (int i = 0; i < kRing; ++i) {
             ptx::mbar_init(rfull + i, 1);
-            ptx::mbar_init(rfree + i, kGatherWarps + 2);
+            ptx::mbar_init(rfree + i, kGatherWarps + kSoftWarps);
         }
-        ptx::mbar_init(dec, 1);
-        ptx::mbar_init(pfull, 4);
+        ptx::mbar_init(pfull, kSoftWarps);
         ptx::mbar_init(pvdone, 1);
         ptx::mbar_init(ofull, 1);
-        ptx::mbar_init(lready, 2);
-        ptx::mbar_init(xmax, 2);
+        ptx::mbar_init(lready, kSoftWarps);
+        ptx::mbar_init(xmax, kSoftWarps);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -592,14 +588,15 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && ntiles > 0) {
-            constexpr uint32_t idesc_s = ptx::idesc_f16_m128(kMH, true);
-            constexpr uint32_t idesc_pv = ptx::idesc_f16_m128(kMH, true, true, true);
-            const uint32_t qb = smem_u32(qs), pb = smem_u32(ps);
+            constexpr uint32_t idesc_s = ptx::idesc_f16(64, kMH, true);
+            constexpr uint32_t idesc_pv = ptx::idesc_f16(128, kMH, true, true, true);
+            const uint32_t qb = smem_u32(qs);
             bool ok = ptx::mbar_wait(qfull, 0, abort_flag, d_status);
             auto issue_pv = [&](int i) -> bool {  // O^T += V^T P^T for tile i
                 if (!ptx::mbar_wait(pfull, i & 1, abort_flag, d_status)) return false;
                 ptx::tc_fence_after();
                 const uint32_t kbase = smem_u32(stage + (i & 1) * kStage);
+                const uint32_t pb = kbase + 8 * kKBlock;
 #pragma unroll
                 for (int db = 0; db < 4; ++db)
 #pragma unroll
@@ -695,178 +692,158 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
             if (lane == 0) ptx::mbar_arrive(kfull + st);
         }
     } else {
-        // ------------------------------------------------------------ softmax (4,5) and output (2..5)
-        const bool sm = warp >= 4;
+        // ------------------------------------------------------------ softmax and output (warps 2-5)
         const int quarter = warp & 3;                       // TMEM lanes 32*quarter ..
-        const int sw = warp - 4;                            // softmax warp index
-        const int key = quarter * 32 + lane;                // softmax: key row of the tile (< 64)
+        const int sw = warp - 2;                            // softmax warp index 0..3
+        const bool mine = lane < 16;                        // lanes holding a key of the tile
+        const int key = quarter * 16 + (lane & 15);         // key row of the tile
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's TMEM lanes
-        float* my_mu = mu + (sm ? sw : 0) * kMH;
-        if (sm) {
-            my_mu[lane] = -INFINITY;
-            my_mu[lane + 32] = -INFINITY;
+        float* my_mu = mu + sw * kMH;
+        my_mu[lane] = -INFINITY;
+        my_mu[lane + 32] = -INFINITY;
+        {
             float z[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) z[j] = 0.f;
             ptx::tmem_st32(tl + kLCol, z);
             ptx::tmem_st32(tl + kLCol + 32, z);
-            __syncwarp();
         }
+        __syncwarp();
         bool alive = true;
-        int n_grow = 0;  // exact-maxima exchanges so far (same count in both softmax warps)
+        int n_grow = 0;  // exact-maxima exchanges so far (same count in every softmax warp)
         for (int i = 0; alive && i < ntiles; ++i) {
             const int st = i & 1, r = i % kRing;
-            if (sm) {
-                if (!__all_sync(0xffffffffu, ptx::mbar_wait(rfull + r, (i / kRing) & 1, abort_flag, d_status) &&
-                                                 ptx::mbar_wait(sfull + st, (i >> 1) & 1, abort_flag, d_status))) {
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(rfull + r, (i / kRing) & 1, abort_flag, d_status) &&
+                                             ptx::mbar_wait(sfull + st, (i >> 1) & 1, abort_flag, d_status))) {
+                alive = false;
+                break;
+            }
+            const bool valid = mine && srow[r * TK + key] >= 0;
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(rfree + r);
+            ptx::tc_fence_after();
+            const uint32_t s_addr = tl + kSCol + st * kMH;
+            // does any score of this tile rise more than 2^64 above the running max?
+            bool grow = i == 0;
+            if (i > 0) {
+                float sv[64];
+                ptx::tmem_ld64(s_addr, sv);
+                float over = -INFINITY;
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const float4 m4 = reinterpret_cast<const float4*>(my_mu)[q];
+                    over = fmaxf(over, fmaxf(fmaxf(sv[4 * q] * scale_log2 - m4.x, sv[4 * q + 1] * scale_log2 - m4.y),
+                                             fmaxf(sv[4 * q + 2] * scale_log2 - m4.z, sv[4 * q + 3] * scale_log2 - m4.w)));
+                }
+                const bool g = __any_sync(0xffffffffu, valid && over > kRescale);
+                if (lane == 0) wflag[st * 4 + sw] = g ? 1 : 0;
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(xch + st);
+                // xch[st] serves tiles 1, 2, 3, ... (not 0): use u of it is tile 2u+1 or 2u+2
+                if (!__all_sync(0xffffffffu, ptx::mbar_wait(xch + st, ((i - 1) >> 1) & 1, abort_flag, d_status))) {
                     alive = false;
                     break;
                 }
-                const bool valid = srow[r * TK + key] >= 0;
+                grow = (wflag[st * 4] | wflag[st * 4 + 1] | wflag[st * 4 + 2] | wflag[st * 4 + 3]) != 0;
+            }
+            float a_lo = 1.f, a_hi = 1.f;
+            if (grow) {
+                // exact per-head maxima of this tile (first tile, or a growth)
+                float sv[64];
+                ptx::tmem_ld64(s_addr, sv);
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    const float m = ptx::warp_max(valid ? sv[j] * scale_log2 : -INFINITY);
+                    if (lane == (j & 31)) wmax[sw * kMH + j] = m;
+                }
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(rfree + r);
+                if (lane == 0) ptx::mbar_arrive(xmax);
+                if (!__all_sync(0xffffffffu, ptx::mbar_wait(xmax, n_grow & 1, abort_flag, d_status))) {
+                    alive = false;
+                    break;
+                }
+                ++n_grow;
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int h = lane + 32 * u;
+                    const float mt = fmaxf(fmaxf(wmax[h], wmax[kMH + h]), fmaxf(wmax[2 * kMH + h], wmax[3 * kMH + h]));
+                    const float mo = my_mu[h];
+                    const float mn = fmaxf(mo, mt);
+                    const float a = (mo == -INFINITY || mn == mo) ? (mo == mn ? 1.f : 0.f) : exp2f(mo - mn);
+                    if (u == 0) a_lo = a; else a_hi = a;
+                    my_mu[h] = mn;
+                }
+                __syncwarp();
+            }
+            const bool rescale = grow && i > 0;
+            if (rescale) {
+                // O^T holds the products of tiles 0 .. i-1 once the previous one completes
+                if (!__all_sync(0xffffffffu, ptx::mbar_wait(pvdone, (i - 1) & 1, abort_flag, d_status))) {
+                    alive = false;
+                    break;
+                }
                 ptx::tc_fence_after();
-                // does any score of this tile rise more than 2^64 above the running max?
-                bool grow = i == 0;
-                if (i > 0) {
-                    float over = -INFINITY;
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        float sv[32];
-                        ptx::tmem_ld32(tl + kSCol + st * kMH + half * 32, sv);
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) over = fmaxf(over, sv[j] * scale_log2 - my_mu[half * 32 + j]);
-                    }
-                    const bool g = __any_sync(0xffffffffu, valid && over > kRescale);
-                    if (lane == 0) wflag[st * 2 + sw] = g ? 1 : 0;
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(xch + st);
-                    // xch[st] serves tiles 1, 2, 3, ... (not 0): use u of it is tile 2u+1 or 2u+2
-                    if (!__all_sync(0xffffffffu, ptx::mbar_wait(xch + st, ((i - 1) >> 1) & 1, abort_flag, d_status))) {
-                        alive = false;
-                        break;
-                    }
-                    grow = wflag[st * 2] || wflag[st * 2 + 1];
-                }
-                float a_lo = 1.f, a_hi = 1.f;
-                if (grow) {
-                    // exact per-head maxima of this tile (first tile, or a growth)
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        float sv[32];
-                        ptx::tmem_ld32(tl + kSCol + st * kMH + half * 32, sv);
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float m = ptx::warp_max(valid ? sv[j] * scale_log2 : -INFINITY);
-                            if (lane == j) wmax[sw * kMH + half * 32 + j] = m;
-                        }
-                    }
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(xmax);
-                    if (!__all_sync(0xffffffffu, ptx::mbar_wait(xmax, n_grow & 1, abort_flag, d_status))) {
-                        alive = false;
-                        break;
-                    }
-                    ++n_grow;
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int h = lane + 32 * u;
-                        const float mt = fmaxf(wmax[h], wmax[kMH + h]);
-                        const float mo = my_mu[h];
-                        const float mn = fmaxf(mo, mt);
-                        const float a = (mo == -INFINITY || mn == mo) ? (mo == mn ? 1.f : 0.f) : exp2f(mo - mn);
-                        if (u == 0) a_lo = a; else a_hi = a;
-                        my_mu[h] = mn;
-                    }
-                    __syncwarp();
-                }
-                const bool rescale = grow && i > 0;
-                if (sw == 0) {
-                    alpha[st * kMH + lane] = a_lo;
-                    alpha[st * kMH + lane + 32] = a_hi;
-                    if (lane == 0) need[st] = rescale ? 1 : 0;
-                }
-                __syncwarp();
-                if (sw == 0 && lane == 0) ptx::mbar_arrive(dec);
-                // P^T buffer and O^T are free once the previous product completes
-                if (i >= 1 && !__all_sync(0xffffffffu, ptx::mbar_wait(pvdone, (i - 1) & 1, abort_flag, d_status))) {
-                    alive = false;
-                    break;
-                }
-                if (rescale) {
-                    ptx::tc_fence_after();
 #pragma unroll 1
-                    for (int c = 0; c < 8; ++c) {
-                        float o[32];
-                        ptx::tmem_ld32(tl + kOCol + c * 32, o);
+                for (int c = 0; c < 16; ++c) {  // columns 16c .. 16c+15 = heads 16 (c % 4) ..
+                    float o[16];
+                    ptx::tmem_ld16(tl + kOCol + c * 16, o);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] *= __shfl_sync(0xffffffffu, (c & 1) ? a_hi : a_lo, j);
-                        ptx::tmem_st32(tl + kOCol + c * 32, o);
-                    }
+                    for (int j = 0; j < 16; ++j)
+                        o[j] *= __shfl_sync(0xffffffffu, (c & 2) ? a_hi : a_lo, (c & 1) * 16 + j);
+                    ptx::tmem_st16(tl + kOCol + c * 16, o);
                 }
-                // pass 2: probabilities, row sums (TMEM), P^T row (128 bytes, swizzled)
-                uint8_t* prow = ps + key * 128;
+                // and the row sums: columns 16g .. 16g+15 = heads 16g ..
+#pragma unroll 1
+                for (int g = 0; g < 4; ++g) {
+                    float lv[16];
+                    ptx::tmem_ld16(tl + kLCol + g * 16, lv);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float sv[32], lv[32];
-                    ptx::tmem_ld32(tl + kSCol + st * kMH + half * 32, sv);
-                    ptx::tmem_ld32(tl + kLCol + half * 32, lv);
-                    uint32_t pk[16];
+                    for (int j = 0; j < 16; ++j)
+                        lv[j] *= __shfl_sync(0xffffffffu, (g & 2) ? a_hi : a_lo, (g & 1) * 16 + j);
+                    ptx::tmem_st16(tl + kLCol + g * 16, lv);
+                }
+            }
+            // probabilities, row sums (TMEM), P^T row (128 bytes, swizzled) over the rope block
+            uint8_t* prow = stage + st * kStage + 8 * kKBlock + key * 128;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        const int h = half * 32 + j;
-                        const float m0 = my_mu[h], m1 = my_mu[h + 1];
-                        const float p0 = (!valid || m0 == -INFINITY) ? 0.f : exp2f(sv[j] * scale_log2 - m0);
-                        const float p1 = (!valid || m1 == -INFINITY) ? 0.f : exp2f(sv[j + 1] * scale_log2 - m1);
-                        const float s0 = rescale ? __shfl_sync(0xffffffffu, half ? a_hi : a_lo, j) : 1.f;
-                        const float s1 = rescale ? __shfl_sync(0xffffffffu, half ? a_hi : a_lo, j + 1) : 1.f;
-                        lv[j] = lv[j] * s0 + p0;
-                        lv[j + 1] = lv[j + 1] * s1 + p1;
-                        pk[j / 2] = pack_bf16(p0, p1);
+            for (int g = 0; g < 4; ++g) {  // 16 heads at a time
+                float sv[16], lv[16];
+                ptx::tmem_ld16(s_addr + g * 16, sv);
+                ptx::tmem_ld16(tl + kLCol + g * 16, lv);
+                uint32_t pk[8];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 m4 = reinterpret_cast<const float4*>(my_mu)[g * 4 + q];
+                    const float mq[4] = {m4.x, m4.y, m4.z, m4.w};
+                    float p[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        p[e] = (!valid || mq[e] == -INFINITY) ? 0.f : fast_exp2(sv[4 * q + e] * scale_log2 - mq[e]);
+                        lv[4 * q + e] += p[e];
                     }
-                    ptx::tmem_st32(tl + kLCol + half * 32, lv);
+                    pk[2 * q] = pack_bf16(p[0], p[1]);
+                    pk[2 * q + 1] = pack_bf16(p[2], p[3]);
+                }
+                ptx::tmem_st16(tl + kLCol + g * 16, lv);
+                if (mine) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int cc = half * 4 + c;
+                    for (int c = 0; c < 2; ++c) {
+                        const int cc = g * 2 + c;
                         *reinterpret_cast<uint4*>(prow + ((cc ^ (key & 7)) << 4)) =
                             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
                     }
                 }
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(sempty + st);
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(pfull);
-            } else {
-                // helpers: rescale the O^T lanes 64..127 when the softmax asks for it
-                if (!__all_sync(0xffffffffu, ptx::mbar_wait(dec, i & 1, abort_flag, d_status))) {
-                    alive = false;
-                    break;
-                }
-                if (need[st]) {
-                    if (i >= 1 && !__all_sync(0xffffffffu, ptx::mbar_wait(pvdone, (i - 1) & 1, abort_flag, d_status))) {
-                        alive = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-#pragma unroll 1
-                    for (int c = 0; c < 8; ++c) {
-                        float o[32];
-                        ptx::tmem_ld32(tl + kOCol + c * 32, o);
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] *= alpha[st * kMH + ((c & 1) * 32 + j)];
-                        ptx::tmem_st32(tl + kOCol + c * 32, o);
-                    }
-                }
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(pfull);
+            }
+            ptx::tc_fence_before();
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(sempty + st);
+                ptx::mbar_arrive(pfull);
             }
         }
-        // ---- row sums of the softmax warps -> lsum[2][64]
-        float* ml_m = mu;  // warp 4's running max
-        if (sm && alive && ntiles > 0) {
+        // ---- row sums of this warp -> lsum[sw][64]
+        if (alive && ntiles > 0) {
             ptx::tc_fence_after();
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -876,7 +853,7 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                 for (int j = 0; j < 32; ++j) {
                     float v = lv[j];
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);  // lanes 16-31 add zeros
                     if (lane == j) lsum[sw * kMH + half * 32 + j] = v;
                 }
             }
@@ -884,11 +861,13 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
             if (lane == 0) ptx::mbar_arrive(lready);
         }
         // ---- output: all four warps, one value dim per thread of each 128-dim block
+        const float* ml_m = mu;  // every warp's copy of the running max is the same
         const int dim = quarter * 32 + lane;
         bool have = alive && ntiles > 0;
         if (have) have = __all_sync(0xffffffffu, ptx::mbar_wait(lready, 0, abort_flag, d_status));
         if (have) have = __all_sync(0xffffffffu, ptx::mbar_wait(ofull, 0, abort_flag, d_status));
         if (have) ptx::tc_fence_after();
+        auto total_l = [&](int h) { return lsum[h] + lsum[kMH + h] + lsum[2 * kMH + h] + lsum[3 * kMH + h]; };
         if (splits == 1) {
             __nv_bfloat16* ot = out + (int64_t)t * kMH * kMV;
 #pragma unroll 1
@@ -899,14 +878,14 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int h = h0 + j;
-                    const float L = have ? lsum[h] + lsum[kMH + h] : 0.f;
+                    const float L = have ? total_l(h) : 0.f;
                     const float v = L > 0.f ? o[j] / L : 0.f;
                     ot[(int64_t)h * kMV + db * 128 + dim] = __float2bfloat16_rn(v);
                 }
             }
             if (lse && warp == 2) {
                 for (int h = lane; h < kMH; h += 32) {
-                    const float L = have ? lsum[h] + lsum[kMH + h] : 0.f;
+                    const float L = have ? total_l(h) : 0.f;
                     lse[(int64_t)t * kMH + h] = L > 0.f ? (ml_m[h] + log2f(L)) * 0.69314718055994531f : -INFINITY;
                 }
             }
@@ -923,7 +902,7 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
             if (warp == 2) {
                 for (int h = lane; h < kMH; h += 32) {
                     float* ml = part_ml + (((int64_t)t * splits + sp) * kMH + h) * 2;
-                    const float L = have ? lsum[h] + lsum[kMH + h] : 0.f;
+                    const float L = have ? total_l(h) : 0.f;
                     ml[0] = L > 0.f ? ml_m[h] : -INFINITY;
                     ml[1] = L;
                 }
