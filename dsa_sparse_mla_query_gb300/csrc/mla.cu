@@ -439,18 +439,19 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restric
 // One CTA = one query x one split of its selected slots, tiles of 64 rows:
 //   warp 0      loads the 64 query heads (TMA) and resolves each tile's slots
 //               to physical rows (page table) up to three tiles ahead;
-//   warps 6-13  gather the tile's rows: 16-byte loads, 18 per thread in flight,
+//   warps 10-17 gather the tile's rows: 16-byte loads, 18 per thread in flight,
 //               stored into the 128-byte-swizzled K-major layout (two stages);
 //               random 1,152-byte rows stream fastest this way on GB300;
 //   warp 1      issues tcgen05.mma: S^T = K Q^T (M = 64 keys, N = 64 heads,
 //               K = 576; key r lands in TMEM lane 32 (r / 16) + r % 16) and
 //               O^T += V^T P^T (M = 128 value dims per block, N = 64 heads,
 //               K = 64 keys; V^T is the same gathered tile read MN-major);
-//   warps 2-5   softmax, 16 keys per warp straight from TMEM: exact per-head
-//               maxima of the first tile set the running max; later tiles only
-//               check that no score exceeds it by more than 2^64 (one flag per
-//               warp exchanged) and raise it, each warp rescaling its own lanes
-//               of O^T, only when one does; exp2, row sums kept in TMEM, P^T
+//   warps 2-9   softmax, two warps per TMEM lane quarter (16 keys), each with
+//               32 of the heads, straight from TMEM: exact per-head maxima of
+//               the first tile set the running max; later tiles only check
+//               that no score exceeds it by more than 2^64 (one flag per warp
+//               exchanged) and raise it, each warp rescaling its own part of
+//               O^T, only when one does; exp2, row sums kept in TMEM, P^T
 //               written over the tile's rope block (64 keys x 64 heads, bf16,
 //               exactly its size), which the scores no longer need; then the
 //               output or the split partial.
@@ -460,16 +461,16 @@ constexpr int KB = kMD / 64;               // 9 blocks of 64 dims
 constexpr int kKBlock = TK * 128;          // bytes of one 64-dim block of a tile
 constexpr int kStage = KB * kKBlock;       // 73728
 constexpr int kQBytes = KB * kMH * 128;    // 73728
-constexpr int kMisc = 4096;
+constexpr int kMisc = 4608;
 constexpr size_t kSmem = 2 * (size_t)kStage + kQBytes + kMisc;
 constexpr float kRescale = 64.f;           // log2 headroom before O^T is rescaled (bf16 P, fp32 O)
 constexpr uint32_t kOCol = 0;              // O^T: 4 blocks x 64 heads
 constexpr uint32_t kSCol = 256;            // S^T: 2 buffers x 64 heads
 constexpr uint32_t kLCol = 384;            // row sums: lanes = keys, columns = heads
 constexpr uint32_t kTmemCols = 512;
-constexpr int kThreads = 448;              // 14 warps
+constexpr int kThreads = 576;              // 18 warps
 constexpr int kGatherWarps = 8;
-constexpr int kSoftWarps = 4;
+constexpr int kSoftWarps = 8;
 constexpr int kRing = 3;                   // resolved-row ring depth
 static_assert(kKBlock == TK * kMH * 2, "P^T must fit the rope block of its tile");
 }  // namespace tcmla
@@ -486,25 +487,27 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
     uint8_t* misc = qs + kQBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
     uint64_t* qfull = bars + 0;
-    uint64_t* kfull = bars + 1;   // [2] gathered tile stored (8 gather warps)
-    uint64_t* kempty = bars + 3;  // [2] tile no longer read by the MMA
-    uint64_t* sfull = bars + 5;   // [2] S^T ready
-    uint64_t* sempty = bars + 7;  // [2] S^T read by the softmax warps
-    uint64_t* xch = bars + 9;     // [2] growth flags of the softmax warps written
-    uint64_t* pfull = bars + 11;  // P^T written (and O^T rescaled) by the softmax warps
-    uint64_t* pvdone = bars + 12; // O^T += V^T P^T of the tile complete
-    uint64_t* ofull = bars + 13;  // last product complete
-    uint64_t* lready = bars + 14; // row sums of the softmax warps written
-    uint64_t* rfull = bars + 15;  // [3] rows of a tile resolved
-    uint64_t* rfree = bars + 18;  // [3] rows of a tile no longer read (gather + softmax warps)
-    uint64_t* xmax = bars + 21;   // per-head maxima of the softmax warps written (first tile, growth)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 192);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 196);
-    int* wflag = reinterpret_cast<int*>(misc + 208);         // [2 parity][4 warps] growth flags
-    int* srow = reinterpret_cast<int*>(misc + 256);          // [3][TK] physical row (-1 = masked)
-    float* wmax = reinterpret_cast<float*>(misc + 1024);     // [4 warps][64] per-head maxima
-    float* mu = reinterpret_cast<float*>(misc + 2048);       // [4 warps][64] running max (log2 units)
-    float* lsum = reinterpret_cast<float*>(misc + 3072);     // [4 warps][64] row sums
+    // A tile is stored and released in two halves: blocks 0-3 (value dims
+    // 0-255) and blocks 4-8 (value dims 256-511, the rope block, later P^T).
+    uint64_t* kfull = bars + 1;   // [2 halves][2 stages] half of a gathered tile stored (8 gather warps)
+    uint64_t* kempty = bars + 5;  // [2 halves][2 stages] half of a tile no longer read by the MMA
+    uint64_t* sfull = bars + 9;   // [2] S^T ready
+    uint64_t* sempty = bars + 11; // [2] S^T read by the softmax warps
+    uint64_t* xch = bars + 13;    // [2] growth flags of the softmax warps written
+    uint64_t* pfull = bars + 15;  // P^T written (and O^T rescaled) by the softmax warps
+    uint64_t* pvdone = bars + 16; // O^T += V^T P^T of the tile complete
+    uint64_t* ofull = bars + 17;  // last product complete
+    uint64_t* lready = bars + 18; // row sums of the softmax warps written
+    uint64_t* rfull = bars + 19;  // [3] rows of a tile resolved
+    uint64_t* rfree = bars + 22;  // [3] rows of a tile no longer read (gather + softmax warps)
+    uint64_t* xmax = bars + 25;   // per-head maxima of the softmax warps written (first tile, growth)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
+    int* srow = reinterpret_cast<int*>(misc + 512);          // [3][TK] physical row (-1 = masked)
+    float* wmax = reinterpret_cast<float*>(misc + 1280);     // [4 lane quarters][64] per-head maxima
+    float* mu = reinterpret_cast<float*>(misc + 2304);       // [8 warps][32 heads] running max (log2 units)
+    float* lsum = reinterpret_cast<float*>(misc + 3328);     // [4 lane quarters][64] row sums
+    int* wflag = reinterpret_cast<int*>(misc + 4352);        // [2 parity][8 warps] growth flags
 
     const int t = blockIdx.y, sp = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -523,9 +526,11 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(qfull, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 4; ++i) {
             ptx::mbar_init(kfull + i, kGatherWarps);
             ptx::mbar_init(kempty + i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(sfull + i, 1);
             ptx::mbar_init(sempty + i, kSoftWarps);
             ptx::mbar_init(xch + i, kSoftWarps);
@@ -598,45 +603,60 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                 const uint32_t kbase = smem_u32(stage + (i & 1) * kStage);
                 const uint32_t pb = kbase + 8 * kKBlock;
 #pragma unroll
-                for (int db = 0; db < 4; ++db)
+                for (int db = 0; db < 4; ++db) {
 #pragma unroll
                     for (int kk = 0; kk < TK / 16; ++kk) {
                         const uint64_t ad = ptx::sdesc_sw128_mn(kbase + 2 * db * kKBlock + kk * 2048, kKBlock, 1024);
                         const uint64_t bd = ptx::sdesc_sw128_mn(pb + kk * 2048, kKBlock, 1024);
                         ptx::mma_ss(tmem + kOCol + db * kMH, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
                     }
-                ptx::mma_commit(kempty + (i & 1));
+                    if (db == 1) ptx::mma_commit(kempty + (i & 1));  // blocks 0-3 read
+                }
+                ptx::mma_commit(kempty + 2 + (i & 1));              // blocks 4-8 (with P^T) read
                 ptx::mma_commit(pvdone);
                 return true;
             };
             // S^T of a tile is issued as soon as its rows are stored and its TMEM
             // buffer is free; O^T += V^T P^T as soon as its P^T is written.  The
             // two streams interleave, so the scores of tile i+1 are computed
-            // while the softmax of tile i runs.
-            int s_next = 0, pv_next = 0;
+            // while the softmax of tile i runs.  The barriers are probed without
+            // blocking: a blocking wait on one would miss the other completing.
+            // S^T of a tile in two parts, blocks 0-3 then 4-8, each as soon as
+            // that half of the tile is stored.
+            auto issue_s = [&](int st, int kb0, int kb1) {
+                ptx::tc_fence_after();
+                const uint32_t kbase = smem_u32(stage + st * kStage);
+#pragma unroll
+                for (int kb = kb0; kb < kb1; ++kb)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t ad = ptx::sdesc_sw128(kbase + kb * kKBlock + ks * 32);
+                        const uint64_t bd = ptx::sdesc_sw128(qb + kb * kMH * 128 + ks * 32);
+                        ptx::mma_ss(tmem + kSCol + st * kMH, ad, bd, idesc_s, (kb > 0 || ks > 0) ? 1u : 0u);
+                    }
+            };
+            int s_next = 0, s_half = 0, pv_next = 0;
             uint64_t t_idle = 0;
             while (ok && pv_next < ntiles) {
                 bool progressed = false;
                 if (s_next < ntiles) {
                     const int st = s_next & 1;
-                    if (ptx::mbar_try_wait(kfull + st, (s_next >> 1) & 1) &&
-                        (s_next < 2 || ptx::mbar_try_wait(sempty + st, ((s_next >> 1) - 1) & 1))) {
-                        ptx::tc_fence_after();
-                        const uint32_t kbase = smem_u32(stage + st * kStage);
-#pragma unroll
-                        for (int kb = 0; kb < KB; ++kb)
-#pragma unroll
-                            for (int ks = 0; ks < 4; ++ks) {
-                                const uint64_t ad = ptx::sdesc_sw128(kbase + kb * kKBlock + ks * 32);
-                                const uint64_t bd = ptx::sdesc_sw128(qb + kb * kMH * 128 + ks * 32);
-                                ptx::mma_ss(tmem + kSCol + st * kMH, ad, bd, idesc_s, (kb > 0 || ks > 0) ? 1u : 0u);
-                            }
+                    const uint32_t ph = (s_next >> 1) & 1;
+                    if (s_half == 0 && ptx::mbar_test_wait(kfull + st, ph) &&
+                        (s_next < 2 || ptx::mbar_test_wait(sempty + st, ph ^ 1))) {
+                        issue_s(st, 0, 4);
+                        s_half = 1;
+                        progressed = true;
+                    }
+                    if (s_half == 1 && ptx::mbar_test_wait(kfull + 2 + st, ph)) {
+                        issue_s(st, 4, KB);
                         ptx::mma_commit(sfull + st);
+                        s_half = 0;
                         ++s_next;
                         progressed = true;
                     }
                 }
-                if (pv_next < s_next && ptx::mbar_try_wait(pfull, pv_next & 1)) {
+                if (pv_next < s_next && ptx::mbar_test_wait(pfull, pv_next & 1)) {
                     if (!issue_pv(pv_next)) {
                         ok = false;
                         break;
@@ -662,51 +682,57 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
             }
             if (ok) ptx::mma_commit(ofull);
         }
-    } else if (warp >= 6) {
+    } else if (warp >= 2 + kSoftWarps) {
         // ------------------------------------------------------------ gather
-        const int gt = threadIdx.x - 6 * 32;  // 0..255
+        // thread gt: 16-byte chunk c8 of rows r0 and r0 + 32 in every 64-dim
+        // block (eight threads read one row's 128 contiguous bytes of a block)
+        const int gt = threadIdx.x - (2 + kSoftWarps) * 32;  // 0..255
+        const int c8 = gt & 7, r0 = gt >> 3;
+        const uint32_t soff = (uint32_t)r0 * 128 + ((c8 ^ (r0 & 7)) << 4);  // same swizzle for r0 + 32
         for (int i = 0; i < ntiles; ++i) {
             const int st = i & 1, r = i % kRing;
             if (!__all_sync(0xffffffffu, ptx::mbar_wait(rfull + r, (i / kRing) & 1, abort_flag, d_status))) break;
-            uint4 v[18];
+            const uint4* g0 = reinterpret_cast<const uint4*>(latent + (size_t)max(srow[r * TK + r0], 0) * (kMD * 2)) + c8;
+            const uint4* g1 = reinterpret_cast<const uint4*>(latent + (size_t)max(srow[r * TK + r0 + 32], 0) * (kMD * 2)) + c8;
+            uint4 v[18];  // v[2 kb + h]: block kb of row r0 + 32 h
 #pragma unroll
-            for (int u = 0; u < 18; ++u) {
-                const int e = gt + u * 256;
-                const int row = e / 72, c = e - row * 72;
-                const int pr = srow[r * TK + row];
-                v[u] = __ldg(reinterpret_cast<const uint4*>(latent + (size_t)max(pr, 0) * (kMD * 2)) + c);
-            }
+            for (int u = 0; u < 18; ++u) v[u] = __ldg(((u & 1) ? g1 : g0) + (u >> 1) * 8);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(rfree + r);
-            if (i >= 2 && !__all_sync(0xffffffffu, ptx::mbar_wait(kempty + st, ((i >> 1) - 1) & 1, abort_flag, d_status)))
-                break;
-            uint8_t* dst = stage + st * kStage;
+            uint8_t* dst = stage + st * kStage + soff;
+            bool ok = true;
 #pragma unroll
-            for (int u = 0; u < 18; ++u) {
-                const int e = gt + u * 256;
-                const int row = e / 72, c = e - row * 72;
-                *reinterpret_cast<uint4*>(dst + (c >> 3) * kKBlock + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = v[u];
+            for (int half = 0; half < 2; ++half) {
+                // blocks 0-3 once the product two tiles back has read them, then blocks 4-8
+                if (i >= 2 && !__all_sync(0xffffffffu, ptx::mbar_wait(kempty + 2 * half + st, ((i >> 1) - 1) & 1,
+                                                                      abort_flag, d_status))) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int u = half ? 8 : 0; u < (half ? 18 : 8); ++u)
+                    *reinterpret_cast<uint4*>(dst + (u >> 1) * kKBlock + (u & 1) * 32 * 128) = v[u];
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(kfull + 2 * half + st);
             }
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(kfull + st);
+            if (!ok) break;
         }
     } else {
-        // ------------------------------------------------------------ softmax and output (warps 2-5)
+        // ------------------------------------------------------------ softmax and output (warps 2-9)
         const int quarter = warp & 3;                       // TMEM lanes 32*quarter ..
-        const int sw = warp - 2;                            // softmax warp index 0..3
+        const int sw = warp - 2;                            // softmax warp index 0..7
+        const int hb = (sw >> 2) * 32;                      // this warp's heads hb .. hb+31
         const bool mine = lane < 16;                        // lanes holding a key of the tile
         const int key = quarter * 16 + (lane & 15);         // key row of the tile
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's TMEM lanes
-        float* my_mu = mu + sw * kMH;
+        float* my_mu = mu + sw * 32;                        // running max of heads hb .. hb+31
         my_mu[lane] = -INFINITY;
-        my_mu[lane + 32] = -INFINITY;
         {
             float z[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) z[j] = 0.f;
-            ptx::tmem_st32(tl + kLCol, z);
-            ptx::tmem_st32(tl + kLCol + 32, z);
+            ptx::tmem_st32(tl + kLCol + hb, z);
         }
         __syncwarp();
         bool alive = true;
@@ -722,21 +748,21 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(rfree + r);
             ptx::tc_fence_after();
-            const uint32_t s_addr = tl + kSCol + st * kMH;
+            const uint32_t s_addr = tl + kSCol + st * kMH + hb;
             // does any score of this tile rise more than 2^64 above the running max?
             bool grow = i == 0;
             if (i > 0) {
-                float sv[64];
-                ptx::tmem_ld64(s_addr, sv);
+                float sv[32];
+                ptx::tmem_ld32(s_addr, sv);
                 float over = -INFINITY;
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
+                for (int q = 0; q < 8; ++q) {
                     const float4 m4 = reinterpret_cast<const float4*>(my_mu)[q];
                     over = fmaxf(over, fmaxf(fmaxf(sv[4 * q] * scale_log2 - m4.x, sv[4 * q + 1] * scale_log2 - m4.y),
                                              fmaxf(sv[4 * q + 2] * scale_log2 - m4.z, sv[4 * q + 3] * scale_log2 - m4.w)));
                 }
                 const bool g = __any_sync(0xffffffffu, valid && over > kRescale);
-                if (lane == 0) wflag[st * 4 + sw] = g ? 1 : 0;
+                if (lane == 0) wflag[st * kSoftWarps + sw] = g ? 1 : 0;
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(xch + st);
                 // xch[st] serves tiles 1, 2, 3, ... (not 0): use u of it is tile 2u+1 or 2u+2
@@ -744,17 +770,20 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                     alive = false;
                     break;
                 }
-                grow = (wflag[st * 4] | wflag[st * 4 + 1] | wflag[st * 4 + 2] | wflag[st * 4 + 3]) != 0;
+                int any = 0;
+#pragma unroll
+                for (int w = 0; w < kSoftWarps; ++w) any |= wflag[st * kSoftWarps + w];
+                grow = any != 0;
             }
-            float a_lo = 1.f, a_hi = 1.f;
+            float alpha = 1.f;  // lane j: rescale factor of head hb + j
             if (grow) {
                 // exact per-head maxima of this tile (first tile, or a growth)
-                float sv[64];
-                ptx::tmem_ld64(s_addr, sv);
+                float sv[32];
+                ptx::tmem_ld32(s_addr, sv);
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
+                for (int j = 0; j < 32; ++j) {
                     const float m = ptx::warp_max(valid ? sv[j] * scale_log2 : -INFINITY);
-                    if (lane == (j & 31)) wmax[sw * kMH + j] = m;
+                    if (lane == j) wmax[quarter * kMH + hb + j] = m;
                 }
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(xmax);
@@ -763,16 +792,13 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                     break;
                 }
                 ++n_grow;
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int h = lane + 32 * u;
-                    const float mt = fmaxf(fmaxf(wmax[h], wmax[kMH + h]), fmaxf(wmax[2 * kMH + h], wmax[3 * kMH + h]));
-                    const float mo = my_mu[h];
-                    const float mn = fmaxf(mo, mt);
-                    const float a = (mo == -INFINITY || mn == mo) ? (mo == mn ? 1.f : 0.f) : exp2f(mo - mn);
-                    if (u == 0) a_lo = a; else a_hi = a;
-                    my_mu[h] = mn;
-                }
+                const int h = hb + lane;
+                const float mt = fmaxf(fmaxf(wmax[h], wmax[kMH + h]), fmaxf(wmax[2 * kMH + h], wmax[3 * kMH + h]));
+                const float mo = my_mu[lane];
+                const float mn = fmaxf(mo, mt);
+                alpha = (mo == -INFINITY || mn == mo) ? (mo == mn ? 1.f : 0.f) : exp2f(mo - mn);
+                __syncwarp();
+                my_mu[lane] = mn;
                 __syncwarp();
             }
             const bool rescale = grow && i > 0;
@@ -784,32 +810,22 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                 }
                 ptx::tc_fence_after();
 #pragma unroll 1
-                for (int c = 0; c < 16; ++c) {  // columns 16c .. 16c+15 = heads 16 (c % 4) ..
+                for (int c = 0; c < 10; ++c) {  // 4 value blocks x 2 halves of this warp's heads, then the row sums
+                    const uint32_t col = c < 8 ? kOCol + (c >> 1) * kMH + hb + (c & 1) * 16 : kLCol + hb + (c & 1) * 16;
                     float o[16];
-                    ptx::tmem_ld16(tl + kOCol + c * 16, o);
+                    ptx::tmem_ld16(tl + col, o);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        o[j] *= __shfl_sync(0xffffffffu, (c & 2) ? a_hi : a_lo, (c & 1) * 16 + j);
-                    ptx::tmem_st16(tl + kOCol + c * 16, o);
-                }
-                // and the row sums: columns 16g .. 16g+15 = heads 16g ..
-#pragma unroll 1
-                for (int g = 0; g < 4; ++g) {
-                    float lv[16];
-                    ptx::tmem_ld16(tl + kLCol + g * 16, lv);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        lv[j] *= __shfl_sync(0xffffffffu, (g & 2) ? a_hi : a_lo, (g & 1) * 16 + j);
-                    ptx::tmem_st16(tl + kLCol + g * 16, lv);
+                    for (int j = 0; j < 16; ++j) o[j] *= __shfl_sync(0xffffffffu, alpha, (c & 1) * 16 + j);
+                    ptx::tmem_st16(tl + col, o);
                 }
             }
-            // probabilities, row sums (TMEM), P^T row (128 bytes, swizzled) over the rope block
+            // probabilities, row sums (TMEM), this warp's half of the P^T row over the rope block
             uint8_t* prow = stage + st * kStage + 8 * kKBlock + key * 128;
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {  // 16 heads at a time
+            for (int g = 0; g < 2; ++g) {  // 16 heads at a time
                 float sv[16], lv[16];
                 ptx::tmem_ld16(s_addr + g * 16, sv);
-                ptx::tmem_ld16(tl + kLCol + g * 16, lv);
+                ptx::tmem_ld16(tl + kLCol + hb + g * 16, lv);
                 uint32_t pk[8];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -824,11 +840,11 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                     pk[2 * q] = pack_bf16(p[0], p[1]);
                     pk[2 * q + 1] = pack_bf16(p[2], p[3]);
                 }
-                ptx::tmem_st16(tl + kLCol + g * 16, lv);
+                ptx::tmem_st16(tl + kLCol + hb + g * 16, lv);
                 if (mine) {
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
-                        const int cc = g * 2 + c;
+                        const int cc = (hb >> 3) + g * 2 + c;
                         *reinterpret_cast<uint4*>(prow + ((cc ^ (key & 7)) << 4)) =
                             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
                     }
@@ -842,68 +858,63 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                 ptx::mbar_arrive(pfull);
             }
         }
-        // ---- row sums of this warp -> lsum[sw][64]
+        // ---- row sums of this warp's 16 keys -> lsum[quarter][hb .. hb+31]
         if (alive && ntiles > 0) {
             ptx::tc_fence_after();
+            float lv[32];
+            ptx::tmem_ld32(tl + kLCol + hb, lv);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float lv[32];
-                ptx::tmem_ld32(tl + kLCol + half * 32, lv);
+            for (int j = 0; j < 32; ++j) {
+                float v = lv[j];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    float v = lv[j];
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);  // lanes 16-31 add zeros
-                    if (lane == j) lsum[sw * kMH + half * 32 + j] = v;
-                }
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);  // lanes 16-31 add zeros
+                if (lane == j) lsum[quarter * kMH + hb + j] = v;
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(lready);
         }
-        // ---- output: all four warps, one value dim per thread of each 128-dim block
-        const float* ml_m = mu;  // every warp's copy of the running max is the same
+        // ---- output: value dim quarter*32 + lane of each 128-dim block, heads hb .. hb+31
         const int dim = quarter * 32 + lane;
         bool have = alive && ntiles > 0;
         if (have) have = __all_sync(0xffffffffu, ptx::mbar_wait(lready, 0, abort_flag, d_status));
         if (have) have = __all_sync(0xffffffffu, ptx::mbar_wait(ofull, 0, abort_flag, d_status));
         if (have) ptx::tc_fence_after();
         auto total_l = [&](int h) { return lsum[h] + lsum[kMH + h] + lsum[2 * kMH + h] + lsum[3 * kMH + h]; };
+        auto run_max = [&](int h) { return mu[(h >> 5) * 4 * 32 + (h & 31)]; };  // copy of warp sw = 4 (h / 32)
         if (splits == 1) {
             __nv_bfloat16* ot = out + (int64_t)t * kMH * kMV;
 #pragma unroll 1
-            for (int c = 0; c < 8; ++c) {  // 32 columns = 32 heads of one 128-dim block
+            for (int db = 0; db < 4; ++db) {  // 32 columns = heads hb .. hb+31 of one 128-dim block
                 float o[32];
-                const int db = c >> 1, h0 = (c & 1) * 32;
-                if (have) ptx::tmem_ld32(tl + kOCol + c * 32, o);
+                if (have) ptx::tmem_ld32(tl + kOCol + db * kMH + hb, o);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const int h = h0 + j;
+                    const int h = hb + j;
                     const float L = have ? total_l(h) : 0.f;
                     const float v = L > 0.f ? o[j] / L : 0.f;
                     ot[(int64_t)h * kMV + db * 128 + dim] = __float2bfloat16_rn(v);
                 }
             }
-            if (lse && warp == 2) {
+            if (lse && sw == 0) {
                 for (int h = lane; h < kMH; h += 32) {
                     const float L = have ? total_l(h) : 0.f;
-                    lse[(int64_t)t * kMH + h] = L > 0.f ? (ml_m[h] + log2f(L)) * 0.69314718055994531f : -INFINITY;
+                    lse[(int64_t)t * kMH + h] = L > 0.f ? (run_max(h) + log2f(L)) * 0.69314718055994531f : -INFINITY;
                 }
             }
         } else {
             float* po = part_o + ((int64_t)t * splits + sp) * kMH * kMV;
 #pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
+            for (int db = 0; db < 4; ++db) {
                 float o[32];
-                const int db = c >> 1, h0 = (c & 1) * 32;
-                if (have) ptx::tmem_ld32(tl + kOCol + c * 32, o);
+                if (have) ptx::tmem_ld32(tl + kOCol + db * kMH + hb, o);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) po[(int64_t)(h0 + j) * kMV + db * 128 + dim] = have ? o[j] : 0.f;
+                for (int j = 0; j < 32; ++j) po[(int64_t)(hb + j) * kMV + db * 128 + dim] = have ? o[j] : 0.f;
             }
-            if (warp == 2) {
+            if (sw == 0) {
                 for (int h = lane; h < kMH; h += 32) {
                     float* ml = part_ml + (((int64_t)t * splits + sp) * kMH + h) * 2;
                     const float L = have ? total_l(h) : 0.f;
-                    ml[0] = L > 0.f ? ml_m[h] : -INFINITY;
+                    ml[0] = L > 0.f ? run_max(h) : -INFINITY;
                     ml[1] = L;
                 }
             }
