@@ -5,12 +5,17 @@
 // select; top-k compaction with topk_length instead of slots full of -1).
 //
 // The selection never sorts the context.  Scores map to order-preserving
-// 32-bit keys (-0.0 folded onto +0.0); four 8-bit digit passes, each a shared-
-// memory histogram of the keys that still match the selected prefix, pin the
-// exact k-th largest key T and how many keys equal to T are needed.  A final
-// pass in index order writes every key > T and the first needed keys == T
-// (ties to the smaller index) with block-wide prefix sums, so the output is
-// the selected positions in ascending order: deterministic and compacted.
+// 32-bit keys (-0.0 folded onto +0.0); digit passes, each a shared-memory
+// histogram of the keys that still match the selected prefix, pin the exact
+// k-th largest key T and how many keys equal to T are needed.  A final pass in
+// index order writes every key > T and the first needed keys == T (ties to the
+// smaller index) with block-wide prefix sums, so the output is the selected
+// positions in ascending order: deterministic and compacted.
+//
+// Three kernels share that scheme: rows up to 32,768 keys take one CTA each
+// with the row in registers (three passes of 11 + 11 + 10 bits); longer rows
+// up to 16 x 32,768 keys a thread-block cluster per row; anything longer one
+// CTA per row with four 8-bit passes over memory.
 #include <cooperative_groups.h>
 
 #include <mutex>
@@ -150,6 +155,206 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
     }
     for (int i = base_out + tid; i < k; i += kTopkThreads) out[i] = -1;
     if (tid == 0) topk_len[t] = min(base_out, k);
+}
+
+// exclusive prefix sum over the THREADS threads of a block; *total = sum
+template <int THREADS>
+__device__ __forceinline__ int scan_threads(int v, int* buf, int* total) {
+    constexpr int W = THREADS / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) buf[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < W ? buf[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        buf[32 + lane] = w;
+    }
+    __syncthreads();
+    const int before = (warp ? buf[32 + warp - 1] : 0) + x - v;
+    *total = buf[32 + W - 1];
+    __syncthreads();
+    return before;
+}
+
+// ---------------------------------------------------------------------------
+// One CTA per row, the row held in registers (THREADS threads x EPT
+// consecutive scores, rows up to 32,768 keys).  Three digit passes (11 + 11 + 10 bits)
+// with __syncthreads only.  Scores of a row crowd into few bins of the first
+// digit, so that histogram is counted into eight private copies (four warps
+// each) to spread the same-address atomics; the keys of the chosen bin are
+// then compacted into shared memory and the two finer passes run over them.
+constexpr int kRowBins = 2048;
+constexpr int kRowSub = 8;             // private copies of the first histogram
+constexpr int kRowCandCap = 4096;
+constexpr size_t kRowSmem = (size_t)kRowSub * kRowBins * 4 + kRowCandCap * 4;
+
+template <int THREADS, int EPT>
+__global__ void __launch_bounds__(THREADS, 1) topk_row_kernel(const float* __restrict__ scores, int64_t ld,
+                                                                dsa_seqs s, int k, int32_t* __restrict__ idx,
+                                                                int32_t* __restrict__ topk_len, int32_t* d_status) {
+    extern __shared__ __align__(16) int row_smem[];
+    int* sub = row_smem;                                                   // [kRowSub][kRowBins]
+    uint32_t* cand = reinterpret_cast<uint32_t*>(row_smem + kRowSub * kRowBins);  // [kRowCandCap]
+    __shared__ int scan_buf[64];
+    __shared__ int sel_digit, sel_above, ncand;
+    const int t = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = seq_of(s.q_start, s.num_seqs, t);
+    const int pos = __ldg(s.q_pos + t);
+    const int ctx = __ldg(s.ctx_len + b);
+    int32_t* out = idx + (int64_t)t * k;
+    if (pos < 0 || pos >= ctx || ctx > s.max_ctx || pos + 1 > THREADS * EPT) {
+        if (tid == 0) {
+            report(d_status, DSA_ERR_BAD_INPUT);
+            topk_len[t] = 0;
+        }
+        for (int i = tid; i < k; i += THREADS) out[i] = -1;
+        return;
+    }
+    const int n = pos + 1;
+    if (n <= k) {
+        for (int i = tid; i < k; i += THREADS) out[i] = i < n ? i : -1;
+        if (tid == 0) topk_len[t] = n;
+        return;
+    }
+    // ---- this thread's EPT consecutive keys: every load issued before any is
+    // used (indexes clamped into the row, so no load waits on a bounds branch)
+    const float* row = scores + (int64_t)t * ld;
+    const int base = tid * EPT;
+    const int last4 = (int)((ld - 4) & ~(int64_t)3);  // the row holds ld >= n floats, ld a multiple of 4
+    uint32_t u[EPT];  // raw bits first, order keys after
+    if (base + EPT <= ld) {  // the whole run lies in the row: offsets from one pointer
+        const uint4* p = reinterpret_cast<const uint4*>(row + base);
+#pragma unroll
+        for (int v = 0; v < EPT / 4; ++v) {
+            const uint4 r = __ldg(p + v);
+            u[4 * v] = r.x;
+            u[4 * v + 1] = r.y;
+            u[4 * v + 2] = r.z;
+            u[4 * v + 3] = r.w;
+        }
+    } else {
+#pragma unroll
+        for (int v = 0; v < EPT / 4; ++v) {
+            const uint4 r = __ldg(reinterpret_cast<const uint4*>(row + min(base + 4 * v, last4)));
+            u[4 * v] = r.x;
+            u[4 * v + 1] = r.y;
+            u[4 * v + 2] = r.z;
+            u[4 * v + 3] = r.w;
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) u[e] = order_key(__uint_as_float(u[e]));
+    const int nv = min(max(n - base, 0), EPT);  // this thread's keys inside the row: u[0 .. nv)
+    uint32_t prefix = 0, mask = 0;
+    int remaining = k;
+    bool use_cand = false;
+    if (tid == 0) ncand = 0;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int nb = pass == 2 ? 1024 : 2048;
+        const int copies = use_cand ? 1 : kRowSub;
+        for (int i = tid; i < copies * kRowBins; i += THREADS) sub[i] = 0;
+        __syncthreads();
+        if (use_cand) {
+            for (int i = tid; i < ncand; i += THREADS) {
+                const uint32_t c = cand[i];
+                if ((c & mask) == prefix) atomicAdd(sub + ((c >> shift) & (nb - 1)), 1);
+            }
+        } else {
+            int* h = sub + (warp % kRowSub) * kRowBins;
+#pragma unroll
+            for (int e = 0; e < EPT; ++e)
+                if ((e < nv) && (u[e] & mask) == prefix) atomicAdd(h + ((u[e] >> shift) & (nb - 1)), 1);
+        }
+        __syncthreads();
+        // digits in descending order, nb / 1024 per thread, summed over the copies
+        constexpr int kMaxPer = kRowBins / THREADS;
+        const int per = nb / THREADS;
+        static_assert(kRowBins % THREADS == 0 && 1024 % THREADS == 0, "bins per thread");
+        int c[kMaxPer], csum = 0;
+#pragma unroll
+        for (int q = 0; q < kMaxPer; ++q) {
+            int v = 0;
+            if (q < per) {
+                const int d = nb - 1 - per * tid - q;
+                for (int cp = 0; cp < copies; ++cp) v += sub[cp * kRowBins + d];
+            }
+            c[q] = v;
+            csum += v;
+        }
+        int tot;
+        int before = scan_threads<THREADS>(csum, scan_buf, &tot);
+#pragma unroll
+        for (int q = 0; q < kMaxPer; ++q) {
+            if (q < per && before < remaining && before + c[q] >= remaining) {
+                sel_digit = nb - 1 - per * tid - q;
+                sel_above = before;
+            }
+            before += c[q];
+        }
+        __syncthreads();
+        prefix |= (uint32_t)sel_digit << shift;
+        mask |= (uint32_t)(nb - 1) << shift;
+        remaining -= sel_above;
+        if (pass == 0) {
+            // keep the keys of the chosen bin for the next two passes (prefix-sum slots)
+            int mine = 0;
+#pragma unroll
+            for (int e = 0; e < EPT; ++e) mine += (e < nv) && (u[e] & mask) == prefix;
+            int nc;
+            int sl = scan_threads<THREADS>(mine, scan_buf, &nc);
+            if (nc <= kRowCandCap) {
+#pragma unroll
+                for (int e = 0; e < EPT; ++e)
+                    if ((e < nv) && (u[e] & mask) == prefix) cand[sl++] = u[e];
+            }
+            if (tid == 0) ncand = nc;
+            __syncthreads();
+            use_cand = nc <= kRowCandCap;
+        } else {
+            __syncthreads();  // the next pass clears the histogram this one read
+        }
+    }
+    const uint32_t T = prefix;
+    const int need_eq = remaining;
+    // ---- ranks in index order: every key > T, the first need_eq keys == T
+    int n_gt = 0, n_eq = 0;
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+        const bool vld = e < nv;
+        n_gt += vld && u[e] > T;
+        n_eq += vld && u[e] == T;
+    }
+    int tot_eq;
+    int eq_rank = scan_threads<THREADS>(n_eq, scan_buf, &tot_eq);
+    const int n_sel = n_gt + max(0, min(need_eq - eq_rank, n_eq));
+    int tot_sel;
+    int o = scan_threads<THREADS>(n_sel, scan_buf, &tot_sel);
+    // positions staged in shared memory (the candidate buffer, k <= its size),
+    // then written out with coalesced stores
+    int* stage_out = reinterpret_cast<int*>(cand);
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+        if (!(e < nv)) continue;
+        bool take = u[e] > T;
+        if (u[e] == T) take = eq_rank++ < need_eq;
+        if (take && o < k) stage_out[o++] = base + e;
+    }
+    __syncthreads();
+    for (int i = tid; i < k; i += THREADS) out[i] = stage_out[i];
+    if (tid == 0) topk_len[t] = k;
 }
 
 // ---------------------------------------------------------------------------
@@ -442,8 +647,29 @@ cudaError_t launch_cluster(int cl, const float* scores, int64_t ld, const dsa_se
 
 }  // namespace
 
+template <int THREADS, int EPT>
+cudaError_t launch_row(const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int k, int32_t* idx,
+                       int32_t* topk_len, int32_t* d_status, cudaStream_t stream) {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(topk_row_kernel<THREADS, EPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kRowSmem);
+    });
+    if (attr != cudaSuccess) return attr;
+    topk_row_kernel<THREADS, EPT><<<num_q, THREADS, kRowSmem, stream>>>(scores, ld, s, k, idx, topk_len, d_status);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_topk(const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int k, int32_t* idx,
                         int32_t* topk_len, int32_t* d_status, cudaStream_t stream) {
+    // rows up to 32,768 keys: one CTA per row, held in registers
+    if (s.max_ctx <= 1024 * 8)
+        return launch_row<1024, 8>(scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
+    if (s.max_ctx <= 1024 * 16)
+        return launch_row<1024, 16>(scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
+    if (s.max_ctx <= 512 * 64)
+        return launch_row<512, 64>(scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
     const ClusterPlan p = topk_plan(s.max_ctx, num_q);
     if (p.cl <= 16 && p.ept <= 64) {
         if (p.ept == 16 && p.cl <= max_cluster<16>())
