@@ -11,7 +11,7 @@
 //   relu(f x) = |f| relu(sgn(f) x), and sqrt(128) sqrt(32) = 64, so
 //   score = sum_h w'_h relu(q'_h . k_j) with w'_h = w_h |f_h| / 64 and
 //   q'_h = sgn(f_h) rot(q_h).  The unrotated dims of q' stay exact bf16; the 64
-//   rotated dims (fp64 angle, fp32 rotation) are split into hi + lo 16-bit
+//   rotated dims (exact fp64 angle, fp32 rotation) are split into hi + lo 16-bit
 //   parts, so the contraction runs over K = 192 columns [hi | lo | unrotated]
 //   against key dims [0..63 | 0..63 | 64..127] and reproduces the fp64 query to
 //   ~2^-17 relative.  That keeps the top-k boundary exact (see dsa_topk).
@@ -30,11 +30,13 @@ namespace dsa {
 // ---------------------------------------------------------------------------
 // query preparation: q' [Q, 32, KP] (KP = 192 RoPE, 128 NoPE), w' [Q, 32]
 //
-// The 32 SSMax factors and the 32 rotation angles of a query are computed in
-// fp64 (the angle pos*inv_freq reaches ~5e5 rad at 512K context, where fp32
-// would lose the phase); cos and sin of the fp64 angle are then rounded to
-// fp32 and the rotation of the exact bf16 inputs runs in fp32 with fused
-// multiply-adds (relative error ~2^-23, below the 2^-17 of the hi + lo split).
+// The 32 rotation angles of a query are formed in fp64, where pos*inv_freq is
+// exact (it reaches ~5e5 rad at 512K context, where an fp32 angle would lose
+// the phase), reduced by 2 pi in fp64 and passed to fp32 sincos; the 32 SSMax
+// factors s log(pos + 1) + b are fp32.  The rotation of the exact bf16 inputs
+// runs in fp32 with fused multiply-adds (relative error ~2^-22, below the
+// 2^-17 of the hi + lo split).  GB300's fp64 rate is tiny: only the angle and
+// its reduction stay in fp64.
 template <typename T>
 __device__ __forceinline__ T from_float(float x);
 template <>
@@ -47,6 +49,13 @@ template <>
 __device__ __forceinline__ float to_float<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
 template <>
 __device__ __forceinline__ float to_float<__half>(__half x) { return __half2float(x); }
+
+// 2 pi = kTwoPi1 + kTwoPi2 + kTwoPi3 (within 1e-33 relative); the first two
+// have 26 significant bits each
+constexpr double kTwoPi1 = 0x1.921fb58p+2;
+constexpr double kTwoPi2 = -0x1.dde974p-25;
+constexpr double kTwoPi3 = 0x1.1a62633145c07p-52;
+constexpr double kInvTwoPi = 0x1.45f306dc9c883p-3;
 
 template <typename T>
 __global__ void __launch_bounds__(128) qprep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ w,
@@ -68,15 +77,32 @@ __global__ void __launch_bounds__(128) qprep_kernel(const __nv_bfloat16* __restr
     }
     if (threadIdx.x < 32) {
         const int h = threadIdx.x;
-        const double f = (double)__ldg(ss + h) * log((double)pos + 1.0) + (double)__ldg(sb + h);
-        sgn[h] = f < 0.0 ? -1.f : 1.f;
-        wp[(int64_t)t * kIH + h] = (float)((double)__ldg(w + (int64_t)t * kIH + h) * fabs(f) / 64.0);
+        const float f = fmaf(__ldg(ss + h), logf((float)pos + 1.f), __ldg(sb + h));
+        sgn[h] = f < 0.f ? -1.f : 1.f;
+        wp[(int64_t)t * kIH + h] = __ldg(w + (int64_t)t * kIH + h) * fabsf(f) * (1.f / 64.f);
     } else if (threadIdx.x < 64 && rope) {
         const int i = threadIdx.x - 32;  // rotation pair
-        double sd, cd;
-        sincos((double)pos * (double)__ldg(inv_freq + i), &sd, &cd);
-        cs[i] = (float)cd;
-        sn[i] = (float)sd;
+        // The angle pos * inv_freq is exact in fp64 (a 31-bit integer times a
+        // float).  Cody & Waite's reduction by 2 pi, split into two 26-bit
+        // parts and an fp64 remainder, keeps that accuracy for |k| < 2^27
+        // (k * C1 and k * C2 are exact); cos and sin of the reduced angle in
+        // fp32.  Larger angles take the fp64 library sincos.
+        const double th = (double)pos * (double)__ldg(inv_freq + i);
+        const double kq = rint(th * kInvTwoPi);
+        float sf, cf;
+        if (fabs(kq) < 134217728.0) {
+            double r = fma(-kq, kTwoPi1, th);
+            r = fma(-kq, kTwoPi2, r);
+            r = fma(-kq, kTwoPi3, r);
+            sincosf((float)r, &sf, &cf);
+        } else {
+            double sd, cd;
+            sincos(th, &sd, &cd);
+            sf = (float)sd;
+            cf = (float)cd;
+        }
+        cs[i] = cf;
+        sn[i] = sf;
     }
     __syncthreads();
     // one work item = 4 consecutive pairs (8 dims) of one head
