@@ -70,7 +70,7 @@ def load(path: str = LIB_PATH):
         L.dsa_decode_layer.argtypes = [ctypes.POINTER(DsaLayerArgsC), S, I32, P, SZ, P, P]
         L.sparse_mla_decode_noalloc.argtypes = [P, P, ctypes.c_int, S, I32, P, P, I32, ctypes.c_float, P, P, P, P]
         L.sparse_mla_decode_noalloc.restype = ctypes.c_int
-        L.dsa_decode_layer_launches.argtypes = [S, I32, I32, I32]
+        L.dsa_decode_layer_launches.argtypes = [S, I32, I32, I32, ctypes.c_int]
         L.dsa_decode_layer_launches.restype = ctypes.c_int32
         for f in ("dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode", "dsa_decode_layer"):
             getattr(L, f).restype = ctypes.c_int
@@ -164,9 +164,9 @@ def sparse_mla_decode_noalloc(q, latent, latent_dtype: int, seqs: Seqs, num_q: i
                                             _stream(stream)))
 
 
-def dsa_decode_layer_launches(seqs: Seqs, num_q: int, k: int, reuse_idx: int = 0) -> int:
+def dsa_decode_layer_launches(seqs: Seqs, num_q: int, k: int, reuse_idx: int = 0, latent_dtype: int = 0) -> int:
     sc = seqs.c()
-    return int(load().dsa_decode_layer_launches(ctypes.byref(sc), num_q, k, reuse_idx))
+    return int(load().dsa_decode_layer_launches(ctypes.byref(sc), num_q, k, reuse_idx, latent_dtype))
 
 
 def dsa_decode_layer(args: dict, seqs: Seqs, num_q: int, workspace, workspace_bytes: int, d_status=None,

@@ -274,13 +274,18 @@ dsa_status dsa_decode_layer(const dsa_layer_args* a, const dsa_seqs* seqs, int32
     return cuda_status(e, "dsa_decode_layer launch");
 }
 
-int32_t dsa_decode_layer_launches(const dsa_seqs* seqs, int32_t num_q, int32_t k, int32_t reuse_idx) {
+int32_t dsa_decode_layer_launches(const dsa_seqs* seqs, int32_t num_q, int32_t k, int32_t reuse_idx,
+                                  dsa_dtype latent_dtype) {
     Check c;
     check_seqs(c, seqs, num_q);
     c.need(k >= 1 && k <= DSA_MAX_TOPK, DSA_ERR_UNSUPPORTED, "k %d outside [1, %d]", k, DSA_MAX_TOPK);
+    c.need(latent_dtype == DSA_BF16 || latent_dtype == DSA_FP8_DS_MLA, DSA_ERR_INVALID_ARG, "latent_dtype %d",
+           (int)latent_dtype);
     if (c.done() != DSA_OK || num_q == 0) return 0;
-    const int mla = mla_splits(num_q, k) > 1 ? 2 : 1;  // attention (+ LSE combine)
-    return (reuse_idx ? 0 : 3) + mla;                  // query prep, scores, top-k
+    const int splits = mla_splits(num_q, k);
+    // attention, plus the LSE combine unless the splits combine in-kernel (bf16, two splits)
+    const int mla = (splits == 1 || (latent_dtype == DSA_BF16 && splits == 2)) ? 1 : 2;
+    return (reuse_idx ? 0 : 3) + mla;  // query prep, scores, top-k
 }
 
 }  // extern "C"

@@ -19,6 +19,7 @@
 // fp8_ds_mla rows are dequantised in-kernel: e4m3 codes decode exactly to
 // bf16, the four per-group scales multiply the per-group partial scores and
 // fold into the probabilities of the value product.
+#include <cooperative_groups.h>
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -433,6 +434,17 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restric
     }
 }
 
+// 16-byte read-only load that does not allocate in L1: gathered rows are used
+// once, and skipping the L1 fill leaves the shared-memory banks (the same SRAM)
+// to the tensor-core operand reads.
+__device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
 // ---------------------------------------------------------------------------
 // bf16 latent cache on the 5th-generation tensor cores.
 //
@@ -478,10 +490,11 @@ static_assert(kKBlock == TK * kMH * 2, "P^T must fit the rope block of its tile"
 __global__ void __launch_bounds__(tcmla::kThreads, 1)
     mla_tc_kernel(const __grid_constant__ CUtensorMap qmap, const uint8_t* __restrict__ latent, dsa_seqs s,
                   const int32_t* __restrict__ idx, const int32_t* __restrict__ topk_len, int k, float scale_log2,
-                  int splits, __nv_bfloat16* __restrict__ out, float* __restrict__ lse, float* __restrict__ part_o,
-                  float* __restrict__ part_ml, int32_t* d_status) {
+                  int splits, int pair, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                  float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* d_status) {
     using namespace tcmla;
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t tc_smem[];   // 1024-aligned for the 128-byte swizzle atoms
+    uint8_t* const smem = tc_smem;
     uint8_t* stage = smem;                                  // [2][KB][TK rows x 128 B]; block 8 later holds P^T
     uint8_t* qs = smem + 2 * kStage;                        // [KB][64 heads x 128 B]
     uint8_t* misc = qs + kQBytes;
@@ -696,7 +709,7 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
             const uint4* g1 = reinterpret_cast<const uint4*>(latent + (size_t)max(srow[r * TK + r0 + 32], 0) * (kMD * 2)) + c8;
             uint4 v[18];  // v[2 kb + h]: block kb of row r0 + 32 h
 #pragma unroll
-            for (int u = 0; u < 18; ++u) v[u] = __ldg(((u & 1) ? g1 : g0) + (u >> 1) * 8);
+            for (int u = 0; u < 18; ++u) v[u] = ldg_stream(((u & 1) ? g1 : g0) + (u >> 1) * 8);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(rfree + r);
             uint8_t* dst = stage + st * kStage + soff;
@@ -901,7 +914,7 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                     lse[(int64_t)t * kMH + h] = L > 0.f ? (run_max(h) + log2f(L)) * 0.69314718055994531f : -INFINITY;
                 }
             }
-        } else {
+        } else if (!pair) {
             float* po = part_o + ((int64_t)t * splits + sp) * kMH * kMV;
 #pragma unroll 1
             for (int db = 0; db < 4; ++db) {
@@ -918,7 +931,68 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                     ml[1] = L;
                 }
             }
+        } else {
+            // Two splits of this query form a cluster: CTA r keeps heads 32r ..
+            // 32r+31 and sends the other half of its unnormalised O^T, with the
+            // running max and row sum of those heads, into the partner's
+            // stages (free once every product of both CTAs is complete: the
+            // first cluster barrier), then combines its half after the second.
+            cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
+            const int me = (int)cluster.block_rank();
+            float* xo = reinterpret_cast<float*>(stage);   // [32 heads][512] partner's partial of my heads
+            float* xml = xo + 32 * kMV;                     // [32 heads][2] partner's (max, sum)
+            const float m_own = have ? run_max(hb + lane) : -INFINITY;
+            const float l_own = have ? total_l(hb + lane) : 0.f;
+            cluster.sync();  // 1: stages of both CTAs free
+            if (hb != me * 32) {
+                float* rxo = cluster.map_shared_rank(xo, me ^ 1);
+                float* rml = cluster.map_shared_rank(xml, me ^ 1);
+#pragma unroll 1
+                for (int db = 0; db < 4; ++db) {
+                    float o[32];
+                    if (have) ptx::tmem_ld32(tl + kOCol + db * kMH + hb, o);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) rxo[j * kMV + db * 128 + dim] = have ? o[j] : 0.f;
+                }
+                if (quarter == 0) {
+                    rml[lane * 2] = l_own > 0.f ? m_own : -INFINITY;
+                    rml[lane * 2 + 1] = l_own;
+                }
+            }
+            cluster.sync();  // 2: the partner's half is in my stages
+            if (hb == me * 32) {
+                // lane j: weights of head hb + j
+                const float m1 = xml[lane * 2], l1 = xml[lane * 2 + 1];
+                const float m0 = l_own > 0.f ? m_own : -INFINITY;
+                const float mx = fmaxf(m0, m1);
+                const float w0 = l_own > 0.f ? exp2f(m0 - mx) : 0.f;
+                const float w1 = l1 > 0.f ? exp2f(m1 - mx) : 0.f;
+                const float L = w0 * l_own + w1 * l1;
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                const float a0 = w0 * inv, a1 = w1 * inv;
+                __nv_bfloat16* ot = out + (int64_t)t * kMH * kMV;
+#pragma unroll 1
+                for (int db = 0; db < 4; ++db) {
+                    float o[32];
+                    if (have) ptx::tmem_ld32(tl + kOCol + db * kMH + hb, o);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float x = xo[j * kMV + db * 128 + dim];
+                        const float v = __shfl_sync(0xffffffffu, a0, j) * (have ? o[j] : 0.f) +
+                                        __shfl_sync(0xffffffffu, a1, j) * x;
+                        ot[(int64_t)(hb + j) * kMV + db * 128 + dim] = __float2bfloat16_rn(v);
+                    }
+                }
+                if (lse && quarter == 0)
+                    lse[(int64_t)t * kMH + hb + lane] = L > 0.f ? (mx + log2f(L)) * 0.69314718055994531f : -INFINITY;
+            }
         }
+    }
+    if (pair && (warp < 2 || warp >= 2 + kSoftWarps)) {
+        // the other roles take part in the two cluster barriers of the epilogue
+        cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
+        cluster.sync();
+        cluster.sync();
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -975,8 +1049,27 @@ cudaError_t launch_sparse_mla(const void* q, const void* latent, dsa_dtype laten
             if (e != cudaSuccess) return e;
             attr = true;
         }
+        if (splits == 2) {
+            // the two splits of a query run as a cluster and combine through
+            // distributed shared memory: no partials, no combine launch
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2, num_q, 1);
+            cfg.blockDim = dim3(tcmla::kThreads, 1, 1);
+            cfg.dynamicSmemBytes = tcmla::kSmem;
+            cfg.stream = stream;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            return cudaLaunchKernelEx(&cfg, mla_tc_kernel, qmap, reinterpret_cast<const uint8_t*>(latent), s, idx,
+                                      topk_len, k, scale_log2, splits, 1, reinterpret_cast<__nv_bfloat16*>(out), lse,
+                                      ws.mla_part, ws.mla_ml, d_status);
+        }
         mla_tc_kernel<<<dim3(splits, num_q), tcmla::kThreads, tcmla::kSmem, stream>>>(
-            qmap, reinterpret_cast<const uint8_t*>(latent), s, idx, topk_len, k, scale_log2, splits,
+            qmap, reinterpret_cast<const uint8_t*>(latent), s, idx, topk_len, k, scale_log2, splits, 0,
             reinterpret_cast<__nv_bfloat16*>(out), lse, ws.mla_part, ws.mla_ml, d_status);
         e = cudaGetLastError();
         if (e != cudaSuccess || splits == 1) return e;

@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(THREADS, 1) topk_row_kernel(const float* __res
     __shared__ int scan_buf[64];
     __shared__ int sel_digit, sel_above, ncand;
     const int t = blockIdx.x;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int b = seq_of(s.q_start, s.num_seqs, t);
     const int pos = __ldg(s.q_pos + t);
     const int ctx = __ldg(s.ctx_len + b);

@@ -57,9 +57,10 @@ class DecodeStep:
         return a
 
     def launches_per_step(self) -> int:
-        n = B.dsa_decode_layer_launches(self.seqs, self.num_q, self.k, 0)
+        lat = B.DSA_FP8_DS_MLA if self.lat_fp8 else B.DSA_BF16
+        n = B.dsa_decode_layer_launches(self.seqs, self.num_q, self.k, 0, lat)
         if self.shared:
-            n += B.dsa_decode_layer_launches(self.seqs, self.num_q, self.k, 1)
+            n += B.dsa_decode_layer_launches(self.seqs, self.num_q, self.k, 1, lat)
         return n
 
     def run(self, stream=None, events=None, events2=None):

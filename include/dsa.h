@@ -212,10 +212,12 @@ dsa_status sparse_mla_decode_noalloc(const void* q, const void* latent, dsa_dtyp
                                      const int32_t* topk_len, int32_t k, float sm_scale, void* out, float* lse,
                                      int32_t* d_status, cudaStream_t stream);
 
-/* Number of kernels dsa_decode_layer enqueues for these sizes (reuse_idx as
- * in dsa_layer_args); 0 when the sizes are refused.  For callers that count
- * or capture launches. */
-int32_t dsa_decode_layer_launches(const dsa_seqs* seqs, int32_t num_q, int32_t k, int32_t reuse_idx);
+/* Number of kernels dsa_decode_layer enqueues for these sizes (reuse_idx and
+ * latent_dtype as in dsa_layer_args); 0 when the sizes are refused.  For
+ * callers that count or capture launches.  (With a bf16 latent and two splits
+ * per query the attention combines its splits inside one launch.) */
+int32_t dsa_decode_layer_launches(const dsa_seqs* seqs, int32_t num_q, int32_t k, int32_t reuse_idx,
+                                  dsa_dtype latent_dtype);
 
 /* Text of the last non-OK status returned on this thread ("" if none). */
 const char* dsa_last_error_string(void);
