@@ -95,6 +95,17 @@ __device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Programmatic dependent launch.  The kernels of a layer run back to back on
+// one stream; each is launched with programmatic stream serialisation, lets
+// its own dependents launch at once and waits (griddepcontrol.wait: until the
+// preceding kernel has completed and its writes are visible) before its first
+// access to global memory.  The next kernel's CTAs are thus placed and ready
+// while the previous one drains, and no kernel reads anything early.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 2^x on the special-function unit (PTX ex2.approx.ftz.f32): relative error
 // near 2^-22, subnormal results flushed to zero, 2^-inf = 0.  Ample for
 // softmax probabilities, which are rounded to bf16 right after.
@@ -113,6 +124,33 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
     __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
     return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// Launch with programmatic stream serialisation (and a cluster of cluster_x
+// CTAs along x when cluster_x > 1).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       int cluster_x, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 // ---------------------------------------------------------------------------

@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(128) qprep_kernel(const __nv_bfloat16* __restr
                                                     const float* __restrict__ inv_freq, dsa_seqs s, int num_q,
                                                     T* __restrict__ qp, float* __restrict__ wp,
                                                     int32_t* d_status) {
+    pdl_enter();
     const int t = blockIdx.x;
     const bool rope = inv_freq != nullptr;
     const int KP = rope ? 192 : 128;
@@ -264,6 +265,7 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
                     const float* __restrict__ wp, const float* __restrict__ k_scale, dsa_seqs s,
                     float* __restrict__ scores, int64_t ld, int tiles_per_seq, int chunks, int64_t total_tiles,
                     int box_rows, int32_t* d_status) {
+    pdl_enter();
     using C = IdxCfg<NQ, KP, FP8>;
     constexpr int S = C::S, N = C::N;
     extern __shared__ uint8_t smem_raw[];
@@ -613,9 +615,8 @@ cudaError_t launch_tc(const void* qp, int num_q, const float* wp, const void* k_
     const int chunks = (s.max_q_per_seq + NQ - 1) / NQ;
     const int64_t total = (int64_t)s.num_seqs * chunks * tiles_per_seq;
     const int grid = (int)std::min<int64_t>((int64_t)C::ctas_per_sm * num_sms(), total);
-    kern<<<grid, C::threads, C::smem, stream>>>(kmap, qmap, wp, k_scale, s, scores, ld, tiles_per_seq, chunks, total,
-                                                box_rows, d_status);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(C::threads), C::smem, stream, 1, kmap, qmap, wp, k_scale, s, scores, ld,
+                      tiles_per_seq, chunks, total, box_rows, d_status);
 }
 
 template <int NQ>
@@ -637,15 +638,12 @@ cudaError_t launch_index_scores(const void* q_idx, const float* w, const float* 
                                 int32_t* d_status, cudaStream_t stream) {
     const bool fp8 = k_dtype == DSA_FP8_E4M3_ROWSCALE;
     const bool rope = inv_freq != nullptr;
-    if (fp8)
-        qprep_kernel<__half><<<num_q, 128, 0, stream>>>(
-            reinterpret_cast<const __nv_bfloat16*>(q_idx), w, ssmax_s, ssmax_b, inv_freq, s, num_q,
-            reinterpret_cast<__half*>(ws.qprep), ws.wprep, d_status);
-    else
-        qprep_kernel<__nv_bfloat16><<<num_q, 128, 0, stream>>>(
-            reinterpret_cast<const __nv_bfloat16*>(q_idx), w, ssmax_s, ssmax_b, inv_freq, s, num_q,
-            reinterpret_cast<__nv_bfloat16*>(ws.qprep), ws.wprep, d_status);
-    cudaError_t e = cudaGetLastError();
+    const __nv_bfloat16* qi = reinterpret_cast<const __nv_bfloat16*>(q_idx);
+    cudaError_t e =
+        fp8 ? launch_pdl(qprep_kernel<__half>, dim3(num_q), dim3(128), 0, stream, 1, qi, w, ssmax_s, ssmax_b, inv_freq,
+                         s, num_q, reinterpret_cast<__half*>(ws.qprep), ws.wprep, d_status)
+            : launch_pdl(qprep_kernel<__nv_bfloat16>, dim3(num_q), dim3(128), 0, stream, 1, qi, w, ssmax_s, ssmax_b,
+                         inv_freq, s, num_q, reinterpret_cast<__nv_bfloat16*>(ws.qprep), ws.wprep, d_status);
     if (e != cudaSuccess) return e;
     const int mq = s.max_q_per_seq;
     if (mq <= 1) return launch_tc_nq<1>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, d_status, stream);

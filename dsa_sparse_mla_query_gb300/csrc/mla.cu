@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
                const int32_t* __restrict__ idx, const int32_t* __restrict__ topk_len, int k, float scale_log2,
                int splits, __nv_bfloat16* __restrict__ out, float* __restrict__ lse, float* __restrict__ part_o,
                float* __restrict__ part_ml, int32_t* d_status) {
+    pdl_enter();
     extern __shared__ __align__(128) uint8_t smem[];
     uint16_t* sq = reinterpret_cast<uint16_t*>(smem);
     uint8_t* p = smem + MlaSmem::q;
@@ -394,6 +395,7 @@ constexpr int kCombineHeads = 4;
 __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restrict__ part_o,
                                                           const float* __restrict__ part_ml, int splits,
                                                           __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+    pdl_enter();
     __shared__ float wgt[kCombineHeads * 16];
     __shared__ float inv_l[kCombineHeads];
     const int t = blockIdx.x, h0 = blockIdx.y * kCombineHeads;
@@ -492,6 +494,7 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                   const int32_t* __restrict__ idx, const int32_t* __restrict__ topk_len, int k, float scale_log2,
                   int splits, int pair, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                   float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* d_status) {
+    pdl_enter();
     using namespace tcmla;
     extern __shared__ __align__(1024) uint8_t tc_smem[];   // 1024-aligned for the 128-byte swizzle atoms
     uint8_t* const smem = tc_smem;
@@ -1049,46 +1052,26 @@ cudaError_t launch_sparse_mla(const void* q, const void* latent, dsa_dtype laten
             if (e != cudaSuccess) return e;
             attr = true;
         }
-        if (splits == 2) {
-            // the two splits of a query run as a cluster and combine through
-            // distributed shared memory: no partials, no combine launch
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(2, num_q, 1);
-            cfg.blockDim = dim3(tcmla::kThreads, 1, 1);
-            cfg.dynamicSmemBytes = tcmla::kSmem;
-            cfg.stream = stream;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 2;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            return cudaLaunchKernelEx(&cfg, mla_tc_kernel, qmap, reinterpret_cast<const uint8_t*>(latent), s, idx,
-                                      topk_len, k, scale_log2, splits, 1, reinterpret_cast<__nv_bfloat16*>(out), lse,
-                                      ws.mla_part, ws.mla_ml, d_status);
-        }
-        mla_tc_kernel<<<dim3(splits, num_q), tcmla::kThreads, tcmla::kSmem, stream>>>(
-            qmap, reinterpret_cast<const uint8_t*>(latent), s, idx, topk_len, k, scale_log2, splits, 0,
-            reinterpret_cast<__nv_bfloat16*>(out), lse, ws.mla_part, ws.mla_ml, d_status);
-        e = cudaGetLastError();
-        if (e != cudaSuccess || splits == 1) return e;
-        mla_combine_kernel<<<dim3(num_q, kMH / kCombineHeads), 128, 0, stream>>>(
-            ws.mla_part, ws.mla_ml, splits, reinterpret_cast<__nv_bfloat16*>(out), lse);
-        return cudaGetLastError();
+        // with two splits, the pair runs as a cluster and combines through
+        // distributed shared memory: no partials, no combine launch
+        const int pair = splits == 2 ? 1 : 0;
+        e = launch_pdl(mla_tc_kernel, dim3(splits, num_q), dim3(tcmla::kThreads), tcmla::kSmem, stream, pair ? 2 : 1,
+                       qmap, reinterpret_cast<const uint8_t*>(latent), s, idx, topk_len, k, scale_log2, splits, pair,
+                       reinterpret_cast<__nv_bfloat16*>(out), lse, ws.mla_part, ws.mla_ml, d_status);
+        if (e != cudaSuccess || splits == 1 || pair) return e;
+        return launch_pdl(mla_combine_kernel, dim3(num_q, kMH / kCombineHeads), dim3(128), 0, stream, 1, ws.mla_part,
+                          ws.mla_ml, splits, reinterpret_cast<__nv_bfloat16*>(out), lse);
     }
     const size_t smem = MlaSmem::total(fp8);
     auto kern = fp8 ? mla_kernel<true> : mla_kernel<false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(splits, num_q), kMlaThreads, smem, stream>>>(
-        reinterpret_cast<const uint16_t*>(q), reinterpret_cast<const uint8_t*>(latent), s, idx, topk_len, k,
-        scale_log2, splits, reinterpret_cast<__nv_bfloat16*>(out), lse, ws.mla_part, ws.mla_ml, d_status);
-    e = cudaGetLastError();
+    e = launch_pdl(kern, dim3(splits, num_q), dim3(kMlaThreads), smem, stream, 1, reinterpret_cast<const uint16_t*>(q),
+                   reinterpret_cast<const uint8_t*>(latent), s, idx, topk_len, k, scale_log2, splits,
+                   reinterpret_cast<__nv_bfloat16*>(out), lse, ws.mla_part, ws.mla_ml, d_status);
     if (e != cudaSuccess || splits == 1) return e;
-    mla_combine_kernel<<<dim3(num_q, kMH / kCombineHeads), 128, 0, stream>>>(ws.mla_part, ws.mla_ml, splits,
-                                                   reinterpret_cast<__nv_bfloat16*>(out), lse);
-    return cudaGetLastError();
+    return launch_pdl(mla_combine_kernel, dim3(num_q, kMH / kCombineHeads), dim3(128), 0, stream, 1, ws.mla_part,
+                      ws.mla_ml, splits, reinterpret_cast<__nv_bfloat16*>(out), lse);
 }
 
 }  // namespace dsa

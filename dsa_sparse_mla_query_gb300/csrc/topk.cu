@@ -65,6 +65,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_buf, int* t
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ scores, int64_t ld, dsa_seqs s,
                                                              int k, int32_t* __restrict__ idx,
                                                              int32_t* __restrict__ topk_len, int32_t* d_status) {
+    pdl_enter();
     __shared__ int hist[256];
     __shared__ int scan_buf[64];
     __shared__ int sel_digit, sel_above;
@@ -202,6 +203,7 @@ template <int THREADS, int EPT>
 __global__ void __launch_bounds__(THREADS, 1) topk_row_kernel(const float* __restrict__ scores, int64_t ld,
                                                                 dsa_seqs s, int k, int32_t* __restrict__ idx,
                                                                 int32_t* __restrict__ topk_len, int32_t* d_status) {
+    pdl_enter();
     extern __shared__ __align__(16) int row_smem[];
     int* sub = row_smem;                                                   // [kRowSub][kRowBins]
     uint32_t* cand = reinterpret_cast<uint32_t*>(row_smem + kRowSub * kRowBins);  // [kRowCandCap]
@@ -412,6 +414,7 @@ template <int EPT>
 __global__ void __launch_bounds__(kCT, EPT <= 16 ? 2 : 1)
     topk_cluster_kernel(const float* __restrict__ scores, int64_t ld, dsa_seqs s, int k, int32_t* __restrict__ idx,
                         int32_t* __restrict__ topk_len, int32_t* d_status) {
+    pdl_enter();
     constexpr int kChunk = kCT * EPT;
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
@@ -631,19 +634,10 @@ int max_cluster() {
 template <int EPT>
 cudaError_t launch_cluster(int cl, const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int k,
                            int32_t* idx, int32_t* topk_len, int32_t* d_status, cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(cl, num_q, 1);
-    cfg.blockDim = dim3(kCT, 1, 1);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cl;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<EPT>, scores, ld, s, k, idx, topk_len, d_status);
+    return launch_pdl(topk_cluster_kernel<EPT>, dim3(cl, num_q), dim3(kCT), 0, stream, cl, scores, ld, s, k, idx,
+                      topk_len, d_status);
 }
+
 
 }  // namespace
 
@@ -657,8 +651,8 @@ cudaError_t launch_row(const float* scores, int64_t ld, const dsa_seqs& s, int n
                                     (int)kRowSmem);
     });
     if (attr != cudaSuccess) return attr;
-    topk_row_kernel<THREADS, EPT><<<num_q, THREADS, kRowSmem, stream>>>(scores, ld, s, k, idx, topk_len, d_status);
-    return cudaGetLastError();
+    return launch_pdl(topk_row_kernel<THREADS, EPT>, dim3(num_q), dim3(THREADS), kRowSmem, stream, 1, scores, ld, s, k,
+                      idx, topk_len, d_status);
 }
 
 cudaError_t launch_topk(const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int k, int32_t* idx,
@@ -680,8 +674,8 @@ cudaError_t launch_topk(const float* scores, int64_t ld, const dsa_seqs& s, int 
             return launch_cluster<64>(p.cl, scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
     }
     // rows longer than 16 x 32,768 keys: one CTA per row, passes over memory
-    topk_kernel<<<num_q, kTopkThreads, 0, stream>>>(scores, ld, s, k, idx, topk_len, d_status);
-    return cudaGetLastError();
+    return launch_pdl(topk_kernel, dim3(num_q), dim3(kTopkThreads), 0, stream, 1, scores, ld, s, k, idx, topk_len,
+                      d_status);
 }
 
 }  // namespace dsa
