@@ -360,6 +360,155 @@ __global__ void __launch_bounds__(THREADS, 1) topk_row_kernel(const float* __res
 }
 
 // ---------------------------------------------------------------------------
+// The same selection with the row in shared memory ([key e][thread t] so that
+// the threads of a warp touch consecutive words): loops stay rolled, so the
+// code is small (the register-resident version is instruction-fetch bound)
+// and nothing spills.  1024 threads, EPT keys each.
+template <int EPT>
+constexpr size_t smem_row_bytes() {
+    return (size_t)EPT * 1024 * 4 + (size_t)kRowSub * kRowBins * 4 + kRowCandCap * 4;
+}
+
+template <int EPT>
+__global__ void __launch_bounds__(1024, 1) topk_smem_kernel(const float* __restrict__ scores, int64_t ld, dsa_seqs s,
+                                                             int k, int32_t* __restrict__ idx,
+                                                             int32_t* __restrict__ topk_len, int32_t* d_status) {
+    constexpr int NT = 1024;
+    pdl_enter();
+    extern __shared__ __align__(16) int sm_smem[];
+    uint32_t* keys = reinterpret_cast<uint32_t*>(sm_smem);                    // [EPT][NT]
+    int* sub = sm_smem + EPT * NT;                                             // [kRowSub][kRowBins]
+    uint32_t* cand = reinterpret_cast<uint32_t*>(sub + kRowSub * kRowBins);   // [kRowCandCap]
+    __shared__ int scan_buf[64];
+    __shared__ int sel_digit, sel_above, ncand;
+    const int t = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int b = seq_of(s.q_start, s.num_seqs, t);
+    const int pos = __ldg(s.q_pos + t);
+    const int ctx = __ldg(s.ctx_len + b);
+    int32_t* out = idx + (int64_t)t * k;
+    if (pos < 0 || pos >= ctx || ctx > s.max_ctx || pos + 1 > NT * EPT) {
+        if (tid == 0) {
+            report(d_status, DSA_ERR_BAD_INPUT);
+            topk_len[t] = 0;
+        }
+        for (int i = tid; i < k; i += NT) out[i] = -1;
+        return;
+    }
+    const int n = pos + 1;
+    if (n <= k) {
+        for (int i = tid; i < k; i += NT) out[i] = i < n ? i : -1;
+        if (tid == 0) topk_len[t] = n;
+        return;
+    }
+    // ---- this thread's EPT consecutive keys into shared memory (all loads in flight first)
+    const float* row = scores + (int64_t)t * ld;
+    const int base = tid * EPT;
+    const int last4 = (int)((ld - 4) & ~(int64_t)3);
+    {
+        uint4 r[EPT / 4];
+#pragma unroll
+        for (int v = 0; v < EPT / 4; ++v) r[v] = __ldg(reinterpret_cast<const uint4*>(row + min(base + 4 * v, last4)));
+#pragma unroll
+        for (int v = 0; v < EPT / 4; ++v) {
+            keys[(4 * v + 0) * NT + tid] = order_key(__uint_as_float(r[v].x));
+            keys[(4 * v + 1) * NT + tid] = order_key(__uint_as_float(r[v].y));
+            keys[(4 * v + 2) * NT + tid] = order_key(__uint_as_float(r[v].z));
+            keys[(4 * v + 3) * NT + tid] = order_key(__uint_as_float(r[v].w));
+        }
+    }
+    const int nv = min(max(n - base, 0), EPT);  // this thread's keys inside the row
+    uint32_t prefix = 0, mask = 0;
+    int remaining = k;
+    bool use_cand = false;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int nb = pass == 2 ? 1024 : 2048;
+        const int copies = use_cand ? 1 : kRowSub;
+        for (int i = tid; i < copies * kRowBins; i += NT) sub[i] = 0;
+        __syncthreads();
+        if (use_cand) {
+            for (int i = tid; i < ncand; i += NT) {
+                const uint32_t c = cand[i];
+                if ((c & mask) == prefix) atomicAdd(sub + ((c >> shift) & (nb - 1)), 1);
+            }
+        } else {
+            int* h = sub + (warp % kRowSub) * kRowBins;
+#pragma unroll 4
+            for (int e = 0; e < nv; ++e) {
+                const uint32_t u = keys[e * NT + tid];
+                if ((u & mask) == prefix) atomicAdd(h + ((u >> shift) & (nb - 1)), 1);
+            }
+        }
+        __syncthreads();
+        // digits in descending order, 2 (or 1) per thread, summed over the copies
+        const int per = nb / NT;
+        int c0 = 0, c1 = 0;
+        {
+            const int d0 = nb - 1 - per * tid;
+            for (int cp = 0; cp < copies; ++cp) c0 += sub[cp * kRowBins + d0];
+            if (per == 2)
+                for (int cp = 0; cp < copies; ++cp) c1 += sub[cp * kRowBins + d0 - 1];
+        }
+        int tot;
+        const int before = scan_threads<NT>(c0 + c1, scan_buf, &tot);
+        if (before < remaining && before + c0 >= remaining) {
+            sel_digit = nb - 1 - per * tid;
+            sel_above = before;
+        } else if (per == 2 && before + c0 < remaining && before + c0 + c1 >= remaining) {
+            sel_digit = nb - 2 - per * tid;
+            sel_above = before + c0;
+        }
+        __syncthreads();
+        prefix |= (uint32_t)sel_digit << shift;
+        mask |= (uint32_t)(nb - 1) << shift;
+        remaining -= sel_above;
+        if (pass == 0) {
+            // keep the keys of the chosen bin for the next two passes (prefix-sum slots)
+            int mine = 0;
+            for (int e = 0; e < nv; ++e) mine += (keys[e * NT + tid] & mask) == prefix;
+            int nc;
+            int sl = scan_threads<NT>(mine, scan_buf, &nc);
+            if (nc <= kRowCandCap)
+                for (int e = 0; e < nv; ++e) {
+                    const uint32_t u = keys[e * NT + tid];
+                    if ((u & mask) == prefix) cand[sl++] = u;
+                }
+            if (tid == 0) ncand = nc;
+            __syncthreads();
+            use_cand = nc <= kRowCandCap;
+        } else {
+            __syncthreads();  // the next pass clears the histogram this one read
+        }
+    }
+    const uint32_t T = prefix;
+    const int need_eq = remaining;
+    // ---- ranks in index order: every key > T, the first need_eq keys == T
+    int n_gt = 0, n_eq = 0;
+    for (int e = 0; e < nv; ++e) {
+        const uint32_t u = keys[e * NT + tid];
+        n_gt += u > T;
+        n_eq += u == T;
+    }
+    int tot_eq;
+    int eq_rank = scan_threads<NT>(n_eq, scan_buf, &tot_eq);
+    const int n_sel = n_gt + max(0, min(need_eq - eq_rank, n_eq));
+    int tot_sel;
+    int o = scan_threads<NT>(n_sel, scan_buf, &tot_sel);
+    int* stage_out = reinterpret_cast<int*>(cand);  // k <= kRowCandCap
+    for (int e = 0; e < nv; ++e) {
+        const uint32_t u = keys[e * NT + tid];
+        bool take = u > T;
+        if (u == T) take = eq_rank++ < need_eq;
+        if (take && o < k) stage_out[o++] = base + e;
+    }
+    __syncthreads();
+    for (int i = tid; i < k; i += NT) out[i] = stage_out[i];
+    if (tid == 0) topk_len[t] = k;
+}
+
+// ---------------------------------------------------------------------------
 // Register-resident variant: a thread-block cluster of CL CTAs per query row,
 // each CTA holding 512 x EPT scores in registers, so the row is read from
 // memory exactly once.  Three digit passes (11 + 11 + 10 bits): each CTA
@@ -655,15 +804,29 @@ cudaError_t launch_row(const float* scores, int64_t ld, const dsa_seqs& s, int n
                       idx, topk_len, d_status);
 }
 
+template <int EPT>
+cudaError_t launch_smem_row(const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int k, int32_t* idx,
+                            int32_t* topk_len, int32_t* d_status, cudaStream_t stream) {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(topk_smem_kernel<EPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem_row_bytes<EPT>());
+    });
+    if (attr != cudaSuccess) return attr;
+    return launch_pdl(topk_smem_kernel<EPT>, dim3(num_q), dim3(1024), smem_row_bytes<EPT>(), stream, 1, scores, ld, s,
+                      k, idx, topk_len, d_status);
+}
+
 cudaError_t launch_topk(const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int k, int32_t* idx,
                         int32_t* topk_len, int32_t* d_status, cudaStream_t stream) {
-    // rows up to 32,768 keys: one CTA per row, held in registers
+    // rows up to 32,768 keys: one CTA per row
     if (s.max_ctx <= 1024 * 8)
         return launch_row<1024, 8>(scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
     if (s.max_ctx <= 1024 * 16)
         return launch_row<1024, 16>(scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
-    if (s.max_ctx <= 512 * 64)
-        return launch_row<512, 64>(scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
+    if (s.max_ctx <= 1024 * 32)
+        return launch_smem_row<32>(scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
     const ClusterPlan p = topk_plan(s.max_ctx, num_q);
     if (p.cl <= 16 && p.ept <= 64) {
         if (p.ept == 16 && p.cl <= max_cluster<16>())
