@@ -360,13 +360,16 @@ __global__ void __launch_bounds__(THREADS, 1) topk_row_kernel(const float* __res
 }
 
 // ---------------------------------------------------------------------------
-// The same selection with the row in shared memory ([key e][thread t] so that
-// the threads of a warp touch consecutive words): loops stay rolled, so the
+// The same selection with the row in shared memory: loops stay rolled, so the
 // code is small (the register-resident version is instruction-fetch bound)
-// and nothing spills.  1024 threads, EPT keys each.
+// and nothing spills.  1024 threads; thread t owns keys t*EPT .. t*EPT+EPT-1,
+// key i stored at (i mod 32) * 1025 + i / 32.  The row is read with coalesced
+// 16-byte loads (a warp reads 512 contiguous bytes); with the padded stride
+// both those stores and a thread's reads of its own keys are free of bank
+// conflicts.
 template <int EPT>
 constexpr size_t smem_row_bytes() {
-    return (size_t)EPT * 1024 * 4 + (size_t)kRowSub * kRowBins * 4 + kRowCandCap * 4;
+    return (size_t)32 * (EPT * 1024 / 32 + 1) * 4 + (size_t)kRowSub * kRowBins * 4 + kRowCandCap * 4;
 }
 
 template <int EPT>
@@ -376,8 +379,9 @@ __global__ void __launch_bounds__(1024, 1) topk_smem_kernel(const float* __restr
     constexpr int NT = 1024;
     pdl_enter();
     extern __shared__ __align__(16) int sm_smem[];
-    uint32_t* keys = reinterpret_cast<uint32_t*>(sm_smem);                    // [EPT][NT]
-    int* sub = sm_smem + EPT * NT;                                             // [kRowSub][kRowBins]
+    constexpr int KS = EPT * NT / 32 + 1;                                     // padded stride
+    uint32_t* keys = reinterpret_cast<uint32_t*>(sm_smem);                    // key i at (i % 32) * KS + i / 32
+    int* sub = sm_smem + 32 * KS;                                             // [kRowSub][kRowBins]
     uint32_t* cand = reinterpret_cast<uint32_t*>(sub + kRowSub * kRowBins);   // [kRowCandCap]
     __shared__ int scan_buf[64];
     __shared__ int sel_digit, sel_above, ncand;
@@ -401,22 +405,24 @@ __global__ void __launch_bounds__(1024, 1) topk_smem_kernel(const float* __restr
         if (tid == 0) topk_len[t] = n;
         return;
     }
-    // ---- this thread's EPT consecutive keys into shared memory (all loads in flight first)
+    // ---- the row into shared memory: coalesced loads, all in flight first
     const float* row = scores + (int64_t)t * ld;
-    const int base = tid * EPT;
     const int last4 = (int)((ld - 4) & ~(int64_t)3);
     {
         uint4 r[EPT / 4];
 #pragma unroll
-        for (int v = 0; v < EPT / 4; ++v) r[v] = __ldg(reinterpret_cast<const uint4*>(row + min(base + 4 * v, last4)));
+        for (int v = 0; v < EPT / 4; ++v)
+            r[v] = __ldg(reinterpret_cast<const uint4*>(row + min((v * NT + tid) * 4, last4)));
 #pragma unroll
         for (int v = 0; v < EPT / 4; ++v) {
-            keys[(4 * v + 0) * NT + tid] = order_key(__uint_as_float(r[v].x));
-            keys[(4 * v + 1) * NT + tid] = order_key(__uint_as_float(r[v].y));
-            keys[(4 * v + 2) * NT + tid] = order_key(__uint_as_float(r[v].z));
-            keys[(4 * v + 3) * NT + tid] = order_key(__uint_as_float(r[v].w));
+            const int i0 = (v * NT + tid) * 4;
+            const uint32_t w4[4] = {r[v].x, r[v].y, r[v].z, r[v].w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) keys[((i0 + c) & 31) * KS + ((i0 + c) >> 5)] = order_key(__uint_as_float(w4[c]));
         }
     }
+    __syncthreads();
+    const int base = tid * EPT;
     const int nv = min(max(n - base, 0), EPT);  // this thread's keys inside the row
     uint32_t prefix = 0, mask = 0;
     int remaining = k;
@@ -437,7 +443,7 @@ __global__ void __launch_bounds__(1024, 1) topk_smem_kernel(const float* __restr
             int* h = sub + (warp % kRowSub) * kRowBins;
 #pragma unroll 4
             for (int e = 0; e < nv; ++e) {
-                const uint32_t u = keys[e * NT + tid];
+                const uint32_t u = keys[e * KS + tid];
                 if ((u & mask) == prefix) atomicAdd(h + ((u >> shift) & (nb - 1)), 1);
             }
         }
@@ -467,12 +473,12 @@ __global__ void __launch_bounds__(1024, 1) topk_smem_kernel(const float* __restr
         if (pass == 0) {
             // keep the keys of the chosen bin for the next two passes (prefix-sum slots)
             int mine = 0;
-            for (int e = 0; e < nv; ++e) mine += (keys[e * NT + tid] & mask) == prefix;
+            for (int e = 0; e < nv; ++e) mine += (keys[e * KS + tid] & mask) == prefix;
             int nc;
             int sl = scan_threads<NT>(mine, scan_buf, &nc);
             if (nc <= kRowCandCap)
                 for (int e = 0; e < nv; ++e) {
-                    const uint32_t u = keys[e * NT + tid];
+                    const uint32_t u = keys[e * KS + tid];
                     if ((u & mask) == prefix) cand[sl++] = u;
                 }
             if (tid == 0) ncand = nc;
@@ -487,7 +493,7 @@ __global__ void __launch_bounds__(1024, 1) topk_smem_kernel(const float* __restr
     // ---- ranks in index order: every key > T, the first need_eq keys == T
     int n_gt = 0, n_eq = 0;
     for (int e = 0; e < nv; ++e) {
-        const uint32_t u = keys[e * NT + tid];
+        const uint32_t u = keys[e * KS + tid];
         n_gt += u > T;
         n_eq += u == T;
     }
@@ -498,7 +504,7 @@ __global__ void __launch_bounds__(1024, 1) topk_smem_kernel(const float* __restr
     int o = scan_threads<NT>(n_sel, scan_buf, &tot_sel);
     int* stage_out = reinterpret_cast<int*>(cand);  // k <= kRowCandCap
     for (int e = 0; e < nv; ++e) {
-        const uint32_t u = keys[e * NT + tid];
+        const uint32_t u = keys[e * KS + tid];
         bool take = u > T;
         if (u == T) take = eq_rank++ < need_eq;
         if (take && o < k) stage_out[o++] = base + e;
