@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(1024, 1) topk_smem_kernel(const float* __restr
             }
         } else {
             int* h = sub + (warp % kRowSub) * kRowBins;
-#pragma unroll 4
+#pragma unroll 8
             for (int e = 0; e < nv; ++e) {
                 const uint32_t u = keys[e * KS + tid];
                 if ((u & mask) == prefix) atomicAdd(h + ((u >> shift) & (nb - 1)), 1);
@@ -473,10 +473,12 @@ __global__ void __launch_bounds__(1024, 1) topk_smem_kernel(const float* __restr
         if (pass == 0) {
             // keep the keys of the chosen bin for the next two passes (prefix-sum slots)
             int mine = 0;
+#pragma unroll 8
             for (int e = 0; e < nv; ++e) mine += (keys[e * KS + tid] & mask) == prefix;
             int nc;
             int sl = scan_threads<NT>(mine, scan_buf, &nc);
             if (nc <= kRowCandCap)
+#pragma unroll 8
                 for (int e = 0; e < nv; ++e) {
                     const uint32_t u = keys[e * KS + tid];
                     if ((u & mask) == prefix) cand[sl++] = u;
@@ -492,6 +494,7 @@ __global__ void __launch_bounds__(1024, 1) topk_smem_kernel(const float* __restr
     const int need_eq = remaining;
     // ---- ranks in index order: every key > T, the first need_eq keys == T
     int n_gt = 0, n_eq = 0;
+#pragma unroll 8
     for (int e = 0; e < nv; ++e) {
         const uint32_t u = keys[e * KS + tid];
         n_gt += u > T;
@@ -503,6 +506,7 @@ __global__ void __launch_bounds__(1024, 1) topk_smem_kernel(const float* __restr
     int tot_sel;
     int o = scan_threads<NT>(n_sel, scan_buf, &tot_sel);
     int* stage_out = reinterpret_cast<int*>(cand);  // k <= kRowCandCap
+#pragma unroll 8
     for (int e = 0; e < nv; ++e) {
         const uint32_t u = keys[e * KS + tid];
         bool take = u > T;
