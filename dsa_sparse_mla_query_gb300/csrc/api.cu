@@ -283,8 +283,8 @@ int32_t dsa_decode_layer_launches(const dsa_seqs* seqs, int32_t num_q, int32_t k
            (int)latent_dtype);
     if (c.done() != DSA_OK || num_q == 0) return 0;
     const int splits = mla_splits(num_q, k);
-    // attention, plus the LSE combine unless the splits combine in-kernel (bf16, two splits)
-    const int mla = (splits == 1 || (latent_dtype == DSA_BF16 && splits == 2)) ? 1 : 2;
+    // attention, plus the LSE combine unless the splits combine in-kernel (two splits)
+    const int mla = splits <= 2 ? 1 : 2;
     return (reuse_idx ? 0 : 3) + mla;  // query prep, scores, top-k
 }
 

@@ -10,15 +10,11 @@
 // For query t and head h over the selected rows c_j (576 dims):
 //   s_j = sm_scale q_h . c_j,  out_h = sum_j softmax(s)_j c_j[0:512],
 //   lse_h = ln sum_j exp(s_j).
-// One CTA takes one query and one split of its selected slots; all 64 heads
-// are the M rows of the tensor-core tiles.  Rows are gathered through the page
-// table with 16-byte async copies into a double-buffered shared tile; the
-// softmax runs online in base 2 (max, sum, rescale) and the value product
-// reuses the gathered tile (V = latent dims 0..511).  Splits write unnormalised
-// partial outputs with their (max, sum), merged by an LSE combine.
-// fp8_ds_mla rows are dequantised in-kernel: e4m3 codes decode exactly to
-// bf16, the four per-group scales multiply the per-group partial scores and
-// fold into the probabilities of the value product.
+// One CTA takes one query and one split of its selected slots; the kernel is
+// described above mla_tc_kernel.  Splits combine in-kernel when there are two
+// (a thread-block cluster), else they write unnormalised partial outputs with
+// their (max, sum), merged by the LSE combine kernel.  fp8_ds_mla rows are
+// dequantised by the gather (code x group scale, one rounding to f16).
 #include <cooperative_groups.h>
 #include <cudaTypedefs.h>
 
@@ -28,21 +24,6 @@
 
 namespace dsa {
 
-constexpr int kBN = 32;              // selected rows per tile
-constexpr int kRS = kMD + 8;         // smem row stride, 16-bit elements
-constexpr int kMlaThreads = 256;
-constexpr int kSS = kBN + 4;         // score tile row stride (floats)
-
-struct MlaSmem {
-    static constexpr size_t q = (size_t)kMH * kRS * 2;
-    static constexpr size_t tile = (size_t)kBN * kRS * 2;
-    static constexpr size_t raw = (size_t)kBN * kDsRow;
-    static constexpr size_t s = (size_t)kMH * kSS * 4;
-    static size_t total(bool fp8) {
-        return q + (fp8 ? tile + 2 * raw : 2 * tile) + s + 2 * kBN * 8 + 2 * kBN * 4 * 4 + 64;
-    }
-};
-
 int mla_splits(int num_q, int k) {
     // one resident CTA per SM: as many splits as fill one wave of 152 SMs
     const int tiles = (k + 63) / 64;
@@ -51,341 +32,6 @@ int mla_splits(int num_q, int k) {
     int max_sp = tiles / 2 > 0 ? tiles / 2 : 1;  // at least two 64-row tiles per split
     if (max_sp > 16) max_sp = 16;                  // the combine holds 16 weights per head
     return sp > max_sp ? max_sp : sp;
-}
-
-template <bool FP8>
-__global__ void __launch_bounds__(kMlaThreads, 1)
-    mla_kernel(const uint16_t* __restrict__ q, const uint8_t* __restrict__ latent, dsa_seqs s,
-               const int32_t* __restrict__ idx, const int32_t* __restrict__ topk_len, int k, float scale_log2,
-               int splits, __nv_bfloat16* __restrict__ out, float* __restrict__ lse, float* __restrict__ part_o,
-               float* __restrict__ part_ml, int32_t* d_status) {
-    pdl_enter();
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint16_t* sq = reinterpret_cast<uint16_t*>(smem);
-    uint8_t* p = smem + MlaSmem::q;
-    uint16_t* stile[2];
-    uint8_t* sraw[2] = {nullptr, nullptr};
-    if (FP8) {
-        stile[0] = stile[1] = reinterpret_cast<uint16_t*>(p);
-        p += MlaSmem::tile;
-        sraw[0] = p;
-        sraw[1] = p + MlaSmem::raw;
-        p += 2 * MlaSmem::raw;
-    } else {
-        stile[0] = reinterpret_cast<uint16_t*>(p);
-        stile[1] = reinterpret_cast<uint16_t*>(p + MlaSmem::tile);
-        p += 2 * MlaSmem::tile;
-    }
-    float* sS = reinterpret_cast<float*>(p);
-    p += MlaSmem::s;
-    int64_t* srow = reinterpret_cast<int64_t*>(p);          // [2][kBN] physical rows (-1 = empty)
-    float* sscale = reinterpret_cast<float*>(p + 2 * kBN * 8);  // [2][kBN][4]
-
-    const int t = blockIdx.y, sp = blockIdx.x;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = seq_of(s.q_start, s.num_seqs, t);
-    const int ctx = __ldg(s.ctx_len + b);
-    int len = __ldg(topk_len + t);
-    if (len < 0 || len > k || ctx > s.max_ctx) {
-        if (tid == 0 && sp == 0) report(d_status, DSA_ERR_BAD_INPUT);
-        len = 0;
-    }
-    const int per = ((k + splits - 1) / splits + kBN - 1) / kBN * kBN;
-    const int slot0 = sp * per;
-    const int slot1 = min(slot0 + per, len);
-    const int ntiles = slot1 > slot0 ? (slot1 - slot0 + kBN - 1) / kBN : 0;
-    const int32_t* tidx = idx + (int64_t)t * k;
-
-    // ---- stage all 64 query heads
-    const uint16_t* qt = q + (int64_t)t * kMH * kMD;
-    for (int e = tid; e < kMH * (kMD / 8); e += kMlaThreads) {
-        const int r = e / (kMD / 8), c = e % (kMD / 8);
-        cp_async16(sq + r * kRS + c * 8, qt + r * kMD + c * 8, true);
-    }
-
-    auto resolve_rows = [&](int tile, int buf) {
-        if (tid < kBN) {
-            const int slot = slot0 + tile * kBN + tid;
-            int64_t row = -1;
-            if (slot < slot1) {
-                const int j = __ldg(tidx + slot);
-                if (j >= ctx || j < -1) {
-                    report(d_status, DSA_ERR_BAD_INPUT);
-                } else if (j >= 0) {
-                    row = phys_row(s, b, j);
-                    if (row < 0) report(d_status, DSA_ERR_BAD_INPUT);
-                }
-            }
-            srow[buf * kBN + tid] = row;
-        }
-    };
-    auto issue_tile = [&](int buf) {
-        if (!FP8) {
-            const uint16_t* lat = reinterpret_cast<const uint16_t*>(latent);
-            for (int e = tid; e < kBN * (kMD / 8); e += kMlaThreads) {
-                const int r = e / (kMD / 8), c = e % (kMD / 8);
-                const int64_t row = srow[buf * kBN + r];
-                cp_async16(stile[buf] + r * kRS + c * 8, lat + (row < 0 ? 0 : row) * kMD + c * 8, row >= 0);
-            }
-        } else {
-            for (int e = tid; e < kBN * (kDsRow / 16); e += kMlaThreads) {
-                const int r = e / (kDsRow / 16), c = e % (kDsRow / 16);
-                const int64_t row = srow[buf * kBN + r];
-                cp_async16(sraw[buf] + r * kDsRow + c * 16, latent + (row < 0 ? 0 : row) * kDsRow + c * 16,
-                           row >= 0);
-            }
-        }
-        cp_async_commit();
-    };
-
-    if (ntiles > 0) {
-        resolve_rows(0, 0);
-        __syncthreads();
-        issue_tile(0);
-    } else {
-        cp_async_commit();
-    }
-
-    // ---- per-warp roles
-    const int mt = warp & 3;       // heads 16mt .. 16mt+15
-    const int nh = warp >> 2;      // score phase: keys 16nh .. 16nh+15 of the tile
-    const int dh = warp >> 2;      // value phase: dims 256dh .. 256dh+255
-    const int g = lane >> 2, c4 = lane & 3;
-    const int bl = lane & 7, bm = lane >> 3;
-    float acc_o[32][4];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) acc_o[i][0] = acc_o[i][1] = acc_o[i][2] = acc_o[i][3] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-
-    for (int tile = 0; tile < ntiles; ++tile) {
-        const int buf = tile & 1;
-        if (tile + 1 < ntiles) {
-            resolve_rows(tile + 1, buf ^ 1);
-            __syncthreads();
-            issue_tile(buf ^ 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-        uint16_t* kt = stile[buf];
-        if (FP8) {
-            // dequantise codes to bf16 (exact), copy RoPE dims, unpack scales
-            const uint8_t* raw = sraw[buf];
-            for (int e = tid; e < kBN * (kMV / 8); e += kMlaThreads) {
-                const int r = e / (kMV / 8), c = e % (kMV / 8);
-                uint2 v = *reinterpret_cast<const uint2*>(raw + r * kDsRow + c * 8);
-                uint32_t w4[4] = {v.x & 0xFFFF, v.x >> 16, v.y & 0xFFFF, v.y >> 16};
-                uint32_t o[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)w4[i], __NV_E4M3);
-                    float2 f = __half22float2(*reinterpret_cast<__half2*>(&hr));
-                    o[i] = pack_bf16(f.x, f.y);
-                }
-                *reinterpret_cast<uint4*>(kt + r * kRS + c * 8) = make_uint4(o[0], o[1], o[2], o[3]);
-            }
-            for (int e = tid; e < kBN * 8; e += kMlaThreads) {
-                const int r = e >> 3, c = e & 7;
-                *reinterpret_cast<uint4*>(kt + r * kRS + kMV + c * 8) =
-                    *reinterpret_cast<const uint4*>(raw + r * kDsRow + kMV + 16 + c * 16);
-            }
-            if (tid < kBN * 4) {
-                const int r = tid >> 2, gi = tid & 3;
-                float v;
-                memcpy(&v, raw + r * kDsRow + kMV + gi * 4, 4);
-                sscale[buf * kBN * 4 + tid] = srow[buf * kBN + r] >= 0 ? v : 0.f;
-            }
-            __syncthreads();
-        }
-
-        // ---- scores S = Q K^T for heads 16mt.., keys 16nh..
-        float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        {
-            const uint16_t* arow = sq + (mt * 16 + (lane & 15)) * kRS + (lane >> 4) * 8;
-            const uint16_t* brow = kt + (nh * 16 + (bm >> 1) * 8 + bl) * kRS + (bm & 1) * 8;
-            if (!FP8) {
-#pragma unroll 4
-                for (int ks = 0; ks < kMD / 16; ++ks) {
-                    uint32_t a[4], b0, b1, b2, b3;
-                    ldsm_x4(a[0], a[1], a[2], a[3], arow + ks * 16);
-                    ldsm_x4(b0, b1, b2, b3, brow + ks * 16);
-                    mma_bf16(sacc[0], a, b0, b1);
-                    mma_bf16(sacc[1], a, b2, b3);
-                }
-            } else {
-                const float* sc = sscale + buf * kBN * 4;
-#pragma unroll 1
-                for (int grp = 0; grp < 5; ++grp) {
-                    float gacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                    const int k0 = grp * 8, k1 = grp < 4 ? k0 + 8 : kMD / 16;
-                    for (int ks = k0; ks < k1; ++ks) {
-                        uint32_t a[4], b0, b1, b2, b3;
-                        ldsm_x4(a[0], a[1], a[2], a[3], arow + ks * 16);
-                        ldsm_x4(b0, b1, b2, b3, brow + ks * 16);
-                        mma_bf16(gacc[0], a, b0, b1);
-                        mma_bf16(gacc[1], a, b2, b3);
-                    }
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const int key = nh * 16 + nt * 8 + 2 * c4;
-                        const float s0 = grp < 4 ? sc[key * 4 + grp] : 1.f;
-                        const float s1 = grp < 4 ? sc[(key + 1) * 4 + grp] : 1.f;
-                        sacc[nt][0] += s0 * gacc[nt][0];
-                        sacc[nt][1] += s1 * gacc[nt][1];
-                        sacc[nt][2] += s0 * gacc[nt][2];
-                        sacc[nt][3] += s1 * gacc[nt][3];
-                    }
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int key = nh * 16 + nt * 8 + 2 * c4;
-                const bool v0 = srow[buf * kBN + key] >= 0, v1 = srow[buf * kBN + key + 1] >= 0;
-                const int r0 = mt * 16 + g;
-                sS[r0 * kSS + key] = v0 ? sacc[nt][0] * scale_log2 : -INFINITY;
-                sS[r0 * kSS + key + 1] = v1 ? sacc[nt][1] * scale_log2 : -INFINITY;
-                sS[(r0 + 8) * kSS + key] = v0 ? sacc[nt][2] * scale_log2 : -INFINITY;
-                sS[(r0 + 8) * kSS + key + 1] = v1 ? sacc[nt][3] * scale_log2 : -INFINITY;
-            }
-        }
-        __syncthreads();
-
-        // ---- online softmax for rows r0 = 16mt+g and r1 = r0+8 over the 32 keys
-        float pr[2][8];
-        {
-            const int r0 = mt * 16 + g;
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const float* srw = sS + (r0 + 8 * hr) * kSS;
-                float mx = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int key = (i >> 1) * 8 + 2 * c4 + (i & 1);
-                    pr[hr][i] = srw[key];
-                    mx = fmaxf(mx, pr[hr][i]);
-                }
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const float m_new = fmaxf(m_run[hr], mx);
-                float alpha, sum = 0.f;
-                if (m_new == -INFINITY) {
-                    alpha = 1.f;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) pr[hr][i] = 0.f;
-                } else {
-                    alpha = fast_exp2(m_run[hr] - m_new);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        pr[hr][i] = fast_exp2(pr[hr][i] - m_new);
-                        sum += pr[hr][i];
-                    }
-                }
-                m_run[hr] = m_new;
-                l_run[hr] = l_run[hr] * alpha + sum;
-#pragma unroll
-                for (int nt = 0; nt < 32; ++nt) {
-                    acc_o[nt][2 * hr] *= alpha;
-                    acc_o[nt][2 * hr + 1] *= alpha;
-                }
-            }
-        }
-
-        // ---- O += P V over dims 256dh .. 256dh+255
-        {
-            const uint16_t* vbase = kt + ((bm & 1) * 8 + bl) * kRS + dh * 256 + (bm >> 1) * 8;
-            if (!FP8) {
-                uint32_t pa[2][4];
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    pa[kk][0] = pack_bf16(pr[0][4 * kk + 0], pr[0][4 * kk + 1]);
-                    pa[kk][1] = pack_bf16(pr[1][4 * kk + 0], pr[1][4 * kk + 1]);
-                    pa[kk][2] = pack_bf16(pr[0][4 * kk + 2], pr[0][4 * kk + 3]);
-                    pa[kk][3] = pack_bf16(pr[1][4 * kk + 2], pr[1][4 * kk + 3]);
-                }
-#pragma unroll
-                for (int nt = 0; nt < 32; nt += 2) {
-#pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4_t(b0, b1, b2, b3, vbase + kk * 16 * kRS + nt * 8);
-                        mma_bf16(acc_o[nt], pa[kk], b0, b1);
-                        mma_bf16(acc_o[nt + 1], pa[kk], b2, b3);
-                    }
-                }
-            } else {
-                const float* sc = sscale + buf * kBN * 4;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int grp = dh * 2 + half;  // 128-dim scale group
-                    uint32_t pa[2][4];
-#pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        const int ka = kk * 16 + 2 * c4;
-                        const float sa0 = sc[ka * 4 + grp], sa1 = sc[(ka + 1) * 4 + grp];
-                        const float sb0 = sc[(ka + 8) * 4 + grp], sb1 = sc[(ka + 9) * 4 + grp];
-                        pa[kk][0] = pack_bf16(pr[0][4 * kk + 0] * sa0, pr[0][4 * kk + 1] * sa1);
-                        pa[kk][1] = pack_bf16(pr[1][4 * kk + 0] * sa0, pr[1][4 * kk + 1] * sa1);
-                        pa[kk][2] = pack_bf16(pr[0][4 * kk + 2] * sb0, pr[0][4 * kk + 3] * sb1);
-                        pa[kk][3] = pack_bf16(pr[1][4 * kk + 2] * sb0, pr[1][4 * kk + 3] * sb1);
-                    }
-#pragma unroll
-                    for (int nt = half * 16; nt < half * 16 + 16; nt += 2) {
-#pragma unroll
-                        for (int kk = 0; kk < 2; ++kk) {
-                            uint32_t b0, b1, b2, b3;
-                            ldsm_x4_t(b0, b1, b2, b3, vbase + kk * 16 * kRS + nt * 8);
-                            mma_bf16(acc_o[nt], pa[kk], b0, b1);
-                            mma_bf16(acc_o[nt + 1], pa[kk], b2, b3);
-                        }
-                    }
-                }
-            }
-        }
-        __syncthreads();  // tile buffer and score tile are reused
-    }
-
-    cp_async_wait<0>();
-    // ---- finish: reduce the row sums over the 4 lanes of a quad
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-        l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 1);
-        l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 2);
-    }
-    const int r0 = mt * 16 + g;
-    if (splits == 1) {
-        __nv_bfloat16* ot = out + (int64_t)t * kMH * kMV;
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-            const int h = r0 + 8 * hr;
-            const float inv = l_run[hr] > 0.f ? 1.f / l_run[hr] : 0.f;
-#pragma unroll
-            for (int nt = 0; nt < 32; ++nt) {
-                const int d = dh * 256 + nt * 8 + 2 * c4;
-                *reinterpret_cast<uint32_t*>(ot + h * kMV + d) =
-                    pack_bf16(acc_o[nt][2 * hr] * inv, acc_o[nt][2 * hr + 1] * inv);
-            }
-            if (lse && dh == 0 && c4 == 0)
-                lse[(int64_t)t * kMH + h] =
-                    l_run[hr] > 0.f ? (m_run[hr] + log2f(l_run[hr])) * 0.69314718055994531f : -INFINITY;
-        }
-    } else {
-        float* po = part_o + ((int64_t)t * splits + sp) * kMH * kMV;
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-            const int h = r0 + 8 * hr;
-#pragma unroll
-            for (int nt = 0; nt < 32; ++nt) {
-                const int d = dh * 256 + nt * 8 + 2 * c4;
-                *reinterpret_cast<float2*>(po + h * kMV + d) = make_float2(acc_o[nt][2 * hr], acc_o[nt][2 * hr + 1]);
-            }
-            if (dh == 0 && c4 == 0) {
-                float* ml = part_ml + (((int64_t)t * splits + sp) * kMH + h) * 2;
-                ml[0] = m_run[hr];
-                ml[1] = l_run[hr];
-            }
-        }
-    }
 }
 
 // LSE combine of the splits of one query ([vLLM-ML4] DCP: LSE combine):
@@ -447,8 +93,50 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
     return r;
 }
 
+__device__ __forceinline__ uint2 ldg_stream8(const void* p) {
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 8 e4m3 codes x their group scale -> 8 f16 (one rounding, from fp32); sets
+// `over` when a value leaves the f16 range
+__device__ __forceinline__ uint4 dequant8_f16(uint2 codes, float scale, bool& over) {
+    const uint32_t w[4] = {codes.x & 0xFFFFu, codes.x >> 16, codes.y & 0xFFFFu, codes.y >> 16};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)w[i]);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+        const float a = f.x * scale, b = f.y * scale;
+        over |= fabsf(a) >= 65520.f || fabsf(b) >= 65520.f;
+        o[i] = pack_f16(a, b);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// 8 bf16 -> 8 f16 (exact inside the f16 range)
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, bool& over) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float a = __uint_as_float(w[i] << 16), b = __uint_as_float(w[i] & 0xFFFF0000u);
+        over |= fabsf(a) >= 65520.f || fabsf(b) >= 65520.f;
+        o[i] = pack_f16(a, b);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // ---------------------------------------------------------------------------
-// bf16 latent cache on the 5th-generation tensor cores.
+// Latent cache on the 5th-generation tensor cores: bf16 rows, or fp8_ds_mla
+// rows dequantised to f16 by the gather (the query is then converted to f16
+// in shared memory, exact inside the f16 range, and the products run in f16).
 //
 // One CTA = one query x one split of its selected slots, tiles of 64 rows:
 //   warp 0      loads the 64 query heads (TMA) and resolves each tile's slots
@@ -489,6 +177,7 @@ constexpr int kRing = 3;                   // resolved-row ring depth
 static_assert(kKBlock == TK * kMH * 2, "P^T must fit the rope block of its tile");
 }  // namespace tcmla
 
+template <bool FP8>
 __global__ void __launch_bounds__(tcmla::kThreads, 1)
     mla_tc_kernel(const __grid_constant__ CUtensorMap qmap, const uint8_t* __restrict__ latent, dsa_seqs s,
                   const int32_t* __restrict__ idx, const int32_t* __restrict__ topk_len, int k, float scale_log2,
@@ -517,6 +206,7 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
     uint64_t* rfull = bars + 19;  // [3] rows of a tile resolved
     uint64_t* rfree = bars + 22;  // [3] rows of a tile no longer read (gather + softmax warps)
     uint64_t* xmax = bars + 25;   // per-head maxima of the softmax warps written (first tile, growth)
+    uint64_t* qconv = bars + 26;  // fp8 cache: the query converted to f16 (softmax warps)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
     int* srow = reinterpret_cast<int*>(misc + 512);          // [3][TK] physical row (-1 = masked)
@@ -560,6 +250,7 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
         ptx::mbar_init(ofull, 1);
         ptx::mbar_init(lready, kSoftWarps);
         ptx::mbar_init(xmax, kSoftWarps);
+        ptx::mbar_init(qconv, kSoftWarps);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -609,10 +300,10 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && ntiles > 0) {
-            constexpr uint32_t idesc_s = ptx::idesc_f16(64, kMH, true);
-            constexpr uint32_t idesc_pv = ptx::idesc_f16(128, kMH, true, true, true);
+            constexpr uint32_t idesc_s = ptx::idesc_f16(64, kMH, !FP8);
+            constexpr uint32_t idesc_pv = ptx::idesc_f16(128, kMH, !FP8, true, true);
             const uint32_t qb = smem_u32(qs);
-            bool ok = ptx::mbar_wait(qfull, 0, abort_flag, d_status);
+            bool ok = ptx::mbar_wait(FP8 ? qconv : qfull, 0, abort_flag, d_status);
             auto issue_pv = [&](int i) -> bool {  // O^T += V^T P^T for tile i
                 if (!ptx::mbar_wait(pfull, i & 1, abort_flag, d_status)) return false;
                 ptx::tc_fence_after();
@@ -708,13 +399,37 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
         for (int i = 0; i < ntiles; ++i) {
             const int st = i & 1, r = i % kRing;
             if (!__all_sync(0xffffffffu, ptx::mbar_wait(rfull + r, (i / kRing) & 1, abort_flag, d_status))) break;
-            const uint4* g0 = reinterpret_cast<const uint4*>(latent + (size_t)max(srow[r * TK + r0], 0) * (kMD * 2)) + c8;
-            const uint4* g1 = reinterpret_cast<const uint4*>(latent + (size_t)max(srow[r * TK + r0 + 32], 0) * (kMD * 2)) + c8;
-            uint4 v[18];  // v[2 kb + h]: block kb of row r0 + 32 h
+            uint4 v[18];  // v[2 kb + h]: block kb of row r0 + 32 h, 16-bit values as stored in the stage
+            if constexpr (FP8) {
+                // fp8_ds_mla row: [0,512) e4m3 codes, [512,528) four fp32 scales
+                // (one per 128 dims), [528,656) 64 bf16 rope dims.  Thread (c8, r0):
+                // codes 8 c8 .. 8 c8 + 7 of every 64-dim block of rows r0, r0 + 32.
+                const uint8_t* b0 = latent + (size_t)max(srow[r * TK + r0], 0) * kDsRow;
+                const uint8_t* b1 = latent + (size_t)max(srow[r * TK + r0 + 32], 0) * kDsRow;
+                uint2 cv[16];
 #pragma unroll
-            for (int u = 0; u < 18; ++u) v[u] = ldg_stream(((u & 1) ? g1 : g0) + (u >> 1) * 8);
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(rfree + r);
+                for (int u = 0; u < 16; ++u) cv[u] = ldg_stream8(((u & 1) ? b1 : b0) + (u >> 1) * 64 + c8 * 8);
+                const float4 sc0 = __ldg(reinterpret_cast<const float4*>(b0 + kMV));
+                const float4 sc1 = __ldg(reinterpret_cast<const float4*>(b1 + kMV));
+                const uint4 rp0 = ldg_stream(reinterpret_cast<const uint4*>(b0 + kMV + 16) + c8);
+                const uint4 rp1 = ldg_stream(reinterpret_cast<const uint4*>(b1 + kMV + 16) + c8);
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(rfree + r);
+                bool over = false;
+                const float s0[4] = {sc0.x, sc0.y, sc0.z, sc0.w}, s1[4] = {sc1.x, sc1.y, sc1.z, sc1.w};
+#pragma unroll
+                for (int u = 0; u < 16; ++u) v[u] = dequant8_f16(cv[u], (u & 1) ? s1[u >> 2] : s0[u >> 2], over);
+                v[16] = bf16x8_to_f16x8(rp0, over);
+                v[17] = bf16x8_to_f16x8(rp1, over);
+                if (over) report(d_status, DSA_ERR_UNSUPPORTED);
+            } else {
+                const uint4* g0 = reinterpret_cast<const uint4*>(latent + (size_t)max(srow[r * TK + r0], 0) * (kMD * 2)) + c8;
+                const uint4* g1 = reinterpret_cast<const uint4*>(latent + (size_t)max(srow[r * TK + r0 + 32], 0) * (kMD * 2)) + c8;
+#pragma unroll
+                for (int u = 0; u < 18; ++u) v[u] = ldg_stream(((u & 1) ? g1 : g0) + (u >> 1) * 8);
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(rfree + r);
+            }
             uint8_t* dst = stage + st * kStage + soff;
             bool ok = true;
 #pragma unroll
@@ -743,6 +458,21 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
         const int key = quarter * 16 + (lane & 15);         // key row of the tile
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's TMEM lanes
         float* my_mu = mu + sw * 32;                        // running max of heads hb .. hb+31
+        if constexpr (FP8) {
+            // the query to f16 in place (its 16-bit elements keep their positions)
+            if (ntiles > 0) {
+                const bool got = __all_sync(0xffffffffu, ptx::mbar_wait(qfull, 0, abort_flag, d_status));
+                bool over = false;
+                if (got) {
+                    uint4* q4 = reinterpret_cast<uint4*>(qs);
+                    for (int e = sw * 32 + lane; e < kQBytes / 16; e += kSoftWarps * 32) q4[e] = bf16x8_to_f16x8(q4[e], over);
+                }
+                if (over) report(d_status, DSA_ERR_UNSUPPORTED);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(qconv);
+            }
+        }
         my_mu[lane] = -INFINITY;
         {
             float z[32];
@@ -853,8 +583,8 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                         p[e] = (!valid || mq[e] == -INFINITY) ? 0.f : fast_exp2(sv[4 * q + e] * scale_log2 - mq[e]);
                         lv[4 * q + e] += p[e];
                     }
-                    pk[2 * q] = pack_bf16(p[0], p[1]);
-                    pk[2 * q + 1] = pack_bf16(p[2], p[3]);
+                    pk[2 * q] = FP8 ? pack_f16(p[0], p[1]) : pack_bf16(p[0], p[1]);
+                    pk[2 * q + 1] = FP8 ? pack_f16(p[2], p[3]) : pack_bf16(p[2], p[3]);
                 }
                 ptx::tmem_st16(tl + kLCol + hb + g * 16, lv);
                 if (mine) {
@@ -1042,34 +772,26 @@ cudaError_t launch_sparse_mla(const void* q, const void* latent, dsa_dtype laten
     const bool fp8 = latent_dtype == DSA_FP8_DS_MLA;
     const int splits = mla_splits(num_q, k);
     const float scale_log2 = sm_scale * 1.4426950408889634f;
-    cudaError_t e;
-    if (!fp8) {
-        CUtensorMap qmap;
-        if ((e = bf16_map(&qmap, q, (uint64_t)num_q * kMH, 64)) != cudaSuccess) return e;
-        static bool attr = false;
-        if (!attr) {
-            e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcmla::kSmem);
-            if (e != cudaSuccess) return e;
-            attr = true;
-        }
-        // with two splits, the pair runs as a cluster and combines through
-        // distributed shared memory: no partials, no combine launch
-        const int pair = splits == 2 ? 1 : 0;
-        e = launch_pdl(mla_tc_kernel, dim3(splits, num_q), dim3(tcmla::kThreads), tcmla::kSmem, stream, pair ? 2 : 1,
-                       qmap, reinterpret_cast<const uint8_t*>(latent), s, idx, topk_len, k, scale_log2, splits, pair,
-                       reinterpret_cast<__nv_bfloat16*>(out), lse, ws.mla_part, ws.mla_ml, d_status);
-        if (e != cudaSuccess || splits == 1 || pair) return e;
-        return launch_pdl(mla_combine_kernel, dim3(num_q, kMH / kCombineHeads), dim3(128), 0, stream, 1, ws.mla_part,
-                          ws.mla_ml, splits, reinterpret_cast<__nv_bfloat16*>(out), lse);
-    }
-    const size_t smem = MlaSmem::total(fp8);
-    auto kern = fp8 ? mla_kernel<true> : mla_kernel<false>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    CUtensorMap qmap;
+    cudaError_t e = bf16_map(&qmap, q, (uint64_t)num_q * kMH, 64);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(kern, dim3(splits, num_q), dim3(kMlaThreads), smem, stream, 1, reinterpret_cast<const uint16_t*>(q),
-                   reinterpret_cast<const uint8_t*>(latent), s, idx, topk_len, k, scale_log2, splits,
-                   reinterpret_cast<__nv_bfloat16*>(out), lse, ws.mla_part, ws.mla_ml, d_status);
-    if (e != cudaSuccess || splits == 1) return e;
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(mla_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcmla::kSmem);
+        if (attr == cudaSuccess)
+            attr = cudaFuncSetAttribute(mla_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)tcmla::kSmem);
+    });
+    if (attr != cudaSuccess) return attr;
+    // with two splits, the pair runs as a cluster and combines through
+    // distributed shared memory: no partials, no combine launch
+    const int pair = splits == 2 ? 1 : 0;
+    e = launch_pdl(fp8 ? mla_tc_kernel<true> : mla_tc_kernel<false>, dim3(splits, num_q), dim3(tcmla::kThreads),
+                   tcmla::kSmem, stream, pair ? 2 : 1, qmap, reinterpret_cast<const uint8_t*>(latent), s, idx, topk_len,
+                   k, scale_log2, splits, pair, reinterpret_cast<__nv_bfloat16*>(out), lse, ws.mla_part, ws.mla_ml,
+                   d_status);
+    if (e != cudaSuccess || splits == 1 || pair) return e;
     return launch_pdl(mla_combine_kernel, dim3(num_q, kMH / kCombineHeads), dim3(128), 0, stream, 1, ws.mla_part,
                       ws.mla_ml, splits, reinterpret_cast<__nv_bfloat16*>(out), lse);
 }

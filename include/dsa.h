@@ -213,9 +213,9 @@ dsa_status sparse_mla_decode_noalloc(const void* q, const void* latent, dsa_dtyp
                                      int32_t* d_status, cudaStream_t stream);
 
 /* Number of kernels dsa_decode_layer enqueues for these sizes (reuse_idx and
- * latent_dtype as in dsa_layer_args); 0 when the sizes are refused.  For
- * callers that count or capture launches.  (With a bf16 latent and two splits
- * per query the attention combines its splits inside one launch.) */
+ * latent_dtype as in dsa_layer_args); 0 when the sizes or the dtype are
+ * refused.  For callers that count or capture launches.  (With two splits per
+ * query the attention combines its splits inside one launch.) */
 int32_t dsa_decode_layer_launches(const dsa_seqs* seqs, int32_t num_q, int32_t k, int32_t reuse_idx,
                                   dsa_dtype latent_dtype);
 
