@@ -102,6 +102,11 @@ size_t workspace_bytes(const dsa_seqs& s, int num_q, int k, int64_t* scores_ld) 
     b += up256((size_t)num_q * splits * kMH * kMV * 4);              // partial outputs
     b += up256((size_t)num_q * splits * kMH * 2 * 4);                // partial (max, sum)
     b += up256((size_t)num_q * ld * 4);                              // scores (fused layer)
+    if (topk_long_rows(s.max_ctx)) {                                  // long-row top-k
+        b += up256((size_t)num_q * (2048 + 2) * 4);                  // histograms + two counters
+        b += up256((size_t)num_q * kLongCand * 8);                   // candidates
+        b += up256((size_t)num_q * DSA_MAX_TOPK * 4);                // positions above the chosen digit
+    }
     return b;
 }
 
@@ -122,6 +127,16 @@ Workspace carve_workspace(void* base, const dsa_seqs& s, int num_q, int k) {
     p += up256((size_t)num_q * splits * kMH * 2 * 4);
     w.scores = reinterpret_cast<float*>(p);
     w.scores_ld = ld;
+    p += up256((size_t)num_q * ld * 4);
+    if (topk_long_rows(s.max_ctx)) {
+        w.tk_hist = reinterpret_cast<int*>(p);
+        w.tk_ncand = w.tk_hist + (size_t)num_q * 2048;
+        w.tk_nabove = w.tk_ncand + num_q;
+        p += up256((size_t)num_q * (2048 + 2) * 4);
+        w.tk_cand = reinterpret_cast<uint2*>(p);
+        p += up256((size_t)num_q * kLongCand * 8);
+        w.tk_above = reinterpret_cast<int*>(p);
+    }
     return w;
 }
 
@@ -193,8 +208,6 @@ dsa_status dsa_index_scores(const void* q_idx, const float* w, const float* ssma
 dsa_status dsa_topk(const float* scores, int64_t ld, const dsa_seqs* seqs, int32_t num_q, int32_t k, int32_t* idx,
                     int32_t* topk_len, void* workspace, size_t workspace_bytes, int32_t* d_status,
                     cudaStream_t stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     Check c;
     check_seqs(c, seqs, num_q);
     c.ptr(scores, "scores");
@@ -202,9 +215,14 @@ dsa_status dsa_topk(const float* scores, int64_t ld, const dsa_seqs* seqs, int32
     c.ptr(topk_len, "topk_len", 4);
     c.need(k >= 1 && k <= DSA_MAX_TOPK, DSA_ERR_UNSUPPORTED, "k %d outside [1, %d]", k, DSA_MAX_TOPK);
     if (seqs) c.need(ld >= seqs->max_ctx && ld % 4 == 0, DSA_ERR_INVALID_ARG, "ld %lld must be >= max_ctx and a multiple of 4", (long long)ld);
+    const bool long_rows = seqs && topk_long_rows(seqs->max_ctx);
+    if (long_rows) check_workspace(c, seqs, num_q, k, workspace, workspace_bytes);  // rows > 32K keys use scratch
     dsa_status st = c.done();
     if (st != DSA_OK || num_q == 0) return st;
-    return cuda_status(launch_topk(scores, ld, *seqs, num_q, k, idx, topk_len, d_status, stream), "dsa_topk launch");
+    Workspace ws{};
+    if (long_rows) ws = carve_workspace(workspace, *seqs, num_q, k);
+    return cuda_status(launch_topk(scores, ld, *seqs, num_q, k, idx, topk_len, ws, d_status, stream),
+                       "dsa_topk launch");
 }
 
 static void check_mla_args(Check& c, const void* q, const void* latent, dsa_dtype latent_dtype, const int32_t* idx,
@@ -261,7 +279,7 @@ dsa_status dsa_decode_layer(const dsa_layer_args* a, const dsa_seqs* seqs, int32
                                     a->k_dtype, *seqs, num_q, ws.scores, ws.scores_ld, ws, d_status, stream);
         mark(1);
         if (e == cudaSuccess)
-            e = launch_topk(ws.scores, ws.scores_ld, *seqs, num_q, a->k, a->idx, a->topk_len, d_status, stream);
+            e = launch_topk(ws.scores, ws.scores_ld, *seqs, num_q, a->k, a->idx, a->topk_len, ws, d_status, stream);
         mark(2);
     } else {
         mark(1);
@@ -285,7 +303,9 @@ int32_t dsa_decode_layer_launches(const dsa_seqs* seqs, int32_t num_q, int32_t k
     const int splits = mla_splits(num_q, k);
     // attention, plus the LSE combine unless the splits combine in-kernel (two splits)
     const int mla = splits <= 2 ? 1 : 2;
-    return (reuse_idx ? 0 : 3) + mla;  // query prep, scores, top-k
+    // top-k: one kernel, or three for rows longer than 32,768 keys (chunked)
+    const int tk = topk_chunked(seqs->max_ctx) ? 3 : 1;
+    return (reuse_idx ? 0 : 2 + tk) + mla;  // query prep, scores, top-k
 }
 
 }  // extern "C"

@@ -125,7 +125,21 @@ struct Workspace {
     float* mla_ml;    // (m, l) partials [Q, splits, 64, 2]
     float* scores;    // [Q, ld] for dsa_decode_layer
     int64_t scores_ld;
+    // top-k of rows longer than 32,768 keys (null otherwise)
+    int* tk_hist;        // [Q, 2048] first-digit histograms, then the two [Q] counters (cleared per call)
+    int* tk_ncand;       // [Q] keys of the chosen first digit
+    int* tk_nabove;      // [Q] keys above the chosen first digit (< k)
+    uint2* tk_cand;      // [Q, kLongCand] (key, position) of the chosen first digit
+    int* tk_above;       // [Q, DSA_MAX_TOPK] positions of the keys above it
 };
+
+constexpr int kLongChunk = 16384;      // keys per CTA in the long-row top-k
+constexpr int kLongCand = 8192;        // candidate slots per row
+constexpr int kLongMaxChunks = 1024;   // rows up to 16M keys take the chunked path
+
+inline bool topk_long_rows(int max_ctx) { return max_ctx > 32768; }
+inline int topk_chunks(int max_ctx) { return (max_ctx + kLongChunk - 1) / kLongChunk; }
+inline bool topk_chunked(int max_ctx) { return topk_long_rows(max_ctx) && topk_chunks(max_ctx) <= kLongMaxChunks; }
 
 int mla_splits(int num_q, int k);
 size_t workspace_bytes(const dsa_seqs& s, int num_q, int k, int64_t* scores_ld);
@@ -136,7 +150,7 @@ cudaError_t launch_index_scores(const void* q_idx, const float* w, const float* 
                                 const dsa_seqs& s, int num_q, float* scores, int64_t ld, const Workspace& ws,
                                 int32_t* d_status, cudaStream_t stream);
 cudaError_t launch_topk(const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int k, int32_t* idx,
-                        int32_t* topk_len, int32_t* d_status, cudaStream_t stream);
+                        int32_t* topk_len, const Workspace& ws, int32_t* d_status, cudaStream_t stream);
 cudaError_t launch_sparse_mla(const void* q, const void* latent, dsa_dtype latent_dtype, const dsa_seqs& s,
                               int num_q, const int32_t* idx, const int32_t* topk_len, int k, float sm_scale,
                               void* out, float* lse, const Workspace& ws, int32_t* d_status, cudaStream_t stream);

@@ -16,13 +16,12 @@
 // with the row in registers (three passes of 11 + 11 + 10 bits); longer rows
 // up to 16 x 32,768 keys a thread-block cluster per row; anything longer one
 // CTA per row with four 8-bit passes over memory.
-#include <cooperative_groups.h>
 
+#include <climits>
 #include <mutex>
 
 #include "dsa_internal.cuh"
 
-namespace cg = cooperative_groups;
 
 namespace dsa {
 
@@ -519,286 +518,326 @@ __global__ void __launch_bounds__(1024, 1) topk_smem_kernel(const float* __restr
 }
 
 // ---------------------------------------------------------------------------
-// Register-resident variant: a thread-block cluster of CL CTAs per query row,
-// each CTA holding 512 x EPT scores in registers, so the row is read from
-// memory exactly once.  Three digit passes (11 + 11 + 10 bits): each CTA
-// histograms its keys in shared memory (lanes of a warp that hit the same bin
-// add with one atomic), CTA r of the cluster sums slice r of the CL histograms
-// through distributed shared memory, and every CTA reads the merged slices
-// and finds the same digit.  After the first pass only the keys of the chosen
-// bin take part, compacted into shared memory when they fit.  The compaction
-// ranks ties and positions across the cluster with prefix sums of per-CTA
-// counts, so the output is the same as the one-CTA kernel's.
-constexpr int kCT = 512;                 // threads per CTA
-constexpr int kCBins = 2048;
-constexpr int kCandCap = 4096;           // keys of the chosen bin kept in shared memory
+// Rows longer than 32,768 keys: a chunked pipeline over every SM (no kernel
+// needs the CTAs of a row to be co-resident).  Chunks of kLongChunk keys.
+//   1. topk_hist_kernel  (chunk x row): histogram of the first digit (top 11
+//      bits of the order key) of each chunk, added into the row's histogram;
+//   2. topk_cand_kernel  (chunk x row): the digit d0 of the k-th key from the
+//      row's histogram; the positions of the chunk's keys above d0 (fewer than
+//      k in the row) and the keys of d0 (key, position) are appended to the
+//      row's lists, one reservation per CTA;
+//   3. topk_final_kernel (row): the exact k-th key T among the keys of d0
+//      (11 + 10 more bits; by passes over the row in memory when they
+//      overflowed their list), then the selected positions -- every key above
+//      d0, the keys of d0 above T and the smallest positions of the keys equal
+//      to T that are needed -- sorted ascending in shared memory.
+constexpr int kLongThreads = 1024;
+constexpr int kLongEPT = kLongChunk / kLongThreads;  // 16: four rounds of one float4 per thread
+constexpr int kFinalThreads = 1024;
+constexpr size_t kFinalSmem = (size_t)kLongCand * 8 + (size_t)kLongCand * 4 + 2048 * 4 + DSA_MAX_TOPK * 4;
 
-// exclusive prefix sum over the kCT threads of a CTA
-__device__ __forceinline__ int cta_exclusive_scan(int v, int* buf, int* total) {
-    constexpr int W = kCT / 32;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x = v;
+// false: nothing for the chunk kernels to do on row t (a bad row is reported
+// by the final kernel; a row of at most k keys is written by it)
+__device__ __forceinline__ bool long_row(const dsa_seqs& s, int t, int k, int* n_out) {
+    const int b = seq_of(s.q_start, s.num_seqs, t);
+    const int pos = __ldg(s.q_pos + t);
+    const int ctx = __ldg(s.ctx_len + b);
+    if (pos < 0 || pos >= ctx || ctx > s.max_ctx) return false;
+    *n_out = pos + 1;
+    return pos + 1 > k;
+}
+
+// position of this thread's key e in the chunk starting at j0: round e / 4 of
+// coalesced float4 loads (a warp reads 512 contiguous bytes), component e % 4
+__device__ __forceinline__ int chunk_pos(int j0, int e) {
+    return j0 + ((e >> 2) * kLongThreads + (int)threadIdx.x) * 4 + (e & 3);
+}
+
+__device__ __forceinline__ void chunk_keys(const float* row, int64_t ld, int j0, uint32_t* u) {
+    const int last4 = (int)((ld - 4) & ~(int64_t)3);
+    uint4 r[kLongEPT / 4];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+    for (int v = 0; v < kLongEPT / 4; ++v)
+        r[v] = __ldg(reinterpret_cast<const uint4*>(row + min(j0 + (v * kLongThreads + (int)threadIdx.x) * 4, last4)));
+#pragma unroll
+    for (int v = 0; v < kLongEPT / 4; ++v) {
+        u[4 * v] = order_key(__uint_as_float(r[v].x));
+        u[4 * v + 1] = order_key(__uint_as_float(r[v].y));
+        u[4 * v + 2] = order_key(__uint_as_float(r[v].z));
+        u[4 * v + 3] = order_key(__uint_as_float(r[v].w));
     }
-    if (lane == 31) buf[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        int w = lane < W ? buf[lane] : 0;
+}
+
+// The first digit of the k-th largest key of a row from its histogram, and
+// the number of keys in higher digits; the same result in every thread.
+template <int THREADS>
+__device__ __forceinline__ void first_digit(const int* hr, int k, int* buf, int* sh, int& d0, int& above) {
+    constexpr int PER = 2048 / THREADS;
+    int c[PER], csum = 0;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += y;
+    for (int q = 0; q < PER; ++q) {
+        c[q] = __ldcg(hr + 2047 - PER * (int)threadIdx.x - q);
+        csum += c[q];
+    }
+    int tot;
+    int before = scan_threads<THREADS>(csum, buf, &tot);
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+        if (before < k && before + c[q] >= k) {
+            sh[0] = 2047 - PER * (int)threadIdx.x - q;
+            sh[1] = before;
         }
-        buf[32 + lane] = w;
+        before += c[q];
     }
     __syncthreads();
-    const int before = (warp ? buf[32 + warp - 1] : 0) + x - v;
-    *total = buf[32 + W - 1];
+    d0 = sh[0];
+    above = sh[1];
     __syncthreads();
-    return before;
 }
 
-__device__ __forceinline__ void hist_add(int* hist, bool act, int bin) {
-    const unsigned am = __ballot_sync(0xffffffffu, act);
-    if (act) {
-        const unsigned peers = __match_any_sync(am, bin);
-        if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(hist + bin, __popc(peers));
-    }
-}
-
-template <int EPT>
-__global__ void __launch_bounds__(kCT, EPT <= 16 ? 2 : 1)
-    topk_cluster_kernel(const float* __restrict__ scores, int64_t ld, dsa_seqs s, int k, int32_t* __restrict__ idx,
-                        int32_t* __restrict__ topk_len, int32_t* d_status) {
+__global__ void __launch_bounds__(kLongThreads) topk_hist_kernel(const float* __restrict__ scores, int64_t ld,
+                                                                  dsa_seqs s, int k, int* __restrict__ hist) {
     pdl_enter();
-    constexpr int kChunk = kCT * EPT;
-    cg::cluster_group cluster = cg::this_cluster();
-    const int rank = (int)cluster.block_rank();
-    const int CL = (int)cluster.num_blocks();
-    __shared__ int hist[kCBins];     // this CTA's histogram
-    __shared__ int mhist[kCBins];    // merged counts of the bins this CTA owns
-    __shared__ uint32_t cand[kCandCap];
-    __shared__ int scan_buf[64];
-    __shared__ int sel_digit, sel_above, ncand;
-    __shared__ int cnt[2];
-    const int t = blockIdx.y;
-    const int tid = threadIdx.x;
+    __shared__ int h[4][2048];
+    const int t = blockIdx.y, j0 = blockIdx.x * kLongChunk;
+    int n = 0;
+    if (!long_row(s, t, k, &n) || j0 >= n) return;  // uniform over the CTA
+    for (int i = threadIdx.x; i < 4 * 2048; i += kLongThreads) (&h[0][0])[i] = 0;
+    __syncthreads();
+    uint32_t u[kLongEPT];
+    chunk_keys(scores + (int64_t)t * ld, ld, j0, u);
+    int* hw = h[(threadIdx.x >> 5) & 3];  // four copies spread the same-address atomics
+#pragma unroll
+    for (int e = 0; e < kLongEPT; ++e)
+        if (chunk_pos(j0, e) < n) atomicAdd(hw + (u[e] >> 21), 1);
+    __syncthreads();
+    int* hr = hist + (int64_t)t * 2048;
+    for (int b = threadIdx.x; b < 2048; b += kLongThreads) {
+        const int v = h[0][b] + h[1][b] + h[2][b] + h[3][b];
+        if (v) atomicAdd(hr + b, v);
+    }
+}
+
+__global__ void __launch_bounds__(kLongThreads) topk_cand_kernel(const float* __restrict__ scores, int64_t ld,
+                                                                  dsa_seqs s, int k, const int* __restrict__ hist,
+                                                                  int* __restrict__ ncand, int* __restrict__ nabove,
+                                                                  uint2* __restrict__ cand, int* __restrict__ above_pos) {
+    pdl_enter();
+    __shared__ int buf[64], sh[2];
+    const int t = blockIdx.y, j0 = blockIdx.x * kLongChunk;
+    int n = 0;
+    if (!long_row(s, t, k, &n) || j0 >= n) return;
+    uint32_t u[kLongEPT];
+    chunk_keys(scores + (int64_t)t * ld, ld, j0, u);  // in flight while the digit is found
+    int d0, above;
+    first_digit<kLongThreads>(hist + (int64_t)t * 2048, k, buf, sh, d0, above);
+    int na = 0, nc = 0;
+#pragma unroll
+    for (int e = 0; e < kLongEPT; ++e) {
+        const int dg = chunk_pos(j0, e) < n ? (int)(u[e] >> 21) : -1;
+        na += dg > d0;
+        nc += dg == d0;
+    }
+    // one reservation per CTA and list (the chunks of a row share the counters)
+    int tot_a, tot_c;
+    int sa = scan_threads<kLongThreads>(na, buf, &tot_a);
+    int sc = scan_threads<kLongThreads>(nc, buf, &tot_c);
+    if (threadIdx.x == 0) {
+        sh[0] = tot_a > 0 ? atomicAdd(nabove + t, tot_a) : 0;
+        sh[1] = tot_c > 0 ? atomicAdd(ncand + t, tot_c) : 0;
+    }
+    __syncthreads();
+    sa += sh[0];
+    sc += sh[1];
+    int* ar = above_pos + (int64_t)t * DSA_MAX_TOPK;
+    uint2* cr = cand + (int64_t)t * kLongCand;
+#pragma unroll
+    for (int e = 0; e < kLongEPT; ++e) {
+        const int p = chunk_pos(j0, e);
+        const int dg = p < n ? (int)(u[e] >> 21) : -1;
+        if (dg > d0) {
+            if (sa < DSA_MAX_TOPK) ar[sa] = p;
+            ++sa;
+        } else if (dg == d0) {
+            if (sc < kLongCand) cr[sc] = make_uint2(u[e], (uint32_t)p);
+            ++sc;
+        }
+    }
+}
+
+// ascending bitonic sort of a[0 .. N), N a power of two, by the whole block
+template <int THREADS>
+__device__ void bitonic_sort(int* a, int N) {
+    for (int size = 2; size <= N; size <<= 1)
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < N / 2; i += THREADS) {
+                const int lo = 2 * i - (i & (stride - 1));
+                const int hi = lo + stride;
+                const bool up = (lo & size) == 0;
+                const int x = a[lo], y = a[hi];
+                if ((x > y) == up) {
+                    a[lo] = y;
+                    a[hi] = x;
+                }
+            }
+            __syncthreads();
+        }
+}
+
+__global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(
+    const float* __restrict__ scores, int64_t ld, dsa_seqs s, int k, int32_t* __restrict__ idx,
+    int32_t* __restrict__ topk_len, const int* __restrict__ hist, const int* __restrict__ ncand,
+    const int* __restrict__ nabove, const uint2* __restrict__ cand, const int* __restrict__ above_pos,
+    int32_t* d_status) {
+    constexpr int NT = kFinalThreads;
+    pdl_enter();
+    extern __shared__ __align__(16) int fn_smem[];
+    uint32_t* ck = reinterpret_cast<uint32_t*>(fn_smem);  // [kLongCand] keys of d0
+    int* cp = fn_smem + kLongCand;                        // [kLongCand] their positions
+    int* tie = cp + kLongCand;                            // [kLongCand] positions of keys == T
+    int* hs = tie + kLongCand;                            // [2048] digit histogram
+    int* sel = hs + 2048;                                 // [DSA_MAX_TOPK] selected positions
+    __shared__ int buf[64], sh[4];
+    const int t = blockIdx.x, tid = threadIdx.x;
     const int b = seq_of(s.q_start, s.num_seqs, t);
     const int pos = __ldg(s.q_pos + t);
     const int ctx = __ldg(s.ctx_len + b);
     int32_t* out = idx + (int64_t)t * k;
-    // uniform per row: every CTA of the cluster takes the same branch
-    if (pos < 0 || pos >= ctx || ctx > s.max_ctx || pos + 1 > CL * kChunk) {
-        if (rank == 0) {
-            if (tid == 0) {
-                report(d_status, DSA_ERR_BAD_INPUT);
-                topk_len[t] = 0;
-            }
-            for (int i = tid; i < k; i += kCT) out[i] = -1;
+    if (pos < 0 || pos >= ctx || ctx > s.max_ctx) {
+        if (tid == 0) {
+            report(d_status, DSA_ERR_BAD_INPUT);
+            topk_len[t] = 0;
         }
+        for (int i = tid; i < k; i += NT) out[i] = -1;
         return;
     }
     const int n = pos + 1;
     if (n <= k) {
-        if (rank == 0) {
-            for (int i = tid; i < k; i += kCT) out[i] = i < n ? i : -1;
-            if (tid == 0) topk_len[t] = n;
-        }
+        for (int i = tid; i < k; i += NT) out[i] = i < n ? i : -1;
+        if (tid == 0) topk_len[t] = n;
         return;
     }
-    // ---- this thread's EPT consecutive keys
+    int d0, above;
+    first_digit<NT>(hist + (int64_t)t * 2048, k, buf, sh, d0, above);
+    const uint32_t dpre = (uint32_t)d0 << 21, dmask = 0x7FFu << 21;
+    uint32_t prefix = dpre, mask = dmask;
+    int remaining = k - above;
+    const int nc = __ldcg(ncand + t);
+    const bool in_smem = nc <= kLongCand;
     const float* row = scores + (int64_t)t * ld;
-    const int base = rank * kChunk + tid * EPT;
-    uint32_t u[EPT];
-    uint64_t valid = 0;
-#pragma unroll
-    for (int v = 0; v < EPT / 4; ++v) {
-        const int i0 = base + 4 * v;
-        float4 f;
-        if (i0 + 3 < n) {
-            f = __ldg(reinterpret_cast<const float4*>(row + i0));
-        } else {
-            f.x = i0 < n ? __ldg(row + i0) : 0.f;
-            f.y = i0 + 1 < n ? __ldg(row + i0 + 1) : 0.f;
-            f.z = i0 + 2 < n ? __ldg(row + i0 + 2) : 0.f;
-            f.w = i0 + 3 < n ? __ldg(row + i0 + 3) : 0.f;
+    if (in_smem)
+        for (int i = tid; i < nc; i += NT) {
+            const uint2 e = __ldcg(cand + (int64_t)t * kLongCand + i);
+            ck[i] = e.x;
+            cp[i] = (int)e.y;
         }
-        u[4 * v] = order_key(f.x);
-        u[4 * v + 1] = order_key(f.y);
-        u[4 * v + 2] = order_key(f.z);
-        u[4 * v + 3] = order_key(f.w);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if (i0 + e < n) valid |= 1ull << (4 * v + e);
-    }
-    // ---- three digit passes
-    uint32_t prefix = 0, mask = 0;
-    int remaining = k;
-    bool use_cand = false;
-    if (tid == 0) ncand = 0;
+    // two more digit passes (11 then 10 bits) over the keys of d0
 #pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-        const int nb = pass == 2 ? 1024 : 2048;
-        for (int i = tid; i < kCBins; i += kCT) hist[i] = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        const int shift = pass == 0 ? 10 : 0;
+        const int nb = pass == 0 ? 2048 : 1024;
+        for (int i = tid; i < 2048; i += NT) hs[i] = 0;
         __syncthreads();
-        if (use_cand) {
-            const int nc = ncand, nc_r = (nc + 31) & ~31;  // whole warps take part in hist_add
-            for (int i = tid; i < nc_r; i += kCT) {
-                const bool act = i < nc && (cand[i < nc ? i : 0] & mask) == prefix;
-                hist_add(hist, act, act ? (cand[i] >> shift) & (nb - 1) : 0);
-            }
+        if (in_smem) {
+            for (int i = tid; i < nc; i += NT)
+                if ((ck[i] & mask) == prefix) atomicAdd(hs + ((ck[i] >> shift) & (nb - 1)), 1);
         } else {
-#pragma unroll
-            for (int e = 0; e < EPT; ++e) {
-                const bool act = ((valid >> e) & 1) && (u[e] & mask) == prefix;
-                hist_add(hist, act, (u[e] >> shift) & (nb - 1));
+            for (int j = tid; j < n; j += NT) {
+                const uint32_t u = order_key(__ldg(row + j));
+                if ((u & mask) == prefix) atomicAdd(hs + ((u >> shift) & (nb - 1)), 1);
             }
         }
-        cluster.sync();  // A: every CTA's histogram is final
-        // merge slice `rank` of the bins over the cluster
-        const int slice = nb / CL;
-        for (int i = tid; i < slice; i += kCT) {
-            const int bin = rank * slice + i;
-            int v = 0;
-            for (int r = 0; r < CL; ++r) v += cluster.map_shared_rank(hist, r)[bin];
-            mhist[bin] = v;
-        }
-        cluster.sync();  // B: merged slices final
-        // digits in descending order, 4 per thread, read from their owners
-        int c[4], csum = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int d = nb - 1 - 4 * tid - q;
-            const int v = d >= 0 ? cluster.map_shared_rank(mhist, d / slice)[d] : 0;
-            c[q] = v;
-            csum += v;
-        }
+        __syncthreads();
+        const int per = nb / NT;  // 2 or 1 digits per thread, descending
+        const int dA = nb - 1 - per * tid;
+        const int cA = hs[dA], cB = per == 2 ? hs[dA - 1] : 0;
         int tot;
-        int before = cta_exclusive_scan(csum, scan_buf, &tot);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if (before < remaining && before + c[q] >= remaining) {
-                sel_digit = nb - 1 - 4 * tid - q;
-                sel_above = before;
-            }
-            before += c[q];
+        const int before = scan_threads<NT>(cA + cB, buf, &tot);
+        if (before < remaining && before + cA >= remaining) {
+            sh[0] = dA;
+            sh[1] = before;
+        } else if (per == 2 && before + cA < remaining && before + cA + cB >= remaining) {
+            sh[0] = dA - 1;
+            sh[1] = before + cA;
         }
-        cluster.sync();  // C: every CTA is done reading histograms; the digit is visible
-        prefix |= (uint32_t)sel_digit << shift;
+        __syncthreads();
+        prefix |= (uint32_t)sh[0] << shift;
         mask |= (uint32_t)(nb - 1) << shift;
-        remaining -= sel_above;
-        if (pass == 0) {
-            // keep the keys of the chosen bin for the next two passes
-            const int lane = tid & 31;
-#pragma unroll
-            for (int e = 0; e < EPT; ++e) {
-                const bool act = ((valid >> e) & 1) && (u[e] & mask) == prefix;
-                const unsigned am = __ballot_sync(0xffffffffu, act);
-                int slot0 = 0;
-                if (lane == 0 && am) slot0 = atomicAdd(&ncand, __popc(am));
-                slot0 = __shfl_sync(0xffffffffu, slot0, 0);
-                const int sl = slot0 + __popc(am & ((1u << lane) - 1));
-                if (act && sl < kCandCap) cand[sl] = u[e];
-            }
-            __syncthreads();
-            use_cand = ncand <= kCandCap;
-        }
+        remaining -= sh[1];
+        __syncthreads();
     }
     const uint32_t T = prefix;
-    const int need_eq = remaining;
-    // ---- cluster-wide ranks: keys > T and keys == T, in index order
-    int n_gt = 0, n_eq = 0;
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) {
-        const bool vld = (valid >> e) & 1;
-        n_gt += vld && u[e] > T;
-        n_eq += vld && u[e] == T;
-    }
-    int gt_cta, eq_cta;
-    cta_exclusive_scan(n_gt, scan_buf, &gt_cta);
-    const int eq_before = cta_exclusive_scan(n_eq, scan_buf, &eq_cta);
+    const int need_eq = remaining;  // keys == T to take, >= 1
+    // the selection: every key above d0, the keys of d0 above T, then the
+    // need_eq smallest positions among the keys equal to T
+    const int na = min(__ldcg(nabove + t), DSA_MAX_TOPK);  // == above
+    for (int i = tid; i < na; i += NT) sel[i] = __ldcg(above_pos + (int64_t)t * DSA_MAX_TOPK + i);
     if (tid == 0) {
-        cnt[0] = gt_cta;
-        cnt[1] = eq_cta;
+        sh[2] = na;  // next free slot of sel
+        sh[3] = 0;   // ties found
     }
-    cluster.sync();
-    int gt_prefix = 0, eq_prefix = 0;
-    for (int r = 0; r < rank; ++r) {
-        const int* rc = cluster.map_shared_rank(cnt, r);
-        gt_prefix += rc[0];
-        eq_prefix += rc[1];
+    __syncthreads();
+    if (in_smem) {
+        // compaction by prefix sums: thread tid takes candidates [i0, i1)
+        const int per = (nc + NT - 1) / NT;
+        const int i0 = min(tid * per, nc), i1 = min(i0 + per, nc);
+        int ng = 0, nq = 0;
+        for (int i = i0; i < i1; ++i) {
+            ng += ck[i] > T;
+            nq += ck[i] == T;
+        }
+        int tg, tq;
+        int og = na + scan_threads<NT>(ng, buf, &tg);
+        int oq = scan_threads<NT>(nq, buf, &tq);
+        for (int i = i0; i < i1; ++i) {
+            if (ck[i] > T) sel[og++] = cp[i];
+            else if (ck[i] == T) tie[oq++] = cp[i];
+        }
+        if (tid == 0) {
+            sh[2] = na + tg;
+            sh[3] = tq;
+        }
+        __syncthreads();
+        const int ne = sh[3];
+        if (ne > need_eq) {  // keep the smallest positions
+            int N = 1;
+            while (N < ne) N <<= 1;
+            for (int i = ne + tid; i < N; i += NT) tie[i] = INT_MAX;
+            __syncthreads();
+            bitonic_sort<NT>(tie, N);
+        }
+        const int base = sh[2];
+        for (int i = tid; i < need_eq; i += NT) sel[base + i] = tie[i];
+    } else {
+        // keys of d0 above T from the row; ties in position order, block by block
+        for (int j = tid; j < n; j += NT) {
+            const uint32_t u = order_key(__ldg(row + j));
+            if ((u & dmask) == dpre && u > T) sel[atomicAdd(sh + 2, 1)] = j;
+        }
+        __syncthreads();
+        int taken = 0;
+        const int base = sh[2];
+        for (int j0 = 0; j0 < n && taken < need_eq; j0 += NT) {
+            const int j = j0 + tid;
+            const bool eq = j < n && order_key(__ldg(row + j)) == T;
+            int tot;
+            const int r = scan_threads<NT>(eq ? 1 : 0, buf, &tot);
+            if (eq && taken + r < need_eq) sel[base + taken + r] = j;
+            taken += tot;
+        }
     }
-    int eq_rank = eq_prefix + eq_before;
-    const int n_sel = n_gt + max(0, min(need_eq - eq_rank, n_eq));
-    int sel_cta;
-    int o = gt_prefix + min(need_eq, eq_prefix) + cta_exclusive_scan(n_sel, scan_buf, &sel_cta);
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) {
-        if (!((valid >> e) & 1)) continue;
-        bool take = u[e] > T;
-        if (u[e] == T) take = eq_rank++ < need_eq;
-        if (take && o < k) out[o++] = base + e;
-    }
-    if (rank == 0 && tid == 0) topk_len[t] = k;
-    cluster.sync();  // no CTA leaves while another may still read its counts
+    __syncthreads();
+    // k positions, ascending (k <= 2048 slots, padded to a power of two)
+    int N = 1;
+    while (N < k) N <<= 1;
+    for (int i = k + tid; i < N; i += NT) sel[i] = INT_MAX;
+    __syncthreads();
+    bitonic_sort<NT>(sel, N);
+    for (int i = tid; i < k; i += NT) out[i] = sel[i];
+    if (tid == 0) topk_len[t] = k;
 }
 
 namespace {
-
-struct ClusterPlan {
-    int cl, ept;
-};
-
-// CTAs per row and keys per thread: enough capacity for the longest row, then
-// more CTAs per row (down to 16 keys per thread) until the launch fills the GPU.
-ClusterPlan topk_plan(int max_ctx, int num_q) {
-    ClusterPlan p{1, 64};
-    while (p.cl * kCT * 64 < max_ctx) p.cl *= 2;
-    while (p.cl < 16 && p.cl * num_q < 256 && (p.cl * 2) * kCT * 16 <= max_ctx * 2) p.cl *= 2;
-    p.ept = 16;
-    while (p.cl * kCT * p.ept < max_ctx) p.ept *= 2;
-    return p;
-}
-
-template <int EPT>
-int max_cluster() {
-    static std::once_flag once;
-    static int max_ok = 0;
-    std::call_once(once, [] {
-        cudaFuncSetAttribute(topk_cluster_kernel<EPT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        for (int c = 1; c <= 16; c *= 2) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(c, 1, 1);
-            cfg.blockDim = dim3(kCT, 1, 1);
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = c;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel<EPT>, &cfg) == cudaSuccess && n > 0) max_ok = c;
-            else break;
-        }
-        cudaGetLastError();
-    });
-    return max_ok;
-}
-
-template <int EPT>
-cudaError_t launch_cluster(int cl, const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int k,
-                           int32_t* idx, int32_t* topk_len, int32_t* d_status, cudaStream_t stream) {
-    return launch_pdl(topk_cluster_kernel<EPT>, dim3(cl, num_q), dim3(kCT), 0, stream, cl, scores, ld, s, k, idx,
-                      topk_len, d_status);
-}
-
-
-}  // namespace
 
 template <int THREADS, int EPT>
 cudaError_t launch_row(const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int k, int32_t* idx,
@@ -828,8 +867,10 @@ cudaError_t launch_smem_row(const float* scores, int64_t ld, const dsa_seqs& s, 
                       k, idx, topk_len, d_status);
 }
 
+}  // namespace
+
 cudaError_t launch_topk(const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int k, int32_t* idx,
-                        int32_t* topk_len, int32_t* d_status, cudaStream_t stream) {
+                        int32_t* topk_len, const Workspace& ws, int32_t* d_status, cudaStream_t stream) {
     // rows up to 32,768 keys: one CTA per row
     if (s.max_ctx <= 1024 * 8)
         return launch_row<1024, 8>(scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
@@ -837,16 +878,29 @@ cudaError_t launch_topk(const float* scores, int64_t ld, const dsa_seqs& s, int 
         return launch_row<1024, 16>(scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
     if (s.max_ctx <= 1024 * 32)
         return launch_smem_row<32>(scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
-    const ClusterPlan p = topk_plan(s.max_ctx, num_q);
-    if (p.cl <= 16 && p.ept <= 64) {
-        if (p.ept == 16 && p.cl <= max_cluster<16>())
-            return launch_cluster<16>(p.cl, scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
-        if (p.ept == 32 && p.cl <= max_cluster<32>())
-            return launch_cluster<32>(p.cl, scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
-        if (p.ept == 64 && p.cl <= max_cluster<64>())
-            return launch_cluster<64>(p.cl, scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
+    const int C = topk_chunks(s.max_ctx);
+    if (topk_chunked(s.max_ctx) && ws.tk_hist) {
+        static std::once_flag once;
+        static cudaError_t attr = cudaSuccess;
+        std::call_once(once, [] {
+            attr = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kFinalSmem);
+        });
+        if (attr != cudaSuccess) return attr;
+        cudaError_t e = cudaMemsetAsync(ws.tk_hist, 0, (size_t)num_q * (2048 + 2) * 4, stream);
+        if (e == cudaSuccess)
+            e = launch_pdl(topk_hist_kernel, dim3(C, num_q), dim3(kLongThreads), 0, stream, 1, scores, ld, s, k,
+                           ws.tk_hist);
+        if (e == cudaSuccess)
+            e = launch_pdl(topk_cand_kernel, dim3(C, num_q), dim3(kLongThreads), 0, stream, 1, scores, ld, s, k,
+                           (const int*)ws.tk_hist, ws.tk_ncand, ws.tk_nabove, ws.tk_cand, ws.tk_above);
+        if (e == cudaSuccess)
+            e = launch_pdl(topk_final_kernel, dim3(num_q), dim3(kFinalThreads), kFinalSmem, stream, 1, scores, ld, s,
+                           k, idx, topk_len, (const int*)ws.tk_hist, (const int*)ws.tk_ncand,
+                           (const int*)ws.tk_nabove, (const uint2*)ws.tk_cand, (const int*)ws.tk_above, d_status);
+        return e;
     }
-    // rows longer than 16 x 32,768 keys: one CTA per row, passes over memory
+    // rows longer than 16M keys: one CTA per row, passes over memory
     return launch_pdl(topk_kernel, dim3(num_q), dim3(kTopkThreads), 0, stream, 1, scores, ld, s, k, idx, topk_len,
                       d_status);
 }

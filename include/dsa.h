@@ -128,6 +128,9 @@ dsa_status dsa_index_scores(const void* q_idx, const float* w, const float* ssma
  *   scores   fp32 [num_q, ld] (as written by dsa_index_scores)
  *   idx      int32 [num_q, k]: selected positions in ascending order, then -1
  *   topk_len int32 [num_q]: number of selected positions
+ *   workspace: unused (may be NULL) when max_ctx <= 32768; for longer rows at
+ *            least dsa_workspace_size bytes, 256-byte aligned (scratch of the
+ *            chunked selection; calls sharing it must be serialised)
  * 1 <= k <= 2048. */
 dsa_status dsa_topk(const float* scores, int64_t ld, const dsa_seqs* seqs, int32_t num_q, int32_t k, int32_t* idx,
                     int32_t* topk_len, void* workspace, size_t workspace_bytes, int32_t* d_status,
