@@ -154,18 +154,13 @@ __global__ void __launch_bounds__(128) qprep_kernel(const __nv_bfloat16* __restr
 //              accumulators double-buffered in TMEM;
 //   warps 2-5  epilogue: one key row per thread straight from TMEM, relu and
 //              head weights, causal mask, fp8 row scale, coalesced stores;
-//   warps 6-9  (e4m3 keys only) decode the staged codes to f16 in the
-//              swizzled layout the MMA reads.
+//   warps 6-9  (e4m3 keys only) decode the staged codes, one key row per
+//              thread, and store them as f16 into a TMEM operand buffer: the
+//              MMA takes its key operand A from TMEM, so shared memory holds
+//              only the 16 KB raw stages and the ring runs deep.
 // Keys past the context are never stored; pages are read through the page
 // table one TMA box (R rows, R | page size) at a time.
 constexpr int kTileKeys = 128;
-
-template <bool FP8>
-struct StageBytes {
-    static constexpr int raw = FP8 ? kTileKeys * kID : 0;   // e4m3 codes, unswizzled
-    static constexpr int mma = kTileKeys * kID * 2;         // 16-bit, two swizzled 64-dim blocks
-    static constexpr int total = raw + mma;
-};
 
 struct IdxSeg {
     int b, ctx, q0, nq, maxpos;
@@ -244,20 +239,50 @@ template <int NQ, int KP, bool FP8>
 struct IdxCfg {
     static constexpr int N = NQ * kIH;
     static constexpr int q_bytes = N * KP * 2;                         // KP/64 blocks of N x 128 B
-    static constexpr int stage_bytes = StageBytes<FP8>::total;
-    // Decode shapes (small q') run two persistent CTAs per SM, so two
-    // producer / MMA-issuer pairs overlap their per-tile issue work.
-    static constexpr int tail_raw = (3 * 8 + 6) * 8 + 8 + 4 * NQ * kIH * 4 + 4 * NQ * 4;
+    // bf16: two 128-byte swizzled 64-dim blocks; e4m3: the raw codes, one
+    // 128-byte (swizzled) row per key
+    static constexpr int stage_bytes = FP8 ? kTileKeys * kID : kTileKeys * kID * 2;
+    static constexpr int tail_raw = (2 * 8 + 14) * 8 + 8 + 4 * NQ * kIH * 4 + 4 * NQ * 4;
     static constexpr int tail = (tail_raw + 1023) / 1024 * 1024;  // barriers, TMEM slot, per-warp weights
-    static constexpr int ctas_per_sm = (110 * 1024 - q_bytes - 1024 - tail) / stage_bytes >= 2 ? 2 : 1;
+    // Decode shapes (small q') run two persistent CTAs per SM, so two
+    // producer / MMA-issuer pairs overlap their per-tile issue work: when two
+    // CTAs' stages fit and, for e4m3 keys, both accumulators and two 64-column
+    // key operands fit in half the TMEM.
+    static constexpr bool two_fit = (110 * 1024 - q_bytes - 1024 - tail) / stage_bytes >= 2 &&
+                                    (!FP8 || 2 * N + 2 * 64 <= 256);
+    static constexpr int ctas_per_sm = two_fit ? 2 : 1;
     static constexpr int budget = (ctas_per_sm == 2 ? 110 : 220) * 1024;
     static constexpr int stages_fit = (budget - q_bytes - 1024 - tail) / stage_bytes;
     static constexpr int S = stages_fit > 8 ? 8 : stages_fit;
     static constexpr int threads = FP8 ? 320 : 192;
-    static constexpr int tmem_cols = 2 * N < 32 ? 32 : 2 * N;
+    static constexpr int tmem_cols = FP8 ? (ctas_per_sm == 2 ? 256 : 512) : (2 * N < 32 ? 32 : 2 * N);
+    // accumulator buffers (columns [0, nacc N)), then (e4m3) na key operand
+    // buffers of 64 columns: 128 keys x 128 f16 dims
+    static constexpr int nacc = (!FP8 || 2 * N + 2 * 64 <= tmem_cols) ? 2 : 1;
+    static constexpr int na_fit = FP8 ? (tmem_cols - nacc * N) / 64 : 0;
+    static constexpr int na = na_fit > 4 ? 4 : na_fit;
+    static constexpr int a_col = nacc * N;
     static constexpr size_t smem = 1024 + (size_t)S * stage_bytes + q_bytes + tail;  // + alignment slack
     static_assert(S >= 2, "too little shared memory for two stages");
+    static_assert(!FP8 || na >= 2, "too little TMEM for two key operand buffers");
 };
+
+// Two e4m3 codes of w (the bytes that prmt selector sel picks, the lower
+// dimension first) -> f16x2 holding 2^-8 times their values, exactly.  The
+// code's 7 magnitude bits (4 exponent, 3 mantissa), moved to bits 13..7, are
+// the f16 whose exponent field is the e4m3 one: f16's bias is 15 and e4m3's
+// 7, so the f16 is the e4m3 value times 2^-8, for subnormal codes (exponent
+// 0) too.  The sign-replicating selector nibbles fill bit 15 with the code's
+// sign.  The NaN codes (0x7F, 0xFF) come out as +-1.875 (480 before scaling).
+// PRMT, shift and AND run on the integer pipe at about twice the
+// conversion unit's rate.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_div256(uint32_t w, uint32_t sel) {
+    uint32_t x;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(x) : "r"(w), "r"(sel));
+    return (x << 7) & 0xBF80BF80u;
+}
+constexpr uint32_t kSelDims01 = 0x9180u;  // bytes 0, 1 -> halves, each with its sign byte above
+constexpr uint32_t kSelDims23 = 0xB3A2u;  // bytes 2, 3
 
 template <int NQ, int KP, bool FP8>
 __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, FP8>::ctas_per_sm)
@@ -274,13 +299,14 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
     uint8_t* qs = base + S * C::stage_bytes;  // 1024-aligned (stage bytes are multiples of 1024)
     uint64_t* bars = reinterpret_cast<uint64_t*>(qs + C::q_bytes);
     uint64_t* full = bars;               // [S] TMA landed
-    uint64_t* empty = bars + S;          // [S] MMA done reading
-    uint64_t* conv = bars + 2 * S;       // [S] e4m3 decoded (fp8)
-    uint64_t* tfull = bars + 3 * S;      // [2] accumulator ready
-    uint64_t* tempty = bars + 3 * S + 2; // [2] accumulator drained
-    uint64_t* qfull = bars + 3 * S + 4;
-    uint64_t* qempty = bars + 3 * S + 5;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 6);
+    uint64_t* empty = bars + S;          // [S] stage read (bf16: by the MMA; e4m3: by the decoders)
+    uint64_t* tfull = bars + 2 * S;      // [2] accumulator ready
+    uint64_t* tempty = bars + 2 * S + 2; // [2] accumulator drained
+    uint64_t* aconv = bars + 2 * S + 4;  // [4] e4m3: key operand decoded into TMEM
+    uint64_t* aempty = bars + 2 * S + 8; // [4] e4m3: MMA done reading the key operand
+    uint64_t* qfull = bars + 2 * S + 12;
+    uint64_t* qempty = bars + 2 * S + 13;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 14);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     float* sw_all = reinterpret_cast<float*>(tmem_slot + 2);  // [4][NQ*32] head weights, one copy per epilogue warp
     int* spos_all = reinterpret_cast<int*>(sw_all + 4 * NQ * kIH);  // [4][NQ] query positions
@@ -292,12 +318,15 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             ptx::mbar_init(full + i, 1);
-            ptx::mbar_init(empty + i, 1);
-            ptx::mbar_init(conv + i, 4);
+            ptx::mbar_init(empty + i, FP8 ? 4 : 1);
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(tfull + i, 1);
             ptx::mbar_init(tempty + i, 4);
+        }
+        for (int i = 0; i < 4; ++i) {
+            ptx::mbar_init(aconv + i, 4);
+            ptx::mbar_init(aempty + i, 1);
         }
         ptx::mbar_init(qfull, 1);
         ptx::mbar_init(qempty, 1);
@@ -398,6 +427,8 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
         bool have = wk.next(s, 2, d_status, false, seg, j0, kind);
         int q_seg = -1, qloads = 0;
         int64_t consumed = 0;
+        int st = 0, a = 0, ab = 0;         // ring stage, accumulator, key operand buffer
+        uint32_t use = 0, au = 0, abu = 0;  // and how often each has come round
         while (have) {
             const bool have_next = wk.next(s, 2, d_status, false, nseg, nj0, nkind);
             if (seg != q_seg) {
@@ -405,26 +436,33 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
                 ++qloads;
                 q_seg = seg;
             }
-            const int st = (int)(consumed % S);
-            const uint32_t use = (uint32_t)(consumed / S);
-            if (!ptx::mbar_wait(FP8 ? conv + st : full + st, use & 1, abort_flag, d_status)) break;
-            const int a = (int)(consumed & 1);
-            const uint32_t au = (uint32_t)(consumed >> 1);
-            if (consumed >= 2 && !ptx::mbar_wait(tempty + a, (au - 1) & 1, abort_flag, d_status)) break;
+            if (!(FP8 ? ptx::mbar_wait(aconv + ab, abu & 1, abort_flag, d_status)
+                      : ptx::mbar_wait(full + st, use & 1, abort_flag, d_status)))
+                break;
+            if (consumed >= C::nacc && !ptx::mbar_wait(tempty + a, (au - 1) & 1, abort_flag, d_status)) break;
             ptx::tc_fence_after();
-            const uint32_t kbase = smem_u32(stages + st * C::stage_bytes + StageBytes<FP8>::raw);
+            const uint32_t kbase = smem_u32(stages + st * C::stage_bytes);
             const uint32_t qbase = smem_u32(qs);
 #pragma unroll
             for (int ks = 0; ks < KP / 16; ++ks) {
                 int kd;  // key dim of this k-step: [hi | lo | unrotated] all read dims 0..63, 0..63, 64..127
                 if (KP == 192) kd = ks < 4 ? ks * 16 : (ks < 8 ? (ks - 4) * 16 : 64 + (ks - 8) * 16);
                 else kd = ks * 16;
-                const uint64_t ad = ptx::sdesc_sw128(kbase + (kd >> 6) * (kTileKeys * 128) + (kd & 63) * 2);
                 const uint64_t bd = ptx::sdesc_sw128(qbase + ((ks * 16) >> 6) * (N * 128) + ((ks * 16) & 63) * 2);
-                ptx::mma_ss(tmem_base + a * N, ad, bd, idesc, ks > 0 ? 1u : 0u);
+                if (FP8) {
+                    // key operand from TMEM: two f16 dims per column
+                    ptx::mma_ts(tmem_base + a * N, tmem_base + C::a_col + ab * 64 + (kd >> 1), bd, idesc,
+                                ks > 0 ? 1u : 0u);
+                } else {
+                    const uint64_t ad = ptx::sdesc_sw128(kbase + (kd >> 6) * (kTileKeys * 128) + (kd & 63) * 2);
+                    ptx::mma_ss(tmem_base + a * N, ad, bd, idesc, ks > 0 ? 1u : 0u);
+                }
             }
-            ptx::mma_commit(empty + st);
+            ptx::mma_commit(FP8 ? aempty + ab : empty + st);
             ptx::mma_commit(tfull + a);
+            if (++st == S) { st = 0; ++use; }
+            if (++a == C::nacc) { a = 0; ++au; }
+            if (++ab == C::na) { ab = 0; ++abu; }
             if (!have_next || nseg != seg) ptx::mma_commit(qempty);
             ++consumed;
             have = have_next;
@@ -482,8 +520,8 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
             }
             float sigma = 1.f;
             if (FP8) sigma = prow >= 0 ? __ldg(k_scale + prow) : 0.f;
-            const int a = (int)(consumed & 1);
-            const uint32_t au = (uint32_t)(consumed >> 1);
+            const int a = (int)(consumed % C::nacc);
+            const uint32_t au = (uint32_t)(consumed / C::nacc);
             // warp-uniform outcome: a lane that sees an abort takes the whole warp out
             if (!__all_sync(0xffffffffu, ptx::mbar_wait(tfull + a, au & 1, abort_flag, d_status))) break;
             ptx::tc_fence_after();
@@ -492,6 +530,7 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
                 report(d_status, DSA_ERR_BAD_INPUT);
                 sigma = 0.f;
             }
+            if (FP8) sigma *= 256.f;  // the decoded keys are 2^-8 times the codes' values
 #pragma unroll 1
             for (int q = 0; q < NQ; ++q) {
                 float v[32];
@@ -508,37 +547,50 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
             ++consumed;
         }
     } else if (FP8 && warp >= 6) {
-        // ------------------------------------------------------------ e4m3 -> f16 (exact)
-        const int r = threadIdx.x - 192;  // key row of the tile
+        // ------------------------------------------------------------ e4m3 -> f16 x 2^-8 into TMEM
+        // Thread = key row = TMEM lane (a warp reaches its own lane quarter).
+        // The 128-byte swizzle puts the row's 16-byte chunk i at i ^ (row & 7),
+        // so the warp's 16-byte reads spread over all banks.
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t lane_cols = tmem_base + ((uint32_t)(quarter * 32) << 16) + C::a_col;
         TileWalker<NQ> wk(t_begin, t_end, tiles_per_seq, chunks);
         int seg, j0, kind;
         int64_t n = 0;
+        int st = 0, ab = 0;
+        uint32_t use = 0, abu = 0;
         while (wk.next(s, 2, d_status, false, seg, j0, kind)) {
-            const int st = (int)(n % S);
-            const uint32_t use = (uint32_t)(n / S);
             if (!__all_sync(0xffffffffu, ptx::mbar_wait(full + st, use & 1, abort_flag, d_status))) break;
-            const uint8_t* raw = stages + st * C::stage_bytes + r * kID;
-            uint8_t* out = stages + st * C::stage_bytes + StageBytes<FP8>::raw;
+            const uint8_t* rowp = stages + st * C::stage_bytes + r * 128;
+            uint4 c[8];
 #pragma unroll
-            for (int step = 0; step < 8; ++step) {
-                const int i = (step + r) & 7;  // 16 codes -> dims 16i .. 16i+15
-                const uint4 c = *reinterpret_cast<const uint4*>(raw + i * 16);
-                const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
-                uint32_t h[8];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    h[2 * u] = e4m3x2_to_f16x2((uint16_t)(w4[u] & 0xFFFF));
-                    h[2 * u + 1] = e4m3x2_to_f16x2((uint16_t)(w4[u] >> 16));
-                }
-                const int kb = i >> 2, c0 = (i & 3) * 2;
-                uint8_t* rowp = out + kb * (kTileKeys * 128) + r * 128;
-                *reinterpret_cast<uint4*>(rowp + ((c0 ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
-            }
-            ptx::fence_proxy_async_smem();
+            for (int i = 0; i < 8; ++i) c[i] = *reinterpret_cast<const uint4*>(rowp + ((i ^ (r & 7)) << 4));
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(conv + st);
+            if (lane == 0) ptx::mbar_arrive(empty + st);
+            // the MMAs that read this operand buffer last time have completed
+            if (n >= C::na &&
+                !__all_sync(0xffffffffu, ptx::mbar_wait(aempty + ab, (abu - 1) & 1, abort_flag, d_status)))
+                break;
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {  // dims 32g .. 32g+31 -> columns 16g .. 16g+15
+                const uint32_t w[8] = {c[2 * g].x,     c[2 * g].y,     c[2 * g].z,     c[2 * g].w,
+                                       c[2 * g + 1].x, c[2 * g + 1].y, c[2 * g + 1].z, c[2 * g + 1].w};
+                uint32_t v[16];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    v[2 * u] = e4m3x2_to_f16x2_div256(w[u], kSelDims01);
+                    v[2 * u + 1] = e4m3x2_to_f16x2_div256(w[u], kSelDims23);
+                }
+                ptx::tmem_st16_async(lane_cols + ab * 64 + g * 16, v);
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(aconv + ab);
             ++n;
+            if (++st == S) { st = 0; ++use; }
+            if (++ab == C::na) { ab = 0; ++abu; }
         }
     }
     ptx::tc_fence_before();
@@ -596,7 +648,7 @@ cudaError_t launch_tc(const void* qp, int num_q, const float* wp, const void* k_
     cudaError_t e;
     if (FP8)
         e = make_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, k_idx, kID, (uint64_t)s.num_rows, kID, kID, box_rows,
-                     CU_TENSOR_MAP_SWIZZLE_NONE);
+                     CU_TENSOR_MAP_SWIZZLE_128B);
     else
         e = make_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_idx, kID, (uint64_t)s.num_rows, kID * 2, 64,
                      box_rows, CU_TENSOR_MAP_SWIZZLE_128B);

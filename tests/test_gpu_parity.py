@@ -199,6 +199,26 @@ def test_long_rows_all_equal_scores():
         assert np.array_equal(idx[t], np.arange(2048))
 
 
+def test_fp8_index_keys_every_code_class():
+    """e4m3 index keys of one sequence drawn from the subnormal codes (and
+    zero) alone, of the other from every finite code: scores, selection and
+    attention match the oracle for each, so a decode that flushed subnormals
+    or misplaced a sign, exponent or mantissa bit fails."""
+    wl = I.scaled(W["long_fp8"], num_seqs=2, ctx=None, ctx_list=(3000, 2100))
+    d, _ = _inputs_cpu_then_gpu(wl)
+    g = torch.Generator().manual_seed(7)
+    sub = torch.tensor(list(range(8)) + [0x80 + c for c in range(8)], dtype=torch.uint8)
+    fin = torch.tensor([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=torch.uint8)
+    codes = d["k_idx"].cpu()
+    for b, pool in enumerate((sub, fin)):
+        rows = P.seq_rows_host(d, b)
+        codes[rows] = pool[torch.randint(0, len(pool), (len(rows), 128), generator=g)]
+    d["k_idx"].copy_(codes.to(DEV))
+    reps = _check_workload(d, wl, list(range(wl.num_queries)))
+    worst = max(r["score_rel_err"] for r in reps)
+    assert worst < 1e-4, f"scores should be near fp32 accuracy, got {worst:.2e}"
+
+
 def test_all_equal_scores_take_smallest_indices():
     """w = 0 makes every score 0: the selection is positions 0..k-1."""
     wl = I.scaled(W["tiny"], num_seqs=1, ctx=5000, queries_per_seq=2)
