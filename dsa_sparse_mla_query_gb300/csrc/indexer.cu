@@ -235,34 +235,55 @@ struct TileWalker {
     }
 };
 
+// Per contracted tile, the producer hands the epilogue, through a ring of
+// shared-memory slots, the physical row of each TMA box (-1: not loaded) and,
+// for e4m3 keys, the 128 row scales, copied asynchronously (cp.async, tracked
+// by the slot's barrier).  The epilogue then makes no global load per tile:
+// under a saturated HBM a dependent load takes longer than a tile.
+constexpr int kInfoSlots = 16;  // > stages + key operand buffers + accumulators: never the bottleneck
+template <bool FP8>
+struct TileInfo {
+    static constexpr int bytes = 64 + (FP8 ? kTileKeys * 4 : 0);  // int64 box_base[8]; float scale[128]
+};
+
 template <int NQ, int KP, bool FP8>
 struct IdxCfg {
     static constexpr int N = NQ * kIH;
-    static constexpr int q_bytes = N * KP * 2;                         // KP/64 blocks of N x 128 B
+    // e4m3 keys, one rotated query: q''s hi and lo parts are stacked along N
+    // (rows 0-31 hi, 32-63 lo; the lo rows are zero on the unrotated dims) and
+    // contracted in one K = 128 pass over the key, 8 MMAs of N = 64 per tile
+    // instead of 12 of N = 32: at N <= 64 an MMA's cost is mostly per
+    // instruction, and this path is bound by them.
+    static constexpr bool ST = FP8 && KP == 192 && NQ == 1;
+    static constexpr int NM = ST ? 2 * N : N;   // MMA N = accumulator columns per buffer
+    static constexpr int KM = ST ? 128 : KP;     // MMA K
+    static constexpr int q_tma_bytes = N * KP * 2;                     // KP/64 blocks of N x 128 B
+    static constexpr int q_bytes = q_tma_bytes + (ST ? N * 128 : 0);  // + the zero block
     // bf16: two 128-byte swizzled 64-dim blocks; e4m3: the raw codes, one
     // 128-byte (swizzled) row per key
     static constexpr int stage_bytes = FP8 ? kTileKeys * kID : kTileKeys * kID * 2;
-    static constexpr int tail_raw = (2 * 8 + 14) * 8 + 8 + 4 * NQ * kIH * 4 + 4 * NQ * 4;
+    static constexpr int info_bytes = kInfoSlots * TileInfo<FP8>::bytes;
+    static constexpr int tail_raw = (2 * 8 + 14 + 2 * kInfoSlots) * 8 + 16 + 4 * NQ * kIH * 4 + 4 * NQ * 4;
     static constexpr int tail = (tail_raw + 1023) / 1024 * 1024;  // barriers, TMEM slot, per-warp weights
     // Decode shapes (small q') run two persistent CTAs per SM, so two
     // producer / MMA-issuer pairs overlap their per-tile issue work: when two
     // CTAs' stages fit and, for e4m3 keys, both accumulators and two 64-column
     // key operands fit in half the TMEM.
-    static constexpr bool two_fit = (110 * 1024 - q_bytes - 1024 - tail) / stage_bytes >= 2 &&
-                                    (!FP8 || 2 * N + 2 * 64 <= 256);
+    static constexpr bool two_fit = (110 * 1024 - q_bytes - info_bytes - 1024 - tail) / stage_bytes >= 2 &&
+                                    (!FP8 || 2 * NM + 2 * 64 <= 256);
     static constexpr int ctas_per_sm = two_fit ? 2 : 1;
     static constexpr int budget = (ctas_per_sm == 2 ? 110 : 220) * 1024;
-    static constexpr int stages_fit = (budget - q_bytes - 1024 - tail) / stage_bytes;
+    static constexpr int stages_fit = (budget - q_bytes - info_bytes - 1024 - tail) / stage_bytes;
     static constexpr int S = stages_fit > 8 ? 8 : stages_fit;
     static constexpr int threads = FP8 ? 320 : 192;
     static constexpr int tmem_cols = FP8 ? (ctas_per_sm == 2 ? 256 : 512) : (2 * N < 32 ? 32 : 2 * N);
-    // accumulator buffers (columns [0, nacc N)), then (e4m3) na key operand
+    // accumulator buffers (columns [0, nacc NM)), then (e4m3) na key operand
     // buffers of 64 columns: 128 keys x 128 f16 dims
-    static constexpr int nacc = (!FP8 || 2 * N + 2 * 64 <= tmem_cols) ? 2 : 1;
-    static constexpr int na_fit = FP8 ? (tmem_cols - nacc * N) / 64 : 0;
+    static constexpr int nacc = (!FP8 || 2 * NM + 2 * 64 <= tmem_cols) ? 2 : 1;
+    static constexpr int na_fit = FP8 ? (tmem_cols - nacc * NM) / 64 : 0;
     static constexpr int na = na_fit > 4 ? 4 : na_fit;
-    static constexpr int a_col = nacc * N;
-    static constexpr size_t smem = 1024 + (size_t)S * stage_bytes + q_bytes + tail;  // + alignment slack
+    static constexpr int a_col = nacc * NM;
+    static constexpr size_t smem = 1024 + (size_t)S * stage_bytes + q_bytes + info_bytes + tail;  // + alignment slack
     static_assert(S >= 2, "too little shared memory for two stages");
     static_assert(!FP8 || na >= 2, "too little TMEM for two key operand buffers");
 };
@@ -297,7 +318,8 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = base;
     uint8_t* qs = base + S * C::stage_bytes;  // 1024-aligned (stage bytes are multiples of 1024)
-    uint64_t* bars = reinterpret_cast<uint64_t*>(qs + C::q_bytes);
+    uint8_t* info = qs + C::q_bytes;  // [kInfoSlots] TileInfo
+    uint64_t* bars = reinterpret_cast<uint64_t*>(info + C::info_bytes);
     uint64_t* full = bars;               // [S] TMA landed
     uint64_t* empty = bars + S;          // [S] stage read (bf16: by the MMA; e4m3: by the decoders)
     uint64_t* tfull = bars + 2 * S;      // [2] accumulator ready
@@ -306,9 +328,11 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
     uint64_t* aempty = bars + 2 * S + 8; // [4] e4m3: MMA done reading the key operand
     uint64_t* qfull = bars + 2 * S + 12;
     uint64_t* qempty = bars + 2 * S + 13;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 14);
+    uint64_t* ifull = bars + 2 * S + 14;                // [kInfoSlots] tile info written (and scales landed)
+    uint64_t* iempty = bars + 2 * S + 14 + kInfoSlots;  // [kInfoSlots] tile info read
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 14 + 2 * kInfoSlots);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    float* sw_all = reinterpret_cast<float*>(tmem_slot + 2);  // [4][NQ*32] head weights, one copy per epilogue warp
+    float* sw_all = reinterpret_cast<float*>(tmem_slot + 4);  // [4][NQ*32] head weights, one copy per epilogue warp
     int* spos_all = reinterpret_cast<int*>(sw_all + 4 * NQ * kIH);  // [4][NQ] query positions
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -328,6 +352,10 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
             ptx::mbar_init(aconv + i, 4);
             ptx::mbar_init(aempty + i, 1);
         }
+        for (int i = 0; i < kInfoSlots; ++i) {
+            ptx::mbar_init(ifull + i, FP8 ? 33 : 1);  // lane 0, plus each lane's scale copies (e4m3)
+            ptx::mbar_init(iempty + i, 4);
+        }
         ptx::mbar_init(qfull, 1);
         ptx::mbar_init(qempty, 1);
         *abort_flag = 0;
@@ -336,6 +364,12 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
     if (warp == 1) {
         ptx::tmem_alloc(tmem_slot, C::tmem_cols);
         ptx::tmem_relinquish();
+    }
+    if (C::ST) {
+        // the lo rows' unrotated dims: a zero block after the three loaded ones
+        for (int i = threadIdx.x; i < N * 128 / 16; i += blockDim.x)
+            reinterpret_cast<uint4*>(qs + C::q_tma_bytes)[i] = make_uint4(0u, 0u, 0u, 0u);
+        ptx::fence_proxy_async_smem();
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -364,7 +398,7 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
                 if (lane == 0) {
                     ok = qloads == 0 || ptx::mbar_wait(qempty, (qloads - 1) & 1, abort_flag, d_status);
                     if (ok) {
-                        ptx::mbar_expect_tx(qfull, C::q_bytes);
+                        ptx::mbar_expect_tx(qfull, C::q_tma_bytes);
                         for (int kb = 0; kb < KP / 64; ++kb)
                             ptx::tma_load_2d(qs + kb * N * 128, &qmap, kb * 64, g.q0 * kIH, qfull);
                     }
@@ -374,8 +408,9 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
                 ++qloads;
             }
             // One TMA box per lane: lane L takes row block L >> 1 (L for e4m3)
-            // and, for bf16, K-half L & 1.  Rows past the context or behind an
-            // invalid page are not loaded (the epilogue masks and reports them).
+            // and, for bf16, K-half L & 1.  Blocks past the context or behind an
+            // invalid page are not loaded (the epilogue masks and reports them);
+            // rows of a block past the end of the cache read as zeros.
             const int jn = min(kTileKeys, g.ctx - j0);
             const int rb = FP8 ? lane : (lane >> 1), half = FP8 ? 0 : (lane & 1);
             const int j = j0 + rb * box_rows;
@@ -390,24 +425,42 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
                 }
                 const int entry = __shfl_sync(0xffffffffu, win_entry, ((j >> ps_log2) - win_p0) & 31);
                 const int64_t r = ((int64_t)entry << ps_log2) + (j & ps_mask);
-                if (rb < nb && rb * box_rows < jn && entry >= 0 && r + box_rows <= s.num_rows) row = r;
+                if (rb < nb && rb * box_rows < jn && entry >= 0 && r < s.num_rows) row = r;
             } else {
                 const int64_t r = g.base + j;
                 if (rb < nb && rb * box_rows < jn && r >= 0 && r < s.num_rows) row = r;
             }
             const uint32_t loads = __ballot_sync(0xffffffffu, row >= 0);
             const int st = (int)(issued % S);
+            const int is = (int)(issued % kInfoSlots);
             if (lane == 0) {
                 const uint32_t use = (uint32_t)(issued / S);
                 ok = issued < S || ptx::mbar_wait(empty + st, (use - 1) & 1, abort_flag, d_status);
+                if (ok && issued >= kInfoSlots)
+                    ok = ptx::mbar_wait(iempty + is, ((uint32_t)(issued / kInfoSlots) - 1) & 1, abort_flag, d_status);
                 if (ok) ptx::mbar_expect_tx(full + st, (uint32_t)__popc(loads) * box_rows * 128);
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (ok && row >= 0) {
+            if (!ok) break;
+            if (row >= 0) {
                 uint8_t* dst = stages + st * C::stage_bytes + half * (kTileKeys * 128) + rb * box_rows * 128;
                 ptx::tma_load_2d(dst, &kmap, half * 64, (int)row, full + st);
             }
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            uint8_t* ti = info + is * TileInfo<FP8>::bytes;
+            if (half == 0 && rb < 8) reinterpret_cast<int64_t*>(ti)[rb] = row;
+            if (FP8) {
+                float* sc = reinterpret_cast<float*>(ti + 64);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int r = lane + 32 * u;  // key row of the tile
+                    const int64_t bb = __shfl_sync(0xffffffffu, row, r / box_rows);
+                    const int64_t pr = bb + (r & (box_rows - 1));
+                    if (bb >= 0 && pr < s.num_rows) ptx::cp_async4(sc + r, k_scale + pr);
+                }
+                ptx::cp_async_arrive_noinc(ifull + is);
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ifull + is);
             ++issued;
         }
         // drain: every issued copy has landed and every MMA reading a stage is done
@@ -419,9 +472,10 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
             }
             if (qloads > 0) ptx::mbar_drain(qempty, (qloads - 1) & 1);
         }
+        ptx::cp_async_wait_all();
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = ptx::idesc_f16_m128(N, !FP8);
+        constexpr uint32_t idesc = ptx::idesc_f16_m128(C::NM, !FP8);
         TileWalker<NQ> wk(t_begin, t_end, tiles_per_seq, chunks);
         int seg, j0, kind, nseg, nj0, nkind;
         bool have = wk.next(s, 2, d_status, false, seg, j0, kind);
@@ -444,18 +498,27 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
             const uint32_t kbase = smem_u32(stages + st * C::stage_bytes);
             const uint32_t qbase = smem_u32(qs);
 #pragma unroll
-            for (int ks = 0; ks < KP / 16; ++ks) {
-                int kd;  // key dim of this k-step: [hi | lo | unrotated] all read dims 0..63, 0..63, 64..127
-                if (KP == 192) kd = ks < 4 ? ks * 16 : (ks < 8 ? (ks - 4) * 16 : 64 + (ks - 8) * 16);
-                else kd = ks * 16;
-                const uint64_t bd = ptx::sdesc_sw128(qbase + ((ks * 16) >> 6) * (N * 128) + ((ks * 16) & 63) * 2);
+            for (int ks = 0; ks < C::KM / 16; ++ks) {
+                int kd;          // key dim of this k-step
+                uint32_t boff;   // and where its q' slice starts
+                if (C::ST) {
+                    // blocks [hi; lo] (64 rows) for dims 0..63, [unrotated; zero] for 64..127
+                    kd = ks * 16;
+                    boff = (ks >> 2) * (2 * N * 128) + (ks & 3) * 32;
+                } else {
+                    // [hi | lo | unrotated] read key dims 0..63, 0..63, 64..127
+                    if (KP == 192) kd = ks < 4 ? ks * 16 : (ks < 8 ? (ks - 4) * 16 : 64 + (ks - 8) * 16);
+                    else kd = ks * 16;
+                    boff = ((ks * 16) >> 6) * (N * 128) + ((ks * 16) & 63) * 2;
+                }
+                const uint64_t bd = ptx::sdesc_sw128(qbase + boff);
                 if (FP8) {
                     // key operand from TMEM: two f16 dims per column
-                    ptx::mma_ts(tmem_base + a * N, tmem_base + C::a_col + ab * 64 + (kd >> 1), bd, idesc,
+                    ptx::mma_ts(tmem_base + a * C::NM, tmem_base + C::a_col + ab * 64 + (kd >> 1), bd, idesc,
                                 ks > 0 ? 1u : 0u);
                 } else {
                     const uint64_t ad = ptx::sdesc_sw128(kbase + (kd >> 6) * (kTileKeys * 128) + (kd & 63) * 2);
-                    ptx::mma_ss(tmem_base + a * N, ad, bd, idesc, ks > 0 ? 1u : 0u);
+                    ptx::mma_ss(tmem_base + a * C::NM, ad, bd, idesc, ks > 0 ? 1u : 0u);
                 }
             }
             ptx::mma_commit(FP8 ? aempty + ab : empty + st);
@@ -505,45 +568,88 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
                     for (int q = 0; q < g.nq; ++q) scores[(int64_t)(g.q0 + q) * ld + j] = -INFINITY;
                 continue;
             }
-            // the row's physical location and scale load while the MMA runs
-            int64_t prow = -1;
-            if (in_ctx) {
-                if (s.page_table) {
-                    const int ps_log2 = __ffs(s.page_size) - 1;
-                    const int p = j >> ps_log2;
-                    const int64_t page = p < s.max_pages ? __ldg(s.page_table + (int64_t)g.b * s.max_pages + p) : -1;
-                    prow = page >= 0 ? (page << ps_log2) + (j & ((1 << ps_log2) - 1)) : -1;
-                } else {
-                    prow = g.base + j;
-                }
-                if (prow >= s.num_rows) prow = -1;
+            // this row's physical location and scale, from the producer
+            const int is = (int)(consumed % kInfoSlots);
+            if (!__all_sync(0xffffffffu,
+                            ptx::mbar_wait(ifull + is, (uint32_t)(consumed / kInfoSlots) & 1, abort_flag, d_status)))
+                break;
+            const uint8_t* ti = info + is * TileInfo<FP8>::bytes;
+            const int64_t bb = reinterpret_cast<const int64_t*>(ti)[row / box_rows];
+            int64_t prow = bb >= 0 ? bb + (row & (box_rows - 1)) : -1;
+            if (prow >= s.num_rows) prow = -1;
+            float sigma = FP8 ? reinterpret_cast<const float*>(ti + 64)[row] : 1.f;
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(iempty + is);
+            if (in_ctx && prow < 0) report(d_status, DSA_ERR_BAD_INPUT);
+            if (FP8 && prow >= 0 && sigma < 0.f) {
+                report(d_status, DSA_ERR_BAD_INPUT);
+                sigma = 0.f;
             }
-            float sigma = 1.f;
-            if (FP8) sigma = prow >= 0 ? __ldg(k_scale + prow) : 0.f;
+            if (FP8) sigma *= 256.f;  // the decoded keys are 2^-8 times the codes' values
             const int a = (int)(consumed % C::nacc);
             const uint32_t au = (uint32_t)(consumed / C::nacc);
             // warp-uniform outcome: a lane that sees an abort takes the whole warp out
             if (!__all_sync(0xffffffffu, ptx::mbar_wait(tfull + a, au & 1, abort_flag, d_status))) break;
             ptx::tc_fence_after();
-            if (in_ctx && prow < 0) report(d_status, DSA_ERR_BAD_INPUT);
-            if (FP8 && sigma < 0.f) {
-                report(d_status, DSA_ERR_BAD_INPUT);
-                sigma = 0.f;
-            }
-            if (FP8) sigma *= 256.f;  // the decoded keys are 2^-8 times the codes' values
+            const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + a * C::NM;
+            // relu-weighted sum over the 32 heads of query q
+            auto reduce = [&](int q) -> float {
+                const float4* w4 = reinterpret_cast<const float4*>(sw + q * kIH);
+                float r = 0.f;
+                if (C::ST) {
+                    // dot product of head h = hi part (column h) + lo part (column 32 + h)
 #pragma unroll 1
-            for (int q = 0; q < NQ; ++q) {
-                float v[32];
-                ptx::tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + a * N + q * 32, v);
-                float acc = 0.f;
+                    for (int h0 = 0; h0 < 32; h0 += 16) {
+                        float hi[16], lo[16];
+                        ptx::tmem_ld16(tcol + h0, hi);
+                        ptx::tmem_ld16(tcol + 32 + h0, lo);
 #pragma unroll
-                for (int h = 0; h < 32; ++h) acc = fmaf(sw[q * kIH + h], fmaxf(v[h], 0.f), acc);
+                        for (int h = 0; h < 16; h += 4) {
+                            const float4 w = w4[(h0 + h) >> 2];
+                            r = fmaf(w.x, fmaxf(hi[h] + lo[h], 0.f), r);
+                            r = fmaf(w.y, fmaxf(hi[h + 1] + lo[h + 1], 0.f), r);
+                            r = fmaf(w.z, fmaxf(hi[h + 2] + lo[h + 2], 0.f), r);
+                            r = fmaf(w.w, fmaxf(hi[h + 3] + lo[h + 3], 0.f), r);
+                        }
+                    }
+                } else {
+                    float v[32];
+                    ptx::tmem_ld32(tcol + q * 32, v);
+#pragma unroll
+                    for (int h = 0; h < 32; h += 4) {
+                        const float4 w = w4[h >> 2];
+                        r = fmaf(w.x, fmaxf(v[h], 0.f), r);
+                        r = fmaf(w.y, fmaxf(v[h + 1], 0.f), r);
+                        r = fmaf(w.z, fmaxf(v[h + 2], 0.f), r);
+                        r = fmaf(w.w, fmaxf(v[h + 3], 0.f), r);
+                    }
+                }
+                return r;
+            };
+            auto store = [&](int q, float r) {
                 if (in_ctx && q < g.nq)
-                    scores[(int64_t)(g.q0 + q) * ld + j] = (prow >= 0 && j <= spos[q]) ? acc * sigma : -INFINITY;
+                    scores[(int64_t)(g.q0 + q) * ld + j] = (prow >= 0 && j <= spos[q]) ? r * sigma : -INFINITY;
+            };
+            auto release = [&] {
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(tempty + a);
+            };
+            // Where the registers allow (both queries' sums under the fp8
+            // kernel's 96-register cap is too many), the accumulator goes
+            // back to the MMA before the stores.
+            if constexpr (NQ == 1 || (NQ == 2 && !FP8)) {
+                float acc[NQ];
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) acc[q] = reduce(q);
+                release();
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) store(q, acc[q]);
+            } else {
+#pragma unroll 1
+                for (int q = 0; q < NQ; ++q) store(q, reduce(q));
+                release();
             }
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(tempty + a);
             ++consumed;
         }
     } else if (FP8 && warp >= 6) {
