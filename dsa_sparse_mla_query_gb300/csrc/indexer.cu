@@ -249,16 +249,7 @@ struct TileInfo {
 template <int NQ, int KP, bool FP8>
 struct IdxCfg {
     static constexpr int N = NQ * kIH;
-    // e4m3 keys, one rotated query: q''s hi and lo parts are stacked along N
-    // (rows 0-31 hi, 32-63 lo; the lo rows are zero on the unrotated dims) and
-    // contracted in one K = 128 pass over the key, 8 MMAs of N = 64 per tile
-    // instead of 12 of N = 32: at N <= 64 an MMA's cost is mostly per
-    // instruction, and this path is bound by them.
-    static constexpr bool ST = FP8 && KP == 192 && NQ == 1;
-    static constexpr int NM = ST ? 2 * N : N;   // MMA N = accumulator columns per buffer
-    static constexpr int KM = ST ? 128 : KP;     // MMA K
-    static constexpr int q_tma_bytes = N * KP * 2;                     // KP/64 blocks of N x 128 B
-    static constexpr int q_bytes = q_tma_bytes + (ST ? N * 128 : 0);  // + the zero block
+    static constexpr int q_bytes = N * KP * 2;  // KP/64 blocks of N x 128 B
     // bf16: two 128-byte swizzled 64-dim blocks; e4m3: the raw codes, one
     // 128-byte (swizzled) row per key
     static constexpr int stage_bytes = FP8 ? kTileKeys * kID : kTileKeys * kID * 2;
@@ -270,19 +261,19 @@ struct IdxCfg {
     // CTAs' stages fit and, for e4m3 keys, both accumulators and two 64-column
     // key operands fit in half the TMEM.
     static constexpr bool two_fit = (110 * 1024 - q_bytes - info_bytes - 1024 - tail) / stage_bytes >= 2 &&
-                                    (!FP8 || 2 * NM + 2 * 64 <= 256);
+                                    (!FP8 || 2 * N + 2 * 64 <= 256);
     static constexpr int ctas_per_sm = two_fit ? 2 : 1;
     static constexpr int budget = (ctas_per_sm == 2 ? 110 : 220) * 1024;
     static constexpr int stages_fit = (budget - q_bytes - info_bytes - 1024 - tail) / stage_bytes;
     static constexpr int S = stages_fit > 8 ? 8 : stages_fit;
     static constexpr int threads = FP8 ? 320 : 192;
     static constexpr int tmem_cols = FP8 ? (ctas_per_sm == 2 ? 256 : 512) : (2 * N < 32 ? 32 : 2 * N);
-    // accumulator buffers (columns [0, nacc NM)), then (e4m3) na key operand
+    // accumulator buffers (columns [0, nacc N)), then (e4m3) na key operand
     // buffers of 64 columns: 128 keys x 128 f16 dims
-    static constexpr int nacc = (!FP8 || 2 * NM + 2 * 64 <= tmem_cols) ? 2 : 1;
-    static constexpr int na_fit = FP8 ? (tmem_cols - nacc * NM) / 64 : 0;
+    static constexpr int nacc = (!FP8 || 2 * N + 2 * 64 <= tmem_cols) ? 2 : 1;
+    static constexpr int na_fit = FP8 ? (tmem_cols - nacc * N) / 64 : 0;
     static constexpr int na = na_fit > 4 ? 4 : na_fit;
-    static constexpr int a_col = nacc * NM;
+    static constexpr int a_col = nacc * N;
     static constexpr size_t smem = 1024 + (size_t)S * stage_bytes + q_bytes + info_bytes + tail;  // + alignment slack
     static_assert(S >= 2, "too little shared memory for two stages");
     static_assert(!FP8 || na >= 2, "too little TMEM for two key operand buffers");
@@ -365,12 +356,6 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
         ptx::tmem_alloc(tmem_slot, C::tmem_cols);
         ptx::tmem_relinquish();
     }
-    if (C::ST) {
-        // the lo rows' unrotated dims: a zero block after the three loaded ones
-        for (int i = threadIdx.x; i < N * 128 / 16; i += blockDim.x)
-            reinterpret_cast<uint4*>(qs + C::q_tma_bytes)[i] = make_uint4(0u, 0u, 0u, 0u);
-        ptx::fence_proxy_async_smem();
-    }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -398,7 +383,7 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
                 if (lane == 0) {
                     ok = qloads == 0 || ptx::mbar_wait(qempty, (qloads - 1) & 1, abort_flag, d_status);
                     if (ok) {
-                        ptx::mbar_expect_tx(qfull, C::q_tma_bytes);
+                        ptx::mbar_expect_tx(qfull, C::q_bytes);
                         for (int kb = 0; kb < KP / 64; ++kb)
                             ptx::tma_load_2d(qs + kb * N * 128, &qmap, kb * 64, g.q0 * kIH, qfull);
                     }
@@ -475,7 +460,7 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
         ptx::cp_async_wait_all();
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = ptx::idesc_f16_m128(C::NM, !FP8);
+        constexpr uint32_t idesc = ptx::idesc_f16_m128(N, !FP8);
         TileWalker<NQ> wk(t_begin, t_end, tiles_per_seq, chunks);
         int seg, j0, kind, nseg, nj0, nkind;
         bool have = wk.next(s, 2, d_status, false, seg, j0, kind);
@@ -498,27 +483,18 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
             const uint32_t kbase = smem_u32(stages + st * C::stage_bytes);
             const uint32_t qbase = smem_u32(qs);
 #pragma unroll
-            for (int ks = 0; ks < C::KM / 16; ++ks) {
-                int kd;          // key dim of this k-step
-                uint32_t boff;   // and where its q' slice starts
-                if (C::ST) {
-                    // blocks [hi; lo] (64 rows) for dims 0..63, [unrotated; zero] for 64..127
-                    kd = ks * 16;
-                    boff = (ks >> 2) * (2 * N * 128) + (ks & 3) * 32;
-                } else {
-                    // [hi | lo | unrotated] read key dims 0..63, 0..63, 64..127
-                    if (KP == 192) kd = ks < 4 ? ks * 16 : (ks < 8 ? (ks - 4) * 16 : 64 + (ks - 8) * 16);
-                    else kd = ks * 16;
-                    boff = ((ks * 16) >> 6) * (N * 128) + ((ks * 16) & 63) * 2;
-                }
-                const uint64_t bd = ptx::sdesc_sw128(qbase + boff);
+            for (int ks = 0; ks < KP / 16; ++ks) {
+                int kd;  // key dim of this k-step: [hi | lo | unrotated] read dims 0..63, 0..63, 64..127
+                if (KP == 192) kd = ks < 4 ? ks * 16 : (ks < 8 ? (ks - 4) * 16 : 64 + (ks - 8) * 16);
+                else kd = ks * 16;
+                const uint64_t bd = ptx::sdesc_sw128(qbase + ((ks * 16) >> 6) * (N * 128) + ((ks * 16) & 63) * 2);
                 if (FP8) {
                     // key operand from TMEM: two f16 dims per column
-                    ptx::mma_ts(tmem_base + a * C::NM, tmem_base + C::a_col + ab * 64 + (kd >> 1), bd, idesc,
+                    ptx::mma_ts(tmem_base + a * N, tmem_base + C::a_col + ab * 64 + (kd >> 1), bd, idesc,
                                 ks > 0 ? 1u : 0u);
                 } else {
                     const uint64_t ad = ptx::sdesc_sw128(kbase + (kd >> 6) * (kTileKeys * 128) + (kd & 63) * 2);
-                    ptx::mma_ss(tmem_base + a * C::NM, ad, bd, idesc, ks > 0 ? 1u : 0u);
+                    ptx::mma_ss(tmem_base + a * N, ad, bd, idesc, ks > 0 ? 1u : 0u);
                 }
             }
             ptx::mma_commit(FP8 ? aempty + ab : empty + st);
@@ -591,38 +567,20 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
             // warp-uniform outcome: a lane that sees an abort takes the whole warp out
             if (!__all_sync(0xffffffffu, ptx::mbar_wait(tfull + a, au & 1, abort_flag, d_status))) break;
             ptx::tc_fence_after();
-            const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + a * C::NM;
+            const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + a * N;
             // relu-weighted sum over the 32 heads of query q
             auto reduce = [&](int q) -> float {
                 const float4* w4 = reinterpret_cast<const float4*>(sw + q * kIH);
+                float v[32];
+                ptx::tmem_ld32(tcol + q * 32, v);
                 float r = 0.f;
-                if (C::ST) {
-                    // dot product of head h = hi part (column h) + lo part (column 32 + h)
-#pragma unroll 1
-                    for (int h0 = 0; h0 < 32; h0 += 16) {
-                        float hi[16], lo[16];
-                        ptx::tmem_ld16(tcol + h0, hi);
-                        ptx::tmem_ld16(tcol + 32 + h0, lo);
 #pragma unroll
-                        for (int h = 0; h < 16; h += 4) {
-                            const float4 w = w4[(h0 + h) >> 2];
-                            r = fmaf(w.x, fmaxf(hi[h] + lo[h], 0.f), r);
-                            r = fmaf(w.y, fmaxf(hi[h + 1] + lo[h + 1], 0.f), r);
-                            r = fmaf(w.z, fmaxf(hi[h + 2] + lo[h + 2], 0.f), r);
-                            r = fmaf(w.w, fmaxf(hi[h + 3] + lo[h + 3], 0.f), r);
-                        }
-                    }
-                } else {
-                    float v[32];
-                    ptx::tmem_ld32(tcol + q * 32, v);
-#pragma unroll
-                    for (int h = 0; h < 32; h += 4) {
-                        const float4 w = w4[h >> 2];
-                        r = fmaf(w.x, fmaxf(v[h], 0.f), r);
-                        r = fmaf(w.y, fmaxf(v[h + 1], 0.f), r);
-                        r = fmaf(w.z, fmaxf(v[h + 2], 0.f), r);
-                        r = fmaf(w.w, fmaxf(v[h + 3], 0.f), r);
-                    }
+                for (int h = 0; h < 32; h += 4) {
+                    const float4 w = w4[h >> 2];
+                    r = fmaf(w.x, fmaxf(v[h], 0.f), r);
+                    r = fmaf(w.y, fmaxf(v[h + 1], 0.f), r);
+                    r = fmaf(w.z, fmaxf(v[h + 2], 0.f), r);
+                    r = fmaf(w.w, fmaxf(v[h + 3], 0.f), r);
                 }
                 return r;
             };
