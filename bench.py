@@ -83,6 +83,11 @@ def algorithmic_bytes(wl, lay):
     return dict(indexer=indexer, gather=gather, step=keys + qside + gather + mla_small)
 
 
+def indexer_flops(lay):
+    """q.k over 128 dims for 32 heads, per causal (query, key) pair: 2 * 32 * 128 flop."""
+    return sum(p + 1 for p in lay.q_pos) * 2 * 32 * 128
+
+
 # ---------------------------------------------------------------------------
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
@@ -145,6 +150,16 @@ def measured_peaks():
             j = json.load(f)
         return float(j["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def measured_tensor_peak():
+    """dense bf16 (= f16) TFLOP/s, the sustained figure: the indexer is timed inside a long step"""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["bf16_tflops_sustained"]), "measured sustained bf16"
+    return 1700.0, "fallback sustained bf16"
 
 
 def indexer_traffic(wl_name: str):
@@ -331,6 +346,12 @@ def run_ours(args, wl, ws, rank, local):
     peak, peak_kind = measured_peaks()
     achieved = ab["indexer"] / (idx_ms / 1000.0) / 1e9
     traffic = indexer_traffic(wl.name)
+    # The indexer's bound: its bytes at the copy bandwidth or its q.k flops at
+    # the tensor peak, whichever takes longer (the prefill chunk's 4096 queries
+    # share every key, which makes it a dense contraction).
+    flops = indexer_flops(lay)
+    tpeak, tpeak_kind = measured_tensor_peak()
+    tensor_bound = flops / (tpeak * 1e12) > ab["indexer"] / (peak * 1e9)
 
     # ---- end to end through the C ABI with host buffers
     keys = ["q_idx", "w", "q_mla"] + (["q_mla2"] if step.shared else [])
@@ -385,10 +406,18 @@ def run_ours(args, wl, ws, rank, local):
                              % (sum(lay.ctx_len) * index_row_bytes(wl) / 1e6,
                                 lay.num_rows * latent_row_bytes(wl) / 1e6),
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic, "kernel": "indexer (query prep + key scan)",
-                         "algorithmic_bytes_per_launch": ab["indexer"], "ms_per_launch": idx_ms,
-                         "peak_kind": f"{peak_kind} HBM copy"},
+            "roofline": ({"bound": "tensor", "achieved": flops / (idx_ms / 1000.0) / 1e12, "peak": tpeak,
+                          "unit": "TFLOP/s", "frac": flops / (idx_ms / 1000.0) / 1e12 / tpeak, "traffic": traffic,
+                          "kernel": "indexer (query prep + key scan)", "algorithmic_flops_per_launch": flops,
+                          "algorithmic_bytes_per_launch": ab["indexer"], "ms_per_launch": idx_ms,
+                          "peak_kind": tpeak_kind,
+                          "note": "flops of q.k over 128 dims; the kernel's MMAs do %.1fx that%s"
+                                  % ((1.5, " (rotated dims in hi + lo)") if wl.rope else (1.0, ""))}
+                         if tensor_bound else
+                         {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                          "frac": achieved / peak, "traffic": traffic, "kernel": "indexer (query prep + key scan)",
+                          "algorithmic_bytes_per_launch": ab["indexer"], "ms_per_launch": idx_ms,
+                          "peak_kind": f"{peak_kind} HBM copy"}),
             "layer": {"algorithmic_bytes_per_step": ab["step"],
                       "achieved_gbs": ab["step"] / (ms_step / 1000.0) / 1e9,
                       "frac_of_peak": ab["step"] / (ms_step / 1000.0) / 1e9 / peak,

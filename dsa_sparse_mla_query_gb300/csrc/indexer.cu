@@ -254,7 +254,12 @@ struct IdxCfg {
     // 128-byte (swizzled) row per key
     static constexpr int stage_bytes = FP8 ? kTileKeys * kID : kTileKeys * kID * 2;
     static constexpr int info_bytes = kInfoSlots * TileInfo<FP8>::bytes;
-    static constexpr int tail_raw = (2 * 8 + 14 + 2 * kInfoSlots) * 8 + 16 + 4 * NQ * kIH * 4 + 4 * NQ * 4;
+    // epilogue warps: bf16 with several queries and one CTA per SM has warp
+    // slots to spare, so two warps per TMEM lane quarter each reduce half of
+    // the queries (the epilogue, not the MMA, bounds those shapes otherwise)
+    static constexpr int ew_max = (!FP8 && NQ >= 4) ? 8 : 4;
+    static constexpr int tail_raw =
+        (2 * 8 + 14 + 2 * kInfoSlots) * 8 + 16 + ew_max * NQ * kIH * 4 + ew_max * NQ * 4;
     static constexpr int tail = (tail_raw + 1023) / 1024 * 1024;  // barriers, TMEM slot, per-warp weights
     // Decode shapes (small q') run two persistent CTAs per SM, so two
     // producer / MMA-issuer pairs overlap their per-tile issue work: when two
@@ -266,7 +271,9 @@ struct IdxCfg {
     static constexpr int budget = (ctas_per_sm == 2 ? 110 : 220) * 1024;
     static constexpr int stages_fit = (budget - q_bytes - info_bytes - 1024 - tail) / stage_bytes;
     static constexpr int S = stages_fit > 8 ? 8 : stages_fit;
-    static constexpr int threads = FP8 ? 320 : 192;
+    static constexpr int EW = (ew_max == 8 && ctas_per_sm == 1) ? 8 : 4;
+    static constexpr int QPW = NQ * 4 / EW;  // queries per epilogue warp
+    static constexpr int threads = (FP8 || EW == 8) ? 320 : 192;
     static constexpr int tmem_cols = FP8 ? (ctas_per_sm == 2 ? 256 : 512) : (2 * N < 32 ? 32 : 2 * N);
     // accumulator buffers (columns [0, nacc N)), then (e4m3) na key operand
     // buffers of 64 columns: 128 keys x 128 f16 dims
@@ -323,8 +330,8 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
     uint64_t* iempty = bars + 2 * S + 14 + kInfoSlots;  // [kInfoSlots] tile info read
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 14 + 2 * kInfoSlots);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    float* sw_all = reinterpret_cast<float*>(tmem_slot + 4);  // [4][NQ*32] head weights, one copy per epilogue warp
-    int* spos_all = reinterpret_cast<int*>(sw_all + 4 * NQ * kIH);  // [4][NQ] query positions
+    float* sw_all = reinterpret_cast<float*>(tmem_slot + 4);  // [EW][NQ*32] head weights, one copy per epilogue warp
+    int* spos_all = reinterpret_cast<int*>(sw_all + C::EW * NQ * kIH);  // [EW][NQ] query positions
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t_begin = total_tiles * blockIdx.x / gridDim.x;
@@ -337,7 +344,7 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(tfull + i, 1);
-            ptx::mbar_init(tempty + i, 4);
+            ptx::mbar_init(tempty + i, C::EW);
         }
         for (int i = 0; i < 4; ++i) {
             ptx::mbar_init(aconv + i, 4);
@@ -345,7 +352,7 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
         }
         for (int i = 0; i < kInfoSlots; ++i) {
             ptx::mbar_init(ifull + i, FP8 ? 33 : 1);  // lane 0, plus each lane's scale copies (e4m3)
-            ptx::mbar_init(iempty + i, 4);
+            ptx::mbar_init(iempty + i, C::EW);
         }
         ptx::mbar_init(qfull, 1);
         ptx::mbar_init(qempty, 1);
@@ -509,12 +516,14 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
             j0 = nj0;
             kind = nkind;
         }
-    } else if (warp >= 2 && warp < 6) {
+    } else if (warp >= 2 && warp < 2 + C::EW) {
         // ------------------------------------------------------------ epilogue
         // each epilogue warp keeps its own copy of the chunk's weights and
-        // positions, so the warps never wait on each other
+        // positions, so the warps never wait on each other; with eight, the
+        // second four take the upper half of the queries
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
+        const int q_lo = ((warp - 2) >> 2) * C::QPW;
         float* sw = sw_all + (warp - 2) * NQ * kIH;
         int* spos = spos_all + (warp - 2) * NQ;
         TileWalker<NQ> wk(t_begin, t_end, tiles_per_seq, chunks);
@@ -541,7 +550,7 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
             const bool in_ctx = j < g.ctx;
             if (kind == 1) {
                 if (in_ctx)
-                    for (int q = 0; q < g.nq; ++q) scores[(int64_t)(g.q0 + q) * ld + j] = -INFINITY;
+                    for (int q = q_lo; q < min(g.nq, q_lo + C::QPW); ++q) scores[(int64_t)(g.q0 + q) * ld + j] = -INFINITY;
                 continue;
             }
             // this row's physical location and scale, from the producer
@@ -568,21 +577,26 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
             if (!__all_sync(0xffffffffu, ptx::mbar_wait(tfull + a, au & 1, abort_flag, d_status))) break;
             ptx::tc_fence_after();
             const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + a * N;
-            // relu-weighted sum over the 32 heads of query q
-            auto reduce = [&](int q) -> float {
+            // relu-weighted sum over the 32 heads of query q (four partial
+            // sums, so the FMA chain is 8 deep rather than 32)
+            auto relu_sum = [&](const uint32_t (&v)[32], int q) -> float {
                 const float4* w4 = reinterpret_cast<const float4*>(sw + q * kIH);
-                float v[32];
-                ptx::tmem_ld32(tcol + q * 32, v);
-                float r = 0.f;
+                float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
 #pragma unroll
                 for (int h = 0; h < 32; h += 4) {
                     const float4 w = w4[h >> 2];
-                    r = fmaf(w.x, fmaxf(v[h], 0.f), r);
-                    r = fmaf(w.y, fmaxf(v[h + 1], 0.f), r);
-                    r = fmaf(w.z, fmaxf(v[h + 2], 0.f), r);
-                    r = fmaf(w.w, fmaxf(v[h + 3], 0.f), r);
+                    r0 = fmaf(w.x, fmaxf(__uint_as_float(v[h]), 0.f), r0);
+                    r1 = fmaf(w.y, fmaxf(__uint_as_float(v[h + 1]), 0.f), r1);
+                    r2 = fmaf(w.z, fmaxf(__uint_as_float(v[h + 2]), 0.f), r2);
+                    r3 = fmaf(w.w, fmaxf(__uint_as_float(v[h + 3]), 0.f), r3);
                 }
-                return r;
+                return (r0 + r1) + (r2 + r3);
+            };
+            auto reduce = [&](int q) -> float {
+                uint32_t v[32];
+                ptx::tmem_ld32_async(tcol + q * 32, v);
+                ptx::tmem_wait_ld32(v);
+                return relu_sum(v, q);
             };
             auto store = [&](int q, float r) {
                 if (in_ctx && q < g.nq)
@@ -604,8 +618,18 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
 #pragma unroll
                 for (int q = 0; q < NQ; ++q) store(q, acc[q]);
             } else {
-#pragma unroll 1
-                for (int q = 0; q < NQ; ++q) store(q, reduce(q));
+                // this warp's queries; the next one's columns load while this
+                // one's are summed
+                uint32_t v[2][32];
+                ptx::tmem_ld32_async(tcol + q_lo * 32, v[0]);
+                ptx::tmem_wait_ld32(v[0]);
+#pragma unroll
+                for (int i = 0; i < C::QPW; ++i) {
+                    if (i + 1 < C::QPW) ptx::tmem_ld32_async(tcol + (q_lo + i + 1) * 32, v[(i + 1) & 1]);
+                    const float r = relu_sum(v[i & 1], q_lo + i);
+                    if (i + 1 < C::QPW) ptx::tmem_wait_ld32(v[(i + 1) & 1]);
+                    store(q_lo + i, r);
+                }
                 release();
             }
             ++consumed;
