@@ -97,7 +97,7 @@ size_t workspace_bytes(const dsa_seqs& s, int num_q, int k, int64_t* scores_ld) 
     const int kk = k < 1 ? 1 : (k > DSA_MAX_TOPK ? DSA_MAX_TOPK : k);
     const int splits = mla_splits(num_q > 0 ? num_q : 1, kk);
     size_t b = 0;
-    b += up256((size_t)num_q * kIH * 192 * 2);                       // q'
+    b += up256((size_t)num_q * kQprepBytes);                         // q'
     b += up256((size_t)num_q * kIH * 4);                             // w'
     b += up256((size_t)num_q * splits * kMH * kMV * 4);              // partial outputs
     b += up256((size_t)num_q * splits * kMH * 2 * 4);                // partial (max, sum)
@@ -118,7 +118,7 @@ Workspace carve_workspace(void* base, const dsa_seqs& s, int num_q, int k) {
     const int splits = mla_splits(num_q > 0 ? num_q : 1, kk);
     uint8_t* p = reinterpret_cast<uint8_t*>(base);
     w.qprep = p;
-    p += up256((size_t)num_q * kIH * 192 * 2);
+    p += up256((size_t)num_q * kQprepBytes);
     w.wprep = reinterpret_cast<float*>(p);
     p += up256((size_t)num_q * kIH * 4);
     w.mla_part = reinterpret_cast<float*>(p);

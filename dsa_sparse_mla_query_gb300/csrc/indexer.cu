@@ -57,30 +57,25 @@ constexpr double kTwoPi2 = -0x1.dde974p-25;
 constexpr double kTwoPi3 = 0x1.1a62633145c07p-52;
 constexpr double kInvTwoPi = 0x1.45f306dc9c883p-3;
 
-template <typename T>
-__global__ void __launch_bounds__(128) qprep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ w,
-                                                    const float* __restrict__ ss, const float* __restrict__ sb,
-                                                    const float* __restrict__ inv_freq, dsa_seqs s, int num_q,
-                                                    T* __restrict__ qp, float* __restrict__ wp,
-                                                    int32_t* d_status) {
-    pdl_enter();
-    const int t = blockIdx.x;
+// Per query, shared by both preparations: the position check, the SSMax
+// factor's sign and |f| w / 64 per head, and cos / sin of the 32 angles.
+__device__ __forceinline__ void qprep_setup(const float* __restrict__ w, const float* __restrict__ ss,
+                                            const float* __restrict__ sb, const float* __restrict__ inv_freq,
+                                            const dsa_seqs& s, int t, float* cs, float* sn, float* sgn, float* wsc,
+                                            int* ok, int32_t* d_status) {
     const bool rope = inv_freq != nullptr;
-    const int KP = rope ? 192 : 128;
-    __shared__ float cs[32], sn[32], sgn[32];
-    __shared__ int ok;
     const int b = seq_of(s.q_start, s.num_seqs, t);
     const int pos = __ldg(s.q_pos + t);
     if (threadIdx.x == 0) {
         const int ctx = __ldg(s.ctx_len + b);
-        ok = (pos >= 0 && pos < ctx && ctx <= s.max_ctx);
-        if (!ok) report(d_status, DSA_ERR_BAD_INPUT);
+        *ok = (pos >= 0 && pos < ctx && ctx <= s.max_ctx);
+        if (!*ok) report(d_status, DSA_ERR_BAD_INPUT);
     }
     if (threadIdx.x < 32) {
         const int h = threadIdx.x;
         const float f = fmaf(__ldg(ss + h), logf((float)pos + 1.f), __ldg(sb + h));
         sgn[h] = f < 0.f ? -1.f : 1.f;
-        wp[(int64_t)t * kIH + h] = __ldg(w + (int64_t)t * kIH + h) * fabsf(f) * (1.f / 64.f);
+        wsc[h] = __ldg(w + (int64_t)t * kIH + h) * fabsf(f) * (1.f / 64.f);
     } else if (threadIdx.x < 64 && rope) {
         const int i = threadIdx.x - 32;  // rotation pair
         // The angle pos * inv_freq is exact in fp64 (a 31-bit integer times a
@@ -106,6 +101,22 @@ __global__ void __launch_bounds__(128) qprep_kernel(const __nv_bfloat16* __restr
         sn[i] = sf;
     }
     __syncthreads();
+}
+
+template <typename T>
+__global__ void __launch_bounds__(128) qprep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ w,
+                                                    const float* __restrict__ ss, const float* __restrict__ sb,
+                                                    const float* __restrict__ inv_freq, dsa_seqs s, int num_q,
+                                                    T* __restrict__ qp, float* __restrict__ wp,
+                                                    int32_t* d_status) {
+    pdl_enter();
+    const int t = blockIdx.x;
+    const bool rope = inv_freq != nullptr;
+    const int KP = rope ? 192 : 128;
+    __shared__ float cs[32], sn[32], sgn[32], wsc[32];
+    __shared__ int ok;
+    qprep_setup(w, ss, sb, inv_freq, s, t, cs, sn, sgn, wsc, &ok, d_status);
+    if (threadIdx.x < 32) wp[(int64_t)t * kIH + threadIdx.x] = wsc[threadIdx.x];
     // one work item = 4 consecutive pairs (8 dims) of one head
     const __nv_bfloat16* qt = q + (int64_t)t * kIH * kID;
     T* out = qp + (int64_t)t * kIH * KP;
@@ -139,6 +150,72 @@ __global__ void __launch_bounds__(128) qprep_kernel(const __nv_bfloat16* __restr
     }
 }
 
+// e4m3 index keys: the tensor cores take both operands in e4m3
+// (kind::f8f6f4), straight from the key tiles in shared memory.  q' (fp32,
+// sign-folded and rotated as above) is split per head into four e4m3 parts,
+//   q' = s (c_0 + 2^-4 c_1 + 2^-8 c_2 + 2^-12 c_3),
+// with s the smallest power of two that keeps max |q'| / s <= 448 (e4m3's
+// largest value): each part rounds the remaining residual to 4 significant
+// bits, so q' is kept to ~2^-16 relative, and every residual fits its part's
+// range (it is at most half an e4m3 ulp of the previous part, <= 16 units).
+// Each step (scaling by a power of two, the residual's subtraction) is
+// exact.  s is folded into the head weight, since relu(s x) = s relu(x):
+// w'' = w |f| s / 64.  Layout: [Q][4 parts][32 heads][128] e4m3 codes, one
+// 128-byte row per (query, part, head): the MMA's N rows.
+__global__ void __launch_bounds__(128) qprep_e4m3_kernel(const __nv_bfloat16* __restrict__ q,
+                                                         const float* __restrict__ w, const float* __restrict__ ss,
+                                                         const float* __restrict__ sb,
+                                                         const float* __restrict__ inv_freq, dsa_seqs s, int num_q,
+                                                         uint8_t* __restrict__ qp, float* __restrict__ wp,
+                                                         int32_t* d_status) {
+    pdl_enter();
+    const int t = blockIdx.x;
+    const bool rope = inv_freq != nullptr;
+    __shared__ float cs[32], sn[32], sgn[32], wsc[32];
+    __shared__ int ok;
+    qprep_setup(w, ss, sb, inv_freq, s, t, cs, sn, sgn, wsc, &ok, d_status);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int h = warp; h < kIH; h += 4) {
+        // lane: dims 4 lane .. 4 lane + 3, i.e. rotation pairs 2 lane and 2 lane + 1
+        const uint2 raw = *reinterpret_cast<const uint2*>(q + ((int64_t)t * kIH + h) * kID + 4 * lane);
+        const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&raw);
+        const float g = ok ? sgn[h] : 0.f;
+        float y[4];
+        if (rope && lane < 16) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int p = 2 * lane + u;
+                const float x0 = __bfloat162float(x[2 * u]), x1 = __bfloat162float(x[2 * u + 1]);
+                y[2 * u] = g * fmaf(x0, cs[p], -x1 * sn[p]);
+                y[2 * u + 1] = g * fmaf(x0, sn[p], x1 * cs[p]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) y[i] = g * __bfloat162float(x[i]);
+        }
+        float m = fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3])));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        int e = 0;
+        if (m > 0.f) frexpf(m * (1.f / 448.f), &e);  // m / 448 <= 2^e
+        uint8_t* out = qp + (((int64_t)t * 4) * kIH + h) * kID + 4 * lane;
+#pragma unroll
+        for (int part = 0; part < 4; ++part) {
+            const int pe = e - 4 * part;  // this part's scale is 2^pe
+            uint32_t word = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(ldexpf(y[i], -pe), __NV_SATFINITE, __NV_E4M3);
+                const __half_raw hv = __nv_cvt_fp8_to_halfraw(c, __NV_E4M3);
+                y[i] -= ldexpf(__half2float(__half(hv)), pe);
+                word |= (uint32_t)c << (8 * i);
+            }
+            *reinterpret_cast<uint32_t*>(out + (int64_t)part * kIH * kID) = word;
+        }
+        if (lane == 0) wp[(int64_t)t * kIH + h] = ldexpf(wsc[h], e);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // scores on the 5th-generation tensor cores.
 //
@@ -153,11 +230,13 @@ __global__ void __launch_bounds__(128) qprep_kernel(const __nv_bfloat16* __restr
 //              heads, K = 192 (hi | lo | unrotated) or 128 (NoPE), fp32
 //              accumulators double-buffered in TMEM;
 //   warps 2-5  epilogue: one key row per thread straight from TMEM, relu and
-//              head weights, causal mask, fp8 row scale, coalesced stores;
-//   warps 6-9  (e4m3 keys only) decode the staged codes, one key row per
-//              thread, and store them as f16 into a TMEM operand buffer: the
-//              MMA takes its key operand A from TMEM, so shared memory holds
-//              only the 16 KB raw stages and the ring runs deep.
+//              head weights, causal mask, fp8 row scale, coalesced stores
+//              (warps 2-9 for bf16 shapes of four or more queries at one CTA
+//              per SM).
+// e4m3 keys: the MMA runs kind::f8f6f4 on the staged codes themselves (K =
+// 128 bytes, one 128-byte swizzled row per key) against q' split into four
+// e4m3 parts (qprep_e4m3_kernel): N = NQ x 4 x 32 accumulator columns, which
+// the epilogue recombines per head with exact power-of-two scalings.
 // Keys past the context are never stored; pages are read through the page
 // table one TMA box (R rows, R | page size) at a time.
 constexpr int kTileKeys = 128;
@@ -249,8 +328,12 @@ struct TileInfo {
 template <int NQ, int KP, bool FP8>
 struct IdxCfg {
     static constexpr int N = NQ * kIH;
-    static constexpr int q_bytes = N * KP * 2;  // KP/64 blocks of N x 128 B
-    // bf16: two 128-byte swizzled 64-dim blocks; e4m3: the raw codes, one
+    static_assert(!FP8 || NQ <= 2, "e4m3 keys take at most two queries per chunk (TMEM)");
+    static constexpr int NM = FP8 ? 4 * N : N;   // MMA N = accumulator columns per buffer
+    static constexpr int KM = FP8 ? kID : KP;    // contraction length in elements
+    // bf16: KP/64 blocks of N x 128 B; e4m3: NM rows of 128 B
+    static constexpr int q_bytes = FP8 ? NM * kID : N * KP * 2;
+    // bf16: two 128-byte swizzled 64-dim blocks; e4m3: the codes, one
     // 128-byte (swizzled) row per key
     static constexpr int stage_bytes = FP8 ? kTileKeys * kID : kTileKeys * kID * 2;
     static constexpr int info_bytes = kInfoSlots * TileInfo<FP8>::bytes;
@@ -259,49 +342,28 @@ struct IdxCfg {
     // the queries (the epilogue, not the MMA, bounds those shapes otherwise)
     static constexpr int ew_max = (!FP8 && NQ >= 4) ? 8 : 4;
     static constexpr int tail_raw =
-        (2 * 8 + 14 + 2 * kInfoSlots) * 8 + 16 + ew_max * NQ * kIH * 4 + ew_max * NQ * 4;
+        (2 * 8 + 6 + 2 * kInfoSlots) * 8 + 16 + ew_max * NQ * kIH * 4 + ew_max * NQ * 4;
     static constexpr int tail = (tail_raw + 1023) / 1024 * 1024;  // barriers, TMEM slot, per-warp weights
     // Decode shapes (small q') run two persistent CTAs per SM, so two
     // producer / MMA-issuer pairs overlap their per-tile issue work: when two
-    // CTAs' stages fit and, for e4m3 keys, both accumulators and two 64-column
-    // key operands fit in half the TMEM.
-    static constexpr bool two_fit = (110 * 1024 - q_bytes - info_bytes - 1024 - tail) / stage_bytes >= 2 &&
-                                    (!FP8 || 2 * N + 2 * 64 <= 256);
+    // CTAs' stages and double-buffered accumulators fit.
+    // (two CTAs of at most 113 KB each: an SM's 228 KB less 1 KB per CTA)
+    static constexpr bool two_fit =
+        (113 * 1024 - q_bytes - info_bytes - 1024 - tail) / stage_bytes >= 2 && 2 * NM <= 256;
     static constexpr int ctas_per_sm = two_fit ? 2 : 1;
-    static constexpr int budget = (ctas_per_sm == 2 ? 110 : 220) * 1024;
+    static constexpr int budget = (ctas_per_sm == 2 ? 113 : 220) * 1024;
     static constexpr int stages_fit = (budget - q_bytes - info_bytes - 1024 - tail) / stage_bytes;
     static constexpr int S = stages_fit > 8 ? 8 : stages_fit;
     static constexpr int EW = (ew_max == 8 && ctas_per_sm == 1) ? 8 : 4;
     static constexpr int QPW = NQ * 4 / EW;  // queries per epilogue warp
-    static constexpr int threads = (FP8 || EW == 8) ? 320 : 192;
-    static constexpr int tmem_cols = FP8 ? (ctas_per_sm == 2 ? 256 : 512) : (2 * N < 32 ? 32 : 2 * N);
-    // accumulator buffers (columns [0, nacc N)), then (e4m3) na key operand
-    // buffers of 64 columns: 128 keys x 128 f16 dims
-    static constexpr int nacc = (!FP8 || 2 * N + 2 * 64 <= tmem_cols) ? 2 : 1;
-    static constexpr int na_fit = FP8 ? (tmem_cols - nacc * N) / 64 : 0;
-    static constexpr int na = na_fit > 4 ? 4 : na_fit;
-    static constexpr int a_col = nacc * N;
+    static constexpr int threads = EW == 8 ? 320 : 192;
+    static constexpr int tmem_cols = 2 * NM < 32 ? 32 : 2 * NM;  // two accumulator buffers
+    static constexpr int nacc = 2;
     static constexpr size_t smem = 1024 + (size_t)S * stage_bytes + q_bytes + info_bytes + tail;  // + alignment slack
     static_assert(S >= 2, "too little shared memory for two stages");
-    static_assert(!FP8 || na >= 2, "too little TMEM for two key operand buffers");
+    static_assert(2 * NM <= 512, "accumulators exceed TMEM");
 };
 
-// Two e4m3 codes of w (the bytes that prmt selector sel picks, the lower
-// dimension first) -> f16x2 holding 2^-8 times their values, exactly.  The
-// code's 7 magnitude bits (4 exponent, 3 mantissa), moved to bits 13..7, are
-// the f16 whose exponent field is the e4m3 one: f16's bias is 15 and e4m3's
-// 7, so the f16 is the e4m3 value times 2^-8, for subnormal codes (exponent
-// 0) too.  The sign-replicating selector nibbles fill bit 15 with the code's
-// sign.  The NaN codes (0x7F, 0xFF) come out as +-1.875 (480 before scaling).
-// PRMT, shift and AND run on the integer pipe at about twice the
-// conversion unit's rate.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_div256(uint32_t w, uint32_t sel) {
-    uint32_t x;
-    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(x) : "r"(w), "r"(sel));
-    return (x << 7) & 0xBF80BF80u;
-}
-constexpr uint32_t kSelDims01 = 0x9180u;  // bytes 0, 1 -> halves, each with its sign byte above
-constexpr uint32_t kSelDims23 = 0xB3A2u;  // bytes 2, 3
 
 template <int NQ, int KP, bool FP8>
 __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, FP8>::ctas_per_sm)
@@ -319,16 +381,14 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
     uint8_t* info = qs + C::q_bytes;  // [kInfoSlots] TileInfo
     uint64_t* bars = reinterpret_cast<uint64_t*>(info + C::info_bytes);
     uint64_t* full = bars;               // [S] TMA landed
-    uint64_t* empty = bars + S;          // [S] stage read (bf16: by the MMA; e4m3: by the decoders)
+    uint64_t* empty = bars + S;          // [S] stage read by the MMA
     uint64_t* tfull = bars + 2 * S;      // [2] accumulator ready
     uint64_t* tempty = bars + 2 * S + 2; // [2] accumulator drained
-    uint64_t* aconv = bars + 2 * S + 4;  // [4] e4m3: key operand decoded into TMEM
-    uint64_t* aempty = bars + 2 * S + 8; // [4] e4m3: MMA done reading the key operand
-    uint64_t* qfull = bars + 2 * S + 12;
-    uint64_t* qempty = bars + 2 * S + 13;
-    uint64_t* ifull = bars + 2 * S + 14;                // [kInfoSlots] tile info written (and scales landed)
-    uint64_t* iempty = bars + 2 * S + 14 + kInfoSlots;  // [kInfoSlots] tile info read
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 14 + 2 * kInfoSlots);
+    uint64_t* qfull = bars + 2 * S + 4;
+    uint64_t* qempty = bars + 2 * S + 5;
+    uint64_t* ifull = bars + 2 * S + 6;                // [kInfoSlots] tile info written (and scales landed)
+    uint64_t* iempty = bars + 2 * S + 6 + kInfoSlots;  // [kInfoSlots] tile info read
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 6 + 2 * kInfoSlots);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     float* sw_all = reinterpret_cast<float*>(tmem_slot + 4);  // [EW][NQ*32] head weights, one copy per epilogue warp
     int* spos_all = reinterpret_cast<int*>(sw_all + C::EW * NQ * kIH);  // [EW][NQ] query positions
@@ -340,15 +400,11 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             ptx::mbar_init(full + i, 1);
-            ptx::mbar_init(empty + i, FP8 ? 4 : 1);
+            ptx::mbar_init(empty + i, 1);
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(tfull + i, 1);
             ptx::mbar_init(tempty + i, C::EW);
-        }
-        for (int i = 0; i < 4; ++i) {
-            ptx::mbar_init(aconv + i, 4);
-            ptx::mbar_init(aempty + i, 1);
         }
         for (int i = 0; i < kInfoSlots; ++i) {
             ptx::mbar_init(ifull + i, FP8 ? 33 : 1);  // lane 0, plus each lane's scale copies (e4m3)
@@ -391,8 +447,11 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
                     ok = qloads == 0 || ptx::mbar_wait(qempty, (qloads - 1) & 1, abort_flag, d_status);
                     if (ok) {
                         ptx::mbar_expect_tx(qfull, C::q_bytes);
-                        for (int kb = 0; kb < KP / 64; ++kb)
-                            ptx::tma_load_2d(qs + kb * N * 128, &qmap, kb * 64, g.q0 * kIH, qfull);
+                        if (FP8)
+                            ptx::tma_load_2d(qs, &qmap, 0, g.q0 * 4 * kIH, qfull);
+                        else
+                            for (int kb = 0; kb < KP / 64; ++kb)
+                                ptx::tma_load_2d(qs + kb * N * 128, &qmap, kb * 64, g.q0 * kIH, qfull);
                     }
                 }
                 if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -467,14 +526,15 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
         ptx::cp_async_wait_all();
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = ptx::idesc_f16_m128(N, !FP8);
+        // e4m3 x e4m3 (kind::f8f6f4) encodes like f16 x f16: both type fields 0
+        constexpr uint32_t idesc = ptx::idesc_f16_m128(C::NM, !FP8);
         TileWalker<NQ> wk(t_begin, t_end, tiles_per_seq, chunks);
         int seg, j0, kind, nseg, nj0, nkind;
         bool have = wk.next(s, 2, d_status, false, seg, j0, kind);
         int q_seg = -1, qloads = 0;
         int64_t consumed = 0;
-        int st = 0, a = 0, ab = 0;         // ring stage, accumulator, key operand buffer
-        uint32_t use = 0, au = 0, abu = 0;  // and how often each has come round
+        int st = 0, a = 0;     // ring stage, accumulator
+        uint32_t use = 0, au = 0;  // and how often each has come round
         while (have) {
             const bool have_next = wk.next(s, 2, d_status, false, nseg, nj0, nkind);
             if (seg != q_seg) {
@@ -482,33 +542,33 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
                 ++qloads;
                 q_seg = seg;
             }
-            if (!(FP8 ? ptx::mbar_wait(aconv + ab, abu & 1, abort_flag, d_status)
-                      : ptx::mbar_wait(full + st, use & 1, abort_flag, d_status)))
-                break;
+            if (!ptx::mbar_wait(full + st, use & 1, abort_flag, d_status)) break;
             if (consumed >= C::nacc && !ptx::mbar_wait(tempty + a, (au - 1) & 1, abort_flag, d_status)) break;
             ptx::tc_fence_after();
             const uint32_t kbase = smem_u32(stages + st * C::stage_bytes);
             const uint32_t qbase = smem_u32(qs);
+            if (FP8) {
+                // 4 k-steps of 32 codes (32 bytes) within the 128-byte rows
 #pragma unroll
-            for (int ks = 0; ks < KP / 16; ++ks) {
-                int kd;  // key dim of this k-step: [hi | lo | unrotated] read dims 0..63, 0..63, 64..127
-                if (KP == 192) kd = ks < 4 ? ks * 16 : (ks < 8 ? (ks - 4) * 16 : 64 + (ks - 8) * 16);
-                else kd = ks * 16;
-                const uint64_t bd = ptx::sdesc_sw128(qbase + ((ks * 16) >> 6) * (N * 128) + ((ks * 16) & 63) * 2);
-                if (FP8) {
-                    // key operand from TMEM: two f16 dims per column
-                    ptx::mma_ts(tmem_base + a * N, tmem_base + C::a_col + ab * 64 + (kd >> 1), bd, idesc,
-                                ks > 0 ? 1u : 0u);
-                } else {
+                for (int ks = 0; ks < C::KM / 32; ++ks)
+                    ptx::mma_ss_f8(tmem_base + a * C::NM, ptx::sdesc_sw128(kbase + ks * 32),
+                                   ptx::sdesc_sw128(qbase + ks * 32), idesc, ks > 0 ? 1u : 0u);
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < KP / 16; ++ks) {
+                    int kd;  // key dim of this k-step: [hi | lo | unrotated] read dims 0..63, 0..63, 64..127
+                    if (KP == 192) kd = ks < 4 ? ks * 16 : (ks < 8 ? (ks - 4) * 16 : 64 + (ks - 8) * 16);
+                    else kd = ks * 16;
+                    const uint64_t bd =
+                        ptx::sdesc_sw128(qbase + ((ks * 16) >> 6) * (N * 128) + ((ks * 16) & 63) * 2);
                     const uint64_t ad = ptx::sdesc_sw128(kbase + (kd >> 6) * (kTileKeys * 128) + (kd & 63) * 2);
                     ptx::mma_ss(tmem_base + a * N, ad, bd, idesc, ks > 0 ? 1u : 0u);
                 }
             }
-            ptx::mma_commit(FP8 ? aempty + ab : empty + st);
+            ptx::mma_commit(empty + st);
             ptx::mma_commit(tfull + a);
             if (++st == S) { st = 0; ++use; }
             if (++a == C::nacc) { a = 0; ++au; }
-            if (++ab == C::na) { ab = 0; ++abu; }
             if (!have_next || nseg != seg) ptx::mma_commit(qempty);
             ++consumed;
             have = have_next;
@@ -570,13 +630,12 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
                 report(d_status, DSA_ERR_BAD_INPUT);
                 sigma = 0.f;
             }
-            if (FP8) sigma *= 256.f;  // the decoded keys are 2^-8 times the codes' values
             const int a = (int)(consumed % C::nacc);
             const uint32_t au = (uint32_t)(consumed / C::nacc);
             // warp-uniform outcome: a lane that sees an abort takes the whole warp out
             if (!__all_sync(0xffffffffu, ptx::mbar_wait(tfull + a, au & 1, abort_flag, d_status))) break;
             ptx::tc_fence_after();
-            const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + a * N;
+            const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + a * C::NM;
             // relu-weighted sum over the 32 heads of query q (four partial
             // sums, so the FMA chain is 8 deep rather than 32)
             auto relu_sum = [&](const uint32_t (&v)[32], int q) -> float {
@@ -593,6 +652,31 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
                 return (r0 + r1) + (r2 + r3);
             };
             auto reduce = [&](int q) -> float {
+                if (FP8) {
+                    // head h of query q: parts at columns q 128 + p 32 + h,
+                    // q'.k / s = D0 + 2^-4 (D1 + 2^-4 (D2 + 2^-4 D3)), exact scalings
+                    const float4* w4 = reinterpret_cast<const float4*>(sw + q * kIH);
+                    float r0 = 0.f, r1 = 0.f;
+#pragma unroll 1
+                    for (int h0 = 0; h0 < 32; h0 += 16) {
+                        float d[4][16];
+                        ptx::tmem_ld16x4(tcol + q * 4 * kIH + h0, kIH, d);
+#pragma unroll
+                        for (int h = 0; h < 16; h += 4) {
+                            const float4 w = w4[(h0 + h) >> 2];
+                            const float wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                float x = fmaf(d[3][h + u], 0.0625f, d[2][h + u]);
+                                x = fmaf(x, 0.0625f, d[1][h + u]);
+                                x = fmaf(x, 0.0625f, d[0][h + u]);
+                                if (u & 1) r1 = fmaf(wv[u], fmaxf(x, 0.f), r1);
+                                else r0 = fmaf(wv[u], fmaxf(x, 0.f), r0);
+                            }
+                        }
+                    }
+                    return r0 + r1;
+                }
                 uint32_t v[32];
                 ptx::tmem_ld32_async(tcol + q * 32, v);
                 ptx::tmem_wait_ld32(v);
@@ -607,10 +691,9 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(tempty + a);
             };
-            // Where the registers allow (both queries' sums under the fp8
-            // kernel's 96-register cap is too many), the accumulator goes
-            // back to the MMA before the stores.
-            if constexpr (NQ == 1 || (NQ == 2 && !FP8)) {
+            // One or two queries: the accumulator goes back to the MMA before
+            // the stores.
+            if constexpr (NQ <= 2) {
                 float acc[NQ];
 #pragma unroll
                 for (int q = 0; q < NQ; ++q) acc[q] = reduce(q);
@@ -633,52 +716,6 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
                 release();
             }
             ++consumed;
-        }
-    } else if (FP8 && warp >= 6) {
-        // ------------------------------------------------------------ e4m3 -> f16 x 2^-8 into TMEM
-        // Thread = key row = TMEM lane (a warp reaches its own lane quarter).
-        // The 128-byte swizzle puts the row's 16-byte chunk i at i ^ (row & 7),
-        // so the warp's 16-byte reads spread over all banks.
-        const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;
-        const uint32_t lane_cols = tmem_base + ((uint32_t)(quarter * 32) << 16) + C::a_col;
-        TileWalker<NQ> wk(t_begin, t_end, tiles_per_seq, chunks);
-        int seg, j0, kind;
-        int64_t n = 0;
-        int st = 0, ab = 0;
-        uint32_t use = 0, abu = 0;
-        while (wk.next(s, 2, d_status, false, seg, j0, kind)) {
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait(full + st, use & 1, abort_flag, d_status))) break;
-            const uint8_t* rowp = stages + st * C::stage_bytes + r * 128;
-            uint4 c[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) c[i] = *reinterpret_cast<const uint4*>(rowp + ((i ^ (r & 7)) << 4));
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(empty + st);
-            // the MMAs that read this operand buffer last time have completed
-            if (n >= C::na &&
-                !__all_sync(0xffffffffu, ptx::mbar_wait(aempty + ab, (abu - 1) & 1, abort_flag, d_status)))
-                break;
-            ptx::tc_fence_after();
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {  // dims 32g .. 32g+31 -> columns 16g .. 16g+15
-                const uint32_t w[8] = {c[2 * g].x,     c[2 * g].y,     c[2 * g].z,     c[2 * g].w,
-                                       c[2 * g + 1].x, c[2 * g + 1].y, c[2 * g + 1].z, c[2 * g + 1].w};
-                uint32_t v[16];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    v[2 * u] = e4m3x2_to_f16x2_div256(w[u], kSelDims01);
-                    v[2 * u + 1] = e4m3x2_to_f16x2_div256(w[u], kSelDims23);
-                }
-                ptx::tmem_st16_async(lane_cols + ab * 64 + g * 16, v);
-            }
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(aconv + ab);
-            ++n;
-            if (++st == S) { st = 0; ++use; }
-            if (++ab == C::na) { ab = 0; ++abu; }
         }
     }
     ptx::tc_fence_before();
@@ -741,8 +778,12 @@ cudaError_t launch_tc(const void* qp, int num_q, const float* wp, const void* k_
         e = make_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_idx, kID, (uint64_t)s.num_rows, kID * 2, 64,
                      box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
-    e = make_map(&qmap, FP8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qp, KP,
-                 (uint64_t)num_q * kIH, KP * 2, 64, C::N, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (FP8)  // [Q x 4 parts x 32 heads] rows of 128 codes; one box = a chunk's NM rows
+        e = make_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, qp, kID, (uint64_t)num_q * 4 * kIH, kID, kID, C::NM,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+        e = make_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qp, KP, (uint64_t)num_q * kIH, KP * 2, 64, C::N,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
     auto kern = index_tc_kernel<NQ, KP, FP8>;
     static bool attr_set = false;
@@ -763,11 +804,14 @@ template <int NQ>
 cudaError_t launch_tc_nq(bool rope, bool fp8, const void* qp, int num_q, const float* wp, const void* k_idx,
                          const float* k_scale, const dsa_seqs& s, float* scores, int64_t ld, int32_t* d_status,
                          cudaStream_t stream) {
-    if (rope)
-        return fp8 ? launch_tc<NQ, 192, true>(qp, num_q, wp, k_idx, k_scale, s, scores, ld, d_status, stream)
-                   : launch_tc<NQ, 192, false>(qp, num_q, wp, k_idx, k_scale, s, scores, ld, d_status, stream);
-    return fp8 ? launch_tc<NQ, 128, true>(qp, num_q, wp, k_idx, k_scale, s, scores, ld, d_status, stream)
-               : launch_tc<NQ, 128, false>(qp, num_q, wp, k_idx, k_scale, s, scores, ld, d_status, stream);
+    if (fp8) {  // q' parts hold the rotated (or unrotated) 128 dims either way
+        if constexpr (NQ <= 2)
+            return launch_tc<NQ, 128, true>(qp, num_q, wp, k_idx, k_scale, s, scores, ld, d_status, stream);
+        else
+            return cudaErrorInvalidValue;
+    }
+    return rope ? launch_tc<NQ, 192, false>(qp, num_q, wp, k_idx, k_scale, s, scores, ld, d_status, stream)
+                : launch_tc<NQ, 128, false>(qp, num_q, wp, k_idx, k_scale, s, scores, ld, d_status, stream);
 }
 
 }  // namespace
@@ -780,12 +824,17 @@ cudaError_t launch_index_scores(const void* q_idx, const float* w, const float* 
     const bool rope = inv_freq != nullptr;
     const __nv_bfloat16* qi = reinterpret_cast<const __nv_bfloat16*>(q_idx);
     cudaError_t e =
-        fp8 ? launch_pdl(qprep_kernel<__half>, dim3(num_q), dim3(128), 0, stream, 1, qi, w, ssmax_s, ssmax_b, inv_freq,
-                         s, num_q, reinterpret_cast<__half*>(ws.qprep), ws.wprep, d_status)
+        fp8 ? launch_pdl(qprep_e4m3_kernel, dim3(num_q), dim3(128), 0, stream, 1, qi, w, ssmax_s, ssmax_b, inv_freq, s,
+                         num_q, reinterpret_cast<uint8_t*>(ws.qprep), ws.wprep, d_status)
             : launch_pdl(qprep_kernel<__nv_bfloat16>, dim3(num_q), dim3(128), 0, stream, 1, qi, w, ssmax_s, ssmax_b,
                          inv_freq, s, num_q, reinterpret_cast<__nv_bfloat16*>(ws.qprep), ws.wprep, d_status);
     if (e != cudaSuccess) return e;
     const int mq = s.max_q_per_seq;
+    if (fp8)  // e4m3 keys: chunks of at most two queries (four parts each fill the TMEM)
+        return mq <= 1 ? launch_tc_nq<1>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, d_status,
+                                         stream)
+                       : launch_tc_nq<2>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, d_status,
+                                         stream);
     if (mq <= 1) return launch_tc_nq<1>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, d_status, stream);
     if (mq <= 2) return launch_tc_nq<2>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, d_status, stream);
     if (mq <= 4) return launch_tc_nq<4>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, d_status, stream);
