@@ -347,11 +347,12 @@ struct IdxCfg {
     // Decode shapes (small q') run two persistent CTAs per SM, so two
     // producer / MMA-issuer pairs overlap their per-tile issue work: when two
     // CTAs' stages and double-buffered accumulators fit.
-    // (two CTAs of at most 113 KB each: an SM's 228 KB less 1 KB per CTA)
+    // (110 KB per CTA: two fit an SM's 228 KB; the full 113 KB gives the
+    // paged bf16 shape a third stage, measured slower than two)
     static constexpr bool two_fit =
-        (113 * 1024 - q_bytes - info_bytes - 1024 - tail) / stage_bytes >= 2 && 2 * NM <= 256;
+        (110 * 1024 - q_bytes - info_bytes - 1024 - tail) / stage_bytes >= 2 && 2 * NM <= 256;
     static constexpr int ctas_per_sm = two_fit ? 2 : 1;
-    static constexpr int budget = (ctas_per_sm == 2 ? 113 : 220) * 1024;
+    static constexpr int budget = (ctas_per_sm == 2 ? 110 : 220) * 1024;
     static constexpr int stages_fit = (budget - q_bytes - info_bytes - 1024 - tail) / stage_bytes;
     static constexpr int S = stages_fit > 8 ? 8 : stages_fit;
     static constexpr int EW = (ew_max == 8 && ctas_per_sm == 1) ? 8 : 4;
