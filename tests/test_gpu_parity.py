@@ -219,6 +219,18 @@ def test_fp8_index_keys_every_code_class():
     assert worst < 1e-4, f"scores should be near fp32 accuracy, got {worst:.2e}"
 
 
+def test_fp8_rows_at_odd_bases():
+    """e4m3 keys of sequences whose first rows are not multiples of four
+    (contexts 2001, 4163, 130): their row scales cannot be copied in 16-byte
+    blocks and take the per-row path; the last tile runs past the cache."""
+    wl = I.scaled(W["long_fp8"], num_seqs=3, ctx=None, ctx_list=(2001, 4163, 130))
+    d, _ = _inputs_cpu_then_gpu(wl)
+    assert int(P.seq_rows_host(d, 1)[0]) % 4 != 0
+    reps = _check_workload(d, wl, list(range(wl.num_queries)))
+    worst = max(r["score_rel_err"] for r in reps)
+    assert worst < 1e-4, f"scores should be near fp32 accuracy, got {worst:.2e}"
+
+
 def test_all_equal_scores_take_smallest_indices():
     """w = 0 makes every score 0: the selection is positions 0..k-1."""
     wl = I.scaled(W["tiny"], num_seqs=1, ctx=5000, queries_per_seq=2)
