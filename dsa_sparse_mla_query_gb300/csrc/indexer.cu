@@ -694,7 +694,36 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
             };
             // One or two queries: the accumulator goes back to the MMA before
             // the stores.
-            if constexpr (NQ <= 2) {
+            if constexpr (FP8 && NQ == 1) {
+                // all 128 columns (4 parts x 32 heads) into registers, then the
+                // release: the recombination and head sum run off the MMA's path
+                uint32_t d[4][32];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) ptx::tmem_ld32_async(tcol + p * kIH, d[p]);
+#pragma unroll
+                for (int p = 0; p < 4; ++p) ptx::tmem_wait_ld32(d[p]);
+                release();
+                const float4* w4 = reinterpret_cast<const float4*>(sw);
+                float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+#pragma unroll
+                for (int h = 0; h < 32; h += 4) {
+                    const float4 w = w4[h >> 2];
+                    const float wv[4] = {w.x, w.y, w.z, w.w};
+                    float x[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        // q'.k / s = D0 + 2^-4 (D1 + 2^-4 (D2 + 2^-4 D3)), exact scalings
+                        float v = fmaf(__uint_as_float(d[3][h + u]), 0.0625f, __uint_as_float(d[2][h + u]));
+                        v = fmaf(v, 0.0625f, __uint_as_float(d[1][h + u]));
+                        x[u] = fmaxf(fmaf(v, 0.0625f, __uint_as_float(d[0][h + u])), 0.f);
+                    }
+                    r0 = fmaf(wv[0], x[0], r0);
+                    r1 = fmaf(wv[1], x[1], r1);
+                    r2 = fmaf(wv[2], x[2], r2);
+                    r3 = fmaf(wv[3], x[3], r3);
+                }
+                store(0, (r0 + r1) + (r2 + r3));
+            } else if constexpr (NQ <= 2) {
                 float acc[NQ];
 #pragma unroll
                 for (int q = 0; q < NQ; ++q) acc[q] = reduce(q);
