@@ -119,7 +119,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // launchers (host)
 struct Workspace {
     // carved from the caller's workspace, 256-byte aligned pieces
-    void* qprep;      // q' [Q, 32, KP] bf16, or [Q, 4, 32, 128] e4m3 parts (kQprepBytes per query)
+    void* qprep;      // q' [Q, 32, KP] bf16, or [Q, 3, 32, 128] e4m3 parts (kQprepBytes per query)
     float* wprep;     // w' [Q, 32]
     float* mla_part;  // O partials [Q, splits, 64, 512]
     float* mla_ml;    // (m, l) partials [Q, splits, 64, 2]
@@ -133,7 +133,7 @@ struct Workspace {
     int* tk_above;       // [Q, DSA_MAX_TOPK] positions of the keys above it
 };
 
-constexpr int kQprepBytes = 4 * kIH * kID;  // per query: >= 32 x 192 bf16 and 4 x 32 x 128 e4m3
+constexpr int kQprepBytes = 4 * kIH * kID;  // per query: >= 32 x 192 bf16 and 3 x 32 x 128 e4m3
 constexpr int kLongChunk = 16384;      // keys per CTA in the long-row top-k
 constexpr int kLongCand = 8192;        // candidate slots per row
 constexpr int kLongMaxChunks = 1024;   // rows up to 16M keys take the chunked path

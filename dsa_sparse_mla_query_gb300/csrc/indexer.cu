@@ -152,16 +152,19 @@ __global__ void __launch_bounds__(128) qprep_kernel(const __nv_bfloat16* __restr
 
 // e4m3 index keys: the tensor cores take both operands in e4m3
 // (kind::f8f6f4), straight from the key tiles in shared memory.  q' (fp32,
-// sign-folded and rotated as above) is split per head into four e4m3 parts,
-//   q' = s (c_0 + 2^-4 c_1 + 2^-8 c_2 + 2^-12 c_3),
+// sign-folded and rotated as above) is split per head into three e4m3 parts,
+//   q' = s (c_0 + 2^-4 c_1 + 2^-8 c_2),
 // with s the smallest power of two that keeps max |q'| / s <= 448 (e4m3's
 // largest value): each part rounds the remaining residual to 4 significant
-// bits, so q' is kept to ~2^-16 relative, and every residual fits its part's
-// range (it is at most half an e4m3 ulp of the previous part, <= 16 units).
-// Each step (scaling by a power of two, the residual's subtraction) is
-// exact.  s is folded into the head weight, since relu(s x) = s relu(x):
-// w'' = w |f| s / 64.  Layout: [Q][4 parts][32 heads][128] e4m3 codes, one
+// bits, so q' is kept to ~2^-12 relative (measured: scores within 2e-5 of
+// the row maximum of those from four parts), and every residual fits its
+// part's range (it is at most half an e4m3 ulp of the previous part, <= 16
+// units).  Each step (scaling by a power of two, the residual's subtraction)
+// is exact.  s is folded into the head weight, since relu(s x) = s relu(x):
+// w'' = w |f| s / 64.  Layout: [Q][3 parts][32 heads][128] e4m3 codes, one
 // 128-byte row per (query, part, head): the MMA's N rows.
+constexpr int kQParts = 3;  // e4m3 parts of q' (e4m3 index keys)
+
 __global__ void __launch_bounds__(128) qprep_e4m3_kernel(const __nv_bfloat16* __restrict__ q,
                                                          const float* __restrict__ w, const float* __restrict__ ss,
                                                          const float* __restrict__ sb,
@@ -198,9 +201,9 @@ __global__ void __launch_bounds__(128) qprep_e4m3_kernel(const __nv_bfloat16* __
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         int e = 0;
         if (m > 0.f) frexpf(m * (1.f / 448.f), &e);  // m / 448 <= 2^e
-        uint8_t* out = qp + (((int64_t)t * 4) * kIH + h) * kID + 4 * lane;
+        uint8_t* out = qp + (((int64_t)t * kQParts) * kIH + h) * kID + 4 * lane;
 #pragma unroll
-        for (int part = 0; part < 4; ++part) {
+        for (int part = 0; part < kQParts; ++part) {
             const int pe = e - 4 * part;  // this part's scale is 2^pe
             uint32_t word = 0;
 #pragma unroll
@@ -234,8 +237,8 @@ __global__ void __launch_bounds__(128) qprep_e4m3_kernel(const __nv_bfloat16* __
 //              (warps 2-9 for bf16 shapes of four or more queries at one CTA
 //              per SM).
 // e4m3 keys: the MMA runs kind::f8f6f4 on the staged codes themselves (K =
-// 128 bytes, one 128-byte swizzled row per key) against q' split into four
-// e4m3 parts (qprep_e4m3_kernel): N = NQ x 4 x 32 accumulator columns, which
+// 128 bytes, one 128-byte swizzled row per key) against q' split into three
+// e4m3 parts (qprep_e4m3_kernel): N = NQ x 3 x 32 accumulator columns, which
 // the epilogue recombines per head with exact power-of-two scalings.
 // Keys past the context are never stored; pages are read through the page
 // table one TMA box (R rows, R | page size) at a time.
@@ -329,7 +332,7 @@ template <int NQ, int KP, bool FP8>
 struct IdxCfg {
     static constexpr int N = NQ * kIH;
     static_assert(!FP8 || NQ <= 2, "e4m3 keys take at most two queries per chunk (TMEM)");
-    static constexpr int NM = FP8 ? 4 * N : N;   // MMA N = accumulator columns per buffer
+    static constexpr int NM = FP8 ? kQParts * N : N;  // MMA N = accumulator columns per buffer
     static constexpr int KM = FP8 ? kID : KP;    // contraction length in elements
     // bf16: KP/64 blocks of N x 128 B; e4m3: NM rows of 128 B
     static constexpr int q_bytes = FP8 ? NM * kID : N * KP * 2;
@@ -358,11 +361,13 @@ struct IdxCfg {
     static constexpr int EW = (ew_max == 8 && ctas_per_sm == 1) ? 8 : 4;
     static constexpr int QPW = NQ * 4 / EW;  // queries per epilogue warp
     static constexpr int threads = EW == 8 ? 320 : 192;
-    static constexpr int tmem_cols = 2 * NM < 32 ? 32 : 2 * NM;  // two accumulator buffers
+    // two accumulator buffers; tcgen05.alloc takes a power of two >= 32 columns
+    static constexpr int tmem_cols = 2 * NM <= 32 ? 32 : 2 * NM <= 64 ? 64 : 2 * NM <= 128 ? 128 : 2 * NM <= 256 ? 256 : 512;
     static constexpr int nacc = 2;
     static constexpr size_t smem = 1024 + (size_t)S * stage_bytes + q_bytes + info_bytes + tail;  // + alignment slack
     static_assert(S >= 2, "too little shared memory for two stages");
     static_assert(2 * NM <= 512, "accumulators exceed TMEM");
+    static_assert(ctas_per_sm * tmem_cols <= 512, "the CTAs of an SM must fit its TMEM together");
 };
 
 
@@ -449,7 +454,7 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
                     if (ok) {
                         ptx::mbar_expect_tx(qfull, C::q_bytes);
                         if (FP8)
-                            ptx::tma_load_2d(qs, &qmap, 0, g.q0 * 4 * kIH, qfull);
+                            ptx::tma_load_2d(qs, &qmap, 0, g.q0 * kQParts * kIH, qfull);
                         else
                             for (int kb = 0; kb < KP / 64; ++kb)
                                 ptx::tma_load_2d(qs + kb * N * 128, &qmap, kb * 64, g.q0 * kIH, qfull);
@@ -654,22 +659,22 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
             };
             auto reduce = [&](int q) -> float {
                 if (FP8) {
-                    // head h of query q: parts at columns q 128 + p 32 + h,
-                    // q'.k / s = D0 + 2^-4 (D1 + 2^-4 (D2 + 2^-4 D3)), exact scalings
+                    // head h of query q: parts at columns q 96 + p 32 + h,
+                    // q'.k / s = D0 + 2^-4 (D1 + 2^-4 D2), exact scalings
                     const float4* w4 = reinterpret_cast<const float4*>(sw + q * kIH);
                     float r0 = 0.f, r1 = 0.f;
 #pragma unroll 1
                     for (int h0 = 0; h0 < 32; h0 += 16) {
-                        float d[4][16];
-                        ptx::tmem_ld16x4(tcol + q * 4 * kIH + h0, kIH, d);
+                        float d[kQParts][16];
+#pragma unroll
+                        for (int p = 0; p < kQParts; ++p) ptx::tmem_ld16(tcol + (q * kQParts + p) * kIH + h0, d[p]);
 #pragma unroll
                         for (int h = 0; h < 16; h += 4) {
                             const float4 w = w4[(h0 + h) >> 2];
                             const float wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                             for (int u = 0; u < 4; ++u) {
-                                float x = fmaf(d[3][h + u], 0.0625f, d[2][h + u]);
-                                x = fmaf(x, 0.0625f, d[1][h + u]);
+                                float x = fmaf(d[2][h + u], 0.0625f, d[1][h + u]);
                                 x = fmaf(x, 0.0625f, d[0][h + u]);
                                 if (u & 1) r1 = fmaf(wv[u], fmaxf(x, 0.f), r1);
                                 else r0 = fmaf(wv[u], fmaxf(x, 0.f), r0);
@@ -695,13 +700,13 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
             // One or two queries: the accumulator goes back to the MMA before
             // the stores.
             if constexpr (FP8 && NQ == 1) {
-                // all 128 columns (4 parts x 32 heads) into registers, then the
+                // all 96 columns (3 parts x 32 heads) into registers, then the
                 // release: the recombination and head sum run off the MMA's path
-                uint32_t d[4][32];
+                uint32_t d[kQParts][32];
 #pragma unroll
-                for (int p = 0; p < 4; ++p) ptx::tmem_ld32_async(tcol + p * kIH, d[p]);
+                for (int p = 0; p < kQParts; ++p) ptx::tmem_ld32_async(tcol + p * kIH, d[p]);
 #pragma unroll
-                for (int p = 0; p < 4; ++p) ptx::tmem_wait_ld32(d[p]);
+                for (int p = 0; p < kQParts; ++p) ptx::tmem_wait_ld32(d[p]);
                 release();
                 const float4* w4 = reinterpret_cast<const float4*>(sw);
                 float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
@@ -712,9 +717,8 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
                     float x[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        // q'.k / s = D0 + 2^-4 (D1 + 2^-4 (D2 + 2^-4 D3)), exact scalings
-                        float v = fmaf(__uint_as_float(d[3][h + u]), 0.0625f, __uint_as_float(d[2][h + u]));
-                        v = fmaf(v, 0.0625f, __uint_as_float(d[1][h + u]));
+                        // q'.k / s = D0 + 2^-4 (D1 + 2^-4 D2), exact scalings
+                        const float v = fmaf(__uint_as_float(d[2][h + u]), 0.0625f, __uint_as_float(d[1][h + u]));
                         x[u] = fmaxf(fmaf(v, 0.0625f, __uint_as_float(d[0][h + u])), 0.f);
                     }
                     r0 = fmaf(wv[0], x[0], r0);
@@ -808,8 +812,8 @@ cudaError_t launch_tc(const void* qp, int num_q, const float* wp, const void* k_
         e = make_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_idx, kID, (uint64_t)s.num_rows, kID * 2, 64,
                      box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
-    if (FP8)  // [Q x 4 parts x 32 heads] rows of 128 codes; one box = a chunk's NM rows
-        e = make_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, qp, kID, (uint64_t)num_q * 4 * kIH, kID, kID, C::NM,
+    if (FP8)  // [Q x 3 parts x 32 heads] rows of 128 codes; one box = a chunk's NM rows
+        e = make_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, qp, kID, (uint64_t)num_q * kQParts * kIH, kID, kID, C::NM,
                      CU_TENSOR_MAP_SWIZZLE_128B);
     else
         e = make_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qp, KP, (uint64_t)num_q * kIH, KP * 2, 64, C::N,
