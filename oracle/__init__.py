@@ -77,6 +77,11 @@ def _bind(path: str):
     L.oracle_sparse_mla.restype = ctypes.c_int
     L.oracle_latent_row_bytes.argtypes, L.oracle_latent_row_bytes.restype = [I32], I64
     L.oracle_index_row_bytes.argtypes, L.oracle_index_row_bytes.restype = [I32], I64
+    L.oracle_bf16_encode.argtypes, L.oracle_bf16_encode.restype = [D], ctypes.c_uint16
+    L.oracle_e4m3_encode.argtypes, L.oracle_e4m3_encode.restype = [D], ctypes.c_uint8
+    L.oracle_index_k.argtypes, L.oracle_index_k.restype = [I32, P, P, P, D, P, P, P], ctypes.c_int
+    L.oracle_latent_k.argtypes, L.oracle_latent_k.restype = [I32, P, P, P, P, P], ctypes.c_int
+    L.oracle_mla_q.argtypes, L.oracle_mla_q.restype = [I32, P, P, P, P, P, P], ctypes.c_int
     return L
 
 
@@ -198,3 +203,60 @@ def sparse_mla(q, latent, layout: Layout, seq: int, idx, topk_len: int, sm_scale
     _check((L or lib()).oracle_sparse_mla(_ptr(qq), LATENT_DS_MLA if fp8 else LATENT_BF16, _ptr(lat), ctypes.byref(st),
                                    seq, _ptr(ii), topk_len, sm_scale, _ptr(out), _ptr(lse), _ptr(probs)))
     return out, lse, (probs[:, :topk_len] if want_probs else None)
+
+
+# ---- the cache-write side
+def bf16_encode(v: float, L=None) -> int:
+    return int((L or lib()).oracle_bf16_encode(float(v)))
+
+
+def e4m3_encode(v: float, L=None) -> int:
+    return int((L or lib()).oracle_e4m3_encode(float(v)))
+
+
+def index_k(x, gamma, beta, eps: float, pos, inv_freq=None, L=None) -> np.ndarray:
+    """LayerNorm + RoPE of new indexer keys: fp64 [n,128] before storage rounding."""
+    xx = _np(x, np.uint16).reshape(-1, 128)
+    g, b = _np(gamma, np.float32), _np(beta, np.float32)
+    pp = _np(pos, np.int32)
+    fr = None if inv_freq is None else _np(inv_freq, np.float32)
+    out = np.empty((xx.shape[0], 128), np.float64)
+    _check((L or lib()).oracle_index_k(xx.shape[0], _ptr(xx), _ptr(g), _ptr(b), float(eps), _ptr(pp), _ptr(fr),
+                                       _ptr(out)))
+    return out
+
+
+def latent_k(c_kv, k_pe, pos, inv_freq=None, L=None) -> np.ndarray:
+    """New latent rows: fp64 [n,576] (512 copied, 64 rotated) before storage rounding."""
+    c = _np(c_kv, np.uint16).reshape(-1, 512)
+    k = _np(k_pe, np.uint16).reshape(-1, 64)
+    pp = _np(pos, np.int32)
+    fr = None if inv_freq is None else _np(inv_freq, np.float32)
+    out = np.empty((c.shape[0], 576), np.float64)
+    _check((L or lib()).oracle_latent_k(c.shape[0], _ptr(c), _ptr(k), _ptr(pp), _ptr(fr), _ptr(out)))
+    return out
+
+
+def mla_q(q, ssmax_s, ssmax_b, pos, inv_freq=None, L=None) -> np.ndarray:
+    """Attention queries after RoPE + SSMax: fp64 [nq,64,576] before rounding."""
+    qq = _np(q, np.uint16).reshape(-1, 64, 576)
+    ss, sb = _np(ssmax_s, np.float32), _np(ssmax_b, np.float32)
+    pp = _np(pos, np.int32)
+    fr = None if inv_freq is None else _np(inv_freq, np.float32)
+    out = np.empty(qq.shape, np.float64)
+    _check((L or lib()).oracle_mla_q(qq.shape[0], _ptr(qq), _ptr(ss), _ptr(sb), _ptr(fr), _ptr(pp), _ptr(out)))
+    return out
+
+
+def quantize_rows_e4m3(v, group: int, L=None):
+    """Per-group e4m3 quantisation of fp64 rows v [n, d] (groups of `group`
+    consecutive values): scale = amax / 448 (1 when amax is 0), codes =
+    e4m3_encode(v / scale).  Returns (codes uint8 [n, d], scales fp64 [n, d / group])."""
+    v = np.asarray(v, np.float64)
+    n, d = v.shape
+    g = v.reshape(n, d // group, group)
+    amax = np.abs(g).max(axis=2)
+    scale = np.where(amax > 0, amax / 448.0, 1.0)
+    enc = np.vectorize(lambda x: e4m3_encode(x, L), otypes=[np.uint8])
+    codes = enc(g / scale[:, :, None]).reshape(n, d)
+    return codes, scale

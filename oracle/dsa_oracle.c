@@ -282,3 +282,105 @@ int oracle_sparse_mla(const uint16_t* q, int32_t latent_kind, const void* latent
     free(s);
     return 0;
 }
+
+/* ---------------------------------------------------------------------------
+ * The cache-write side.  Encoders: round to nearest, ties to the even
+ * significand, written out from the two formats' definitions. */
+uint16_t oracle_bf16_encode(double v) {
+    if (isnan(v)) return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);                 /* a = m 2^e, m in [0.5, 1): the leading bit is 2^(e-1) */
+    int lead = e - 1;
+    if (lead < -126) lead = -126; /* subnormals: the quantum stays 2^-133 */
+    double q = ldexp(1.0, lead - 7);
+    double r = rint(a / q);       /* exact division by a power of two; rint ties to even */
+    double val = r * q;
+    if (val >= ldexp(2.0, 127)) return sign | 0x7F80;  /* past the largest finite: infinity */
+    int be;
+    frexp(val, &be);
+    if (be - 1 < -126) return sign | (uint16_t)r;      /* subnormal: the significand is the code */
+    uint16_t ebits = (uint16_t)(be - 1 + 127);
+    uint16_t mbits = (uint16_t)((int64_t)rint(ldexp(val, -(be - 1) + 7)) - 128);
+    return sign | (uint16_t)(ebits << 7) | mbits;
+}
+
+uint8_t oracle_e4m3_encode(double v) {
+    if (isnan(v)) return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);
+    int lead = e - 1;
+    if (lead < -6) lead = -6;     /* subnormals: the quantum stays 2^-9 */
+    double q = ldexp(1.0, lead - 3);
+    double val = rint(a / q) * q;
+    if (val > 448.0) val = 448.0; /* saturate */
+    if (val == 0.0) return sign;
+    int be;
+    frexp(val, &be);
+    if (be - 1 < -6) return sign | (uint8_t)rint(val / ldexp(1.0, -9));  /* subnormal */
+    uint8_t ebits = (uint8_t)(be - 1 + 7);
+    uint8_t mbits = (uint8_t)((int64_t)rint(ldexp(val, -(be - 1) + 3)) - 8);
+    return sign | (uint8_t)(ebits << 3) | mbits;
+}
+
+/* rotate 32 interleaved pairs of v by pos * inv_freq_i ([colibri] RoPE and the rest) */
+static void rope32(double* v, int32_t pos, const float* inv_freq) {
+    for (int i = 0; i < RP; ++i) {
+        double ang = (double)inv_freq[i] * (double)pos;
+        double c = cos(ang), s = sin(ang);
+        double x0 = v[2 * i], x1 = v[2 * i + 1];
+        v[2 * i] = x0 * c - x1 * s;
+        v[2 * i + 1] = x0 * s + x1 * c;
+    }
+}
+
+int oracle_index_k(int32_t n, const uint16_t* x, const float* gamma, const float* beta, double eps,
+                   const int32_t* pos, const float* inv_freq, double* out) {
+    if (n < 0 || !x || !gamma || !beta || !pos || !out || !(eps >= 0.0)) return ORACLE_ERR_ARG;
+    for (int32_t t = 0; t < n; ++t) {
+        double v[ID], mean = 0.0, var = 0.0;
+        for (int d = 0; d < ID; ++d) mean += (v[d] = oracle_bf16_value(x[(int64_t)t * ID + d]));
+        mean /= ID;
+        for (int d = 0; d < ID; ++d) var += (v[d] - mean) * (v[d] - mean);
+        var /= ID;
+        double inv = 1.0 / sqrt(var + eps);
+        for (int d = 0; d < ID; ++d) v[d] = (v[d] - mean) * inv * (double)gamma[d] + (double)beta[d];
+        if (inv_freq) rope32(v, pos[t], inv_freq);
+        for (int d = 0; d < ID; ++d) out[(int64_t)t * ID + d] = v[d];
+    }
+    return 0;
+}
+
+int oracle_latent_k(int32_t n, const uint16_t* c_kv, const uint16_t* k_pe, const int32_t* pos,
+                    const float* inv_freq, double* out) {
+    if (n < 0 || !c_kv || !k_pe || !pos || !out) return ORACLE_ERR_ARG;
+    for (int32_t t = 0; t < n; ++t) {
+        double* o = out + (int64_t)t * MD;
+        for (int d = 0; d < MV; ++d) o[d] = oracle_bf16_value(c_kv[(int64_t)t * MV + d]);
+        for (int d = 0; d < MD - MV; ++d) o[MV + d] = oracle_bf16_value(k_pe[(int64_t)t * (MD - MV) + d]);
+        if (inv_freq) rope32(o + MV, pos[t], inv_freq);
+    }
+    return 0;
+}
+
+int oracle_mla_q(int32_t nq, const uint16_t* q, const float* ssmax_s, const float* ssmax_b,
+                 const float* inv_freq, const int32_t* pos, double* out) {
+    if (nq < 0 || !q || !ssmax_s || !ssmax_b || !pos || !out) return ORACLE_ERR_ARG;
+    for (int32_t t = 0; t < nq; ++t) {
+        if (pos[t] < 0) return ORACLE_ERR_POS;
+        for (int h = 0; h < MH; ++h) {
+            const uint16_t* qi = q + ((int64_t)t * MH + h) * MD;
+            double* o = out + ((int64_t)t * MH + h) * MD;
+            double f = (double)ssmax_s[h] * log((double)pos[t] + 1.0) + (double)ssmax_b[h];
+            for (int d = 0; d < MD; ++d) o[d] = oracle_bf16_value(qi[d]);
+            if (inv_freq) rope32(o + MV, pos[t], inv_freq);
+            for (int d = 0; d < MD; ++d) o[d] *= f;
+        }
+    }
+    return 0;
+}

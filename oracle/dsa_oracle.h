@@ -83,6 +83,38 @@ int oracle_sparse_mla(const uint16_t* q /*[64,576]*/, int32_t latent_kind, const
 int64_t oracle_latent_row_bytes(int32_t latent_kind);
 int64_t oracle_index_row_bytes(int32_t key_kind);
 
+/* ---- the cache-write side (the kernels on either side of the decode path) ----
+ *
+ * Round-to-nearest-even encoders (the decoders above are their inverses):
+ * bf16 (8 significant bits, subnormals kept) and OCP e4m3 (4 significant
+ * bits, subnormals 2^-9 apart, saturating at +-448; NaN -> 0x7F). */
+uint16_t oracle_bf16_encode(double v);
+uint8_t oracle_e4m3_encode(double v);
+
+/* Indexer key of n new tokens ([colibri] The indexer: k = LayerNorm(wk(x)),
+ * rotated on its first 64 dims on RoPE layers): x [n,128] bf16 bits (the
+ * projection's output), LayerNorm over the 128 dims with biased variance,
+ * (x - mean) / sqrt(var + eps) * gamma + beta, then on RoPE layers the pairs
+ * (2i, 2i+1), i < 32, rotated by pos[t] * inv_freq[i].  out [n,128], exact
+ * values before storage rounding. */
+int oracle_index_k(int32_t n, const uint16_t* x, const float* gamma, const float* beta, double eps,
+                   const int32_t* pos, const float* inv_freq /*[32] or NULL = NoPE*/, double* out);
+
+/* Latent row of n new tokens ([vLLM-ML4] Model architecture: KV LoRA rank
+ * 512 + RoPE dim 64): c_kv [n,512] bf16 bits copied, k_pe [n,64] bf16 bits
+ * rotated as interleaved pairs by pos[t] * inv_freq[i] on RoPE layers.
+ * out [n,576], exact values before storage rounding. */
+int oracle_latent_k(int32_t n, const uint16_t* c_kv, const uint16_t* k_pe, const int32_t* pos,
+                    const float* inv_freq /*[32] or NULL*/, double* out);
+
+/* Attention query of nq queries ([colibri] SSMax: every head's query times
+ * s_h ln(pos+1) + b_h; [vLLM-ML4] fusions "MLA RoPE + SSMax"): q [nq,64,576]
+ * bf16 bits (absorbed: 512 latent dims + 64 RoPE dims), the RoPE dims
+ * rotated as interleaved pairs by pos * inv_freq on RoPE layers, every dim
+ * of head h times f_h.  out [nq,64,576], exact values before rounding. */
+int oracle_mla_q(int32_t nq, const uint16_t* q, const float* ssmax_s, const float* ssmax_b /*[64]*/,
+                 const float* inv_freq /*[32] or NULL*/, const int32_t* pos, double* out);
+
 #ifdef __cplusplus
 }
 #endif

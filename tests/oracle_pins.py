@@ -517,4 +517,135 @@ def pin_mla_paged(L):
     close(la, lb, 0.0)
 
 
+# ---------------------------------------------------------------------------
+# the cache-write side: encoders, indexer key, latent row, attention query
+def pin_e4m3_encode_roundtrip(L):
+    """Every finite e4m3 code encodes back from its own value (both zeros)."""
+    for c in range(256):
+        if (c & 0x7F) == 0x7F:
+            continue
+        assert oracle.e4m3_encode(oracle.e4m3_value(c, L), L) == c, hex(c)
+
+
+def pin_e4m3_encode_ties_and_range(L):
+    """Midpoints between neighbouring codes go to the even code; past 448 the
+    code saturates; below half the smallest subnormal it is zero."""
+    for c in range(0, 0x7E):
+        lo, hi = oracle.e4m3_value(c, L), oracle.e4m3_value(c + 1, L)
+        want = c if c % 2 == 0 else c + 1
+        assert oracle.e4m3_encode((lo + hi) / 2, L) == want, hex(c)
+        assert oracle.e4m3_encode(lo + (hi - lo) * 0.49, L) == c
+        assert oracle.e4m3_encode(-(lo + (hi - lo) * 0.51), L) == 0x80 | (c + 1)
+    assert oracle.e4m3_encode(449.0, L) == 0x7E and oracle.e4m3_encode(-1e9, L) == 0xFE
+    assert oracle.e4m3_encode(2.0 ** -11, L) == 0 and oracle.e4m3_encode(2.0 ** -10 * 1.01, L) == 1
+
+
+def pin_bf16_encode(L):
+    """Every finite bf16 pattern encodes back from its value; values exact in
+    fp32 round like numpy's nearest-even bit rounding; ties to even."""
+    for b in range(0, 1 << 16, 7):
+        if (b & 0x7F80) == 0x7F80:
+            continue
+        assert oracle.bf16_encode(oracle.bf16_value(b, L), L) == b, hex(b)
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(500) * np.exp(rng.uniform(-20, 20, 500))).astype(np.float32)
+    want = bf16_bits(x)
+    got = np.array([oracle.bf16_encode(float(v), L) for v in x], np.uint16)
+    assert np.array_equal(got, want)
+    assert oracle.bf16_encode(1.0 + 2.0 ** -8, L) == 0x3F80 and oracle.bf16_encode(1.0 + 3 * 2.0 ** -8, L) == 0x3F82
+
+
+def _insert_rows(n, d, seed):
+    rng = np.random.default_rng(seed)
+    return bf16_bits(rng.standard_normal((n, d)) * 2.0 + 0.3)
+
+
+def pin_index_k_layer_norm_library(L):
+    """NoPE: the key is torch's fp64 layer_norm of the bf16 inputs."""
+    import torch
+    x = _insert_rows(6, 128, 11)
+    rng = np.random.default_rng(12)
+    g = rng.uniform(0.5, 1.5, 128).astype(np.float32)
+    b = rng.uniform(-0.2, 0.2, 128).astype(np.float32)
+    got = oracle.index_k(x, g, b, 1e-6, np.arange(6, dtype=np.int32), None, L=L)
+    xv = torch.from_numpy(np.array([[oracle.bf16_value(int(v), L) for v in row] for row in x]))
+    want = torch.nn.functional.layer_norm(xv, (128,), torch.from_numpy(g).double(), torch.from_numpy(b).double(),
+                                          eps=1e-6).numpy()
+    close(got, want, 1e-11)
+
+
+def pin_index_k_constant_row_is_beta(L):
+    """A constant input row normalises to zero, leaving beta (rotated on RoPE layers)."""
+    x = np.full((1, 128), bf16_bits(np.array([3.0]))[0], np.uint16)
+    g = np.full(128, 2.0, np.float32)
+    b = (np.arange(128) / 128.0).astype(np.float32)
+    got = oracle.index_k(x, g, b, 1e-6, np.array([0], np.int32), None, L=L)
+    close(got[0], b.astype(np.float64), 1e-12)
+
+
+def pin_index_k_rope_complex(L):
+    """RoPE layers: dims 0..63 as complex pairs x0 + i x1 times exp(i pos f);
+    dims 64..127 as without rotation."""
+    x = _insert_rows(4, 128, 13)
+    g = np.ones(128, np.float32)
+    b = np.zeros(128, np.float32)
+    fr = (1.0 / 10000.0 ** (np.arange(32) / 32.0)).astype(np.float32)
+    pos = np.array([0, 5, 1000, 77777], np.int32)
+    plain = oracle.index_k(x, g, b, 1e-6, pos, None, L=L)
+    rot = oracle.index_k(x, g, b, 1e-6, pos, fr, L=L)
+    z = (plain[:, 0:64:2] + 1j * plain[:, 1:64:2]) * np.exp(1j * pos[:, None].astype(np.float64) * fr.astype(np.float64))
+    close(rot[:, 0:64:2], z.real, 1e-10)
+    close(rot[:, 1:64:2], z.imag, 1e-10)
+    close(rot[:, 64:], plain[:, 64:], 0.0)
+
+
+def pin_latent_k(L):
+    """The 512 latent dims are the inputs' values; the 64 RoPE dims are the
+    k_pe values rotated as complex pairs (unrotated without a frequency table)."""
+    c = _insert_rows(3, 512, 14)
+    k = _insert_rows(3, 64, 15)
+    fr = (0.5 / 10000.0 ** (np.arange(32) / 32.0)).astype(np.float32)
+    pos = np.array([1, 33, 4095], np.int32)
+    got = oracle.latent_k(c, k, pos, fr, L=L)
+    cv = np.array([[oracle.bf16_value(int(v), L) for v in row] for row in c])
+    kv = np.array([[oracle.bf16_value(int(v), L) for v in row] for row in k])
+    close(got[:, :512], cv, 0.0)
+    z = (kv[:, 0::2] + 1j * kv[:, 1::2]) * np.exp(1j * pos[:, None].astype(np.float64) * fr.astype(np.float64))
+    close(got[:, 512::2], z.real, 1e-10)
+    close(got[:, 513::2], z.imag, 1e-10)
+    close(oracle.latent_k(c, k, pos, None, L=L)[:, 512:], kv, 0.0)
+
+
+def pin_mla_q(L):
+    """Every dim of head h times s_h ln(pos+1) + b_h; RoPE dims rotated first
+    (complex pairs); position 0 gives the factor b_h."""
+    rng = np.random.default_rng(16)
+    q = _insert_rows(2 * 64, 576, 17).reshape(2, 64, 576)
+    ss = rng.uniform(0.05, 0.15, 64).astype(np.float32)
+    sb = rng.uniform(0.9, 1.1, 64).astype(np.float32)
+    fr = (1.0 / 10000.0 ** (np.arange(32) / 32.0)).astype(np.float32)
+    pos = np.array([0, 9000], np.int32)
+    got = oracle.mla_q(q, ss, sb, pos, fr, L=L)
+    qv = np.vectorize(lambda b: oracle.bf16_value(int(b), L))(q)
+    f = ss[None, :].astype(np.float64) * np.log(pos[:, None] + 1.0) + sb[None, :].astype(np.float64)
+    close(got[:, :, :512], qv[:, :, :512] * f[:, :, None], 1e-12)
+    z = (qv[:, :, 512::2] + 1j * qv[:, :, 513::2]) * np.exp(1j * pos[:, None, None] * fr.astype(np.float64))
+    close(got[:, :, 512::2], z.real * f[:, :, None], 1e-10)
+    close(got[:, :, 513::2], z.imag * f[:, :, None], 1e-10)
+    close(got[0, :, :512], qv[0, :, :512] * sb[:, None].astype(np.float64), 1e-12)
+
+
+def pin_quantize_rows_e4m3(L):
+    """Per-group quantisation: the largest magnitude of a group maps to +-448,
+    and every value is recovered within half an e4m3 step of its scaled self."""
+    rng = np.random.default_rng(18)
+    v = rng.standard_normal((5, 512)) * np.exp(rng.uniform(-3, 3, (5, 1)))
+    codes, scale = oracle.quantize_rows_e4m3(v, 128, L=L)
+    dec = np.vectorize(lambda c: oracle.e4m3_value(int(c), L))(codes).reshape(5, 4, 128) * scale[:, :, None]
+    g = v.reshape(5, 4, 128)
+    assert np.all(np.abs(np.abs(dec).max(axis=2) - np.abs(g).max(axis=2)) <= 1e-12 * np.abs(g).max(axis=2))
+    step = np.exp2(np.floor(np.log2(np.maximum(np.abs(g / scale[:, :, None]), 2.0 ** -6))) - 3) * scale[:, :, None]
+    assert np.all(np.abs(dec - g) <= 0.5 * step * (1 + 1e-12))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

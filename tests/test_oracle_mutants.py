@@ -73,6 +73,25 @@ MUTANTS = [
     ("mla_empty_lse_zero", "lse[h] = -INFINITY;", "lse[h] = 0.0;"),
     ("mla_unnormalised", "double p = exp(s[j] - mx) / l;", "double p = exp(s[j] - mx);"),
     ("mla_query_head", "qd[d] = oracle_bf16_value(q[h * MD + d]);", "qd[d] = oracle_bf16_value(q[((h + 1) % MH) * MD + d]);"),
+    # the cache-write side
+    ("e4m3_encode_round_half_up", "double val = rint(a / q) * q;", "double val = floor(a / q + 0.5) * q;"),
+    ("e4m3_encode_no_saturation", "if (val > 448.0) val = 448.0; /* saturate */", ";"),
+    ("e4m3_encode_subnormal_quantum", "if (lead < -6) lead = -6;     /* subnormals: the quantum stays 2^-9 */",
+     "if (lead < -7) lead = -7;"),
+    ("bf16_encode_truncate", "double r = rint(a / q);       /* exact division by a power of two; rint ties to even */",
+     "double r = floor(a / q);"),
+    ("bf16_encode_exponent_bias", "uint16_t ebits = (uint16_t)(be - 1 + 127);", "uint16_t ebits = (uint16_t)(be - 1 + 126);"),
+    ("layer_norm_unbiased_variance", "        var /= ID;", "        var /= (ID - 1);"),
+    ("layer_norm_no_eps", "double inv = 1.0 / sqrt(var + eps);", "double inv = 1.0 / sqrt(var);"),
+    ("layer_norm_gamma_beta_swapped", "v[d] = (v[d] - mean) * inv * (double)gamma[d] + (double)beta[d];",
+     "v[d] = (v[d] - mean) * inv * (double)beta[d] + (double)gamma[d];"),
+    ("rope32_sign", "v[2 * i] = x0 * c - x1 * s;", "v[2 * i] = x0 * c + x1 * s;"),
+    ("latent_rope_not_applied", "        if (inv_freq) rope32(o + MV, pos[t], inv_freq);\n    }\n    return 0;\n}\n\nint oracle_mla_q",
+     "        (void)0;\n    }\n    return 0;\n}\n\nint oracle_mla_q"),
+    ("mla_q_ssmax_skips_rope_dims", "for (int d = 0; d < MD; ++d) o[d] *= f;", "for (int d = 0; d < MV; ++d) o[d] *= f;"),
+    ("mla_q_ssmax_head_index",
+     "double f = (double)ssmax_s[h] * log((double)pos[t] + 1.0) + (double)ssmax_b[h];",
+     "double f = (double)ssmax_s[(h + 1) % MH] * log((double)pos[t] + 1.0) + (double)ssmax_b[h];"),
 ]
 
 RUNNER = r"""
