@@ -45,7 +45,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="paged", choices=sorted(I.WORKLOADS))
+    ap.add_argument("--workload", default="paged", choices=sorted(I.WORKLOADS) + ["insert"],
+                    help="a decode layer workload, or 'insert': the cache-write side")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak-s", type=float, default=1.0, help="untimed load before the timed region (clocks)")
     ap.add_argument("--seqs", type=int, default=0, help="override the number of sequences (small profiling cases)")
@@ -60,7 +61,7 @@ def dist_env():
 
 
 # ---------------------------------------------------------------------------
-# algorithmic bytes (per launch / per step), see DESIGN.md "Roofline"
+# algorithmic bytes per launch and per step: each byte a kernel must move at least once
 def index_row_bytes(wl):
     return 132 if wl.index_fp8 else 256
 
@@ -433,9 +434,117 @@ def run_ours(args, wl, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+INSERT_TOKENS = 1 << 20
+INSERT_BYTES_PER_TOKEN = (256 + 132) + (1024 + 128 + 656) + 2 * (8 + 4)  # key in/out, latent in/out, slot + pos
+
+
+def run_insert(args, ws, rank, local):
+    """The cache-write side: a step inserts INSERT_TOKENS new tokens (indexer
+    key: LayerNorm + RoPE + e4m3 with a row scale; latent: RoPE + fp8_ds_mla)
+    into caches of as many rows, 64-token pages in a random order.  HBM-bound: 2,220 algorithmic
+    bytes per token."""
+    n = INSERT_TOKENS
+    metric, unit = "cache-insert tokens/s (indexer key e4m3 + fp8_ds_mla latent)", "tokens/s"
+    cfg = {"workload": f"insert: {n} new tokens, LayerNorm + RoPE + e4m3/row-scale indexer keys and RoPE + "
+                       f"fp8_ds_mla latent rows into {n}-row caches of 64-token pages in a random page order",
+           "l2": "inputs larger than L2 (%.0f MB in, %.0f MB out per step)" % (n * 1432 / 1e6, n * 788 / 1e6),
+           "parallelism": "single GPU" if ws == 1 else f"replicas x{ws}"}
+    if args.impl == "reference":
+        import oracle
+        oracle.build()
+        h = I.make_insert_inputs(1024, 1, 1024, "cpu", seed=0)
+        K = max(1, args.steps)
+        t0 = time.time()
+        for _ in range(K):
+            k = oracle.index_k(h["x"], h["gamma"], h["beta"], 1e-6, h["pos"], h["inv_freq"])
+            oracle.quantize_rows_e4m3(k, 128)
+            lat = oracle.latent_k(h["c_kv"], h["k_pe"], h["pos"], h["inv_freq"])
+            oracle.quantize_rows_e4m3(lat[:, :512], 128)
+        secs = (time.time() - t0) / K
+        v = 1024 / secs
+        print(json.dumps({"metric": metric, "value": v, "unit": unit, "n_gpus": ws, "steps": K, "warmup": 0,
+                          "ms_per_step": secs * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                          "dtype": "f64", "data": "synthetic", "config": cfg, "impl": "reference",
+                          "cpu_baseline": {"value": v, "unit": unit, "cores": 1, "kind": "oracle",
+                                           "sample": "1024 new tokens per step, key and latent rows with their "
+                                                     "quantisation, one host thread"},
+                          "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+    import dsa_sparse_mla_query_gb300 as dsa
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dsa.load()
+    d = I.make_insert_inputs(n, 1, n, dev, seed=0, page_size=64)
+    keys = torch.zeros((n, 128), dtype=torch.uint8, device=dev)
+    k_scale = torch.zeros(n, dtype=torch.float32, device=dev)
+    latent = torch.zeros((n, I.DS_MLA_ROW_BYTES), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        dsa.dsa_index_k_insert(d["x"], d["gamma"], d["beta"], 1e-6, d["pos"], d["inv_freq"], d["slot"], n, keys,
+                               k_scale, dsa.DSA_FP8_E4M3_ROWSCALE, n, st, stream)
+        dsa.dsa_latent_insert(d["c_kv"], d["k_pe"], d["pos"], d["inv_freq"], d["slot"], n, latent,
+                              dsa.DSA_FP8_DS_MLA, n, st, stream)
+
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local)
+    t_soak = time.time()
+    while time.time() < t_soak + args.soak_s:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_done = time.time()
+    ms = e0.elapsed_time(e1) / K
+    clocks = sampler.stop(t_soak, t_done)
+    # end to end: the new tokens' inputs from pinned host memory each step, the status word back
+    keys_in = ["x", "c_kv", "k_pe", "pos", "slot"]
+    host = {k: d[k].cpu().pin_memory() for k in keys_in}
+    st_h = torch.zeros(1, dtype=torch.int32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    e0.record(stream)
+    for _ in range(K):
+        for k, v in host.items():
+            d[k].copy_(v, non_blocking=True)
+        step()
+        st_h.copy_(st, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / K
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+    peak, peak_kind = measured_peaks()
+    ab = n * INSERT_BYTES_PER_TOKEN
+    achieved = ab / (ms / 1000.0) / 1e9
+    print(json.dumps({"metric": metric, "value": n / (ms / 1000.0), "unit": unit, "n_gpus": ws, "steps": K,
+                      "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                      "vs_baseline": None, "dtype": "e4m3/bf16", "data": "synthetic", "config": cfg,
+                      "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                                   "frac": achieved / peak, "traffic": None,
+                                   "kernel": "index_k_insert + latent_insert (one step)",
+                                   "algorithmic_bytes_per_launch": ab, "peak_kind": f"{peak_kind} HBM copy"},
+                      "e2e": {"value": n / (e2e_ms / 1000.0), "unit": unit, "h2d_bytes_per_step": h2d,
+                              "d2h_bytes_per_step": 4},
+                      "gpu_launches": 2 * K, "clocks": clocks, "cpu_baseline": None}))
+
+
 def main():
     args = parse()
     ws, rank, local = dist_env()
+    if args.workload == "insert":
+        if ws > 1 and rank != 0 and args.impl == "reference":
+            return
+        run_insert(args, ws, rank, local)
+        return
     wl = I.WORKLOADS[args.workload]
     if args.seqs:
         wl = I.scaled(wl, num_seqs=args.seqs)

@@ -1,5 +1,7 @@
 """GB300 (sm_103a) DSA decode path: lightning indexer -> exact top-k -> sparse
-absorbed-MLA attention, as hand-written CUDA behind a C ABI (include/dsa.h).
+absorbed-MLA attention, as hand-written CUDA behind a C ABI (include/dsa.h),
+plus the cache-write side (new indexer keys and latent rows into the caches,
+the attention query's RoPE + SSMax).
 
 The Python names mirror the C entry points; they only marshal arguments.
 Importing the package loads nothing; the first call loads ``libdsa.so`` and
@@ -14,7 +16,10 @@ from ._binding import (  # noqa: F401
     Seqs,
     dsa_decode_layer,
     dsa_decode_layer_launches,
+    dsa_index_k_insert,
     dsa_index_scores,
+    dsa_latent_insert,
+    dsa_mla_q_prep,
     dsa_topk,
     dsa_workspace_size,
     load,
@@ -24,4 +29,5 @@ from ._binding import (  # noqa: F401
 )
 
 __all__ = ["Seqs", "DsaError", "dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode", "sparse_mla_decode_noalloc",
-           "dsa_decode_layer", "dsa_decode_layer_launches", "load", "version", "DSA_BF16", "DSA_FP8_E4M3_ROWSCALE", "DSA_FP8_DS_MLA"]
+           "dsa_decode_layer", "dsa_decode_layer_launches", "dsa_index_k_insert", "dsa_latent_insert", "dsa_mla_q_prep",
+           "load", "version", "DSA_BF16", "DSA_FP8_E4M3_ROWSCALE", "DSA_FP8_DS_MLA"]

@@ -71,6 +71,10 @@ def load(path: str = LIB_PATH):
         L.sparse_mla_decode_noalloc.argtypes = [P, P, ctypes.c_int, S, I32, P, P, I32, ctypes.c_float, P, P, P, P]
         L.sparse_mla_decode_noalloc.restype = ctypes.c_int
         L.dsa_decode_layer_launches.argtypes = [S, I32, I32, I32, ctypes.c_int]
+        F = ctypes.c_float
+        L.dsa_index_k_insert.argtypes = [P, P, P, F, P, P, P, I32, P, P, ctypes.c_int, I64, P, P]
+        L.dsa_latent_insert.argtypes = [P, P, P, P, P, I32, P, ctypes.c_int, I64, P, P]
+        L.dsa_mla_q_prep.argtypes = [P, P, P, P, P, I32, P, P, P]
         L.dsa_decode_layer_launches.restype = ctypes.c_int32
         for f in ("dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode", "dsa_decode_layer"):
             getattr(L, f).restype = ctypes.c_int
@@ -196,3 +200,21 @@ def dsa_decode_layer(args: dict, seqs: Seqs, num_q: int, workspace, workspace_by
 
 def version() -> str:
     return load().dsa_version().decode()
+
+
+# ---- the cache-write side (include/dsa.h)
+def dsa_index_k_insert(x, ln_gamma, ln_beta, ln_eps: float, pos, inv_freq, slot, n: int, k_cache, k_scale,
+                       k_dtype: int, num_rows: int, d_status=None, stream=None):
+    _check(load().dsa_index_k_insert(_p(x), _p(ln_gamma), _p(ln_beta), float(ln_eps), _p(pos), _p(inv_freq), _p(slot),
+                                     n, _p(k_cache), _p(k_scale), k_dtype, num_rows, _p(d_status), _stream(stream)))
+
+
+def dsa_latent_insert(c_kv, k_pe, pos, inv_freq, slot, n: int, latent, latent_dtype: int, num_rows: int,
+                      d_status=None, stream=None):
+    _check(load().dsa_latent_insert(_p(c_kv), _p(k_pe), _p(pos), _p(inv_freq), _p(slot), n, _p(latent), latent_dtype,
+                                    num_rows, _p(d_status), _stream(stream)))
+
+
+def dsa_mla_q_prep(q, ssmax_s, ssmax_b, inv_freq, q_pos, num_q: int, q_out, d_status=None, stream=None):
+    _check(load().dsa_mla_q_prep(_p(q), _p(ssmax_s), _p(ssmax_b), _p(inv_freq), _p(q_pos), num_q, _p(q_out),
+                                 _p(d_status), _stream(stream)))

@@ -142,6 +142,18 @@ Workspace carve_workspace(void* base, const dsa_seqs& s, int num_q, int k) {
 
 }  // namespace dsa
 
+namespace dsa {
+cudaError_t launch_index_k_insert(const void* x, const float* gamma, const float* beta, float eps, const int32_t* pos,
+                                  const float* inv_freq, const int64_t* slot, int32_t n, void* cache, float* k_scale,
+                                  bool fp8, int64_t num_rows, int32_t* d_status, cudaStream_t stream);
+cudaError_t launch_latent_insert(const void* c_kv, const void* k_pe, const int32_t* pos, const float* inv_freq,
+                                 const int64_t* slot, int32_t n, void* latent, bool fp8, int64_t num_rows,
+                                 int32_t* d_status, cudaStream_t stream);
+cudaError_t launch_mla_q_prep(const void* q, const float* ssmax_s, const float* ssmax_b, const float* inv_freq,
+                              const int32_t* q_pos, int32_t num_q, void* q_out, int32_t* d_status,
+                              cudaStream_t stream);
+}  // namespace dsa
+
 using namespace dsa;
 
 extern "C" {
@@ -203,6 +215,75 @@ dsa_status dsa_index_scores(const void* q_idx, const float* w, const float* ssma
     return cuda_status(launch_index_scores(q_idx, w, ssmax_s, ssmax_b, inv_freq, k_idx, k_scale, k_dtype, *seqs,
                                            num_q, scores, ld, ws, d_status, stream),
                        "dsa_index_scores launch");
+}
+
+
+dsa_status dsa_index_k_insert(const void* x, const float* ln_gamma, const float* ln_beta, float ln_eps,
+                              const int32_t* pos, const float* inv_freq, const int64_t* slot, int32_t n,
+                              void* k_cache, float* k_scale, dsa_dtype k_dtype, int64_t num_rows, int32_t* d_status,
+                              cudaStream_t stream) {
+    Check c;
+    c.need(n >= 0, DSA_ERR_INVALID_ARG, "n %d < 0", n);
+    c.need(num_rows >= 1, DSA_ERR_INVALID_ARG, "num_rows %lld < 1", (long long)num_rows);
+    c.need(k_dtype == DSA_BF16 || k_dtype == DSA_FP8_E4M3_ROWSCALE, DSA_ERR_UNSUPPORTED,
+           "k_dtype %d is neither DSA_BF16 nor DSA_FP8_E4M3_ROWSCALE", (int)k_dtype);
+    c.need(ln_eps >= 0.f, DSA_ERR_INVALID_ARG, "ln_eps must be >= 0");
+    if (n > 0) {
+        c.ptr(x, "x");
+        c.ptr(ln_gamma, "ln_gamma");
+        c.ptr(ln_beta, "ln_beta");
+        c.ptr(pos, "pos", 4);
+        c.ptr(slot, "slot", 8);
+        c.ptr(k_cache, "k_cache");
+        if (inv_freq) c.ptr(inv_freq, "inv_freq", 4);
+        if (k_dtype == DSA_FP8_E4M3_ROWSCALE) c.ptr(k_scale, "k_scale", 4);
+    }
+    dsa_status st = c.done();
+    if (st != DSA_OK || n == 0) return st;
+    return cuda_status(launch_index_k_insert(x, ln_gamma, ln_beta, ln_eps, pos, inv_freq, slot, n, k_cache, k_scale,
+                                             k_dtype == DSA_FP8_E4M3_ROWSCALE, num_rows, d_status, stream),
+                       "dsa_index_k_insert launch");
+}
+
+dsa_status dsa_latent_insert(const void* c_kv, const void* k_pe, const int32_t* pos, const float* inv_freq,
+                             const int64_t* slot, int32_t n, void* latent, dsa_dtype latent_dtype, int64_t num_rows,
+                             int32_t* d_status, cudaStream_t stream) {
+    Check c;
+    c.need(n >= 0, DSA_ERR_INVALID_ARG, "n %d < 0", n);
+    c.need(num_rows >= 1, DSA_ERR_INVALID_ARG, "num_rows %lld < 1", (long long)num_rows);
+    c.need(latent_dtype == DSA_BF16 || latent_dtype == DSA_FP8_DS_MLA, DSA_ERR_UNSUPPORTED,
+           "latent_dtype %d is neither DSA_BF16 nor DSA_FP8_DS_MLA", (int)latent_dtype);
+    if (n > 0) {
+        c.ptr(c_kv, "c_kv");
+        c.ptr(k_pe, "k_pe");
+        c.ptr(pos, "pos", 4);
+        c.ptr(slot, "slot", 8);
+        c.ptr(latent, "latent");
+        if (inv_freq) c.ptr(inv_freq, "inv_freq", 4);
+    }
+    dsa_status st = c.done();
+    if (st != DSA_OK || n == 0) return st;
+    return cuda_status(launch_latent_insert(c_kv, k_pe, pos, inv_freq, slot, n, latent,
+                                            latent_dtype == DSA_FP8_DS_MLA, num_rows, d_status, stream),
+                       "dsa_latent_insert launch");
+}
+
+dsa_status dsa_mla_q_prep(const void* q, const float* ssmax_s, const float* ssmax_b, const float* inv_freq,
+                          const int32_t* q_pos, int32_t num_q, void* q_out, int32_t* d_status, cudaStream_t stream) {
+    Check c;
+    c.need(num_q >= 0, DSA_ERR_INVALID_ARG, "num_q %d < 0", num_q);
+    if (num_q > 0) {
+        c.ptr(q, "q");
+        c.ptr(ssmax_s, "ssmax_s", 4);
+        c.ptr(ssmax_b, "ssmax_b", 4);
+        c.ptr(q_pos, "q_pos", 4);
+        c.ptr(q_out, "q_out");
+        if (inv_freq) c.ptr(inv_freq, "inv_freq", 4);
+    }
+    dsa_status st = c.done();
+    if (st != DSA_OK || num_q == 0) return st;
+    return cuda_status(launch_mla_q_prep(q, ssmax_s, ssmax_b, inv_freq, q_pos, num_q, q_out, d_status, stream),
+                       "dsa_mla_q_prep launch");
 }
 
 dsa_status dsa_topk(const float* scores, int64_t ld, const dsa_seqs* seqs, int32_t num_q, int32_t k, int32_t* idx,

@@ -57,6 +57,8 @@ E4M3_MAX = 448.0
 T_Q_IDX, T_W, T_SSMAX_S, T_SSMAX_B, T_ALPHA = 1, 2, 3, 4, 5
 T_K_IDX, T_LATENT, T_Q_MLA, T_CTX, T_PAGES = 6, 7, 8, 9, 10
 T_LATENT2, T_Q_MLA2 = 11, 12
+# new tokens for the cache-write side
+T_NEW_X, T_NEW_GAMMA, T_NEW_BETA, T_NEW_CKV, T_NEW_KPE, T_NEW_Q, T_NEW_SS, T_NEW_SB, T_NEW_SLOT = range(13, 22)
 
 # ---------------------------------------------------------------------------
 # SplitMix64, counter based
@@ -399,3 +401,36 @@ def params(wl: Workload):
 def scaled(wl: Workload, **kw) -> Workload:
     """A copy of a workload with some fields replaced (small test cases)."""
     return dataclasses.replace(wl, **kw)
+
+
+def make_insert_inputs(n: int, nq: int, num_rows: int, device, seed: int = 0, rope: bool = True,
+                       page_size: int = 0) -> Dict[str, object]:
+    """New tokens for the cache-write side: indexer-key projections x bf16
+    [n,128] ~ N(0.3, 2); LayerNorm gamma ~ U(0.5, 1.5), beta ~ U(-0.2, 0.2)
+    [128]; latent c_kv bf16 [n,512] and k_pe [n,64] ~ N(0,1); attention queries
+    q bf16 [nq,64,576] ~ N(0,1) with SSMax s ~ U(0.05, 0.15), b ~ U(0.9, 1.1)
+    per head; positions 0..n-1 (queries at the last nq); distinct physical rows:
+    a random permutation of the cache rows, or with page_size consecutive
+    tokens filling pages taken in a random order; the workloads' RoPE table."""
+    c = lambda k: _counters(0, k, device)  # noqa: E731
+    out: Dict[str, object] = {}
+    out["x"] = to_bf16(normal(stream_key(seed, T_NEW_X), c(n * INDEX_DIM)) * 2.0 + 0.3).view(n, INDEX_DIM)
+    out["gamma"] = (0.5 + uniform(stream_key(seed, T_NEW_GAMMA), c(INDEX_DIM))).to(torch.float32)
+    out["beta"] = (uniform(stream_key(seed, T_NEW_BETA), c(INDEX_DIM)) * 0.4 - 0.2).to(torch.float32)
+    out["c_kv"] = to_bf16(normal(stream_key(seed, T_NEW_CKV), c(n * MLA_VDIM))).view(n, MLA_VDIM)
+    out["k_pe"] = to_bf16(normal(stream_key(seed, T_NEW_KPE), c(n * MLA_ROPE_DIM))).view(n, MLA_ROPE_DIM)
+    out["q"] = to_bf16(normal(stream_key(seed, T_NEW_Q), c(nq * MLA_HEADS * MLA_DIM))).view(nq, MLA_HEADS, MLA_DIM)
+    out["ssmax_s"] = (0.05 + 0.1 * uniform(stream_key(seed, T_NEW_SS), c(MLA_HEADS))).to(torch.float32)
+    out["ssmax_b"] = (0.9 + 0.2 * uniform(stream_key(seed, T_NEW_SB), c(MLA_HEADS))).to(torch.float32)
+    out["pos"] = torch.arange(n, dtype=torch.int32, device=device)
+    out["q_pos"] = torch.arange(n - nq, n, dtype=torch.int32, device=device)
+    if page_size:
+        pages = torch.argsort(bits(stream_key(seed, T_NEW_SLOT), c(num_rows // page_size)))
+        t = torch.arange(n, dtype=torch.int64, device=device)
+        out["slot"] = pages[t // page_size].to(torch.int64) * page_size + t % page_size
+    else:
+        perm = torch.argsort(bits(stream_key(seed, T_NEW_SLOT), c(num_rows)))
+        out["slot"] = perm[:n].to(torch.int64)
+    out["inv_freq"] = (1.0 / 10000.0 ** (torch.arange(ROPE_PAIRS, dtype=torch.float64, device=device) / ROPE_PAIRS)
+                       ).to(torch.float32) if rope else None
+    return out

@@ -153,6 +153,53 @@ dsa_status sparse_mla_decode(const void* q, const void* latent, dsa_dtype latent
                              void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* d_status,
                              cudaStream_t stream);
 
+/* ---- the cache-write side: the kernels on either side of the decode path ----
+ * Each writes new tokens' rows at the physical rows slot[i] (slot < 0: the
+ * token is skipped; slot >= num_rows or pos < 0: DSA_ERR_BAD_INPUT in
+ * *d_status, the token skipped).  Storage rounding: bf16 to nearest even;
+ * e4m3 (OCP) to nearest even of value / scale, saturating at 448, with
+ * scale = max |value| / 448 over the scale's values (1 when they are all 0). */
+
+/* Indexer keys of n new tokens into the indexer cache ([colibri] The indexer:
+ * k = LayerNorm(wk(x)), rotated on its first 64 dims on RoPE layers;
+ * [vLLM-ML4] Implementation details: the indexer K path written straight
+ * into the FP8 cache; DSA indexer on AITER: one FP8 scale per key):
+ *   k = (x - mean) / sqrt(var + ln_eps) * ln_gamma + ln_beta over the 128 dims
+ *   (biased variance); RoPE layers (inv_freq != NULL): pairs (2i, 2i+1), i < 32,
+ *   rotated by pos*inv_freq[i]; stored as k_dtype DSA_BF16 ([rows,128] bf16) or
+ *   DSA_FP8_E4M3_ROWSCALE ([rows,128] e4m3 codes + k_scale fp32 [rows]).
+ *   x bf16 [n,128] (the projection's output); ln_gamma, ln_beta fp32 [128];
+ *   pos int32 [n]; inv_freq fp32 [32] or NULL; slot int64 [n].
+ * The rows dsa_index_scores reads.  Alignment: every pointer 16-byte aligned
+ * (pos, slot, k_scale, inv_freq: their element size). */
+dsa_status dsa_index_k_insert(const void* x, const float* ln_gamma, const float* ln_beta, float ln_eps,
+                              const int32_t* pos, const float* inv_freq, const int64_t* slot, int32_t n,
+                              void* k_cache, float* k_scale, dsa_dtype k_dtype, int64_t num_rows, int32_t* d_status,
+                              cudaStream_t stream);
+
+/* Latent rows of n new tokens ([vLLM-ML4] Model architecture: KV LoRA rank
+ * 512, RoPE dim 64; Sparse MLA + DSA indexer: the fp8_ds_mla cache, 656
+ * bytes per token): c_kv bf16 [n,512] stored as is (DSA_BF16) or as e4m3 with
+ * one fp32 scale per 128 values (DSA_FP8_DS_MLA: [0,512) codes, [512,528) the
+ * four scales, [528,656) the RoPE dims bf16); k_pe bf16 [n,64] rotated as
+ * interleaved pairs by pos*inv_freq on RoPE layers (NULL: stored as given).
+ * latent: [rows,576] bf16 or [rows,656] bytes; the rows sparse_mla_decode
+ * reads. */
+dsa_status dsa_latent_insert(const void* c_kv, const void* k_pe, const int32_t* pos, const float* inv_freq,
+                             const int64_t* slot, int32_t n, void* latent, dsa_dtype latent_dtype, int64_t num_rows,
+                             int32_t* d_status, cudaStream_t stream);
+
+/* The attention query ([colibri] SSMax: every head's query times
+ * s_h ln(pos+1) + b_h; [vLLM-ML4] Implementation details: MLA RoPE + SSMax):
+ *   q_out[t][h] = f_h(pos_t) * (q[t][h] with dims 512..575 rotated as
+ *   interleaved pairs by pos_t*inv_freq on RoPE layers), rounded to bf16.
+ *   q, q_out bf16 [num_q, 64, 576] (may be the same buffer); ssmax_s, ssmax_b
+ *   fp32 [64]; q_pos int32 [num_q]; inv_freq fp32 [32] or NULL.
+ * The query sparse_mla_decode takes.  A negative position: DSA_ERR_BAD_INPUT,
+ * that query's row left unwritten. */
+dsa_status dsa_mla_q_prep(const void* q, const float* ssmax_s, const float* ssmax_b, const float* inv_freq,
+                          const int32_t* q_pos, int32_t num_q, void* q_out, int32_t* d_status, cudaStream_t stream);
+
 /* One decode layer: dsa_index_scores -> dsa_topk -> sparse_mla_decode on one
  * stream, with the scores kept in the workspace.  reuse_idx != 0 is a
  * shared-indexer layer ([vLLM-ML4] Model architecture: 28 layers reuse the
