@@ -435,14 +435,36 @@ def run_ours(args, wl, ws, rank, local):
 
 
 INSERT_TOKENS = 1 << 20
-INSERT_BYTES_PER_TOKEN = (256 + 132) + (1024 + 128 + 656) + 2 * (8 + 4)  # key in/out, latent in/out, slot + pos
+INSERT_KEY_BYTES = 256 + 132 + 8 + 4        # x in; e4m3 row + scale out; slot + position
+INSERT_LATENT_BYTES = 1024 + 128 + 656 + 8 + 4  # c_kv + k_pe in; fp8_ds_mla row out; slot + position
+INSERT_BYTES_PER_TOKEN = INSERT_KEY_BYTES + INSERT_LATENT_BYTES
+INSERT_ORACLE_TOKENS = 1024
+
+
+def insert_oracle_step(h) -> None:
+    """The oracle's cache-write step: key rows and latent rows with their e4m3 codes."""
+    import oracle
+    k = oracle.index_k(h["x"], h["gamma"], h["beta"], 1e-6, h["pos"], h["inv_freq"])
+    oracle.quantize_rows_e4m3(k, 128)
+    lat = oracle.latent_k(h["c_kv"], h["k_pe"], h["pos"], h["inv_freq"])
+    oracle.quantize_rows_e4m3(lat[:, :512], 128)
+
+
+def insert_oracle_inputs():
+    import oracle
+    oracle.build()
+    return I.make_insert_inputs(INSERT_ORACLE_TOKENS, 1, INSERT_ORACLE_TOKENS, "cpu", seed=0, page_size=64)
+
+
+INSERT_SAMPLE = (f"{INSERT_ORACLE_TOKENS} new tokens per step (key and latent rows with their e4m3 codes), "
+                 "one host thread")
 
 
 def run_insert(args, ws, rank, local):
     """The cache-write side: a step inserts INSERT_TOKENS new tokens (indexer
     key: LayerNorm + RoPE + e4m3 with a row scale; latent: RoPE + fp8_ds_mla)
-    into caches of as many rows, 64-token pages in a random order.  HBM-bound: 2,220 algorithmic
-    bytes per token."""
+    into caches of as many rows, 64-token pages in a random order.  HBM-bound:
+    2,220 algorithmic bytes per token, 1,820 of them the latent insert's."""
     n = INSERT_TOKENS
     metric, unit = "cache-insert tokens/s (indexer key e4m3 + fp8_ds_mla latent)", "tokens/s"
     cfg = {"workload": f"insert: {n} new tokens, LayerNorm + RoPE + e4m3/row-scale indexer keys and RoPE + "
@@ -450,27 +472,30 @@ def run_insert(args, ws, rank, local):
            "l2": "inputs larger than L2 (%.0f MB in, %.0f MB out per step)" % (n * 1432 / 1e6, n * 788 / 1e6),
            "parallelism": "single GPU" if ws == 1 else f"replicas x{ws}"}
     if args.impl == "reference":
-        import oracle
-        oracle.build()
-        h = I.make_insert_inputs(1024, 1, 1024, "cpu", seed=0)
+        h = insert_oracle_inputs()
         K = max(1, args.steps)
         t0 = time.time()
         for _ in range(K):
-            k = oracle.index_k(h["x"], h["gamma"], h["beta"], 1e-6, h["pos"], h["inv_freq"])
-            oracle.quantize_rows_e4m3(k, 128)
-            lat = oracle.latent_k(h["c_kv"], h["k_pe"], h["pos"], h["inv_freq"])
-            oracle.quantize_rows_e4m3(lat[:, :512], 128)
+            insert_oracle_step(h)
         secs = (time.time() - t0) / K
-        v = 1024 / secs
+        v = INSERT_ORACLE_TOKENS / secs
         print(json.dumps({"metric": metric, "value": v, "unit": unit, "n_gpus": ws, "steps": K, "warmup": 0,
                           "ms_per_step": secs * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                           "dtype": "f64", "data": "synthetic", "config": cfg, "impl": "reference",
                           "cpu_baseline": {"value": v, "unit": unit, "cores": 1, "kind": "oracle",
-                                           "sample": "1024 new tokens per step, key and latent rows with their "
-                                                     "quantisation, one host thread"},
+                                           "sample": INSERT_SAMPLE},
                           "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
         return
     import dsa_sparse_mla_query_gb300 as dsa
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        h = insert_oracle_inputs()  # before the first CUDA call
+        t0 = time.time()
+        for _ in range(3):
+            insert_oracle_step(h)
+        secs = (time.time() - t0) / 3
+        cpu = {"value": INSERT_ORACLE_TOKENS / secs, "unit": unit, "cores": 1, "kind": "oracle",
+               "sample": INSERT_SAMPLE + ", 3 steps"}
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     dsa.load()
@@ -481,11 +506,17 @@ def run_insert(args, ws, rank, local):
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def key_insert():
         dsa.dsa_index_k_insert(d["x"], d["gamma"], d["beta"], 1e-6, d["pos"], d["inv_freq"], d["slot"], n, keys,
                                k_scale, dsa.DSA_FP8_E4M3_ROWSCALE, n, st, stream)
+
+    def latent_insert():
         dsa.dsa_latent_insert(d["c_kv"], d["k_pe"], d["pos"], d["inv_freq"], d["slot"], n, latent,
                               dsa.DSA_FP8_DS_MLA, n, st, stream)
+
+    def step():
+        key_insert()
+        latent_insert()
 
     K, W = args.steps, args.warmup
     for _ in range(W):
@@ -506,6 +537,17 @@ def run_insert(args, ws, rank, local):
     t_done = time.time()
     ms = e0.elapsed_time(e1) / K
     clocks = sampler.stop(t_soak, t_done)
+    # each kernel alone, events on its stream around each launch
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for i in range(K):
+        ev[i][0].record(stream)
+        key_insert()
+        ev[i][1].record(stream)
+        latent_insert()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    key_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    lat_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
     # end to end: the new tokens' inputs from pinned host memory each step, the status word back
     keys_in = ["x", "c_kv", "k_pe", "pos", "slot"]
     host = {k: d[k].cpu().pin_memory() for k in keys_in}
@@ -523,18 +565,21 @@ def run_insert(args, ws, rank, local):
     if int(st.item()) != 0:
         raise RuntimeError(f"device status {int(st.item())}")
     peak, peak_kind = measured_peaks()
-    ab = n * INSERT_BYTES_PER_TOKEN
-    achieved = ab / (ms / 1000.0) / 1e9
+    lat_bytes = n * INSERT_LATENT_BYTES
+    achieved = lat_bytes / (lat_ms / 1000.0) / 1e9
+    step_gbs = n * INSERT_BYTES_PER_TOKEN / (ms / 1000.0) / 1e9
     print(json.dumps({"metric": metric, "value": n / (ms / 1000.0), "unit": unit, "n_gpus": ws, "steps": K,
                       "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                       "vs_baseline": None, "dtype": "e4m3/bf16", "data": "synthetic", "config": cfg,
                       "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                                   "frac": achieved / peak, "traffic": None,
-                                   "kernel": "index_k_insert + latent_insert (one step)",
-                                   "algorithmic_bytes_per_launch": ab, "peak_kind": f"{peak_kind} HBM copy"},
+                                   "frac": achieved / peak, "traffic": None, "kernel": "latent_insert_kernel<fp8>",
+                                   "algorithmic_bytes_per_launch": lat_bytes, "peak_kind": f"{peak_kind} HBM copy"},
+                      "stages_ms": {"index_k_insert": key_ms, "latent_insert": lat_ms},
+                      "step_hbm": {"achieved": step_gbs, "frac": step_gbs / peak,
+                                   "bytes": n * INSERT_BYTES_PER_TOKEN},
                       "e2e": {"value": n / (e2e_ms / 1000.0), "unit": unit, "h2d_bytes_per_step": h2d,
                               "d2h_bytes_per_step": 4},
-                      "gpu_launches": 2 * K, "clocks": clocks, "cpu_baseline": None}))
+                      "gpu_launches": 2 * K, "clocks": clocks, "cpu_baseline": cpu}))
 
 
 def main():

@@ -235,7 +235,7 @@ dsa_status dsa_index_k_insert(const void* x, const float* ln_gamma, const float*
         c.ptr(pos, "pos", 4);
         c.ptr(slot, "slot", 8);
         c.ptr(k_cache, "k_cache");
-        if (inv_freq) c.ptr(inv_freq, "inv_freq", 4);
+        if (inv_freq) c.ptr(inv_freq, "inv_freq");  // read as float4
         if (k_dtype == DSA_FP8_E4M3_ROWSCALE) c.ptr(k_scale, "k_scale", 4);
     }
     dsa_status st = c.done();

@@ -23,14 +23,33 @@
 namespace dsa {
 namespace {
 
+constexpr float kTwoPi1 = 0x1.921fb6p+2f;  // 2 pi = kTwoPi1 + kTwoPi2 + kTwoPi3, fp32 parts
+constexpr float kTwoPi2 = -0x1.777a5cp-23f;
+constexpr float kTwoPi3 = -0x1.ee59dap-48f;
+constexpr float kInvTwoPiF = 0x1.45f306p-3f;
 constexpr double kTwoPiHi = 0x1.921fb58p+2;  // 2 pi = hi + mid + lo, the first two 26 bits each
 constexpr double kTwoPiMid = -0x1.dde974p-25;
 constexpr double kTwoPiLo = 0x1.1a62633145c07p-52;
 constexpr double kInvTwoPiD = 0x1.45f306dc9c883p-3;
 
-// cos and sin of pos * inv_freq: the angle exact in fp64, reduced by 2 pi
-// (Cody & Waite, exact for |k| < 2^27), then fp32 sincos
+// cos and sin of pos * inv_freq, reduced by 2 pi the Cody & Waite way.  Below
+// 2^24 (position and angle) the angle is held exactly as hi + lo, the fp32
+// product and its FMA residual, and reduced with a three-part fp32 2 pi: the
+// first step is exact (|hi - k c1| < 8 and both are multiples of 2^-21), so the
+// reduced angle is off by under 3e-7.  Larger angles are reduced in fp64, which
+// runs at a small fraction of the fp32 rate on this part.
 __device__ __forceinline__ void rope_cs(int pos, float inv_freq, float& c, float& s) {
+    const float pf = (float)pos;
+    const float hi = pf * inv_freq;
+    if (pos < (1 << 24) && fabsf(hi) < 16777216.f) {
+        const float lo = fmaf(pf, inv_freq, -hi);
+        const float k = rintf(hi * kInvTwoPiF);
+        float r = fmaf(-k, kTwoPi1, hi);
+        r = fmaf(-k, kTwoPi2, r);
+        r = fmaf(-k, kTwoPi3, r) + lo;
+        sincosf(r, &s, &c);
+        return;
+    }
     const double th = (double)pos * (double)inv_freq;
     const double kq = rint(th * kInvTwoPiD);
     if (fabs(kq) < 134217728.0) {
@@ -63,22 +82,114 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// the physical row of new token t, or -1 (skipped: a negative slot; reported: a
-// slot past the cache or a negative position)
-__device__ __forceinline__ int64_t insert_row(const int64_t* slot, const int32_t* pos, int64_t t, int64_t num_rows,
-                                              int32_t* d_status) {
-    const int64_t r = __ldg(slot + t);
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// the physical row of a new token, or -1 (skipped: a negative slot; reported:
+// a slot past the cache or a negative position)
+__device__ __forceinline__ int64_t insert_row(int64_t r, int p, int64_t num_rows, int32_t* d_status) {
     if (r < 0) return -1;
-    if (r >= num_rows || __ldg(pos + t) < 0) {
+    if (r >= num_rows || p < 0) {
         if ((threadIdx.x & 31) == 0) report(d_status, DSA_ERR_BAD_INPUT);
         return -1;
     }
     return r;
 }
 
+// A warp takes one token at a time (one query head for the query kernel);
+// the token kernels walk the tokens with a grid stride and load kUnroll tokens
+// before working on any, so a warp keeps that many rows of loads in flight.
+constexpr int kWarpsPerCta = 4;
+constexpr int kUnroll = 2;
+
 // ---------------------------------------------------------------------------
 // indexer key: LayerNorm over the 128 dims (biased variance), RoPE on dims
-// 0..63, then bf16 or e4m3 with one fp32 scale per row.  Lane l: dims 4l..4l+3.
+// 0..63, then bf16 or e4m3 with one fp32 scale per row.  Eight lanes per key,
+// four keys per warp: lane j of a group holds dims 8j..8j+7 (RoPE pairs
+// 4j..4j+3) and 64+8j..64+8j+7, so each load covers 128 contiguous bytes of a
+// key and every lane has the same RoPE work.
+constexpr int kKeyLanes = 8;
+constexpr int kKeysPerWarp = 32 / kKeyLanes;
+
+__device__ __forceinline__ float group_sum8(float x) {
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+__device__ __forceinline__ void unpack_bf16x8(uint4 w, float* v) {
+    v[0] = bf16_lo(w.x), v[1] = bf16_hi(w.x), v[2] = bf16_lo(w.y), v[3] = bf16_hi(w.y);
+    v[4] = bf16_lo(w.z), v[5] = bf16_hi(w.z), v[6] = bf16_lo(w.w), v[7] = bf16_hi(w.w);
+}
+
+// row < 0: the group's reductions only, nothing stored
+template <bool FP8>
+__device__ __forceinline__ void index_k_row(uint4 ra, uint4 rb, int p, int64_t row, const float* __restrict__ sg,
+                                            const float* __restrict__ sb, float eps,
+                                            const float* __restrict__ inv_freq, void* __restrict__ cache,
+                                            float* __restrict__ k_scale, int j) {
+    float v[16];  // dims 8j..8j+7, then 64+8j..64+8j+7
+    unpack_bf16x8(ra, v);
+    unpack_bf16x8(rb, v + 8);
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc += v[i];
+    const float mean = group_sum8(acc) * (1.f / kID);
+    float d2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) d2 = fmaf(v[i] - mean, v[i] - mean, d2);
+    const float inv = 1.f / sqrtf(group_sum8(d2) * (1.f / kID) + eps);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float4* g4 = reinterpret_cast<const float4*>(sg + 64 * h + 8 * j);
+        const float4* b4 = reinterpret_cast<const float4*>(sb + 64 * h + 8 * j);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const float4 g = g4[q], b = b4[q];
+            float* w = v + 8 * h + 4 * q;
+            w[0] = fmaf((w[0] - mean) * inv, g.x, b.x);
+            w[1] = fmaf((w[1] - mean) * inv, g.y, b.y);
+            w[2] = fmaf((w[2] - mean) * inv, g.z, b.z);
+            w[3] = fmaf((w[3] - mean) * inv, g.w, b.w);
+        }
+    }
+    if (inv_freq) {
+        const float4 f4 = __ldg(reinterpret_cast<const float4*>(inv_freq) + j);  // pairs 4j..4j+3
+        const float fr[4] = {f4.x, f4.y, f4.z, f4.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            float c, s;
+            rope_cs(p, fr[u], c, s);
+            const float x0 = v[2 * u], x1 = v[2 * u + 1];
+            v[2 * u] = fmaf(x0, c, -x1 * s);
+            v[2 * u + 1] = fmaf(x0, s, x1 * c);
+        }
+    }
+    if (FP8) {
+        float m = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (row < 0) return;  // after the group's shuffles
+        const float scale = m > 0.f ? m / 448.f : 1.f;
+        const float rs = 1.f / scale;
+        uint2* dst = reinterpret_cast<uint2*>(static_cast<uint8_t*>(cache) + row * kID);
+        dst[j] = make_uint2(pack_e4m3x4(v[0] * rs, v[1] * rs, v[2] * rs, v[3] * rs),
+                            pack_e4m3x4(v[4] * rs, v[5] * rs, v[6] * rs, v[7] * rs));
+        dst[8 + j] = make_uint2(pack_e4m3x4(v[8] * rs, v[9] * rs, v[10] * rs, v[11] * rs),
+                                pack_e4m3x4(v[12] * rs, v[13] * rs, v[14] * rs, v[15] * rs));
+        if (j == 0) k_scale[row] = scale;
+    } else {
+        if (row < 0) return;
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(cache) + row * kID);
+        dst[j] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                            pack_bf16x2(v[6], v[7]));
+        dst[8 + j] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]),
+                                pack_bf16x2(v[14], v[15]));
+    }
+}
+
 template <bool FP8>
 __global__ void __launch_bounds__(128) index_k_insert_kernel(const __nv_bfloat16* __restrict__ x,
                                                              const float* __restrict__ gamma,
@@ -88,49 +199,44 @@ __global__ void __launch_bounds__(128) index_k_insert_kernel(const __nv_bfloat16
                                                              const int64_t* __restrict__ slot, int32_t n,
                                                              void* __restrict__ cache, float* __restrict__ k_scale,
                                                              int64_t num_rows, int32_t* d_status) {
+    static_assert(kID == 32 * kWarpsPerCta, "one gamma and beta value per thread");
+    __shared__ __align__(16) float sg[kID], sb[kID];
     pdl_enter();
-    const int lane = threadIdx.x & 31;
-    for (int64_t t = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5); t < n; t += (int64_t)gridDim.x * 4) {
-    const int64_t row = insert_row(slot, pos, t, num_rows, d_status);
-    if (row < 0) continue;
-    const uint2 raw = *reinterpret_cast<const uint2*>(x + t * kID + 4 * lane);
-    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&raw);
-    float v[4];
+    sg[threadIdx.x] = gamma[threadIdx.x];
+    sb[threadIdx.x] = beta[threadIdx.x];
+    __syncthreads();
+    const int j = threadIdx.x & (kKeyLanes - 1);
+    // key groups: kKeysPerWarp consecutive keys, one per warp at a time
+    const int64_t groups = ((int64_t)n + kKeysPerWarp - 1) / kKeysPerWarp;
+    const int64_t stride = (int64_t)gridDim.x * kWarpsPerCta;
+    const int sub = (threadIdx.x & 31) / kKeyLanes;
+    for (int64_t g0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5); g0 < groups; g0 += kUnroll * stride) {
+        int64_t r[kUnroll];
+        int p[kUnroll];
+        uint4 ra[kUnroll], rb[kUnroll];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = __bfloat162float(xb[i]);
-    const float mean = warp_sum((v[0] + v[1]) + (v[2] + v[3])) * (1.f / kID);
-    float d2 = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) d2 = fmaf(v[i] - mean, v[i] - mean, d2);
-    const float inv = 1.f / sqrtf(warp_sum(d2) * (1.f / kID) + eps);
-    const float4 g = *reinterpret_cast<const float4*>(gamma + 4 * lane);
-    const float4 b = *reinterpret_cast<const float4*>(beta + 4 * lane);
-    const float gv[4] = {g.x, g.y, g.z, g.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = fmaf((v[i] - mean) * inv, gv[i], bv[i]);
-    if (inv_freq && lane < 16) {  // pairs 2 lane and 2 lane + 1
-        const int p = __ldg(pos + t);
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            float c, s;
-            rope_cs(p, __ldg(inv_freq + 2 * lane + u), c, s);
-            const float x0 = v[2 * u], x1 = v[2 * u + 1];
-            v[2 * u] = fmaf(x0, c, -x1 * s);
-            v[2 * u + 1] = fmaf(x0, s, x1 * c);
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t t = (g0 + u * stride) * kKeysPerWarp + sub;
+            r[u] = -1;
+            p[u] = 0;
+            ra[u] = rb[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (t < n) {
+                r[u] = __ldg(slot + t);
+                p[u] = __ldg(pos + t);
+                const uint4* src = reinterpret_cast<const uint4*>(x + t * kID);
+                ra[u] = __ldcs(src + j);
+                rb[u] = __ldcs(src + 8 + j);
+            }
         }
-    }
-    if (FP8) {
-        float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        const float scale = m > 0.f ? m / 448.f : 1.f;
-        reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(cache) + row * kID)[lane] =
-            pack_e4m3x4(v[0] / scale, v[1] / scale, v[2] / scale, v[3] / scale);
-        if (lane == 0) k_scale[row] = scale;
-    } else {
-        reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(cache) + row * kID)[lane] =
-            make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
-    }
+        for (int u = 0; u < kUnroll; ++u) {
+            // every lane takes part in the group reductions; only valid rows are stored
+            const bool live = r[u] >= 0 && r[u] < num_rows && p[u] >= 0;
+            if (r[u] >= num_rows || (r[u] >= 0 && p[u] < 0)) {
+                if (j == 0) report(d_status, DSA_ERR_BAD_INPUT);
+            }
+            index_k_row<FP8>(ra[u], rb[u], p[u], live ? r[u] : -1, sg, sb, eps, inv_freq, cache, k_scale, j);
+        }
     }
 }
 
@@ -140,40 +246,25 @@ __global__ void __launch_bounds__(128) index_k_insert_kernel(const __nv_bfloat16
 // bf16), the 64 RoPE dims rotated.  Lane l: latent dims 16l..16l+15 (group l / 8)
 // and RoPE pair l.
 template <bool FP8>
-__global__ void __launch_bounds__(128) latent_insert_kernel(const __nv_bfloat16* __restrict__ c_kv,
-                                                            const __nv_bfloat16* __restrict__ k_pe,
-                                                            const int32_t* __restrict__ pos,
-                                                            const float* __restrict__ inv_freq,
-                                                            const int64_t* __restrict__ slot, int32_t n,
-                                                            uint8_t* __restrict__ latent, int64_t num_rows,
-                                                            int32_t* d_status) {
-    pdl_enter();
-    const int lane = threadIdx.x & 31;
-    for (int64_t t = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5); t < n; t += (int64_t)gridDim.x * 4) {
-    const int64_t row = insert_row(slot, pos, t, num_rows, d_status);
-    if (row < 0) continue;
-    const uint4* src = reinterpret_cast<const uint4*>(c_kv + t * kMV + 16 * lane);
-    const uint4 r0 = src[0], r1 = src[1];
-    // the RoPE pair of this lane
-    const uint32_t pe = reinterpret_cast<const uint32_t*>(k_pe + t * (kMD - kMV))[lane];
-    float x0 = __bfloat162float(__ushort_as_bfloat16((unsigned short)(pe & 0xFFFF)));
-    float x1 = __bfloat162float(__ushort_as_bfloat16((unsigned short)(pe >> 16)));
+__device__ __forceinline__ void latent_row(uint4 r0, uint4 r1, uint32_t pe, int p, int64_t row,
+                                           const float* __restrict__ inv_freq, uint8_t* __restrict__ latent,
+                                           int lane) {
+    float x0 = bf16_lo(pe), x1 = bf16_hi(pe);
     if (inv_freq) {
         float c, s;
-        rope_cs(__ldg(pos + t), __ldg(inv_freq + lane), c, s);
+        rope_cs(p, __ldg(inv_freq + lane), c, s);
         const float y0 = fmaf(x0, c, -x1 * s), y1 = fmaf(x0, s, x1 * c);
         x0 = y0;
         x1 = y1;
     }
     if (FP8) {
         uint8_t* dst = latent + row * kDsRow;
+        const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
         float v[16];
-        const __nv_bfloat16* b0 = reinterpret_cast<const __nv_bfloat16*>(&r0);
-        const __nv_bfloat16* b1 = reinterpret_cast<const __nv_bfloat16*>(&r1);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            v[i] = __bfloat162float(b0[i]);
-            v[8 + i] = __bfloat162float(b1[i]);
+            v[2 * i] = bf16_lo(w[i]);
+            v[2 * i + 1] = bf16_hi(w[i]);
         }
         float m = 0.f;
 #pragma unroll
@@ -181,11 +272,12 @@ __global__ void __launch_bounds__(128) latent_insert_kernel(const __nv_bfloat16*
 #pragma unroll
         for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));  // within 8 lanes
         const float scale = m > 0.f ? m / 448.f : 1.f;
+        const float rs = 1.f / scale;
         uint4 codes;
-        codes.x = pack_e4m3x4(v[0] / scale, v[1] / scale, v[2] / scale, v[3] / scale);
-        codes.y = pack_e4m3x4(v[4] / scale, v[5] / scale, v[6] / scale, v[7] / scale);
-        codes.z = pack_e4m3x4(v[8] / scale, v[9] / scale, v[10] / scale, v[11] / scale);
-        codes.w = pack_e4m3x4(v[12] / scale, v[13] / scale, v[14] / scale, v[15] / scale);
+        codes.x = pack_e4m3x4(v[0] * rs, v[1] * rs, v[2] * rs, v[3] * rs);
+        codes.y = pack_e4m3x4(v[4] * rs, v[5] * rs, v[6] * rs, v[7] * rs);
+        codes.z = pack_e4m3x4(v[8] * rs, v[9] * rs, v[10] * rs, v[11] * rs);
+        codes.w = pack_e4m3x4(v[12] * rs, v[13] * rs, v[14] * rs, v[15] * rs);
         reinterpret_cast<uint4*>(dst)[lane] = codes;
         if ((lane & 7) == 0) reinterpret_cast<float*>(dst + kMV)[lane >> 3] = scale;
         reinterpret_cast<uint32_t*>(dst + kMV + 16)[lane] = pack_bf16x2(x0, x1);
@@ -196,6 +288,45 @@ __global__ void __launch_bounds__(128) latent_insert_kernel(const __nv_bfloat16*
         d4[1] = r1;
         reinterpret_cast<uint32_t*>(dst + kMV)[lane] = pack_bf16x2(x0, x1);
     }
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(128) latent_insert_kernel(const __nv_bfloat16* __restrict__ c_kv,
+                                                            const __nv_bfloat16* __restrict__ k_pe,
+                                                            const int32_t* __restrict__ pos,
+                                                            const float* __restrict__ inv_freq,
+                                                            const int64_t* __restrict__ slot, int32_t n,
+                                                            uint8_t* __restrict__ latent, int64_t num_rows,
+                                                            int32_t* d_status) {
+    pdl_enter();
+    const int lane = threadIdx.x & 31;
+    const int64_t stride = (int64_t)gridDim.x * kWarpsPerCta;
+    for (int64_t t0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5); t0 < n; t0 += kUnroll * stride) {
+        int64_t r[kUnroll];
+        int p[kUnroll];
+        uint4 r0[kUnroll], r1[kUnroll];
+        uint32_t pe[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t t = t0 + u * stride;
+            r[u] = -1;
+            p[u] = 0;
+            r0[u] = r1[u] = make_uint4(0u, 0u, 0u, 0u);
+            pe[u] = 0u;
+            if (t < n) {
+                r[u] = __ldg(slot + t);
+                p[u] = __ldg(pos + t);
+                const uint4* src = reinterpret_cast<const uint4*>(c_kv + t * kMV + 16 * lane);
+                r0[u] = __ldcs(src);
+                r1[u] = __ldcs(src + 1);
+                pe[u] = __ldcs(reinterpret_cast<const unsigned int*>(k_pe + t * (kMD - kMV)) + lane);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t row = insert_row(r[u], p[u], num_rows, d_status);
+            if (row >= 0) latent_row<FP8>(r0[u], r1[u], pe[u], p[u], row, inv_freq, latent, lane);
+        }
     }
 }
 
@@ -229,17 +360,14 @@ __global__ void __launch_bounds__(128) mla_q_prep_kernel(const __nv_bfloat16* __
         uint32_t* w = reinterpret_cast<uint32_t*>(&r[k]);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float a = __bfloat162float(__ushort_as_bfloat16((unsigned short)(w[i] & 0xFFFF)));
-            const float b = __bfloat162float(__ushort_as_bfloat16((unsigned short)(w[i] >> 16)));
-            w[i] = pack_bf16x2(a * f, b * f);
+            w[i] = pack_bf16x2(bf16_lo(w[i]) * f, bf16_hi(w[i]) * f);
         }
     }
     uint4* d4 = reinterpret_cast<uint4*>(qo + 16 * lane);
     d4[0] = r[0];
     d4[1] = r[1];
     const uint32_t pe = reinterpret_cast<const uint32_t*>(qi + kMV)[lane];
-    float x0 = __bfloat162float(__ushort_as_bfloat16((unsigned short)(pe & 0xFFFF)));
-    float x1 = __bfloat162float(__ushort_as_bfloat16((unsigned short)(pe >> 16)));
+    float x0 = bf16_lo(pe), x1 = bf16_hi(pe);
     if (inv_freq) {
         float c, s;
         rope_cs(p, __ldg(inv_freq + lane), c, s);
@@ -250,9 +378,10 @@ __global__ void __launch_bounds__(128) mla_q_prep_kernel(const __nv_bfloat16* __
     reinterpret_cast<uint32_t*>(qo + kMV)[lane] = pack_bf16x2(x0 * f, x1 * f);
 }
 
-constexpr int kTokensPerCta = 4;  // a warp per token
+constexpr int kTokensPerCta = kWarpsPerCta;
 
-// a grid of a few waves of CTAs (16 per SM) walking the tokens
+// a grid of a few waves of CTAs (16 per SM) walking the items (keys in groups
+// of kKeysPerWarp, latent rows, query heads), one per warp at a time
 unsigned insert_grid(int64_t items) {
     static int sms = 0;
     if (sms == 0) {
@@ -271,7 +400,7 @@ cudaError_t launch_index_k_insert(const void* x, const float* gamma, const float
                                   const float* inv_freq, const int64_t* slot, int32_t n, void* cache, float* k_scale,
                                   bool fp8, int64_t num_rows, int32_t* d_status, cudaStream_t stream) {
     if (n <= 0) return cudaSuccess;
-    const dim3 grid(insert_grid(n));
+    const dim3 grid(insert_grid(((int64_t)n + kKeysPerWarp - 1) / kKeysPerWarp));
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
     return fp8 ? launch_pdl(index_k_insert_kernel<true>, grid, dim3(128), 0, stream, 1, xb, gamma, beta, eps, pos,
                             inv_freq, slot, n, cache, k_scale, num_rows, d_status)

@@ -171,7 +171,7 @@ dsa_status sparse_mla_decode(const void* q, const void* latent, dsa_dtype latent
  *   x bf16 [n,128] (the projection's output); ln_gamma, ln_beta fp32 [128];
  *   pos int32 [n]; inv_freq fp32 [32] or NULL; slot int64 [n].
  * The rows dsa_index_scores reads.  Alignment: every pointer 16-byte aligned
- * (pos, slot, k_scale, inv_freq: their element size). */
+ * (pos, slot, k_scale: their element size). */
 dsa_status dsa_index_k_insert(const void* x, const float* ln_gamma, const float* ln_beta, float ln_eps,
                               const int32_t* pos, const float* inv_freq, const int64_t* slot, int32_t n,
                               void* k_cache, float* k_scale, dsa_dtype k_dtype, int64_t num_rows, int32_t* d_status,

@@ -73,8 +73,9 @@ def _check_bf16_store(got_bits_t, exact, what):
     assert same > 0.995, f"{what}: only {same:.4f} of the values equal the oracle's rounding"
 
 
-def _check_e4m3_store(codes_t, scale_gpu, exact, group, what):
-    """codes [n, d] uint8, scale_gpu fp64 [n, d / group], exact fp64 [n, d]."""
+def _check_e4m3_store(codes_t, scale_gpu, exact, group, what, agree_rows=None):
+    """codes [n, d] uint8, scale_gpu fp64 [n, d / group], exact fp64 [n, d];
+    agreement with the oracle's own codes on agree_rows (all rows by default)."""
     codes = codes_t.cpu().numpy()
     n, d = exact.shape
     amax = np.abs(exact.reshape(n, d // group, group)).max(axis=2)
@@ -83,14 +84,44 @@ def _check_e4m3_store(codes_t, scale_gpu, exact, group, what):
     t = exact.reshape(n, d // group, group) / scale_gpu[:, :, None]
     dec = _E4M3[codes].reshape(n, d // group, group)
     _nearest(dec, np.clip(t, -448.0, 448.0), _e4m3_quantum(t), what)
-    enc_codes, _ = oracle.quantize_rows_e4m3(exact, group)
-    same = (codes == enc_codes).mean()
+    rows = np.arange(n) if agree_rows is None else np.asarray(agree_rows)
+    enc_codes, _ = oracle.quantize_rows_e4m3(exact[rows], group)
+    same = (codes[rows] == enc_codes).mean()
     assert same > 0.995, f"{what}: only {same:.4f} of the codes equal the oracle's"
 
 
-def _inputs(n, nq, num_rows, rope=True, seed=0):
-    d = I.make_insert_inputs(n, nq, num_rows, DEV, seed=seed, rope=rope)
+def _inputs(n, nq, num_rows, rope=True, seed=0, page_size=0):
+    d = I.make_insert_inputs(n, nq, num_rows, DEV, seed=seed, rope=rope, page_size=page_size)
     return d, {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in d.items()}
+
+
+def _insert_fp8(d, n, rows, pos=None):
+    keys = torch.full((rows, 128), SENTINEL, dtype=torch.uint8, device=DEV)
+    k_scale = torch.zeros(rows, dtype=torch.float32, device=DEV)
+    latent = torch.full((rows, I.DS_MLA_ROW_BYTES), SENTINEL, dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pos = d["pos"] if pos is None else pos
+    dsa.dsa_index_k_insert(d["x"], d["gamma"], d["beta"], 1e-6, pos, d["inv_freq"], d["slot"], n, keys, k_scale,
+                           dsa.DSA_FP8_E4M3_ROWSCALE, rows, st)
+    dsa.dsa_latent_insert(d["c_kv"], d["k_pe"], pos, d["inv_freq"], d["slot"], n, latent, dsa.DSA_FP8_DS_MLA, rows,
+                          st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return keys, k_scale, latent
+
+
+def _check_fp8_tokens(d, keys, k_scale, latent, pick, pos=None):
+    """The e4m3 key and fp8_ds_mla latent rows of the tokens in pick against the oracle."""
+    pk = torch.as_tensor(pick, dtype=torch.long).to(DEV)
+    sl = d["slot"][pk]
+    hp = (d["pos"] if pos is None else pos)[pk].cpu()
+    ek = oracle.index_k(d["x"][pk].cpu(), d["gamma"].cpu(), d["beta"].cpu(), 1e-6, hp, d["inv_freq"].cpu())
+    _check_e4m3_store(keys[sl], k_scale[sl].cpu().numpy().astype(np.float64)[:, None], ek, 128, "index keys")
+    el = oracle.latent_k(d["c_kv"][pk].cpu(), d["k_pe"][pk].cpu(), hp, d["inv_freq"].cpu())
+    got = latent[sl]
+    scales = got[:, 512:528].contiguous().view(torch.float32).cpu().numpy().astype(np.float64)
+    _check_e4m3_store(got[:, :512], scales, el[:, :512], 128, "latent codes")
+    _check_bf16_store(got[:, 528:].contiguous().view(torch.bfloat16), el[:, 512:], "latent RoPE dims")
 
 
 @pytest.mark.parametrize("fp8", [False, True])
@@ -240,28 +271,51 @@ def test_inserted_rows_read_back_through_the_decode_path():
     assert np.max(np.abs(lse[0].cpu().numpy() - rl)) <= 1e-3 * max(1.0, np.max(np.abs(rl)))
 
 
-def test_insert_bench_size_sampled():
-    """The size the benchmark times (65536 new tokens, e4m3 keys, fp8_ds_mla
-    latent), checked on 257 sampled tokens."""
-    n, rows = 65536, 65536
-    d, _ = _inputs(n, 1, rows, seed=6)
-    keys = torch.zeros((rows, 128), dtype=torch.uint8, device=DEV)
-    k_scale = torch.zeros(rows, dtype=torch.float32, device=DEV)
-    latent = torch.zeros((rows, I.DS_MLA_ROW_BYTES), dtype=torch.uint8, device=DEV)
+def test_insert_many_tokens_per_warp():
+    """45001 new tokens: more than two grid passes of both kernels, so every
+    warp takes several keys and rows, two loads ahead, with a ragged end.  Every
+    key row is checked (against the oracle's own codes on a sample), the latent
+    rows on a sample spread over the range and its last 300 tokens; no row
+    outside the slots is written."""
+    n, rows = 45001, 46000
+    d, h = _inputs(n, 1, rows, seed=7)
+    keys, k_scale, latent = _insert_fp8(d, n, rows)
+    ek = oracle.index_k(h["x"], h["gamma"], h["beta"], 1e-6, h["pos"], h["inv_freq"])
+    pick = np.unique(np.concatenate([np.linspace(0, n - 1, 700).astype(np.int64), np.arange(n - 300, n)]))
+    _check_e4m3_store(keys[d["slot"]], k_scale[d["slot"]].cpu().numpy().astype(np.float64)[:, None], ek, 128,
+                      "index keys", agree_rows=pick)
+    _check_fp8_tokens(d, keys, k_scale, latent, pick)
+    untouched = torch.from_numpy(np.setdiff1d(np.arange(rows), h["slot"].numpy())).to(DEV)
+    assert torch.all(keys[untouched] == SENTINEL) and torch.all(latent[untouched] == SENTINEL)
+
+
+def test_insert_positions_past_2_24():
+    """RoPE angles on both sides of 2^24 radians-per-unit positions (the kernels
+    change how they reduce the angle there) and near the largest position."""
+    n, rows = 600, 600
+    d, h = _inputs(n, 5, rows, seed=8)  # 5 attention queries
+    pos = d["pos"].clone()
+    pos[:300] += (1 << 24) - 150        # 2^24 - 150 .. 2^24 + 149
+    pos[300:] += (1 << 31) - 1 - n      # up to 2^31 - 2
+    keys, k_scale, latent = _insert_fp8(d, n, rows, pos=pos)
+    _check_fp8_tokens(d, keys, k_scale, latent, np.arange(n), pos=pos)
+    q = d["q"].clone()
+    assert q.shape == (5, 64, 576)
+    qp = torch.tensor([(1 << 24) - 1, 1 << 24, (1 << 24) + 1, (1 << 30) + 7, (1 << 31) - 2],
+                      dtype=torch.int32, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
-    dsa.dsa_index_k_insert(d["x"], d["gamma"], d["beta"], 1e-6, d["pos"], d["inv_freq"], d["slot"], n, keys, k_scale,
-                           dsa.DSA_FP8_E4M3_ROWSCALE, rows, st)
-    dsa.dsa_latent_insert(d["c_kv"], d["k_pe"], d["pos"], d["inv_freq"], d["slot"], n, latent, dsa.DSA_FP8_DS_MLA,
-                          rows, st)
+    dsa.dsa_mla_q_prep(q, d["ssmax_s"], d["ssmax_b"], d["inv_freq"], qp, 5, q, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    pick = torch.linspace(0, n - 1, 257).long()
-    sl = d["slot"][pick.to(DEV)]
-    hp = d["pos"][pick.to(DEV)].cpu()
-    ek = oracle.index_k(d["x"][pick.to(DEV)].cpu(), d["gamma"].cpu(), d["beta"].cpu(), 1e-6, hp, d["inv_freq"].cpu())
-    _check_e4m3_store(keys[sl], k_scale[sl].cpu().numpy().astype(np.float64)[:, None], ek, 128, "index keys")
-    el = oracle.latent_k(d["c_kv"][pick.to(DEV)].cpu(), d["k_pe"][pick.to(DEV)].cpu(), hp, d["inv_freq"].cpu())
-    got = latent[sl]
-    scales = got[:, 512:528].contiguous().view(torch.float32).cpu().numpy().astype(np.float64)
-    _check_e4m3_store(got[:, :512], scales, el[:, :512], 128, "latent codes")
-    _check_bf16_store(got[:, 528:].contiguous().view(torch.bfloat16), el[:, 512:], "latent RoPE dims")
+    exact = oracle.mla_q(h["q"], h["ssmax_s"], h["ssmax_b"], qp.cpu(), h["inv_freq"])
+    _check_bf16_store(q.reshape(5, -1), exact.reshape(5, -1), "attention query")
+
+
+def test_insert_bench_size_sampled():
+    """The benchmark's step (2^20 new tokens in 64-token pages taken in a random
+    order, e4m3 keys, fp8_ds_mla latent), checked on 257 sampled tokens."""
+    n = rows = 1 << 20
+    d, _ = _inputs(n, 1, rows, seed=6, page_size=64)
+    keys, k_scale, latent = _insert_fp8(d, n, rows)
+    _check_fp8_tokens(d, keys, k_scale, latent, np.linspace(0, n - 1, 257).astype(np.int64))
+    assert not torch.any(torch.all(keys == SENTINEL, dim=1)), "every row is some token's"
