@@ -82,6 +82,17 @@ def _bind(path: str):
     L.oracle_index_k.argtypes, L.oracle_index_k.restype = [I32, P, P, P, D, P, P, P], ctypes.c_int
     L.oracle_latent_k.argtypes, L.oracle_latent_k.restype = [I32, P, P, P, P, P], ctypes.c_int
     L.oracle_mla_q.argtypes, L.oracle_mla_q.restype = [I32, P, P, P, P, P, P], ctypes.c_int
+    L.oracle_dcp_owner.argtypes, L.oracle_dcp_owner.restype = [I32, I32, I32], I32
+    L.oracle_dcp_local.argtypes, L.oracle_dcp_local.restype = [I32, I32, I32], I32
+    L.oracle_dcp_global.argtypes, L.oracle_dcp_global.restype = [I32, I32, I32, I32], I32
+    L.oracle_dcp_pack.argtypes, L.oracle_dcp_pack.restype = [ctypes.c_float, I32], ctypes.c_uint64
+    L.oracle_dcp_unpack.argtypes = [ctypes.c_uint64, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(I32)]
+    L.oracle_dcp_unpack.restype = ctypes.c_int
+    L.oracle_topk_merge.argtypes = [I32, I32, P, I32, P, ctypes.POINTER(I32)]
+    L.oracle_topk_merge.restype = ctypes.c_int
+    L.oracle_topk_compact.argtypes = [I32, P, I32, I32, I32, I32, P, ctypes.POINTER(I32)]
+    L.oracle_topk_compact.restype = ctypes.c_int
+    L.oracle_lse_combine.argtypes, L.oracle_lse_combine.restype = [I32, I64, I32, P, P, P, P], ctypes.c_int
     return L
 
 
@@ -260,3 +271,80 @@ def quantize_rows_e4m3(v, group: int, L=None):
     enc = np.vectorize(lambda x: e4m3_encode(x, L), otypes=[np.uint8])
     codes = enc(g / scale[:, :, None]).reshape(n, d)
     return codes, scale
+
+
+# ---- DCP: the per-rank steps of decode context parallelism ----
+
+def dcp_owner(t: int, world: int, interleave: int, L=None) -> int:
+    return int((L or lib()).oracle_dcp_owner(int(t), int(world), int(interleave)))
+
+
+def dcp_local(t: int, world: int, interleave: int, L=None) -> int:
+    return int((L or lib()).oracle_dcp_local(int(t), int(world), int(interleave)))
+
+
+def dcp_global(local: int, rank: int, world: int, interleave: int, L=None) -> int:
+    return int((L or lib()).oracle_dcp_global(int(local), int(rank), int(world), int(interleave)))
+
+
+def dcp_pack(scores, ids, L=None) -> np.ndarray:
+    """Packed candidates (uint64) of fp32 scores and ids, element by element."""
+    L = L or lib()
+    sc = np.asarray(_np(scores, np.float32), np.float32).ravel()
+    ii = np.asarray(ids, np.int64).ravel()
+    out = np.empty(sc.shape[0], np.uint64)
+    for n in range(sc.shape[0]):
+        out[n] = L.oracle_dcp_pack(float(sc[n]), int(ii[n]))
+    return out.reshape(np.shape(scores))
+
+
+def dcp_unpack(c: int, L=None):
+    """(score, id) of a packed candidate, or None for an empty slot."""
+    sc, i = ctypes.c_float(), ctypes.c_int32()
+    if not (L or lib()).oracle_dcp_unpack(ctypes.c_uint64(int(c)), ctypes.byref(sc), ctypes.byref(i)):
+        return None
+    return float(sc.value), int(i.value)
+
+
+def topk_merge(lists, k: int, L=None):
+    """lists uint64 [R, Q, list_len] -> (ids int32 [Q, k] ascending then -1, len int32 [Q]).
+    Raises on an id present twice among a query's candidates."""
+    L = L or lib()
+    a = np.asarray(_np(lists, np.uint64), np.uint64)
+    R, Q, n = a.shape
+    ids = np.empty((Q, k), np.int32)
+    lens = np.empty(Q, np.int32)
+    for q in range(Q):
+        per = np.ascontiguousarray(a[:, q, :])
+        m = ctypes.c_int32()
+        _check(L.oracle_topk_merge(R, n, _ptr(per), k, _ptr(ids[q]), ctypes.byref(m)))
+        lens[q] = m.value
+    return ids, lens
+
+
+def topk_compact(idx, lens, rank: int, world: int, interleave: int, L=None):
+    """idx int32 [Q, k], lens [Q] -> (local idx int32 [Q, k], local len [Q]) of one rank."""
+    L = L or lib()
+    ii = np.ascontiguousarray(_np(idx, np.int32))
+    ll = _np(lens, np.int32)
+    Q, k = ii.shape
+    out = np.empty((Q, k), np.int32)
+    ol = np.empty(Q, np.int32)
+    for q in range(Q):
+        m = ctypes.c_int32()
+        _check(L.oracle_topk_compact(k, _ptr(ii[q]), int(ll[q]), rank, world, interleave, _ptr(out[q]),
+                                     ctypes.byref(m)))
+        ol[q] = m.value
+    return out, ol
+
+
+def lse_combine(o_parts, lse_parts, L=None):
+    """o_parts [R, ..., dim] (fp64 values), lse_parts [R, ...] -> (out [..., dim], lse [...])."""
+    o = np.ascontiguousarray(np.asarray(o_parts, np.float64))
+    ls = np.ascontiguousarray(np.asarray(lse_parts, np.float64))
+    R, dim = o.shape[0], o.shape[-1]
+    rows = int(np.prod(o.shape[1:-1]))
+    out = np.empty(o.shape[1:], np.float64)
+    lse = np.empty(ls.shape[1:], np.float64)
+    _check((L or lib()).oracle_lse_combine(R, rows, dim, _ptr(o), _ptr(ls), _ptr(out), _ptr(lse)))
+    return out, lse

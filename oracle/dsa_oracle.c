@@ -384,3 +384,131 @@ int oracle_mla_q(int32_t nq, const uint16_t* q, const float* ssmax_s, const floa
     }
     return 0;
 }
+
+/* ---- DCP: the per-rank steps of decode context parallelism ([vLLM-ML4] Long
+ * context: decode and prefill context parallelism) ---- */
+
+/* The cache is sharded by token; token t's turn is t / interleave, and turns go
+ * round the ranks in order. */
+int32_t oracle_dcp_owner(int32_t t, int32_t world, int32_t interleave) {
+    return (t / interleave) % world;
+}
+
+int32_t oracle_dcp_local(int32_t t, int32_t world, int32_t interleave) {
+    int32_t turn = t / interleave;
+    return (turn / world) * interleave + t % interleave;
+}
+
+int32_t oracle_dcp_global(int32_t local, int32_t rank, int32_t world, int32_t interleave) {
+    int32_t own_turn = local / interleave;
+    return (own_turn * world + rank) * interleave + local % interleave;
+}
+
+/* Order-preserving code of a float: negative values map below positive ones
+ * and, among negatives, a larger magnitude maps lower. */
+static uint32_t score_code(float score) {
+    uint32_t b;
+    if (score == 0.0f) score = 0.0f; /* -0 as +0 */
+    memcpy(&b, &score, 4);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+uint64_t oracle_dcp_pack(float score, int32_t id) {
+    return ((uint64_t)score_code(score) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)id);
+}
+
+int oracle_dcp_unpack(uint64_t c, float* score, int32_t* id) {
+    if (c == 0) return 0;
+    uint32_t code = (uint32_t)(c >> 32);
+    uint32_t b = (code & 0x80000000u) ? (code & 0x7FFFFFFFu) : ~code;
+    memcpy(score, &b, 4);
+    *id = (int32_t)(0xFFFFFFFFu - (uint32_t)(c & 0xFFFFFFFFu));
+    return 1;
+}
+
+static int by_id(const void* a, const void* b) {
+    int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+    return (x > y) - (x < y);
+}
+
+/* The selector: every candidate of every list, sorted by score descending and
+ * id ascending (the same rule as oracle_topk, the id in the index's place);
+ * the first k taken and returned in id order. */
+int oracle_topk_merge(int32_t num_lists, int32_t list_len, const uint64_t* lists, int32_t k, int32_t* ids,
+                      int32_t* len) {
+    if (num_lists < 0 || list_len < 0 || k < 0 || (!lists && num_lists && list_len) || (!ids && k) || !len)
+        return ORACLE_ERR_ARG;
+    int64_t total = (int64_t)num_lists * list_len;
+    scored* v = (scored*)malloc(sizeof(scored) * (size_t)(total ? total : 1));
+    if (!v) return ORACLE_ERR_NOMEM;
+    int64_t n = 0;
+    for (int64_t i = 0; i < total; ++i) {
+        float sc;
+        int32_t id;
+        if (oracle_dcp_unpack(lists[i], &sc, &id)) {
+            v[n].s = (double)sc;
+            v[n].j = id;
+            ++n;
+        }
+    }
+    qsort(v, (size_t)n, sizeof(scored), by_score);
+    int32_t m = n < k ? (int32_t)n : k;
+    for (int32_t i = 0; i < m; ++i) ids[i] = v[i].j;
+    qsort(ids, (size_t)m, sizeof(int32_t), by_id);
+    for (int32_t i = m; i < k; ++i) ids[i] = -1;
+    /* an id seen twice among all candidates */
+    int32_t* all = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n ? n : 1));
+    if (!all) {
+        free(v);
+        return ORACLE_ERR_NOMEM;
+    }
+    for (int64_t i = 0; i < n; ++i) all[i] = v[i].j;
+    qsort(all, (size_t)n, sizeof(int32_t), by_id);
+    int dup = 0;
+    for (int64_t i = 1; i < n; ++i) dup |= all[i] == all[i - 1];
+    free(all);
+    free(v);
+    *len = m;
+    return dup ? ORACLE_ERR_INDEX : 0;
+}
+
+int oracle_topk_compact(int32_t k, const int32_t* idx, int32_t len, int32_t rank, int32_t world,
+                        int32_t interleave, int32_t* local_idx, int32_t* local_len) {
+    if (k < 0 || len < 0 || len > k || world < 1 || interleave < 1 || rank < 0 || rank >= world ||
+        (!idx && len) || (!local_idx && k) || !local_len)
+        return ORACLE_ERR_ARG;
+    int32_t m = 0;
+    for (int32_t i = 0; i < len; ++i) {
+        int32_t t = idx[i];
+        if (t >= 0 && oracle_dcp_owner(t, world, interleave) == rank)
+            local_idx[m++] = oracle_dcp_local(t, world, interleave);
+    }
+    for (int32_t i = m; i < k; ++i) local_idx[i] = -1;
+    *local_len = m;
+    return 0;
+}
+
+int oracle_lse_combine(int32_t num_parts, int64_t rows, int32_t dim, const double* o_parts,
+                       const double* lse_parts, double* out, double* lse) {
+    if (num_parts < 1 || rows < 0 || dim < 0 || !o_parts || !lse_parts || !out || !lse) return ORACLE_ERR_ARG;
+    for (int64_t i = 0; i < rows; ++i) {
+        double m = -INFINITY;
+        for (int32_t r = 0; r < num_parts; ++r) m = fmax(m, lse_parts[(int64_t)r * rows + i]);
+        double* o = out + i * dim;
+        for (int32_t d = 0; d < dim; ++d) o[d] = 0.0;
+        if (m == -INFINITY) {
+            lse[i] = -INFINITY;
+            continue;
+        }
+        double sum = 0.0;
+        for (int32_t r = 0; r < num_parts; ++r) sum += exp(lse_parts[(int64_t)r * rows + i] - m);
+        double L = m + log(sum);
+        for (int32_t r = 0; r < num_parts; ++r) {
+            double wgt = exp(lse_parts[(int64_t)r * rows + i] - L);
+            const double* op = o_parts + ((int64_t)r * rows + i) * dim;
+            for (int32_t d = 0; d < dim; ++d) o[d] += wgt * op[d];
+        }
+        lse[i] = L;
+    }
+    return 0;
+}

@@ -115,6 +115,50 @@ int oracle_latent_k(int32_t n, const uint16_t* c_kv, const uint16_t* k_pe, const
 int oracle_mla_q(int32_t nq, const uint16_t* q, const float* ssmax_s, const float* ssmax_b /*[64]*/,
                  const float* inv_freq /*[32] or NULL*/, const int32_t* pos, double* out);
 
+/* ---- DCP: the per-rank steps of decode context parallelism ----
+ *
+ * [vLLM-ML4] Long context: decode and prefill context parallelism: the latent
+ * cache is sharded by token; each rank pushes its packed (score, id) top-k
+ * candidates to its peers and a selector merges them; each rank compacts the
+ * global top-k slots it owns and bounds its attention with topk_length (a
+ * rank owning none of a query's slots gets an empty row); the ranks' partial
+ * outputs are merged by an LSE combine.
+ *
+ * Ownership: `world` ranks take a sequence's tokens in turns of `interleave`:
+ * token t lives on rank (t / interleave) mod world, at local position
+ * (t / (interleave * world)) * interleave + t mod interleave. */
+int32_t oracle_dcp_owner(int32_t t, int32_t world, int32_t interleave);
+int32_t oracle_dcp_local(int32_t t, int32_t world, int32_t interleave);
+int32_t oracle_dcp_global(int32_t local, int32_t rank, int32_t world, int32_t interleave);
+
+/* Packed candidate: the high 32 bits an order-preserving code of the fp32
+ * score (its bits with the sign bit set when positive, all bits inverted when
+ * negative; -0 coded as +0), the low 32 bits 0xFFFFFFFF - id (0 <= id).  A
+ * larger packed value is a larger score or, at equal scores, a smaller id;
+ * 0 is an empty slot.  unpack returns 1 for a candidate, 0 for an empty slot. */
+uint64_t oracle_dcp_pack(float score, int32_t id);
+int oracle_dcp_unpack(uint64_t c, float* score, int32_t* id);
+
+/* The selector: the min(k, #candidates) candidates of num_lists lists of
+ * list_len packed slots (lists[r*list_len + i]; empty slots skipped) with the
+ * largest scores, ties to the smaller id; their ids ascending in ids[0..len),
+ * the rest of ids[0..k) -1.  An id present twice: ORACLE_ERR_INDEX. */
+int oracle_topk_merge(int32_t num_lists, int32_t list_len, const uint64_t* lists, int32_t k, int32_t* ids,
+                      int32_t* len);
+
+/* Top-k compaction for one rank: the slots i < len of idx holding an id >= 0
+ * that `rank` owns, in their order, as local positions; *local_len their
+ * number, the rest of local_idx[0..k) -1. */
+int oracle_topk_compact(int32_t k, const int32_t* idx, int32_t len, int32_t rank, int32_t world,
+                        int32_t interleave, int32_t* local_idx, int32_t* local_len);
+
+/* LSE combine of num_parts partial results for `rows` (query, head) rows:
+ * lse[i] = ln sum_r exp(lse_parts[r*rows + i]), out[i] = sum_r
+ * exp(lse_parts[r*rows + i] - lse[i]) * o_parts[(r*rows + i)*dim + d]; parts
+ * at -inf add nothing; all at -inf give out = 0 and lse = -inf. */
+int oracle_lse_combine(int32_t num_parts, int64_t rows, int32_t dim, const double* o_parts,
+                       const double* lse_parts, double* out, double* lse);
+
 #ifdef __cplusplus
 }
 #endif

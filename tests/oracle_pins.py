@@ -648,4 +648,177 @@ def pin_quantize_rows_e4m3(L):
     assert np.all(np.abs(dec - g) <= 0.5 * step * (1 + 1e-12))
 
 
+# ---------------------------------------------------------------------------
+# DCP: the per-rank steps of decode context parallelism ([vLLM-ML4] Long
+# context: decode and prefill context parallelism)
+def _owner(t, world, interleave):
+    """Ownership restated here: turns of `interleave` tokens go round the ranks."""
+    return (t // interleave) % world
+
+
+def pin_dcp_ownership_partitions_tokens(L):
+    """Every token has one owner; each rank numbers the tokens it owns 0, 1, 2,
+    ... in token order; global(local(t)) = t.  Hand case: two ranks, turns of
+    three: tokens 0-2 and 6-8 on rank 0 (local 0-5), 3-5 on rank 1 (local 0-2)."""
+    assert [oracle.dcp_owner(t, 2, 3, L=L) for t in range(9)] == [0, 0, 0, 1, 1, 1, 0, 0, 0]
+    assert [oracle.dcp_local(t, 2, 3, L=L) for t in range(9)] == [0, 1, 2, 0, 1, 2, 3, 4, 5]
+    for world, inter in ((1, 1), (4, 1), (3, 64), (8, 16), (5, 7), (2, 1000)):
+        seen = [0] * world
+        for t in range(1200):
+            r = oracle.dcp_owner(t, world, inter, L=L)
+            assert r == _owner(t, world, inter)
+            loc = oracle.dcp_local(t, world, inter, L=L)
+            assert loc == seen[r], (world, inter, t)
+            seen[r] += 1
+            assert oracle.dcp_global(loc, r, world, inter, L=L) == t
+
+
+_SPECIAL = [0.0, -0.0, 1.0, -1.0, 0.5, -0.5, 2.0, 1.0000001, float("inf"), float("-inf"), 1e-45, -1e-45,
+            1.1754942e-38, 3.4028235e38, -3.4028235e38, 7.25, -7.25]
+
+
+def pin_dcp_pack_orders_like_score_then_id(L):
+    """Packed candidates sorted as unsigned 64-bit integers (descending) come in
+    the order of Python's own sort by (score descending, id ascending), -0 equal
+    to +0, over infinities, subnormals, the extremes and ties; every candidate
+    unpacks to its (score, id) and none packs to the empty value 0."""
+    ids = [0, 1, 2, 5, 12345, 2 ** 31 - 1]
+    cand = [(float(np.float32(v)), i) for v in _SPECIAL for i in ids]
+    packed = [int(oracle.dcp_pack(np.float32([sc]), [i], L=L)[0]) for sc, i in cand]
+    assert all(p != 0 for p in packed)
+    by_packed = sorted(range(len(cand)), key=lambda j: -packed[j])
+    by_ref = sorted(range(len(cand)), key=lambda j: (-(cand[j][0] + 0.0), cand[j][1]))
+    assert [cand[j][0] + 0.0 for j in by_packed] == [cand[j][0] + 0.0 for j in by_ref]
+    assert [cand[j][1] for j in by_packed] == [cand[j][1] for j in by_ref]
+    for (sc, i), p in zip(cand, packed):
+        got = oracle.dcp_unpack(p, L=L)
+        assert got is not None and got[1] == i and got[0] == sc + 0.0 and math.copysign(1, got[0]) == \
+            math.copysign(1, sc + 0.0)
+    assert oracle.dcp_unpack(0, L=L) is None
+
+
+def _shard_lists(L, s, k, world, inter):
+    """Each rank's candidates: the pinned top-k of the scores it owns, ids global."""
+    n = len(s)
+    lists = np.zeros((world, 1, k), np.uint64)
+    for r in range(world):
+        owned = [t for t in range(n) if _owner(t, world, inter) == r]
+        if not owned:
+            continue
+        ls = s[owned]
+        li, lm = oracle.topk(ls, k, L=L)
+        glob = [owned[j] for j in li[:lm]]
+        lists[r, 0, :lm] = oracle.dcp_pack(ls[li[:lm]].astype(np.float32), glob, L=L)
+    return lists
+
+
+def pin_topk_merge_of_shards_is_global_topk(L):
+    """The DCP identity: a row's global top-k lies within the union of its
+    shards' local top-ks, so merging the shards' candidates gives exactly the
+    global top-k of the pinned oracle.topk (ids ascending, then -1), for
+    several world sizes, interleaves and k, on scores with many ties."""
+    rng = np.random.default_rng(41)
+    for n, k, world, inter in ((1000, 64, 4, 1), (1000, 64, 3, 64), (777, 100, 8, 16), (50, 64, 4, 8),
+                               (4096, 2048, 2, 64), (300, 7, 5, 300), (9, 4, 16, 1)):
+        s = rng.integers(-20, 21, n).astype(np.float64) * 0.25  # exact in fp32, many ties
+        gi, gm = oracle.topk(s, k, L=L)
+        ids, lens = oracle.topk_merge(_shard_lists(L, s, k, world, inter), k, L=L)
+        assert lens[0] == gm
+        assert np.array_equal(ids[0, :gm], np.sort(gi[:gm]))
+        assert np.all(ids[0, gm:] == -1)
+
+
+def pin_topk_merge_library(L):
+    """The selector against numpy's lexsort on lists of distinct random ids with
+    tied scores and empty slots; fewer candidates than k: all of them."""
+    rng = np.random.default_rng(42)
+    for R, n, k in ((4, 16, 8), (3, 50, 64), (8, 32, 32), (1, 10, 3), (2, 5, 0)):
+        ids_all = rng.permutation(10 ** 6)[:R * n].astype(np.int64)
+        sc = (rng.integers(-6, 7, R * n) * 0.5).astype(np.float32)
+        keep = rng.random(R * n) < 0.8
+        lists = np.where(keep, oracle.dcp_pack(sc, ids_all, L=L), 0).astype(np.uint64).reshape(R, 1, n)
+        got, lens = oracle.topk_merge(lists, k, L=L)
+        cs, ci = sc[keep].astype(np.float64), ids_all[keep]
+        order = np.lexsort((ci, -cs))[:k]
+        m = min(k, int(keep.sum()))
+        assert lens[0] == m
+        assert np.array_equal(got[0, :m], np.sort(ci[order]).astype(np.int32))
+        assert np.all(got[0, m:] == -1)
+
+
+def pin_topk_merge_refuses_duplicate_ids(L):
+    """An id offered by two lists cannot come from disjoint shards: refused."""
+    lists = np.zeros((2, 1, 4), np.uint64)
+    lists[0, 0, 0] = oracle.dcp_pack(np.float32([1.0]), [7], L=L)[0]
+    lists[1, 0, 0] = oracle.dcp_pack(np.float32([2.0]), [7], L=L)[0]
+    try:
+        oracle.topk_merge(lists, 4, L=L)
+    except ValueError:
+        return
+    raise AssertionError("a duplicate id was accepted")
+
+
+def pin_topk_compact_partitions_selection(L):
+    """Over the ranks, the compacted local slots mapped back by the ownership
+    rule are exactly the selection's valid slots, each on the rank that owns it
+    and in the selection's order; the lengths add up; slots past topk_len and
+    -1 slots are ignored; the rest of each row is -1."""
+    rng = np.random.default_rng(43)
+    k = 64
+    for world, inter in ((4, 1), (3, 64), (8, 16), (1, 1)):
+        sel = rng.permutation(5000)[:50].astype(np.int32)
+        idx = np.full((1, k), -1, np.int32)
+        idx[0, :50] = sel
+        idx[0, 7] = -1          # a hole inside the valid range
+        idx[0, 55] = 4321       # past topk_len: ignored
+        valid = [int(t) for t in idx[0, :50] if t >= 0]
+        total = 0
+        for r in range(world):
+            li, ll = oracle.topk_compact(idx, np.array([50], np.int32), r, world, inter, L=L)
+            mine = [t for t in valid if _owner(t, world, inter) == r]
+            assert ll[0] == len(mine)
+            back = [oracle.dcp_global(int(x), r, world, inter, L=L) for x in li[0, :ll[0]]]
+            assert back == mine
+            assert np.all(li[0, ll[0]:] == -1)
+            total += int(ll[0])
+        assert total == len(valid)
+
+
+def pin_lse_combine_of_split_attention(L):
+    """Attention over a selection equals the LSE combine of the attentions over
+    disjoint parts of it (each by the pinned oracle.sparse_mla), an empty part
+    (out 0, lse -inf) included; in parts of 1, 2 and 5."""
+    q, lat, lay = mla_case(n=40, seed=44)
+    sel = np.random.default_rng(44).permutation(40)[:29].astype(np.int32)
+    ref_o, ref_l, _ = oracle.sparse_mla(q, lat, lay, 0, sel, 29, 0.07, L=L)
+    for parts in (1, 2, 5):
+        chunks = np.array_split(sel, parts) + [np.zeros(0, np.int32)]
+        os_, ls_ = [], []
+        for c in chunks:
+            o, l, _ = oracle.sparse_mla(q, lat, lay, 0, np.ascontiguousarray(c), len(c), 0.07, L=L)
+            os_.append(o)
+            ls_.append(l)
+        out, lse = oracle.lse_combine(np.stack(os_), np.stack(ls_), L=L)
+        close(out, ref_o, 1e-12)
+        close(lse, ref_l, 1e-12)
+
+
+def pin_lse_combine_closed_forms(L):
+    """Two parts: lse = logaddexp(a, b) (numpy), out = e^(a-lse) x + e^(b-lse) y;
+    one part: itself; every part at -inf: out 0, lse -inf."""
+    rng = np.random.default_rng(45)
+    a, b = rng.standard_normal(6) * 3, rng.standard_normal(6) * 3
+    x, y = rng.standard_normal((6, 5)), rng.standard_normal((6, 5))
+    out, lse = oracle.lse_combine(np.stack([x, y]), np.stack([a, b]), L=L)
+    ref = np.logaddexp(a, b)
+    close(lse, ref)
+    close(out, np.exp(a - ref)[:, None] * x + np.exp(b - ref)[:, None] * y)
+    out, lse = oracle.lse_combine(x[None], a[None], L=L)
+    close(out, x)
+    close(lse, a)
+    ninf = np.full((3, 6), -np.inf)
+    out, lse = oracle.lse_combine(np.zeros((3, 6, 5)), ninf, L=L)
+    assert np.all(out == 0) and np.all(lse == -np.inf)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -92,6 +92,25 @@ MUTANTS = [
     ("mla_q_ssmax_head_index",
      "double f = (double)ssmax_s[h] * log((double)pos[t] + 1.0) + (double)ssmax_b[h];",
      "double f = (double)ssmax_s[(h + 1) % MH] * log((double)pos[t] + 1.0) + (double)ssmax_b[h];"),
+    # DCP
+    ("dcp_owner_ignores_interleave", "return (t / interleave) % world;", "return t % world;"),
+    ("dcp_local_skips_turns", "return (turn / world) * interleave + t % interleave;",
+     "return turn * interleave + t % interleave;"),
+    ("dcp_global_rank_dropped", "return (own_turn * world + rank) * interleave + local % interleave;",
+     "return (own_turn * world) * interleave + local % interleave;"),
+    ("pack_negative_order", "return (b & 0x80000000u) ? ~b : (b | 0x80000000u);",
+     "return (b & 0x80000000u) ? b : (b | 0x80000000u);"),
+    ("pack_negative_zero", "if (score == 0.0f) score = 0.0f; /* -0 as +0 */", ";"),
+    ("pack_id_not_inverted", "return ((uint64_t)score_code(score) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)id);",
+     "return ((uint64_t)score_code(score) << 32) | (uint64_t)(uint32_t)id;"),
+    ("merge_ids_unsorted", "qsort(ids, (size_t)m, sizeof(int32_t), by_id);", ";"),
+    ("merge_duplicates_accepted", "dup |= all[i] == all[i - 1];", ";"),
+    ("merge_takes_one_fewer", "int32_t m = n < k ? (int32_t)n : k;\n    for (int32_t i = 0; i < m; ++i) ids[i]",
+     "int32_t m = n < k ? (int32_t)n : k - 1;\n    for (int32_t i = 0; i < m; ++i) ids[i]"),
+    ("compact_ignores_owner", "if (t >= 0 && oracle_dcp_owner(t, world, interleave) == rank)", "if (t >= 0)"),
+    ("lse_combine_max_not_logsumexp", "double L = m + log(sum);", "double L = m;"),
+    ("lse_combine_weights_unnormalised",
+     "double wgt = exp(lse_parts[(int64_t)r * rows + i] - L);", "double wgt = exp(lse_parts[(int64_t)r * rows + i] - m);"),
 ]
 
 RUNNER = r"""
