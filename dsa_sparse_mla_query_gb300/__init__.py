@@ -1,7 +1,8 @@
 """GB300 (sm_103a) DSA decode path: lightning indexer -> exact top-k -> sparse
 absorbed-MLA attention, as hand-written CUDA behind a C ABI (include/dsa.h),
 plus the cache-write side (new indexer keys and latent rows into the caches,
-the attention query's RoPE + SSMax).
+the attention query's RoPE + SSMax) and one rank's compute steps of decode
+context parallelism (top-k candidates, their merge, compaction, LSE combine).
 
 The Python names mirror the C entry points; they only marshal arguments.
 Importing the package loads nothing; the first call loads ``libdsa.so`` and
@@ -12,6 +13,7 @@ from ._binding import (  # noqa: F401
     DSA_BF16,
     DSA_FP8_DS_MLA,
     DSA_FP8_E4M3_ROWSCALE,
+    DcpShard,
     DsaError,
     Seqs,
     dsa_decode_layer,
@@ -19,8 +21,12 @@ from ._binding import (  # noqa: F401
     dsa_index_k_insert,
     dsa_index_scores,
     dsa_latent_insert,
+    dsa_lse_combine,
     dsa_mla_q_prep,
     dsa_topk,
+    dsa_topk_candidates,
+    dsa_topk_compact,
+    dsa_topk_merge,
     dsa_workspace_size,
     load,
     sparse_mla_decode,
@@ -30,4 +36,5 @@ from ._binding import (  # noqa: F401
 
 __all__ = ["Seqs", "DsaError", "dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode", "sparse_mla_decode_noalloc",
            "dsa_decode_layer", "dsa_decode_layer_launches", "dsa_index_k_insert", "dsa_latent_insert", "dsa_mla_q_prep",
+           "DcpShard", "dsa_topk_candidates", "dsa_topk_merge", "dsa_topk_compact", "dsa_lse_combine",
            "load", "version", "DSA_BF16", "DSA_FP8_E4M3_ROWSCALE", "DSA_FP8_DS_MLA"]

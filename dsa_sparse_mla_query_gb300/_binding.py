@@ -24,6 +24,11 @@ EXPORTS = ("dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_dec
            "dsa_version")
 
 
+class DcpShard(ctypes.Structure):
+    """dsa_dcp_shard: token t lives on rank (t // interleave) % world."""
+    _fields_ = [("world", ctypes.c_int32), ("rank", ctypes.c_int32), ("interleave", ctypes.c_int32)]
+
+
 class DsaError(RuntimeError):
     def __init__(self, status: int, msg: str):
         super().__init__(f"status {status}: {msg}")
@@ -34,7 +39,8 @@ class DsaSeqsC(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("max_ctx", ctypes.c_int32), ("max_q_per_seq", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("max_pages", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("num_rows", ctypes.c_int64), ("ctx_len", ctypes.c_void_p), ("q_start", ctypes.c_void_p),
-                ("q_pos", ctypes.c_void_p), ("page_table", ctypes.c_void_p), ("seq_base", ctypes.c_void_p)]
+                ("q_pos", ctypes.c_void_p), ("page_table", ctypes.c_void_p), ("seq_base", ctypes.c_void_p),
+                ("q_rope_pos", ctypes.c_void_p)]
 
 
 class DsaLayerArgsC(ctypes.Structure):
@@ -75,6 +81,11 @@ def load(path: str = LIB_PATH):
         L.dsa_index_k_insert.argtypes = [P, P, P, F, P, P, P, I32, P, P, ctypes.c_int, I64, P, P]
         L.dsa_latent_insert.argtypes = [P, P, P, P, P, I32, P, ctypes.c_int, I64, P, P]
         L.dsa_mla_q_prep.argtypes = [P, P, P, P, P, I32, P, P, P]
+        SH = ctypes.POINTER(DcpShard)
+        L.dsa_topk_candidates.argtypes = [P, I64, S, I32, I32, SH, P, P, P, P, SZ, P, P]
+        L.dsa_topk_merge.argtypes = [P, I32, I32, I32, I32, P, P, P, P]
+        L.dsa_topk_compact.argtypes = [P, P, I32, I32, SH, P, P, P, P]
+        L.dsa_lse_combine.argtypes = [P, P, I32, I32, P, P, P]
         L.dsa_decode_layer_launches.restype = ctypes.c_int32
         for f in ("dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode", "dsa_decode_layer"):
             getattr(L, f).restype = ctypes.c_int
@@ -113,8 +124,9 @@ class Seqs:
     host-side bounds.  Keeps the tensors alive while calls are enqueued."""
 
     def __init__(self, ctx_len, q_start, q_pos, *, max_ctx: int, max_q_per_seq: int, num_rows: int,
-                 page_table=None, page_size: int = 0, seq_base=None):
+                 page_table=None, page_size: int = 0, seq_base=None, q_rope_pos=None):
         self.ctx_len, self.q_start, self.q_pos = ctx_len, q_start, q_pos
+        self.q_rope_pos = q_rope_pos
         self.page_table, self.seq_base = page_table, seq_base
         self.num_seqs = int(ctx_len.shape[0])
         self.num_q = int(q_pos.shape[0])
@@ -125,7 +137,7 @@ class Seqs:
     def c(self) -> DsaSeqsC:
         return DsaSeqsC(self.num_seqs, self.max_ctx, self.max_q_per_seq, self.page_size, self.max_pages, 0,
                         self.num_rows, _p(self.ctx_len), _p(self.q_start), _p(self.q_pos), _p(self.page_table),
-                        _p(self.seq_base))
+                        _p(self.seq_base), _p(self.q_rope_pos))
 
 
 def dsa_workspace_size(seqs: Seqs, num_q: int, k: int) -> int:
@@ -218,3 +230,38 @@ def dsa_latent_insert(c_kv, k_pe, pos, inv_freq, slot, n: int, latent, latent_dt
 def dsa_mla_q_prep(q, ssmax_s, ssmax_b, inv_freq, q_pos, num_q: int, q_out, d_status=None, stream=None):
     _check(load().dsa_mla_q_prep(_p(q), _p(ssmax_s), _p(ssmax_b), _p(inv_freq), _p(q_pos), num_q, _p(q_out),
                                  _p(d_status), _stream(stream)))
+
+
+# ---- DCP: one rank's compute steps (include/dsa.h)
+def _ptr_array(tensors):
+    """Host array of device pointers (kept alive by the caller's reference)."""
+    arr = (ctypes.c_void_p * len(tensors))(*[_p(t) for t in tensors])
+    return arr
+
+
+def dsa_topk_candidates(scores, ld: int, seqs: Seqs, num_q: int, k: int, shard: DcpShard, idx, topk_len, cand,
+                        workspace=None, workspace_bytes: int = 0, d_status=None, stream=None):
+    sc = seqs.c()
+    _check(load().dsa_topk_candidates(_p(scores), ld, ctypes.byref(sc), num_q, k, ctypes.byref(shard), _p(idx),
+                                      _p(topk_len), _p(cand), _p(workspace), workspace_bytes, _p(d_status),
+                                      _stream(stream)))
+
+
+def dsa_topk_merge(lists, list_len: int, num_q: int, k: int, idx, topk_len, d_status=None, stream=None):
+    arr = _ptr_array(lists)
+    _check(load().dsa_topk_merge(ctypes.cast(arr, ctypes.c_void_p), len(lists), list_len, num_q, k, _p(idx),
+                                 _p(topk_len), _p(d_status), _stream(stream)))
+
+
+def dsa_topk_compact(idx, topk_len, num_q: int, k: int, shard: DcpShard, local_idx, local_len, d_status=None,
+                     stream=None):
+    _check(load().dsa_topk_compact(_p(idx), _p(topk_len), num_q, k, ctypes.byref(shard), _p(local_idx),
+                                   _p(local_len), _p(d_status), _stream(stream)))
+
+
+def dsa_lse_combine(o_parts, lse_parts, num_q: int, out, lse=None, stream=None):
+    if len(o_parts) != len(lse_parts):
+        raise ValueError("o_parts and lse_parts differ in length")
+    oa, la = _ptr_array(o_parts), _ptr_array(lse_parts)
+    _check(load().dsa_lse_combine(ctypes.cast(oa, ctypes.c_void_p), ctypes.cast(la, ctypes.c_void_p), len(o_parts),
+                                  num_q, _p(out), _p(lse), _stream(stream)))

@@ -62,6 +62,7 @@ void check_seqs(Check& c, const dsa_seqs* s, int32_t num_q) {
     c.ptr(s->ctx_len, "seqs.ctx_len", 4);
     c.ptr(s->q_start, "seqs.q_start", 4);
     c.ptr(s->q_pos, "seqs.q_pos", 4);
+    if (s->q_rope_pos) c.ptr(s->q_rope_pos, "seqs.q_rope_pos", 4);
     if (s->page_table) {
         c.ptr(s->page_table, "seqs.page_table", 4);
         c.need(s->page_size >= 16 && (s->page_size & (s->page_size - 1)) == 0, DSA_ERR_UNSUPPORTED,
@@ -152,9 +153,29 @@ cudaError_t launch_latent_insert(const void* c_kv, const void* k_pe, const int32
 cudaError_t launch_mla_q_prep(const void* q, const float* ssmax_s, const float* ssmax_b, const float* inv_freq,
                               const int32_t* q_pos, int32_t num_q, void* q_out, int32_t* d_status,
                               cudaStream_t stream);
+cudaError_t launch_cand_pack(const float* scores, int64_t ld, const int32_t* idx, const int32_t* topk_len, int num_q,
+                             int k, int world, int rank, int inter, uint64_t* cand, int32_t* d_status,
+                             cudaStream_t stream);
+cudaError_t launch_topk_merge(const uint64_t* const* lists, int num_lists, int list_len, int num_q, int k,
+                              int32_t* idx, int32_t* topk_len, int32_t* d_status, cudaStream_t stream);
+cudaError_t launch_topk_compact(const int32_t* idx, const int32_t* topk_len, int num_q, int k, int world, int rank,
+                                int inter, int32_t* local_idx, int32_t* local_len, int32_t* d_status,
+                                cudaStream_t stream);
+cudaError_t launch_lse_combine(const void* const* o_parts, const float* const* lse_parts, int num_parts, int num_q,
+                               void* out, float* lse, cudaStream_t stream);
 }  // namespace dsa
 
+
 using namespace dsa;
+
+static void check_shard(Check& c, const dsa_dcp_shard* sh) {
+    c.need(sh != nullptr, DSA_ERR_INVALID_ARG, "shard is NULL");
+    if (!sh) return;
+    c.need(sh->world >= 1 && sh->world <= DSA_DCP_MAX_RANKS, DSA_ERR_UNSUPPORTED, "shard world %d outside [1, %d]",
+           sh->world, DSA_DCP_MAX_RANKS);
+    c.need(sh->rank >= 0 && sh->rank < sh->world, DSA_ERR_INVALID_ARG, "shard rank %d outside [0, world)", sh->rank);
+    c.need(sh->interleave >= 1, DSA_ERR_INVALID_ARG, "shard interleave %d < 1", sh->interleave);
+}
 
 extern "C" {
 
@@ -304,6 +325,96 @@ dsa_status dsa_topk(const float* scores, int64_t ld, const dsa_seqs* seqs, int32
     if (long_rows) ws = carve_workspace(workspace, *seqs, num_q, k);
     return cuda_status(launch_topk(scores, ld, *seqs, num_q, k, idx, topk_len, ws, d_status, stream),
                        "dsa_topk launch");
+}
+
+dsa_status dsa_topk_candidates(const float* scores, int64_t ld, const dsa_seqs* seqs, int32_t num_q, int32_t k,
+                               const dsa_dcp_shard* shard, int32_t* idx, int32_t* topk_len, uint64_t* cand,
+                               void* workspace, size_t workspace_bytes, int32_t* d_status, cudaStream_t stream) {
+    Check c;
+    check_seqs(c, seqs, num_q);
+    check_shard(c, shard);
+    c.ptr(scores, "scores");
+    c.ptr(idx, "idx", 4);
+    c.ptr(topk_len, "topk_len", 4);
+    c.ptr(cand, "cand", 8);
+    c.need(k >= 1 && k <= DSA_MAX_TOPK, DSA_ERR_UNSUPPORTED, "k %d outside [1, %d]", k, DSA_MAX_TOPK);
+    if (seqs) c.need(ld >= seqs->max_ctx && ld % 4 == 0, DSA_ERR_INVALID_ARG, "ld %lld must be >= max_ctx and a multiple of 4", (long long)ld);
+    const bool long_rows = seqs && topk_long_rows(seqs->max_ctx);
+    if (long_rows) check_workspace(c, seqs, num_q, k, workspace, workspace_bytes);
+    dsa_status st = c.done();
+    if (st != DSA_OK || num_q == 0) return st;
+    Workspace ws{};
+    if (long_rows) ws = carve_workspace(workspace, *seqs, num_q, k);
+    cudaError_t e = launch_topk(scores, ld, *seqs, num_q, k, idx, topk_len, ws, d_status, stream);
+    if (e == cudaSuccess)
+        e = launch_cand_pack(scores, ld, idx, topk_len, num_q, k, shard->world, shard->rank, shard->interleave, cand,
+                             d_status, stream);
+    return cuda_status(e, "dsa_topk_candidates launch");
+}
+
+dsa_status dsa_topk_merge(const uint64_t* const* lists, int32_t num_lists, int32_t list_len, int32_t num_q,
+                          int32_t k, int32_t* idx, int32_t* topk_len, int32_t* d_status, cudaStream_t stream) {
+    Check c;
+    c.need(num_q >= 0, DSA_ERR_INVALID_ARG, "num_q %d < 0", num_q);
+    c.need(lists != nullptr, DSA_ERR_INVALID_ARG, "lists (host array) is NULL");
+    c.need(num_lists >= 1 && num_lists <= DSA_DCP_MAX_RANKS, DSA_ERR_UNSUPPORTED, "num_lists %d outside [1, %d]",
+           num_lists, DSA_DCP_MAX_RANKS);
+    c.need(list_len >= 1, DSA_ERR_INVALID_ARG, "list_len %d < 1", list_len);
+    c.need((int64_t)num_lists * list_len <= DSA_DCP_MAX_CANDIDATES, DSA_ERR_UNSUPPORTED,
+           "num_lists x list_len = %lld exceeds %d", (long long)num_lists * list_len, DSA_DCP_MAX_CANDIDATES);
+    c.need(k >= 1 && k <= DSA_MAX_TOPK, DSA_ERR_UNSUPPORTED, "k %d outside [1, %d]", k, DSA_MAX_TOPK);
+    if (num_q > 0) {
+        if (lists && num_lists >= 1 && num_lists <= DSA_DCP_MAX_RANKS)
+            for (int r = 0; r < num_lists; ++r) c.ptr(lists[r], "lists[r]", 8);
+        c.ptr(idx, "idx", 4);
+        c.ptr(topk_len, "topk_len", 4);
+    }
+    dsa_status st = c.done();
+    if (st != DSA_OK || num_q == 0) return st;
+    return cuda_status(launch_topk_merge(lists, num_lists, list_len, num_q, k, idx, topk_len, d_status, stream),
+                       "dsa_topk_merge launch");
+}
+
+dsa_status dsa_topk_compact(const int32_t* idx, const int32_t* topk_len, int32_t num_q, int32_t k,
+                            const dsa_dcp_shard* shard, int32_t* local_idx, int32_t* local_len, int32_t* d_status,
+                            cudaStream_t stream) {
+    Check c;
+    c.need(num_q >= 0, DSA_ERR_INVALID_ARG, "num_q %d < 0", num_q);
+    c.need(k >= 1 && k <= DSA_MAX_TOPK, DSA_ERR_UNSUPPORTED, "k %d outside [1, %d]", k, DSA_MAX_TOPK);
+    check_shard(c, shard);
+    if (num_q > 0) {
+        c.ptr(idx, "idx", 4);
+        c.ptr(topk_len, "topk_len", 4);
+        c.ptr(local_idx, "local_idx", 4);
+        c.ptr(local_len, "local_len", 4);
+    }
+    dsa_status st = c.done();
+    if (st != DSA_OK || num_q == 0) return st;
+    return cuda_status(launch_topk_compact(idx, topk_len, num_q, k, shard->world, shard->rank, shard->interleave,
+                                           local_idx, local_len, d_status, stream),
+                       "dsa_topk_compact launch");
+}
+
+dsa_status dsa_lse_combine(const void* const* o_parts, const float* const* lse_parts, int32_t num_parts,
+                           int32_t num_q, void* out, float* lse, cudaStream_t stream) {
+    Check c;
+    c.need(num_q >= 0, DSA_ERR_INVALID_ARG, "num_q %d < 0", num_q);
+    c.need(o_parts != nullptr && lse_parts != nullptr, DSA_ERR_INVALID_ARG, "o_parts / lse_parts (host arrays) NULL");
+    c.need(num_parts >= 1 && num_parts <= DSA_DCP_MAX_RANKS, DSA_ERR_UNSUPPORTED, "num_parts %d outside [1, %d]",
+           num_parts, DSA_DCP_MAX_RANKS);
+    if (num_q > 0) {
+        if (o_parts && lse_parts && num_parts >= 1 && num_parts <= DSA_DCP_MAX_RANKS)
+            for (int r = 0; r < num_parts; ++r) {
+                c.ptr(o_parts[r], "o_parts[r]");
+                c.ptr(lse_parts[r], "lse_parts[r]", 4);
+            }
+        c.ptr(out, "out");
+        if (lse) c.ptr(lse, "lse", 4);
+    }
+    dsa_status st = c.done();
+    if (st != DSA_OK || num_q == 0) return st;
+    return cuda_status(launch_lse_combine(o_parts, lse_parts, num_parts, num_q, out, lse, stream),
+                       "dsa_lse_combine launch");
 }
 
 static void check_mla_args(Check& c, const void* q, const void* latent, dsa_dtype latent_dtype, const int32_t* idx,

@@ -65,10 +65,11 @@ __device__ __forceinline__ void qprep_setup(const float* __restrict__ w, const f
                                             int* ok, int32_t* d_status) {
     const bool rope = inv_freq != nullptr;
     const int b = seq_of(s.q_start, s.num_seqs, t);
-    const int pos = __ldg(s.q_pos + t);
+    const int bound = __ldg(s.q_pos + t);                           // causal bound
+    const int pos = s.q_rope_pos ? __ldg(s.q_rope_pos + t) : bound;  // SSMax and RoPE position
     if (threadIdx.x == 0) {
         const int ctx = __ldg(s.ctx_len + b);
-        *ok = (pos >= 0 && pos < ctx && ctx <= s.max_ctx);
+        *ok = (bound >= 0 && bound < ctx && ctx <= s.max_ctx && pos >= 0);
         if (!*ok) report(d_status, DSA_ERR_BAD_INPUT);
     }
     if (threadIdx.x < 32) {

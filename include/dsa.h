@@ -95,6 +95,9 @@ typedef struct {
     const int32_t* q_pos;     /* [num_q] */
     const int32_t* page_table;/* [B, max_pages] or NULL */
     const int64_t* seq_base;  /* [B] when page_table is NULL */
+    const int32_t* q_rope_pos;/* [num_q] or NULL: the queries' absolute positions for the index query's
+                                 SSMax and RoPE when q_pos holds a shard's local causal bounds (DCP);
+                                 NULL: q_pos */
 } dsa_seqs;
 
 /* Bytes of workspace the calls below need for these sizes (host only; no
@@ -199,6 +202,87 @@ dsa_status dsa_latent_insert(const void* c_kv, const void* k_pe, const int32_t* 
  * that query's row left unwritten. */
 dsa_status dsa_mla_q_prep(const void* q, const float* ssmax_s, const float* ssmax_b, const float* inv_freq,
                           const int32_t* q_pos, int32_t num_q, void* q_out, int32_t* d_status, cudaStream_t stream);
+
+/* ---- DCP: one rank's compute steps of decode context parallelism ----
+ * ([vLLM-ML4] Long context: decode and prefill context parallelism.)  The
+ * latent and index caches are sharded by token over `world` ranks.  Each rank
+ * scores its own keys and offers its local top-k as packed (score, id)
+ * candidates (dsa_topk_candidates); the candidate lists are exchanged (peer
+ * inboxes, NCCL: the caller's) and the selector merges them in place into the
+ * exact global top-k (dsa_topk_merge); each rank keeps the selected slots it
+ * owns as local positions with their count (dsa_topk_compact), attends over
+ * them with sparse_mla_decode on its shard (a rank owning none of a query's
+ * slots gets out = 0, lse = -inf), and the partial outputs are merged
+ * (dsa_lse_combine).  On one GPU the ranks' shards can live in one memory and
+ * the same calls run the sharded layer.
+ *
+ * Ownership: turns of `interleave` tokens go round the ranks: token t of a
+ * sequence lives on rank (t / interleave) % world at local position
+ * (t / (interleave * world)) * interleave + t % interleave. */
+#define DSA_DCP_MAX_RANKS 16          /* ranks, candidate lists and combine parts per call */
+#define DSA_DCP_MAX_CANDIDATES 16384  /* num_lists x list_len per query in the selector */
+
+typedef struct {
+    int32_t world;       /* ranks sharing a sequence's tokens, 1..DSA_DCP_MAX_RANKS */
+    int32_t rank;        /* this rank, 0..world-1 */
+    int32_t interleave;  /* tokens per turn, >= 1 (a contiguous shard of S tokens: S) */
+} dsa_dcp_shard;
+
+/* Packed candidate (uint64): the high 32 bits the score's order-preserving
+ * code (its fp32 bits with the sign bit set when positive, all bits inverted
+ * when negative; -0 coded as +0), the low 32 bits 0xFFFFFFFF - id.  A larger
+ * packed value is a larger score or, at equal scores, a smaller id, so the
+ * exact top-k of any set of candidates is the k largest packed values; 0 is
+ * an empty slot. */
+
+/* A rank's top-k candidates: dsa_topk over the rank's local scores (seqs,
+ * scores and the causal bounds q_pos in the rank's local positions), then
+ * each selected local position l packed with its score and its global id
+ * (l / interleave * world + rank) * interleave + l % interleave.
+ *   idx, topk_len, workspace: as dsa_topk (the local selection)
+ *   cand uint64 [num_q, k], 8-byte aligned: slot i < topk_len[t] the packed
+ *        candidate of idx[t][i], the rest 0.
+ * Scores must not be NaN.  A global id past INT32_MAX: DSA_ERR_BAD_INPUT in
+ * *d_status and an empty slot. */
+dsa_status dsa_topk_candidates(const float* scores, int64_t ld, const dsa_seqs* seqs, int32_t num_q, int32_t k,
+                               const dsa_dcp_shard* shard, int32_t* idx, int32_t* topk_len, uint64_t* cand,
+                               void* workspace, size_t workspace_bytes, int32_t* d_status, cudaStream_t stream);
+
+/* The selector: the exact top-k of num_lists candidate lists per query,
+ * read in place (one list per rank).
+ *   lists    host array of num_lists (1..16) device pointers, each uint64
+ *            [num_q, list_len], 8-byte aligned; num_lists * list_len <= 16384
+ *   idx      int32 [num_q, k]: the min(k, #candidates) candidates with the
+ *            largest scores (ties to the smaller id), their ids ascending,
+ *            then -1;  topk_len int32 [num_q]
+ * Ids must be distinct across a query's lists (the shards are disjoint).  A
+ * repeated id among the selected: DSA_ERR_BAD_INPUT in *d_status and that
+ * query's row empty (topk_len 0, all -1).  1 <= k <= 2048. */
+dsa_status dsa_topk_merge(const uint64_t* const* lists, int32_t num_lists, int32_t list_len, int32_t num_q,
+                          int32_t k, int32_t* idx, int32_t* topk_len, int32_t* d_status, cudaStream_t stream);
+
+/* Top-k compaction for one rank: the slots i < topk_len[t] of idx holding a
+ * global id >= 0 that shard->rank owns, in their order, as local positions;
+ * local_len[t] their number; the rest of local_idx[t] -1.  With local_idx and
+ * local_len as idx and topk_len, sparse_mla_decode on the rank's shard reads
+ * only the rank's share of the selection, its loop bounded by local_len.
+ *   idx int32 [num_q, k], topk_len int32 [num_q] (0..k; outside: clamped and
+ *   DSA_ERR_BAD_INPUT); local_idx int32 [num_q, k], local_len int32 [num_q].
+ * The outputs may be the inputs (in place). */
+dsa_status dsa_topk_compact(const int32_t* idx, const int32_t* topk_len, int32_t num_q, int32_t k,
+                            const dsa_dcp_shard* shard, int32_t* local_idx, int32_t* local_len, int32_t* d_status,
+                            cudaStream_t stream);
+
+/* LSE combine of num_parts partial attention results (one per rank), per
+ * query and head: lse = ln sum_r exp(lse_r), out = sum_r exp(lse_r - lse) o_r;
+ * parts at -inf (empty rows) add nothing; all at -inf give out = 0, lse = -inf.
+ *   o_parts   host array of num_parts (1..16) device pointers, each bf16
+ *             [num_q, 64, 512] (16-byte aligned), as sparse_mla_decode writes
+ *   lse_parts host array of num_parts device pointers, each fp32 [num_q, 64]
+ *   out bf16 [num_q, 64, 512]; lse fp32 [num_q, 64] or NULL
+ * Weights and sums in fp32, out rounded to bf16 (nearest even). */
+dsa_status dsa_lse_combine(const void* const* o_parts, const float* const* lse_parts, int32_t num_parts,
+                           int32_t num_q, void* out, float* lse, cudaStream_t stream);
 
 /* One decode layer: dsa_index_scores -> dsa_topk -> sparse_mla_decode on one
  * stream, with the scores kept in the workspace.  reuse_idx != 0 is a

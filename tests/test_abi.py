@@ -102,3 +102,56 @@ def test_binding_fails_loudly_without_library(tmp_path):
             B.load(str(tmp_path / "missing.so"))
         finally:
             B._lib = B._lib_saved
+
+
+def test_dcp_calls_refuse_bad_arguments(lib):
+    """The DCP calls refuse, on the host and with every reason listed, what
+    they cannot serve; nothing is enqueued (no GPU needed)."""
+    from dsa_sparse_mla_query_gb300 import _binding as B
+    P = ctypes.c_void_p
+
+    def msg():
+        return lib.dsa_last_error_string().decode()
+
+    many = (P * 17)(*([0x100] * 17))
+    assert lib.dsa_topk_merge(ctypes.cast(many, P), 17, 64, 1, 2048, 0x200, 0x300, None, None) == \
+        B.DSA_ERR_UNSUPPORTED
+    assert "num_lists 17" in msg()
+    eight = (P * 8)(*([0x100] * 8))
+    assert lib.dsa_topk_merge(ctypes.cast(eight, P), 8, 4096, 1, 2048, 0x200, 0x300, None, None) == \
+        B.DSA_ERR_UNSUPPORTED
+    assert "exceeds 16384" in msg()
+    bad = (P * 3)(0x100, None, 0x104)
+    assert lib.dsa_topk_merge(ctypes.cast(bad, P), 3, 64, 1, 2048, 0x200, 0x300, None, None) == \
+        B.DSA_ERR_INVALID_ARG
+    assert "lists[r] is NULL" in msg() and "lists[r] is not 8-byte aligned" in msg()
+    assert lib.dsa_topk_merge(None, 2, 64, 1, 2048, 0x200, 0x300, None, None) == B.DSA_ERR_INVALID_ARG
+    assert "lists (host array) is NULL" in msg()
+
+    sh = B.DcpShard(4, 4, 0)
+    assert lib.dsa_topk_compact(0x100, 0x200, 1, 2048, ctypes.byref(sh), 0x300, 0x400, None, None) == \
+        B.DSA_ERR_INVALID_ARG
+    assert "shard rank 4" in msg() and "shard interleave 0" in msg()
+    assert lib.dsa_topk_compact(0x100, 0x200, 1, 2048, None, 0x300, 0x400, None, None) == B.DSA_ERR_INVALID_ARG
+    assert "shard is NULL" in msg()
+
+    s = _seqs(B)
+    big = B.DcpShard(17, 0, 1)
+    rc = lib.dsa_topk_candidates(0x100, 4096, ctypes.byref(s), 1, 2048, ctypes.byref(big), 0x200, 0x300, 0x404, None,
+                                 0, None, None)
+    assert rc != 0 and "shard world 17" in msg() and "cand is not 8-byte aligned" in msg()
+
+    assert lib.dsa_lse_combine(ctypes.cast(eight, P), ctypes.cast(eight, P), 0, 1, 0x100, None, None) == \
+        B.DSA_ERR_UNSUPPORTED
+    assert "num_parts 0" in msg()
+    assert lib.dsa_lse_combine(None, None, 2, 1, 0x100, None, None) == B.DSA_ERR_INVALID_ARG
+
+
+def test_dcp_calls_with_zero_queries_are_no_ops(lib):
+    from dsa_sparse_mla_query_gb300 import _binding as B
+    P = ctypes.c_void_p
+    two = (P * 2)(0x100, 0x200)
+    sh = B.DcpShard(2, 1, 64)
+    assert lib.dsa_topk_merge(ctypes.cast(two, P), 2, 64, 0, 2048, None, None, None, None) == 0
+    assert lib.dsa_topk_compact(None, None, 0, 2048, ctypes.byref(sh), None, None, None, None) == 0
+    assert lib.dsa_lse_combine(ctypes.cast(two, P), ctypes.cast(two, P), 2, 0, None, None, None) == 0
