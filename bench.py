@@ -50,6 +50,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak-s", type=float, default=1.0, help="untimed load before the timed region (clocks)")
     ap.add_argument("--seqs", type=int, default=0, help="override the number of sequences (small profiling cases)")
+    ap.add_argument("--dcp", type=int, default=0,
+                    help="run the layer sharded by token over this many ranks on one GPU (DCP calls)")
+    ap.add_argument("--dcp-interleave", type=int, default=0,
+                    help="tokens per turn of the DCP ownership (default: the page size, else 1)")
     return ap.parse_args()
 
 
@@ -434,6 +438,127 @@ def run_ours(args, wl, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_dcp(args, wl, ws, rank, local):
+    """The layer sharded by token over args.dcp ranks whose shards share this
+    GPU: per rank the indexer and its top-k candidates, the selector's merge,
+    per rank compaction and attention, the LSE combine (dcp.ShardedLayer)."""
+    from dsa_sparse_mla_query_gb300.dcp import ShardedLayer
+    import dsa_sparse_mla_query_gb300 as dsa
+    from dsa_sparse_mla_query_gb300 import _binding as B
+
+    R = args.dcp
+    inter = args.dcp_interleave or (wl.page_size or 1)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        threads = cpu_threads()
+        jobs = oracle_sample(wl, 6 * threads)
+        secs = oracle_timed(wl, jobs, threads)
+        cpu = {"value": len(jobs) / secs, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{len(jobs)} queries of {wl.name}, each the whole (unsharded) layer, "
+                         f"{threads} threads of the fp64 oracle, {secs:.1f} s wall"}
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dsa.load()
+    d = I.make_inputs(wl, dev)
+    lay = d["layout"]
+    sh = ShardedLayer(d, wl.queries_per_seq, wl.topk, R, inter, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    K, W = args.steps, args.warmup
+
+    def phase_ok(name):  # outside the timed regions
+        torch.cuda.synchronize(dev)
+        if sh.device_status() != 0:
+            raise RuntimeError(f"device status {sh.device_status()} after {name}")
+
+    for _ in range(W):
+        sh.run(stream)
+    phase_ok("warm-up")
+    sampler = ClockSampler(local)
+    t_soak = time.time()
+    while time.time() < t_soak + args.soak_s:
+        for _ in range(20):
+            sh.run(stream)
+        torch.cuda.synchronize(dev)
+    phase_ok("the untimed load")
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(K):
+        sh.run(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_step = start.elapsed_time(end) / K
+    phase_ok("the timed steps")
+    # stages: a second pass with events between them
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    for i in range(K):
+        sh.run(stream, marks=marks[i])
+    phase_ok("the stage-timing steps")
+    st = lambda a, b: statistics.mean(m[a].elapsed_time(m[b]) for m in marks)  # noqa: E731
+    stages = {"indexers_and_candidates": st(0, 1), "merge": st(1, 2), "compact_and_attention": st(2, 3),
+              "lse_combine": st(3, 4)}
+    # the indexer of every rank alone, events around each launch
+    kd = B.DSA_FP8_E4M3_ROWSCALE if sh.k_fp8 else B.DSA_BF16
+    iev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * R)] for _ in range(K)]
+    for i in range(K):
+        for r, v in enumerate(sh.views):
+            iev[i][2 * r].record(stream)
+            B.dsa_index_scores(d["q_idx"], d["w"], d["ssmax_s"], d["ssmax_b"], d["inv_freq"], v.k_idx, v.k_scale, kd,
+                               v.seqs, sh.num_q, v.scores, v.ld, sh.ws, sh.ws_bytes, sh.status, stream)
+            iev[i][2 * r + 1].record(stream)
+    phase_ok("the indexer-timing pass")
+    t_done = time.time()
+    clocks = sampler.stop(t_soak, t_done)
+    idx_ms = statistics.mean(sum(e[2 * r].elapsed_time(e[2 * r + 1]) for r in range(R)) for e in iev)
+    # end to end: the step's query inputs from pinned host memory, outputs back
+    keys = ["q_idx", "w", "q_mla"] + (["q_mla2"] if sh.shared else [])
+    host_in = {k: d[k].cpu().pin_memory() for k in keys}
+    host_pos = d["q_pos"].cpu().pin_memory()
+    outs = [sh.out, sh.lse, sh.idx, sh.topk_len] + ([sh.out2, sh.lse2] if sh.shared else [])
+    host_out = [o.cpu().pin_memory() for o in outs]
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values()) + host_pos.numel() * 4
+    d2h = sum(o.numel() * o.element_size() for o in host_out)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        for k, v in host_in.items():
+            d[k].copy_(v, non_blocking=True)
+        d["q_pos"].copy_(host_pos, non_blocking=True)
+        sh.run(stream)
+        for o, h in zip(outs, host_out):
+            h.copy_(o, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / K
+    phase_ok("the end-to-end steps")
+    ab = algorithmic_bytes(wl, lay)
+    peak, peak_kind = measured_peaks()
+    achieved = ab["indexer"] / (idx_ms / 1000.0) / 1e9
+    lat = B.DSA_FP8_DS_MLA if sh.lat_fp8 else B.DSA_BF16
+    per_rank = [B.dsa_decode_layer_launches(v.seqs, sh.num_q, wl.topk, 0, lat) + 2 +
+                (B.dsa_decode_layer_launches(v.seqs, sh.num_q, wl.topk, 1, lat) if sh.shared else 0)
+                for v in sh.views]
+    launches = sum(per_rank) + 1 + (2 if sh.shared else 1)
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": ws * wl.num_queries / (ms_step / 1000.0), "unit": UNIT, "n_gpus": ws,
+            "steps": K, "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if not wl.index_fp8 else "e4m3/bf16", "data": "synthetic",
+            "config": {"workload": wl.describe(), "queries": wl.num_queries,
+                       "dcp": f"sharded by token over {R} ranks in turns of {inter} tokens, every shard on this GPU",
+                       "l2": "inputs larger than L2",
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": None, "kernel": f"indexer over the {R} shards (query prep + key scan per rank)",
+                         "algorithmic_bytes_per_launch": ab["indexer"], "ms_per_launch": idx_ms,
+                         "peak_kind": f"{peak_kind} HBM copy"},
+            "stages_ms": stages,
+            "e2e": {"value": ws * wl.num_queries / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": K * launches, "clocks": clocks, "cpu_baseline": cpu}), flush=True)
+
+
 INSERT_TOKENS = 1 << 20
 INSERT_KEY_BYTES = 256 + 132 + 8 + 4        # x in; e4m3 row + scale out; slot + position
 INSERT_LATENT_BYTES = 1024 + 128 + 656 + 8 + 4  # c_kv + k_pe in; fp8_ds_mla row out; slot + position
@@ -601,7 +726,10 @@ def main():
     if ws > 1:
         torch.distributed.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
     try:
-        run_ours(args, wl, ws, rank, local)
+        if args.dcp:
+            run_dcp(args, wl, ws, rank, local)
+        else:
+            run_ours(args, wl, ws, rank, local)
     finally:
         if ws > 1:
             torch.distributed.destroy_process_group()

@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                     }
             };
             int s_next = 0, s_half = 0, pv_next = 0;
-            uint64_t t_idle = 0;
+            ptx::WaitClock idle;  // time without progress
             while (ok && pv_next < ntiles) {
                 bool progressed = false;
                 if (s_next < ntiles) {
@@ -372,12 +372,10 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                     progressed = true;
                 }
                 if (progressed) {
-                    t_idle = 0;
+                    idle.reset();
                 } else {
                     // bounded idle: give up after the wait limit like every other wait
-                    const uint64_t now = ptx::globaltimer();
-                    if (t_idle == 0) t_idle = now;
-                    else if (now - t_idle > ptx::kWaitTimeoutNs || *abort_flag) {
+                    if (idle.expired(ptx::kWaitTimeoutNs) || *abort_flag) {
                         if (!*abort_flag) {
                             *abort_flag = 1;
                             report(d_status, DSA_ERR_TIMEOUT);

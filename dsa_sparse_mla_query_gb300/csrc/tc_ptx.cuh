@@ -4,7 +4,9 @@
 // Every wait is bounded by wall time (%globaltimer).  A wait that gives up
 // raises the CTA's abort flag and the device status DSA_ERR_TIMEOUT; the
 // other roles of the CTA see the flag and leave their loops, so no CTA can
-// spin forever.
+// spin forever.  The time a wait has spent is the sum of the steps between
+// successive timer reads, each step counted as at most kMaxStepNs, so that a
+// jump of the timer (or a read that goes backwards) cannot end a healthy wait.
 #pragma once
 
 #include <cuda.h>
@@ -16,12 +18,30 @@ namespace ptx {
 
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s
 constexpr uint64_t kDrainTimeoutNs = 100000000ull;  // 0.1 s (after an abort)
+constexpr uint64_t kMaxStepNs = 1000000ull;         // 1 ms: the most one step between reads counts
 
 __device__ __forceinline__ uint64_t globaltimer() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+
+// Time spent waiting, as a sum of clamped steps between timer reads.
+struct WaitClock {
+    uint64_t prev, spent;
+    __device__ __forceinline__ WaitClock() : prev(globaltimer()), spent(0) {}
+    __device__ __forceinline__ void reset() {
+        prev = globaltimer();
+        spent = 0;
+    }
+    __device__ __forceinline__ bool expired(uint64_t limit) {
+        const uint64_t now = globaltimer();
+        const uint64_t d = now - prev;  // a read that went backwards wraps to a huge step
+        prev = now;
+        spent += d < kMaxStepNs ? d : kMaxStepNs;
+        return spent > limit;
+    }
+};
 
 // ---------------------------------------------------------------------------
 // mbarrier
@@ -76,11 +96,11 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int32_t* d_status) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
+    WaitClock clk;
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, 20000)) return true;
         if (*abort_flag) return false;
-        if (globaltimer() - t0 > kWaitTimeoutNs) {
+        if (clk.expired(kWaitTimeoutNs)) {
             *abort_flag = 1;
             report(d_status, DSA_ERR_TIMEOUT);
             return false;
@@ -90,9 +110,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 
 // Short bounded wait that ignores the abort flag (draining after an abort).
 __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer();
+    WaitClock clk;
     while (!mbar_try_wait_sleep(bar, parity, 20000))
-        if (globaltimer() - t0 > kDrainTimeoutNs) return false;
+        if (clk.expired(kDrainTimeoutNs)) return false;
     return true;
 }
 
