@@ -224,7 +224,9 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
         if (threadIdx.x == 0 && sp == 0) report(d_status, DSA_ERR_BAD_INPUT);
         len = 0;
     }
-    const int per = ((k + splits - 1) / splits + TK - 1) / TK * TK;
+    // the query's live slots [0, len) in equal whole tiles per split (a
+    // compacted selection, len << k, keeps every split busy)
+    const int per = ((len + splits - 1) / splits + TK - 1) / TK * TK;
     const int slot0 = sp * per;
     const int slot1 = min(slot0 + per, len);
     const int ntiles = slot1 > slot0 ? (slot1 - slot0 + TK - 1) / TK : 0;
