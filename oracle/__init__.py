@@ -93,6 +93,10 @@ def _bind(path: str):
     L.oracle_topk_compact.argtypes = [I32, P, I32, I32, I32, I32, P, ctypes.POINTER(I32)]
     L.oracle_topk_compact.restype = ctypes.c_int
     L.oracle_lse_combine.argtypes, L.oracle_lse_combine.restype = [I32, I64, I32, P, P, P, P], ctypes.c_int
+    L.oracle_e2m1_value.argtypes, L.oracle_e2m1_value.restype = [ctypes.c_uint8], D
+    L.oracle_e2m1_encode.argtypes, L.oracle_e2m1_encode.restype = [D], ctypes.c_uint8
+    L.oracle_nvfp4_quantize.argtypes, L.oracle_nvfp4_quantize.restype = [I32, P, D, P, P], ctypes.c_int
+    L.oracle_nvfp4_dequantize.argtypes, L.oracle_nvfp4_dequantize.restype = [I32, P, P, D, P], ctypes.c_int
     return L
 
 
@@ -348,3 +352,33 @@ def lse_combine(o_parts, lse_parts, L=None):
     lse = np.empty(ls.shape[1:], np.float64)
     _check((L or lib()).oracle_lse_combine(R, rows, dim, _ptr(o), _ptr(ls), _ptr(out), _ptr(lse)))
     return out, lse
+
+
+# ---- NVFP4 (4.5-bit cache values)
+def e2m1_value(nibble: int, L=None) -> float:
+    return float((L or lib()).oracle_e2m1_value(nibble & 15))
+
+
+def e2m1_encode(v: float, L=None) -> int:
+    return int((L or lib()).oracle_e2m1_encode(float(v)))
+
+
+def nvfp4_quantize(v, g: float, L=None):
+    """fp64 values [..., n] (n % 16 == 0) -> (codes uint8 [..., n/2], scales uint8 [..., n/16])."""
+    a = np.ascontiguousarray(np.asarray(v, np.float64))
+    n = a.shape[-1]
+    flat = a.reshape(-1)
+    codes = np.empty(flat.size // 2, np.uint8)
+    scales = np.empty(flat.size // 16, np.uint8)
+    _check((L or lib()).oracle_nvfp4_quantize(flat.size, _ptr(flat), float(g), _ptr(codes), _ptr(scales)))
+    return codes.reshape(a.shape[:-1] + (n // 2,)), scales.reshape(a.shape[:-1] + (n // 16,))
+
+
+def nvfp4_dequantize(codes, scales, g: float, L=None) -> np.ndarray:
+    c = np.ascontiguousarray(np.asarray(codes, np.uint8))
+    s = np.ascontiguousarray(np.asarray(scales, np.uint8))
+    n = c.shape[-1] * 2
+    out = np.empty(c.shape[:-1] + (n,), np.float64)
+    _check((L or lib()).oracle_nvfp4_dequantize(c.size * 2, _ptr(c.reshape(-1)), _ptr(s.reshape(-1)), float(g),
+                                                _ptr(out.reshape(-1))))
+    return out

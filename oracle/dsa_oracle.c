@@ -512,3 +512,58 @@ int oracle_lse_combine(int32_t num_parts, int64_t rows, int32_t dim, const doubl
     }
     return 0;
 }
+
+/* ---- NVFP4 ("vLLM adds NVFP4 serving for MiniMax M3.1 Flash": NVFP4
+ * attention and indexer caches at 4.5 bits per value) ---- */
+
+/* E2M1: exponent field 0 is subnormal (m / 2), otherwise (1 + m / 2) 2^(e - 1). */
+double oracle_e2m1_value(uint8_t nibble) {
+    int sgn = (nibble >> 3) & 1, e = (nibble >> 1) & 3, m = nibble & 1;
+    double v = e == 0 ? m * 0.5 : ldexp(1.0 + m * 0.5, e - 1);
+    return sgn ? -v : v;
+}
+
+/* the magnitude codes 0..7 in increasing order; nearest by distance, a tie
+ * to the code with mantissa bit 0, past 6 the largest */
+uint8_t oracle_e2m1_encode(double v) {
+    if (isnan(v)) return 0;
+    uint8_t sgn = signbit(v) ? 8 : 0;
+    double a = fabs(v);
+    uint8_t best = 0;
+    double best_d = INFINITY;
+    for (uint8_t c = 0; c < 8; ++c) {
+        double d = fabs(a - oracle_e2m1_value(c));
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(sgn | best);
+}
+
+int oracle_nvfp4_quantize(int32_t n, const double* v, double g, uint8_t* codes, uint8_t* scales) {
+    if (n < 0 || n % 16 || !(g > 0.0) || (n && (!v || !codes || !scales))) return ORACLE_ERR_ARG;
+    for (int32_t b = 0; b < n / 16; ++b) {
+        const double* x = v + 16 * b;
+        double amax = 0.0;
+        for (int i = 0; i < 16; ++i) amax = fmax(amax, fabs(x[i]));
+        scales[b] = oracle_e4m3_encode(amax / (6.0 * g));
+        double s = oracle_e4m3_value(scales[b]);
+        for (int i = 0; i < 16; i += 2) {
+            uint8_t lo = s > 0.0 ? oracle_e2m1_encode(x[i] / (g * s)) : 0;
+            uint8_t hi = s > 0.0 ? oracle_e2m1_encode(x[i + 1] / (g * s)) : 0;
+            codes[8 * b + i / 2] = (uint8_t)(lo | (hi << 4));
+        }
+    }
+    return 0;
+}
+
+int oracle_nvfp4_dequantize(int32_t n, const uint8_t* codes, const uint8_t* scales, double g, double* out) {
+    if (n < 0 || n % 16 || (n && (!codes || !scales || !out))) return ORACLE_ERR_ARG;
+    for (int32_t i = 0; i < n; ++i) {
+        uint8_t byte = codes[i / 2];
+        uint8_t nib = (i % 2) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+        out[i] = g * oracle_e4m3_value(scales[i / 16]) * oracle_e2m1_value(nib);
+    }
+    return 0;
+}

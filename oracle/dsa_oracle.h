@@ -159,6 +159,24 @@ int oracle_topk_compact(int32_t k, const int32_t* idx, int32_t len, int32_t rank
 int oracle_lse_combine(int32_t num_parts, int64_t rows, int32_t dim, const double* o_parts,
                        const double* lse_parts, double* out, double* lse);
 
+/* ---- NVFP4: 4.5-bit cache values ("vLLM adds NVFP4 serving for MiniMax
+ * M3.1 Flash": NVFP4 attention and indexer caches, 4-bit values costing 4.5
+ * bits with their block scales) ----
+ * Elements are E2M1 (sign, 2 exponent bits with bias 1, 1 mantissa bit:
+ * magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), two per byte with the even element
+ * in the low nibble; every 16 consecutive elements share one E4M3 block scale
+ * (4 + 8/16 = 4.5 bits per value) and a tensor shares one fp32 scale g:
+ * value = g * e4m3(block scale) * e2m1(code). */
+double oracle_e2m1_value(uint8_t nibble);
+/* nearest E2M1 (ties to the even mantissa), saturating at +-6; the sign of
+ * v (also of a zero) in the sign bit; NaN -> +0 */
+uint8_t oracle_e2m1_encode(double v);
+/* n values (n % 16 == 0), tensor scale g > 0: block b's scale s_b =
+ * e4m3_encode(max |v| over the block / (6 g)); its codes e2m1_encode(v /
+ * (g * e4m3(s_b))), all +0 when the scale is 0.  codes [n/2], scales [n/16]. */
+int oracle_nvfp4_quantize(int32_t n, const double* v, double g, uint8_t* codes, uint8_t* scales);
+int oracle_nvfp4_dequantize(int32_t n, const uint8_t* codes, const uint8_t* scales, double g, double* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -821,4 +821,93 @@ def pin_lse_combine_closed_forms(L):
     assert np.all(out == 0) and np.all(lse == -np.inf)
 
 
+# ---------------------------------------------------------------------------
+# NVFP4 ("vLLM adds NVFP4 serving for MiniMax M3.1 Flash": 4.5-bit cache values)
+# The E2M1 element values, written out: magnitudes of codes 0..7.
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def _nearest_e2m1(x):
+    """Brute force on the table: nearest magnitude, a tie to the even code."""
+    a = abs(x)
+    d = [abs(a - t) for t in E2M1_TABLE]
+    best = [i for i in range(8) if d[i] == min(d)]
+    c = best[0] if len(best) == 1 else next(i for i in best if i % 2 == 0)
+    return (8 if math.copysign(1.0, x) < 0 else 0) | c
+
+
+def pin_e2m1_table(L):
+    """The 16 E2M1 codes decode to the format's table, the sign bit negating."""
+    for c in range(16):
+        v = oracle.e2m1_value(c, L=L)
+        want = E2M1_TABLE[c & 7] * (-1.0 if c & 8 else 1.0)
+        assert v == want and math.copysign(1.0, v) == math.copysign(1.0, want), (c, v)
+
+
+def pin_e2m1_encode_nearest(L):
+    """Encoding is the nearest table value (ties to the even code, 6 past the
+    top, sign kept, zeros included) on a grid through every midpoint, and
+    decoding then encoding returns every code."""
+    grid = [i / 16.0 for i in range(-130, 131)] + [6.5, 7.0, 100.0, -9.0, 1e-300, -1e-300, 0.25, 0.75, 1.25,
+                                                      1.75, 2.5, 3.5, 5.0, -5.0]
+    for x in grid:
+        assert oracle.e2m1_encode(x, L=L) == _nearest_e2m1(x), x
+    for c in range(16):
+        assert oracle.e2m1_encode(oracle.e2m1_value(c, L=L), L=L) == c
+
+
+def pin_nvfp4_hand_block(L):
+    """A block whose values sit on the grid: scale and codes by hand.  Max
+    |v| = 12 with g = 1 gives the E4M3 block scale 2.0 (code 0x40), so each
+    v / 2 is an exact E2M1 value; the even element goes to the low nibble
+    (1.0 and -6.0 -> 0x2 | 0xF << 4)."""
+    v = np.array([2.0, -12.0, 1.0, 3.0, 0.0, 8.0, -4.0, 6.0, 0.5 * 2, 1.5 * 2, -0.0, 2.0, 4.0, -1.0, 12.0, 0.0])
+    codes, scales = oracle.nvfp4_quantize(v, 1.0, L=L)
+    assert scales.tolist() == [0x40]
+    assert codes[0] == 0xF2  # 2/2 = 1.0 -> 0x2 (low), -12/2 = -6.0 -> 0xF (high)
+    assert codes[1] == 0x31  # 1/2 = 0.5 -> 0x1 (low), 3/2 = 1.5 -> 0x3 (high)
+    back = oracle.nvfp4_dequantize(codes, scales, 1.0, L=L)
+    assert np.array_equal(back, v)
+
+
+def pin_nvfp4_quantize_properties(L):
+    """Random blocks and tensor scales (powers of two and not): each block
+    scale is the pinned E4M3 encoding of max|v| / (6 g); each code is the
+    table's nearest value of v / (g s); dequantisation is g * s * value; a
+    block of zeros has scale 0 and codes 0."""
+    rng = np.random.default_rng(47)
+    for g in (1.0, 0.25, 3.0e-3, 17.0):
+        v = rng.standard_normal((5, 64)) * rng.choice([1e-3, 1.0, 50.0], size=(5, 1))
+        v[2, 16:32] = 0.0
+        codes, scales = oracle.nvfp4_quantize(v, g, L=L)
+        back = oracle.nvfp4_dequantize(codes, scales, g, L=L)
+        for r in range(5):
+            for b in range(4):
+                blk = v[r, 16 * b:16 * b + 16]
+                sc = int(scales[r, b])
+                assert sc == oracle.e4m3_encode(np.max(np.abs(blk)) / (6.0 * g), L=L)
+                s_val = oracle.e4m3_value(sc, L=L)
+                for i in range(16):
+                    byte = int(codes[r, 8 * b + i // 2])
+                    nib = (byte >> 4) if i % 2 else (byte & 15)
+                    want = _nearest_e2m1(blk[i] / (g * s_val)) if s_val > 0 else 0
+                    assert nib == want, (g, r, b, i)
+                    assert back[r, 16 * b + i] == g * s_val * E2M1_TABLE[nib & 7] * (-1 if nib & 8 else 1)
+        assert np.all(scales[2, 1] == 0) and np.all(codes[2, 8:16] == 0)
+
+
+def pin_nvfp4_bits_per_value(L):
+    """4-bit values plus their block scales cost 4.5 bits per value, the
+    pages' figure, and 4.5 / 8 is the pages' FP8 -> NVFP4 byte ratio
+    (tests/golden/nvfp4.json)."""
+    with open(os.path.join(GOLDEN, "nvfp4.json")) as f:
+        g = json.load(f)
+    n = 4096
+    codes, scales = oracle.nvfp4_quantize(np.ones(n), 1.0, L=L)
+    bits = 8.0 * (codes.size + scales.size) / n
+    assert bits == g["bits_per_value"]
+    assert g["kv_bytes_per_token_fp8"] * bits / 8.0 == g["kv_bytes_per_token_nvfp4"]
+    assert 100.0 * (1.0 - bits / 8.0) == g["reduction_percent"]
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -109,6 +109,20 @@ MUTANTS = [
      "int32_t m = n < k ? (int32_t)n : k - 1;\n    for (int32_t i = 0; i < m; ++i) ids[i]"),
     ("compact_ignores_owner", "if (t >= 0 && oracle_dcp_owner(t, world, interleave) == rank)", "if (t >= 0)"),
     ("lse_combine_max_not_logsumexp", "double L = m + log(sum);", "double L = m;"),
+    # NVFP4
+    ("e2m1_subnormal", "double v = e == 0 ? m * 0.5 : ldexp(1.0 + m * 0.5, e - 1);",
+     "double v = e == 0 ? m * 1.0 : ldexp(1.0 + m * 0.5, e - 1);"),
+    ("e2m1_bias", "double v = e == 0 ? m * 0.5 : ldexp(1.0 + m * 0.5, e - 1);",
+     "double v = e == 0 ? m * 0.5 : ldexp(1.0 + m * 0.5, e - 2);"),
+    ("e2m1_ties_to_odd", "if (d < best_d || (d == best_d && (c & 1) == 0)) {",
+     "if (d < best_d || (d == best_d && (c & 1) == 1)) {"),
+    ("e2m1_negative_zero_unsigned", "uint8_t sgn = signbit(v) ? 8 : 0;", "uint8_t sgn = v < 0.0 ? 8 : 0;"),
+    ("nvfp4_scale_over_4", "scales[b] = oracle_e4m3_encode(amax / (6.0 * g));",
+     "scales[b] = oracle_e4m3_encode(amax / (4.0 * g));"),
+    ("nvfp4_nibble_order", "codes[8 * b + i / 2] = (uint8_t)(lo | (hi << 4));",
+     "codes[8 * b + i / 2] = (uint8_t)(hi | (lo << 4));"),
+    ("nvfp4_tensor_scale_dropped", "out[i] = g * oracle_e4m3_value(scales[i / 16]) * oracle_e2m1_value(nib);",
+     "out[i] = oracle_e4m3_value(scales[i / 16]) * oracle_e2m1_value(nib);"),
     ("lse_combine_weights_unnormalised",
      "double wgt = exp(lse_parts[(int64_t)r * rows + i] - L);", "double wgt = exp(lse_parts[(int64_t)r * rows + i] - m);"),
 ]
