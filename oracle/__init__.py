@@ -97,6 +97,8 @@ def _bind(path: str):
     L.oracle_e2m1_encode.argtypes, L.oracle_e2m1_encode.restype = [D], ctypes.c_uint8
     L.oracle_nvfp4_quantize.argtypes, L.oracle_nvfp4_quantize.restype = [I32, P, D, P, P], ctypes.c_int
     L.oracle_nvfp4_dequantize.argtypes, L.oracle_nvfp4_dequantize.restype = [I32, P, P, D, P], ctypes.c_int
+    L.oracle_block_topk.argtypes = [P, I32, I32, I32, P, ctypes.POINTER(I32)]
+    L.oracle_block_topk.restype = ctypes.c_int
     return L
 
 
@@ -382,3 +384,13 @@ def nvfp4_dequantize(codes, scales, g: float, L=None) -> np.ndarray:
     _check((L or lib()).oracle_nvfp4_dequantize(c.size * 2, _ptr(c.reshape(-1)), _ptr(s.reshape(-1)), float(g),
                                                 _ptr(out.reshape(-1))))
     return out
+
+
+# ---- block-sparse selection (MiniMax Sparse Attention)
+def block_topk(scores, block: int = 128, nsel: int = 16, L=None):
+    """Causal scores [n] (the query at n-1) -> (idx int32 [nsel*block], len)."""
+    sc = np.ascontiguousarray(np.asarray(scores, np.float64))
+    idx = np.empty(nsel * block, np.int32)
+    m = ctypes.c_int32()
+    _check((L or lib()).oracle_block_topk(_ptr(sc), sc.shape[0], block, nsel, _ptr(idx), ctypes.byref(m)))
+    return idx, int(m.value)

@@ -567,3 +567,42 @@ int oracle_nvfp4_dequantize(int32_t n, const uint8_t* codes, const uint8_t* scal
     }
     return 0;
 }
+
+/* ---- block-sparse selection ("vLLM adds NVFP4 serving for MiniMax M3.1
+ * Flash", MiniMax Sparse Attention) ---- */
+int oracle_block_topk(const double* scores, int32_t n, int32_t block, int32_t nsel, int32_t* idx, int32_t* len) {
+    if (n < 1 || block < 1 || nsel < 1 || !scores || !idx || !len) return ORACLE_ERR_ARG;
+    const int32_t nb = (n + block - 1) / block; /* blocks holding causal keys */
+    const int32_t last = nb - 1;                /* the query's own block */
+    scored* v = (scored*)malloc(sizeof(scored) * (size_t)nb);
+    char* chosen = (char*)calloc((size_t)nb, 1);
+    if (!v || !chosen) {
+        free(v);
+        free(chosen);
+        return ORACLE_ERR_NOMEM;
+    }
+    for (int32_t b = 0; b < nb; ++b) {
+        double m = -INFINITY;
+        for (int32_t j = b * block; j < n && j < (b + 1) * block; ++j) m = fmax(m, scores[j]);
+        v[b].s = m;
+        v[b].j = b;
+    }
+    chosen[last] = 1;
+    /* the other blocks by score descending, block ascending */
+    qsort(v, (size_t)nb, sizeof(scored), by_score);
+    int32_t taken = 1;
+    for (int32_t i = 0; i < nb && taken < nsel; ++i) {
+        if (v[i].j == last) continue;
+        chosen[v[i].j] = 1;
+        ++taken;
+    }
+    int32_t m = 0;
+    for (int32_t b = 0; b < nb; ++b)
+        if (chosen[b])
+            for (int32_t j = b * block; j < n && j < (b + 1) * block; ++j) idx[m++] = j;
+    for (int32_t i = m; i < nsel * block; ++i) idx[i] = -1;
+    *len = m;
+    free(v);
+    free(chosen);
+    return 0;
+}

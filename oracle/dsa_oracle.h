@@ -177,6 +177,18 @@ uint8_t oracle_e2m1_encode(double v);
 int oracle_nvfp4_quantize(int32_t n, const double* v, double g, uint8_t* codes, uint8_t* scales);
 int oracle_nvfp4_dequantize(int32_t n, const uint8_t* codes, const uint8_t* scales, double g, double* out);
 
+/* ---- block-sparse selection ("vLLM adds NVFP4 serving for MiniMax M3.1
+ * Flash", MiniMax Sparse Attention: 128-token KV blocks, 16 blocks selected by
+ * scanning the index keys with the most recent block always kept, exact
+ * attention over the selected blocks' 2,048 keys) ----
+ * Over the n causal scores of a query (keys 0..n-1, the query at n-1): block
+ * b holds keys [b*block, (b+1)*block) and scores the maximum of its keys'
+ * scores; the query's own block (the most recent) is always selected, then the
+ * nsel-1 other blocks with the largest scores (ties to the smaller block).
+ * idx[0..len) are the selected blocks' causal keys in ascending order, the
+ * rest of idx[0..nsel*block) -1. */
+int oracle_block_topk(const double* scores, int32_t n, int32_t block, int32_t nsel, int32_t* idx, int32_t* len);
+
 #ifdef __cplusplus
 }
 #endif

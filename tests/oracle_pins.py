@@ -910,4 +910,51 @@ def pin_nvfp4_bits_per_value(L):
     assert 100.0 * (1.0 - bits / 8.0) == g["reduction_percent"]
 
 
+# ---------------------------------------------------------------------------
+# block-sparse selection (MiniMax Sparse Attention)
+def pin_block_topk_closed_forms(L):
+    """Scores rising with position select the 16 most recent blocks; falling
+    scores select blocks 0..14 and the query's own block; a context of at most
+    16 blocks is selected whole."""
+    n = 5000  # 40 blocks, the last holding keys 4992..4999
+    idx, m = oracle.block_topk(np.arange(n, dtype=np.float64), L=L)
+    assert m == 15 * 128 + 8 and np.array_equal(idx[:m], np.arange(24 * 128, n)) and np.all(idx[m:] == -1)
+    idx, m = oracle.block_topk(np.arange(n, dtype=np.float64)[::-1].copy(), L=L)
+    assert np.array_equal(idx[:m], np.concatenate([np.arange(15 * 128), np.arange(4992, n)]))
+    for n in (1, 127, 128, 129, 2047, 2048):
+        idx, m = oracle.block_topk(np.random.default_rng(n).standard_normal(n), L=L)
+        assert m == n and np.array_equal(idx[:m], np.arange(n))
+
+
+def pin_block_topk_library(L):
+    """Against numpy: block maxima (np.maximum.reduceat), blocks ordered by
+    (max descending, block ascending) with numpy's lexsort, the query's block
+    forced; many ties, ragged last blocks, other block sizes and counts."""
+    rng = np.random.default_rng(48)
+    for n, block, nsel in ((9000, 128, 16), (2049, 128, 16), (3000, 64, 5), (777, 7, 16), (40000, 128, 16),
+                           (5, 2, 1), (300, 128, 2)):
+        s = rng.integers(-8, 9, n).astype(np.float64) * 0.5
+        idx, m = oracle.block_topk(s, block, nsel, L=L)
+        starts = np.arange(0, n, block)
+        bmax = np.maximum.reduceat(s, starts)
+        nb, last = len(starts), len(starts) - 1
+        order = [b for b in np.lexsort((np.arange(nb), -bmax)) if b != last][:nsel - 1]
+        chosen = sorted(order + [last])
+        want = np.concatenate([np.arange(b * block, min(n, (b + 1) * block)) for b in chosen])
+        assert m == len(want) and np.array_equal(idx[:m], want), (n, block, nsel)
+        assert np.all(idx[m:] == -1)
+
+
+def pin_block_topk_block_one_is_topk(L):
+    """With blocks of one key, nsel = k, and the query's own key scoring
+    highest, the selection is the pinned top-k's (as a sorted set)."""
+    rng = np.random.default_rng(49)
+    for n, k in ((500, 64), (3000, 2048), (40, 64)):
+        s = np.round(rng.standard_normal(n), 1)
+        s[-1] = 100.0
+        idx, m = oracle.block_topk(s, 1, k, L=L)
+        ti, tm = oracle.topk(s, k, L=L)
+        assert m == tm and np.array_equal(idx[:m], np.sort(ti[:tm]))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

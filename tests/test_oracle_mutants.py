@@ -123,6 +123,13 @@ MUTANTS = [
      "codes[8 * b + i / 2] = (uint8_t)(hi | (lo << 4));"),
     ("nvfp4_tensor_scale_dropped", "out[i] = g * oracle_e4m3_value(scales[i / 16]) * oracle_e2m1_value(nib);",
      "out[i] = oracle_e4m3_value(scales[i / 16]) * oracle_e2m1_value(nib);"),
+    # block-sparse selection
+    ("block_score_sum", "for (int32_t j = b * block; j < n && j < (b + 1) * block; ++j) m = fmax(m, scores[j]);",
+     "for (int32_t j = b * block; j < n && j < (b + 1) * block; ++j) m = (m == -INFINITY ? 0.0 : m) + scores[j];"),
+    ("block_recent_not_forced", "    chosen[last] = 1;\n", "\n"),
+    ("block_recent_counted_twice", "if (v[i].j == last) continue;", ";"),
+    ("block_score_spills_over", "for (int32_t j = b * block; j < n && j < (b + 1) * block; ++j) m = fmax(m, scores[j]);",
+     "for (int32_t j = b * block; j < n && j <= (b + 1) * block; ++j) m = fmax(m, scores[j]);"),
     ("lse_combine_weights_unnormalised",
      "double wgt = exp(lse_parts[(int64_t)r * rows + i] - L);", "double wgt = exp(lse_parts[(int64_t)r * rows + i] - m);"),
 ]
