@@ -64,6 +64,26 @@ def dist_env():
     return ws, rank, local
 
 
+def barrier(ws: int):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    """The largest of every rank's x (the slowest rank's time)."""
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, ws: int, ms_per_step: float) -> float:
+    """Units all ranks processed per second, each rank a full copy of the
+    workload (weak scaling), timed by the slowest rank."""
+    return ws * units_per_rank / (ms_per_step / 1000.0)
+
+
 # ---------------------------------------------------------------------------
 # algorithmic bytes per launch and per step: each byte a kernel must move at least once
 def index_row_bytes(wl):
@@ -303,10 +323,6 @@ def run_ours(args, wl, ws, rank, local):
     if step.device_status() != 0:
         raise RuntimeError(f"device status {step.device_status()} after warm-up")
 
-    def barrier():
-        if ws > 1:
-            torch.distributed.barrier()
-
     sampler = ClockSampler(local)
     t_soak = time.time()
     t_end_soak = t_soak + args.soak_s
@@ -314,7 +330,7 @@ def run_ours(args, wl, ws, rank, local):
         for _ in range(20):
             step.run(stream)
         torch.cuda.synchronize(dev)
-    barrier()
+    barrier(ws)
     torch.cuda.synchronize(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
@@ -322,7 +338,7 @@ def run_ours(args, wl, ws, rank, local):
         step.run(stream)
     end.record(stream)
     torch.cuda.synchronize(dev)
-    barrier()
+    barrier(ws)
     ms = start.elapsed_time(end)
     # Per-stage times: a second pass of K steps with events between the stages.
     # An event between two kernels costs their programmatic overlap, so the
@@ -331,15 +347,12 @@ def run_ours(args, wl, ws, rank, local):
     for i in range(K):
         step.run(stream, events=ev[i], events2=ev2[i])
     torch.cuda.synchronize(dev)
-    barrier()
+    barrier(ws)
     t_done = time.time()
     clocks = sampler.stop(t_soak, t_done)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, ws, dev)
     ms_step = ms / K
-    value = ws * wl.num_queries / (ms_step / 1000.0)
+    value = whole_job_rate(wl.num_queries, ws, ms_step)
 
     stage = lambda i, a, b: ev[i][a].elapsed_time(ev[i][b])  # noqa: E731
     idx_ms = statistics.mean(stage(i, 0, 1) for i in range(K))
@@ -367,7 +380,7 @@ def run_ours(args, wl, ws, rank, local):
     h2d = sum(v.numel() * v.element_size() for v in host_in.values()) + host_pos.numel() * 4
     d2h = sum(o.numel() * o.element_size() for o in host_out)
     Ke = max(1, K)
-    barrier()
+    barrier(ws)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -380,12 +393,9 @@ def run_ours(args, wl, ws, rank, local):
             h.copy_(o, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    barrier()
+    barrier(ws)
     e2e_ms = e0.elapsed_time(e1) / Ke
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, ws, dev)
     if step.device_status() != 0:
         raise RuntimeError(f"device status {step.device_status()}")
 
@@ -429,7 +439,7 @@ def run_ours(args, wl, ws, rank, local):
                       "stage_ms": {"indexer": idx_ms, "topk": topk_ms, "mla": mla_ms, "mla_shared_layer": mla2_ms},
                       "stage_timing": "second pass of the same K steps with CUDA events between the stages",
                       "keys_scanned_per_s": ws * sum(lay.ctx_len) / (ms_step / 1000.0)},
-            "e2e": {"value": ws * wl.num_queries / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "e2e": {"value": whole_job_rate(wl.num_queries, ws, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": K * step.launches_per_step(),  # kernels of the timed pass
             "clocks": clocks,
@@ -482,13 +492,15 @@ def run_dcp(args, wl, ws, rank, local):
             sh.run(stream)
         torch.cuda.synchronize(dev)
     phase_ok("the untimed load")
+    barrier(ws)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for _ in range(K):
         sh.run(stream)
     end.record(stream)
     torch.cuda.synchronize(dev)
-    ms_step = start.elapsed_time(end) / K
+    barrier(ws)
+    ms_step = max_over_ranks(start.elapsed_time(end) / K, ws, dev)
     phase_ok("the timed steps")
     # stages: a second pass with events between them
     marks = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
@@ -530,7 +542,7 @@ def run_dcp(args, wl, ws, rank, local):
             h.copy_(o, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / K
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, ws, dev)
     phase_ok("the end-to-end steps")
     ab = algorithmic_bytes(wl, lay)
     peak, peak_kind = measured_peaks()
@@ -542,7 +554,7 @@ def run_dcp(args, wl, ws, rank, local):
     launches = sum(per_rank) + 1 + (2 if sh.shared else 1)
     if rank == 0:
         print(json.dumps({
-            "metric": METRIC, "value": ws * wl.num_queries / (ms_step / 1000.0), "unit": UNIT, "n_gpus": ws,
+            "metric": METRIC, "value": whole_job_rate(wl.num_queries, ws, ms_step), "unit": UNIT, "n_gpus": ws,
             "steps": K, "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if not wl.index_fp8 else "e4m3/bf16", "data": "synthetic",
             "config": {"workload": wl.describe(), "queries": wl.num_queries,
@@ -554,7 +566,7 @@ def run_dcp(args, wl, ws, rank, local):
                          "algorithmic_bytes_per_launch": ab["indexer"], "ms_per_launch": idx_ms,
                          "peak_kind": f"{peak_kind} HBM copy"},
             "stages_ms": stages,
-            "e2e": {"value": ws * wl.num_queries / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "e2e": {"value": whole_job_rate(wl.num_queries, ws, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": K * launches, "clocks": clocks, "cpu_baseline": cpu}), flush=True)
 
@@ -653,14 +665,17 @@ def run_insert(args, ws, rank, local):
         for _ in range(20):
             step()
         torch.cuda.synchronize(dev)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(K):
         step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    barrier(ws)
     t_done = time.time()
-    ms = e0.elapsed_time(e1) / K
+    ms = max_over_ranks(e0.elapsed_time(e1) / K, ws, dev)
     clocks = sampler.stop(t_soak, t_done)
     # each kernel alone, events on its stream around each launch
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
@@ -686,14 +701,16 @@ def run_insert(args, ws, rank, local):
         st_h.copy_(st, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / K
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, ws, dev)
     if int(st.item()) != 0:
         raise RuntimeError(f"device status {int(st.item())}")
     peak, peak_kind = measured_peaks()
     lat_bytes = n * INSERT_LATENT_BYTES
     achieved = lat_bytes / (lat_ms / 1000.0) / 1e9
     step_gbs = n * INSERT_BYTES_PER_TOKEN / (ms / 1000.0) / 1e9
-    print(json.dumps({"metric": metric, "value": n / (ms / 1000.0), "unit": unit, "n_gpus": ws, "steps": K,
+    if rank != 0:
+        return
+    print(json.dumps({"metric": metric, "value": whole_job_rate(n, ws, ms), "unit": unit, "n_gpus": ws, "steps": K,
                       "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                       "vs_baseline": None, "dtype": "e4m3/bf16", "data": "synthetic", "config": cfg,
                       "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -702,7 +719,7 @@ def run_insert(args, ws, rank, local):
                       "stages_ms": {"index_k_insert": key_ms, "latent_insert": lat_ms},
                       "step_hbm": {"achieved": step_gbs, "frac": step_gbs / peak,
                                    "bytes": n * INSERT_BYTES_PER_TOKEN},
-                      "e2e": {"value": n / (e2e_ms / 1000.0), "unit": unit, "h2d_bytes_per_step": h2d,
+                      "e2e": {"value": whole_job_rate(n, ws, e2e_ms), "unit": unit, "h2d_bytes_per_step": h2d,
                               "d2h_bytes_per_step": 4},
                       "gpu_launches": 2 * K, "clocks": clocks, "cpu_baseline": cpu}))
 
@@ -710,23 +727,26 @@ def run_insert(args, ws, rank, local):
 def main():
     args = parse()
     ws, rank, local = dist_env()
-    if args.workload == "insert":
-        if ws > 1 and rank != 0 and args.impl == "reference":
-            return
-        run_insert(args, ws, rank, local)
-        return
-    wl = I.WORKLOADS[args.workload]
-    if args.seqs:
-        wl = I.scaled(wl, num_seqs=args.seqs)
+    wl = None
+    if args.workload != "insert":
+        wl = I.WORKLOADS[args.workload]
+        if args.seqs:
+            wl = I.scaled(wl, num_seqs=args.seqs)
     if args.impl == "reference":
+        # the oracle on the host cores: rank 0 alone runs and prints
         if ws > 1 and rank != 0:
             return
-        run_reference(args, wl, ws, rank)
+        if wl is None:
+            run_insert(args, ws, rank, local)
+        else:
+            run_reference(args, wl, ws, rank)
         return
     if ws > 1:
         torch.distributed.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
     try:
-        if args.dcp:
+        if wl is None:
+            run_insert(args, ws, rank, local)
+        elif args.dcp:
             run_dcp(args, wl, ws, rank, local)
         else:
             run_ours(args, wl, ws, rank, local)
