@@ -7,7 +7,10 @@
  *   3. absorbed-MLA attention of 64 heads over only the selected latent rows
  *      (sparse_mla_decode),
  * and the three chained on one stream (dsa_decode_layer), including the
- * shared-indexer variant that reuses an earlier layer's selection.
+ * shared-indexer variant that reuses an earlier layer's selection.  Around it:
+ * the cache-write side (new indexer keys and latent rows into their caches,
+ * the attention query's RoPE + SSMax) and one rank's compute steps of decode
+ * context parallelism (top-k candidates, their merge, compaction, LSE combine).
  *
  * Sources (web pages, cited by title and section):
  *   [vLLM-ML4] "Day 0 support for Mistral Large 4" (vLLM blog), Implementation
@@ -19,6 +22,9 @@
  *              latent cache (656-byte fp8_ds_mla rows, 1,152-byte bf16 rows).
  *   [colibri]  "Mistral-Large-4 (c/colibri.c)", What differs from GLM-5.2:
  *              NoPE layers; SSMax; The indexer; RoPE and the rest.
+ *   [vLLM-ML4] Long context: decode and prefill context parallelism (the DCP
+ *              calls); Implementation details, fusions (the indexer K path
+ *              written straight into the FP8 cache; MLA RoPE + SSMax).
  *
  * Conventions for every entry point:
  *   - Pointers are DEVICE memory owned by the caller unless marked "host".  The
