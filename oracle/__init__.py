@@ -22,8 +22,8 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-KEYS_BF16, KEYS_E4M3_ROW = 0, 1
-LATENT_BF16, LATENT_DS_MLA = 0, 2
+KEYS_BF16, KEYS_E4M3_ROW, KEYS_NVFP4 = 0, 1, 2
+LATENT_BF16, LATENT_DS_MLA, LATENT_NVFP4 = 0, 2, 3
 ERRORS = {-1: "bad argument", -2: "query position outside the context", -3: "page or row outside the cache",
           -4: "selected index outside the context", -5: "out of memory"}
 
@@ -99,6 +99,10 @@ def _bind(path: str):
     L.oracle_nvfp4_dequantize.argtypes, L.oracle_nvfp4_dequantize.restype = [I32, P, P, D, P], ctypes.c_int
     L.oracle_block_topk.argtypes = [P, I32, I32, I32, P, ctypes.POINTER(I32)]
     L.oracle_block_topk.restype = ctypes.c_int
+    L.oracle_index_scores_nvfp4.argtypes = [I32, P, P, P, P, P, P, P, P, P, D, ctypes.POINTER(Seqs), P, I64]
+    L.oracle_index_scores_nvfp4.restype = ctypes.c_int
+    L.oracle_sparse_mla_nvfp4.argtypes = [P, P, P, D, ctypes.POINTER(Seqs), I32, P, I32, D, P, P, P]
+    L.oracle_sparse_mla_nvfp4.restype = ctypes.c_int
     return L
 
 
@@ -394,3 +398,36 @@ def block_topk(scores, block: int = 128, nsel: int = 16, L=None):
     m = ctypes.c_int32()
     _check((L or lib()).oracle_block_topk(_ptr(sc), sc.shape[0], block, nsel, _ptr(idx), ctypes.byref(m)))
     return idx, int(m.value)
+
+
+def index_scores_nvfp4(q, w, ssmax_s, ssmax_b, inv_freq, q_seq, q_pos, codes, block_scales, g: float,
+                       layout: Layout, ld=None, L=None) -> np.ndarray:
+    """Scores [nq, ld] over NVFP4 index keys (codes [rows,64], E4M3 scales [rows,8], tensor scale g)."""
+    qq = _np(q, np.uint16)
+    ww = _np(w, np.float32)
+    ss, sb = _np(ssmax_s, np.float32), _np(ssmax_b, np.float32)
+    fr = None if inv_freq is None else _np(inv_freq, np.float32)
+    qs, qp = _np(q_seq, np.int32), _np(q_pos, np.int32)
+    cc, bs = _np(codes, np.uint8), _np(block_scales, np.uint8)
+    nq = qp.shape[0]
+    ld = int(layout.ctx_len.max()) if ld is None else int(ld)
+    out = np.full((nq, ld), -np.inf, np.float64)
+    st = layout.struct()
+    _check((L or lib()).oracle_index_scores_nvfp4(nq, _ptr(qq), _ptr(ww), _ptr(ss), _ptr(sb), _ptr(fr), _ptr(qs),
+                                                  _ptr(qp), _ptr(cc), _ptr(bs), float(g), ctypes.byref(st),
+                                                  _ptr(out), ld))
+    return out
+
+
+def sparse_mla_nvfp4(q, codes, block_scales, g: float, layout: Layout, seq: int, idx, topk_len: int,
+                     sm_scale: float, L=None):
+    """(out fp64 [64,512], lse fp64 [64]) over NVFP4 latent rows (codes [rows,288], scales [rows,36])."""
+    qq = _np(q, np.uint16)
+    cc, bs = _np(codes, np.uint8), _np(block_scales, np.uint8)
+    ii = _np(idx, np.int32)
+    out = np.empty((64, 512), np.float64)
+    lse = np.empty(64, np.float64)
+    st = layout.struct()
+    _check((L or lib()).oracle_sparse_mla_nvfp4(_ptr(qq), _ptr(cc), _ptr(bs), float(g), ctypes.byref(st), seq,
+                                                _ptr(ii), topk_len, sm_scale, _ptr(out), _ptr(lse), None))
+    return out, lse

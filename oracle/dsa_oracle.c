@@ -58,12 +58,14 @@ int oracle_ds_mla_row(const uint8_t* row, double* out) {
 int64_t oracle_latent_row_bytes(int32_t kind) {
     if (kind == ORACLE_LATENT_BF16) return 2 * MD; /* 1,152 */
     if (kind == ORACLE_LATENT_DS_MLA) return MV + 4 * 4 + 2 * (MD - MV); /* 656 */
+    if (kind == ORACLE_LATENT_NVFP4) return MD / 2 + MD / 16;           /* 324: 288 code bytes, 36 scales */
     return -1;
 }
 
 int64_t oracle_index_row_bytes(int32_t kind) {
     if (kind == ORACLE_KEYS_BF16) return 2 * ID;        /* 256 */
     if (kind == ORACLE_KEYS_E4M3_ROW) return ID + 4;    /* 132 */
+    if (kind == ORACLE_KEYS_NVFP4) return ID / 2 + ID / 16; /* 72: 64 code bytes, 8 scales */
     return -1;
 }
 
@@ -83,14 +85,26 @@ static int64_t phys_row(const oracle_seqs* s, int32_t b, int64_t j) {
     return row;
 }
 
-static void decode_key(int32_t kind, const void* keys, const float* key_scale, int64_t row, double* k) {
-    if (kind == ORACLE_KEYS_BF16) {
-        const uint16_t* p = (const uint16_t*)keys + row * ID;
+/* where and how the index keys are stored */
+typedef struct {
+    int32_t kind;
+    const void* keys;            /* bf16 or e4m3 [rows,128]; NVFP4: codes [rows,64] */
+    const float* row_scale;      /* e4m3: [rows] */
+    const uint8_t* block_scale;  /* NVFP4: E4M3 [rows,8] */
+    double global;               /* NVFP4: tensor scale */
+} key_store;
+
+static void decode_key(const key_store* ks, int64_t row, double* k) {
+    if (ks->kind == ORACLE_KEYS_BF16) {
+        const uint16_t* p = (const uint16_t*)ks->keys + row * ID;
         for (int d = 0; d < ID; ++d) k[d] = oracle_bf16_value(p[d]);
-    } else {
-        const uint8_t* p = (const uint8_t*)keys + row * ID;
-        double sc = (double)key_scale[row];
+    } else if (ks->kind == ORACLE_KEYS_E4M3_ROW) {
+        const uint8_t* p = (const uint8_t*)ks->keys + row * ID;
+        double sc = (double)ks->row_scale[row];
         for (int d = 0; d < ID; ++d) k[d] = oracle_e4m3_value(p[d]) * sc;
+    } else {
+        oracle_nvfp4_dequantize(ID, (const uint8_t*)ks->keys + row * (ID / 2), ks->block_scale + row * (ID / 16),
+                                ks->global, k);
     }
 }
 
@@ -108,8 +122,8 @@ static void decode_key(int32_t kind, const void* keys, const float* key_scale, i
  * LeRoPE factor ([vLLM-ML4] NoPE, SSMax and LeRoPE: LeRoPE is folded into the
  * YaRN frequencies).  NoPE layers: no rotation (inv_freq == NULL). */
 static int score_query(const uint16_t* q, const float* w, const float* ss, const float* sb,
-                       const float* inv_freq, int32_t b, int32_t pos, int32_t kind, const void* keys,
-                       const float* key_scale, const oracle_seqs* seqs, double* out) {
+                       const float* inv_freq, int32_t b, int32_t pos, const key_store* ks,
+                       const oracle_seqs* seqs, double* out) {
     double qh[IH][ID];
     double k[ID];
     for (int h = 0; h < IH; ++h) {
@@ -128,7 +142,7 @@ static int score_query(const uint16_t* q, const float* w, const float* ss, const
     for (int64_t j = 0; j <= pos; ++j) {
         int64_t row = phys_row(seqs, b, j);
         if (row < 0) return ORACLE_ERR_PAGE;
-        decode_key(kind, keys, key_scale, row, k);
+        decode_key(ks, row, k);
         double total = 0.0;
         for (int h = 0; h < IH; ++h) {
             double dot = 0.0;
@@ -142,14 +156,11 @@ static int score_query(const uint16_t* q, const float* w, const float* ss, const
     return 0;
 }
 
-int oracle_index_scores(int32_t nq, const uint16_t* q, const float* w, const float* ssmax_s,
-                        const float* ssmax_b, const float* inv_freq, const int32_t* q_seq,
-                        const int32_t* q_pos, int32_t key_kind, const void* keys, const float* key_scale,
-                        const oracle_seqs* seqs, double* scores, int64_t ld) {
-    if (nq < 0 || !q || !w || !ssmax_s || !ssmax_b || !q_seq || !q_pos || !keys || !seqs || !scores)
+static int index_scores(int32_t nq, const uint16_t* q, const float* w, const float* ssmax_s,
+                        const float* ssmax_b, const float* inv_freq, const int32_t* q_seq, const int32_t* q_pos,
+                        const key_store* ks, const oracle_seqs* seqs, double* scores, int64_t ld) {
+    if (nq < 0 || !q || !w || !ssmax_s || !ssmax_b || !q_seq || !q_pos || !ks->keys || !seqs || !scores)
         return ORACLE_ERR_ARG;
-    if (key_kind != ORACLE_KEYS_BF16 && key_kind != ORACLE_KEYS_E4M3_ROW) return ORACLE_ERR_ARG;
-    if (key_kind == ORACLE_KEYS_E4M3_ROW && !key_scale) return ORACLE_ERR_ARG;
     for (int32_t t = 0; t < nq; ++t) {
         int32_t b = q_seq[t], pos = q_pos[t];
         if (b < 0 || b >= seqs->num_seqs) return ORACLE_ERR_ARG;
@@ -159,11 +170,30 @@ int oracle_index_scores(int32_t nq, const uint16_t* q, const float* w, const flo
         int32_t b = q_seq[t], pos = q_pos[t];
         double* row = scores + (int64_t)t * ld;
         int rc = score_query(q + (int64_t)t * IH * ID, w + (int64_t)t * IH, ssmax_s, ssmax_b, inv_freq, b, pos,
-                             key_kind, keys, key_scale, seqs, row);
+                             ks, seqs, row);
         if (rc) return rc;
         for (int64_t j = (int64_t)pos + 1; j < seqs->ctx_len[b]; ++j) row[j] = -INFINITY;
     }
     return 0;
+}
+
+int oracle_index_scores(int32_t nq, const uint16_t* q, const float* w, const float* ssmax_s,
+                        const float* ssmax_b, const float* inv_freq, const int32_t* q_seq,
+                        const int32_t* q_pos, int32_t key_kind, const void* keys, const float* key_scale,
+                        const oracle_seqs* seqs, double* scores, int64_t ld) {
+    if (key_kind != ORACLE_KEYS_BF16 && key_kind != ORACLE_KEYS_E4M3_ROW) return ORACLE_ERR_ARG;
+    if (key_kind == ORACLE_KEYS_E4M3_ROW && !key_scale) return ORACLE_ERR_ARG;
+    key_store ks = {key_kind, keys, key_scale, NULL, 1.0};
+    return index_scores(nq, q, w, ssmax_s, ssmax_b, inv_freq, q_seq, q_pos, &ks, seqs, scores, ld);
+}
+
+int oracle_index_scores_nvfp4(int32_t nq, const uint16_t* q, const float* w, const float* ssmax_s,
+                              const float* ssmax_b, const float* inv_freq, const int32_t* q_seq,
+                              const int32_t* q_pos, const uint8_t* codes, const uint8_t* block_scales, double g,
+                              const oracle_seqs* seqs, double* scores, int64_t ld) {
+    if (!codes || !block_scales || !(g > 0.0)) return ORACLE_ERR_ARG;
+    key_store ks = {ORACLE_KEYS_NVFP4, codes, NULL, block_scales, g};
+    return index_scores(nq, q, w, ssmax_s, ssmax_b, inv_freq, q_seq, q_pos, &ks, seqs, scores, ld);
 }
 
 typedef struct {
@@ -214,11 +244,20 @@ int oracle_topk(const double* scores, int32_t n, int32_t k, int32_t* idx, int32_
  * empty selection gives O = 0 and LSE = -inf ([vLLM-ML4] DCP: a fused kernel
  * neutralises empty rows).  NoPE layers are MLA with zero RoPE dims ([vLLM-ML4]
  * NoPE, SSMax and LeRoPE): their inputs carry zeros in dims 512..575. */
-int oracle_sparse_mla(const uint16_t* q, int32_t latent_kind, const void* latent, const oracle_seqs* seqs,
-                      int32_t seq, const int32_t* idx, int32_t topk_len, double sm_scale, double* out,
-                      double* lse, double* probs) {
+/* where and how the latent rows are stored */
+typedef struct {
+    int32_t kind;
+    const void* latent;          /* bf16 [rows,576] or fp8_ds_mla [rows,656]; NVFP4: codes [rows,288] */
+    const uint8_t* block_scale;  /* NVFP4: E4M3 [rows,36] */
+    double global;               /* NVFP4: tensor scale */
+} latent_store;
+
+static int sparse_mla(const uint16_t* q, const latent_store* ls, const oracle_seqs* seqs, int32_t seq,
+                      const int32_t* idx, int32_t topk_len, double sm_scale, double* out, double* lse,
+                      double* probs) {
+    const int32_t latent_kind = ls->kind;
+    const void* latent = ls->latent;
     if (!q || !latent || !seqs || !out || !lse || topk_len < 0 || (topk_len && !idx)) return ORACLE_ERR_ARG;
-    if (latent_kind != ORACLE_LATENT_BF16 && latent_kind != ORACLE_LATENT_DS_MLA) return ORACLE_ERR_ARG;
     if (seq < 0 || seq >= seqs->num_seqs) return ORACLE_ERR_ARG;
     int64_t row_bytes = oracle_latent_row_bytes(latent_kind);
     double* c = (double*)malloc(sizeof(double) * MD * (size_t)(topk_len ? topk_len : 1));
@@ -245,8 +284,11 @@ int oracle_sparse_mla(const uint16_t* q, int32_t latent_kind, const void* latent
         if (latent_kind == ORACLE_LATENT_BF16) {
             const uint16_t* p = (const uint16_t*)latent + row * MD;
             for (int d = 0; d < MD; ++d) cj[d] = oracle_bf16_value(p[d]);
-        } else {
+        } else if (latent_kind == ORACLE_LATENT_DS_MLA) {
             oracle_ds_mla_row((const uint8_t*)latent + row * row_bytes, cj);
+        } else {
+            oracle_nvfp4_dequantize(MD, (const uint8_t*)latent + row * (MD / 2), ls->block_scale + row * (MD / 16),
+                                    ls->global, cj);
         }
         slot[n++] = i;
     }
@@ -281,6 +323,22 @@ int oracle_sparse_mla(const uint16_t* q, int32_t latent_kind, const void* latent
     free(slot);
     free(s);
     return 0;
+}
+
+int oracle_sparse_mla(const uint16_t* q, int32_t latent_kind, const void* latent, const oracle_seqs* seqs,
+                      int32_t seq, const int32_t* idx, int32_t topk_len, double sm_scale, double* out,
+                      double* lse, double* probs) {
+    if (latent_kind != ORACLE_LATENT_BF16 && latent_kind != ORACLE_LATENT_DS_MLA) return ORACLE_ERR_ARG;
+    latent_store ls = {latent_kind, latent, NULL, 1.0};
+    return sparse_mla(q, &ls, seqs, seq, idx, topk_len, sm_scale, out, lse, probs);
+}
+
+int oracle_sparse_mla_nvfp4(const uint16_t* q, const uint8_t* codes, const uint8_t* block_scales, double g,
+                            const oracle_seqs* seqs, int32_t seq, const int32_t* idx, int32_t topk_len,
+                            double sm_scale, double* out, double* lse, double* probs) {
+    if (!codes || !block_scales || !(g > 0.0)) return ORACLE_ERR_ARG;
+    latent_store ls = {ORACLE_LATENT_NVFP4, codes, block_scales, g};
+    return sparse_mla(q, &ls, seqs, seq, idx, topk_len, sm_scale, out, lse, probs);
 }
 
 /* ---------------------------------------------------------------------------

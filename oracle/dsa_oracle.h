@@ -31,9 +31,11 @@ extern "C" {
 /* key storage kinds */
 #define ORACLE_KEYS_BF16 0        /* [rows,128] bf16 bits                          */
 #define ORACLE_KEYS_E4M3_ROW 1    /* [rows,128] e4m3 codes + [rows] fp32 scale      */
+#define ORACLE_KEYS_NVFP4 2       /* [rows,64] E2M1 pairs + [rows,8] E4M3, x tensor scale (72 B) */
 /* latent storage kinds */
 #define ORACLE_LATENT_BF16 0      /* [rows,576] bf16 bits                           */
 #define ORACLE_LATENT_DS_MLA 2    /* [rows,656] bytes: 512 e4m3, 4 fp32, 64 bf16    */
+#define ORACLE_LATENT_NVFP4 3     /* [rows,288] E2M1 pairs + [rows,36] E4M3, x tensor scale (324 B) */
 
 #define ORACLE_ERR_ARG (-1)
 #define ORACLE_ERR_POS (-2)       /* query position outside [0, ctx_len)            */
@@ -176,6 +178,18 @@ uint8_t oracle_e2m1_encode(double v);
  * (g * e4m3(s_b))), all +0 when the scale is 0.  codes [n/2], scales [n/16]. */
 int oracle_nvfp4_quantize(int32_t n, const double* v, double g, uint8_t* codes, uint8_t* scales);
 int oracle_nvfp4_dequantize(int32_t n, const uint8_t* codes, const uint8_t* scales, double g, double* out);
+
+/* NVFP4 caches: the indexer scores and the attention of oracle_index_scores
+ * and oracle_sparse_mla over keys and latent rows stored as NVFP4 planes: index
+ * keys codes [rows,64] with E4M3 scales [rows,8]; latent rows (all 576 dims)
+ * codes [rows,288] with scales [rows,36]; g the cache's tensor scale. */
+int oracle_index_scores_nvfp4(int32_t nq, const uint16_t* q, const float* w, const float* ssmax_s,
+                              const float* ssmax_b, const float* inv_freq, const int32_t* q_seq,
+                              const int32_t* q_pos, const uint8_t* codes, const uint8_t* block_scales, double g,
+                              const oracle_seqs* seqs, double* scores, int64_t ld);
+int oracle_sparse_mla_nvfp4(const uint16_t* q, const uint8_t* codes, const uint8_t* block_scales, double g,
+                            const oracle_seqs* seqs, int32_t seq, const int32_t* idx, int32_t topk_len,
+                            double sm_scale, double* out, double* lse, double* probs);
 
 /* ---- block-sparse selection ("vLLM adds NVFP4 serving for MiniMax M3.1
  * Flash", MiniMax Sparse Attention: 128-token KV blocks, 16 blocks selected by

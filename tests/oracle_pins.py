@@ -908,6 +908,49 @@ def pin_nvfp4_bits_per_value(L):
     assert bits == g["bits_per_value"]
     assert g["kv_bytes_per_token_fp8"] * bits / 8.0 == g["kv_bytes_per_token_nvfp4"]
     assert 100.0 * (1.0 - bits / 8.0) == g["reduction_percent"]
+    # the NVFP4 cache rows: 128 index dims and 576 latent dims at 4.5 bits
+    assert oracle.index_row_bytes(oracle.KEYS_NVFP4, L=L) * 8 == 128 * g["bits_per_value"]
+    assert oracle.latent_row_bytes(oracle.LATENT_NVFP4, L=L) * 8 == 576 * g["bits_per_value"]
+
+
+def _nvfp4_rows(rng, n, dims):
+    """Random NVFP4 rows: any E2M1 codes, positive finite E4M3 block scales."""
+    codes = rng.integers(0, 256, (n, dims // 2)).astype(np.uint8)
+    scales = rng.integers(0, 0x7F, (n, dims // 16)).astype(np.uint8)  # 0x7F is NaN
+    return codes, scales
+
+
+def pin_nvfp4_keys_equal_their_values(L):
+    """NVFP4 index keys (a power-of-two tensor scale) score like bf16 keys
+    holding their decoded values: E2M1 x E4M3 has at most 6 significant bits,
+    so the values are exact in bf16."""
+    rng = np.random.default_rng(50)
+    n, g = 19, 0.25
+    codes, scales = _nvfp4_rows(rng, n, 128)
+    vals = oracle.nvfp4_dequantize(codes, scales, g, L=L)
+    assert np.array_equal(oracle.e2m1_value(int(codes[3, 5]) >> 4, L=L) * oracle.e4m3_value(int(scales[3, 0]), L=L)
+                          * g, vals[3, 11])
+    c = index_case(n=n, rope=True, seed=13)
+    a = oracle.index_scores_nvfp4(c["q"], c["w"], c["ssmax_s"], c["ssmax_b"], c["inv_freq"], c["q_seq"], c["q_pos"],
+                                  codes, scales, g, contiguous([n], n), L=L)
+    b = scores_of(L, c, keys=bf16_bits(vals))
+    close(a[0], b, 0.0)
+
+
+def pin_mla_nvfp4_equals_values(L):
+    """NVFP4 latent rows (all 576 dims) score and average like bf16 rows
+    holding their decoded values."""
+    rng = np.random.default_rng(51)
+    n, g = 22, 0.5
+    codes, scales = _nvfp4_rows(rng, n, 576)
+    vals = oracle.nvfp4_dequantize(codes, scales, g, L=L)
+    q = bf16_bits(rng.standard_normal((64, 576)) * 1e-3)
+    lay = contiguous([n], n)
+    idx = rng.permutation(n)[:13].astype(np.int32)
+    a, la = oracle.sparse_mla_nvfp4(q, codes, scales, g, lay, 0, idx, 13, 0.1, L=L)
+    b, lb, _ = oracle.sparse_mla(q, bf16_bits(vals), lay, 0, idx, 13, 0.1, L=L)
+    close(a, b, 0.0)
+    close(la, lb, 0.0)
 
 
 # ---------------------------------------------------------------------------

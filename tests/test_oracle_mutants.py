@@ -130,6 +130,11 @@ MUTANTS = [
     ("block_recent_counted_twice", "if (v[i].j == last) continue;", ";"),
     ("block_score_spills_over", "for (int32_t j = b * block; j < n && j < (b + 1) * block; ++j) m = fmax(m, scores[j]);",
      "for (int32_t j = b * block; j < n && j <= (b + 1) * block; ++j) m = fmax(m, scores[j]);"),
+    ("nvfp4_key_row_stride", "oracle_nvfp4_dequantize(ID, (const uint8_t*)ks->keys + row * (ID / 2),",
+     "oracle_nvfp4_dequantize(ID, (const uint8_t*)ks->keys + row * (ID / 4),"),
+    ("nvfp4_latent_scale_row", "ls->block_scale + row * (MD / 16),", "ls->block_scale + row * (MD / 32),"),
+    ("nvfp4_latent_tensor_scale", "                                    ls->global, cj);",
+     "                                    1.0, cj);"),
     ("lse_combine_weights_unnormalised",
      "double wgt = exp(lse_parts[(int64_t)r * rows + i] - L);", "double wgt = exp(lse_parts[(int64_t)r * rows + i] - m);"),
 ]
