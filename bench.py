@@ -204,7 +204,7 @@ def indexer_traffic(wl_name: str):
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("indexer.cu", "dsa_internal.cuh"):
+    for f in ("indexer.cu", "dsa_internal.cuh", "tc_ptx.cuh"):
         with open(os.path.join(ROOT, "dsa_sparse_mla_query_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
