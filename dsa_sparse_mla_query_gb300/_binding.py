@@ -86,6 +86,7 @@ def load(path: str = LIB_PATH):
         L.dsa_topk_merge.argtypes = [P, I32, I32, I32, I32, P, P, P, P]
         L.dsa_topk_compact.argtypes = [P, P, I32, I32, SH, P, P, P, P]
         L.dsa_lse_combine.argtypes = [P, P, I32, I32, P, P, P]
+        L.dsa_block_topk.argtypes = [P, I64, S, I32, I32, I32, P, P, P, P]
         L.dsa_decode_layer_launches.restype = ctypes.c_int32
         for f in ("dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode", "dsa_decode_layer"):
             getattr(L, f).restype = ctypes.c_int
@@ -265,3 +266,11 @@ def dsa_lse_combine(o_parts, lse_parts, num_q: int, out, lse=None, stream=None):
     oa, la = _ptr_array(o_parts), _ptr_array(lse_parts)
     _check(load().dsa_lse_combine(ctypes.cast(oa, ctypes.c_void_p), ctypes.cast(la, ctypes.c_void_p), len(o_parts),
                                   num_q, _p(out), _p(lse), _stream(stream)))
+
+
+# ---- block-sparse selection (include/dsa.h)
+def dsa_block_topk(scores, ld: int, seqs: Seqs, num_q: int, block: int, nsel: int, idx, topk_len, d_status=None,
+                   stream=None):
+    sc = seqs.c()
+    _check(load().dsa_block_topk(_p(scores), ld, ctypes.byref(sc), num_q, block, nsel, _p(idx), _p(topk_len),
+                                 _p(d_status), _stream(stream)))

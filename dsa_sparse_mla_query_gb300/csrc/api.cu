@@ -163,6 +163,9 @@ cudaError_t launch_topk_compact(const int32_t* idx, const int32_t* topk_len, int
                                 cudaStream_t stream);
 cudaError_t launch_lse_combine(const void* const* o_parts, const float* const* lse_parts, int num_parts, int num_q,
                                void* out, float* lse, cudaStream_t stream);
+size_t block_topk_smem(int max_ctx, int block, int nsel);
+cudaError_t launch_block_topk(const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int block, int nsel,
+                              int32_t* idx, int32_t* topk_len, int32_t* d_status, cudaStream_t stream);
 }  // namespace dsa
 
 
@@ -415,6 +418,30 @@ dsa_status dsa_lse_combine(const void* const* o_parts, const float* const* lse_p
     if (st != DSA_OK || num_q == 0) return st;
     return cuda_status(launch_lse_combine(o_parts, lse_parts, num_parts, num_q, out, lse, stream),
                        "dsa_lse_combine launch");
+}
+
+dsa_status dsa_block_topk(const float* scores, int64_t ld, const dsa_seqs* seqs, int32_t num_q, int32_t block,
+                          int32_t nsel, int32_t* idx, int32_t* topk_len, int32_t* d_status, cudaStream_t stream) {
+    Check c;
+    check_seqs(c, seqs, num_q);
+    c.ptr(scores, "scores");
+    c.ptr(idx, "idx", 4);
+    c.ptr(topk_len, "topk_len", 4);
+    c.need(block >= 1 && nsel >= 1 && nsel <= DSA_BLOCK_TOPK_MAX_NSEL, DSA_ERR_UNSUPPORTED,
+           "block %d must be >= 1 and nsel %d in [1, %d]", block, nsel, DSA_BLOCK_TOPK_MAX_NSEL);
+    c.need((int64_t)block * nsel <= DSA_MAX_TOPK, DSA_ERR_UNSUPPORTED, "nsel x block = %lld exceeds %d",
+           (long long)block * nsel, DSA_MAX_TOPK);
+    if (seqs) {
+        c.need(ld >= seqs->max_ctx && ld % 4 == 0, DSA_ERR_INVALID_ARG, "ld %lld must be >= max_ctx and a multiple of 4",
+               (long long)ld);
+        if (block >= 1 && nsel >= 1 && seqs->max_ctx >= 1)
+            c.need(block_topk_smem(seqs->max_ctx, block, nsel) <= DSA_BLOCK_TOPK_MAX_SMEM, DSA_ERR_UNSUPPORTED,
+                   "max_ctx %d / block %d: too many blocks for one CTA's shared memory", seqs->max_ctx, block);
+    }
+    dsa_status st = c.done();
+    if (st != DSA_OK || num_q == 0) return st;
+    return cuda_status(launch_block_topk(scores, ld, *seqs, num_q, block, nsel, idx, topk_len, d_status, stream),
+                       "dsa_block_topk launch");
 }
 
 static void check_mla_args(Check& c, const void* q, const void* latent, dsa_dtype latent_dtype, const int32_t* idx,

@@ -145,6 +145,25 @@ dsa_status dsa_topk(const float* scores, int64_t ld, const dsa_seqs* seqs, int32
                     int32_t* topk_len, void* workspace, size_t workspace_bytes, int32_t* d_status,
                     cudaStream_t stream);
 
+/* Block-sparse selection ("vLLM adds NVFP4 serving for MiniMax M3.1 Flash",
+ * MiniMax Sparse Attention: 128-token KV blocks, 16 selected by scanning the
+ * index keys with the most recent block always kept, exact attention over the
+ * selected blocks' keys).  Over the causal scores j <= pos_t of each query:
+ * block i holds keys [i*block, (i+1)*block) and scores the maximum of its
+ * causal keys' scores; the query's own block is always selected, then the
+ * nsel-1 other blocks with the largest scores (ties to the smaller block).
+ *   scores   fp32 [num_q, ld] (as written by dsa_index_scores)
+ *   idx      int32 [num_q, nsel*block]: the selected blocks' causal keys in
+ *            ascending order, then -1;  topk_len int32 [num_q]
+ * As dsa_topk's output, for sparse_mla_decode with k = nsel*block.
+ * 1 <= nsel <= DSA_BLOCK_TOPK_MAX_NSEL, nsel*block <= 2048, and
+ * ceil(max_ctx / block) blocks must fit one CTA's shared memory (4 bytes each,
+ * DSA_BLOCK_TOPK_MAX_SMEM in all). */
+#define DSA_BLOCK_TOPK_MAX_NSEL 64
+#define DSA_BLOCK_TOPK_MAX_SMEM (200u << 10)
+dsa_status dsa_block_topk(const float* scores, int64_t ld, const dsa_seqs* seqs, int32_t num_q, int32_t block,
+                          int32_t nsel, int32_t* idx, int32_t* topk_len, int32_t* d_status, cudaStream_t stream);
+
 /* Absorbed-MLA attention over selected latent rows ([vLLM-ML4] Model
  * architecture: 64 heads, KV LoRA rank 512, RoPE dim 64; Sparse MLA + DSA
  * indexer; NoPE, SSMax and LeRoPE: NoPE layers are MLA with zero RoPE dims):

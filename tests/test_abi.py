@@ -155,3 +155,24 @@ def test_dcp_calls_with_zero_queries_are_no_ops(lib):
     assert lib.dsa_topk_merge(ctypes.cast(two, P), 2, 64, 0, 2048, None, None, None, None) == 0
     assert lib.dsa_topk_compact(None, None, 0, 2048, ctypes.byref(sh), None, None, None, None) == 0
     assert lib.dsa_lse_combine(ctypes.cast(two, P), ctypes.cast(two, P), 2, 0, None, None, None) == 0
+
+
+def test_block_topk_refuses_what_it_cannot_serve(lib):
+    """Block selection: sizes past the selection width, too many blocks for one
+    CTA, bad counts and pointers are refused on the host (no GPU needed)."""
+    from dsa_sparse_mla_query_gb300 import _binding as B
+    s = _seqs(B)
+
+    def call(block, nsel, seqs=s, scores=0x100, idx=0x200):
+        return lib.dsa_block_topk(scores, 4096, ctypes.byref(seqs), 1, block, nsel, idx, 0x300, None, None)
+
+    assert call(128, 17) == B.DSA_ERR_UNSUPPORTED and "exceeds 2048" in lib.dsa_last_error_string().decode()
+    assert call(0, 16) == B.DSA_ERR_UNSUPPORTED
+    assert call(32, 65) == B.DSA_ERR_UNSUPPORTED
+    big = _seqs(B, max_ctx=1 << 30)
+    rc = lib.dsa_block_topk(0x100, 1 << 30, ctypes.byref(big), 1, 128, 16, 0x200, 0x300, None, None)
+    assert rc == B.DSA_ERR_UNSUPPORTED and "too many blocks" in lib.dsa_last_error_string().decode()
+    assert call(128, 16, scores=None, idx=0x202) == B.DSA_ERR_INVALID_ARG
+    msg = lib.dsa_last_error_string().decode()
+    assert "scores is NULL" in msg and "idx is not 4-byte aligned" in msg
+    assert lib.dsa_block_topk(0x100, 4096, ctypes.byref(s), 0, 128, 16, 0x200, 0x300, None, None) == 0
