@@ -176,3 +176,28 @@ def test_block_topk_refuses_what_it_cannot_serve(lib):
     msg = lib.dsa_last_error_string().decode()
     assert "scores is NULL" in msg and "idx is not 4-byte aligned" in msg
     assert lib.dsa_block_topk(0x100, 4096, ctypes.byref(s), 0, 128, 16, 0x200, 0x300, None, None) == 0
+
+
+def _declared_arities():
+    """Parameter count of every function include/dsa.h declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(([^;{]*?)\)\s*;", text, flags=re.M | re.S):
+        name, params = m.group(1), m.group(2).strip()
+        out[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_argtypes_match_the_header(lib):
+    """Every entry point the binding declares argument types for takes as many
+    arguments as the header says (a drift would shift arguments silently)."""
+    ar = _declared_arities()
+    assert set(ar) == set(declared_functions()), "every declaration parsed"
+    checked = 0
+    for name, n in ar.items():
+        fn = getattr(lib, name)
+        if fn.argtypes is None:
+            continue
+        assert len(fn.argtypes) == n, f"{name}: binding has {len(fn.argtypes)} argument types, header {n}"
+        checked += 1
+    assert checked >= len(ar) - 3  # all but the argument-free ones
