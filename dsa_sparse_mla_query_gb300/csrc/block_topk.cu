@@ -13,6 +13,8 @@
 // coalesced reads of its scores); nsel rounds of a block-wide argmax over
 // packed (order-preserving score code, inverted block id) values pick the
 // blocks; the chosen ids are sorted and their keys written in order.
+#include <mutex>
+
 #include "dsa_internal.cuh"
 
 namespace dsa {
@@ -130,12 +132,14 @@ size_t block_topk_smem(int max_ctx, int block, int nsel) {
 cudaError_t launch_block_topk(const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int block, int nsel,
                               int32_t* idx, int32_t* topk_len, int32_t* d_status, cudaStream_t stream) {
     if (num_q <= 0) return cudaSuccess;
-    const size_t smem = block_topk_smem(s.max_ctx, block, nsel);
-    if (smem > 48 * 1024) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(block_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
+    const size_t smem = block_topk_smem(s.max_ctx, block, nsel);  // <= DSA_BLOCK_TOPK_MAX_SMEM (checked)
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(block_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)DSA_BLOCK_TOPK_MAX_SMEM);
+    });
+    if (attr != cudaSuccess) return attr;
     return launch_pdl(block_topk_kernel, dim3((unsigned)num_q), dim3(kBtThreads), smem, stream, 1, scores, ld, s,
                       block, nsel, idx, topk_len, d_status);
 }

@@ -17,6 +17,7 @@
 #include <cuda_fp8.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "dsa_internal.cuh"
 
@@ -384,12 +385,15 @@ constexpr int kTokensPerCta = kWarpsPerCta;
 // of kKeysPerWarp, latent rows, query heads), one per warp at a time
 unsigned insert_grid(int64_t items) {
     static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
-                                                       cudaSuccess || sms <= 0)
+    static std::once_flag once;
+    std::call_once(once, [] {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+            sms = n;
+        else
             sms = 148;
-    }
+    });
     const int64_t need = (items + kTokensPerCta - 1) / kTokensPerCta;
     return (unsigned)std::min<int64_t>(need, (int64_t)sms * 16);
 }

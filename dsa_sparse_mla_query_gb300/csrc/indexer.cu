@@ -821,12 +821,12 @@ cudaError_t launch_tc(const void* qp, int num_q, const float* wp, const void* k_
                      CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
     auto kern = index_tc_kernel<NQ, KP, FP8>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::once_flag once;  // one per instantiation
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [kern] {
+        attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem);
+    });
+    if (attr != cudaSuccess) return attr;
     const int tiles_per_seq = (s.max_ctx + kTileKeys - 1) / kTileKeys;
     const int chunks = (s.max_q_per_seq + NQ - 1) / NQ;
     const int64_t total = (int64_t)s.num_seqs * chunks * tiles_per_seq;
