@@ -20,8 +20,8 @@ DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA = 0, 1, 2, 3
 DSA_ERR_WORKSPACE, DSA_ERR_TIMEOUT, DSA_ERR_BAD_INPUT = 4, 5, 6
 DSA_BF16, DSA_FP8_E4M3_ROWSCALE, DSA_FP8_DS_MLA = 0, 1, 2
 EXPORTS = ("dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode", "dsa_decode_layer",
-           "dsa_decode_layer_launches", "sparse_mla_decode_noalloc", "dsa_last_error_string", "dsa_status_string",
-           "dsa_version")
+           "dsa_decode_layer_launches", "dsa_decode_layer_launches_for", "sparse_mla_decode_noalloc",
+           "dsa_last_error_string", "dsa_status_string", "dsa_version")
 
 
 class DcpShard(ctypes.Structure):
@@ -47,7 +47,7 @@ class DsaLayerArgsC(ctypes.Structure):
     _fields_ = [("q_idx", ctypes.c_void_p), ("w", ctypes.c_void_p), ("ssmax_s", ctypes.c_void_p),
                 ("ssmax_b", ctypes.c_void_p), ("inv_freq", ctypes.c_void_p), ("k_idx", ctypes.c_void_p),
                 ("k_scale", ctypes.c_void_p), ("k_dtype", ctypes.c_int), ("reuse_idx", ctypes.c_int32),
-                ("k", ctypes.c_int32), ("reserved", ctypes.c_int32), ("idx", ctypes.c_void_p),
+                ("k", ctypes.c_int32), ("select_block", ctypes.c_int32), ("idx", ctypes.c_void_p),
                 ("topk_len", ctypes.c_void_p), ("q_mla", ctypes.c_void_p), ("latent", ctypes.c_void_p),
                 ("latent_dtype", ctypes.c_int), ("sm_scale", ctypes.c_float), ("out", ctypes.c_void_p),
                 ("lse", ctypes.c_void_p), ("events", ctypes.c_void_p)]
@@ -77,6 +77,8 @@ def load(path: str = LIB_PATH):
         L.sparse_mla_decode_noalloc.argtypes = [P, P, ctypes.c_int, S, I32, P, P, I32, ctypes.c_float, P, P, P, P]
         L.sparse_mla_decode_noalloc.restype = ctypes.c_int
         L.dsa_decode_layer_launches.argtypes = [S, I32, I32, I32, ctypes.c_int]
+        L.dsa_decode_layer_launches_for.argtypes = [ctypes.POINTER(DsaLayerArgsC), S, I32]
+        L.dsa_decode_layer_launches_for.restype = ctypes.c_int32
         F = ctypes.c_float
         L.dsa_index_k_insert.argtypes = [P, P, P, F, P, P, P, I32, P, P, ctypes.c_int, I64, P, P]
         L.dsa_latent_insert.argtypes = [P, P, P, P, P, I32, P, ctypes.c_int, I64, P, P]
@@ -186,10 +188,9 @@ def dsa_decode_layer_launches(seqs: Seqs, num_q: int, k: int, reuse_idx: int = 0
     return int(load().dsa_decode_layer_launches(ctypes.byref(sc), num_q, k, reuse_idx, latent_dtype))
 
 
-def dsa_decode_layer(args: dict, seqs: Seqs, num_q: int, workspace, workspace_bytes: int, d_status=None,
-                     stream=None):
-    """``args`` holds the dsa_layer_args fields by name (tensors or None);
-    ``events`` may be a list of 4 recorded torch.cuda.Event objects."""
+def _layer_args(args: dict):
+    """dsa_layer_args from fields by name (tensors or None); returns the struct
+    and what must stay alive while it is used."""
     a = DsaLayerArgsC()
     keep = None
     for name, ctype in DsaLayerArgsC._fields_:
@@ -206,9 +207,24 @@ def dsa_decode_layer(args: dict, seqs: Seqs, num_q: int, workspace, workspace_by
             setattr(a, name, float(v))
         else:
             setattr(a, name, int(v))
+    return a, keep
+
+
+def dsa_decode_layer(args: dict, seqs: Seqs, num_q: int, workspace, workspace_bytes: int, d_status=None,
+                     stream=None):
+    """``args`` holds the dsa_layer_args fields by name (tensors or None);
+    ``events`` may be a list of 4 recorded torch.cuda.Event objects."""
+    a, keep = _layer_args(args)
     sc = seqs.c()
     _check(load().dsa_decode_layer(ctypes.byref(a), ctypes.byref(sc), num_q, _p(workspace), workspace_bytes,
                                    _p(d_status), _stream(stream)))
+    del keep
+
+
+def dsa_decode_layer_launches_for(args: dict, seqs: Seqs, num_q: int) -> int:
+    a, _ = _layer_args({k: v for k, v in args.items() if k != "events"})
+    sc = seqs.c()
+    return int(load().dsa_decode_layer_launches_for(ctypes.byref(a), ctypes.byref(sc), num_q))
 
 
 def version() -> str:

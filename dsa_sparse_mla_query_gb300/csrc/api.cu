@@ -96,12 +96,12 @@ size_t workspace_bytes(const dsa_seqs& s, int num_q, int k, int64_t* scores_ld) 
     const int64_t ld = ((int64_t)s.max_ctx + 3) / 4 * 4;
     if (scores_ld) *scores_ld = ld;
     const int kk = k < 1 ? 1 : (k > DSA_MAX_TOPK ? DSA_MAX_TOPK : k);
-    const int splits = mla_splits(num_q > 0 ? num_q : 1, kk);
+    const int nq = num_q > 0 ? num_q : 1;
     size_t b = 0;
     b += up256((size_t)num_q * kQprepBytes);                         // q'
     b += up256((size_t)num_q * kIH * 4);                             // w'
-    b += up256((size_t)num_q * splits * kMH * kMV * 4);              // partial outputs
-    b += up256((size_t)num_q * splits * kMH * 2 * 4);                // partial (max, sum)
+    b += up256(mla_part_bytes(nq, kk));                              // partial outputs
+    b += up256(mla_ml_bytes(nq, kk));                                // partial (max, sum)
     b += up256((size_t)num_q * ld * 4);                              // scores (fused layer)
     if (topk_long_rows(s.max_ctx)) {                                  // long-row top-k
         b += up256((size_t)num_q * (2048 + 2) * 4);                  // histograms + two counters
@@ -116,16 +116,16 @@ Workspace carve_workspace(void* base, const dsa_seqs& s, int num_q, int k) {
     int64_t ld;
     workspace_bytes(s, num_q, k, &ld);
     const int kk = k < 1 ? 1 : (k > DSA_MAX_TOPK ? DSA_MAX_TOPK : k);
-    const int splits = mla_splits(num_q > 0 ? num_q : 1, kk);
+    const int nq = num_q > 0 ? num_q : 1;
     uint8_t* p = reinterpret_cast<uint8_t*>(base);
     w.qprep = p;
     p += up256((size_t)num_q * kQprepBytes);
     w.wprep = reinterpret_cast<float*>(p);
     p += up256((size_t)num_q * kIH * 4);
     w.mla_part = reinterpret_cast<float*>(p);
-    p += up256((size_t)num_q * splits * kMH * kMV * 4);
+    p += up256(mla_part_bytes(nq, kk));
     w.mla_ml = reinterpret_cast<float*>(p);
-    p += up256((size_t)num_q * splits * kMH * 2 * 4);
+    p += up256(mla_ml_bytes(nq, kk));
     w.scores = reinterpret_cast<float*>(p);
     w.scores_ld = ld;
     p += up256((size_t)num_q * ld * 4);
@@ -170,6 +170,16 @@ cudaError_t launch_block_topk(const float* scores, int64_t ld, const dsa_seqs& s
 
 
 using namespace dsa;
+
+// kernels one dsa_decode_layer call enqueues
+static int32_t layer_launches(const dsa_seqs& s, int num_q, int k, bool reuse, int select_block) {
+    // attention, plus the LSE combine unless every query's splits combine in-kernel
+    const int mla = mla_launches(num_q, k);
+    // selection: block-sparse one kernel; top-k one kernel, or three for rows
+    // longer than 32,768 keys (chunked)
+    const int tk = select_block > 0 ? 1 : (topk_chunked(s.max_ctx) ? 3 : 1);
+    return (reuse ? 0 : 2 + tk) + mla;  // query prep, scores, selection
+}
 
 static void check_shard(Check& c, const dsa_dcp_shard* sh) {
     c.need(sh != nullptr, DSA_ERR_INVALID_ARG, "shard is NULL");
@@ -474,15 +484,35 @@ dsa_status sparse_mla_decode(const void* q, const void* latent, dsa_dtype latent
                        "sparse_mla_decode launch");
 }
 
+// the block-sparse selection mode of dsa_decode_layer: k / select_block
+// blocks, within dsa_block_topk's limits
+static void check_block_select(Check& c, const dsa_seqs* seqs, int32_t k, int32_t block) {
+    c.need(block >= 0, DSA_ERR_INVALID_ARG, "select_block %d < 0", block);
+    if (block <= 0) return;
+    c.need(k % block == 0, DSA_ERR_UNSUPPORTED, "k %d is not a multiple of select_block %d", k, block);
+    const int nsel = k / block;
+    c.need(nsel >= 1 && nsel <= DSA_BLOCK_TOPK_MAX_NSEL, DSA_ERR_UNSUPPORTED,
+           "k / select_block = %d blocks outside [1, %d]", nsel, DSA_BLOCK_TOPK_MAX_NSEL);
+    if (seqs && seqs->max_ctx >= 1 && nsel >= 1)
+        c.need(block_topk_smem(seqs->max_ctx, block, nsel) <= DSA_BLOCK_TOPK_MAX_SMEM, DSA_ERR_UNSUPPORTED,
+               "max_ctx %d / select_block %d: too many blocks for one CTA's shared memory", seqs->max_ctx, block);
+}
+
+static void check_layer(Check& c, const dsa_layer_args* a, const dsa_seqs* seqs, int32_t num_q) {
+    check_seqs(c, seqs, num_q);
+    if (!a->reuse_idx) {
+        check_index_args(c, a->q_idx, a->w, a->ssmax_s, a->ssmax_b, a->inv_freq, a->k_idx, a->k_scale, a->k_dtype);
+        check_block_select(c, seqs, a->k, a->select_block);
+    }
+    check_mla_args(c, a->q_mla, a->latent, a->latent_dtype, a->idx, a->topk_len, a->k, a->sm_scale, a->out, a->lse);
+}
+
 dsa_status dsa_decode_layer(const dsa_layer_args* a, const dsa_seqs* seqs, int32_t num_q, void* workspace,
                             size_t workspace_bytes, int32_t* d_status, cudaStream_t stream) {
     Check c;
     c.need(a != nullptr, DSA_ERR_INVALID_ARG, "args is NULL");
     if (!a) return c.done();
-    check_seqs(c, seqs, num_q);
-    if (!a->reuse_idx)
-        check_index_args(c, a->q_idx, a->w, a->ssmax_s, a->ssmax_b, a->inv_freq, a->k_idx, a->k_scale, a->k_dtype);
-    check_mla_args(c, a->q_mla, a->latent, a->latent_dtype, a->idx, a->topk_len, a->k, a->sm_scale, a->out, a->lse);
+    check_layer(c, a, seqs, num_q);
     check_workspace(c, seqs, num_q, a->k, workspace, workspace_bytes);
     dsa_status st = c.done();
     if (st != DSA_OK || num_q == 0) return st;
@@ -497,8 +527,14 @@ dsa_status dsa_decode_layer(const dsa_layer_args* a, const dsa_seqs* seqs, int32
             e = launch_index_scores(a->q_idx, a->w, a->ssmax_s, a->ssmax_b, a->inv_freq, a->k_idx, a->k_scale,
                                     a->k_dtype, *seqs, num_q, ws.scores, ws.scores_ld, ws, d_status, stream);
         mark(1);
-        if (e == cudaSuccess)
-            e = launch_topk(ws.scores, ws.scores_ld, *seqs, num_q, a->k, a->idx, a->topk_len, ws, d_status, stream);
+        if (e == cudaSuccess) {
+            if (a->select_block > 0)
+                e = launch_block_topk(ws.scores, ws.scores_ld, *seqs, num_q, a->select_block, a->k / a->select_block,
+                                      a->idx, a->topk_len, d_status, stream);
+            else
+                e = launch_topk(ws.scores, ws.scores_ld, *seqs, num_q, a->k, a->idx, a->topk_len, ws, d_status,
+                                stream);
+        }
         mark(2);
     } else {
         mark(1);
@@ -519,12 +555,20 @@ int32_t dsa_decode_layer_launches(const dsa_seqs* seqs, int32_t num_q, int32_t k
     c.need(latent_dtype == DSA_BF16 || latent_dtype == DSA_FP8_DS_MLA, DSA_ERR_INVALID_ARG, "latent_dtype %d",
            (int)latent_dtype);
     if (c.done() != DSA_OK || num_q == 0) return 0;
-    const int splits = mla_splits(num_q, k);
-    // attention, plus the LSE combine unless the splits combine in-kernel (two splits)
-    const int mla = splits <= 2 ? 1 : 2;
-    // top-k: one kernel, or three for rows longer than 32,768 keys (chunked)
-    const int tk = topk_chunked(seqs->max_ctx) ? 3 : 1;
-    return (reuse_idx ? 0 : 2 + tk) + mla;  // query prep, scores, top-k
+    return layer_launches(*seqs, num_q, k, reuse_idx != 0, 0);
+}
+
+int32_t dsa_decode_layer_launches_for(const dsa_layer_args* a, const dsa_seqs* seqs, int32_t num_q) {
+    Check c;
+    c.need(a != nullptr, DSA_ERR_INVALID_ARG, "args is NULL");
+    if (!a) return 0;
+    check_seqs(c, seqs, num_q);
+    c.need(a->k >= 1 && a->k <= DSA_MAX_TOPK, DSA_ERR_UNSUPPORTED, "k %d outside [1, %d]", a->k, DSA_MAX_TOPK);
+    c.need(a->latent_dtype == DSA_BF16 || a->latent_dtype == DSA_FP8_DS_MLA, DSA_ERR_INVALID_ARG, "latent_dtype %d",
+           (int)a->latent_dtype);
+    if (!a->reuse_idx) check_block_select(c, seqs, a->k, a->select_block);
+    if (c.done() != DSA_OK || num_q == 0) return 0;
+    return layer_launches(*seqs, num_q, a->k, a->reuse_idx != 0, a->reuse_idx ? 0 : a->select_block);
 }
 
 }  // extern "C"
@@ -571,14 +615,13 @@ extern "C" dsa_status sparse_mla_decode_noalloc(const void* q, const void* laten
     check_mla_args(c, q, latent, latent_dtype, idx, topk_len, k, sm_scale, out, lse);
     size_t part_bytes = 0, ml_bytes = 0;
     if (c.st == DSA_OK && num_q > 0) {
-        const int splits = mla_splits(num_q, k);
-        if (splits > 1) {
-            part_bytes = up256((size_t)num_q * splits * kMH * kMV * 4);
-            ml_bytes = up256((size_t)num_q * splits * kMH * 2 * 4);
-        }
+        // exactly the scratch the launch below writes (none for one split or
+        // a two-split cluster pair, which combines on chip)
+        part_bytes = up256(mla_part_bytes(num_q, k));
+        ml_bytes = up256(mla_ml_bytes(num_q, k));
         c.need(part_bytes + ml_bytes <= (size_t)DSA_NOALLOC_SCRATCH_BYTES, DSA_ERR_UNSUPPORTED,
-               "%d queries x %d splits need %zu bytes of scratch; the static scratch holds %zu", num_q, splits,
-               part_bytes + ml_bytes, (size_t)DSA_NOALLOC_SCRATCH_BYTES);
+               "%d queries x %d splits need %zu bytes of scratch; the static scratch holds %zu", num_q,
+               mla_splits(num_q, k), part_bytes + ml_bytes, (size_t)DSA_NOALLOC_SCRATCH_BYTES);
     }
     dsa_status st = c.done();
     if (st != DSA_OK || num_q == 0) return st;

@@ -56,19 +56,25 @@ __global__ void __launch_bounds__(kBtThreads) block_topk_kernel(const float* __r
     const int n = pos + 1;                    // causal keys
     const int nb = (n + block - 1) / block;   // blocks holding them
     const float* row = scores + (int64_t)t * ld;
-    // block maxima, a warp per block
+    // block maxima, a warp per block; fmaxf skips NaN scores, so a maximum is
+    // never NaN and NaN below marks a block already chosen
     for (int bi = warp; bi < nb; bi += kBtWarps) {
         float m = -INFINITY;
         const int j1 = min(n, (bi + 1) * block);
         for (int j = bi * block + lane; j < j1; j += 32) m = fmaxf(m, __ldg(row + j));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) bmax[bi] = bi == nb - 1 ? INFINITY : m;  // the query's own block: always chosen
+        if (lane == 0) bmax[bi] = bi == nb - 1 ? __int_as_float(0x7FC00000) : m;  // own block: taken first
+    }
+    if (tid == 0) {
+        chosen[0] = nb - 1;
+        s_pick = 1;
     }
     __syncthreads();
-    // nsel rounds of argmax: larger packed value = larger score, then smaller block
+    // nsel - 1 rounds of argmax over the other blocks: larger packed value =
+    // larger score, then smaller block
     const int rounds = min(nsel, nb);
-    for (int r = 0; r < rounds; ++r) {
+    for (int r = 1; r < rounds; ++r) {
         unsigned long long best = 0;
         for (int bi = tid; bi < nb; bi += kBtThreads) {
             const float v = bmax[bi];
@@ -86,15 +92,23 @@ __global__ void __launch_bounds__(kBtThreads) block_topk_kernel(const float* __r
         if (tid == 0) {
             unsigned long long m = 0;
             for (int w = 0; w < kBtWarps; ++w) m = wbest[w] > m ? wbest[w] : m;
-            const int bi = (int)(0xFFFFFFFFu - (uint32_t)m);
-            chosen[r] = bi;
-            bmax[bi] = __int_as_float(0x7FC00000);  // NaN: taken
+            // m == 0 would mean no block left: impossible while r < nb, but
+            // never index with it
+            const int bi = m ? (int)(0xFFFFFFFFu - (uint32_t)m) : -1;
+            if (bi >= 0 && bi < nb) {
+                chosen[r] = bi;
+                bmax[bi] = __int_as_float(0x7FC00000);  // NaN: taken
+                s_pick = r + 1;
+            } else {
+                report(d_status, DSA_ERR_BAD_INPUT);
+            }
         }
         __syncthreads();
+        if (s_pick != r + 1) break;
     }
     // the chosen ids in ascending order (at most a few dozen: one thread)
     if (tid == 0) {
-        for (int i = 1; i < rounds; ++i) {
+        for (int i = 1; i < s_pick; ++i) {
             const int x = chosen[i];
             int j = i - 1;
             while (j >= 0 && chosen[j] > x) {
@@ -103,7 +117,6 @@ __global__ void __launch_bounds__(kBtThreads) block_topk_kernel(const float* __r
             }
             chosen[j + 1] = x;
         }
-        s_pick = rounds;
     }
     __syncthreads();
     // the own block is the highest chosen id and the only partial one, so

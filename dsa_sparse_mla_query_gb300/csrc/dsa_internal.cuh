@@ -143,6 +143,9 @@ inline int topk_chunks(int max_ctx) { return (max_ctx + kLongChunk - 1) / kLongC
 inline bool topk_chunked(int max_ctx) { return topk_long_rows(max_ctx) && topk_chunks(max_ctx) <= kLongMaxChunks; }
 
 int mla_splits(int num_q, int k);
+size_t mla_part_bytes(int num_q, int k);  // split partial outputs the attention writes (0: none)
+size_t mla_ml_bytes(int num_q, int k);    // their (max, sum) pairs
+int mla_launches(int num_q, int k);       // kernels one attention call enqueues
 size_t workspace_bytes(const dsa_seqs& s, int num_q, int k, int64_t* scores_ld);
 Workspace carve_workspace(void* base, const dsa_seqs& s, int num_q, int k);
 

@@ -34,6 +34,25 @@ int mla_splits(int num_q, int k) {
     return sp > max_sp ? max_sp : sp;
 }
 
+// Two splits run as a cluster pair and combine in distributed shared memory;
+// more write fp32 partials that the combine kernel merges.
+static bool mla_pair(int splits) { return splits == 2; }
+
+size_t mla_part_bytes(int num_q, int k) {
+    const int sp = mla_splits(num_q, k);
+    return sp > 1 && !mla_pair(sp) ? (size_t)num_q * sp * kMH * kMV * 4 : 0;
+}
+
+size_t mla_ml_bytes(int num_q, int k) {
+    const int sp = mla_splits(num_q, k);
+    return sp > 1 && !mla_pair(sp) ? (size_t)num_q * sp * kMH * 2 * 4 : 0;
+}
+
+int mla_launches(int num_q, int k) {
+    const int sp = mla_splits(num_q, k);
+    return sp > 1 && !mla_pair(sp) ? 2 : 1;
+}
+
 // LSE combine of the splits of one query ([vLLM-ML4] DCP: LSE combine):
 //   M = max_s m_s, out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 // One block per (query, 4 heads).
@@ -786,7 +805,7 @@ cudaError_t launch_sparse_mla(const void* q, const void* latent, dsa_dtype laten
     if (attr != cudaSuccess) return attr;
     // with two splits, the pair runs as a cluster and combines through
     // distributed shared memory: no partials, no combine launch
-    const int pair = splits == 2 ? 1 : 0;
+    const int pair = mla_pair(splits) ? 1 : 0;
     e = launch_pdl(fp8 ? mla_tc_kernel<true> : mla_tc_kernel<false>, dim3(splits, num_q), dim3(tcmla::kThreads),
                    tcmla::kSmem, stream, pair ? 2 : 1, qmap, reinterpret_cast<const uint8_t*>(latent), s, idx, topk_len,
                    k, scale_log2, splits, pair, reinterpret_cast<__nv_bfloat16*>(out), lse, ws.mla_part, ws.mla_ml,

@@ -159,6 +159,7 @@ class Workload:
     latent_fp8: bool = False
     shared_layer: bool = False
     topk: int = 2048
+    select_block: int = 0                  # 0: exact top-k; > 0: block-sparse selection, blocks of this size
     seed: int = 0
 
     @property
@@ -172,7 +173,9 @@ class Workload:
                 f"{'RoPE' if self.rope else 'NoPE'}, index {'e4m3+rowscale' if self.index_fp8 else 'bf16'}, "
                 f"latent {'fp8_ds_mla' if self.latent_fp8 else 'bf16'}"
                 f"{', pages of %d' % self.page_size if self.page_size else ''}"
-                f"{', + shared-indexer layer' if self.shared_layer else ''}, top-{self.topk}")
+                f"{', + shared-indexer layer' if self.shared_layer else ''}, "
+                + (f"{self.topk // self.select_block} blocks of {self.select_block}" if self.select_block
+                   else f"top-{self.topk}"))
 
 
 WORKLOADS: Dict[str, Workload] = {
@@ -181,6 +184,9 @@ WORKLOADS: Dict[str, Workload] = {
     "specv": Workload("specv", 128, 4, ctx_range=(8192, 131072), rope=False, shared_layer=True),
     "long_fp8": Workload("long_fp8", 32, 1, ctx=524288, index_fp8=True, latent_fp8=True),
     "prefill": Workload("prefill", 1, 4096, ctx=131072),
+    # block-sparse selection as the MiniMax M3.1 page describes it: 128-token
+    # blocks, 16 selected (2,048 keys) at long context; caches as long_fp8
+    "block_fp8": Workload("block_fp8", 32, 1, ctx=524288, index_fp8=True, latent_fp8=True, select_block=128),
 }
 
 

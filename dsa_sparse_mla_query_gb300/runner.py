@@ -23,8 +23,9 @@ def seqs_from_inputs(d: dict, queries_per_seq: int) -> B.Seqs:
 class DecodeStep:
     """Owns workspace and outputs for one workload; ``run()`` enqueues a step."""
 
-    def __init__(self, d: dict, queries_per_seq: int, k: int, device="cuda"):
+    def __init__(self, d: dict, queries_per_seq: int, k: int, device="cuda", select_block: int = 0):
         self.d = d
+        self.select_block = int(select_block)  # 0: exact top-k; > 0: block-sparse selection
         self.seqs = seqs_from_inputs(d, queries_per_seq)
         self.num_q = int(d["q_pos"].shape[0])
         self.k = int(k)
@@ -44,11 +45,14 @@ class DecodeStep:
         self.lat_fp8 = d["latent"].dtype == torch.uint8
         self.launches = 0
 
-    def layer_args(self, shared: bool = False) -> dict:
-        d = self.d
+    def layer_args(self, shared: bool = False, queries: dict = None) -> dict:
+        """dsa_layer_args fields; ``queries`` (q_idx, w, q_mla, q_mla2) replaces
+        the workload's own query tensors (same shapes)."""
+        d = dict(self.d, **queries) if queries else self.d
         a = dict(q_idx=d["q_idx"], w=d["w"], ssmax_s=d["ssmax_s"], ssmax_b=d["ssmax_b"], inv_freq=d["inv_freq"],
                  k_idx=d["k_idx"], k_scale=d.get("k_scale"),
                  k_dtype=B.DSA_FP8_E4M3_ROWSCALE if self.k_fp8 else B.DSA_BF16, reuse_idx=0, k=self.k,
+                 select_block=self.select_block,
                  idx=self.idx, topk_len=self.topk_len, q_mla=d["q_mla"], latent=d["latent"],
                  latent_dtype=B.DSA_FP8_DS_MLA if self.lat_fp8 else B.DSA_BF16, sm_scale=d["sm_scale"],
                  out=self.out, lse=self.lse)
@@ -57,20 +61,20 @@ class DecodeStep:
         return a
 
     def launches_per_step(self) -> int:
-        lat = B.DSA_FP8_DS_MLA if self.lat_fp8 else B.DSA_BF16
-        n = B.dsa_decode_layer_launches(self.seqs, self.num_q, self.k, 0, lat)
+        n = B.dsa_decode_layer_launches_for(self.layer_args(False), self.seqs, self.num_q)
         if self.shared:
-            n += B.dsa_decode_layer_launches(self.seqs, self.num_q, self.k, 1, lat)
+            n += B.dsa_decode_layer_launches_for(self.layer_args(True), self.seqs, self.num_q)
         return n
 
-    def run(self, stream=None, events=None, events2=None):
+    def run(self, stream=None, events=None, events2=None, queries=None):
         """One step; ``events``/``events2``: optional 4 recorded CUDA events per
-        layer (before the indexer, after the indexer, top-k, attention)."""
-        a = self.layer_args(False)
+        layer (before the indexer, after the indexer, top-k, attention);
+        ``queries``: another set of query tensors for this step."""
+        a = self.layer_args(False, queries)
         a["events"] = events
         B.dsa_decode_layer(a, self.seqs, self.num_q, self.ws, self.ws_bytes, self.status, stream)
         if self.shared:
-            a = self.layer_args(True)
+            a = self.layer_args(True, queries)
             a["events"] = events2
             B.dsa_decode_layer(a, self.seqs, self.num_q, self.ws, self.ws_bytes, self.status, stream)
 

@@ -313,7 +313,12 @@ dsa_status dsa_lse_combine(const void* const* o_parts, const float* const* lse_p
  * stream, with the scores kept in the workspace.  reuse_idx != 0 is a
  * shared-indexer layer ([vLLM-ML4] Model architecture: 28 layers reuse the
  * top-k of the nearest earlier indexer layer; [colibri] The indexer): idx and
- * topk_len are inputs and only the attention runs; otherwise they are outputs. */
+ * topk_len are inputs and only the attention runs; otherwise they are outputs.
+ * select_block > 0 selects by blocks instead of keys ("vLLM adds NVFP4 serving
+ * for MiniMax M3.1 Flash", MiniMax Sparse Attention): dsa_block_topk with
+ * blocks of select_block keys and nsel = k / select_block blocks takes the
+ * place of dsa_topk (k a multiple of select_block, and dsa_block_topk's
+ * limits); select_block = 0 is the exact top-k. */
 typedef struct {
     /* indexer (ignored when reuse_idx != 0) */
     const void* q_idx;
@@ -327,7 +332,7 @@ typedef struct {
     int32_t reuse_idx;
     /* selection */
     int32_t k;
-    int32_t reserved;
+    int32_t select_block;  /* 0: exact top-k; > 0: block-sparse selection, blocks of this many keys */
     int32_t* idx;
     int32_t* topk_len;
     /* attention */
@@ -377,6 +382,10 @@ dsa_status sparse_mla_decode_noalloc(const void* q, const void* latent, dsa_dtyp
  * query the attention combines its splits inside one launch.) */
 int32_t dsa_decode_layer_launches(const dsa_seqs* seqs, int32_t num_q, int32_t k, int32_t reuse_idx,
                                   dsa_dtype latent_dtype);
+/* The same count for a full argument set (it also reads select_block); 0 when
+ * dsa_decode_layer would refuse the sizes, the selection mode or the dtypes.
+ * Host only: no pointer in args is read. */
+int32_t dsa_decode_layer_launches_for(const dsa_layer_args* args, const dsa_seqs* seqs, int32_t num_q);
 
 /* Text of the last non-OK status returned on this thread ("" if none). */
 const char* dsa_last_error_string(void);

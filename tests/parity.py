@@ -59,6 +59,36 @@ def check_topk(gpu_idx: np.ndarray, gpu_len: int, ref_causal: np.ndarray, k: int
     return len(diff)
 
 
+def check_block_select(gpu_idx: np.ndarray, gpu_len: int, ref_causal: np.ndarray, block: int, nsel: int) -> int:
+    """Block-sparse selection against the oracle's on the oracle's scores:
+    the output is the selected blocks' causal keys ascending, then -1; the
+    query's own block is always in; the other chosen blocks equal the
+    oracle's except blocks whose oracle maximum lies within 1e-3 (relative)
+    of the last chosen block's maximum.  Returns the number of such blocks."""
+    n = ref_causal.shape[0]
+    k = nsel * block
+    sel = np.asarray(gpu_idx[:gpu_len], np.int64)
+    assert np.all(np.asarray(gpu_idx[gpu_len:k]) == -1), "slots after topk_len must be -1"
+    assert np.all(np.diff(sel) > 0) and (gpu_len == 0 or (sel[0] >= 0 and sel[-1] < n))
+    blocks = np.unique(sel // block)
+    # whole blocks (the own block up to the query)
+    for b in blocks:
+        want = np.arange(b * block, min(n, (b + 1) * block))
+        assert np.array_equal(sel[(sel >= b * block) & (sel < (b + 1) * block)], want), f"block {b} not whole"
+    nb = (n + block - 1) // block
+    assert nb - 1 in blocks, "the query's own block must be selected"
+    assert len(blocks) == min(nsel, nb)
+    ref_idx, ref_m = oracle.block_topk(ref_causal, block, nsel)
+    ref_blocks = np.unique(ref_idx[:ref_m] // block)
+    diff = set(blocks.tolist()) ^ set(ref_blocks.tolist())
+    if diff:
+        bmax = np.array([np.max(ref_causal[b * block:min(n, (b + 1) * block)]) for b in range(nb)])
+        last = min(bmax[b] for b in ref_blocks if b != nb - 1)
+        bad = [b for b in diff if abs(bmax[b] - last) > TIE_RTOL * abs(last)]
+        assert not bad, f"blocks {bad[:5]} differ outside the tie band"
+    return len(diff)
+
+
 def check_mla(out_gpu, lse_gpu, out_ref: np.ndarray, lse_ref: np.ndarray) -> float:
     o = np.asarray(out_gpu, np.float64)
     scale = float(np.max(np.abs(out_ref)))
