@@ -122,7 +122,7 @@ Workspace carve_workspace(void* base, const dsa_seqs& s, int num_q, int k) {
     p += up256((size_t)num_q * kQprepBytes);
     w.wprep = reinterpret_cast<float*>(p);
     p += up256((size_t)num_q * kIH * 4);
-    w.mla_part = reinterpret_cast<float*>(p);
+    w.mla_part = p;
     p += up256(mla_part_bytes(nq, kk));
     w.mla_ml = reinterpret_cast<float*>(p);
     p += up256(mla_ml_bytes(nq, kk));
@@ -613,15 +613,16 @@ extern "C" dsa_status sparse_mla_decode_noalloc(const void* q, const void* laten
     Check c;
     check_seqs(c, seqs, num_q);
     check_mla_args(c, q, latent, latent_dtype, idx, topk_len, k, sm_scale, out, lse);
+    // at most as many CTAs as leave their partials room in the static array
+    // (fewer CTAs than sparse_mla_decode on large batches; no size refused)
+    const int max_ctas = mla_max_ctas_for_scratch(DSA_NOALLOC_SCRATCH_BYTES);
     size_t part_bytes = 0, ml_bytes = 0;
     if (c.st == DSA_OK && num_q > 0) {
-        // exactly the scratch the launch below writes (none for one split or
-        // a two-split cluster pair, which combines on chip)
-        part_bytes = up256(mla_part_bytes(num_q, k));
-        ml_bytes = up256(mla_ml_bytes(num_q, k));
-        c.need(part_bytes + ml_bytes <= (size_t)DSA_NOALLOC_SCRATCH_BYTES, DSA_ERR_UNSUPPORTED,
-               "%d queries x %d splits need %zu bytes of scratch; the static scratch holds %zu", num_q,
-               mla_splits(num_q, k), part_bytes + ml_bytes, (size_t)DSA_NOALLOC_SCRATCH_BYTES);
+        part_bytes = up256(mla_part_bytes(num_q, k, max_ctas));
+        ml_bytes = up256(mla_ml_bytes(num_q, k, max_ctas));
+        c.need(max_ctas >= 1 && part_bytes + ml_bytes <= (size_t)DSA_NOALLOC_SCRATCH_BYTES, DSA_ERR_UNSUPPORTED,
+               "%d queries need %zu bytes of scratch; the static scratch holds %zu", num_q, part_bytes + ml_bytes,
+               (size_t)DSA_NOALLOC_SCRATCH_BYTES);
     }
     dsa_status st = c.done();
     if (st != DSA_OK || num_q == 0) return st;
@@ -629,9 +630,9 @@ extern "C" dsa_status sparse_mla_decode_noalloc(const void* q, const void* laten
     cudaError_t e = noalloc_scratch(&base);
     if (e != cudaSuccess) return cuda_status(e, "sparse_mla_decode_noalloc scratch address");
     Workspace ws{};
-    ws.mla_part = reinterpret_cast<float*>(base);
+    ws.mla_part = base;
     ws.mla_ml = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(base) + part_bytes);
     return cuda_status(launch_sparse_mla(q, latent, latent_dtype, *seqs, num_q, idx, topk_len, k, sm_scale, out, lse,
-                                         ws, d_status, stream),
+                                         ws, d_status, stream, max_ctas),
                        "sparse_mla_decode_noalloc launch");
 }

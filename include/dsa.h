@@ -357,12 +357,14 @@ dsa_status dsa_decode_layer(const dsa_layer_args* args, const dsa_seqs* seqs, in
  * start-up, a plugin ABI that hands over only input and output buffers), so it
  * has no way to provide the workspace the other entry points take.  The pages
  * have no counterpart of this call; it is a deployment convenience.
- *   Same arguments, semantics and results as sparse_mla_decode, minus the
- *   workspace.  The split-K partial results go to a static device array of
+ *   Same arguments, semantics and results (within rounding: the split of the
+ *   work may differ) as sparse_mla_decode, minus the workspace.  The partial
+ *   results of queries cut between CTAs go to a static device array of
  *   DSA_NOALLOC_SCRATCH_BYTES owned by the library: every GPU that loads the
- *   library holds it until the process exits.  Sizes whose partials do not fit
- *   (num_q x splits x 131,584 bytes, rounded up) are refused with
- *   DSA_ERR_UNSUPPORTED and a message giving both sizes; nothing is enqueued.
+ *   library holds it until the process exits.  The array holds the partials of
+ *   127 CTAs (2 x 66,048 bytes each), so this call spreads the work over at
+ *   most 127 CTAs where sparse_mla_decode takes one per SM (152 on a GB300):
+ *   no batch size is refused, large ones run somewhat slower.
  *   The first call on each device looks up the array's device address with
  *   that device current (a runtime query, no allocation); make that first call
  *   before any stream capture on the device.  Every call shares the one array
@@ -378,8 +380,9 @@ dsa_status sparse_mla_decode_noalloc(const void* q, const void* latent, dsa_dtyp
 
 /* Number of kernels dsa_decode_layer enqueues for these sizes (reuse_idx and
  * latent_dtype as in dsa_layer_args); 0 when the sizes or the dtype are
- * refused.  For callers that count or capture launches.  (With two splits per
- * query the attention combines its splits inside one launch.) */
+ * refused.  For callers that count or capture launches.  (The attention adds
+ * its combine kernel only when some query's work is cut between CTAs; the
+ * count reads the current device's SM count.) */
 int32_t dsa_decode_layer_launches(const dsa_seqs* seqs, int32_t num_q, int32_t k, int32_t reuse_idx,
                                   dsa_dtype latent_dtype);
 /* The same count for a full argument set (it also reads select_block); 0 when
