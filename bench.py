@@ -101,7 +101,9 @@ def algorithmic_bytes(wl, lay):
     ctx = lay.ctx_len
     Q = wl.num_queries
     keys = sum(ctx) * index_row_bytes(wl)
-    scores = sum(lay.ctx_len[b] for b in lay.q_seq) * 4
+    # block selection in 32-key groups: the indexer writes one maximum per group
+    per_key = 4 / 32 if wl.select_block and wl.select_block % 32 == 0 else 4
+    scores = int(sum(lay.ctx_len[b] for b in lay.q_seq) * per_key)
     qside = Q * (32 * 128 * 2 + 32 * 4)
     indexer = keys + scores + qside
     sel = sum(min(p + 1, wl.topk) for p in lay.q_pos)

@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     dsa_decode_layer,
     dsa_decode_layer_launches,
     dsa_decode_layer_launches_for,
+    dsa_dcp_shard_seqs,
     dsa_index_k_insert,
     dsa_index_scores,
     dsa_latent_insert,
@@ -39,5 +40,5 @@ from ._binding import (  # noqa: F401
 __all__ = ["Seqs", "DsaError", "dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode", "sparse_mla_decode_noalloc",
            "dsa_decode_layer", "dsa_decode_layer_launches", "dsa_decode_layer_launches_for", "dsa_index_k_insert", "dsa_latent_insert", "dsa_mla_q_prep",
            "DcpShard", "dsa_topk_candidates", "dsa_topk_merge", "dsa_topk_compact", "dsa_lse_combine",
-           "dsa_block_topk",
+           "dsa_block_topk", "dsa_dcp_shard_seqs",
            "load", "version", "DSA_BF16", "DSA_FP8_E4M3_ROWSCALE", "DSA_FP8_DS_MLA"]

@@ -88,6 +88,7 @@ def load(path: str = LIB_PATH):
         L.dsa_topk_merge.argtypes = [P, I32, I32, I32, I32, P, P, P, P]
         L.dsa_topk_compact.argtypes = [P, P, I32, I32, SH, P, P, P, P]
         L.dsa_lse_combine.argtypes = [P, P, I32, I32, P, P, P]
+        L.dsa_dcp_shard_seqs.argtypes = [S, I32, SH, P, P, P, I32, ctypes.POINTER(I32), P, P]
         L.dsa_block_topk.argtypes = [P, I64, S, I32, I32, I32, P, P, P, P]
         L.dsa_decode_layer_launches.restype = ctypes.c_int32
         for f in ("dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode", "dsa_decode_layer"):
@@ -274,6 +275,18 @@ def dsa_topk_compact(idx, topk_len, num_q: int, k: int, shard: DcpShard, local_i
                      stream=None):
     _check(load().dsa_topk_compact(_p(idx), _p(topk_len), num_q, k, ctypes.byref(shard), _p(local_idx),
                                    _p(local_len), _p(d_status), _stream(stream)))
+
+
+def dsa_dcp_shard_seqs(seqs: Seqs, num_q: int, shard: DcpShard, local_ctx_len, local_q_pos, local_page_table=None,
+                       local_max_pages: int = 0, d_status=None, stream=None) -> int:
+    """Fills one rank's local context lengths, causal bounds and (optionally)
+    page table; returns the rank's local max_ctx (host)."""
+    sc = seqs.c()
+    out = ctypes.c_int32(0)
+    _check(load().dsa_dcp_shard_seqs(ctypes.byref(sc), num_q, ctypes.byref(shard), _p(local_ctx_len), _p(local_q_pos),
+                                     _p(local_page_table), int(local_max_pages), ctypes.byref(out), _p(d_status),
+                                     _stream(stream)))
+    return int(out.value)
 
 
 def dsa_lse_combine(o_parts, lse_parts, num_q: int, out, lse=None, stream=None):

@@ -163,9 +163,14 @@ cudaError_t launch_topk_compact(const int32_t* idx, const int32_t* topk_len, int
                                 cudaStream_t stream);
 cudaError_t launch_lse_combine(const void* const* o_parts, const float* const* lse_parts, int num_parts, int num_q,
                                void* out, float* lse, cudaStream_t stream);
+int64_t dcp_owned_tokens(int64_t n, int world, int rank, int inter);
+cudaError_t launch_dcp_shard_seqs(const dsa_seqs& s, int num_q, int world, int rank, int inter, int32_t* lctx,
+                                  int32_t* lpos, int32_t* ltable, int lmax_pages, int32_t* d_status,
+                                  cudaStream_t stream);
 size_t block_topk_smem(int max_ctx, int block, int nsel);
 cudaError_t launch_block_topk(const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int block, int nsel,
-                              int32_t* idx, int32_t* topk_len, int32_t* d_status, cudaStream_t stream);
+                              int32_t* idx, int32_t* topk_len, int32_t* d_status, cudaStream_t stream,
+                              bool from_groups = false);
 }  // namespace dsa
 
 
@@ -247,7 +252,7 @@ dsa_status dsa_index_scores(const void* q_idx, const float* w, const float* ssma
     if (st != DSA_OK || num_q == 0) return st;
     Workspace ws = carve_workspace(workspace, *seqs, num_q, 1);
     return cuda_status(launch_index_scores(q_idx, w, ssmax_s, ssmax_b, inv_freq, k_idx, k_scale, k_dtype, *seqs,
-                                           num_q, scores, ld, ws, d_status, stream),
+                                           num_q, scores, ld, nullptr, 0, ws, d_status, stream),
                        "dsa_index_scores launch");
 }
 
@@ -408,6 +413,37 @@ dsa_status dsa_topk_compact(const int32_t* idx, const int32_t* topk_len, int32_t
                        "dsa_topk_compact launch");
 }
 
+dsa_status dsa_dcp_shard_seqs(const dsa_seqs* seqs, int32_t num_q, const dsa_dcp_shard* shard,
+                              int32_t* local_ctx_len, int32_t* local_q_pos, int32_t* local_page_table,
+                              int32_t local_max_pages, int32_t* local_max_ctx, int32_t* d_status,
+                              cudaStream_t stream) {
+    Check c;
+    check_seqs(c, seqs, num_q);
+    check_shard(c, shard);
+    c.ptr(local_ctx_len, "local_ctx_len", 4);
+    if (num_q > 0) c.ptr(local_q_pos, "local_q_pos", 4);
+    c.need(local_max_ctx != nullptr, DSA_ERR_INVALID_ARG, "local_max_ctx (host) is NULL");
+    int64_t lmax = 0;
+    if (seqs && c.st == DSA_OK) lmax = dcp_owned_tokens(seqs->max_ctx, shard->world, shard->rank, shard->interleave);
+    if (local_page_table && seqs && c.st == DSA_OK) {
+        c.ptr(local_page_table, "local_page_table", 4);
+        c.need(seqs->page_table != nullptr, DSA_ERR_INVALID_ARG, "local_page_table needs seqs.page_table");
+        c.need(seqs->page_size >= 1 && shard->interleave % seqs->page_size == 0, DSA_ERR_UNSUPPORTED,
+               "interleave %d is not a whole number of %d-token pages", shard->interleave, seqs->page_size);
+        if (seqs->page_size >= 1)
+            c.need((int64_t)local_max_pages * seqs->page_size >= lmax, DSA_ERR_INVALID_ARG,
+                   "local_max_pages %d x page_size %d < %lld local tokens", local_max_pages, seqs->page_size,
+                   (long long)lmax);
+    }
+    dsa_status st = c.done();
+    if (st != DSA_OK) return st;
+    *local_max_ctx = (int32_t)(lmax < 1 ? 1 : lmax);
+    return cuda_status(launch_dcp_shard_seqs(*seqs, num_q, shard->world, shard->rank, shard->interleave,
+                                             local_ctx_len, local_q_pos, local_page_table, local_max_pages, d_status,
+                                             stream),
+                       "dsa_dcp_shard_seqs launch");
+}
+
 dsa_status dsa_lse_combine(const void* const* o_parts, const float* const* lse_parts, int32_t num_parts,
                            int32_t num_q, void* out, float* lse, cudaStream_t stream) {
     Check c;
@@ -523,14 +559,20 @@ dsa_status dsa_decode_layer(const dsa_layer_args* a, const dsa_seqs* seqs, int32
     };
     mark(0);
     if (!a->reuse_idx) {
+        // block selection with blocks of whole 32-key groups needs only the
+        // groups' maxima: the indexer writes those (1/32 of the row) in place
+        // of the scores
+        const bool groups = a->select_block > 0 && a->select_block % 32 == 0;
+        const int64_t ldg = (((int64_t)seqs->max_ctx + 31) / 32 + 3) / 4 * 4;
         if (e == cudaSuccess)
             e = launch_index_scores(a->q_idx, a->w, a->ssmax_s, a->ssmax_b, a->inv_freq, a->k_idx, a->k_scale,
-                                    a->k_dtype, *seqs, num_q, ws.scores, ws.scores_ld, ws, d_status, stream);
+                                    a->k_dtype, *seqs, num_q, groups ? nullptr : ws.scores, ws.scores_ld,
+                                    groups ? ws.scores : nullptr, ldg, ws, d_status, stream);
         mark(1);
         if (e == cudaSuccess) {
             if (a->select_block > 0)
-                e = launch_block_topk(ws.scores, ws.scores_ld, *seqs, num_q, a->select_block, a->k / a->select_block,
-                                      a->idx, a->topk_len, d_status, stream);
+                e = launch_block_topk(ws.scores, groups ? ldg : ws.scores_ld, *seqs, num_q, a->select_block,
+                                      a->k / a->select_block, a->idx, a->topk_len, d_status, stream, groups);
             else
                 e = launch_topk(ws.scores, ws.scores_ld, *seqs, num_q, a->k, a->idx, a->topk_len, ws, d_status,
                                 stream);

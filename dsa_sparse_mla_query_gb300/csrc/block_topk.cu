@@ -10,7 +10,8 @@
 // topk_len), so sparse_mla_decode reads it with k = nsel * block.
 //
 // One CTA per query.  Block maxima go to shared memory (a warp per block,
-// coalesced reads of its scores); nsel rounds of a block-wide argmax over
+// coalesced reads of its scores, or, in the fused layer, a thread per block
+// over the 32-key group maxima the indexer wrote in place of the scores); nsel rounds of a block-wide argmax over
 // packed (order-preserving score code, inverted block id) values pick the
 // blocks; the chosen ids are sorted and their keys written in order.
 #include <mutex>
@@ -28,6 +29,11 @@ __device__ __forceinline__ uint32_t bt_code(float s) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// FromGroups: `scores` holds, per query, the maxima of the 32-key groups of
+// its score row (group i: keys [32 i, 32 i + 32), -inf past the query's
+// position), which the indexer writes in place of the row; block must then be
+// a multiple of 32, and a block's maximum is the maximum of its groups.
+template <bool FromGroups>
 __global__ void __launch_bounds__(kBtThreads) block_topk_kernel(const float* __restrict__ scores, int64_t ld,
                                                                 dsa_seqs s, int block, int nsel,
                                                                 int32_t* __restrict__ idx,
@@ -56,15 +62,27 @@ __global__ void __launch_bounds__(kBtThreads) block_topk_kernel(const float* __r
     const int n = pos + 1;                    // causal keys
     const int nb = (n + block - 1) / block;   // blocks holding them
     const float* row = scores + (int64_t)t * ld;
-    // block maxima, a warp per block; fmaxf skips NaN scores, so a maximum is
-    // never NaN and NaN below marks a block already chosen
-    for (int bi = warp; bi < nb; bi += kBtWarps) {
-        float m = -INFINITY;
-        const int j1 = min(n, (bi + 1) * block);
-        for (int j = bi * block + lane; j < j1; j += 32) m = fmaxf(m, __ldg(row + j));
+    // block maxima; fmaxf skips NaN scores, so a maximum is never NaN and NaN
+    // below marks a block already chosen
+    if constexpr (FromGroups) {
+        // a thread per block over its groups (keys past the position are -inf)
+        const int gpb = block >> 5, ng = (n + 31) >> 5;
+        for (int bi = tid; bi < nb; bi += kBtThreads) {
+            float m = -INFINITY;
+            const int g1 = min(ng, (bi + 1) * gpb);
+            for (int gi = bi * gpb; gi < g1; ++gi) m = fmaxf(m, __ldg(row + gi));
+            bmax[bi] = bi == nb - 1 ? __int_as_float(0x7FC00000) : m;  // own block: taken first
+        }
+    } else {
+        // a warp per block, coalesced reads of its scores
+        for (int bi = warp; bi < nb; bi += kBtWarps) {
+            float m = -INFINITY;
+            const int j1 = min(n, (bi + 1) * block);
+            for (int j = bi * block + lane; j < j1; j += 32) m = fmaxf(m, __ldg(row + j));
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) bmax[bi] = bi == nb - 1 ? __int_as_float(0x7FC00000) : m;  // own block: taken first
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) bmax[bi] = bi == nb - 1 ? __int_as_float(0x7FC00000) : m;  // own block: taken first
+        }
     }
     if (tid == 0) {
         chosen[0] = nb - 1;
@@ -143,18 +161,22 @@ size_t block_topk_smem(int max_ctx, int block, int nsel) {
 }
 
 cudaError_t launch_block_topk(const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int block, int nsel,
-                              int32_t* idx, int32_t* topk_len, int32_t* d_status, cudaStream_t stream) {
+                              int32_t* idx, int32_t* topk_len, int32_t* d_status, cudaStream_t stream,
+                              bool from_groups) {
     if (num_q <= 0) return cudaSuccess;
     const size_t smem = block_topk_smem(s.max_ctx, block, nsel);  // <= DSA_BLOCK_TOPK_MAX_SMEM (checked)
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(block_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr = cudaFuncSetAttribute(block_topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)DSA_BLOCK_TOPK_MAX_SMEM);
+        if (attr == cudaSuccess)
+            attr = cudaFuncSetAttribute(block_topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)DSA_BLOCK_TOPK_MAX_SMEM);
     });
     if (attr != cudaSuccess) return attr;
-    return launch_pdl(block_topk_kernel, dim3((unsigned)num_q), dim3(kBtThreads), smem, stream, 1, scores, ld, s,
-                      block, nsel, idx, topk_len, d_status);
+    return launch_pdl(from_groups ? block_topk_kernel<true> : block_topk_kernel<false>, dim3((unsigned)num_q),
+                      dim3(kBtThreads), smem, stream, 1, scores, ld, s, block, nsel, idx, topk_len, d_status);
 }
 
 }  // namespace dsa

@@ -280,7 +280,66 @@ __global__ void __launch_bounds__(128) lse_combine_kernel(PartPtrs parts, int nu
     if (lse && lane == 0) lse[wi] = L;
 }
 
+// ---------------------------------------------------------------------------
+// One rank's view of the sequences: the tokens of a sequence of n tokens the
+// rank owns are f I + clamp(n mod (I R) - r I, 0, I) with f = n / (I R) (whole
+// turns, then the rank's part of the last); a query at position p sees its
+// owned tokens <= p, so its local causal bound is owned(p + 1) - 1 (-1: the
+// rank owns none, DSA_ERR_BAD_INPUT); with a page table and I a whole number
+// m of pages, local page l is global page ((l / m) R + r) m + l mod m.
+__host__ __device__ __forceinline__ int64_t dcp_owned(int64_t n, int world, int rank, int inter) {
+    const int64_t turn = (int64_t)inter * world;
+    const int64_t f = n / turn, rem = n - f * turn - (int64_t)rank * inter;
+    return f * inter + (rem < 0 ? 0 : (rem > inter ? inter : rem));
+}
+
+__global__ void __launch_bounds__(128) dcp_shard_seqs_kernel(dsa_seqs s, int num_q, int world, int rank, int inter,
+                                                             int32_t* __restrict__ lctx, int32_t* __restrict__ lpos,
+                                                             int32_t* __restrict__ ltable, int lmax_pages,
+                                                             int32_t* d_status) {
+    pdl_enter();
+    const int i = blockIdx.x * 128 + threadIdx.x;
+    if (i < s.num_seqs) {
+        const int c = __ldg(s.ctx_len + i);
+        if (c < 0 || c > s.max_ctx) report(d_status, DSA_ERR_BAD_INPUT);
+        lctx[i] = (int32_t)dcp_owned(c < 0 ? 0 : c, world, rank, inter);
+    }
+    if (i < num_q) {
+        const int b = seq_of(s.q_start, s.num_seqs, i);
+        const int c = __ldg(s.ctx_len + b), p = __ldg(s.q_pos + i);
+        int64_t bound = -1;
+        if (p >= 0 && p < c) bound = dcp_owned((int64_t)p + 1, world, rank, inter) - 1;
+        if (bound < 0) report(d_status, DSA_ERR_BAD_INPUT);
+        lpos[i] = (int32_t)bound;
+    }
+    if (ltable) {
+        const int m = inter / s.page_size;  // pages per turn
+        const int64_t cells = (int64_t)s.num_seqs * lmax_pages;
+        for (int64_t e = (int64_t)blockIdx.x * 128 + threadIdx.x; e < cells; e += (int64_t)gridDim.x * 128) {
+            const int b = (int)(e / lmax_pages), l = (int)(e - (int64_t)b * lmax_pages);
+            const int64_t gp = ((int64_t)(l / m) * world + rank) * m + l % m;
+            ltable[e] = gp < s.max_pages ? __ldg(s.page_table + (int64_t)b * s.max_pages + gp) : -1;
+        }
+    }
+}
+
 }  // namespace
+
+int64_t dcp_owned_tokens(int64_t n, int world, int rank, int inter) { return dcp_owned(n, world, rank, inter); }
+
+cudaError_t launch_dcp_shard_seqs(const dsa_seqs& s, int num_q, int world, int rank, int inter, int32_t* lctx,
+                                  int32_t* lpos, int32_t* ltable, int lmax_pages, int32_t* d_status,
+                                  cudaStream_t stream) {
+    const int n = num_q > s.num_seqs ? num_q : s.num_seqs;
+    int blocks = (n + 127) / 128;
+    if (ltable) {
+        const int64_t cells = (int64_t)s.num_seqs * lmax_pages;
+        const int64_t tb = (cells + 127) / 128;
+        if (tb > blocks) blocks = (int)(tb < 4096 ? tb : 4096);
+    }
+    return launch_pdl(dcp_shard_seqs_kernel, dim3(blocks < 1 ? 1 : blocks), dim3(128), 0, stream, 1, s, num_q, world,
+                      rank, inter, lctx, lpos, ltable, lmax_pages, d_status);
+}
 
 cudaError_t launch_cand_pack(const float* scores, int64_t ld, const int32_t* idx, const int32_t* topk_len, int num_q,
                              int k, int world, int rank, int inter, uint64_t* cand, int32_t* d_status,

@@ -20,6 +20,9 @@ constexpr int kMD = DSA_MLA_DIM;       // 576
 constexpr int kMV = DSA_MLA_VDIM;      // 512
 constexpr int kDsRow = DSA_DS_MLA_ROW; // 656
 
+// kernel tags in a timeout's device status (bits 8-15)
+constexpr int kTagIndexer = 1, kTagMla = 2, kTagMlaFp8 = 3;
+
 // ---------------------------------------------------------------------------
 // device-side error reporting: first error wins, never traps
 __device__ __forceinline__ void report(int32_t* d_status, int32_t code) {
@@ -121,7 +124,7 @@ struct Workspace {
     // carved from the caller's workspace, 256-byte aligned pieces
     void* qprep;      // q' [Q, 32, KP] bf16, or [Q, 3, 32, 128] e4m3 parts (kQprepBytes per query)
     float* wprep;     // w' [Q, 32]
-    void* mla_part;   // partial outputs [2 x CTAs, 64, 512] bf16 (normalised)
+    void* mla_part;   // partial outputs [2 x CTAs, 64, 512] fp32 (normalised)
     float* mla_ml;    // their (max, sum) [2 x CTAs, 64, 2]
     float* scores;    // [Q, ld] for dsa_decode_layer
     int64_t scores_ld;
@@ -158,8 +161,8 @@ Workspace carve_workspace(void* base, const dsa_seqs& s, int num_q, int k);
 
 cudaError_t launch_index_scores(const void* q_idx, const float* w, const float* ssmax_s, const float* ssmax_b,
                                 const float* inv_freq, const void* k_idx, const float* k_scale, dsa_dtype k_dtype,
-                                const dsa_seqs& s, int num_q, float* scores, int64_t ld, const Workspace& ws,
-                                int32_t* d_status, cudaStream_t stream);
+                                const dsa_seqs& s, int num_q, float* scores, int64_t ld, float* gmax, int64_t ldg,
+                                const Workspace& ws, int32_t* d_status, cudaStream_t stream);
 cudaError_t launch_topk(const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int k, int32_t* idx,
                         int32_t* topk_len, const Workspace& ws, int32_t* d_status, cudaStream_t stream);
 cudaError_t launch_sparse_mla(const void* q, const void* latent, dsa_dtype latent_dtype, const dsa_seqs& s,

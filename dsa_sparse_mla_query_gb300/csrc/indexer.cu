@@ -376,8 +376,8 @@ template <int NQ, int KP, bool FP8>
 __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, FP8>::ctas_per_sm)
     index_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                     const float* __restrict__ wp, const float* __restrict__ k_scale, dsa_seqs s,
-                    float* __restrict__ scores, int64_t ld, int tiles_per_seq, int chunks, int64_t total_tiles,
-                    int box_rows, int32_t* d_status) {
+                    float* __restrict__ scores, int64_t ld, float* __restrict__ gmax, int64_t ldg,
+                    int tiles_per_seq, int chunks, int64_t total_tiles, int box_rows, int32_t* d_status) {
     pdl_enter();
     using C = IdxCfg<NQ, KP, FP8>;
     constexpr int S = C::S, N = C::N;
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
     uint64_t* ifull = bars + 2 * S + 6;                // [kInfoSlots] tile info written (and scales landed)
     uint64_t* iempty = bars + 2 * S + 6 + kInfoSlots;  // [kInfoSlots] tile info read
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 6 + 2 * kInfoSlots);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);  // and the kernel tag at +1
     float* sw_all = reinterpret_cast<float*>(tmem_slot + 4);  // [EW][NQ*32] head weights, one copy per epilogue warp
     int* spos_all = reinterpret_cast<int*>(sw_all + C::EW * NQ * kIH);  // [EW][NQ] query positions
 
@@ -420,6 +420,7 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
         ptx::mbar_init(qfull, 1);
         ptx::mbar_init(qempty, 1);
         *abort_flag = 0;
+        abort_flag[1] = kTagIndexer;  // names this kernel in a timeout's status
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -615,9 +616,14 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
             }
             const int j = j0 + row;
             const bool in_ctx = j < g.ctx;
+            // this warp's 32 keys are group grp of the row (gmax: their maximum)
+            const int grp = (j0 >> 5) + quarter;
+            const bool grp_live = j0 + quarter * 32 < g.ctx;
             if (kind == 1) {
-                if (in_ctx)
-                    for (int q = q_lo; q < min(g.nq, q_lo + C::QPW); ++q) scores[(int64_t)(g.q0 + q) * ld + j] = -INFINITY;
+                for (int q = q_lo; q < min(g.nq, q_lo + C::QPW); ++q) {
+                    if (scores && in_ctx) scores[(int64_t)(g.q0 + q) * ld + j] = -INFINITY;
+                    if (gmax && lane == 0 && grp_live) gmax[(int64_t)(g.q0 + q) * ldg + grp] = -INFINITY;
+                }
                 continue;
             }
             // this row's physical location and scale, from the producer
@@ -689,9 +695,16 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
                 ptx::tmem_wait_ld32(v);
                 return relu_sum(v, q);
             };
+            // the row's score (-inf past the query's position); with gmax, the
+            // maximum of the warp's 32 keys too (called by the whole warp)
             auto store = [&](int q, float r) {
-                if (in_ctx && q < g.nq)
-                    scores[(int64_t)(g.q0 + q) * ld + j] = (prow >= 0 && j <= spos[q]) ? r * sigma : -INFINITY;
+                if (q >= g.nq) return;
+                const float v = (in_ctx && prow >= 0 && j <= spos[q]) ? r * sigma : -INFINITY;
+                if (scores && in_ctx) scores[(int64_t)(g.q0 + q) * ld + j] = v;
+                if (gmax) {
+                    const float m = ptx::warp_max(v);
+                    if (lane == 0 && grp_live) gmax[(int64_t)(g.q0 + q) * ldg + grp] = m;
+                }
             };
             auto release = [&] {
                 ptx::tc_fence_before();
@@ -801,7 +814,8 @@ int num_sms() {
 
 template <int NQ, int KP, bool FP8>
 cudaError_t launch_tc(const void* qp, int num_q, const float* wp, const void* k_idx, const float* k_scale,
-                      const dsa_seqs& s, float* scores, int64_t ld, int32_t* d_status, cudaStream_t stream) {
+                      const dsa_seqs& s, float* scores, int64_t ld, float* gmax, int64_t ldg, int32_t* d_status,
+                      cudaStream_t stream) {
     using C = IdxCfg<NQ, KP, FP8>;
     const int box_rows = s.page_table ? std::min(64, s.page_size & -s.page_size) : kTileKeys;
     CUtensorMap kmap, qmap;
@@ -832,29 +846,29 @@ cudaError_t launch_tc(const void* qp, int num_q, const float* wp, const void* k_
     const int64_t total = (int64_t)s.num_seqs * chunks * tiles_per_seq;
     const int grid = (int)std::min<int64_t>((int64_t)C::ctas_per_sm * num_sms(), total);
     return launch_pdl(kern, dim3(grid), dim3(C::threads), C::smem, stream, 1, kmap, qmap, wp, k_scale, s, scores, ld,
-                      tiles_per_seq, chunks, total, box_rows, d_status);
+                      gmax, ldg, tiles_per_seq, chunks, total, box_rows, d_status);
 }
 
 template <int NQ>
 cudaError_t launch_tc_nq(bool rope, bool fp8, const void* qp, int num_q, const float* wp, const void* k_idx,
-                         const float* k_scale, const dsa_seqs& s, float* scores, int64_t ld, int32_t* d_status,
-                         cudaStream_t stream) {
+                         const float* k_scale, const dsa_seqs& s, float* scores, int64_t ld, float* gmax, int64_t ldg,
+                         int32_t* d_status, cudaStream_t stream) {
     if (fp8) {  // q' parts hold the rotated (or unrotated) 128 dims either way
         if constexpr (NQ <= 2)
-            return launch_tc<NQ, 128, true>(qp, num_q, wp, k_idx, k_scale, s, scores, ld, d_status, stream);
+            return launch_tc<NQ, 128, true>(qp, num_q, wp, k_idx, k_scale, s, scores, ld, gmax, ldg, d_status, stream);
         else
             return cudaErrorInvalidValue;
     }
-    return rope ? launch_tc<NQ, 192, false>(qp, num_q, wp, k_idx, k_scale, s, scores, ld, d_status, stream)
-                : launch_tc<NQ, 128, false>(qp, num_q, wp, k_idx, k_scale, s, scores, ld, d_status, stream);
+    return rope ? launch_tc<NQ, 192, false>(qp, num_q, wp, k_idx, k_scale, s, scores, ld, gmax, ldg, d_status, stream)
+                : launch_tc<NQ, 128, false>(qp, num_q, wp, k_idx, k_scale, s, scores, ld, gmax, ldg, d_status, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_index_scores(const void* q_idx, const float* w, const float* ssmax_s, const float* ssmax_b,
                                 const float* inv_freq, const void* k_idx, const float* k_scale, dsa_dtype k_dtype,
-                                const dsa_seqs& s, int num_q, float* scores, int64_t ld, const Workspace& ws,
-                                int32_t* d_status, cudaStream_t stream) {
+                                const dsa_seqs& s, int num_q, float* scores, int64_t ld, float* gmax, int64_t ldg,
+                                const Workspace& ws, int32_t* d_status, cudaStream_t stream) {
     const bool fp8 = k_dtype == DSA_FP8_E4M3_ROWSCALE;
     const bool rope = inv_freq != nullptr;
     const __nv_bfloat16* qi = reinterpret_cast<const __nv_bfloat16*>(q_idx);
@@ -866,14 +880,14 @@ cudaError_t launch_index_scores(const void* q_idx, const float* w, const float* 
     if (e != cudaSuccess) return e;
     const int mq = s.max_q_per_seq;
     if (fp8)  // e4m3 keys: chunks of at most two queries (four parts each fill the TMEM)
-        return mq <= 1 ? launch_tc_nq<1>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, d_status,
+        return mq <= 1 ? launch_tc_nq<1>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, gmax, ldg, d_status,
                                          stream)
-                       : launch_tc_nq<2>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, d_status,
+                       : launch_tc_nq<2>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, gmax, ldg, d_status,
                                          stream);
-    if (mq <= 1) return launch_tc_nq<1>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, d_status, stream);
-    if (mq <= 2) return launch_tc_nq<2>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, d_status, stream);
-    if (mq <= 4) return launch_tc_nq<4>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, d_status, stream);
-    return launch_tc_nq<8>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, d_status, stream);
+    if (mq <= 1) return launch_tc_nq<1>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, gmax, ldg, d_status, stream);
+    if (mq <= 2) return launch_tc_nq<2>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, gmax, ldg, d_status, stream);
+    if (mq <= 4) return launch_tc_nq<4>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, gmax, ldg, d_status, stream);
+    return launch_tc_nq<8>(rope, fp8, ws.qprep, num_q, ws.wprep, k_idx, k_scale, s, scores, ld, gmax, ldg, d_status, stream);
 }
 
 }  // namespace dsa

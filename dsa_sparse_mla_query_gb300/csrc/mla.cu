@@ -17,7 +17,7 @@
 // gets the same number of tiles whatever the batch.  A CTA's range is walked
 // as segments, each the piece of one query that falls in it.  A segment
 // holding a whole query writes that query's output; the pieces of a query cut
-// between CTAs write normalised partial outputs with their (max, sum) -- the
+// between CTAs write normalised fp32 partial outputs with their (max, sum) -- the
 // first segment of CTA c to partial slot 2c, its last to slot 2c + 1 -- and
 // the combine kernel merges them with their LSE weights.  When a query's live
 // slots [0, topk_len) are fewer than k, each piece's nominal tiles map
@@ -87,7 +87,7 @@ constexpr int KB = kMD / 64;               // 9 blocks of 64 dims
 constexpr int kKBlock = TK * 128;          // bytes of one 64-dim block of a tile
 constexpr int kStage = KB * kKBlock;       // 73728
 constexpr int kQBytes = KB * kMH * 128;    // 73728
-constexpr int kMisc = 6144;
+constexpr int kMisc = 9728;
 constexpr size_t kSmem = 2 * (size_t)kStage + kQBytes + kMisc;
 static_assert(kSmem <= 232448, "one CTA per SM within the 227 KB of shared memory a CTA may use");
 constexpr float kRescale = 64.f;           // log2 headroom before O^T is rescaled (bf16 P, fp32 O)
@@ -101,7 +101,8 @@ constexpr int kSoftWarps = 8;
 constexpr int kRing = 4;                   // resolved-row ring: rows resolved and prefetched to L2 ahead
 constexpr int kMinTiles = 2;               // fewest tiles a CTA is given
 constexpr int kMaxParts = 64;              // pieces of one query the combine merges
-constexpr int kSlotBytes = kMH * kMV * 2;  // one partial output, bf16
+constexpr int kMaxSegs = 128;              // segments of one CTA (its table in shared memory)
+constexpr int kSlotBytes = kMH * kMV * 4;  // one partial output, fp32
 constexpr int kSlotMl = kMH * 2 * 4;       // its (max, sum) per head
 static_assert(kKBlock == TK * kMH * 2, "P^T must fit the rope block of its tile");
 static_assert((DSA_MAX_TOPK + TK - 1) / TK + 1 <= kMaxParts, "a query's pieces fit the combine");
@@ -129,6 +130,11 @@ static MlaPlan mla_plan(int num_q, int k, int max_ctas) {
     p.total = (int64_t)(num_q > 0 ? num_q : 1) * p.T;
     int64_t g = (p.total + tcmla::kMinTiles - 1) / tcmla::kMinTiles;
     if (g > max_ctas) g = max_ctas;
+    // a range of at most (kMaxSegs - 2) T tiles touches at most kMaxSegs - 1
+    // queries: very large batches take more CTAs (several waves)
+    const int64_t per = (int64_t)(tcmla::kMaxSegs - 2) * p.T;
+    const int64_t g_min = (p.total + per - 1) / per;
+    if (g < g_min) g = g_min;
     p.G = g < 1 ? 1 : (int)g;
     return p;
 }
@@ -217,32 +223,37 @@ __device__ __forceinline__ Live seg_live(const Seg& sg, const dsa_seqs& s, const
     v.l1 = (int)((int64_t)sg.a1 * L / T);
     return v;
 }
+// A CTA's segments, resolved once at the start into shared memory (their
+// query lengths and sequences are global loads the roles' loops must not wait
+// on).
+struct SegEntry {
+    int q, l0, l1, len;  // query, live tiles [l0, l1), live slots
+    int b, ctx, flags, pad;  // its sequence and context; kWhole | kFirst
+};
+constexpr int kWhole = 1, kFirst = 2;
+
 // The tiles of a CTA's non-empty segments, in order.
 struct TileCursor {
-    int j, nseg;          // next segment to look at, segments of the CTA
+    int j;                // next table entry to look at
     int seg, q, n, i, g;  // non-empty segment index, its query, its tiles, tile in it, tile in the CTA
     bool done;
-    __device__ __forceinline__ TileCursor(const MlaPlan& p, int c)
-        : j(0), nseg(plan_nseg(p, c)), seg(-1), q(0), n(0), i(0), g(0), done(false) {}
-    __device__ __forceinline__ void next_segment(const MlaPlan& p, int c, const dsa_seqs& s, const int32_t* topk_len,
-                                                 int k) {
+    __device__ __forceinline__ TileCursor() : j(0), seg(-1), q(0), n(0), i(0), g(0), done(false) {}
+    __device__ __forceinline__ void next_segment(const SegEntry* tab, int nseg) {
         while (j < nseg) {
-            const Seg sg = plan_seg(p, c, j++);
-            const Live lv = seg_live(sg, s, topk_len, k, p.T, nullptr);
-            if (lv.l1 > lv.l0) {
+            const SegEntry e = tab[j++];
+            if (e.l1 > e.l0) {
                 ++seg;
-                q = sg.q;
-                n = lv.l1 - lv.l0;
+                q = e.q;
+                n = e.l1 - e.l0;
                 i = 0;
                 return;
             }
         }
         done = true;
     }
-    __device__ __forceinline__ void advance(const MlaPlan& p, int c, const dsa_seqs& s, const int32_t* topk_len,
-                                           int k) {
+    __device__ __forceinline__ void advance(const SegEntry* tab, int nseg) {
         ++g;
-        if (++i == n) next_segment(p, c, s, topk_len, k);
+        if (++i == n) next_segment(tab, nseg);
     }
 };
 
@@ -252,7 +263,7 @@ struct TileCursor {
 // normalised partial outputs).  One block per (query, 4 heads); queries held
 // whole by one CTA were written by the attention kernel.
 constexpr int kCombineHeads = 4;
-__global__ void __launch_bounds__(128) mla_combine_kernel(const __nv_bfloat16* __restrict__ part_o,
+__global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restrict__ part_o,
                                                           const float* __restrict__ part_ml, MlaPlan plan,
                                                           __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
     using namespace tcmla;
@@ -290,26 +301,22 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const __nv_bfloat16* _
     }
     __syncthreads();
     __nv_bfloat16* ot = out + ((int64_t)q * kMH + h0) * kMV;
-    for (int e = threadIdx.x; e < kCombineHeads * kMV / 8; e += blockDim.x) {
-        const int hh = (e * 8) / kMV;
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int e = threadIdx.x; e < kCombineHeads * kMV / 4; e += blockDim.x) {
+        const int hh = (e * 4) / kMV;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int p = 0; p < parts; ++p) {
             const float wv = wgt[hh][p];
             if (wv == 0.f) continue;
-            const uint4 v = *reinterpret_cast<const uint4*>(part_o + ((int64_t)slot_of[p] * kMH + h0) * kMV + e * 8);
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                acc[2 * j] += wv * __uint_as_float(w4[j] << 16);
-                acc[2 * j + 1] += wv * __uint_as_float(w4[j] & 0xFFFF0000u);
-            }
+            const float4 v = *reinterpret_cast<const float4*>(part_o + ((int64_t)slot_of[p] * kMH + h0) * kMV + e * 4);
+            acc.x += wv * v.x;
+            acc.y += wv * v.y;
+            acc.z += wv * v.z;
+            acc.w += wv * v.w;
         }
-        uint4 o;
-        o.x = pack_bf16(acc[0], acc[1]);
-        o.y = pack_bf16(acc[2], acc[3]);
-        o.z = pack_bf16(acc[4], acc[5]);
-        o.w = pack_bf16(acc[6], acc[7]);
-        *reinterpret_cast<uint4*>(ot + e * 8) = o;
+        uint2 o;
+        o.x = pack_bf16(acc.x, acc.y);
+        o.y = pack_bf16(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(ot + e * 4) = o;
     }
 }
 
@@ -344,7 +351,7 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
     mla_tc_kernel(const __grid_constant__ CUtensorMap qmap, const uint8_t* __restrict__ latent, dsa_seqs s,
                   const int32_t* __restrict__ idx, const int32_t* __restrict__ topk_len, int k, float scale_log2,
                   MlaPlan plan, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
-                  __nv_bfloat16* __restrict__ part_o, float* __restrict__ part_ml, int32_t* d_status) {
+                  float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* d_status) {
     pdl_enter();
     using namespace tcmla;
     extern __shared__ __align__(1024) uint8_t tc_smem[];   // 1024-aligned for the 128-byte swizzle atoms
@@ -374,17 +381,36 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
     uint64_t* rfree = rfull + kRing;  // [kRing] rows of a tile no longer read (gather + softmax warps)
     static_assert(25 + 2 * kRing <= 64, "barriers fit their 512 bytes");
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 512);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 516);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 516);  // and the kernel tag at +520
     int* srow = reinterpret_cast<int*>(misc + 1024);                 // [kRing][TK] physical row (-1 = masked)
     float* wmax = reinterpret_cast<float*>(misc + 1024 + kRing * TK * 4);  // [4 lane quarters][64] maxima
     float* mu = wmax + 4 * kMH;                                      // [8 warps][32 heads] running max (log2)
     float* lsum = mu + kSoftWarps * 32;                              // [4 lane quarters][64] row sums
     int* wflag = reinterpret_cast<int*>(lsum + 4 * kMH);             // [2][8 warps] growth flags
-    static_assert(1024 + kRing * TK * 4 + (4 * kMH + kSoftWarps * 32 + 4 * kMH) * 4 + 2 * kSoftWarps * 4 <= kMisc,
-                  "misc fits");
+    SegEntry* segtab = reinterpret_cast<SegEntry*>(misc + 5632);     // [kMaxSegs] the CTA's segments
+    static_assert(1024 + kRing * TK * 4 + (4 * kMH + kSoftWarps * 32 + 4 * kMH) * 4 + 2 * kSoftWarps * 4 <= 5632,
+                  "misc fits below the segment table");
+    static_assert(5632 + kMaxSegs * sizeof(SegEntry) <= (size_t)kMisc, "segment table fits");
 
     const int c = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the CTA's segments, all resolved at once (the plan keeps them <= kMaxSegs)
+    const int nseg = min(plan_nseg(plan, c), kMaxSegs);
+    for (int j = threadIdx.x; j < nseg; j += kThreads) {
+        const Seg sg = plan_seg(plan, c, j);
+        // the CTA holding a query's first tile reports its bad length
+        const Live lv = seg_live(sg, s, topk_len, k, plan.T, sg.a0 == 0 ? d_status : nullptr);
+        SegEntry e;
+        e.q = sg.q;
+        e.l0 = lv.l0;
+        e.l1 = lv.l1;
+        e.len = lv.len;
+        e.b = lv.b;
+        e.ctx = lv.ctx;
+        e.flags = (sg.a0 == 0 && sg.a1 == plan.T ? kWhole : 0) | (sg.first ? kFirst : 0);
+        e.pad = 0;
+        segtab[j] = e;
+    }
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(qfull, 1);
@@ -411,6 +437,7 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
         ptx::mbar_init(oempty, kSoftWarps);
         ptx::mbar_init(mdone, 1);
         *abort_flag = 0;
+        abort_flag[1] = FP8 ? kTagMlaFp8 : kTagMla;  // names this kernel in a timeout's status
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -424,44 +451,76 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ row resolution, L2 prefetch
+        // Tiles go in groups of kRing: the slot loads of the whole group are
+        // issued together, then its page-table loads, so a group costs two
+        // dependent load latencies rather than two per tile.  Lane l takes
+        // slots 2l and 2l + 1 of each tile.
         const uint32_t row_bytes = FP8 ? (uint32_t)kDsRow : (uint32_t)(kMD * 2);
-        const int nseg = plan_nseg(plan, c);
+        int j = 0, lt = 0;  // cursor: segment, live tile within it
+        if (nseg > 0) lt = segtab[0].l0;
         int gi = 0;
         bool ok = true;
-        for (int j = 0; ok && j < nseg; ++j) {
-            const Seg sg = plan_seg(plan, c, j);
-            // the CTA holding a query's first tile reports its bad length
-            const Live lv = seg_live(sg, s, topk_len, k, plan.T, (lane == 0 && sg.a0 == 0) ? d_status : nullptr);
-            const int32_t* tidx = idx + (int64_t)sg.q * k;
-            for (int lt = lv.l0; lt < lv.l1; ++lt, ++gi) {
-                const int r = gi % kRing;
-                int rows2[2];
+        while (ok) {
+            int tj[kRing], tlt[kRing], n = 0;  // the group's tiles: segment entry, live tile
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int slot = lt * TK + 2 * lane + u;
+            for (int u = 0; u < kRing; ++u) {
+                while (j < nseg && lt >= segtab[j].l1)
+                    if (++j < nseg) lt = segtab[j].l0;
+                tj[u] = j < nseg ? j : 0;
+                tlt[u] = j < nseg ? lt++ : 0;
+                if (j < nseg) n = u + 1;
+            }
+            if (n == 0) break;
+            int jv[kRing][2];
+#pragma unroll
+            for (int u = 0; u < kRing; ++u)
+#pragma unroll
+                for (int v = 0; v < 2; ++v) {
+                    jv[u][v] = -2;  // no slot
+                    if (u < n) {
+                        const SegEntry& e = segtab[tj[u]];
+                        const int slot = tlt[u] * TK + 2 * lane + v;
+                        if (slot < e.len) jv[u][v] = __ldg(idx + (int64_t)e.q * k + slot);
+                    }
+                }
+            int rows[kRing][2];
+#pragma unroll
+            for (int u = 0; u < kRing; ++u)
+#pragma unroll
+                for (int v = 0; v < 2; ++v) {
                     int row = -1;
-                    if (slot < lv.len) {
-                        const int j = __ldg(tidx + slot);
-                        if (j >= lv.ctx || j < -1) {
+                    if (u < n && jv[u][v] != -2) {
+                        const SegEntry& e = segtab[tj[u]];
+                        const int jj = jv[u][v];
+                        if (jj >= e.ctx || jj < -1) {
                             report(d_status, DSA_ERR_BAD_INPUT);
-                        } else if (j >= 0) {
-                            const int64_t pr = phys_row(s, lv.b, j);
+                        } else if (jj >= 0) {
+                            const int64_t pr = phys_row(s, e.b, jj);
                             if (pr < 0) report(d_status, DSA_ERR_BAD_INPUT);
                             else row = (int)pr;
                         }
                     }
-                    rows2[u] = row;
-                    if (row >= 0) ptx::prefetch_l2_bulk(latent + (size_t)row * row_bytes, row_bytes);
+                    rows[u][v] = row;
                 }
+#pragma unroll
+            for (int u = 0; u < kRing; ++u)
+#pragma unroll
+                for (int v = 0; v < 2; ++v)
+                    if (rows[u][v] >= 0) ptx::prefetch_l2_bulk(latent + (size_t)rows[u][v] * row_bytes, row_bytes);
+#pragma unroll
+            for (int u = 0; u < kRing; ++u) {
+                if (u >= n) break;
+                const int r = gi % kRing;
                 if (lane == 0 && gi >= kRing) ok = ptx::mbar_wait(rfree + r, ((gi / kRing) - 1) & 1, abort_flag, d_status);
                 if (!__shfl_sync(0xffffffffu, ok, 0)) {
                     ok = false;
                     break;
                 }
-                srow[r * TK + 2 * lane] = rows2[0];
-                srow[r * TK + 2 * lane + 1] = rows2[1];
+                srow[r * TK + 2 * lane] = rows[u][0];
+                srow[r * TK + 2 * lane + 1] = rows[u][1];
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(rfull + r);
+                ++gi;
             }
         }
     } else if (warp == 1) {
@@ -471,9 +530,9 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
             constexpr uint32_t idesc_pv = ptx::idesc_f16(128, kMH, !FP8, true, true);
             const uint32_t qb = smem_u32(qs);
             ptx::prefetch_tmap(&qmap);
-            TileCursor sc(plan, c), pc(plan, c);  // the S^T stream and the O^T stream
-            sc.next_segment(plan, c, s, topk_len, k);
-            pc.next_segment(plan, c, s, topk_len, k);
+            TileCursor sc, pc;  // the S^T stream and the O^T stream
+            sc.next_segment(segtab, nseg);
+            pc.next_segment(segtab, nseg);
             int q_loaded = -1;  // last segment whose query load was issued
             int q_ready = -1;   // last segment whose query is known loaded (and converted)
             bool issued = false;
@@ -543,7 +602,7 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                         ptx::mma_commit(sfull + st);
                         if (sc.i + 1 == sc.n) ptx::mma_commit(qfree);  // the segment's last S^T
                         s_half = 0;
-                        sc.advance(plan, c, s, topk_len, k);
+                        sc.advance(segtab, nseg);
                         progressed = true;
                     }
                 }
@@ -551,7 +610,7 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                     (pc.i > 0 || pc.seg == 0 || ptx::mbar_test_wait(oempty, (pc.seg - 1) & 1))) {
                     issue_pv(pc.g, pc.i == 0);
                     if (pc.i + 1 == pc.n) ptx::mma_commit(ofull);  // the segment's O^T complete
-                    pc.advance(plan, c, s, topk_len, k);
+                    pc.advance(segtab, nseg);
                     progressed = true;
                 }
                 if (progressed) {
@@ -561,7 +620,7 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                     if (idle.expired(ptx::kWaitTimeoutNs) || *abort_flag) {
                         if (!*abort_flag) {
                             *abort_flag = 1;
-                            report(d_status, DSA_ERR_TIMEOUT);
+                            report(d_status, ptx::timeout_code(abort_flag, ptx::kLoopSite));
                         }
                         ok = false;
                     }
@@ -583,11 +642,10 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
         const int gt = threadIdx.x - (2 + kSoftWarps) * 32;  // 0..255
         const int c8 = gt & 7, r0 = gt >> 3;
         const uint32_t soff = (uint32_t)r0 * 128 + ((c8 ^ (r0 & 7)) << 4);  // same swizzle for r0 + 32
-        const int nseg = plan_nseg(plan, c);
         int gi = 0;
         bool alive = true;
         for (int j = 0; alive && j < nseg; ++j) {
-            const Live lv = seg_live(plan_seg(plan, c, j), s, topk_len, k, plan.T, nullptr);
+            const SegEntry lv = segtab[j];
             for (int lt = lv.l0; lt < lv.l1; ++lt, ++gi) {
                 const int st = gi & 1, r = gi % kRing;
                 if (!__all_sync(0xffffffffu, ptx::mbar_wait(rfull + r, (gi / kRing) & 1, abort_flag, d_status))) {
@@ -662,17 +720,12 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
         const int dim = quarter * 32 + lane;                // output: value dim of each 128-dim block
         auto total_l = [&](int h) { return lsum[h] + lsum[kMH + h] + lsum[2 * kMH + h] + lsum[3 * kMH + h]; };
         auto run_max = [&](int h) { return mu[(h >> 5) * 4 * 32 + (h & 31)]; };  // copy of warp sw = 4 (h / 32)
-        const int nseg = plan_nseg(plan, c);
         bool alive = true;
         int gi = 0, sn = 0;
         int n_grow = 0;  // exact-maxima exchanges so far (same count in every softmax warp)
         int n_xch = 0;   // growth-flag exchanges so far
         for (int j = 0; j < nseg; ++j) {
-            int ntl;
-            {
-                const Live lv = seg_live(plan_seg(plan, c, j), s, topk_len, k, plan.T, nullptr);
-                ntl = alive ? lv.l1 - lv.l0 : 0;
-            }
+            const int ntl = alive ? segtab[j].l1 - segtab[j].l0 : 0;
             bool have = false;
             if (ntl > 0) {
                 if constexpr (FP8) {
@@ -852,11 +905,14 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                 if (have) ptx::tc_fence_after();
             }
             // ---- output of the segment: value dim `dim` of each 128-dim block, heads hb .. hb+31
-            const Seg sg = plan_seg(plan, c, j);  // recomputed: nothing of it lives across the tiles
-            const bool whole = sg.a0 == 0 && sg.a1 == plan.T;
-            const int slot = 2 * c + (sg.first ? 0 : 1);
+            // lane jj: 1 / (row sum) of head hb + jj, shared by shuffle
+            const float my_l = have ? total_l(hb + lane) : 0.f;
+            const float my_inv = my_l > 0.f ? 1.f / my_l : 0.f;
+            const int sq = segtab[j].q, sflags = segtab[j].flags;
+            const bool whole = (sflags & kWhole) != 0;
+            const int slot = 2 * c + ((sflags & kFirst) ? 0 : 1);
             if (whole) {
-                __nv_bfloat16* ot = out + (int64_t)sg.q * kMH * kMV;
+                __nv_bfloat16* ot = out + (int64_t)sq * kMH * kMV;
 #pragma unroll 1
                 for (int cb = 0; cb < 8; ++cb) {  // 16 columns = heads of one 128-dim block at a time
                     const int db = cb >> 1, h0 = hb + (cb & 1) * 16;
@@ -864,21 +920,19 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                     if (have) ptx::tmem_ld16(tl + kOCol + db * kMH + h0, o);
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
-                        const int h = h0 + jj;
-                        const float L = have ? total_l(h) : 0.f;
-                        const float v = L > 0.f ? o[jj] / L : 0.f;
-                        ot[(int64_t)h * kMV + db * 128 + dim] = __float2bfloat16_rn(v);
+                        const float inv = __shfl_sync(0xffffffffu, my_inv, (cb & 1) * 16 + jj);
+                        ot[(int64_t)(h0 + jj) * kMV + db * 128 + dim] = __float2bfloat16_rn(have ? o[jj] * inv : 0.f);
                     }
                 }
                 if (lse && sw == 0) {
                     for (int h = lane; h < kMH; h += 32) {
                         const float L = have ? total_l(h) : 0.f;
-                        lse[(int64_t)sg.q * kMH + h] = L > 0.f ? (run_max(h) + log2f(L)) * 0.69314718055994531f : -INFINITY;
+                        lse[(int64_t)sq * kMH + h] = L > 0.f ? (run_max(h) + log2f(L)) * 0.69314718055994531f : -INFINITY;
                     }
                 }
             } else {
                 // a piece of a query cut between CTAs: normalised output + (max, sum)
-                __nv_bfloat16* po = part_o + (int64_t)slot * kMH * kMV;
+                float* po = part_o + (int64_t)slot * kMH * kMV;
 #pragma unroll 1
                 for (int cb = 0; cb < 8; ++cb) {  // 16 columns = heads of one 128-dim block at a time
                     const int db = cb >> 1, h0 = hb + (cb & 1) * 16;
@@ -886,9 +940,8 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                     if (have) ptx::tmem_ld16(tl + kOCol + db * kMH + h0, o);
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
-                        const int h = h0 + jj;
-                        const float L = have ? total_l(h) : 0.f;
-                        po[(int64_t)h * kMV + db * 128 + dim] = __float2bfloat16_rn(L > 0.f ? o[jj] / L : 0.f);
+                        const float inv = __shfl_sync(0xffffffffu, my_inv, (cb & 1) * 16 + jj);
+                        po[(int64_t)(h0 + jj) * kMV + db * 128 + dim] = have ? o[jj] * inv : 0.f;
                     }
                 }
                 if (sw == 0) {
@@ -970,13 +1023,13 @@ cudaError_t launch_sparse_mla(const void* q, const void* latent, dsa_dtype laten
                                         (int)tcmla::kSmem);
     });
     if (attr != cudaSuccess) return attr;
-    auto* part_o = reinterpret_cast<__nv_bfloat16*>(ws.mla_part);
+    auto* part_o = reinterpret_cast<float*>(ws.mla_part);
     e = launch_pdl(fp8 ? mla_tc_kernel<true> : mla_tc_kernel<false>, dim3(plan.G), dim3(tcmla::kThreads), tcmla::kSmem,
                    stream, 1, qmap, reinterpret_cast<const uint8_t*>(latent), s, idx, topk_len, k, scale_log2, plan,
                    reinterpret_cast<__nv_bfloat16*>(out), lse, part_o, ws.mla_ml, d_status);
     if (e != cudaSuccess || !plan_splits(plan)) return e;
     return launch_pdl(mla_combine_kernel, dim3(num_q, kMH / kCombineHeads), dim3(128), 0, stream, 1,
-                      (const __nv_bfloat16*)part_o, (const float*)ws.mla_ml, plan,
+                      (const float*)part_o, (const float*)ws.mla_ml, plan,
                       reinterpret_cast<__nv_bfloat16*>(out), lse);
 }
 

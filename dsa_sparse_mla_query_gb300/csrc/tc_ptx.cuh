@@ -90,9 +90,19 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
     return ok != 0;
 }
 
+// The device status of a wait that gave up names it: DSA_ERR_TIMEOUT in bits
+// 0-7, the kernel's tag (the word after its abort flag, set at start) in bits
+// 8-15, and the barrier's shared-memory offset / 8 in bits 16-30 (kLoopSite:
+// a kernel's own issue loop, which polls several barriers).
+constexpr uint32_t kLoopSite = 0x7FFF;
+__device__ __forceinline__ int32_t timeout_code(volatile int* abort_flag, uint32_t site) {
+    const uint32_t tag = (uint32_t)abort_flag[1] & 0xFFu;
+    return (int32_t)((uint32_t)DSA_ERR_TIMEOUT | (tag << 8) | ((site & 0x7FFFu) << 16));
+}
+
 // Waits for the phase with this parity to complete.  Returns false when the
 // CTA aborts (another role timed out) or this wait times out (then it raises
-// the abort flag and reports DSA_ERR_TIMEOUT).
+// the abort flag and reports DSA_ERR_TIMEOUT with the wait's site).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int32_t* d_status) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -102,7 +112,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
         if (*abort_flag) return false;
         if (clk.expired(kWaitTimeoutNs)) {
             *abort_flag = 1;
-            report(d_status, DSA_ERR_TIMEOUT);
+            report(d_status, timeout_code(abort_flag, smem_u32(bar) >> 3));
             return false;
         }
     }

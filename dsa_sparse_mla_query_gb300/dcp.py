@@ -8,12 +8,13 @@ place into the global top-k, each rank compacts the slots it owns and attends
 over them, and the partial outputs are LSE-combined ("Day 0 support for
 Mistral Large 4", Long context: decode and prefill context parallelism).
 
-Setup builds each rank's view of a workload: its local token counts, the
-local causal bound of every query (the last token it owns at or before the
-query's position) with the query's absolute position for RoPE and SSMax, and
-its cache rows.  When the interleave is a whole number of pages, a rank's
-tokens are whole pages and its page table is a slice of the workload's (no
-copy); otherwise its rows are gathered into contiguous shard caches.  Only
+Setup builds each rank's view of a workload with dsa_dcp_shard_seqs: its
+local token counts, the local causal bound of every query (the last token it
+owns at or before the query's position) with the query's absolute position
+for RoPE and SSMax, and, when the interleave is a whole number of pages, its
+page table (its tokens are then whole pages of the shared caches); otherwise
+its rows are gathered into contiguous shard caches, as a rank that holds only
+its own tokens would have them.  Only
 marshalling and that setup happen here; every step of the layer runs in the
 library's kernels.
 """
@@ -63,42 +64,43 @@ class ShardedLayer:
         self.views: List[RankView] = []
         self.shards = [B.DcpShard(world, r, interleave) for r in range(world)]
         rope_pos = d["q_pos"]  # absolute positions
+        full = B.Seqs(d["ctx_len"], d["q_start"], d["q_pos"], max_ctx=max(lay.ctx_len),
+                      max_q_per_seq=queries_per_seq, num_rows=lay.num_rows, page_table=d.get("page_table"),
+                      page_size=ps, seq_base=d.get("seq_base"))
         for r in range(world):
-            ctx_r, bound_r, rows_r = [], np.zeros(Q, np.int64), []
-            for b, c in enumerate(lay.ctx_len):
-                t = np.arange(c, dtype=np.int64)
-                mine = owner(t, world, interleave) == r
-                ctx_r.append(int(mine.sum()))
-                # local causal bound: tokens owned at or before each query's position, minus one
-                cum = np.cumsum(mine)
-                for qi in np.flatnonzero(q_seq == b):
-                    bound_r[qi] = cum[q_pos[qi]] - 1
-                if not by_pages:
-                    rows_r.append(lay.phys_rows(b)[torch.from_numpy(np.flatnonzero(mine))])
-            if min(ctx_r) < 1 or bound_r.min() < 0:
+            shard = self.shards[r]
+            # the rank's view from the library: local lengths, causal bounds and,
+            # for page-aligned turns, its page table
+            ctx_t = torch.empty(len(lay.ctx_len), dtype=torch.int32, device=device)
+            bound_t = torch.empty(Q, dtype=torch.int32, device=device)
+            lmaxp = (lay.max_pages + world - 1) // world + 1 if by_pages else 0
+            table = torch.empty(len(lay.ctx_len), max(lmaxp, 1), dtype=torch.int32, device=device) if by_pages else None
+            status = torch.zeros(1, dtype=torch.int32, device=device)
+            lmax = B.dsa_dcp_shard_seqs(full, Q, shard, ctx_t, bound_t, table, lmaxp, status)
+            ctx_r = ctx_t.cpu().tolist()
+            if int(status.item()) != 0 or min(ctx_r) < 1:
                 raise ValueError(f"rank {r} owns no token at or before some query's position; use longer contexts "
                                  "or fewer ranks")
-            ctx_t = torch.tensor(ctx_r, dtype=torch.int32, device=device)
-            bound_t = torch.from_numpy(bound_r.astype(np.int32)).to(device)
             if by_pages:
-                m = interleave // ps  # pages per turn
-                max_pages_r = max((c + ps - 1) // ps for c in ctx_r)
-                pl = np.arange(max_pages_r)
-                gpage = ((pl // m) * world + r) * m + pl % m
-                gpage = np.minimum(gpage, lay.max_pages - 1)  # columns past a sequence's pages are never read
-                table = lay.page_table[:, torch.from_numpy(gpage)].contiguous().to(device)
-                seqs = B.Seqs(ctx_t, d["q_start"], bound_t, max_ctx=max(ctx_r), max_q_per_seq=queries_per_seq,
+                seqs = B.Seqs(ctx_t, d["q_start"], bound_t, max_ctx=lmax, max_q_per_seq=queries_per_seq,
                               num_rows=lay.num_rows, page_table=table, page_size=ps, q_rope_pos=rope_pos)
-                view = RankView(seqs, d["k_idx"], d.get("k_scale"), d["latent"], d.get("latent2"), max(ctx_r))
+                view = RankView(seqs, d["k_idx"], d.get("k_scale"), d["latent"], d.get("latent2"), lmax)
             else:
+                # a contiguous shard cache of the rank's own rows (what a rank
+                # holds in a real deployment; here gathered from the full cache)
+                rows_r = []
+                for b, c in enumerate(lay.ctx_len):
+                    t = np.arange(c, dtype=np.int64)
+                    mine = owner(t, world, interleave) == r
+                    rows_r.append(lay.phys_rows(b)[torch.from_numpy(np.flatnonzero(mine))])
                 rows = torch.cat(rows_r).to(device)
                 base = torch.tensor(np.concatenate([[0], np.cumsum(ctx_r)[:-1]]), dtype=torch.int64, device=device)
-                seqs = B.Seqs(ctx_t, d["q_start"], bound_t, max_ctx=max(ctx_r), max_q_per_seq=queries_per_seq,
+                seqs = B.Seqs(ctx_t, d["q_start"], bound_t, max_ctx=lmax, max_q_per_seq=queries_per_seq,
                               num_rows=int(rows.shape[0]), seq_base=base, q_rope_pos=rope_pos)
                 ks = d["k_scale"].index_select(0, rows) if self.k_fp8 else None
                 lat2 = d["latent2"].index_select(0, rows) if self.shared else None
                 view = RankView(seqs, d["k_idx"].index_select(0, rows), ks, d["latent"].index_select(0, rows), lat2,
-                                max(ctx_r))
+                                lmax)
             view.bound = bound_t
             self.views.append(view)
         # buffers

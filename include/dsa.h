@@ -40,7 +40,11 @@
  *     row outside the cache, an out-of-range selected index, a malformed
  *     q_start) is written to *d_status (device int32; first error wins, the
  *     caller clears it) and the affected work item is skipped.  No kernel traps
- *     or asserts.
+ *     or asserts.  The status code is in bits 0-7; for DSA_ERR_TIMEOUT (a
+ *     bounded in-kernel wait that gave up after 1 s) bits 8-15 name the kernel
+ *     (1 indexer scan, 2 attention, 3 attention over fp8_ds_mla) and bits
+ *     16-30 the wait (its mbarrier's shared-memory offset / 8, or 0x7FFF for
+ *     the attention's issue loop).
  *   - Indices are logical token positions within a sequence.  The page table or
  *     seq_base maps them to physical cache rows.
  */
@@ -298,6 +302,27 @@ dsa_status dsa_topk_compact(const int32_t* idx, const int32_t* topk_len, int32_t
                             const dsa_dcp_shard* shard, int32_t* local_idx, int32_t* local_len, int32_t* d_status,
                             cudaStream_t stream);
 
+/* One rank's view of the sequences, for its calls on its own shard (the
+ * shard's tokens at local positions, by the ownership rule above):
+ *   local_ctx_len int32 [B]: the tokens the rank owns of each sequence;
+ *   local_q_pos   int32 [num_q]: each query's local causal bound, the number
+ *                 of tokens the rank owns at or before the query's position
+ *                 minus one (-1 and DSA_ERR_BAD_INPUT when it owns none);
+ *   local_page_table int32 [B, local_max_pages] or NULL: the rank's pages in
+ *                 local order (-1 past the table); needs seqs->page_table and
+ *                 an interleave that is a whole number of pages;
+ *   local_max_ctx (host out): the most tokens the rank owns of a sequence of
+ *                 max_ctx tokens.
+ * The rank's dsa_seqs is then seqs with max_ctx = *local_max_ctx, ctx_len =
+ * local_ctx_len, q_pos = local_q_pos, q_rope_pos = seqs->q_pos, and either
+ * page_table = local_page_table with max_pages = local_max_pages, or (a
+ * contiguous shard cache) the shard's own seq_base and num_rows.  The same
+ * positions are what dsa_topk_candidates packs and dsa_topk_compact returns. */
+dsa_status dsa_dcp_shard_seqs(const dsa_seqs* seqs, int32_t num_q, const dsa_dcp_shard* shard,
+                              int32_t* local_ctx_len, int32_t* local_q_pos, int32_t* local_page_table,
+                              int32_t local_max_pages, int32_t* local_max_ctx, int32_t* d_status,
+                              cudaStream_t stream);
+
 /* LSE combine of num_parts partial attention results (one per rank), per
  * query and head: lse = ln sum_r exp(lse_r), out = sum_r exp(lse_r - lse) o_r;
  * parts at -inf (empty rows) add nothing; all at -inf give out = 0, lse = -inf.
@@ -362,9 +387,12 @@ dsa_status dsa_decode_layer(const dsa_layer_args* args, const dsa_seqs* seqs, in
  *   results of queries cut between CTAs go to a static device array of
  *   DSA_NOALLOC_SCRATCH_BYTES owned by the library: every GPU that loads the
  *   library holds it until the process exits.  The array holds the partials of
- *   127 CTAs (2 x 66,048 bytes each), so this call spreads the work over at
- *   most 127 CTAs where sparse_mla_decode takes one per SM (152 on a GB300):
- *   no batch size is refused, large ones run somewhat slower.
+ *   63 CTAs (2 x 131,584 bytes each), so this call spreads the work over at
+ *   most 63 CTAs where sparse_mla_decode takes one per SM (152 on a GB300):
+ *   batches of more than 63 x 2 tiles of 64 slots run slower.  Batches of
+ *   more than 7,938 queries need more CTAs than that (a CTA takes at most
+ *   126 queries) and are refused with DSA_ERR_UNSUPPORTED; nothing is
+ *   enqueued.
  *   The first call on each device looks up the array's device address with
  *   that device current (a runtime query, no allocation); make that first call
  *   before any stream capture on the device.  Every call shares the one array

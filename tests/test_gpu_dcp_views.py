@@ -1,5 +1,5 @@
-"""The host side of the sharded layer (dcp.ShardedLayer), on the CPU: every
-rank's view of a workload against the oracle's ownership rule.  Each rank
+"""Every rank's view of a workload (dsa_dcp_shard_seqs, through
+dcp.ShardedLayer) against the oracle's ownership rule.  Each rank
 holds exactly the tokens it owns, numbered in token order; each query's local
 causal bound is its last owned token at or before its position; a rank's
 local token l reads the same cache row as global token global(l), through a
@@ -15,7 +15,9 @@ from dsa_sparse_mla_query_gb300 import inputs as I
 from dsa_sparse_mla_query_gb300.dcp import ShardedLayer
 import oracle
 
+pytestmark = pytest.mark.gpu
 W = I.WORKLOADS
+DEV = "cuda"
 
 
 def _local_rows(view, b, n):
@@ -23,8 +25,8 @@ def _local_rows(view, b, n):
     s = view.seqs
     j = torch.arange(n, dtype=torch.int64)
     if s.page_table is not None:
-        return s.page_table[b].to(torch.int64)[j // s.page_size] * s.page_size + j % s.page_size
-    return s.seq_base[b] + j
+        return s.page_table[b].cpu().to(torch.int64)[j // s.page_size] * s.page_size + j % s.page_size
+    return s.seq_base[b].cpu() + j
 
 
 @pytest.mark.parametrize("name,world,inter", [
@@ -37,11 +39,11 @@ def test_rank_views_follow_the_ownership_rule(name, world, inter):
         wl = I.scaled(wl, num_seqs=len(ctx), ctx=None, ctx_list=ctx)
     elif name == "specv":
         wl = I.scaled(wl, num_seqs=3, ctx_range=(2100, 3000))
-    d = I.make_inputs(wl, "cpu")
+    d = I.make_inputs(wl, DEV)
     lay = d["layout"]
-    sh = ShardedLayer(d, wl.queries_per_seq, wl.topk, world, inter, device="cpu")
+    sh = ShardedLayer(d, wl.queries_per_seq, wl.topk, world, inter, device=DEV)
     by_pages = lay.page_table is not None and inter % lay.page_size == 0
-    keys = d["k_idx"]
+    keys = d["k_idx"].cpu()
     for r, v in enumerate(sh.views):
         ctx_r = v.seqs.ctx_len.tolist()
         bound = v.bound.tolist()
@@ -55,16 +57,16 @@ def test_rank_views_follow_the_ownership_rule(name, world, inter):
             if by_pages:
                 assert torch.equal(loc, glob_rows), f"rank {r} seq {b}: page slice maps the wrong rows"
             else:
-                assert torch.equal(v.k_idx[loc], keys[glob_rows]), f"rank {r} seq {b}: gathered rows differ"
+                assert torch.equal(v.k_idx.cpu()[loc], keys[glob_rows]), f"rank {r} seq {b}: gathered rows differ"
         for t, (b, pos) in enumerate(zip(lay.q_seq, lay.q_pos)):
             last = max(u for u in range(pos + 1) if oracle.dcp_owner(u, world, inter) == r)
             assert bound[t] == oracle.dcp_local(last, world, inter)
-        assert torch.equal(v.seqs.q_rope_pos, d["q_pos"])
+        assert torch.equal(v.seqs.q_rope_pos.cpu(), d["q_pos"].cpu())
 
 
 def test_a_rank_without_tokens_is_refused():
     """A query before any token of some rank: the view cannot be built."""
     wl = I.scaled(W["tiny"], num_seqs=1, ctx=300, queries_per_seq=1)
-    d = I.make_inputs(wl, "cpu")
+    d = I.make_inputs(wl, DEV)
     with pytest.raises(ValueError, match="owns no token"):
-        ShardedLayer(d, 1, wl.topk, 4, 128, device="cpu")
+        ShardedLayer(d, 1, wl.topk, 4, 128, device=DEV)
