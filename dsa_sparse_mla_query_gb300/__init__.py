@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     DSA_BF16,
     DSA_FP8_DS_MLA,
     DSA_FP8_E4M3_ROWSCALE,
+    DSA_NVFP4,
     DcpShard,
     DsaError,
     Seqs,
@@ -34,10 +35,11 @@ from ._binding import (  # noqa: F401
     load,
     sparse_mla_decode,
     sparse_mla_decode_noalloc,
+    sparse_mla_decode_nvfp4,
     version,
 )
 
-__all__ = ["Seqs", "DsaError", "dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode", "sparse_mla_decode_noalloc",
+__all__ = ["Seqs", "DsaError", "dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode", "sparse_mla_decode_noalloc", "sparse_mla_decode_nvfp4",
            "dsa_decode_layer", "dsa_decode_layer_launches", "dsa_decode_layer_launches_for", "dsa_index_k_insert", "dsa_latent_insert", "dsa_mla_q_prep",
            "DcpShard", "dsa_topk_candidates", "dsa_topk_merge", "dsa_topk_compact", "dsa_lse_combine",
            "dsa_block_topk", "dsa_dcp_shard_seqs",

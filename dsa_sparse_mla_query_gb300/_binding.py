@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libdsa.so")
 
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA = 0, 1, 2, 3
 DSA_ERR_WORKSPACE, DSA_ERR_TIMEOUT, DSA_ERR_BAD_INPUT = 4, 5, 6
-DSA_BF16, DSA_FP8_E4M3_ROWSCALE, DSA_FP8_DS_MLA = 0, 1, 2
+DSA_BF16, DSA_FP8_E4M3_ROWSCALE, DSA_FP8_DS_MLA, DSA_NVFP4 = 0, 1, 2, 3
 EXPORTS = ("dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode", "dsa_decode_layer",
            "dsa_decode_layer_launches", "dsa_decode_layer_launches_for", "sparse_mla_decode_noalloc",
            "dsa_last_error_string", "dsa_status_string", "dsa_version")
@@ -50,7 +50,8 @@ class DsaLayerArgsC(ctypes.Structure):
                 ("k", ctypes.c_int32), ("select_block", ctypes.c_int32), ("idx", ctypes.c_void_p),
                 ("topk_len", ctypes.c_void_p), ("q_mla", ctypes.c_void_p), ("latent", ctypes.c_void_p),
                 ("latent_dtype", ctypes.c_int), ("sm_scale", ctypes.c_float), ("out", ctypes.c_void_p),
-                ("lse", ctypes.c_void_p), ("events", ctypes.c_void_p)]
+                ("lse", ctypes.c_void_p), ("events", ctypes.c_void_p), ("latent_scales", ctypes.c_void_p),
+                ("latent_global", ctypes.c_float), ("k_global", ctypes.c_float), ("k_block_scales", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -76,6 +77,9 @@ def load(path: str = LIB_PATH):
         L.dsa_decode_layer.argtypes = [ctypes.POINTER(DsaLayerArgsC), S, I32, P, SZ, P, P]
         L.sparse_mla_decode_noalloc.argtypes = [P, P, ctypes.c_int, S, I32, P, P, I32, ctypes.c_float, P, P, P, P]
         L.sparse_mla_decode_noalloc.restype = ctypes.c_int
+        L.sparse_mla_decode_nvfp4.argtypes = [P, P, P, ctypes.c_float, S, I32, P, P, I32, ctypes.c_float, P, P, P, SZ,
+                                              P, P]
+        L.sparse_mla_decode_nvfp4.restype = ctypes.c_int
         L.dsa_decode_layer_launches.argtypes = [S, I32, I32, I32, ctypes.c_int]
         L.dsa_decode_layer_launches_for.argtypes = [ctypes.POINTER(DsaLayerArgsC), S, I32]
         L.dsa_decode_layer_launches_for.restype = ctypes.c_int32
@@ -172,6 +176,15 @@ def sparse_mla_decode(q, latent, latent_dtype: int, seqs: Seqs, num_q: int, idx,
     _check(load().sparse_mla_decode(_p(q), _p(latent), latent_dtype, ctypes.byref(sc), num_q, _p(idx), _p(topk_len),
                                     k, float(sm_scale), _p(out), _p(lse), _p(workspace), workspace_bytes,
                                     _p(d_status), _stream(stream)))
+
+
+def sparse_mla_decode_nvfp4(q, codes, block_scales, g: float, seqs: Seqs, num_q: int, idx, topk_len, k: int,
+                            sm_scale: float, out, lse=None, workspace=None, workspace_bytes: int = 0, d_status=None,
+                            stream=None):
+    sc = seqs.c()
+    _check(load().sparse_mla_decode_nvfp4(_p(q), _p(codes), _p(block_scales), float(g), ctypes.byref(sc), num_q,
+                                          _p(idx), _p(topk_len), k, float(sm_scale), _p(out), _p(lse), _p(workspace),
+                                          workspace_bytes, _p(d_status), _stream(stream)))
 
 
 def sparse_mla_decode_noalloc(q, latent, latent_dtype: int, seqs: Seqs, num_q: int, idx, topk_len, k: int,

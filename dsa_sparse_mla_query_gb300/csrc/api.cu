@@ -122,7 +122,7 @@ Workspace carve_workspace(void* base, const dsa_seqs& s, int num_q, int k) {
     p += up256((size_t)num_q * kQprepBytes);
     w.wprep = reinterpret_cast<float*>(p);
     p += up256((size_t)num_q * kIH * 4);
-    w.mla_part = p;
+    w.mla_part = reinterpret_cast<float*>(p);
     p += up256(mla_part_bytes(nq, kk));
     w.mla_ml = reinterpret_cast<float*>(p);
     p += up256(mla_ml_bytes(nq, kk));
@@ -491,11 +491,17 @@ dsa_status dsa_block_topk(const float* scores, int64_t ld, const dsa_seqs* seqs,
 }
 
 static void check_mla_args(Check& c, const void* q, const void* latent, dsa_dtype latent_dtype, const int32_t* idx,
-                           const int32_t* topk_len, int32_t k, float sm_scale, const void* out, const float* lse) {
+                           const int32_t* topk_len, int32_t k, float sm_scale, const void* out, const float* lse,
+                           const void* lat_scales = nullptr, float lat_global = 0.f) {
     c.ptr(q, "q");
     c.ptr(latent, "latent");
-    c.need(latent_dtype == DSA_BF16 || latent_dtype == DSA_FP8_DS_MLA, DSA_ERR_UNSUPPORTED,
-           "latent dtype %d is neither DSA_BF16 nor DSA_FP8_DS_MLA", (int)latent_dtype);
+    c.need(latent_dtype == DSA_BF16 || latent_dtype == DSA_FP8_DS_MLA || latent_dtype == DSA_NVFP4,
+           DSA_ERR_UNSUPPORTED, "latent dtype %d is not DSA_BF16, DSA_FP8_DS_MLA or DSA_NVFP4", (int)latent_dtype);
+    if (latent_dtype == DSA_NVFP4) {
+        c.ptr(lat_scales, "NVFP4 latent block scales", 4);
+        c.need(lat_global > 0.f && lat_global < 1e30f, DSA_ERR_INVALID_ARG,
+               "NVFP4 latent tensor scale must be positive and finite");
+    }
     c.ptr(idx, "idx", 4);
     c.ptr(topk_len, "topk_len", 4);
     c.need(k >= 1 && k <= DSA_MAX_TOPK, DSA_ERR_UNSUPPORTED, "k %d outside [1, %d]", k, DSA_MAX_TOPK);
@@ -510,6 +516,7 @@ dsa_status sparse_mla_decode(const void* q, const void* latent, dsa_dtype latent
                              cudaStream_t stream) {
     Check c;
     check_seqs(c, seqs, num_q);
+    c.need(latent_dtype != DSA_NVFP4, DSA_ERR_UNSUPPORTED, "an NVFP4 latent cache takes sparse_mla_decode_nvfp4");
     check_mla_args(c, q, latent, latent_dtype, idx, topk_len, k, sm_scale, out, lse);
     check_workspace(c, seqs, num_q, k, workspace, workspace_bytes);
     dsa_status st = c.done();
@@ -540,7 +547,24 @@ static void check_layer(Check& c, const dsa_layer_args* a, const dsa_seqs* seqs,
         check_index_args(c, a->q_idx, a->w, a->ssmax_s, a->ssmax_b, a->inv_freq, a->k_idx, a->k_scale, a->k_dtype);
         check_block_select(c, seqs, a->k, a->select_block);
     }
-    check_mla_args(c, a->q_mla, a->latent, a->latent_dtype, a->idx, a->topk_len, a->k, a->sm_scale, a->out, a->lse);
+    check_mla_args(c, a->q_mla, a->latent, a->latent_dtype, a->idx, a->topk_len, a->k, a->sm_scale, a->out, a->lse,
+                   a->latent_scales, a->latent_global);
+}
+
+dsa_status sparse_mla_decode_nvfp4(const void* q, const void* codes, const void* block_scales, float g,
+                                   const dsa_seqs* seqs, int32_t num_q, const int32_t* idx, const int32_t* topk_len,
+                                   int32_t k, float sm_scale, void* out, float* lse, void* workspace,
+                                   size_t workspace_bytes, int32_t* d_status, cudaStream_t stream) {
+    Check c;
+    check_seqs(c, seqs, num_q);
+    check_mla_args(c, q, codes, DSA_NVFP4, idx, topk_len, k, sm_scale, out, lse, block_scales, g);
+    check_workspace(c, seqs, num_q, k, workspace, workspace_bytes);
+    dsa_status st = c.done();
+    if (st != DSA_OK || num_q == 0) return st;
+    Workspace ws = carve_workspace(workspace, *seqs, num_q, k);
+    return cuda_status(launch_sparse_mla(q, codes, DSA_NVFP4, *seqs, num_q, idx, topk_len, k, sm_scale, out, lse, ws,
+                                         d_status, stream, kNoCap, block_scales, g),
+                       "sparse_mla_decode_nvfp4 launch");
 }
 
 dsa_status dsa_decode_layer(const dsa_layer_args* a, const dsa_seqs* seqs, int32_t num_q, void* workspace,
@@ -584,7 +608,8 @@ dsa_status dsa_decode_layer(const dsa_layer_args* a, const dsa_seqs* seqs, int32
     }
     if (e == cudaSuccess)
         e = launch_sparse_mla(a->q_mla, a->latent, a->latent_dtype, *seqs, num_q, a->idx, a->topk_len, a->k,
-                              a->sm_scale, a->out, a->lse, ws, d_status, stream);
+                              a->sm_scale, a->out, a->lse, ws, d_status, stream, kNoCap, a->latent_scales,
+                              a->latent_global);
     mark(3);
     return cuda_status(e, "dsa_decode_layer launch");
 }
@@ -606,8 +631,8 @@ int32_t dsa_decode_layer_launches_for(const dsa_layer_args* a, const dsa_seqs* s
     if (!a) return 0;
     check_seqs(c, seqs, num_q);
     c.need(a->k >= 1 && a->k <= DSA_MAX_TOPK, DSA_ERR_UNSUPPORTED, "k %d outside [1, %d]", a->k, DSA_MAX_TOPK);
-    c.need(a->latent_dtype == DSA_BF16 || a->latent_dtype == DSA_FP8_DS_MLA, DSA_ERR_INVALID_ARG, "latent_dtype %d",
-           (int)a->latent_dtype);
+    c.need(a->latent_dtype == DSA_BF16 || a->latent_dtype == DSA_FP8_DS_MLA || a->latent_dtype == DSA_NVFP4,
+           DSA_ERR_INVALID_ARG, "latent_dtype %d", (int)a->latent_dtype);
     if (!a->reuse_idx) check_block_select(c, seqs, a->k, a->select_block);
     if (c.done() != DSA_OK || num_q == 0) return 0;
     return layer_launches(*seqs, num_q, a->k, a->reuse_idx != 0, a->reuse_idx ? 0 : a->select_block);
@@ -654,17 +679,19 @@ extern "C" dsa_status sparse_mla_decode_noalloc(const void* q, const void* laten
                                                 float* lse, int32_t* d_status, cudaStream_t stream) {
     Check c;
     check_seqs(c, seqs, num_q);
+    c.need(latent_dtype != DSA_NVFP4, DSA_ERR_UNSUPPORTED, "no no-workspace entry point for an NVFP4 latent cache");
     check_mla_args(c, q, latent, latent_dtype, idx, topk_len, k, sm_scale, out, lse);
-    // at most as many CTAs as leave their partials room in the static array
-    // (fewer CTAs than sparse_mla_decode on large batches; no size refused)
-    const int max_ctas = mla_max_ctas_for_scratch(DSA_NOALLOC_SCRATCH_BYTES);
+    // the split count is held so that the partials fit the static array
+    // (fewer splits than sparse_mla_decode on some batches; no size refused:
+    // one split or a two-split cluster pair needs no scratch)
+    const size_t cap = DSA_NOALLOC_SCRATCH_BYTES;
     size_t part_bytes = 0, ml_bytes = 0;
     if (c.st == DSA_OK && num_q > 0) {
-        part_bytes = up256(mla_part_bytes(num_q, k, max_ctas));
-        ml_bytes = up256(mla_ml_bytes(num_q, k, max_ctas));
-        c.need(max_ctas >= 1 && part_bytes + ml_bytes <= (size_t)DSA_NOALLOC_SCRATCH_BYTES, DSA_ERR_UNSUPPORTED,
+        part_bytes = up256(mla_part_bytes(num_q, k, cap));
+        ml_bytes = up256(mla_ml_bytes(num_q, k, cap));
+        c.need(part_bytes + ml_bytes <= cap, DSA_ERR_UNSUPPORTED,
                "%d queries need %zu bytes of scratch; the static scratch holds %zu", num_q, part_bytes + ml_bytes,
-               (size_t)DSA_NOALLOC_SCRATCH_BYTES);
+               cap);
     }
     dsa_status st = c.done();
     if (st != DSA_OK || num_q == 0) return st;
@@ -672,9 +699,9 @@ extern "C" dsa_status sparse_mla_decode_noalloc(const void* q, const void* laten
     cudaError_t e = noalloc_scratch(&base);
     if (e != cudaSuccess) return cuda_status(e, "sparse_mla_decode_noalloc scratch address");
     Workspace ws{};
-    ws.mla_part = base;
+    ws.mla_part = reinterpret_cast<float*>(base);
     ws.mla_ml = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(base) + part_bytes);
     return cuda_status(launch_sparse_mla(q, latent, latent_dtype, *seqs, num_q, idx, topk_len, k, sm_scale, out, lse,
-                                         ws, d_status, stream, max_ctas),
+                                         ws, d_status, stream, cap),
                        "sparse_mla_decode_noalloc launch");
 }

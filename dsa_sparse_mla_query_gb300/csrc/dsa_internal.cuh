@@ -21,7 +21,7 @@ constexpr int kMV = DSA_MLA_VDIM;      // 512
 constexpr int kDsRow = DSA_DS_MLA_ROW; // 656
 
 // kernel tags in a timeout's device status (bits 8-15)
-constexpr int kTagIndexer = 1, kTagMla = 2, kTagMlaFp8 = 3;
+constexpr int kTagIndexer = 1, kTagMla = 2, kTagMlaFp8 = 3, kTagMlaNvfp4 = 4;
 
 // ---------------------------------------------------------------------------
 // device-side error reporting: first error wins, never traps
@@ -124,8 +124,8 @@ struct Workspace {
     // carved from the caller's workspace, 256-byte aligned pieces
     void* qprep;      // q' [Q, 32, KP] bf16, or [Q, 3, 32, 128] e4m3 parts (kQprepBytes per query)
     float* wprep;     // w' [Q, 32]
-    void* mla_part;   // partial outputs [2 x CTAs, 64, 512] fp32 (normalised)
-    float* mla_ml;    // their (max, sum) [2 x CTAs, 64, 2]
+    float* mla_part;  // O partials [Q, splits, 64, 512]
+    float* mla_ml;    // (m, l) partials [Q, splits, 64, 2]
     float* scores;    // [Q, ld] for dsa_decode_layer
     int64_t scores_ld;
     // top-k of rows longer than 32,768 keys (null otherwise)
@@ -145,17 +145,14 @@ inline bool topk_long_rows(int max_ctx) { return max_ctx > 32768; }
 inline int topk_chunks(int max_ctx) { return (max_ctx + kLongChunk - 1) / kLongChunk; }
 inline bool topk_chunked(int max_ctx) { return topk_long_rows(max_ctx) && topk_chunks(max_ctx) <= kLongMaxChunks; }
 
-// The attention spreads every query's 64-slot tiles evenly over at most this
-// many CTAs (one per SM of a GB300; fewer on a device with fewer SMs).
-constexpr int kMlaMaxCtas = 152;
-// bytes of the partial outputs (and their (max, sum) pairs) of the pieces of
-// queries cut between CTAs, for at most max_ctas CTAs
-size_t mla_part_bytes(int num_q, int k, int max_ctas = kMlaMaxCtas);
-size_t mla_ml_bytes(int num_q, int k, int max_ctas = kMlaMaxCtas);
-// kernels one attention call enqueues (the combine only when a query is cut)
-int mla_launches(int num_q, int k, int max_ctas = kMlaMaxCtas);
-// the most CTAs whose partials fit `bytes` of scratch
-int mla_max_ctas_for_scratch(size_t bytes);
+// The attention's split count per query, and the scratch its partials take
+// (none for one split or a two-split cluster pair), with the partials held to
+// `cap` bytes (fewer splits otherwise)
+constexpr size_t kNoCap = ~size_t(0);
+int mla_splits(int num_q, int k, size_t cap = kNoCap);
+size_t mla_part_bytes(int num_q, int k, size_t cap = kNoCap);  // fp32 partial outputs
+size_t mla_ml_bytes(int num_q, int k, size_t cap = kNoCap);    // their (max, sum) pairs
+int mla_launches(int num_q, int k, size_t cap = kNoCap);       // kernels one attention call enqueues
 size_t workspace_bytes(const dsa_seqs& s, int num_q, int k, int64_t* scores_ld);
 Workspace carve_workspace(void* base, const dsa_seqs& s, int num_q, int k);
 
@@ -168,6 +165,6 @@ cudaError_t launch_topk(const float* scores, int64_t ld, const dsa_seqs& s, int 
 cudaError_t launch_sparse_mla(const void* q, const void* latent, dsa_dtype latent_dtype, const dsa_seqs& s,
                               int num_q, const int32_t* idx, const int32_t* topk_len, int k, float sm_scale,
                               void* out, float* lse, const Workspace& ws, int32_t* d_status, cudaStream_t stream,
-                              int max_ctas = kMlaMaxCtas);
+                              size_t scratch_cap = kNoCap, const void* lat_scales = nullptr, float lat_global = 1.f);
 
 }  // namespace dsa

@@ -82,9 +82,13 @@ typedef enum {
     DSA_BF16 = 0,               /* bf16 rows: index keys [rows,128], latent [rows,576] */
     DSA_FP8_E4M3_ROWSCALE = 1,  /* index keys: [rows,128] OCP e4m3 codes + k_scale fp32 [rows]
                                    (132 B/token, [vLLM-ML4] DSA indexer on AITER) */
-    DSA_FP8_DS_MLA = 2          /* latent: [rows,656] bytes = [0,512) e4m3 latent codes,
+    DSA_FP8_DS_MLA = 2,         /* latent: [rows,656] bytes = [0,512) e4m3 latent codes,
                                    [512,528) 4 fp32 scales (one per 128 latent dims),
                                    [528,656) 64 bf16 RoPE dims ([vLLM-ML4] FP8 latent cache) */
+    DSA_NVFP4 = 3               /* latent: codes [rows,288] bytes (576 E2M1 values, value 2i in the low
+                                   nibble of byte i) + E4M3 block scales [rows,36] (one per 16 values) +
+                                   one fp32 tensor scale g: value = g * scale * code, 4.5 bits/value
+                                   ("vLLM adds NVFP4 serving for MiniMax M3.1 Flash": NVFP4 caches) */
 } dsa_dtype;
 
 /* Where tokens live.  Sequence b holds ctx_len[b] tokens; its queries are rows
@@ -184,6 +188,19 @@ dsa_status sparse_mla_decode(const void* q, const void* latent, dsa_dtype latent
                              int32_t num_q, const int32_t* idx, const int32_t* topk_len, int32_t k, float sm_scale,
                              void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* d_status,
                              cudaStream_t stream);
+
+/* sparse_mla_decode over an NVFP4 latent cache (DSA_NVFP4: codes [rows,288],
+ * block_scales [rows,36], tensor scale g > 0; "vLLM adds NVFP4 serving for
+ * MiniMax M3.1 Flash": NVFP4 caches, converted inside the decode kernel).
+ * The gather decodes each row to f16, exactly (an E2M1 value times its E4M3
+ * block scale), and g folds into the score scale and the output:
+ * s_i = sm_scale g q . c~_i, out = g sum_i p_i c~_i[0:512].  Arguments and
+ * results otherwise as sparse_mla_decode.  Alignment: codes 16 bytes,
+ * block_scales 4 bytes. */
+dsa_status sparse_mla_decode_nvfp4(const void* q, const void* codes, const void* block_scales, float g,
+                                   const dsa_seqs* seqs, int32_t num_q, const int32_t* idx, const int32_t* topk_len,
+                                   int32_t k, float sm_scale, void* out, float* lse, void* workspace,
+                                   size_t workspace_bytes, int32_t* d_status, cudaStream_t stream);
 
 /* ---- the cache-write side: the kernels on either side of the decode path ----
  * Each writes new tokens' rows at the physical rows slot[i] (slot < 0: the
@@ -371,6 +388,14 @@ typedef struct {
        after the indexer, the top-k and the attention (a shared-indexer layer
        records the first three back to back), for per-stage timing */
     cudaEvent_t* events;
+    /* latent_dtype == DSA_NVFP4: E4M3 block scales [rows,36] and the tensor
+       scale of the latent cache (latent holds the codes [rows,288]) */
+    const void* latent_scales;
+    float latent_global;
+    /* k_dtype == DSA_NVFP4: E4M3 block scales [rows,8] and the tensor scale of
+       the index keys (k_idx holds the codes [rows,64]) */
+    float k_global;
+    const void* k_block_scales;
 } dsa_layer_args;
 
 dsa_status dsa_decode_layer(const dsa_layer_args* args, const dsa_seqs* seqs, int32_t num_q, void* workspace,
@@ -384,15 +409,12 @@ dsa_status dsa_decode_layer(const dsa_layer_args* args, const dsa_seqs* seqs, in
  * have no counterpart of this call; it is a deployment convenience.
  *   Same arguments, semantics and results (within rounding: the split of the
  *   work may differ) as sparse_mla_decode, minus the workspace.  The partial
- *   results of queries cut between CTAs go to a static device array of
+ *   results of a query's splits go to a static device array of
  *   DSA_NOALLOC_SCRATCH_BYTES owned by the library: every GPU that loads the
- *   library holds it until the process exits.  The array holds the partials of
- *   63 CTAs (2 x 131,584 bytes each), so this call spreads the work over at
- *   most 63 CTAs where sparse_mla_decode takes one per SM (152 on a GB300):
- *   batches of more than 63 x 2 tiles of 64 slots run slower.  Batches of
- *   more than 7,938 queries need more CTAs than that (a CTA takes at most
- *   126 queries) and are refused with DSA_ERR_UNSUPPORTED; nothing is
- *   enqueued.
+ *   library holds it until the process exits.  Where sparse_mla_decode's
+ *   splits would need more than the array holds, this call takes fewer splits
+ *   per query (down to two, which combine on chip and need none), so no batch
+ *   size is refused; such batches run somewhat slower.
  *   The first call on each device looks up the array's device address with
  *   that device current (a runtime query, no allocation); make that first call
  *   before any stream capture on the device.  Every call shares the one array

@@ -156,19 +156,17 @@ def test_small_k(k):
     _check_workload(d, wl, list(range(wl.num_queries)))
 
 
-def test_queries_cut_between_ctas():
-    """70 queries of 32 tiles over the SMs' equal ranges: most queries are cut
-    between two or three CTAs whose partials the combine kernel merges.
-    Contexts leave pieces empty (1, 500, 1000 keys: fewer live tiles than
-    pieces), end on a tile boundary (1024, 1025) or fill every piece (2048,
-    2049, 3000, 6000)."""
+def test_two_splits_combine_in_cluster():
+    """70 queries give two splits per query, whose pair combines in-kernel
+    (thread-block cluster); contexts leave the second split empty (1, 500,
+    1000 keys), split at the boundary (1024, 1025) or fill both (2048, 2049,
+    3000, 6000)."""
     ctx_cycle = (1, 500, 1000, 1024, 1025, 2048, 2049, 3000, 6000, 4163)
     ctx_list = tuple(ctx_cycle[i % len(ctx_cycle)] for i in range(70))
     wl = I.scaled(W["tiny"], num_seqs=70, ctx=None, ctx_list=ctx_list, queries_per_seq=1)
     d, _ = _inputs_cpu_then_gpu(wl)
     step = DecodeStep(d, wl.queries_per_seq, wl.topk)
-    # query prep, scores, top-k, attention and its combine
-    assert step.launches_per_step() == 5
+    assert step.launches_per_step() == 4, "bf16 with two splits runs without a combine launch"
     _check_workload(d, wl, list(range(wl.num_queries)))
 
 
