@@ -42,7 +42,8 @@
  *     caller clears it) and the affected work item is skipped.  No kernel traps
  *     or asserts.  The status code is in bits 0-7; for DSA_ERR_TIMEOUT (a
  *     bounded in-kernel wait that gave up after 1 s) bits 8-15 name the kernel
- *     (1 indexer scan, 2 attention, 3 attention over fp8_ds_mla) and bits
+ *     (1 indexer scan, 2 attention, 3 attention over fp8_ds_mla, 4 attention
+ *     over NVFP4 latent rows) and bits
  *     16-30 the wait (its mbarrier's shared-memory offset / 8, or 0x7FFF for
  *     the attention's issue loop).
  *   - Indices are logical token positions within a sequence.  The page table or
