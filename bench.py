@@ -90,11 +90,20 @@ def whole_job_rate(units_per_rank: int, ws: int, ms_per_step: float) -> float:
 # ---------------------------------------------------------------------------
 # algorithmic bytes per launch and per step: each byte a kernel must move at least once
 def index_row_bytes(wl):
-    return 132 if wl.index_fp8 else 256
+    return 132 if wl.index_fp8 else 72 if wl.index_nvfp4 else 256
 
 
 def latent_row_bytes(wl):
-    return 656 if wl.latent_fp8 else 1152
+    return 656 if wl.latent_fp8 else 324 if wl.latent_nvfp4 else 1152
+
+
+def dtype_name(wl) -> str:
+    """The tensor-core input types the path computes in (fp32 accumulation):
+    the indexer's, then the attention's when they differ.  e4m3 keys run as
+    e4m3; NVFP4 keys and fp8 / NVFP4 latent rows are decoded exactly to f16."""
+    idx = "e4m3" if wl.index_fp8 else "f16" if wl.index_nvfp4 else "bf16"
+    att = "f16" if (wl.latent_fp8 or wl.latent_nvfp4) else "bf16"
+    return idx if idx == att else f"{idx}/{att}"
 
 
 def algorithmic_bytes(wl, lay):
@@ -207,7 +216,7 @@ def indexer_traffic(wl_name: str):
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("indexer.cu", "dsa_internal.cuh", "tc_ptx.cuh"):
+    for f in ("indexer.cu", "indexer_nvfp4.cu", "indexer_common.cuh", "dsa_internal.cuh", "tc_ptx.cuh"):
         with open(os.path.join(ROOT, "dsa_sparse_mla_query_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -232,18 +241,39 @@ def oracle_sample(wl, n_queries: int):
         cache = I.make_cache_rows(wl, rows, "cpu", which="index")
         q = I.make_queries(wl, "cpu", t, 1)
         jobs.append(dict(t=t, pos=lay.q_pos[t], ctx=lay.ctx_len[bq], rows=rows, keys=cache["k_idx"],
-                         k_scale=cache.get("k_scale"), q=q, s=s, b=b, inv=inv))
+                         k_scale=cache.get("k_scale"), k_bscale=cache.get("k_bscale"), q=q, s=s, b=b, inv=inv))
     # the latent rows the oracle will select: run its indexer once here
     for j in jobs:
-        olay = oracle.Layout(np.array([j["ctx"]], np.int32), j["ctx"], seq_base=np.zeros(1, np.int64))
-        sc = oracle.index_scores(j["q"]["q_idx"], j["q"]["w"], j["s"], j["b"], j["inv"], np.zeros(1, np.int32),
-                                 np.array([j["pos"]], np.int32), j["keys"], olay, key_scale=j["k_scale"])[0]
+        j["olay"] = oracle.Layout(np.array([j["ctx"]], np.int32), j["ctx"], seq_base=np.zeros(1, np.int64))
+        sc = oracle_scores(j)
         sel, m = select(wl, sc[:j["pos"] + 1])
         j["lat"] = I.make_cache_rows(wl, j["rows"][torch.from_numpy(sel[:m].astype(np.int64))], "cpu",
                                      which="latent")
         j["m"] = m
-        j["olay"] = olay
     return jobs
+
+
+def oracle_scores(job):
+    """The oracle's indexer scores of one sampled query over its context."""
+    import numpy as np
+    import oracle
+    q, pos = job["q"], np.array([job["pos"]], np.int32)
+    if job["k_bscale"] is not None:  # NVFP4 keys
+        return oracle.index_scores_nvfp4(q["q_idx"], q["w"], job["s"], job["b"], job["inv"], np.zeros(1, np.int32),
+                                         pos, job["keys"], job["k_bscale"], I.NVFP4_GLOBAL, job["olay"])[0]
+    return oracle.index_scores(q["q_idx"], q["w"], job["s"], job["b"], job["inv"], np.zeros(1, np.int32), pos,
+                               job["keys"], job["olay"], key_scale=job["k_scale"])[0]
+
+
+def oracle_attention(wl, q, lat, m: int, which: str = "latent"):
+    import numpy as np
+    import oracle
+    mlay = oracle.Layout(np.array([m], np.int32), m, seq_base=np.zeros(1, np.int64))
+    sel = np.arange(m, dtype=np.int32)
+    if wl.latent_nvfp4:
+        return oracle.sparse_mla_nvfp4(q, lat[which], lat["lat_bscale"], I.NVFP4_GLOBAL, mlay, 0, sel, m,
+                                       1.0 / math.sqrt(192.0))
+    return oracle.sparse_mla(q, lat[which], mlay, 0, sel, m, 1.0 / math.sqrt(192.0), fp8=wl.latent_fp8)
 
 
 def select(wl, causal_scores):
@@ -258,16 +288,12 @@ def oracle_run(wl, job):
     """The oracle's whole layer for one query (indexer, top-k, attention)."""
     import numpy as np
     import oracle
-    sc = oracle.index_scores(job["q"]["q_idx"], job["q"]["w"], job["s"], job["b"], job["inv"], np.zeros(1, np.int32),
-                             np.array([job["pos"]], np.int32), job["keys"], job["olay"], key_scale=job["k_scale"])[0]
+    sc = oracle_scores(job)
     sel, m = select(wl, sc[:job["pos"] + 1])
     m = job["m"]
-    mlay = oracle.Layout(np.array([m], np.int32), m, seq_base=np.zeros(1, np.int64))
-    oracle.sparse_mla(job["q"]["q_mla"][0], job["lat"]["latent"], mlay, 0, np.arange(m, dtype=np.int32), m,
-                      1.0 / math.sqrt(192.0), fp8=wl.latent_fp8)
+    oracle_attention(wl, job["q"]["q_mla"][0], job["lat"], m)
     if wl.shared_layer:
-        oracle.sparse_mla(job["q"]["q_mla2"][0], job["lat"]["latent2"], mlay, 0, np.arange(m, dtype=np.int32), m,
-                          1.0 / math.sqrt(192.0), fp8=wl.latent_fp8)
+        oracle_attention(wl, job["q"]["q_mla2"][0], job["lat"], m, "latent2")
 
 
 def oracle_timed(wl, jobs, threads: int) -> float:
@@ -433,7 +459,7 @@ def run_ours(args, wl, ws, rank, local):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": W,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if not wl.index_fp8 else "e4m3/bf16", "data": "synthetic",
+            "dtype": dtype_name(wl), "data": "synthetic",
             "config": {"workload": wl.describe(), "queries": wl.num_queries, "global_batch": ws * wl.num_queries,
                        "l2": "inputs larger than L2 (index keys %.0f MB read every step, latent cache %.0f MB); "
                              "two query sets alternate between steps, so consecutive steps gather different "
@@ -577,7 +603,7 @@ def run_dcp(args, wl, ws, rank, local):
         print(json.dumps({
             "metric": METRIC, "value": whole_job_rate(wl.num_queries, ws, ms_step), "unit": UNIT, "n_gpus": ws,
             "steps": K, "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16" if not wl.index_fp8 else "e4m3/bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": dtype_name(wl), "data": "synthetic",
             "config": {"workload": wl.describe(), "queries": wl.num_queries,
                        "dcp": f"sharded by token over {R} ranks in turns of {inter} tokens, every shard on this GPU",
                        "l2": "inputs larger than L2",
@@ -754,6 +780,8 @@ def main():
         wl = I.WORKLOADS[args.workload]
         if args.seqs:
             wl = I.scaled(wl, num_seqs=args.seqs)
+        if args.dcp and (wl.index_nvfp4 or wl.latent_nvfp4):
+            raise SystemExit("--dcp shards bf16 and e4m3 caches; the NVFP4 workloads run unsharded")
     if args.impl == "reference":
         # the oracle on the host cores: rank 0 alone runs and prints
         if ws > 1 and rank != 0:

@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     dsa_dcp_shard_seqs,
     dsa_index_k_insert,
     dsa_index_scores,
+    dsa_index_scores_nvfp4,
     dsa_latent_insert,
     dsa_lse_combine,
     dsa_mla_q_prep,
@@ -39,7 +40,7 @@ from ._binding import (  # noqa: F401
     version,
 )
 
-__all__ = ["Seqs", "DsaError", "dsa_workspace_size", "dsa_index_scores", "dsa_topk", "sparse_mla_decode", "sparse_mla_decode_noalloc", "sparse_mla_decode_nvfp4",
+__all__ = ["Seqs", "DsaError", "dsa_workspace_size", "dsa_index_scores", "dsa_index_scores_nvfp4", "dsa_topk", "sparse_mla_decode", "sparse_mla_decode_noalloc", "sparse_mla_decode_nvfp4",
            "dsa_decode_layer", "dsa_decode_layer_launches", "dsa_decode_layer_launches_for", "dsa_index_k_insert", "dsa_latent_insert", "dsa_mla_q_prep",
            "DcpShard", "dsa_topk_candidates", "dsa_topk_merge", "dsa_topk_compact", "dsa_lse_combine",
            "dsa_block_topk", "dsa_dcp_shard_seqs",

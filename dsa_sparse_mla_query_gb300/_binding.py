@@ -72,6 +72,8 @@ def load(path: str = LIB_PATH):
         S = ctypes.POINTER(DsaSeqsC)
         L.dsa_workspace_size.argtypes = [S, I32, I32, ctypes.POINTER(SZ)]
         L.dsa_index_scores.argtypes = [P, P, P, P, P, P, P, ctypes.c_int, S, I32, P, I64, P, SZ, P, P]
+        L.dsa_index_scores_nvfp4.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, S, I32, P, I64, P, SZ, P, P]
+        L.dsa_index_scores_nvfp4.restype = ctypes.c_int
         L.dsa_topk.argtypes = [P, I64, S, I32, I32, P, P, P, SZ, P, P]
         L.sparse_mla_decode.argtypes = [P, P, ctypes.c_int, S, I32, P, P, I32, ctypes.c_float, P, P, P, SZ, P, P]
         L.dsa_decode_layer.argtypes = [ctypes.POINTER(DsaLayerArgsC), S, I32, P, SZ, P, P]
@@ -161,6 +163,15 @@ def dsa_index_scores(q_idx, w, ssmax_s, ssmax_b, inv_freq, k_idx, k_scale, k_dty
     _check(load().dsa_index_scores(_p(q_idx), _p(w), _p(ssmax_s), _p(ssmax_b), _p(inv_freq), _p(k_idx), _p(k_scale),
                                    k_dtype, ctypes.byref(sc), num_q, _p(scores), ld, _p(workspace), workspace_bytes,
                                    _p(d_status), _stream(stream)))
+
+
+def dsa_index_scores_nvfp4(q_idx, w, ssmax_s, ssmax_b, inv_freq, k_codes, k_block_scales, k_global: float,
+                           seqs: Seqs, num_q: int, scores, ld: int, workspace, workspace_bytes: int, d_status=None,
+                           stream=None):
+    sc = seqs.c()
+    _check(load().dsa_index_scores_nvfp4(_p(q_idx), _p(w), _p(ssmax_s), _p(ssmax_b), _p(inv_freq), _p(k_codes),
+                                         _p(k_block_scales), float(k_global), ctypes.byref(sc), num_q, _p(scores), ld,
+                                         _p(workspace), workspace_bytes, _p(d_status), _stream(stream)))
 
 
 def dsa_topk(scores, ld: int, seqs: Seqs, num_q: int, k: int, idx, topk_len, workspace=None,

@@ -19,7 +19,7 @@ ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libdsa.so")
 BUILD_DIR = os.path.join(ROOT, "_build", platform.machine())
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "indexer.cu", "topk.cu", "mla.cu", "cache_write.cu", "dcp.cu", "block_topk.cu"]
+SOURCES = ["api.cu", "indexer.cu", "indexer_nvfp4.cu", "topk.cu", "mla.cu", "cache_write.cu", "dcp.cu", "block_topk.cu"]
 
 
 def nvcc() -> str:

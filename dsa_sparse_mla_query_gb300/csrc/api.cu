@@ -226,25 +226,33 @@ dsa_status dsa_workspace_size(const dsa_seqs* seqs, int32_t num_q, int32_t k, si
 }
 
 static void check_index_args(Check& c, const void* q_idx, const float* w, const float* ssmax_s, const float* ssmax_b,
-                             const float* inv_freq, const void* k_idx, const float* k_scale, dsa_dtype k_dtype) {
+                             const float* inv_freq, const void* k_idx, const float* k_scale, dsa_dtype k_dtype,
+                             const void* k_block_scales = nullptr, float k_global = 0.f) {
     c.ptr(q_idx, "q_idx");
     c.ptr(w, "w", 4);
     c.ptr(ssmax_s, "ssmax_s", 4);
     c.ptr(ssmax_b, "ssmax_b", 4);
     if (inv_freq) c.ptr(inv_freq, "inv_freq", 4);
     c.ptr(k_idx, "k_idx");
-    c.need(k_dtype == DSA_BF16 || k_dtype == DSA_FP8_E4M3_ROWSCALE, DSA_ERR_UNSUPPORTED,
-           "index key dtype %d is neither DSA_BF16 nor DSA_FP8_E4M3_ROWSCALE", (int)k_dtype);
+    c.need(k_dtype == DSA_BF16 || k_dtype == DSA_FP8_E4M3_ROWSCALE || k_dtype == DSA_NVFP4, DSA_ERR_UNSUPPORTED,
+           "index key dtype %d is not DSA_BF16, DSA_FP8_E4M3_ROWSCALE or DSA_NVFP4", (int)k_dtype);
     if (k_dtype == DSA_FP8_E4M3_ROWSCALE) c.ptr(k_scale, "k_scale", 4);
+    if (k_dtype == DSA_NVFP4) {
+        c.ptr(k_block_scales, "NVFP4 index key block scales", 8);
+        c.need(k_global > 0.f && k_global < INFINITY, DSA_ERR_INVALID_ARG,
+               "NVFP4 index key tensor scale must be positive and finite");
+    }
 }
 
-dsa_status dsa_index_scores(const void* q_idx, const float* w, const float* ssmax_s, const float* ssmax_b,
-                            const float* inv_freq, const void* k_idx, const float* k_scale, dsa_dtype k_dtype,
-                            const dsa_seqs* seqs, int32_t num_q, float* scores, int64_t ld, void* workspace,
-                            size_t workspace_bytes, int32_t* d_status, cudaStream_t stream) {
+static dsa_status index_scores_common(const char* name, const void* q_idx, const float* w, const float* ssmax_s,
+                                      const float* ssmax_b, const float* inv_freq, const void* k_idx,
+                                      const float* k_scale, dsa_dtype k_dtype, const void* k_block_scales,
+                                      float k_global, const dsa_seqs* seqs, int32_t num_q, float* scores, int64_t ld,
+                                      void* workspace, size_t workspace_bytes, int32_t* d_status,
+                                      cudaStream_t stream) {
     Check c;
     check_seqs(c, seqs, num_q);
-    check_index_args(c, q_idx, w, ssmax_s, ssmax_b, inv_freq, k_idx, k_scale, k_dtype);
+    check_index_args(c, q_idx, w, ssmax_s, ssmax_b, inv_freq, k_idx, k_scale, k_dtype, k_block_scales, k_global);
     c.ptr(scores, "scores");
     if (seqs) c.need(ld >= seqs->max_ctx && ld % 4 == 0, DSA_ERR_INVALID_ARG, "ld %lld must be >= max_ctx and a multiple of 4", (long long)ld);
     check_workspace(c, seqs, num_q, 1, workspace, workspace_bytes);
@@ -252,10 +260,33 @@ dsa_status dsa_index_scores(const void* q_idx, const float* w, const float* ssma
     if (st != DSA_OK || num_q == 0) return st;
     Workspace ws = carve_workspace(workspace, *seqs, num_q, 1);
     return cuda_status(launch_index_scores(q_idx, w, ssmax_s, ssmax_b, inv_freq, k_idx, k_scale, k_dtype, *seqs,
-                                           num_q, scores, ld, nullptr, 0, ws, d_status, stream),
-                       "dsa_index_scores launch");
+                                           num_q, scores, ld, nullptr, 0, ws, d_status, stream, k_block_scales,
+                                           k_global),
+                       name);
 }
 
+dsa_status dsa_index_scores(const void* q_idx, const float* w, const float* ssmax_s, const float* ssmax_b,
+                            const float* inv_freq, const void* k_idx, const float* k_scale, dsa_dtype k_dtype,
+                            const dsa_seqs* seqs, int32_t num_q, float* scores, int64_t ld, void* workspace,
+                            size_t workspace_bytes, int32_t* d_status, cudaStream_t stream) {
+    if (k_dtype == DSA_NVFP4) {
+        Check c;
+        c.need(false, DSA_ERR_UNSUPPORTED, "NVFP4 index keys take dsa_index_scores_nvfp4");
+        return c.done();
+    }
+    return index_scores_common("dsa_index_scores launch", q_idx, w, ssmax_s, ssmax_b, inv_freq, k_idx, k_scale,
+                               k_dtype, nullptr, 0.f, seqs, num_q, scores, ld, workspace, workspace_bytes, d_status,
+                               stream);
+}
+
+dsa_status dsa_index_scores_nvfp4(const void* q_idx, const float* w, const float* ssmax_s, const float* ssmax_b,
+                                  const float* inv_freq, const void* k_codes, const void* k_block_scales,
+                                  float k_global, const dsa_seqs* seqs, int32_t num_q, float* scores, int64_t ld,
+                                  void* workspace, size_t workspace_bytes, int32_t* d_status, cudaStream_t stream) {
+    return index_scores_common("dsa_index_scores_nvfp4 launch", q_idx, w, ssmax_s, ssmax_b, inv_freq, k_codes,
+                               nullptr, DSA_NVFP4, k_block_scales, k_global, seqs, num_q, scores, ld, workspace,
+                               workspace_bytes, d_status, stream);
+}
 
 dsa_status dsa_index_k_insert(const void* x, const float* ln_gamma, const float* ln_beta, float ln_eps,
                               const int32_t* pos, const float* inv_freq, const int64_t* slot, int32_t n,
@@ -544,7 +575,8 @@ static void check_block_select(Check& c, const dsa_seqs* seqs, int32_t k, int32_
 static void check_layer(Check& c, const dsa_layer_args* a, const dsa_seqs* seqs, int32_t num_q) {
     check_seqs(c, seqs, num_q);
     if (!a->reuse_idx) {
-        check_index_args(c, a->q_idx, a->w, a->ssmax_s, a->ssmax_b, a->inv_freq, a->k_idx, a->k_scale, a->k_dtype);
+        check_index_args(c, a->q_idx, a->w, a->ssmax_s, a->ssmax_b, a->inv_freq, a->k_idx, a->k_scale, a->k_dtype,
+                         a->k_block_scales, a->k_global);
         check_block_select(c, seqs, a->k, a->select_block);
     }
     check_mla_args(c, a->q_mla, a->latent, a->latent_dtype, a->idx, a->topk_len, a->k, a->sm_scale, a->out, a->lse,
@@ -591,7 +623,8 @@ dsa_status dsa_decode_layer(const dsa_layer_args* a, const dsa_seqs* seqs, int32
         if (e == cudaSuccess)
             e = launch_index_scores(a->q_idx, a->w, a->ssmax_s, a->ssmax_b, a->inv_freq, a->k_idx, a->k_scale,
                                     a->k_dtype, *seqs, num_q, groups ? nullptr : ws.scores, ws.scores_ld,
-                                    groups ? ws.scores : nullptr, ldg, ws, d_status, stream);
+                                    groups ? ws.scores : nullptr, ldg, ws, d_status, stream, a->k_block_scales,
+                                    a->k_global);
         mark(1);
         if (e == cudaSuccess) {
             if (a->select_block > 0)

@@ -21,7 +21,7 @@ constexpr int kMV = DSA_MLA_VDIM;      // 512
 constexpr int kDsRow = DSA_DS_MLA_ROW; // 656
 
 // kernel tags in a timeout's device status (bits 8-15)
-constexpr int kTagIndexer = 1, kTagMla = 2, kTagMlaFp8 = 3, kTagMlaNvfp4 = 4;
+constexpr int kTagIndexer = 1, kTagMla = 2, kTagMlaFp8 = 3, kTagMlaNvfp4 = 4, kTagIndexerNvfp4 = 5;
 
 // ---------------------------------------------------------------------------
 // device-side error reporting: first error wins, never traps
@@ -122,7 +122,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // launchers (host)
 struct Workspace {
     // carved from the caller's workspace, 256-byte aligned pieces
-    void* qprep;      // q' [Q, 32, KP] bf16, or [Q, 3, 32, 128] e4m3 parts (kQprepBytes per query)
+    void* qprep;      // q' [Q, 32, KP] bf16 or f16, or [Q, 3, 32, 128] e4m3 parts (kQprepBytes per query)
     float* wprep;     // w' [Q, 32]
     float* mla_part;  // O partials [Q, splits, 64, 512]
     float* mla_ml;    // (m, l) partials [Q, splits, 64, 2]
@@ -136,7 +136,7 @@ struct Workspace {
     int* tk_above;       // [Q, DSA_MAX_TOPK] positions of the keys above it
 };
 
-constexpr int kQprepBytes = 4 * kIH * kID;  // per query: >= 32 x 192 bf16 and 3 x 32 x 128 e4m3
+constexpr int kQprepBytes = 4 * kIH * kID;  // per query: >= 32 x 192 16-bit values and 3 x 32 x 128 e4m3
 constexpr int kLongChunk = 16384;      // keys per CTA in the long-row top-k
 constexpr int kLongCand = 8192;        // candidate slots per row
 constexpr int kLongMaxChunks = 1024;   // rows up to 16M keys take the chunked path
@@ -159,7 +159,14 @@ Workspace carve_workspace(void* base, const dsa_seqs& s, int num_q, int k);
 cudaError_t launch_index_scores(const void* q_idx, const float* w, const float* ssmax_s, const float* ssmax_b,
                                 const float* inv_freq, const void* k_idx, const float* k_scale, dsa_dtype k_dtype,
                                 const dsa_seqs& s, int num_q, float* scores, int64_t ld, float* gmax, int64_t ldg,
-                                const Workspace& ws, int32_t* d_status, cudaStream_t stream);
+                                const Workspace& ws, int32_t* d_status, cudaStream_t stream,
+                                const void* k_block_scales = nullptr, float k_global = 1.f);
+// NVFP4 index keys: codes [rows, 64], E4M3 block scales [rows, 8], tensor scale k_global
+cudaError_t launch_index_scores_nvfp4(const void* q_idx, const float* w, const float* ssmax_s, const float* ssmax_b,
+                                      const float* inv_freq, const void* k_codes, const void* k_block_scales,
+                                      float k_global, const dsa_seqs& s, int num_q, float* scores, int64_t ld,
+                                      float* gmax, int64_t ldg, const Workspace& ws, int32_t* d_status,
+                                      cudaStream_t stream);
 cudaError_t launch_topk(const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int k, int32_t* idx,
                         int32_t* topk_len, const Workspace& ws, int32_t* d_status, cudaStream_t stream);
 cudaError_t launch_sparse_mla(const void* q, const void* latent, dsa_dtype latent_dtype, const dsa_seqs& s,

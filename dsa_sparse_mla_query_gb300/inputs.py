@@ -30,6 +30,12 @@ top-k 2048, MLA with KV LoRA rank 512 and RoPE dim 64, 64 heads):
                with one fp32 scale per row (132 B/token) and the fp8_ds_mla
                latent row (656 B/token).
 * ``prefill``  1 sequence, 4096 queries at 126976..131071 over 131072 keys.
+* ``block_fp8`` as ``long_fp8``, with block-sparse selection (16 blocks of
+               128 keys, "vLLM adds NVFP4 serving for MiniMax M3.1 Flash",
+               MiniMax Sparse Attention).
+* ``long_nvfp4`` as ``long_fp8``, with NVFP4 caches ("vLLM adds NVFP4
+               serving for MiniMax M3.1 Flash": 4.5 bits per value): index
+               keys of 72 B/token and latent rows of 324 B/token.
 """
 
 from __future__ import annotations
@@ -52,6 +58,11 @@ MLA_ROPE_DIM = 64
 DS_MLA_ROW_BYTES = 656      # 512 e4m3 + 4 fp32 scales + 64 bf16
 FP8_GROUP = 128
 E4M3_MAX = 448.0
+NVFP4_BLOCK = 16
+# Tensor scale of the synthetic NVFP4 caches: their values are N(0, 1), so a
+# block maximum above 8 (probability ~1e-15 per value) is the only case whose
+# E4M3 block scale amax / (6 g) would pass 448 (it saturates there).
+NVFP4_GLOBAL = 8.0 / (6.0 * E4M3_MAX)
 
 # tensor ids of the counter streams
 T_Q_IDX, T_W, T_SSMAX_S, T_SSMAX_B, T_ALPHA = 1, 2, 3, 4, 5
@@ -142,6 +153,29 @@ def quantize_e4m3_groups(v: torch.Tensor, group: int):
     return codes, scale.squeeze(-1)
 
 
+def quantize_nvfp4(v: torch.Tensor, g: float):
+    """NVFP4 encoding of the last dim of ``v`` (a multiple of 16): per block of
+    16 values the E4M3 scale s = e4m3(amax / (6 g)) (nearest, at most 448),
+    then each value's E2M1 code of v / (g s): the nearest of 0, 0.5, 1, 1.5,
+    2, 3, 4, 6, a tie to the code with mantissa bit 0, beyond 6 the largest;
+    a block with s = 0 gets zero codes.  Value 2i in the low nibble of byte i.
+    Returns (uint8 codes [..., n/2], uint8 scale codes [..., n/16])."""
+    shp = v.shape
+    n = shp[-1]
+    x = v.to(torch.float64).reshape(*shp[:-1], n // NVFP4_BLOCK, NVFP4_BLOCK)
+    amax = x.abs().amax(dim=-1, keepdim=True)
+    sc = (amax / (6.0 * g)).clamp(max=E4M3_MAX).to(torch.float8_e4m3fn)
+    s = sc.to(torch.float64)
+    live = s > 0
+    y = torch.where(live, x / (g * torch.where(live, s, torch.ones_like(s))), torch.zeros_like(x))
+    a = y.abs()
+    code = ((a > 0.25).to(torch.uint8) + (a >= 0.75) + (a > 1.25) + (a >= 1.75) + (a > 2.5) + (a >= 3.5) + (a > 5))
+    code = code + torch.where(torch.signbit(y) & live, 8, 0).to(torch.uint8)
+    code = code.reshape(*shp[:-1], n // 2, 2)
+    codes = (code[..., 0] | (code[..., 1] << 4)).to(torch.uint8)
+    return codes, sc.view(torch.uint8).reshape(*shp[:-1], n // NVFP4_BLOCK)
+
+
 # ---------------------------------------------------------------------------
 # workloads
 @dataclasses.dataclass(frozen=True)
@@ -157,6 +191,8 @@ class Workload:
     page_size: int = 0                     # 0 = contiguous rows per sequence
     index_fp8: bool = False
     latent_fp8: bool = False
+    index_nvfp4: bool = False
+    latent_nvfp4: bool = False
     shared_layer: bool = False
     topk: int = 2048
     select_block: int = 0                  # 0: exact top-k; > 0: block-sparse selection, blocks of this size
@@ -170,8 +206,9 @@ class Workload:
         c = (f"{self.ctx}" if self.ctx else f"U{{{self.ctx_range[0]}..{self.ctx_range[1]}}}" if self.ctx_range
              else f"{list(self.ctx_list)}")
         return (f"{self.name}: {self.num_seqs} seq x ctx {c}, {self.queries_per_seq} q/seq, "
-                f"{'RoPE' if self.rope else 'NoPE'}, index {'e4m3+rowscale' if self.index_fp8 else 'bf16'}, "
-                f"latent {'fp8_ds_mla' if self.latent_fp8 else 'bf16'}"
+                f"{'RoPE' if self.rope else 'NoPE'}, index "
+                f"{'e4m3+rowscale' if self.index_fp8 else 'nvfp4' if self.index_nvfp4 else 'bf16'}, "
+                f"latent {'fp8_ds_mla' if self.latent_fp8 else 'nvfp4' if self.latent_nvfp4 else 'bf16'}"
                 f"{', pages of %d' % self.page_size if self.page_size else ''}"
                 f"{', + shared-indexer layer' if self.shared_layer else ''}, "
                 + (f"{self.topk // self.select_block} blocks of {self.select_block}" if self.select_block
@@ -187,6 +224,9 @@ WORKLOADS: Dict[str, Workload] = {
     # block-sparse selection as the MiniMax M3.1 page describes it: 128-token
     # blocks, 16 selected (2,048 keys) at long context; caches as long_fp8
     "block_fp8": Workload("block_fp8", 32, 1, ctx=524288, index_fp8=True, latent_fp8=True, select_block=128),
+    # NVFP4 caches as the MiniMax M3.1 page describes them (72 B index keys,
+    # 324 B latent rows), at the long_fp8 shape
+    "long_nvfp4": Workload("long_nvfp4", 32, 1, ctx=524288, index_nvfp4=True, latent_nvfp4=True),
 }
 
 
@@ -314,6 +354,26 @@ def gen_ds_mla_rows(key: int, rows: torch.Tensor, device):
     return out
 
 
+def gen_nvfp4_rows(key: int, rows: torch.Tensor, width: int, device, zero_from: Optional[int] = None):
+    """NVFP4 rows of the same N(0,1) stream as gen_bf16_rows (rounded to bf16
+    first, as a bf16 cache quantised to NVFP4): codes [n, width/2] and E4M3
+    block scales [n, width/16], tensor scale NVFP4_GLOBAL."""
+    codes = torch.empty(rows.numel(), width // 2, dtype=torch.uint8, device=device)
+    scales = torch.empty(rows.numel(), width // NVFP4_BLOCK, dtype=torch.uint8, device=device)
+
+    def make(x):
+        y = to_bf16(x)
+        if zero_from is not None:
+            y[:, zero_from:] = 0
+        return quantize_nvfp4(y, NVFP4_GLOBAL)
+
+    def store(sl, chunk):
+        codes[sl] = chunk[0]
+        scales[sl] = chunk[1]
+    _fill_rows(store, rows, width, key, device, make)
+    return codes, scales
+
+
 def _params(wl: Workload):
     s = (0.05 + 0.10 * uniform(stream_key(wl.seed, T_SSMAX_S), _counters(0, INDEX_HEADS, "cpu"))).to(torch.float32)
     b = (0.9 + 0.2 * uniform(stream_key(wl.seed, T_SSMAX_B), _counters(0, INDEX_HEADS, "cpu"))).to(torch.float32)
@@ -367,14 +427,23 @@ def make_cache_rows(wl: Workload, rows: torch.Tensor, device, which: str = "all"
     if which in ("all", "index"):
         if wl.index_fp8:
             out["k_idx"], out["k_scale"] = gen_e4m3_rowscale_rows(stream_key(wl.seed, T_K_IDX), rows, device)
+        elif wl.index_nvfp4:
+            out["k_idx"], out["k_bscale"] = gen_nvfp4_rows(stream_key(wl.seed, T_K_IDX), rows, INDEX_DIM, device)
+            out["k_global"] = NVFP4_GLOBAL
         else:
             out["k_idx"] = gen_bf16_rows(stream_key(wl.seed, T_K_IDX), rows, INDEX_DIM, device)
     if which in ("all", "latent"):
         if wl.latent_fp8:
             out["latent"] = gen_ds_mla_rows(stream_key(wl.seed, T_LATENT), rows, device)
+        elif wl.latent_nvfp4:
+            out["latent"], out["lat_bscale"] = gen_nvfp4_rows(stream_key(wl.seed, T_LATENT), rows, MLA_DIM, device,
+                                                              zero)
+            out["lat_global"] = NVFP4_GLOBAL
         else:
             out["latent"] = gen_bf16_rows(stream_key(wl.seed, T_LATENT), rows, MLA_DIM, device, zero)
         if wl.shared_layer:
+            if wl.latent_nvfp4:
+                raise ValueError("the shared-indexer layer's second latent cache has no NVFP4 form here")
             if wl.latent_fp8:
                 out["latent2"] = gen_ds_mla_rows(stream_key(wl.seed, T_LATENT2), rows, device)
             else:

@@ -49,13 +49,16 @@ class DecodeStep:
         """dsa_layer_args fields; ``queries`` (q_idx, w, q_mla, q_mla2) replaces
         the workload's own query tensors (same shapes)."""
         d = dict(self.d, **queries) if queries else self.d
+        k_nv4, lat_nv4 = "k_bscale" in d, "lat_bscale" in d  # NVFP4 caches
         a = dict(q_idx=d["q_idx"], w=d["w"], ssmax_s=d["ssmax_s"], ssmax_b=d["ssmax_b"], inv_freq=d["inv_freq"],
                  k_idx=d["k_idx"], k_scale=d.get("k_scale"),
-                 k_dtype=B.DSA_FP8_E4M3_ROWSCALE if self.k_fp8 else B.DSA_BF16, reuse_idx=0, k=self.k,
-                 select_block=self.select_block,
+                 k_dtype=B.DSA_NVFP4 if k_nv4 else B.DSA_FP8_E4M3_ROWSCALE if self.k_fp8 else B.DSA_BF16,
+                 k_block_scales=d.get("k_bscale"), k_global=d.get("k_global", 0.0),
+                 reuse_idx=0, k=self.k, select_block=self.select_block,
                  idx=self.idx, topk_len=self.topk_len, q_mla=d["q_mla"], latent=d["latent"],
-                 latent_dtype=B.DSA_FP8_DS_MLA if self.lat_fp8 else B.DSA_BF16, sm_scale=d["sm_scale"],
-                 out=self.out, lse=self.lse)
+                 latent_dtype=B.DSA_NVFP4 if lat_nv4 else B.DSA_FP8_DS_MLA if self.lat_fp8 else B.DSA_BF16,
+                 latent_scales=d.get("lat_bscale"), latent_global=d.get("lat_global", 0.0),
+                 sm_scale=d["sm_scale"], out=self.out, lse=self.lse)
         if shared:
             a.update(reuse_idx=1, q_mla=d["q_mla2"], latent=d["latent2"], out=self.out2, lse=self.lse2)
         return a

@@ -43,7 +43,7 @@
  *     or asserts.  The status code is in bits 0-7; for DSA_ERR_TIMEOUT (a
  *     bounded in-kernel wait that gave up after 1 s) bits 8-15 name the kernel
  *     (1 indexer scan, 2 attention, 3 attention over fp8_ds_mla, 4 attention
- *     over NVFP4 latent rows) and bits
+ *     over NVFP4 latent rows, 5 indexer scan over NVFP4 keys) and bits
  *     16-30 the wait (its mbarrier's shared-memory offset / 8, or 0x7FFF for
  *     the attention's issue loop).
  *   - Indices are logical token positions within a sequence.  The page table or
@@ -88,7 +88,8 @@ typedef enum {
                                    [528,656) 64 bf16 RoPE dims ([vLLM-ML4] FP8 latent cache) */
     DSA_NVFP4 = 3               /* latent: codes [rows,288] bytes (576 E2M1 values, value 2i in the low
                                    nibble of byte i) + E4M3 block scales [rows,36] (one per 16 values) +
-                                   one fp32 tensor scale g: value = g * scale * code, 4.5 bits/value
+                                   one fp32 tensor scale g: value = g * scale * code, 4.5 bits/value;
+                                   index keys: codes [rows,64] + scales [rows,8] + g (72 B/token)
                                    ("vLLM adds NVFP4 serving for MiniMax M3.1 Flash": NVFP4 caches) */
 } dsa_dtype;
 
@@ -138,6 +139,21 @@ dsa_status dsa_index_scores(const void* q_idx, const float* w, const float* ssma
                             const float* inv_freq, const void* k_idx, const float* k_scale, dsa_dtype k_dtype,
                             const dsa_seqs* seqs, int32_t num_q, float* scores, int64_t ld, void* workspace,
                             size_t workspace_bytes, int32_t* d_status, cudaStream_t stream);
+
+/* dsa_index_scores over NVFP4 index keys ("vLLM adds NVFP4 serving for
+ * MiniMax M3.1 Flash": NVFP4 indexer caches at 4.5 bits per value, converted
+ * inside the kernel).  Key j is k_j = k_global * scale * code:
+ *   k_codes        [rows, 64] bytes: 128 E2M1 values, value 2i in the low
+ *                  nibble of byte i (16-byte aligned)
+ *   k_block_scales [rows, 8] E4M3 codes, one per 16 values (8-byte aligned)
+ *   k_global       fp32 tensor scale, > 0 and finite
+ * The kernel decodes each key exactly to f16 (an E2M1 value times its E4M3
+ * scale) and folds k_global into the head weight.  Scores, layout and errors
+ * otherwise as dsa_index_scores (which refuses DSA_NVFP4). */
+dsa_status dsa_index_scores_nvfp4(const void* q_idx, const float* w, const float* ssmax_s, const float* ssmax_b,
+                                  const float* inv_freq, const void* k_codes, const void* k_block_scales,
+                                  float k_global, const dsa_seqs* seqs, int32_t num_q, float* scores, int64_t ld,
+                                  void* workspace, size_t workspace_bytes, int32_t* d_status, cudaStream_t stream);
 
 /* Exact top-k per query ([vLLM-ML4] Model architecture: top-k 2048; DCP: an
  * exact top-k, top-k compaction with topk_length, unused slots -1):

@@ -130,6 +130,10 @@ def oracle_scores_for_query(d: Dict, t: int) -> np.ndarray:
     keys = d["k_idx"].index_select(0, rows)
     ks = d["k_scale"].index_select(0, rows) if "k_scale" in d else None
     olay = oracle.Layout(np.array([ctx], np.int32), ctx, seq_base=np.zeros(1, np.int64))
+    if "k_bscale" in d:  # NVFP4 keys
+        return oracle.index_scores_nvfp4(d["q_idx"][t:t + 1], d["w"][t:t + 1], d["ssmax_s"], d["ssmax_b"],
+                                         d["inv_freq"], np.zeros(1, np.int32), np.array([lay.q_pos[t]], np.int32),
+                                         keys, d["k_bscale"].index_select(0, rows), d["k_global"], olay)[0]
     return oracle.index_scores(d["q_idx"][t:t + 1], d["w"][t:t + 1], d["ssmax_s"], d["ssmax_b"], d["inv_freq"],
                                np.zeros(1, np.int32), np.array([lay.q_pos[t]], np.int32), keys, olay,
                                key_scale=ks)[0]
@@ -144,6 +148,9 @@ def oracle_mla_for_query(d: Dict, t: int, sel: np.ndarray, shared: bool = False)
     q = d["q_mla2" if shared else "q_mla"][t]
     n = len(sel)
     olay = oracle.Layout(np.array([max(n, 1)], np.int32), max(n, 1), seq_base=np.zeros(1, np.int64))
+    if "lat_bscale" in d and not shared:  # NVFP4 latent rows
+        return oracle.sparse_mla_nvfp4(q, lat, d["lat_bscale"].index_select(0, rows), d["lat_global"], olay, 0,
+                                       np.arange(n, dtype=np.int32), n, d["sm_scale"])
     out, lse, _ = oracle.sparse_mla(q, lat, olay, 0, np.arange(n, dtype=np.int32), n, d["sm_scale"],
                                     fp8=lat.dtype == torch.uint8)
     return out, lse

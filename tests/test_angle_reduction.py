@@ -1,5 +1,5 @@
 """The kernels reduce the RoPE angle pos * inv_freq by 2 pi the Cody & Waite
-way.  The indexer's query prep (csrc/indexer.cu) splits 2 pi into two 26-bit
+way.  The indexer's query prep (csrc/indexer_common.cuh) splits 2 pi into two 26-bit
 parts and an fp64 remainder; the cache-write kernels (csrc/cache_write.cu)
 hold the angle as an exact fp32 pair and reduce it with a three-part fp32 2 pi
 below 2^24, in fp64 above.  Checked here on the CPU against exact rational
@@ -18,7 +18,7 @@ import pytest
 sympy = pytest.importorskip("sympy")
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-SRC = os.path.join(ROOT, "dsa_sparse_mla_query_gb300", "csrc", "indexer.cu")
+SRC = os.path.join(ROOT, "dsa_sparse_mla_query_gb300", "csrc", "indexer_common.cuh")
 SRC_CW = os.path.join(ROOT, "dsa_sparse_mla_query_gb300", "csrc", "cache_write.cu")
 
 

@@ -95,3 +95,42 @@ def test_generated_fp8_follows_the_recipe():
     oc, os_ = oracle.quantize_rows_e4m3(v.double().numpy(), 128)
     assert np.allclose(scale.double().numpy(), os_, rtol=1e-6, atol=0)
     assert (codes.numpy() == oc).mean() > 0.999
+
+
+def test_nvfp4_encoding_matches_the_oracles_encoder():
+    """The NVFP4 storage encoding that both sides read is byte for byte the
+    oracle's own encoder ("vLLM adds NVFP4 serving for MiniMax M3.1 Flash":
+    E2M1 codes, one E4M3 scale per 16 values, one tensor scale): on bf16
+    N(0,1) rows, on the E2M1 ties and past 6, and on an all-zero block."""
+    g = 2.0 ** -9  # a power of two, so that the ties below stay exact ties
+    x = I.gen_bf16_rows(I.stream_key(5, I.T_K_IDX), torch.arange(300), 128, "cpu").to(torch.float64) * (g / I.NVFP4_GLOBAL)
+    # one block at scale 1.5 (its largest value 6 x 1.5 g) holding every E2M1
+    # tie, and one whose scale saturates at 448 so that values pass 6
+    ties = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -2.5, -5.0, 6.0, -0.75, 0.0, 4.9, 1.0, 3.0])
+    x[0, :16] = ties * g * 1.5
+    x[2, :16] = torch.linspace(-4000.0, 5000.0, 16, dtype=torch.float64) * g
+    x[1, 16:32] = 0.0
+    codes, scales = I.quantize_nvfp4(x, g)
+    oc, os_ = oracle.nvfp4_quantize(x.numpy(), g)
+    assert np.array_equal(scales.numpy(), os_)
+    assert np.array_equal(codes.numpy(), oc)
+    assert scales[0, 0] == 0x3C and scales[2, 0] == 0x7E  # 1.5, 448
+    assert scales[1, 1] == 0 and np.all(codes[1, 8:16].numpy() == 0)
+    lo, hi = codes[0, :8] & 15, codes[0, :8] >> 4
+    assert [int(v) for v in torch.stack([lo, hi], 1).reshape(-1)] == [0, 2, 2, 4, 4, 6, 6, 8, 12, 14, 7, 10, 0, 6, 2, 5]
+    assert int(codes[2, 7] >> 4) == 7 and int(codes[2, 0] & 15) == 15
+
+
+def test_generated_nvfp4_follows_the_recipe():
+    wl = I.scaled(I.WORKLOADS["long_nvfp4"], num_seqs=2, ctx=300)
+    d = I.make_inputs(wl, "cpu")
+    assert d["k_idx"].shape == (600, 64) and d["k_bscale"].shape == (600, 8)
+    assert d["latent"].shape == (600, 288) and d["lat_bscale"].shape == (600, 36)
+    assert d["k_global"] == d["lat_global"] == I.NVFP4_GLOBAL
+    ref = I.gen_bf16_rows(I.stream_key(wl.seed, I.T_K_IDX), torch.arange(600), 128, "cpu")
+    back = oracle.nvfp4_dequantize(d["k_idx"].numpy(), d["k_bscale"].numpy(), I.NVFP4_GLOBAL)
+    # E2M1 rounds to within half its widest step (2, between 4 and 6) of g s,
+    # and s = amax / (6 g) rounds to E4M3 within 1/16
+    err = np.abs(back - ref.double().numpy()).reshape(600, 8, 16).max(-1)
+    amax = np.abs(ref.double().numpy()).reshape(600, 8, 16).max(-1)
+    assert np.all(err <= amax / 6.0 * (1 + 1 / 16) + 1e-12)
