@@ -238,7 +238,7 @@ static void check_index_args(Check& c, const void* q_idx, const float* w, const 
            "index key dtype %d is not DSA_BF16, DSA_FP8_E4M3_ROWSCALE or DSA_NVFP4", (int)k_dtype);
     if (k_dtype == DSA_FP8_E4M3_ROWSCALE) c.ptr(k_scale, "k_scale", 4);
     if (k_dtype == DSA_NVFP4) {
-        c.ptr(k_block_scales, "NVFP4 index key block scales", 8);
+        c.ptr(k_block_scales, "NVFP4 index key block scales", 16);
         c.need(k_global > 0.f && k_global < INFINITY, DSA_ERR_INVALID_ARG,
                "NVFP4 index key tensor scale must be positive and finite");
     }

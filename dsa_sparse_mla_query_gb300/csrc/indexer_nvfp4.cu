@@ -20,8 +20,10 @@
 //
 // Work split and roles (one CTA per SM for four-query chunks, two otherwise):
 //   warp 0     TMA producer: code tiles (128 keys x 64 bytes, 64-byte
-//              swizzle), the 128 rows' block scales by cp.async beside them,
-//              and the chunk's q' at each new (sequence, chunk);
+//              swizzle), the rows' block scales beside them (a map of 8-byte
+//              elements, one per row: each box starts at the even row at or
+//              below its first row, 16-byte aligned, and takes two more), and the
+//              chunk's q' at each new (sequence, chunk);
 //   warp 1     allocates TMEM and issues the MMAs: M = 128 keys from TMEM,
 //              N = NQ x 32 heads, fp32 accumulators double-buffered;
 //   warps 2-5  epilogue (as the bf16 path's): relu, head weights, mask, stores;
@@ -35,18 +37,23 @@
 namespace dsa {
 
 // ---------------------------------------------------------------------------
-// query preparation, f16: q' [Q, 32, KP] as the bf16 path's layout
-// ([hi(0..63) | lo(0..63) | dims 64..127] on RoPE layers, dims 0..127 on
-// NoPE layers), scaled per head by 2^-e so that max |q'| lies in
+// query preparation, f16, scaled per head by 2^-e so that max |q'| lies in
 // [2^14, 2^15); w'' = w |f| g 2^e / 64.  The rotated dims keep ~2^-22 of their
-// value through hi + lo; the unrotated dims are bf16 values times a power of
-// two, exact in f16 down to 2^-29 of the head's largest value.
+// value through an f16 hi + lo pair; the unrotated dims are bf16 values times
+// a power of two, exact in f16 down to 2^-29 of the head's largest value.
+// Layouts:
+//   split_n = 0: q' [Q, 32, KP] as the bf16 path's ([hi(0..63) | lo(0..63) |
+//                dims 64..127] on RoPE layers, dims 0..127 on NoPE layers):
+//                the lo part extends K (K = 192);
+//   split_n = 1: q' [Q, 64, 128], rows 0..31 the heads' hi parts over all 128
+//                dims, rows 32..63 their lo parts (zero on dims 64..127): the
+//                lo part extends N instead (RoPE layers, one query per chunk).
 __global__ void __launch_bounds__(128) qprep_f16_kernel(const __nv_bfloat16* __restrict__ q,
                                                         const float* __restrict__ w, const float* __restrict__ ss,
                                                         const float* __restrict__ sb,
                                                         const float* __restrict__ inv_freq, dsa_seqs s, int num_q,
-                                                        float g, __half* __restrict__ qp, float* __restrict__ wp,
-                                                        int32_t* d_status) {
+                                                        float g, int split_n, __half* __restrict__ qp,
+                                                        float* __restrict__ wp, int32_t* d_status) {
     pdl_enter();
     const int t = blockIdx.x;
     const bool rope = inv_freq != nullptr;
@@ -91,6 +98,13 @@ __global__ void __launch_bounds__(128) qprep_f16_kernel(const __nv_bfloat16* __r
             hi[i] = __float2half_rn(v);
             lo[i] = __float2half_rn(v - __half2float(hi[i]));
         }
+        if (split_n) {
+            __half* o = qp + ((int64_t)t * 2 * kIH + h) * kID + 4 * lane;
+            *reinterpret_cast<uint2*>(o) = *reinterpret_cast<const uint2*>(hi);
+            *reinterpret_cast<uint2*>(o + kIH * kID) = rot ? *reinterpret_cast<const uint2*>(lo) : make_uint2(0, 0);
+            if (lane == 0) wp[(int64_t)t * kIH + h] = ldexpf(wsc[h] * g, e);
+            continue;
+        }
         __half* o = qp + ((int64_t)t * kIH + h) * KP;
         if (rot) {
             *reinterpret_cast<uint2*>(o + 4 * lane) = *reinterpret_cast<const uint2*>(hi);
@@ -103,14 +117,23 @@ __global__ void __launch_bounds__(128) qprep_f16_kernel(const __nv_bfloat16* __r
 }
 
 // ---------------------------------------------------------------------------
-// E2M1 codes x E4M3 block scale -> f16, exact.  One byte = two values (the
-// low nibble first); s2 = the block scale in both halves.
-__device__ __forceinline__ uint32_t nv4_pair(uint32_t byte, __half2 s2) {
-    const __half2_raw r = __nv_cvt_fp4x2_to_halfraw2(static_cast<__nv_fp4x2_storage_t>(byte), __NV_E2M1);
-    __half2 v;
-    reinterpret_cast<__half2_raw&>(v) = r;
-    v = __hmul2(v, s2);
-    return *reinterpret_cast<const uint32_t*>(&v);
+// E2M1 codes x E4M3 block scale -> f16, exact.  A 32-bit word holds 8 codes
+// (value 2i in the low nibble of byte i); its four bytes are unpacked into
+// byte registers and each converted as is (cvt.rn.f16x2.e2m1x2, low nibble to
+// the low half), so no shift or mask per pair; s2 = the block scale in both
+// halves.
+__device__ __forceinline__ void nv4_word(uint32_t w, __half2 s2, uint32_t* out) {
+    uint32_t o[4];
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+        : "r"(w));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&o[i]), s2);
+        out[i] = *reinterpret_cast<const uint32_t*>(&v);
+    }
 }
 
 // Decodes 16 code bytes (32 values of two blocks, scales s01 = the blocks'
@@ -120,30 +143,39 @@ __device__ __forceinline__ void nv4_chunk(const uint4& c, uint32_t s01, uint32_t
     __half2 sp;
     reinterpret_cast<__half2_raw&>(sp) = sr;
     const __half2 s0 = __low2half2(sp), s1 = __high2half2(sp);
-    const uint32_t wd[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) out[4 * u + i] = nv4_pair((wd[u] >> (8 * i)) & 0xFFu, u < 2 ? s0 : s1);
+    nv4_word(c.x, s0, out);
+    nv4_word(c.y, s0, out + 4);
+    nv4_word(c.z, s1, out + 8);
+    nv4_word(c.w, s1, out + 12);
 }
 
 constexpr int kNvCodeBytes = kID / 2;   // 64 code bytes per key
 constexpr int kNvScaleBytes = kID / 16; // 8 E4M3 block scales per key
 constexpr int kNvInfoSlots = 16;        // box bases handed to the epilogue (> stages in flight)
 
+// MMA cost on GB300 is close to a fixed ~50 cycles per M = 128 x K = 16
+// instruction for N up to 64, so a RoPE chunk of one query (N = 32) takes its
+// lo part in N (N = 64, K = 128: 8 instructions per tile) rather than in K
+// (N = 32, K = 192: 12); wider chunks keep it in K, where N is already large.
 template <int NQ, int KP>
 struct Nv4Cfg {
-    static constexpr int N = NQ * kIH;
-    static constexpr int q_bytes = N * KP * 2;
-    // codes (64-byte swizzled rows) then the rows' block scales
+    static constexpr int N = NQ * kIH;                  // heads of the chunk (score columns)
+    static constexpr bool split_n = NQ == 1 && KP == 192;
+    static constexpr int NM = split_n ? 2 * N : N;      // MMA N: accumulator columns per buffer
+    static constexpr int KM = split_n ? kID : KP;       // MMA K
+    static constexpr int q_bytes = NM * KM * 2;
+    // codes (64-byte swizzled rows) then the boxes' block scales, one slot of
+    // round_up((box rows + 2) x 8, 128) bytes per box: at most 2 KB
     static constexpr int codes_bytes = kTileKeys * kNvCodeBytes;
-    static constexpr int stage_bytes = codes_bytes + kTileKeys * kNvScaleBytes;  // 9 KB, 1024-aligned
+    static constexpr int scale_region = 2048;
+    static constexpr int stage_bytes = codes_bytes + scale_region;  // 10 KB, 1024-aligned
     static constexpr int info_bytes = kNvInfoSlots * 64;                         // int64 box_base[8]
     static constexpr int a_cols = kID / 2;  // one decoded tile: 128 lanes x 64 columns
-    static constexpr int tmem_need = 2 * N + 2 * a_cols;
+    static constexpr int tmem_need = 2 * NM + 2 * a_cols;
     static constexpr int tmem_cols = tmem_need <= 256 ? 256 : 512;
     static constexpr int ctas_per_sm = tmem_cols <= 256 ? 2 : 1;
-    static constexpr int tail_raw = (2 * 8 + 4 + 4 + 2 + 2 * kNvInfoSlots) * 8 + 16 + 4 * N * 4 + 4 * NQ * 4;
+    // barriers, TMEM slot and flag, weights, positions, box parities [8][8]
+    static constexpr int tail_raw = (2 * 8 + 4 + 4 + 2 + 2 * kNvInfoSlots) * 8 + 16 + 4 * N * 4 + 4 * NQ * 4 + 64;
     static constexpr int tail = (tail_raw + 1023) / 1024 * 1024;
     static constexpr int budget = (ctas_per_sm == 2 ? 110 : 220) * 1024;
     static constexpr int stages_fit = (budget - q_bytes - info_bytes - 1024 - tail) / stage_bytes;
@@ -158,12 +190,12 @@ struct Nv4Cfg {
 template <int NQ, int KP>
 __global__ void __launch_bounds__(320, Nv4Cfg<NQ, KP>::ctas_per_sm)
     index_nv4_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
-                     const float* __restrict__ wp, const uint8_t* __restrict__ kscales, dsa_seqs s,
+                     const __grid_constant__ CUtensorMap smap, const float* __restrict__ wp, dsa_seqs s,
                      float* __restrict__ scores, int64_t ld, float* __restrict__ gmax, int64_t ldg,
                      int tiles_per_seq, int chunks, int64_t total_tiles, int box_rows, int32_t* d_status) {
     pdl_enter();
     using C = Nv4Cfg<NQ, KP>;
-    constexpr int S = C::S, N = C::N;
+    constexpr int S = C::S, N = C::N, NM = C::NM, KM = C::KM;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = base;
@@ -184,14 +216,16 @@ __global__ void __launch_bounds__(320, Nv4Cfg<NQ, KP>::ctas_per_sm)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     float* sw_all = reinterpret_cast<float*>(tmem_slot + 4);  // [4][N] head weights, one copy per epilogue warp
     int* spos_all = reinterpret_cast<int*>(sw_all + 4 * N);   // [4][NQ] query positions
+    uint8_t* bpar = reinterpret_cast<uint8_t*>(spos_all + 4 * NQ);  // [S][8] first row & 1 of each scale box
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t_begin = total_tiles * blockIdx.x / gridDim.x;
     const int64_t t_end = total_tiles * (blockIdx.x + 1) / gridDim.x;
+    const int sc_slot = ((box_rows + 2) * kNvScaleBytes + 127) & ~127;  // bytes per box of scales
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
-            ptx::mbar_init(full + i, 33);  // lane 0's expect_tx, plus each lane's scale copies
+            ptx::mbar_init(full + i, 1);  // lane 0's expect_tx
             ptx::mbar_init(empty + i, 4);
         }
         for (int i = 0; i < 2; ++i) {
@@ -218,13 +252,14 @@ __global__ void __launch_bounds__(320, Nv4Cfg<NQ, KP>::ctas_per_sm)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const uint32_t acol0 = 2 * N;  // A buffers after the two accumulators
+    const uint32_t acol0 = 2 * NM;  // A buffers after the two accumulators
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             ptx::prefetch_tmap(&kmap);
             ptx::prefetch_tmap(&qmap);
+            ptx::prefetch_tmap(&smap);
         }
         TileWalker<NQ> wk(t_begin, t_end, tiles_per_seq, chunks);
         int seg, j0, kind, q_seg = -1, qloads = 0;
@@ -241,8 +276,8 @@ __global__ void __launch_bounds__(320, Nv4Cfg<NQ, KP>::ctas_per_sm)
                     ok = qloads == 0 || ptx::mbar_wait(qempty, (qloads - 1) & 1, abort_flag, d_status);
                     if (ok) {
                         ptx::mbar_expect_tx(qfull, C::q_bytes);
-                        for (int kb = 0; kb < KP / 64; ++kb)
-                            ptx::tma_load_2d(qs + kb * N * 128, &qmap, kb * 64, g.q0 * kIH, qfull);
+                        for (int kb = 0; kb < KM / 64; ++kb)
+                            ptx::tma_load_2d(qs + kb * NM * 128, &qmap, kb * 64, g.q0 * (NM / NQ), qfull);
                     }
                 }
                 if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -277,22 +312,22 @@ __global__ void __launch_bounds__(320, Nv4Cfg<NQ, KP>::ctas_per_sm)
                 if (ok && issued >= kNvInfoSlots)
                     ok = ptx::mbar_wait(iempty + is, ((uint32_t)(issued / kNvInfoSlots) - 1) & 1, abort_flag,
                                         d_status);
-                if (ok) ptx::mbar_expect_tx(full + st, (uint32_t)__popc(loads) * box_rows * kNvCodeBytes);
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
+            // the stage is free: the boxes' parities, then (ordered by the warp
+            // barrier and lane 0's arrival) the copies
+            if (row >= 0) bpar[st * 8 + rb] = (uint8_t)(row & 1);
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_expect_tx(full + st, (uint32_t)__popc(loads) *
+                                                   (box_rows * kNvCodeBytes + (box_rows + 2) * kNvScaleBytes));
+            __syncwarp();
             uint8_t* stg = stages + st * C::stage_bytes;
-            if (row >= 0) ptx::tma_load_2d(stg + rb * box_rows * kNvCodeBytes, &kmap, 0, (int)row, full + st);
-            // the 128 rows' block scales (8 bytes each) beside the codes
-            uint8_t* sc = stg + C::codes_bytes;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int r = lane + 32 * u;
-                const int64_t bb = __shfl_sync(0xffffffffu, row, r / box_rows);
-                const int64_t pr = bb + (r & (box_rows - 1));
-                if (bb >= 0 && pr < s.num_rows) ptx::cp_async8(sc + r * kNvScaleBytes, kscales + pr * kNvScaleBytes);
+            if (row >= 0) {
+                ptx::tma_load_2d(stg + rb * box_rows * kNvCodeBytes, &kmap, 0, (int)row, full + st);
+                ptx::tma_load_2d(stg + C::codes_bytes + rb * sc_slot, &smap, (int)(row & ~int64_t(1)), 0, full + st);
             }
-            ptx::cp_async_arrive_noinc(full + st);
             int64_t* ti = reinterpret_cast<int64_t*>(info + is * 64);
             if (rb < 8) ti[rb] = row;
             __syncwarp();
@@ -307,10 +342,9 @@ __global__ void __launch_bounds__(320, Nv4Cfg<NQ, KP>::ctas_per_sm)
             }
             if (qloads > 0) ptx::mbar_drain(qempty, (qloads - 1) & 1);
         }
-        ptx::cp_async_wait_all();
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = ptx::idesc_f16_m128(N, false);  // f16 x f16
+        constexpr uint32_t idesc = ptx::idesc_f16_m128(NM, false);  // f16 x f16
         TileWalker<NQ> wk(t_begin, t_end, tiles_per_seq, chunks);
         int seg, j0, kind, nseg, nj0, nkind;
         bool have = wk.next(s, 2, d_status, false, seg, j0, kind);
@@ -331,12 +365,12 @@ __global__ void __launch_bounds__(320, Nv4Cfg<NQ, KP>::ctas_per_sm)
             const uint32_t qbase = smem_u32(qs);
             const uint32_t abuf = tmem_base + acol0 + b * C::a_cols;
 #pragma unroll
-            for (int ks = 0; ks < KP / 16; ++ks) {
+            for (int ks = 0; ks < KM / 16; ++ks) {
                 int kd;  // key dim of this k-step: [hi | lo | unrotated] read dims 0..63, 0..63, 64..127
-                if (KP == 192) kd = ks < 4 ? ks * 16 : (ks < 8 ? (ks - 4) * 16 : 64 + (ks - 8) * 16);
+                if (KM == 192) kd = ks < 4 ? ks * 16 : (ks < 8 ? (ks - 4) * 16 : 64 + (ks - 8) * 16);
                 else kd = ks * 16;
-                const uint64_t bd = ptx::sdesc_sw128(qbase + ((ks * 16) >> 6) * (N * 128) + ((ks * 16) & 63) * 2);
-                ptx::mma_ts(tmem_base + b * N, abuf + kd / 2, bd, idesc, ks > 0 ? 1u : 0u);
+                const uint64_t bd = ptx::sdesc_sw128(qbase + ((ks * 16) >> 6) * (NM * 128) + ((ks * 16) & 63) * 2);
+                ptx::mma_ts(tmem_base + b * NM, abuf + kd / 2, bd, idesc, ks > 0 ? 1u : 0u);
             }
             ptx::mma_commit(aempty + b);
             ptx::mma_commit(tfull + b);
@@ -354,6 +388,7 @@ __global__ void __launch_bounds__(320, Nv4Cfg<NQ, KP>::ctas_per_sm)
         const int row = quarter * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const int swz = (row >> 1) & 3;  // 64-byte swizzle: 16-byte chunk c sits at c ^ swz
+        const int rbx = row / box_rows, rin = row & (box_rows - 1);
         TileWalker<NQ> wk(t_begin, t_end, tiles_per_seq, chunks);
         int seg, j0, kind;
         int64_t c = 0;
@@ -366,7 +401,8 @@ __global__ void __launch_bounds__(320, Nv4Cfg<NQ, KP>::ctas_per_sm)
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 cw[k] = *reinterpret_cast<const uint4*>(stg + row * kNvCodeBytes + ((k ^ swz) << 4));
-            const uint2 sc = *reinterpret_cast<const uint2*>(stg + C::codes_bytes + row * kNvScaleBytes);
+            const uint2 sc = *reinterpret_cast<const uint2*>(stg + C::codes_bytes + rbx * sc_slot +
+                                                             (rin + bpar[st * 8 + rbx]) * kNvScaleBytes);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(empty + st);  // codes in registers: the stage may refill
             const int b = (int)(c & 1);
@@ -439,7 +475,7 @@ __global__ void __launch_bounds__(320, Nv4Cfg<NQ, KP>::ctas_per_sm)
             const uint32_t au = (uint32_t)(consumed >> 1);
             if (!__all_sync(0xffffffffu, ptx::mbar_wait(tfull + a, au & 1, abort_flag, d_status))) break;
             ptx::tc_fence_after();
-            const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + a * N;
+            const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + a * NM;
             auto relu_sum = [&](const uint32_t (&v)[32], int q) -> float {
                 const float4* w4 = reinterpret_cast<const float4*>(sw + q * kIH);
                 float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
@@ -467,7 +503,19 @@ __global__ void __launch_bounds__(320, Nv4Cfg<NQ, KP>::ctas_per_sm)
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(tempty + a);
             };
-            if constexpr (NQ == 1) {
+            if constexpr (C::split_n) {
+                // hi and lo columns into registers, the accumulator back, their sums
+                uint32_t v[2][32];
+                ptx::tmem_ld32_async(tcol, v[0]);
+                ptx::tmem_ld32_async(tcol + 32, v[1]);
+                ptx::tmem_wait_ld32(v[0]);
+                ptx::tmem_wait_ld32(v[1]);
+                release();
+#pragma unroll
+                for (int h = 0; h < 32; ++h)
+                    v[0][h] = __float_as_uint(__uint_as_float(v[0][h]) + __uint_as_float(v[1][h]));
+                store(0, relu_sum(v[0], 0));
+            } else if constexpr (NQ == 1) {
                 // every column into registers, then the accumulator goes back
                 uint32_t v[NQ][32];
 #pragma unroll
@@ -512,12 +560,18 @@ cudaError_t launch_nv4(const void* qp, int num_q, const float* wp, const void* c
                        cudaStream_t stream) {
     using C = Nv4Cfg<NQ, KP>;
     const int box_rows = s.page_table ? std::min(64, s.page_size & -s.page_size) : kTileKeys;
-    CUtensorMap kmap, qmap;
+    CUtensorMap kmap, qmap, smap;
     cudaError_t e = make_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, kNvCodeBytes, (uint64_t)s.num_rows,
                              kNvCodeBytes, kNvCodeBytes, box_rows, CU_TENSOR_MAP_SWIZZLE_64B);
     if (e != cudaSuccess) return e;
-    e = make_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qp, KP, (uint64_t)num_q * kIH, KP * 2, 64, C::N,
-                 CU_TENSOR_MAP_SWIZZLE_128B);
+    // the block scales as one 8-byte element per row (a single outer row); a
+    // box covers its rows plus two
+    e = make_map(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT64, kscales, (uint64_t)s.num_rows, 1,
+                 ((uint64_t)s.num_rows * kNvScaleBytes + 15) / 16 * 16, (uint32_t)box_rows + 2, 1,
+                 CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+    e = make_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qp, C::KM, (uint64_t)num_q * (C::NM / NQ), C::KM * 2, 64,
+                 C::NM, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
     auto kern = index_nv4_kernel<NQ, KP>;
     static std::once_flag once;
@@ -530,9 +584,8 @@ cudaError_t launch_nv4(const void* qp, int num_q, const float* wp, const void* c
     const int chunks = (s.max_q_per_seq + NQ - 1) / NQ;
     const int64_t total = (int64_t)s.num_seqs * chunks * tiles_per_seq;
     const int grid = (int)std::min<int64_t>((int64_t)C::ctas_per_sm * num_sms(), total);
-    return launch_pdl(kern, dim3(grid), dim3(C::threads), C::smem, stream, 1, kmap, qmap, wp,
-                      reinterpret_cast<const uint8_t*>(kscales), s, scores, ld, gmax, ldg, tiles_per_seq, chunks,
-                      total, box_rows, d_status);
+    return launch_pdl(kern, dim3(grid), dim3(C::threads), C::smem, stream, 1, kmap, qmap, smap, wp, s, scores, ld,
+                      gmax, ldg, tiles_per_seq, chunks, total, box_rows, d_status);
 }
 
 template <int NQ>
@@ -552,11 +605,12 @@ cudaError_t launch_index_scores_nvfp4(const void* q_idx, const float* w, const f
                                       cudaStream_t stream) {
     const bool rope = inv_freq != nullptr;
     __half* qp = reinterpret_cast<__half*>(ws.qprep);
+    const int mq = s.max_q_per_seq;
+    const int split_n = Nv4Cfg<1, 192>::split_n && rope && mq <= 1;  // the layout the kernel below reads
     cudaError_t e = launch_pdl(qprep_f16_kernel, dim3(num_q), dim3(128), 0, stream, 1,
                                reinterpret_cast<const __nv_bfloat16*>(q_idx), w, ssmax_s, ssmax_b, inv_freq, s, num_q,
-                               k_global, qp, ws.wprep, d_status);
+                               k_global, split_n, qp, ws.wprep, d_status);
     if (e != cudaSuccess) return e;
-    const int mq = s.max_q_per_seq;
     if (mq <= 1)
         return launch_nv4_nq<1>(rope, qp, num_q, ws.wprep, k_codes, k_block_scales, s, scores, ld, gmax, ldg, d_status,
                                 stream);

@@ -156,12 +156,16 @@ __device__ __forceinline__ uint4 nvfp4x8_to_f16x8(uint32_t codes, uint32_t scale
     const __half2_raw sr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(scale_code | (scale_code << 8)),
                                                       __NV_E4M3);
     const __half2 sc = *reinterpret_cast<const __half2*>(&sr);
-    uint32_t o[4];
+    // the four code bytes unpacked into byte registers, each converted as is
+    uint32_t h[4], o[4];
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(codes));
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const __half2_raw h = __nv_cvt_fp4x2_to_halfraw2(static_cast<__nv_fp4x2_storage_t>((codes >> (8 * i)) & 0xFFu),
-                                                         __NV_E2M1);
-        const __half2 pr = __hmul2(*reinterpret_cast<const __half2*>(&h), sc);
+        const __half2 pr = __hmul2(*reinterpret_cast<const __half2*>(&h[i]), sc);
         o[i] = *reinterpret_cast<const uint32_t*>(&pr);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);

@@ -145,7 +145,7 @@ dsa_status dsa_index_scores(const void* q_idx, const float* w, const float* ssma
  * inside the kernel).  Key j is k_j = k_global * scale * code:
  *   k_codes        [rows, 64] bytes: 128 E2M1 values, value 2i in the low
  *                  nibble of byte i (16-byte aligned)
- *   k_block_scales [rows, 8] E4M3 codes, one per 16 values (8-byte aligned)
+ *   k_block_scales [rows, 8] E4M3 codes, one per 16 values (16-byte aligned)
  *   k_global       fp32 tensor scale, > 0 and finite
  * The kernel decodes each key exactly to f16 (an E2M1 value times its E4M3
  * scale) and folds k_global into the head weight.  Scores, layout and errors

@@ -1,7 +1,7 @@
 """Parity of the CUDA path (through the C ABI) with the CPU oracle on a GB300.
 
 Small workloads span several key tiles, ragged tails, pages, several queries
-per sequence, NoPE + a shared-indexer layer, fp8 caches and a prefill chunk;
+per sequence, NoPE + a shared-indexer layer, fp8 and NVFP4 caches and a prefill chunk;
 every query is checked.  The full-size workloads run in the launch
 configuration the benchmark times and are checked on sampled queries.
 Tolerances are in tests/parity.py.
@@ -30,6 +30,7 @@ SMALL = {
     "paged_small": I.scaled(W["paged"], num_seqs=3, ctx=None, ctx_list=(1500, 4163, 130)),
     "specv_small": I.scaled(W["specv"], num_seqs=4, ctx_range=(2100, 6000)),
     "fp8_small": I.scaled(W["long_fp8"], num_seqs=3, ctx=None, ctx_list=(2000, 9000, 2049)),
+    "nvfp4_small": I.scaled(W["long_nvfp4"], num_seqs=3, ctx=None, ctx_list=(2000, 9000, 2049)),
     "prefill_small": I.scaled(W["prefill"], ctx=3000, queries_per_seq=40),
 }
 
@@ -53,9 +54,14 @@ def _separate_scores(d, wl, step):
     entries inside the context would show)."""
     ld = P.ld_of(step.seqs.max_ctx)
     scores = torch.full((step.num_q, ld), float("nan"), dtype=torch.float32, device=DEV)
-    dsa.dsa_index_scores(d["q_idx"], d["w"], d["ssmax_s"], d["ssmax_b"], d["inv_freq"], d["k_idx"], d.get("k_scale"),
-                         dsa.DSA_FP8_E4M3_ROWSCALE if step.k_fp8 else dsa.DSA_BF16, step.seqs, step.num_q, scores,
-                         ld, step.ws, step.ws_bytes, step.status)
+    if "k_bscale" in d:  # NVFP4 keys
+        dsa.dsa_index_scores_nvfp4(d["q_idx"], d["w"], d["ssmax_s"], d["ssmax_b"], d["inv_freq"], d["k_idx"],
+                                   d["k_bscale"], d["k_global"], step.seqs, step.num_q, scores, ld, step.ws,
+                                   step.ws_bytes, step.status)
+    else:
+        dsa.dsa_index_scores(d["q_idx"], d["w"], d["ssmax_s"], d["ssmax_b"], d["inv_freq"], d["k_idx"],
+                             d.get("k_scale"), dsa.DSA_FP8_E4M3_ROWSCALE if step.k_fp8 else dsa.DSA_BF16, step.seqs,
+                             step.num_q, scores, ld, step.ws, step.ws_bytes, step.status)
     return scores, ld
 
 
@@ -101,9 +107,14 @@ def _check_workload(d, wl, queries, threads=8):
     for lat_key, q_key, shared in layers:
         out = torch.empty(step.num_q, 64, 512, dtype=torch.bfloat16, device=DEV)
         lse = torch.empty(step.num_q, 64, dtype=torch.float32, device=DEV)
-        dsa.sparse_mla_decode(d[q_key], d[lat_key], dsa.DSA_FP8_DS_MLA if step.lat_fp8 else dsa.DSA_BF16, step.seqs,
-                              step.num_q, oidx_d, olen_d, k, d["sm_scale"], out, lse, step.ws, step.ws_bytes,
-                              step.status)
+        if "lat_bscale" in d and not shared:  # NVFP4 latent rows
+            dsa.sparse_mla_decode_nvfp4(d[q_key], d[lat_key], d["lat_bscale"], d["lat_global"], step.seqs,
+                                        step.num_q, oidx_d, olen_d, k, d["sm_scale"], out, lse, step.ws,
+                                        step.ws_bytes, step.status)
+        else:
+            dsa.sparse_mla_decode(d[q_key], d[lat_key], dsa.DSA_FP8_DS_MLA if step.lat_fp8 else dsa.DSA_BF16,
+                                  step.seqs, step.num_q, oidx_d, olen_d, k, d["sm_scale"], out, lse, step.ws,
+                                  step.ws_bytes, step.status)
         torch.cuda.synchronize()
         assert step.device_status() == 0
         out_h, lse_h = out.float().cpu().numpy(), lse.cpu().numpy()
@@ -286,8 +297,8 @@ def test_bad_position_sets_device_status():
     torch.cuda.synchronize()
 
 
-FULL = ["paged", "specv", "long_fp8", "prefill"]
-SAMPLES = {"paged": 6, "specv": 6, "long_fp8": 3, "prefill": 4}
+FULL = ["paged", "specv", "long_fp8", "prefill", "long_nvfp4"]
+SAMPLES = {"paged": 6, "specv": 6, "long_fp8": 3, "prefill": 4, "long_nvfp4": 3}
 
 
 @pytest.mark.parametrize("name", FULL)
