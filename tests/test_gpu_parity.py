@@ -210,6 +210,39 @@ def test_long_rows_all_equal_scores():
         assert np.array_equal(idx[t], np.arange(2048))
 
 
+@pytest.mark.parametrize("seed", [0, 1])
+def test_topk_rows_in_shared_memory(seed):
+    """Rows of 16,385 to 32,768 keys (one CTA per row, the row in shared
+    memory) on crafted scores against the oracle's exact top-k: ties at the
+    boundary (8 distinct values), one first digit holding more keys than the
+    candidate buffer (values within 2^-10 of 1), signed values with -0.0 and
+    +0.0 mixed, and all scores equal (positions 0..k-1)."""
+    ctx_list = (16385, 32768, 25000, 20001)
+    wl = I.scaled(W["tiny"], num_seqs=4, ctx=None, ctx_list=ctx_list, queries_per_seq=1)
+    d, _ = _inputs_cpu_then_gpu(wl)
+    step = DecodeStep(d, wl.queries_per_seq, wl.topk)
+    ld = P.ld_of(step.seqs.max_ctx)
+    g = torch.Generator().manual_seed(100 + seed)
+    sc = torch.full((4, ld), float("nan"), dtype=torch.float32)
+    n0, n1, n2, n3 = ctx_list
+    sc[0, :n0] = torch.randint(0, 8, (n0,), generator=g).float() * 0.5
+    sc[1, :n1] = 1.0 + torch.rand(n1, generator=g) * 2.0 ** -10
+    v = torch.randn(n2, generator=g)
+    v[torch.randint(0, n2, (3000,), generator=g)] = 0.0
+    v[torch.randint(0, n2, (3000,), generator=g)] = -0.0
+    sc[2, :n2] = v
+    sc[3, :n3] = 0.25
+    dsa.dsa_topk(sc.to(DEV), ld, step.seqs, 4, wl.topk, step.idx, step.topk_len, step.ws, step.ws_bytes, step.status)
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+    idx, tlen = step.idx.cpu().numpy(), step.topk_len.cpu().numpy()
+    oracle = __import__("oracle")
+    for t, n in enumerate(ctx_list):
+        ref, m = oracle.topk(sc[t, :n].double().numpy(), wl.topk)
+        assert tlen[t] == m == wl.topk
+        assert np.array_equal(idx[t], np.sort(ref[:m])), f"row {t}"
+
+
 def test_fp8_index_keys_every_code_class():
     """e4m3 index keys of one sequence drawn from the subnormal codes (and
     zero) alone, of the other from every finite code: scores, selection and
