@@ -17,7 +17,9 @@
 // up to 16 x 32,768 keys a thread-block cluster per row; anything longer one
 // CTA per row with four 8-bit passes over memory.
 
+#include <algorithm>
 #include <climits>
+#include <cstdint>
 #include <mutex>
 
 #include "dsa_internal.cuh"
@@ -366,9 +368,15 @@ __global__ void __launch_bounds__(THREADS, 1) topk_row_kernel(const float* __res
 // 16-byte loads (a warp reads 512 contiguous bytes); with the padded stride
 // both those stores and a thread's reads of its own keys are free of bank
 // conflicts.
+// The list of keys from the chosen first digit up (key and 16-bit position)
+// lives after the first histogram copy, over the other copies, which are free
+// once that digit is chosen.
+constexpr int kSmemCand = 12288;
+constexpr size_t kSmemListBytes = (size_t)kSmemCand * (4 + 2);
 template <int EPT>
 constexpr size_t smem_row_bytes() {
-    return (size_t)32 * (EPT * 1024 / 32 + 1) * 4 + (size_t)kRowSub * kRowBins * 4 + kRowCandCap * 4;
+    return (size_t)32 * (EPT * 1024 / 32 + 1) * 4 + (size_t)kRowBins * 4 +
+           std::max(kSmemListBytes, (size_t)(kRowSub - 1) * kRowBins * 4);
 }
 
 template <int EPT>
@@ -381,7 +389,8 @@ __global__ void __launch_bounds__(1024, 1) topk_smem_kernel(const float* __restr
     constexpr int KS = EPT * NT / 32 + 1;                                     // padded stride
     uint32_t* keys = reinterpret_cast<uint32_t*>(sm_smem);                    // key i at (i % 32) * KS + i / 32
     int* sub = sm_smem + 32 * KS;                                             // [kRowSub][kRowBins]
-    uint32_t* cand = reinterpret_cast<uint32_t*>(sub + kRowSub * kRowBins);   // [kRowCandCap]
+    uint32_t* cand = reinterpret_cast<uint32_t*>(sub + kRowBins);  // [kSmemCand] keys, over copies 1..
+    uint16_t* cpos = reinterpret_cast<uint16_t*>(cand + kSmemCand);  // [kSmemCand] their positions
     __shared__ int scan_buf[64];
     __shared__ int sel_digit, sel_above, ncand;
     const int t = blockIdx.x;
@@ -470,27 +479,57 @@ __global__ void __launch_bounds__(1024, 1) topk_smem_kernel(const float* __restr
         mask |= (uint32_t)(nb - 1) << shift;
         remaining -= sel_above;
         if (pass == 0) {
-            // keep the keys of the chosen bin for the next two passes (prefix-sum slots)
+            // every key of the chosen first digit or above -- the selection
+            // lies among them -- with its position, in ascending position
+            // (prefix-sum slots; thread t holds positions t EPT ..): the two
+            // finer passes and the final selection then walk this list alone
             int mine = 0;
 #pragma unroll 8
-            for (int e = 0; e < nv; ++e) mine += (keys[e * KS + tid] & mask) == prefix;
+            for (int e = 0; e < nv; ++e) mine += keys[e * KS + tid] >= prefix;
             int nc;
             int sl = scan_threads<NT>(mine, scan_buf, &nc);
-            if (nc <= kRowCandCap)
+            if (nc <= kSmemCand)
 #pragma unroll 8
                 for (int e = 0; e < nv; ++e) {
                     const uint32_t u = keys[e * KS + tid];
-                    if ((u & mask) == prefix) cand[sl++] = u;
+                    if (u >= prefix) {
+                        cand[sl] = u;
+                        cpos[sl++] = (uint16_t)(base + e);
+                    }
                 }
             if (tid == 0) ncand = nc;
             __syncthreads();
-            use_cand = nc <= kRowCandCap;
+            use_cand = nc <= kSmemCand;
         } else {
             __syncthreads();  // the next pass clears the histogram this one read
         }
     }
     const uint32_t T = prefix;
     const int need_eq = remaining;
+    if (use_cand) {
+        // ---- from the list: every key > T, the first need_eq keys == T,
+        // consecutive entries per thread, written in ascending position
+        const int nc = ncand, per_t = (nc + NT - 1) / NT;
+        const int j0 = min(tid * per_t, nc), j1 = min(j0 + per_t, nc);
+        int n_gt = 0, n_eq = 0;
+        for (int j = j0; j < j1; ++j) {
+            n_gt += cand[j] > T;
+            n_eq += cand[j] == T;
+        }
+        int tot_eq;
+        int eq_rank = scan_threads<NT>(n_eq, scan_buf, &tot_eq);
+        const int n_sel = n_gt + max(0, min(need_eq - eq_rank, n_eq));
+        int tot_sel;
+        int o = scan_threads<NT>(n_sel, scan_buf, &tot_sel);
+        for (int j = j0; j < j1; ++j) {
+            const uint32_t c = cand[j];
+            bool take = c > T;
+            if (c == T) take = eq_rank++ < need_eq;
+            if (take && o < k) out[o++] = cpos[j];
+        }
+        if (tid == 0) topk_len[t] = k;
+        return;
+    }
     // ---- ranks in index order: every key > T, the first need_eq keys == T
     int n_gt = 0, n_eq = 0;
 #pragma unroll 8
@@ -504,7 +543,7 @@ __global__ void __launch_bounds__(1024, 1) topk_smem_kernel(const float* __restr
     const int n_sel = n_gt + max(0, min(need_eq - eq_rank, n_eq));
     int tot_sel;
     int o = scan_threads<NT>(n_sel, scan_buf, &tot_sel);
-    int* stage_out = reinterpret_cast<int*>(cand);  // k <= kRowCandCap
+    int* stage_out = reinterpret_cast<int*>(cand);  // k <= kSmemCand
 #pragma unroll 8
     for (int e = 0; e < nv; ++e) {
         const uint32_t u = keys[e * KS + tid];
