@@ -267,8 +267,9 @@ __global__ void __launch_bounds__(IdxCfg<NQ, KP, FP8>::threads, IdxCfg<NQ, KP, F
     int* spos_all = reinterpret_cast<int*>(sw_all + C::EW * NQ * kIH);  // [EW][NQ] query positions
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t t_begin = total_tiles * blockIdx.x / gridDim.x;
-    const int64_t t_end = total_tiles * (blockIdx.x + 1) / gridDim.x;
+    int64_t t_begin, t_end;  // every warp computes the same range
+    balanced_range<NQ>(s, chunks, tiles_per_seq, &t_begin, &t_end);
+    (void)total_tiles;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {

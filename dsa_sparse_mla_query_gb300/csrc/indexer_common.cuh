@@ -142,6 +142,76 @@ struct TileWalker {
     }
 };
 
+// This CTA's contiguous range [*t0, *t1) of the tile space (segment g =
+// sequence x query chunk, tile i: index g * tiles_per_seq + i), balanced over
+// the tiles that exist -- tile i of segment g when i * 128 < ctx and the chunk
+// has queries -- rather than over the space padded to the longest context, so
+// that contexts of very different lengths still give every CTA the same work.
+// Called by a whole warp (every lane gets the result).
+template <int NQ>
+__device__ __forceinline__ void balanced_range(const dsa_seqs& s, int chunks, int tiles_per_seq, int64_t* t0,
+                                               int64_t* t1) {
+    const int lane = threadIdx.x & 31;
+    const int nseg = s.num_seqs * chunks;
+    auto real = [&](int g) -> int {
+        if (g >= nseg) return 0;
+        const int b = g / chunks, c = g - b * chunks;
+        const int ctx = __ldg(s.ctx_len + b);
+        const int nq = __ldg(s.q_start + b + 1) - __ldg(s.q_start + b);
+        if (ctx <= 0 || ctx > s.max_ctx || nq <= c * NQ) return 0;
+        return (ctx + kTileKeys - 1) / kTileKeys;
+    };
+    // the first 128 segments' counts are loaded together and kept; the rest
+    // (more than 128 segments) are recomputed on the second walk
+    constexpr int kKept = 4;
+    int kept[kKept];
+#pragma unroll
+    for (int i = 0; i < kKept; ++i) kept[i] = real(32 * i + lane);
+    auto count = [&](int g0) -> int {
+        int v = g0 >= 32 * kKept ? real(g0 + lane) : 0;
+#pragma unroll
+        for (int i = 0; i < kKept; ++i)
+            if (g0 == 32 * i) v = kept[i];
+        return v;
+    };
+    int64_t total = 0;
+    for (int g0 = 0; g0 < nseg; g0 += 32) {
+        int v = count(g0);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        total += v;
+    }
+    const int64_t r0 = total * blockIdx.x / gridDim.x, r1 = total * (blockIdx.x + 1) / gridDim.x;
+    // full-space index of compact index r (r == total: the end of the space)
+    int64_t f0 = (int64_t)nseg * tiles_per_seq, f1 = f0;
+    int64_t before = 0;  // real tiles of the segments before this group of 32
+    for (int g0 = 0; g0 < nseg && before <= r1; g0 += 32) {
+        const int v = count(g0);
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int64_t lo = before + incl - v, hi = before + incl;  // this lane's segment: [lo, hi)
+        const uint32_t h0 = __ballot_sync(0xffffffffu, v > 0 && r0 >= lo && r0 < hi);
+        const uint32_t h1 = __ballot_sync(0xffffffffu, v > 0 && r1 >= lo && r1 < hi);
+        if (h0 && f0 == (int64_t)nseg * tiles_per_seq) {
+            const int l = __ffs(h0) - 1;
+            const int64_t off = r0 - __shfl_sync(0xffffffffu, lo, l);
+            f0 = (int64_t)(g0 + l) * tiles_per_seq + off;
+        }
+        if (h1 && f1 == (int64_t)nseg * tiles_per_seq) {
+            const int l = __ffs(h1) - 1;
+            const int64_t off = r1 - __shfl_sync(0xffffffffu, lo, l);
+            f1 = (int64_t)(g0 + l) * tiles_per_seq + off;
+        }
+        before += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    *t0 = r0 < r1 ? f0 : 0;
+    *t1 = r0 < r1 ? f1 : 0;
+}
+
 // ---------------------------------------------------------------------------
 // host side
 inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {

@@ -219,8 +219,9 @@ __global__ void __launch_bounds__(320, Nv4Cfg<NQ, KP>::ctas_per_sm)
     uint8_t* bpar = reinterpret_cast<uint8_t*>(spos_all + 4 * NQ);  // [S][8] first row & 1 of each scale box
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t t_begin = total_tiles * blockIdx.x / gridDim.x;
-    const int64_t t_end = total_tiles * (blockIdx.x + 1) / gridDim.x;
+    int64_t t_begin, t_end;  // every warp computes the same range
+    balanced_range<NQ>(s, chunks, tiles_per_seq, &t_begin, &t_end);
+    (void)total_tiles;
     const int sc_slot = ((box_rows + 2) * kNvScaleBytes + 127) & ~127;  // bytes per box of scales
 
     if (threadIdx.x == 0) {
