@@ -34,15 +34,30 @@ static size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 // pair and combine in distributed shared memory; more write fp32 partials
 // that the combine kernel merges, which must fit `cap` bytes of scratch
 // (fewer splits otherwise; one or two always fit).
+// One CTA per SM at a time: a query split s ways is num_q * s CTAs of
+// ceil(tiles / s) tiles, which run in ceil(num_q * s / 152) waves.  The split
+// count minimises waves x (tiles per split + a CTA's fixed cost), in tenths
+// of a tile: the query's load and the pipeline's fill (about one tile), the
+// pair's exchange in distributed shared memory (two splits, 0.3), or the fp32
+// partials of three or more splits and their combine (128 KB per split and
+// query, about two tiles more).  At least two tiles per split, at most 16.
 int mla_splits(int num_q, int k, size_t cap) {
     const int tiles = (k + 63) / 64;
-    int sp = 152 / (num_q > 0 ? num_q : 1);
-    sp = sp < 1 ? 1 : sp;
+    const int64_t nq = num_q > 0 ? num_q : 1;
     int max_sp = tiles / 2 > 0 ? tiles / 2 : 1;  // at least two 64-row tiles per split
     if (max_sp > 16) max_sp = 16;                  // the combine holds 16 weights per head
-    sp = sp > max_sp ? max_sp : sp;
-    const size_t nq = (size_t)(num_q > 0 ? num_q : 1);
-    while (sp > 2 && up256(nq * sp * kMH * kMV * 4) + up256(nq * sp * kMH * 2 * 4) > cap) --sp;
+    int sp = 1;
+    int64_t best = -1;
+    for (int c = 1; c <= max_sp; ++c) {
+        const int64_t waves = (nq * c + 151) / 152;
+        const int64_t fixed = 10 + (c > 2 ? 20 : c == 2 ? 3 : 0);
+        const int64_t cost = waves * (10 * ((tiles + c - 1) / c) + fixed);
+        if (best < 0 || cost < best) {
+            best = cost;
+            sp = c;
+        }
+    }
+    while (sp > 2 && up256((size_t)nq * sp * kMH * kMV * 4) + up256((size_t)nq * sp * kMH * 2 * 4) > cap) --sp;
     return sp;
 }
 
