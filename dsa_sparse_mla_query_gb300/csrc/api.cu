@@ -103,11 +103,6 @@ size_t workspace_bytes(const dsa_seqs& s, int num_q, int k, int64_t* scores_ld) 
     b += up256(mla_part_bytes(nq, kk));                              // partial outputs
     b += up256(mla_ml_bytes(nq, kk));                                // partial (max, sum)
     b += up256((size_t)num_q * ld * 4);                              // scores (fused layer)
-    if (topk_long_rows(s.max_ctx)) {                                  // long-row top-k
-        b += up256((size_t)num_q * (2048 + 2) * 4);                  // histograms + two counters
-        b += up256((size_t)num_q * kLongCand * 8);                   // candidates
-        b += up256((size_t)num_q * DSA_MAX_TOPK * 4);                // positions above the chosen digit
-    }
     return b;
 }
 
@@ -129,15 +124,6 @@ Workspace carve_workspace(void* base, const dsa_seqs& s, int num_q, int k) {
     w.scores = reinterpret_cast<float*>(p);
     w.scores_ld = ld;
     p += up256((size_t)num_q * ld * 4);
-    if (topk_long_rows(s.max_ctx)) {
-        w.tk_hist = reinterpret_cast<int*>(p);
-        w.tk_ncand = w.tk_hist + (size_t)num_q * 2048;
-        w.tk_nabove = w.tk_ncand + num_q;
-        p += up256((size_t)num_q * (2048 + 2) * 4);
-        w.tk_cand = reinterpret_cast<uint2*>(p);
-        p += up256((size_t)num_q * kLongCand * 8);
-        w.tk_above = reinterpret_cast<int*>(p);
-    }
     return w;
 }
 
@@ -180,10 +166,9 @@ using namespace dsa;
 static int32_t layer_launches(const dsa_seqs& s, int num_q, int k, bool reuse, int select_block) {
     // attention, plus the LSE combine unless every query's splits combine in-kernel
     const int mla = mla_launches(num_q, k);
-    // selection: block-sparse one kernel; top-k one kernel, or three for rows
-    // longer than 32,768 keys (chunked)
-    const int tk = select_block > 0 ? 1 : (topk_chunked(s.max_ctx) ? 3 : 1);
-    return (reuse ? 0 : 2 + tk) + mla;  // query prep, scores, selection
+    (void)s;
+    (void)select_block;
+    return (reuse ? 0 : 3) + mla;  // query prep, scores, selection (top-k or blocks: one kernel)
 }
 
 static void check_shard(Check& c, const dsa_dcp_shard* sh) {
@@ -366,13 +351,11 @@ dsa_status dsa_topk(const float* scores, int64_t ld, const dsa_seqs* seqs, int32
     c.ptr(topk_len, "topk_len", 4);
     c.need(k >= 1 && k <= DSA_MAX_TOPK, DSA_ERR_UNSUPPORTED, "k %d outside [1, %d]", k, DSA_MAX_TOPK);
     if (seqs) c.need(ld >= seqs->max_ctx && ld % 4 == 0, DSA_ERR_INVALID_ARG, "ld %lld must be >= max_ctx and a multiple of 4", (long long)ld);
-    const bool long_rows = seqs && topk_long_rows(seqs->max_ctx);
-    if (long_rows) check_workspace(c, seqs, num_q, k, workspace, workspace_bytes);  // rows > 32K keys use scratch
+    (void)workspace;  // no scratch at any row length
+    (void)workspace_bytes;
     dsa_status st = c.done();
     if (st != DSA_OK || num_q == 0) return st;
-    Workspace ws{};
-    if (long_rows) ws = carve_workspace(workspace, *seqs, num_q, k);
-    return cuda_status(launch_topk(scores, ld, *seqs, num_q, k, idx, topk_len, ws, d_status, stream),
+    return cuda_status(launch_topk(scores, ld, *seqs, num_q, k, idx, topk_len, Workspace{}, d_status, stream),
                        "dsa_topk launch");
 }
 
@@ -388,13 +371,11 @@ dsa_status dsa_topk_candidates(const float* scores, int64_t ld, const dsa_seqs* 
     c.ptr(cand, "cand", 8);
     c.need(k >= 1 && k <= DSA_MAX_TOPK, DSA_ERR_UNSUPPORTED, "k %d outside [1, %d]", k, DSA_MAX_TOPK);
     if (seqs) c.need(ld >= seqs->max_ctx && ld % 4 == 0, DSA_ERR_INVALID_ARG, "ld %lld must be >= max_ctx and a multiple of 4", (long long)ld);
-    const bool long_rows = seqs && topk_long_rows(seqs->max_ctx);
-    if (long_rows) check_workspace(c, seqs, num_q, k, workspace, workspace_bytes);
+    (void)workspace;  // no scratch at any row length
+    (void)workspace_bytes;
     dsa_status st = c.done();
     if (st != DSA_OK || num_q == 0) return st;
-    Workspace ws{};
-    if (long_rows) ws = carve_workspace(workspace, *seqs, num_q, k);
-    cudaError_t e = launch_topk(scores, ld, *seqs, num_q, k, idx, topk_len, ws, d_status, stream);
+    cudaError_t e = launch_topk(scores, ld, *seqs, num_q, k, idx, topk_len, Workspace{}, d_status, stream);
     if (e == cudaSuccess)
         e = launch_cand_pack(scores, ld, idx, topk_len, num_q, k, shard->world, shard->rank, shard->interleave, cand,
                              d_status, stream);

@@ -128,23 +128,9 @@ struct Workspace {
     float* mla_ml;    // (m, l) partials [Q, splits, 64, 2]
     float* scores;    // [Q, ld] for dsa_decode_layer
     int64_t scores_ld;
-    // top-k of rows longer than 32,768 keys (null otherwise)
-    int* tk_hist;        // [Q, 2048] first-digit histograms, then the two [Q] counters (cleared per call)
-    int* tk_ncand;       // [Q] keys of the chosen first digit
-    int* tk_nabove;      // [Q] keys above the chosen first digit (< k)
-    uint2* tk_cand;      // [Q, kLongCand] (key, position) of the chosen first digit
-    int* tk_above;       // [Q, DSA_MAX_TOPK] positions of the keys above it
 };
 
 constexpr int kQprepBytes = 4 * kIH * kID;  // per query: >= 32 x 192 16-bit values and 3 x 32 x 128 e4m3
-constexpr int kLongChunk = 16384;      // keys per CTA in the long-row top-k
-constexpr int kLongCand = 8192;        // candidate slots per row
-constexpr int kLongMaxChunks = 1024;   // rows up to 16M keys take the chunked path
-
-inline bool topk_long_rows(int max_ctx) { return max_ctx > 32768; }
-inline int topk_chunks(int max_ctx) { return (max_ctx + kLongChunk - 1) / kLongChunk; }
-inline bool topk_chunked(int max_ctx) { return topk_long_rows(max_ctx) && topk_chunks(max_ctx) <= kLongMaxChunks; }
-
 // The attention's split count per query, and the scratch its partials take
 // (none for one split or a two-split cluster pair), with the partials held to
 // `cap` bytes (fewer splits otherwise)

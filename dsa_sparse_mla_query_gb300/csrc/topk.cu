@@ -12,10 +12,13 @@
 // smaller index) with block-wide prefix sums, so the output is the selected
 // positions in ascending order: deterministic and compacted.
 //
-// Three kernels share that scheme: rows up to 32,768 keys take one CTA each
-// with the row in registers (three passes of 11 + 11 + 10 bits); longer rows
-// up to 16 x 32,768 keys a thread-block cluster per row; anything longer one
-// CTA per row with four 8-bit passes over memory.
+// Three kernels share that scheme, one CTA per row each: rows up to 16,384
+// keys with the row in registers, up to 32,768 keys with the row in shared
+// memory (three passes of 11 + 11 + 10 bits), longer rows streamed from
+// memory in blocks (the first digit over the row, the finer two over the
+// keys of the chosen first digit).
+
+#include <cooperative_groups.h>
 
 #include <algorithm>
 #include <climits>
@@ -27,136 +30,10 @@
 
 namespace dsa {
 
-constexpr int kTopkThreads = 1024;
-constexpr int kTopkWarps = kTopkThreads / 32;
-
 __device__ __forceinline__ uint32_t order_key(float f) {
     uint32_t u = __float_as_uint(f);
     if (u == 0x80000000u) u = 0u;  // -0.0 ranks as +0.0
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// exclusive block prefix sum of v over kTopkThreads threads; *total = sum
-__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_buf, int* total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) warp_buf[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        int w = lane < kTopkWarps ? warp_buf[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += y;
-        }
-        warp_buf[32 + lane] = w;  // inclusive warp totals
-    }
-    __syncthreads();
-    const int before = (warp ? warp_buf[32 + warp - 1] : 0) + x - v;
-    *total = warp_buf[32 + kTopkWarps - 1];
-    __syncthreads();
-    return before;
-}
-
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ scores, int64_t ld, dsa_seqs s,
-                                                             int k, int32_t* __restrict__ idx,
-                                                             int32_t* __restrict__ topk_len, int32_t* d_status) {
-    pdl_enter();
-    __shared__ int hist[256];
-    __shared__ int scan_buf[64];
-    __shared__ int sel_digit, sel_above;
-    const int t = blockIdx.x;
-    const int tid = threadIdx.x;
-    const int b = seq_of(s.q_start, s.num_seqs, t);
-    const int pos = __ldg(s.q_pos + t);
-    const int ctx = __ldg(s.ctx_len + b);
-    int32_t* out = idx + (int64_t)t * k;
-    if (pos < 0 || pos >= ctx || ctx > s.max_ctx) {
-        if (tid == 0) {
-            report(d_status, DSA_ERR_BAD_INPUT);
-            topk_len[t] = 0;
-        }
-        for (int i = tid; i < k; i += kTopkThreads) out[i] = -1;
-        return;
-    }
-    const int n = pos + 1;
-    const float* row = scores + (int64_t)t * ld;
-    if (n <= k) {  // every causal key
-        for (int i = tid; i < k; i += kTopkThreads) out[i] = i < n ? i : -1;
-        if (tid == 0) topk_len[t] = n;
-        return;
-    }
-
-    // ---- radix select of the k-th largest order key
-    uint32_t prefix = 0, mask = 0;
-    int remaining = k;  // keys still to take among those matching prefix
-    for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        if (tid < 256) hist[tid] = 0;
-        __syncthreads();
-        for (int i = tid; i < n; i += kTopkThreads) {
-            const uint32_t u = order_key(__ldg(row + i));
-            if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255], 1);
-        }
-        __syncthreads();
-        // digits in descending order: thread i <-> digit 255 - i
-        int c = tid < 256 ? hist[255 - tid] : 0;
-        int tot;
-        const int before = block_exclusive_scan(c, scan_buf, &tot);
-        if (tid < 256 && before < remaining && before + c >= remaining) {
-            sel_digit = 255 - tid;
-            sel_above = before;
-        }
-        __syncthreads();
-        prefix |= (uint32_t)sel_digit << shift;
-        mask |= 255u << shift;
-        remaining -= sel_above;
-        __syncthreads();
-    }
-    const uint32_t T = prefix;  // exact key of the k-th largest score
-    const int need_eq = remaining;
-
-    // ---- compaction in index order (4 consecutive scores per thread)
-    int base_out = 0, base_eq = 0;
-    for (int start = 0; start < n; start += 4 * kTopkThreads) {
-        const int i0 = start + 4 * tid;
-        uint32_t u[4];
-        int n_eq = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            u[e] = (i0 + e < n) ? order_key(__ldg(row + i0 + e)) : 0u;
-            n_eq += (i0 + e < n && u[e] == T);
-        }
-        int tot_eq;
-        int eq_rank = base_eq + block_exclusive_scan(n_eq, scan_buf, &tot_eq);
-        bool take[4];
-        int n_sel = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const bool valid = i0 + e < n;
-            bool tk = valid && u[e] > T;
-            if (valid && u[e] == T) {
-                tk = eq_rank < need_eq;
-                ++eq_rank;
-            }
-            take[e] = tk;
-            n_sel += tk;
-        }
-        int tot_sel;
-        int o = base_out + block_exclusive_scan(n_sel, scan_buf, &tot_sel);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if (take[e] && o < k) out[o++] = i0 + e;
-        base_out += tot_sel;
-        base_eq += tot_eq;
-    }
-    for (int i = base_out + tid; i < k; i += kTopkThreads) out[i] = -1;
-    if (tid == 0) topk_len[t] = min(base_out, k);
 }
 
 // exclusive prefix sum over the THREADS threads of a block; *total = sum
@@ -557,49 +434,42 @@ __global__ void __launch_bounds__(1024, 1) topk_smem_kernel(const float* __restr
 }
 
 // ---------------------------------------------------------------------------
-// Rows longer than 32,768 keys: a chunked pipeline over every SM (no kernel
-// needs the CTAs of a row to be co-resident).  Chunks of kLongChunk keys.
-//   1. topk_hist_kernel  (chunk x row): histogram of the first digit (top 11
-//      bits of the order key) of each chunk, added into the row's histogram;
-//   2. topk_cand_kernel  (chunk x row): the digit d0 of the k-th key from the
-//      row's histogram; the positions of the chunk's keys above d0 (fewer than
-//      k in the row) and the keys of d0 (key, position) are appended to the
-//      row's lists, one reservation per CTA;
-//   3. topk_final_kernel (row): the exact k-th key T among the keys of d0
-//      (11 + 10 more bits; by passes over the row in memory when they
-//      overflowed their list), then the selected positions -- every key above
-//      d0, the keys of d0 above T and the smallest positions of the keys equal
-//      to T that are needed -- sorted ascending in shared memory.
-constexpr int kLongThreads = 1024;
-constexpr int kLongEPT = kLongChunk / kLongThreads;  // 16: four rounds of one float4 per thread
-constexpr int kFinalThreads = 1024;
-constexpr size_t kFinalSmem = (size_t)kLongCand * 8 + (size_t)kLongCand * 4 + 2048 * 4 + DSA_MAX_TOPK * 4;
+// Rows longer than 32,768 keys (any length): a thread-block cluster of P CTAs
+// per row (P = 1 when the rows alone fill the GPU, up to 8 for a few long
+// rows); CTA r streams its contiguous share of the row's 16,384-key blocks,
+// thread t holding 16 consecutive positions of a block (four float4 from one
+// 64-byte run), so that thread order is position order:
+//   1. the first digit's histogram over the row (the row from HBM), summed
+//      over the cluster in distributed shared memory: the digit d0 of the
+//      k-th key and the number of keys above it;
+//   2. the positions above d0 (fewer than k) and the keys of d0 with their
+//      positions, each list ascending (the row again, mostly from L2);
+//   3. two finer digits (11 + 10 bits) over the lists of the cluster (over
+//      the row when a list overflowed): the k-th key T and how many keys == T
+//      to take;
+//   4. each CTA's count of selected keys (and of keys == T) through the
+//      cluster: its slice of the output, where it merges its two ascending
+//      lists.
+// No global atomics, no scratch, no sort; every barrier is over the cluster,
+// whose CTAs run together.
+constexpr int kStreamThreads = 1024;
+constexpr int kStreamEPT = 16;
+constexpr int kStreamBlock = kStreamThreads * kStreamEPT;  // 16384 keys
+constexpr int kStreamCand = 8192;                           // keys of d0 a CTA lists
+constexpr int kStreamMaxP = 8;
+// h [4][2048], hs [2048], ck/cp [kStreamCand], ap [2048], sel [2048]
+constexpr size_t kStreamSmem = (size_t)(5 * 2048 + 2 * kStreamCand + 2 * DSA_MAX_TOPK) * 4;
 
-// false: nothing for the chunk kernels to do on row t (a bad row is reported
-// by the final kernel; a row of at most k keys is written by it)
-__device__ __forceinline__ bool long_row(const dsa_seqs& s, int t, int k, int* n_out) {
-    const int b = seq_of(s.q_start, s.num_seqs, t);
-    const int pos = __ldg(s.q_pos + t);
-    const int ctx = __ldg(s.ctx_len + b);
-    if (pos < 0 || pos >= ctx || ctx > s.max_ctx) return false;
-    *n_out = pos + 1;
-    return pos + 1 > k;
-}
+__device__ __forceinline__ int stream_pos(int j0, int e) { return j0 + (int)threadIdx.x * kStreamEPT + e; }
 
-// position of this thread's key e in the chunk starting at j0: round e / 4 of
-// coalesced float4 loads (a warp reads 512 contiguous bytes), component e % 4
-__device__ __forceinline__ int chunk_pos(int j0, int e) {
-    return j0 + ((e >> 2) * kLongThreads + (int)threadIdx.x) * 4 + (e & 3);
-}
-
-__device__ __forceinline__ void chunk_keys(const float* row, int64_t ld, int j0, uint32_t* u) {
-    const int last4 = (int)((ld - 4) & ~(int64_t)3);
-    uint4 r[kLongEPT / 4];
+// this thread's 16 positions of the block at j0 as order keys (loads clamped into the row)
+__device__ __forceinline__ void stream_block(const float* row, int last4, int j0, uint32_t (&u)[kStreamEPT]) {
+    uint4 r[kStreamEPT / 4];
 #pragma unroll
-    for (int v = 0; v < kLongEPT / 4; ++v)
-        r[v] = __ldg(reinterpret_cast<const uint4*>(row + min(j0 + (v * kLongThreads + (int)threadIdx.x) * 4, last4)));
+    for (int v = 0; v < kStreamEPT / 4; ++v)
+        r[v] = __ldg(reinterpret_cast<const uint4*>(row + min(stream_pos(j0, 4 * v), last4)));
 #pragma unroll
-    for (int v = 0; v < kLongEPT / 4; ++v) {
+    for (int v = 0; v < kStreamEPT / 4; ++v) {
         u[4 * v] = order_key(__uint_as_float(r[v].x));
         u[4 * v + 1] = order_key(__uint_as_float(r[v].y));
         u[4 * v + 2] = order_key(__uint_as_float(r[v].z));
@@ -607,273 +477,292 @@ __device__ __forceinline__ void chunk_keys(const float* row, int64_t ld, int j0,
     }
 }
 
-// The first digit of the k-th largest key of a row from its histogram, and
-// the number of keys in higher digits; the same result in every thread.
-template <int THREADS>
-__device__ __forceinline__ void first_digit(const int* hr, int k, int* buf, int* sh, int& d0, int& above) {
-    constexpr int PER = 2048 / THREADS;
-    int c[PER], csum = 0;
-#pragma unroll
-    for (int q = 0; q < PER; ++q) {
-        c[q] = __ldcg(hr + 2047 - PER * (int)threadIdx.x - q);
-        csum += c[q];
-    }
+// the digit (of nb, descending, 1 or 2 per thread) holding the remaining-th
+// key in the histogram hs, and the keys in higher digits; every thread
+template <int NT>
+__device__ __forceinline__ void select_digit(const int* hs, int nb, int remaining, int* buf, int* sh, int& digit,
+                                             int& above) {
+    const int per = nb / NT;
+    const int dA = nb - 1 - per * (int)threadIdx.x;
+    const int cA = hs[dA], cB = per == 2 ? hs[dA - 1] : 0;
     int tot;
-    int before = scan_threads<THREADS>(csum, buf, &tot);
-#pragma unroll
-    for (int q = 0; q < PER; ++q) {
-        if (before < k && before + c[q] >= k) {
-            sh[0] = 2047 - PER * (int)threadIdx.x - q;
-            sh[1] = before;
-        }
-        before += c[q];
+    const int before = scan_threads<NT>(cA + cB, buf, &tot);
+    if (before < remaining && before + cA >= remaining) {
+        sh[0] = dA;
+        sh[1] = before;
+    } else if (per == 2 && before + cA < remaining && before + cA + cB >= remaining) {
+        sh[0] = dA - 1;
+        sh[1] = before + cA;
     }
     __syncthreads();
-    d0 = sh[0];
+    digit = sh[0];
     above = sh[1];
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kLongThreads) topk_hist_kernel(const float* __restrict__ scores, int64_t ld,
-                                                                  dsa_seqs s, int k, int* __restrict__ hist) {
-    pdl_enter();
-    __shared__ int h[4][2048];
-    const int t = blockIdx.y, j0 = blockIdx.x * kLongChunk;
-    int n = 0;
-    if (!long_row(s, t, k, &n) || j0 >= n) return;  // uniform over the CTA
-    for (int i = threadIdx.x; i < 4 * 2048; i += kLongThreads) (&h[0][0])[i] = 0;
-    __syncthreads();
-    uint32_t u[kLongEPT];
-    chunk_keys(scores + (int64_t)t * ld, ld, j0, u);
-    int* hw = h[(threadIdx.x >> 5) & 3];  // four copies spread the same-address atomics
-#pragma unroll
-    for (int e = 0; e < kLongEPT; ++e)
-        if (chunk_pos(j0, e) < n) atomicAdd(hw + (u[e] >> 21), 1);
-    __syncthreads();
-    int* hr = hist + (int64_t)t * 2048;
-    for (int b = threadIdx.x; b < 2048; b += kLongThreads) {
-        const int v = h[0][b] + h[1][b] + h[2][b] + h[3][b];
-        if (v) atomicAdd(hr + b, v);
+// hs = the sum over the cluster's CTAs of their local histograms h (after a
+// cluster barrier that makes them complete)
+__device__ __forceinline__ void cluster_hist_sum(cooperative_groups::cluster_group& cl, int* h, int* hs, int P) {
+    for (int i = threadIdx.x; i < 2048; i += kStreamThreads) {
+        int v = 0;
+        for (int r = 0; r < P; ++r) v += cl.map_shared_rank(h, r)[i];
+        hs[i] = v;
     }
 }
 
-__global__ void __launch_bounds__(kLongThreads) topk_cand_kernel(const float* __restrict__ scores, int64_t ld,
-                                                                  dsa_seqs s, int k, const int* __restrict__ hist,
-                                                                  int* __restrict__ ncand, int* __restrict__ nabove,
-                                                                  uint2* __restrict__ cand, int* __restrict__ above_pos) {
-    pdl_enter();
-    __shared__ int buf[64], sh[2];
-    const int t = blockIdx.y, j0 = blockIdx.x * kLongChunk;
-    int n = 0;
-    if (!long_row(s, t, k, &n) || j0 >= n) return;
-    uint32_t u[kLongEPT];
-    chunk_keys(scores + (int64_t)t * ld, ld, j0, u);  // in flight while the digit is found
-    int d0, above;
-    first_digit<kLongThreads>(hist + (int64_t)t * 2048, k, buf, sh, d0, above);
-    int na = 0, nc = 0;
-#pragma unroll
-    for (int e = 0; e < kLongEPT; ++e) {
-        const int dg = chunk_pos(j0, e) < n ? (int)(u[e] >> 21) : -1;
-        na += dg > d0;
-        nc += dg == d0;
+// first index i of a[0 .. n) (ascending) with a[i] > v
+__device__ __forceinline__ int upper_idx(const int* a, int n, int v) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] <= v) lo = mid + 1;
+        else hi = mid;
     }
-    // one reservation per CTA and list (the chunks of a row share the counters)
-    int tot_a, tot_c;
-    int sa = scan_threads<kLongThreads>(na, buf, &tot_a);
-    int sc = scan_threads<kLongThreads>(nc, buf, &tot_c);
-    if (threadIdx.x == 0) {
-        sh[0] = tot_a > 0 ? atomicAdd(nabove + t, tot_a) : 0;
-        sh[1] = tot_c > 0 ? atomicAdd(ncand + t, tot_c) : 0;
-    }
-    __syncthreads();
-    sa += sh[0];
-    sc += sh[1];
-    int* ar = above_pos + (int64_t)t * DSA_MAX_TOPK;
-    uint2* cr = cand + (int64_t)t * kLongCand;
-#pragma unroll
-    for (int e = 0; e < kLongEPT; ++e) {
-        const int p = chunk_pos(j0, e);
-        const int dg = p < n ? (int)(u[e] >> 21) : -1;
-        if (dg > d0) {
-            if (sa < DSA_MAX_TOPK) ar[sa] = p;
-            ++sa;
-        } else if (dg == d0) {
-            if (sc < kLongCand) cr[sc] = make_uint2(u[e], (uint32_t)p);
-            ++sc;
-        }
-    }
+    return lo;
 }
 
-// ascending bitonic sort of a[0 .. N), N a power of two, by the whole block
-template <int THREADS>
-__device__ void bitonic_sort(int* a, int N) {
-    for (int size = 2; size <= N; size <<= 1)
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = threadIdx.x; i < N / 2; i += THREADS) {
-                const int lo = 2 * i - (i & (stride - 1));
-                const int hi = lo + stride;
-                const bool up = (lo & size) == 0;
-                const int x = a[lo], y = a[hi];
-                if ((x > y) == up) {
-                    a[lo] = y;
-                    a[hi] = x;
-                }
-            }
-            __syncthreads();
-        }
-}
-
-__global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(
-    const float* __restrict__ scores, int64_t ld, dsa_seqs s, int k, int32_t* __restrict__ idx,
-    int32_t* __restrict__ topk_len, const int* __restrict__ hist, const int* __restrict__ ncand,
-    const int* __restrict__ nabove, const uint2* __restrict__ cand, const int* __restrict__ above_pos,
-    int32_t* d_status) {
-    constexpr int NT = kFinalThreads;
+__global__ void __launch_bounds__(kStreamThreads, 1) topk_stream_kernel(const float* __restrict__ scores, int64_t ld,
+                                                                         dsa_seqs s, int k, int32_t* __restrict__ idx,
+                                                                         int32_t* __restrict__ topk_len,
+                                                                         int32_t* d_status) {
+    constexpr int NT = kStreamThreads;
     pdl_enter();
-    extern __shared__ __align__(16) int fn_smem[];
-    uint32_t* ck = reinterpret_cast<uint32_t*>(fn_smem);  // [kLongCand] keys of d0
-    int* cp = fn_smem + kLongCand;                        // [kLongCand] their positions
-    int* tie = cp + kLongCand;                            // [kLongCand] positions of keys == T
-    int* hs = tie + kLongCand;                            // [2048] digit histogram
-    int* sel = hs + 2048;                                 // [DSA_MAX_TOPK] selected positions
-    __shared__ int buf[64], sh[4];
-    const int t = blockIdx.x, tid = threadIdx.x;
+    cooperative_groups::cluster_group cl = cooperative_groups::this_cluster();
+    const int P = (int)cl.num_blocks(), me = (int)cl.block_rank();
+    extern __shared__ __align__(16) int st_smem[];
+    int* h = st_smem;                                        // [4][2048] local histograms (h[0..2048): their sum)
+    int* hs = h + 4 * 2048;                                  // [2048] the cluster's histogram
+    uint32_t* ck = reinterpret_cast<uint32_t*>(hs + 2048);  // [kStreamCand] keys of d0 in this CTA's range
+    int* cp = reinterpret_cast<int*>(ck + kStreamCand);     // [kStreamCand] their positions
+    int* ap = cp + kStreamCand;                              // [DSA_MAX_TOPK] positions above d0 (this range)
+    int* sel = ap + DSA_MAX_TOPK;                            // [DSA_MAX_TOPK] selected positions of d0 (this range)
+    __shared__ int buf[64], sh[2], xch[4];
+    const int t = blockIdx.x / P, tid = threadIdx.x, warp = tid >> 5;
     const int b = seq_of(s.q_start, s.num_seqs, t);
     const int pos = __ldg(s.q_pos + t);
     const int ctx = __ldg(s.ctx_len + b);
     int32_t* out = idx + (int64_t)t * k;
+    // (the same row for every CTA of the cluster: these exits are uniform)
     if (pos < 0 || pos >= ctx || ctx > s.max_ctx) {
-        if (tid == 0) {
-            report(d_status, DSA_ERR_BAD_INPUT);
-            topk_len[t] = 0;
+        if (me == 0) {
+            if (tid == 0) {
+                report(d_status, DSA_ERR_BAD_INPUT);
+                topk_len[t] = 0;
+            }
+            for (int i = tid; i < k; i += NT) out[i] = -1;
         }
-        for (int i = tid; i < k; i += NT) out[i] = -1;
         return;
     }
     const int n = pos + 1;
     if (n <= k) {
-        for (int i = tid; i < k; i += NT) out[i] = i < n ? i : -1;
-        if (tid == 0) topk_len[t] = n;
+        if (me == 0) {
+            for (int i = tid; i < k; i += NT) out[i] = i < n ? i : -1;
+            if (tid == 0) topk_len[t] = n;
+        }
         return;
     }
-    int d0, above;
-    first_digit<NT>(hist + (int64_t)t * 2048, k, buf, sh, d0, above);
-    const uint32_t dpre = (uint32_t)d0 << 21, dmask = 0x7FFu << 21;
-    uint32_t prefix = dpre, mask = dmask;
-    int remaining = k - above;
-    const int nc = __ldcg(ncand + t);
-    const bool in_smem = nc <= kLongCand;
     const float* row = scores + (int64_t)t * ld;
-    if (in_smem)
-        for (int i = tid; i < nc; i += NT) {
-            const uint2 e = __ldcg(cand + (int64_t)t * kLongCand + i);
-            ck[i] = e.x;
-            cp[i] = (int)e.y;
+    const int last4 = (int)((ld - 4) & ~(int64_t)3);
+    const int nblk = (n + kStreamBlock - 1) / kStreamBlock;
+    const int b0 = (int)((int64_t)nblk * me / P), b1 = (int)((int64_t)nblk * (me + 1) / P);  // this CTA's blocks
+    uint32_t u[kStreamEPT];
+
+    // ---- 1: the first digit over the row
+    for (int i = tid; i < 4 * 2048; i += NT) h[i] = 0;
+    __syncthreads();
+    {
+        int* hw = h + (warp & 3) * 2048;  // four copies spread the same-address atomics
+        for (int blk = b0; blk < b1; ++blk) {
+            const int j0 = blk * kStreamBlock;
+            stream_block(row, last4, j0, u);
+#pragma unroll
+            for (int e = 0; e < kStreamEPT; ++e)
+                if (stream_pos(j0, e) < n) atomicAdd(hw + (u[e] >> 21), 1);
         }
-    // two more digit passes (11 then 10 bits) over the keys of d0
+    }
+    __syncthreads();
+    for (int i = tid; i < 2048; i += NT) h[i] += h[2048 + i] + h[4096 + i] + h[6144 + i];
+    cl.sync();
+    cluster_hist_sum(cl, h, hs, P);
+    __syncthreads();
+    int d0, above;
+    select_digit<NT>(hs, 2048, k, buf, sh, d0, above);
+    uint32_t prefix = (uint32_t)d0 << 21, mask = 0x7FFu << 21;
+    int remaining = k - above;
+
+    // ---- 2: the positions above d0 and the keys of d0, ascending
+    int na = 0, nc = 0;  // this CTA's so far (the same in every thread)
+    for (int blk = b0; blk < b1; ++blk) {
+        const int j0 = blk * kStreamBlock;
+        stream_block(row, last4, j0, u);
+        int ca = 0, cc = 0;
+#pragma unroll
+        for (int e = 0; e < kStreamEPT; ++e) {
+            const int dg = stream_pos(j0, e) < n ? (int)(u[e] >> 21) : -1;
+            ca += dg > d0;
+            cc += dg == d0;
+        }
+        int tot;
+        const int pk = scan_threads<NT>((ca << 16) | cc, buf, &tot);  // each at most 16384 per block
+        int oa = na + (pk >> 16), oc = nc + (pk & 0xFFFF);
+#pragma unroll
+        for (int e = 0; e < kStreamEPT; ++e) {
+            const int p = stream_pos(j0, e);
+            const int dg = p < n ? (int)(u[e] >> 21) : -1;
+            if (dg > d0) {
+                if (oa < DSA_MAX_TOPK) ap[oa] = p;
+                ++oa;
+            } else if (dg == d0) {
+                if (oc < kStreamCand) {
+                    ck[oc] = u[e];
+                    cp[oc] = p;
+                }
+                ++oc;
+            }
+        }
+        na += tot >> 16;
+        nc += tot & 0xFFFF;
+    }
+    if (tid == 0) xch[0] = nc > kStreamCand;
+    cl.sync();  // also: every CTA has summed the others' first histograms
+    bool over = false;  // some CTA's list of d0 overflowed: the finer digits come from the row
+    for (int r = 0; r < P; ++r) over |= cl.map_shared_rank(xch, r)[0] != 0;
+
+    // ---- 3: two finer digits over the cluster's keys of d0
 #pragma unroll 1
     for (int pass = 0; pass < 2; ++pass) {
         const int shift = pass == 0 ? 10 : 0;
         const int nb = pass == 0 ? 2048 : 1024;
-        for (int i = tid; i < 2048; i += NT) hs[i] = 0;
+        for (int i = tid; i < 2048; i += NT) h[i] = 0;
         __syncthreads();
-        if (in_smem) {
+        if (!over) {
             for (int i = tid; i < nc; i += NT)
-                if ((ck[i] & mask) == prefix) atomicAdd(hs + ((ck[i] >> shift) & (nb - 1)), 1);
+                if ((ck[i] & mask) == prefix) atomicAdd(h + ((ck[i] >> shift) & (nb - 1)), 1);
         } else {
-            for (int j = tid; j < n; j += NT) {
-                const uint32_t u = order_key(__ldg(row + j));
-                if ((u & mask) == prefix) atomicAdd(hs + ((u >> shift) & (nb - 1)), 1);
+            for (int blk = b0; blk < b1; ++blk) {
+                const int j0 = blk * kStreamBlock;
+                stream_block(row, last4, j0, u);
+#pragma unroll
+                for (int e = 0; e < kStreamEPT; ++e)
+                    if (stream_pos(j0, e) < n && (u[e] & mask) == prefix)
+                        atomicAdd(h + ((u[e] >> shift) & (nb - 1)), 1);
             }
         }
-        __syncthreads();
-        const int per = nb / NT;  // 2 or 1 digits per thread, descending
-        const int dA = nb - 1 - per * tid;
-        const int cA = hs[dA], cB = per == 2 ? hs[dA - 1] : 0;
-        int tot;
-        const int before = scan_threads<NT>(cA + cB, buf, &tot);
-        if (before < remaining && before + cA >= remaining) {
-            sh[0] = dA;
-            sh[1] = before;
-        } else if (per == 2 && before + cA < remaining && before + cA + cB >= remaining) {
-            sh[0] = dA - 1;
-            sh[1] = before + cA;
-        }
-        __syncthreads();
-        prefix |= (uint32_t)sh[0] << shift;
+        cl.sync();
+        cluster_hist_sum(cl, h, hs, P);
+        cl.sync();  // every CTA has read the others' histograms before they change
+        int dg, ab;
+        select_digit<NT>(hs, nb, remaining, buf, sh, dg, ab);
+        prefix |= (uint32_t)dg << shift;
         mask |= (uint32_t)(nb - 1) << shift;
-        remaining -= sh[1];
-        __syncthreads();
+        remaining -= ab;
     }
     const uint32_t T = prefix;
-    const int need_eq = remaining;  // keys == T to take, >= 1
-    // the selection: every key above d0, the keys of d0 above T, then the
-    // need_eq smallest positions among the keys equal to T
-    const int na = min(__ldcg(nabove + t), DSA_MAX_TOPK);  // == above
-    for (int i = tid; i < na; i += NT) sel[i] = __ldcg(above_pos + (int64_t)t * DSA_MAX_TOPK + i);
-    if (tid == 0) {
-        sh[2] = na;  // next free slot of sel
-        sh[3] = 0;   // ties found
+    const int need_eq = remaining;  // keys == T to take over the row, >= 1
+
+    // ---- 4: this CTA's keys of d0 above T and equal to T; through the
+    // cluster, its slice of the output and its share of the keys == T
+    int g_me, e_me;
+    {
+        int gt = 0, eq = 0;
+        if (!over) {
+            for (int i = tid; i < nc; i += NT) {
+                gt += ck[i] > T;
+                eq += ck[i] == T;
+            }
+        } else {
+            for (int blk = b0; blk < b1; ++blk) {
+                const int j0 = blk * kStreamBlock;
+                stream_block(row, last4, j0, u);
+#pragma unroll
+                for (int e = 0; e < kStreamEPT; ++e)
+                    if (stream_pos(j0, e) < n && (int)(u[e] >> 21) == d0) {
+                        gt += u[e] > T;
+                        eq += u[e] == T;
+                    }
+            }
+        }
+        scan_threads<NT>(gt, buf, &g_me);
+        scan_threads<NT>(eq, buf, &e_me);
     }
-    __syncthreads();
-    if (in_smem) {
-        // compaction by prefix sums: thread tid takes candidates [i0, i1)
-        const int per = (nc + NT - 1) / NT;
+    if (tid == 0) {
+        xch[1] = na;
+        xch[2] = g_me;
+        xch[3] = e_me;
+    }
+    cl.sync();
+    int eq_before = 0, out_before = 0;  // over the cluster's earlier CTAs (earlier positions)
+    for (int r = 0; r < me; ++r) {
+        const int* x = cl.map_shared_rank(xch, r);
+        out_before += x[1] + x[2] + max(0, min(need_eq - eq_before, x[3]));
+        eq_before += x[3];
+    }
+    const int quota = max(0, min(need_eq - eq_before, e_me));  // keys == T this CTA takes
+    const int m = min(g_me + quota, DSA_MAX_TOPK);
+
+    // ---- 5: this CTA's selected keys of d0, ascending, merged with its
+    // positions above d0 into its slice of the output
+    if (!over) {
+        const int per = (nc + NT - 1) / NT;  // consecutive list entries per thread
         const int i0 = min(tid * per, nc), i1 = min(i0 + per, nc);
         int ng = 0, nq = 0;
         for (int i = i0; i < i1; ++i) {
             ng += ck[i] > T;
             nq += ck[i] == T;
         }
-        int tg, tq;
-        int og = na + scan_threads<NT>(ng, buf, &tg);
-        int oq = scan_threads<NT>(nq, buf, &tq);
+        int tq;
+        int er = scan_threads<NT>(nq, buf, &tq);
+        const int ns = ng + max(0, min(quota - er, nq));
+        int tb;
+        int o = scan_threads<NT>(ns, buf, &tb);
         for (int i = i0; i < i1; ++i) {
-            if (ck[i] > T) sel[og++] = cp[i];
-            else if (ck[i] == T) tie[oq++] = cp[i];
+            bool take = ck[i] > T;
+            if (ck[i] == T) take = er++ < quota;
+            if (take && o < DSA_MAX_TOPK) sel[o++] = cp[i];
         }
-        if (tid == 0) {
-            sh[2] = na + tg;
-            sh[3] = tq;
-        }
-        __syncthreads();
-        const int ne = sh[3];
-        if (ne > need_eq) {  // keep the smallest positions
-            int N = 1;
-            while (N < ne) N <<= 1;
-            for (int i = ne + tid; i < N; i += NT) tie[i] = INT_MAX;
-            __syncthreads();
-            bitonic_sort<NT>(tie, N);
-        }
-        const int base = sh[2];
-        for (int i = tid; i < need_eq; i += NT) sel[base + i] = tie[i];
     } else {
-        // keys of d0 above T from the row; ties in position order, block by block
-        for (int j = tid; j < n; j += NT) {
-            const uint32_t u = order_key(__ldg(row + j));
-            if ((u & dmask) == dpre && u > T) sel[atomicAdd(sh + 2, 1)] = j;
-        }
-        __syncthreads();
-        int taken = 0;
-        const int base = sh[2];
-        for (int j0 = 0; j0 < n && taken < need_eq; j0 += NT) {
-            const int j = j0 + tid;
-            const bool eq = j < n && order_key(__ldg(row + j)) == T;
+        int o_base = 0, er_base = 0;
+        for (int blk = b0; blk < b1 && o_base < m; ++blk) {
+            const int j0 = blk * kStreamBlock;
+            stream_block(row, last4, j0, u);
+            int ng = 0, nq = 0;
+#pragma unroll
+            for (int e = 0; e < kStreamEPT; ++e)
+                if (stream_pos(j0, e) < n && (int)(u[e] >> 21) == d0) {
+                    ng += u[e] > T;
+                    nq += u[e] == T;
+                }
             int tot;
-            const int r = scan_threads<NT>(eq ? 1 : 0, buf, &tot);
-            if (eq && taken + r < need_eq) sel[base + taken + r] = j;
-            taken += tot;
+            const int pk = scan_threads<NT>((ng << 16) | nq, buf, &tot);  // each at most 16384 per block
+            const int left = max(quota - er_base, 0);                     // keys == T still to take
+            int er = er_base + (pk & 0xFFFF);
+            int o = o_base + (pk >> 16) + min(left, pk & 0xFFFF);
+#pragma unroll
+            for (int e = 0; e < kStreamEPT; ++e) {
+                const int p = stream_pos(j0, e);
+                if (p >= n || (int)(u[e] >> 21) != d0) continue;
+                bool take = u[e] > T;
+                if (u[e] == T) take = er++ < quota;
+                if (take && o < DSA_MAX_TOPK) sel[o++] = p;
+            }
+            o_base += (tot >> 16) + min(left, tot & 0xFFFF);
+            er_base += tot & 0xFFFF;
         }
     }
     __syncthreads();
-    // k positions, ascending (k <= 2048 slots, padded to a power of two)
-    int N = 1;
-    while (N < k) N <<= 1;
-    for (int i = k + tid; i < N; i += NT) sel[i] = INT_MAX;
-    __syncthreads();
-    bitonic_sort<NT>(sel, N);
-    for (int i = tid; i < k; i += NT) out[i] = sel[i];
-    if (tid == 0) topk_len[t] = k;
+    const int nna = min(na, DSA_MAX_TOPK);
+    for (int i = tid; i < nna; i += NT) {
+        const int v = ap[i];
+        const int at = out_before + i + upper_idx(sel, m, v);
+        if (at < k) out[at] = v;
+    }
+    for (int j = tid; j < m; j += NT) {
+        const int v = sel[j];
+        const int at = out_before + j + upper_idx(ap, nna, v);
+        if (at < k) out[at] = v;
+    }
+    if (me == 0 && tid == 0) topk_len[t] = k;
+    cl.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 namespace {
@@ -910,6 +799,7 @@ cudaError_t launch_smem_row(const float* scores, int64_t ld, const dsa_seqs& s, 
 
 cudaError_t launch_topk(const float* scores, int64_t ld, const dsa_seqs& s, int num_q, int k, int32_t* idx,
                         int32_t* topk_len, const Workspace& ws, int32_t* d_status, cudaStream_t stream) {
+    (void)ws;  // no scratch
     // rows up to 32,768 keys: one CTA per row
     if (s.max_ctx <= 1024 * 8)
         return launch_row<1024, 8>(scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
@@ -917,31 +807,19 @@ cudaError_t launch_topk(const float* scores, int64_t ld, const dsa_seqs& s, int 
         return launch_row<1024, 16>(scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
     if (s.max_ctx <= 1024 * 32)
         return launch_smem_row<32>(scores, ld, s, num_q, k, idx, topk_len, d_status, stream);
-    const int C = topk_chunks(s.max_ctx);
-    if (topk_chunked(s.max_ctx) && ws.tk_hist) {
-        static std::once_flag once;
-        static cudaError_t attr = cudaSuccess;
-        std::call_once(once, [] {
-            attr = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kFinalSmem);
-        });
-        if (attr != cudaSuccess) return attr;
-        cudaError_t e = cudaMemsetAsync(ws.tk_hist, 0, (size_t)num_q * (2048 + 2) * 4, stream);
-        if (e == cudaSuccess)
-            e = launch_pdl(topk_hist_kernel, dim3(C, num_q), dim3(kLongThreads), 0, stream, 1, scores, ld, s, k,
-                           ws.tk_hist);
-        if (e == cudaSuccess)
-            e = launch_pdl(topk_cand_kernel, dim3(C, num_q), dim3(kLongThreads), 0, stream, 1, scores, ld, s, k,
-                           (const int*)ws.tk_hist, ws.tk_ncand, ws.tk_nabove, ws.tk_cand, ws.tk_above);
-        if (e == cudaSuccess)
-            e = launch_pdl(topk_final_kernel, dim3(num_q), dim3(kFinalThreads), kFinalSmem, stream, 1, scores, ld, s,
-                           k, idx, topk_len, (const int*)ws.tk_hist, (const int*)ws.tk_ncand,
-                           (const int*)ws.tk_nabove, (const uint2*)ws.tk_cand, (const int*)ws.tk_above, d_status);
-        return e;
-    }
-    // rows longer than 16M keys: one CTA per row, passes over memory
-    return launch_pdl(topk_kernel, dim3(num_q), dim3(kTopkThreads), 0, stream, 1, scores, ld, s, k, idx, topk_len,
-                      d_status);
+    // longer rows: a cluster of P CTAs per row streams the row; P fills the
+    // GPU's SMs when the rows are few (a power of two, at most 8, and no more
+    // than the longest row's blocks)
+    int P = 1;
+    while (P < kStreamMaxP && (int64_t)num_q * P * 2 <= 152 && P * kStreamBlock < s.max_ctx) P *= 2;
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(topk_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStreamSmem);
+    });
+    if (attr != cudaSuccess) return attr;
+    return launch_pdl(topk_stream_kernel, dim3((unsigned)num_q * P), dim3(kStreamThreads), kStreamSmem, stream, P,
+                      scores, ld, s, k, idx, topk_len, d_status);
 }
 
 }  // namespace dsa

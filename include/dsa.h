@@ -162,9 +162,8 @@ dsa_status dsa_index_scores_nvfp4(const void* q_idx, const float* w, const float
  *   scores   fp32 [num_q, ld] (as written by dsa_index_scores)
  *   idx      int32 [num_q, k]: selected positions in ascending order, then -1
  *   topk_len int32 [num_q]: number of selected positions
- *   workspace: unused (may be NULL) when max_ctx <= 32768; for longer rows at
- *            least dsa_workspace_size bytes, 256-byte aligned (scratch of the
- *            chunked selection; calls sharing it must be serialised)
+ *   workspace, workspace_bytes: unused (may be NULL and 0): the selection
+ *            needs no scratch at any row length
  * 1 <= k <= 2048. */
 dsa_status dsa_topk(const float* scores, int64_t ld, const dsa_seqs* seqs, int32_t num_q, int32_t k, int32_t* idx,
                     int32_t* topk_len, void* workspace, size_t workspace_bytes, int32_t* d_status,
@@ -448,8 +447,8 @@ dsa_status sparse_mla_decode_noalloc(const void* q, const void* latent, dsa_dtyp
 /* Number of kernels dsa_decode_layer enqueues for these sizes (reuse_idx and
  * latent_dtype as in dsa_layer_args); 0 when the sizes or the dtype are
  * refused.  For callers that count or capture launches.  (The attention adds
- * its combine kernel only when some query's work is cut between CTAs; the
- * count reads the current device's SM count.) */
+ * its combine kernel when three or more CTAs share a query's selection; the
+ * split count is planned for GB300's 152 SMs.) */
 int32_t dsa_decode_layer_launches(const dsa_seqs* seqs, int32_t num_q, int32_t k, int32_t reuse_idx,
                                   dsa_dtype latent_dtype);
 /* The same count for a full argument set (it also reads select_block); 0 when

@@ -181,22 +181,23 @@ def test_two_splits_combine_in_cluster():
     _check_workload(d, wl, list(range(wl.num_queries)))
 
 
-def test_long_rows_chunked_topk():
-    """Rows longer than 32,768 keys take the chunked top-k: ragged chunks
-    (32769, 40001), a longer row (70000) and, in the same launch, a row of at
-    most k keys (1000)."""
+def test_long_rows_streamed_topk():
+    """Rows longer than 32,768 keys take the streamed top-k: ragged last
+    blocks (32769, 40001), a longer row (70000) and, in the same launch, a row
+    of at most k keys (1000)."""
     wl = I.scaled(W["tiny"], num_seqs=4, ctx=None, ctx_list=(40001, 1000, 70000, 32769), queries_per_seq=1)
     d, _ = _inputs_cpu_then_gpu(wl)
     step = DecodeStep(d, wl.queries_per_seq, wl.topk)
-    # query prep, scores, three top-k kernels, attention in 16 splits + their combine
-    assert step.launches_per_step() == 2 + 3 + 2
+    # query prep, scores, top-k, attention in 16 splits + their combine
+    assert step.launches_per_step() == 2 + 1 + 2
     _check_workload(d, wl, list(range(wl.num_queries)), threads=4)
 
 
 def test_long_rows_all_equal_scores():
     """w = 0 makes every score 0: every key of a long row falls into one
-    first digit, more than the candidate buffer holds, so the exact k-th key
-    is found by passes over the row; the selection is positions 0..k-1."""
+    first digit, more than the list of that digit's keys holds, so the finer
+    digits are found by passes over the row; the selection is positions
+    0..k-1."""
     wl = I.scaled(W["tiny"], num_seqs=2, ctx=None, ctx_list=(40000, 50000), queries_per_seq=1)
     d, _ = _inputs_cpu_then_gpu(wl)
     d["w"].zero_()
