@@ -4,8 +4,15 @@
  * definitions on the pages.  Only the tests, the package smoke check and the
  * benchmark's CPU-baseline leg use it.  See dsa_oracle.h for the sources.
  *
- * Parity pins live in tests/test_oracle.py (closed forms, invariants, special
- * cases, brute force on tiny inputs).
+ * Its pins are defined in tests/oracle_pins.py and run by tests/test_oracle.py
+ * (closed forms, invariants, special cases, brute force on tiny inputs);
+ * tests/test_oracle_mutants.py plants mistakes in a copy and checks each is
+ * caught.
+ *
+ * Plain C rather than C++: every operation is written out where it happens
+ * (no overloads, templates or library algorithms between a formula and the
+ * code), the same gcc build with -ffp-contract=off rounds alike on x86 and
+ * Arm, and the unmangled symbols load directly through ctypes.
  */
 #include "dsa_oracle.h"
 
