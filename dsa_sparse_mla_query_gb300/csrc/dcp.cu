@@ -202,37 +202,58 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(ListPtrs list
 }
 
 // ---------------------------------------------------------------------------
-// Top-k compaction for one rank: one warp per query keeps, in order, the
-// slots i < topk_len holding an id >= 0 that the rank owns, as local
-// positions; the rest of the row -1.  Every slot is read before any write at
-// or after it, so the output may be the input.
-__global__ void __launch_bounds__(128) topk_compact_kernel(const int32_t* idx, const int32_t* topk_len,
-                                                           int num_q, int k, int world, int rank, int inter,
-                                                           int32_t* local_idx, int32_t* local_len,
-                                                           int32_t* d_status) {
+// Top-k compaction for one rank: the slots i < topk_len holding an id >= 0
+// that the rank owns, in order, as local positions; the rest of the row -1.
+// One CTA of 256 threads per query, thread i holding the 8 consecutive slots
+// 8i .. 8i + 7 (k <= 2048): every slot is read before the block's prefix sum
+// and written after it, so the output may be the input.
+constexpr int kCompactThreads = 256;
+constexpr int kCompactPer = DSA_MAX_TOPK / kCompactThreads;  // 8
+
+__global__ void __launch_bounds__(kCompactThreads) topk_compact_kernel(const int32_t* idx, const int32_t* topk_len,
+                                                                       int num_q, int k, int world, int rank,
+                                                                       int inter, int32_t* local_idx,
+                                                                       int32_t* local_len, int32_t* d_status) {
     pdl_enter();
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
-    if (t >= num_q) return;
+    __shared__ int wsum[kCompactThreads / 32];
+    const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int len = topk_len[t];
     if (len < 0 || len > k) {
-        if (lane == 0) report(d_status, DSA_ERR_BAD_INPUT);
+        if (tid == 0) report(d_status, DSA_ERR_BAD_INPUT);
         len = len < 0 ? 0 : k;
     }
     const int32_t* in = idx + (int64_t)t * k;
     int32_t* out = local_idx + (int64_t)t * k;
-    int cnt = 0;
-    for (int base = 0; base < len; base += 32) {
-        const int i = base + lane;
+    int loc[kCompactPer];
+    int c = 0;
+#pragma unroll
+    for (int u = 0; u < kCompactPer; ++u) {
+        const int i = tid * kCompactPer + u;
         const int id = i < len ? in[i] : -1;
         const bool own = id >= 0 && (id / inter) % world == rank;
-        const unsigned m = __ballot_sync(0xffffffffu, own);
-        if (own) out[cnt + __popc(m & ((1u << lane) - 1u))] = (id / inter / world) * inter + id % inter;
-        cnt += __popc(m);
+        loc[u] = own ? (id / inter / world) * inter + id % inter : -1;
+        c += own;
     }
-    __syncwarp();
-    for (int i = cnt + lane; i < k; i += 32) out[i] = -1;
-    if (lane == 0) local_len[t] = cnt;
+    // exclusive prefix of the owned counts over the block
+    int x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();  // every slot has been read
+    int before = x - c, total = 0;
+#pragma unroll
+    for (int w = 0; w < kCompactThreads / 32; ++w) {
+        before += w < warp ? wsum[w] : 0;
+        total += wsum[w];
+    }
+#pragma unroll
+    for (int u = 0; u < kCompactPer; ++u)
+        if (loc[u] >= 0) out[before++] = loc[u];
+    for (int i = total + tid; i < k; i += kCompactThreads) out[i] = -1;
+    if (tid == 0) local_len[t] = total;
 }
 
 // ---------------------------------------------------------------------------
@@ -373,8 +394,8 @@ cudaError_t launch_topk_compact(const int32_t* idx, const int32_t* topk_len, int
                                 int inter, int32_t* local_idx, int32_t* local_len, int32_t* d_status,
                                 cudaStream_t stream) {
     if (num_q <= 0) return cudaSuccess;
-    return launch_pdl(topk_compact_kernel, dim3((unsigned)((num_q + 3) / 4)), dim3(128), 0, stream, 1, idx,
-                      topk_len, num_q, k, world, rank, inter, local_idx, local_len, d_status);
+    return launch_pdl(topk_compact_kernel, dim3((unsigned)num_q), dim3(kCompactThreads), 0, stream, 1, idx, topk_len,
+                      num_q, k, world, rank, inter, local_idx, local_len, d_status);
 }
 
 cudaError_t launch_lse_combine(const void* const* o_parts, const float* const* lse_parts, int num_parts, int num_q,
