@@ -244,6 +244,64 @@ def test_topk_rows_in_shared_memory(seed):
         assert np.array_equal(idx[t], np.sort(ref[:m])), f"row {t}"
 
 
+def test_topk_rows_narrow_key_range():
+    """Rows whose scores span a few ulps (the digits of the selection then
+    have 1 to 3 significant bits): two adjacent floats, five adjacent floats
+    with ties across the boundary, and one key above a row of equal keys."""
+    ctx_list = (20000, 30000, 17000)
+    wl = I.scaled(W["tiny"], num_seqs=3, ctx=None, ctx_list=ctx_list, queries_per_seq=1)
+    d, _ = _inputs_cpu_then_gpu(wl)
+    step = DecodeStep(d, wl.queries_per_seq, wl.topk)
+    ld = P.ld_of(step.seqs.max_ctx)
+    g = torch.Generator().manual_seed(5)
+    sc = torch.full((3, ld), float("nan"), dtype=torch.float32)
+    ulp = np.nextafter(np.float32(1.0), np.float32(2.0)) - np.float32(1.0)
+    n0, n1, n2 = ctx_list
+    sc[0, :n0] = 1.0 + float(ulp) * torch.randint(0, 2, (n0,), generator=g).float()
+    sc[1, :n1] = -3.0 + 2 * float(ulp) * torch.randint(0, 5, (n1,), generator=g).float()
+    sc[2, :n2] = 0.5
+    sc[2, 12345] = float(np.nextafter(np.float32(0.5), np.float32(1.0)))
+    dsa.dsa_topk(sc.to(DEV), ld, step.seqs, 3, wl.topk, step.idx, step.topk_len, step.ws, step.ws_bytes, step.status)
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+    idx, tlen = step.idx.cpu().numpy(), step.topk_len.cpu().numpy()
+    oracle = __import__("oracle")
+    for t, n in enumerate(ctx_list):
+        ref, m = oracle.topk(sc[t, :n].double().numpy(), wl.topk)
+        assert tlen[t] == m == wl.topk
+        assert np.array_equal(idx[t], np.sort(ref[:m])), f"row {t}"
+
+
+def test_topk_rows_top_keys_on_a_sparse_lattice():
+    """Rows of 16,385 to 32,768 keys whose largest scores sit on a sparse,
+    irregular lattice of positions (one key in 32: 1024 w + 4 l + 128 (l mod
+    8), w and l < 32), fewer than k of them, with a quarter of the row tied
+    just below: the oracle's exact top-k, ties to the smaller position."""
+    ctx_list = (32768, 20001)
+    wl = I.scaled(W["tiny"], num_seqs=2, ctx=None, ctx_list=ctx_list, queries_per_seq=1)
+    d, _ = _inputs_cpu_then_gpu(wl)
+    step = DecodeStep(d, wl.queries_per_seq, wl.topk)
+    ld = P.ld_of(step.seqs.max_ctx)
+    g = torch.Generator().manual_seed(11)
+    sc = torch.full((2, ld), float("nan"), dtype=torch.float32)
+    for r, n in enumerate(ctx_list):
+        v = torch.randn(n, generator=g)
+        v[torch.randint(0, n, (n // 4,), generator=g)] = 1.5  # ties below the sampled keys
+        sp = [1024 * w + 4 * l + 128 * (l % 8) for w in range(32) for l in range(32)]
+        sp = torch.tensor([q for q in sp if q < n])
+        v[sp] = 8.0 + torch.rand(len(sp), generator=g)
+        sc[r, :n] = v
+    dsa.dsa_topk(sc.to(DEV), ld, step.seqs, 2, wl.topk, step.idx, step.topk_len, step.ws, step.ws_bytes, step.status)
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+    idx, tlen = step.idx.cpu().numpy(), step.topk_len.cpu().numpy()
+    oracle = __import__("oracle")
+    for t, n in enumerate(ctx_list):
+        ref, m = oracle.topk(sc[t, :n].double().numpy(), wl.topk)
+        assert tlen[t] == m == wl.topk
+        assert np.array_equal(idx[t], np.sort(ref[:m])), f"row {t}"
+
+
 def test_fp8_index_keys_every_code_class():
     """e4m3 index keys of one sequence drawn from the subnormal codes (and
     zero) alone, of the other from every finite code: scores, selection and
