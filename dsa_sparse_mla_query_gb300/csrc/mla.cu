@@ -80,9 +80,11 @@ int mla_launches(int num_q, int k, size_t cap) {
 
 // LSE combine of the splits of one query ([vLLM-ML4] DCP: LSE combine):
 //   M = max_s m_s, out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
-// One block per (query, 4 heads).
+// One block per (query, 4 heads), one thread per 4 output dims, every
+// split's load of them in flight together.
 constexpr int kCombineHeads = 4;
-__global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restrict__ part_o,
+constexpr int kCombineThreads = kCombineHeads * kMV / 4;  // 512
+__global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const float* __restrict__ part_o,
                                                           const float* __restrict__ part_ml, int splits,
                                                           __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
     pdl_enter();
@@ -90,26 +92,33 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restric
     __shared__ float inv_l[kCombineHeads];
     const int t = blockIdx.x, h0 = blockIdx.y * kCombineHeads;
     const float* ml = part_ml + (int64_t)t * splits * kMH * 2;
-    if (threadIdx.x < kCombineHeads) {
-        const int h = h0 + threadIdx.x;
-        float M = -INFINITY;
-        for (int sp = 0; sp < splits; ++sp) M = fmaxf(M, ml[(sp * kMH + h) * 2]);
-        float L = 0.f;
-        for (int sp = 0; sp < splits; ++sp) {
-            const float m = ml[(sp * kMH + h) * 2];
-            const float wv = (M == -INFINITY) ? 0.f : exp2f(m - M);
-            wgt[threadIdx.x * 16 + sp] = wv;
-            L += wv * ml[(sp * kMH + h) * 2 + 1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < kCombineHeads) {  // warp hh: the weights of head h0 + hh, lane s those of split s
+        const int h = h0 + warp;
+        const bool has = lane < splits;
+        const float m = has ? ml[(lane * kMH + h) * 2] : -INFINITY;
+        const float l = has ? ml[(lane * kMH + h) * 2 + 1] : 0.f;
+        float M = m;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float wv = (!has || M == -INFINITY) ? 0.f : exp2f(m - M);
+        float L = wv * l;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        if (has) wgt[warp * 16 + lane] = wv;
+        if (lane == 0) {
+            inv_l[warp] = L > 0.f ? 1.f / L : 0.f;
+            if (lse) lse[(int64_t)t * kMH + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
         }
-        inv_l[threadIdx.x] = L > 0.f ? 1.f / L : 0.f;
-        if (lse) lse[(int64_t)t * kMH + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
     }
     __syncthreads();
     const float* po = part_o + (int64_t)t * splits * kMH * kMV + (int64_t)h0 * kMV;
     __nv_bfloat16* ot = out + (int64_t)t * kMH * kMV + (int64_t)h0 * kMV;
-    for (int e = threadIdx.x; e < kCombineHeads * kMV / 4; e += blockDim.x) {
+    {
+        const int e = threadIdx.x;
         const int hh = (e * 4) / kMV;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
         for (int sp = 0; sp < splits; ++sp) {
             const float wv = wgt[hh * 16 + sp];
             const float4 v = *reinterpret_cast<const float4*>(po + (int64_t)sp * kMH * kMV + e * 4);
@@ -904,7 +913,7 @@ cudaError_t launch_sparse_mla(const void* q, const void* latent, dsa_dtype laten
                    topk_len, k, scale_log2, g, splits, pair, reinterpret_cast<__nv_bfloat16*>(out), lse, ws.mla_part,
                    ws.mla_ml, d_status);
     if (e != cudaSuccess || splits == 1 || pair) return e;
-    return launch_pdl(mla_combine_kernel, dim3(num_q, kMH / kCombineHeads), dim3(128), 0, stream, 1, ws.mla_part,
+    return launch_pdl(mla_combine_kernel, dim3(num_q, kMH / kCombineHeads), dim3(kCombineThreads), 0, stream, 1, ws.mla_part,
                       ws.mla_ml, splits, reinterpret_cast<__nv_bfloat16*>(out), lse);
 }
 
