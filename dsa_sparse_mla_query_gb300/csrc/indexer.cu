@@ -46,7 +46,7 @@ template <>
 __device__ __forceinline__ float to_float<__half>(__half x) { return __half2float(x); }
 
 template <typename T>
-__global__ void __launch_bounds__(128) qprep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ w,
+__global__ void __launch_bounds__(kIH * 16) qprep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ w,
                                                     const float* __restrict__ ss, const float* __restrict__ sb,
                                                     const float* __restrict__ inv_freq, dsa_seqs s, int num_q,
                                                     T* __restrict__ qp, float* __restrict__ wp,
@@ -57,14 +57,15 @@ __global__ void __launch_bounds__(128) qprep_kernel(const __nv_bfloat16* __restr
     const int KP = rope ? 192 : 128;
     __shared__ float cs[32], sn[32], sgn[32], wsc[32];
     __shared__ int ok;
-    qprep_setup(w, ss, sb, inv_freq, s, t, cs, sn, sgn, wsc, &ok, d_status);
-    if (threadIdx.x < 32) wp[(int64_t)t * kIH + threadIdx.x] = wsc[threadIdx.x];
-    // one work item = 4 consecutive pairs (8 dims) of one head
+    // one thread = 4 consecutive pairs (8 dims) of one head, its load in
+    // flight during the per-query setup
     const __nv_bfloat16* qt = q + (int64_t)t * kIH * kID;
     T* out = qp + (int64_t)t * kIH * KP;
-    for (int e = threadIdx.x; e < kIH * 16; e += blockDim.x) {
-        const int h = e >> 4, c8 = e & 15;  // dims 8*c8 .. 8*c8+7
-        const uint4 raw = *reinterpret_cast<const uint4*>(qt + h * kID + c8 * 8);
+    const int h = threadIdx.x >> 4, c8 = threadIdx.x & 15;  // dims 8*c8 .. 8*c8+7
+    const uint4 raw = *reinterpret_cast<const uint4*>(qt + h * kID + c8 * 8);
+    qprep_setup(w, ss, sb, inv_freq, s, t, cs, sn, sgn, wsc, &ok, d_status);
+    if (threadIdx.x < 32) wp[(int64_t)t * kIH + threadIdx.x] = wsc[threadIdx.x];
+    {
         const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&raw);
         const float g = ok ? sgn[h] : 0.f;
         T* o = out + h * KP;
@@ -107,7 +108,7 @@ __global__ void __launch_bounds__(128) qprep_kernel(const __nv_bfloat16* __restr
 // 128-byte row per (query, part, head): the MMA's N rows.
 constexpr int kQParts = 3;  // e4m3 parts of q' (e4m3 index keys)
 
-__global__ void __launch_bounds__(128) qprep_e4m3_kernel(const __nv_bfloat16* __restrict__ q,
+__global__ void __launch_bounds__(kIH * 32) qprep_e4m3_kernel(const __nv_bfloat16* __restrict__ q,
                                                          const float* __restrict__ w, const float* __restrict__ ss,
                                                          const float* __restrict__ sb,
                                                          const float* __restrict__ inv_freq, dsa_seqs s, int num_q,
@@ -118,11 +119,12 @@ __global__ void __launch_bounds__(128) qprep_e4m3_kernel(const __nv_bfloat16* __
     const bool rope = inv_freq != nullptr;
     __shared__ float cs[32], sn[32], sgn[32], wsc[32];
     __shared__ int ok;
+    // warp h: head h; lane: dims 4 lane .. 4 lane + 3, i.e. rotation pairs 2
+    // lane and 2 lane + 1 (the load in flight during the per-query setup)
+    const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint2 raw = *reinterpret_cast<const uint2*>(q + ((int64_t)t * kIH + h) * kID + 4 * lane);
     qprep_setup(w, ss, sb, inv_freq, s, t, cs, sn, sgn, wsc, &ok, d_status);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int h = warp; h < kIH; h += 4) {
-        // lane: dims 4 lane .. 4 lane + 3, i.e. rotation pairs 2 lane and 2 lane + 1
-        const uint2 raw = *reinterpret_cast<const uint2*>(q + ((int64_t)t * kIH + h) * kID + 4 * lane);
+    {
         const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&raw);
         const float g = ok ? sgn[h] : 0.f;
         float y[4];
@@ -710,9 +712,9 @@ cudaError_t launch_index_scores(const void* q_idx, const float* w, const float* 
     const bool rope = inv_freq != nullptr;
     const __nv_bfloat16* qi = reinterpret_cast<const __nv_bfloat16*>(q_idx);
     cudaError_t e =
-        fp8 ? launch_pdl(qprep_e4m3_kernel, dim3(num_q), dim3(128), 0, stream, 1, qi, w, ssmax_s, ssmax_b, inv_freq, s,
+        fp8 ? launch_pdl(qprep_e4m3_kernel, dim3(num_q), dim3(kIH * 32), 0, stream, 1, qi, w, ssmax_s, ssmax_b, inv_freq, s,
                          num_q, reinterpret_cast<uint8_t*>(ws.qprep), ws.wprep, d_status)
-            : launch_pdl(qprep_kernel<__nv_bfloat16>, dim3(num_q), dim3(128), 0, stream, 1, qi, w, ssmax_s, ssmax_b,
+            : launch_pdl(qprep_kernel<__nv_bfloat16>, dim3(num_q), dim3(kIH * 16), 0, stream, 1, qi, w, ssmax_s, ssmax_b,
                          inv_freq, s, num_q, reinterpret_cast<__nv_bfloat16*>(ws.qprep), ws.wprep, d_status);
     if (e != cudaSuccess) return e;
     const int mq = s.max_q_per_seq;

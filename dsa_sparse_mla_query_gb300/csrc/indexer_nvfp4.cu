@@ -48,7 +48,7 @@ namespace dsa {
 //   split_n = 1: q' [Q, 64, 128], rows 0..31 the heads' hi parts over all 128
 //                dims, rows 32..63 their lo parts (zero on dims 64..127): the
 //                lo part extends N instead (RoPE layers, one query per chunk).
-__global__ void __launch_bounds__(128) qprep_f16_kernel(const __nv_bfloat16* __restrict__ q,
+__global__ void __launch_bounds__(kIH * 32) qprep_f16_kernel(const __nv_bfloat16* __restrict__ q,
                                                         const float* __restrict__ w, const float* __restrict__ ss,
                                                         const float* __restrict__ sb,
                                                         const float* __restrict__ inv_freq, dsa_seqs s, int num_q,
@@ -60,11 +60,12 @@ __global__ void __launch_bounds__(128) qprep_f16_kernel(const __nv_bfloat16* __r
     const int KP = rope ? 192 : 128;
     __shared__ float cs[32], sn[32], sgn[32], wsc[32];
     __shared__ int ok;
+    // warp h: head h; lane: dims 4 lane .. 4 lane + 3 (rotation pairs 2 lane,
+    // 2 lane + 1; the load in flight during the per-query setup)
+    const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint2 raw = *reinterpret_cast<const uint2*>(q + ((int64_t)t * kIH + h) * kID + 4 * lane);
     qprep_setup(w, ss, sb, inv_freq, s, t, cs, sn, sgn, wsc, &ok, d_status);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int h = warp; h < kIH; h += 4) {
-        // lane: dims 4 lane .. 4 lane + 3 (rotation pairs 2 lane, 2 lane + 1)
-        const uint2 raw = *reinterpret_cast<const uint2*>(q + ((int64_t)t * kIH + h) * kID + 4 * lane);
+    {
         const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&raw);
         const float sg = ok ? sgn[h] : 0.f;
         const bool rot = rope && lane < 16;
@@ -103,7 +104,7 @@ __global__ void __launch_bounds__(128) qprep_f16_kernel(const __nv_bfloat16* __r
             *reinterpret_cast<uint2*>(o) = *reinterpret_cast<const uint2*>(hi);
             *reinterpret_cast<uint2*>(o + kIH * kID) = rot ? *reinterpret_cast<const uint2*>(lo) : make_uint2(0, 0);
             if (lane == 0) wp[(int64_t)t * kIH + h] = ldexpf(wsc[h] * g, e);
-            continue;
+            return;
         }
         __half* o = qp + ((int64_t)t * kIH + h) * KP;
         if (rot) {
@@ -608,7 +609,7 @@ cudaError_t launch_index_scores_nvfp4(const void* q_idx, const float* w, const f
     __half* qp = reinterpret_cast<__half*>(ws.qprep);
     const int mq = s.max_q_per_seq;
     const int split_n = Nv4Cfg<1, 192>::split_n && rope && mq <= 1;  // the layout the kernel below reads
-    cudaError_t e = launch_pdl(qprep_f16_kernel, dim3(num_q), dim3(128), 0, stream, 1,
+    cudaError_t e = launch_pdl(qprep_f16_kernel, dim3(num_q), dim3(kIH * 32), 0, stream, 1,
                                reinterpret_cast<const __nv_bfloat16*>(q_idx), w, ssmax_s, ssmax_b, inv_freq, s, num_q,
                                k_global, split_n, qp, ws.wprep, d_status);
     if (e != cudaSuccess) return e;
