@@ -201,9 +201,12 @@ def measured_tensor_peak():
     return 1700.0, "fallback sustained bf16"
 
 
-def indexer_traffic(wl_name: str):
+def indexer_traffic(wl_name: str, alg_bytes: int):
     """dram bytes per launch of the indexer kernel from the committed ncu
-    summary, if the kernel sources still hash the same; else None."""
+    summary, if the kernel sources still hash the same; else None.  The
+    summary holds full-size launches; a launch of another size (fewer
+    sequences) scales by its algorithmic bytes, as the captures themselves
+    were scaled (traffic grows with the keys scanned)."""
     p = os.path.join(ROOT, "profiles", "indexer_traffic.json")
     if not os.path.exists(p):
         return None
@@ -211,7 +214,10 @@ def indexer_traffic(wl_name: str):
         j = json.load(f)
     if j.get("source_sha256") != kernel_source_hash() or wl_name not in j.get("per_launch_bytes", {}):
         return None
-    return j["per_launch_bytes"][wl_name]
+    full = j.get("algorithmic_bytes_per_launch", {}).get(wl_name)
+    if not full:
+        return None
+    return int(round(j["per_launch_bytes"][wl_name] * alg_bytes / full))
 
 
 def kernel_source_hash() -> str:
@@ -407,7 +413,7 @@ def run_ours(args, wl, ws, rank, local):
     ab = algorithmic_bytes(wl, lay)
     peak, peak_kind = measured_peaks()
     achieved = ab["indexer"] / (idx_ms / 1000.0) / 1e9
-    traffic = indexer_traffic(wl.name)
+    traffic = indexer_traffic(wl.name, ab["indexer"])
     # The indexer's bound: its bytes at the copy bandwidth or its q.k flops at
     # the tensor peak, whichever takes longer (the prefill chunk's 4096 queries
     # share every key, which makes it a dense contraction).

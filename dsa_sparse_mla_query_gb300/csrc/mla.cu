@@ -219,10 +219,11 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, bool& over) {
 //   warps 10-17 gather the tile's rows: 16-byte loads, 18 per thread in flight,
 //               stored into the 128-byte-swizzled K-major layout (two stages);
 //               random 1,152-byte rows stream fastest this way on GB300;
-//   warp 1      issues tcgen05.mma: S^T = K Q^T (M = 64 keys, N = 64 heads,
-//               K = 576; key r lands in TMEM lane 32 (r / 16) + r % 16) and
-//               O^T += V^T P^T (M = 128 value dims per block, N = 64 heads,
-//               K = 64 keys; V^T is the same gathered tile read MN-major);
+//   warp 1      issues S^T = K Q^T on the tensor cores (M = 64 keys, N = 64
+//               heads, K = 576; key r lands in TMEM lane 32 (r / 16) + r % 16);
+//   warp 18     issues O^T += V^T P^T (M = 128 value dims per block, N = 64
+//               heads, K = 64 keys; V^T is the same gathered tile read
+//               MN-major), each product as soon as its P^T is written;
 //   warps 2-9   softmax, two warps per TMEM lane quarter (16 keys), each with
 //               32 of the heads, straight from TMEM: exact per-head maxima of
 //               the first tile set the running max; later tiles only check
@@ -245,9 +246,10 @@ constexpr uint32_t kOCol = 0;              // O^T: 4 blocks x 64 heads
 constexpr uint32_t kSCol = 256;            // S^T: 2 buffers x 64 heads
 constexpr uint32_t kLCol = 384;            // row sums: lanes = keys, columns = heads
 constexpr uint32_t kTmemCols = 512;
-constexpr int kThreads = 576;              // 18 warps
+constexpr int kThreads = 608;              // 19 warps
 constexpr int kGatherWarps = 8;
 constexpr int kSoftWarps = 8;
+constexpr int kPvWarp = 2 + kSoftWarps + kGatherWarps;  // 18: issues O^T += V^T P^T
 constexpr int kRing = 3;                   // resolved-row ring depth
 constexpr int kBf16Rows = 0, kDsMlaRows = 1, kNvfp4Rows = 2;  // latent cache kinds
 constexpr int kNvRow = kMD / 2;            // NVFP4 code bytes per row (288)
@@ -385,15 +387,52 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(rfull + r);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && ntiles > 0) {
+    } else if (warp == 1 || warp == kPvWarp) {
+        // ------------------------------------------------------------ MMA issuers
+        // Two threads issue the tensor-core work, each in its own order: warp
+        // 1 the scores S^T of every tile, warp 18 the products O^T += V^T P^T.
+        // A thread issuing MMAs is held ~60 cycles per instruction whatever
+        // its size, while a 64 x 64 x 16 MMA keeps the pipe only a fraction of
+        // that: with two issuers the product of tile i goes in as soon as its
+        // P^T is written, not behind S^T of tile i+1, and the stage it frees
+        // reaches the gather of tile i+2 that much sooner.  Each thread's
+        // commits track its own MMAs; the product of tile i follows S^T of tile
+        // i (its P^T needs those scores), so its commits release the stage.
+        if (lane == 0 && ntiles > 0 && warp == 1) {
             constexpr uint32_t idesc_s = ptx::idesc_f16(64, kMH, !F16);
-            constexpr uint32_t idesc_pv = ptx::idesc_f16(128, kMH, !F16, true, true);
             const uint32_t qb = smem_u32(qs);
+            // S^T of a tile in two parts, blocks 0-3 then 4-8, each as soon as
+            // that half of the tile is stored
+            auto issue_s = [&](int st, int kb0, int kb1) {
+                ptx::tc_fence_after();
+                const uint32_t kbase = smem_u32(stage + st * kStage);
+#pragma unroll
+                for (int kb = kb0; kb < kb1; ++kb)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t ad = ptx::sdesc_sw128(kbase + kb * kKBlock + ks * 32);
+                        const uint64_t bd = ptx::sdesc_sw128(qb + kb * kMH * 128 + ks * 32);
+                        ptx::mma_ss(tmem + kSCol + st * kMH, ad, bd, idesc_s, (kb > 0 || ks > 0) ? 1u : 0u);
+                    }
+            };
             bool ok = ptx::mbar_wait(F16 ? qconv : qfull, 0, abort_flag, d_status);
-            auto issue_pv = [&](int i) -> bool {  // O^T += V^T P^T for tile i
-                if (!ptx::mbar_wait(pfull + (i & 1), (i >> 1) & 1, abort_flag, d_status)) return false;
+            for (int i = 0; ok && i < ntiles; ++i) {
+                const int st = i & 1;
+                const uint32_t ph = (i >> 1) & 1;
+                // the S^T buffer read by the softmax two tiles back, then each half stored
+                ok = (i < 2 || ptx::mbar_wait(sempty + st, ph ^ 1, abort_flag, d_status)) &&
+                     ptx::mbar_wait(kfull + st, ph, abort_flag, d_status);
+                if (!ok) break;
+                issue_s(st, 0, 4);
+                if (!(ok = ptx::mbar_wait(kfull + 2 + st, ph, abort_flag, d_status))) break;
+                issue_s(st, 4, KB);
+                ptx::mma_commit(sfull + st);
+            }
+        } else if (lane == 0 && ntiles > 0) {
+            constexpr uint32_t idesc_pv = ptx::idesc_f16(128, kMH, !F16, true, true);
+            bool ok = true;
+            for (int i = 0; ok && i < ntiles; ++i) {
+                if (!(ok = ptx::mbar_wait(pfull + (i & 1), (i >> 1) & 1, abort_flag, d_status))) break;
                 ptx::tc_fence_after();
                 const uint32_t kbase = smem_u32(stage + (i & 1) * kStage);
                 const uint32_t pb = kbase + 8 * kKBlock;
@@ -409,73 +448,8 @@ __global__ void __launch_bounds__(tcmla::kThreads, 1)
                 }
                 ptx::mma_commit(kempty + 2 + (i & 1));              // blocks 4-8 (with P^T) read
                 ptx::mma_commit(pvdone);
-                return true;
-            };
-            // S^T of a tile is issued as soon as its rows are stored and its TMEM
-            // buffer is free; O^T += V^T P^T as soon as its P^T is written.  The
-            // two streams interleave, so the scores of tile i+1 are computed
-            // while the softmax of tile i runs.  The barriers are probed without
-            // blocking: a blocking wait on one would miss the other completing.
-            // S^T of a tile in two parts, blocks 0-3 then 4-8, each as soon as
-            // that half of the tile is stored.
-            auto issue_s = [&](int st, int kb0, int kb1) {
-                ptx::tc_fence_after();
-                const uint32_t kbase = smem_u32(stage + st * kStage);
-#pragma unroll
-                for (int kb = kb0; kb < kb1; ++kb)
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t ad = ptx::sdesc_sw128(kbase + kb * kKBlock + ks * 32);
-                        const uint64_t bd = ptx::sdesc_sw128(qb + kb * kMH * 128 + ks * 32);
-                        ptx::mma_ss(tmem + kSCol + st * kMH, ad, bd, idesc_s, (kb > 0 || ks > 0) ? 1u : 0u);
-                    }
-            };
-            int s_next = 0, s_half = 0, pv_next = 0;
-            ptx::WaitClock idle;  // time without progress
-            while (ok && pv_next < ntiles) {
-                bool progressed = false;
-                if (s_next < ntiles) {
-                    const int st = s_next & 1;
-                    const uint32_t ph = (s_next >> 1) & 1;
-                    if (s_half == 0 && ptx::mbar_test_wait(kfull + st, ph) &&
-                        (s_next < 2 || ptx::mbar_test_wait(sempty + st, ph ^ 1))) {
-                        issue_s(st, 0, 4);
-                        s_half = 1;
-                        progressed = true;
-                    }
-                    if (s_half == 1 && ptx::mbar_test_wait(kfull + 2 + st, ph)) {
-                        issue_s(st, 4, KB);
-                        ptx::mma_commit(sfull + st);
-                        s_half = 0;
-                        ++s_next;
-                        progressed = true;
-                    }
-                }
-                // P^T-ready is double-buffered: the softmax warps can complete the
-                // next tile's phase before this loop sees the current one's
-                if (pv_next < s_next && ptx::mbar_test_wait(pfull + (pv_next & 1), (pv_next >> 1) & 1)) {
-                    if (!issue_pv(pv_next)) {
-                        ok = false;
-                        break;
-                    }
-                    ++pv_next;
-                    progressed = true;
-                }
-                if (progressed) {
-                    idle.reset();
-                } else {
-                    // bounded idle: give up after the wait limit like every other wait
-                    if (idle.expired(ptx::kWaitTimeoutNs) || *abort_flag) {
-                        if (!*abort_flag) {
-                            *abort_flag = 1;
-                            report(d_status, ptx::timeout_code(abort_flag, ptx::kLoopSite));
-                        }
-                        ok = false;
-                    }
-                    __nanosleep(32);
-                }
             }
-            if (ok) ptx::mma_commit(ofull);
+            if (ok) ptx::mma_commit(ofull);  // every product complete (the last follows every S^T)
         }
     } else if (warp >= 2 + kSoftWarps) {
         // ------------------------------------------------------------ gather
