@@ -456,6 +456,7 @@ constexpr int kStreamThreads = 1024;
 constexpr int kStreamEPT = 16;
 constexpr int kStreamBlock = kStreamThreads * kStreamEPT;  // 16384 keys
 constexpr int kStreamCand = 8192;                           // keys of d0 a CTA lists
+constexpr int kSampleBlocks = 4;                            // blocks a CTA needs for the sampled pass
 constexpr int kStreamMaxP = 8;
 // h [4][2048], hs [2048], ck/cp [kStreamCand], ap [2048], sel [2048]
 constexpr size_t kStreamSmem = (size_t)(5 * 2048 + 2 * kStreamCand + 2 * DSA_MAX_TOPK) * 4;
@@ -566,73 +567,153 @@ __global__ void __launch_bounds__(kStreamThreads, 1) topk_stream_kernel(const fl
     const int nblk = (n + kStreamBlock - 1) / kStreamBlock;
     const int b0 = (int)((int64_t)nblk * me / P), b1 = (int)((int64_t)nblk * (me + 1) / P);  // this CTA's blocks
     uint32_t u[kStreamEPT];
+    int d0 = 0, na = 0, nc = 0, remaining = k;  // na, nc: this CTA's so far (the same in every thread)
+    uint32_t prefix = 0, mask = 0;
+    bool over = false;
 
-    // ---- 1: the first digit over the row
-    for (int i = tid; i < 4 * 2048; i += NT) h[i] = 0;
-    __syncthreads();
-    {
-        int* hw = h + (warp & 3) * 2048;  // four copies spread the same-address atomics
+    // ---- 0: one pass, when a sample allows: every CTA samples one key per
+    // thread over its range; the cluster's sample histogram gives the first
+    // digit holding its (mu + 4 sqrt(mu) + 2)-th largest key, mu = the number
+    // of sampled keys expected among the top k; each CTA then lists every key
+    // of that digit or above, with its position, in position order.  When the
+    // lists fit and hold at least k keys (the row's k-th key is then theirs),
+    // three digit passes over them pin the k-th key; otherwise steps 1-2 run.
+    // Only CTAs with kSampleBlocks blocks or more sample: over fewer, the
+    // second pass of steps 1-2 reads blocks still in L2, and the sample's
+    // fixed costs (scattered loads, a digit selection, one more pass over a
+    // longer list) outweigh it.  (nblk and P are the cluster's: uniform.)
+    bool sampled = false;
+    if (nblk >= kSampleBlocks * P) {
+        for (int i = tid; i < 2048; i += NT) h[i] = 0;
+        const int j_lo = b0 * kStreamBlock, j_hi = min(b1 * kStreamBlock, n);
+        const bool has = j_hi > j_lo;
+        const int sp = has ? j_lo + (int)((int64_t)(j_hi - j_lo) * tid / NT) : 0;
+        const uint32_t sk = has ? order_key(__ldg(row + sp)) : 0u;
+        __syncthreads();
+        if (has) atomicAdd(h + (sk >> 21), 1);
+        const int ns_me = __syncthreads_count(has);
+        if (tid == 0) xch[0] = ns_me;
+        cl.sync();  // every CTA's sample histogram and count
+        cluster_hist_sum(cl, h, hs, P);
+        int ns = 0;
+        for (int r = 0; r < P; ++r) ns += cl.map_shared_rank(xch, r)[0];
+        __syncthreads();
+        const float mu = (float)ns * (float)k / (float)n;
+        const int target = (int)ceilf(mu + 4.f * sqrtf(mu) + 2.f);
+        const bool try_list = ns >= target;  // the same in every CTA of the cluster
+        if (try_list) {
+            int dth, abv;
+            select_digit<NT>(hs, 2048, target, buf, sh, dth, abv);
+            const uint32_t thr = (uint32_t)dth << 21;
+            for (int blk = b0; blk < b1; ++blk) {
+                const int j0 = blk * kStreamBlock;
+                stream_block(row, last4, j0, u);
+                int cc = 0;
+#pragma unroll
+                for (int e = 0; e < kStreamEPT; ++e) cc += stream_pos(j0, e) < n && u[e] >= thr;
+                int tot;
+                int oc = nc + scan_threads<NT>(cc, buf, &tot);
+#pragma unroll
+                for (int e = 0; e < kStreamEPT; ++e) {
+                    const int p = stream_pos(j0, e);
+                    if (p < n && u[e] >= thr) {
+                        if (oc < kStreamCand) {
+                            ck[oc] = u[e];
+                            cp[oc] = p;
+                        }
+                        ++oc;
+                    }
+                }
+                nc += tot;
+            }
+        }
+        // (also: every CTA is done with the others' sample histograms)
+        if (tid == 0) {
+            xch[1] = nc;
+            xch[2] = nc > kStreamCand;
+        }
+        cl.sync();
+        int total = 0;
+        bool ovf = false;
+        for (int r = 0; r < P; ++r) {
+            const int* x = cl.map_shared_rank(xch, r);
+            total += x[1];
+            ovf |= x[2] != 0;
+        }
+        sampled = try_list && !ovf && total >= k;
+    }
+    if (!sampled) {
+        nc = 0;
+        // ---- 1: the first digit over the row
+        for (int i = tid; i < 4 * 2048; i += NT) h[i] = 0;
+        __syncthreads();
+        {
+            int* hw = h + (warp & 3) * 2048;  // four copies spread the same-address atomics
+            for (int blk = b0; blk < b1; ++blk) {
+                const int j0 = blk * kStreamBlock;
+                stream_block(row, last4, j0, u);
+    #pragma unroll
+                for (int e = 0; e < kStreamEPT; ++e)
+                    if (stream_pos(j0, e) < n) atomicAdd(hw + (u[e] >> 21), 1);
+            }
+        }
+        __syncthreads();
+        for (int i = tid; i < 2048; i += NT) h[i] += h[2048 + i] + h[4096 + i] + h[6144 + i];
+        cl.sync();
+        cluster_hist_sum(cl, h, hs, P);
+        __syncthreads();
+        int above;
+        select_digit<NT>(hs, 2048, k, buf, sh, d0, above);
+        prefix = (uint32_t)d0 << 21;
+        mask = 0x7FFu << 21;
+        remaining = k - above;
+
+        // ---- 2: the positions above d0 and the keys of d0, ascending
+        na = 0;
+        nc = 0;  // this CTA's so far (the same in every thread)
         for (int blk = b0; blk < b1; ++blk) {
             const int j0 = blk * kStreamBlock;
             stream_block(row, last4, j0, u);
-#pragma unroll
-            for (int e = 0; e < kStreamEPT; ++e)
-                if (stream_pos(j0, e) < n) atomicAdd(hw + (u[e] >> 21), 1);
-        }
-    }
-    __syncthreads();
-    for (int i = tid; i < 2048; i += NT) h[i] += h[2048 + i] + h[4096 + i] + h[6144 + i];
-    cl.sync();
-    cluster_hist_sum(cl, h, hs, P);
-    __syncthreads();
-    int d0, above;
-    select_digit<NT>(hs, 2048, k, buf, sh, d0, above);
-    uint32_t prefix = (uint32_t)d0 << 21, mask = 0x7FFu << 21;
-    int remaining = k - above;
-
-    // ---- 2: the positions above d0 and the keys of d0, ascending
-    int na = 0, nc = 0;  // this CTA's so far (the same in every thread)
-    for (int blk = b0; blk < b1; ++blk) {
-        const int j0 = blk * kStreamBlock;
-        stream_block(row, last4, j0, u);
-        int ca = 0, cc = 0;
-#pragma unroll
-        for (int e = 0; e < kStreamEPT; ++e) {
-            const int dg = stream_pos(j0, e) < n ? (int)(u[e] >> 21) : -1;
-            ca += dg > d0;
-            cc += dg == d0;
-        }
-        int tot;
-        const int pk = scan_threads<NT>((ca << 16) | cc, buf, &tot);  // each at most 16384 per block
-        int oa = na + (pk >> 16), oc = nc + (pk & 0xFFFF);
-#pragma unroll
-        for (int e = 0; e < kStreamEPT; ++e) {
-            const int p = stream_pos(j0, e);
-            const int dg = p < n ? (int)(u[e] >> 21) : -1;
-            if (dg > d0) {
-                if (oa < DSA_MAX_TOPK) ap[oa] = p;
-                ++oa;
-            } else if (dg == d0) {
-                if (oc < kStreamCand) {
-                    ck[oc] = u[e];
-                    cp[oc] = p;
-                }
-                ++oc;
+            int ca = 0, cc = 0;
+    #pragma unroll
+            for (int e = 0; e < kStreamEPT; ++e) {
+                const int dg = stream_pos(j0, e) < n ? (int)(u[e] >> 21) : -1;
+                ca += dg > d0;
+                cc += dg == d0;
             }
+            int tot;
+            const int pk = scan_threads<NT>((ca << 16) | cc, buf, &tot);  // each at most 16384 per block
+            int oa = na + (pk >> 16), oc = nc + (pk & 0xFFFF);
+    #pragma unroll
+            for (int e = 0; e < kStreamEPT; ++e) {
+                const int p = stream_pos(j0, e);
+                const int dg = p < n ? (int)(u[e] >> 21) : -1;
+                if (dg > d0) {
+                    if (oa < DSA_MAX_TOPK) ap[oa] = p;
+                    ++oa;
+                } else if (dg == d0) {
+                    if (oc < kStreamCand) {
+                        ck[oc] = u[e];
+                        cp[oc] = p;
+                    }
+                    ++oc;
+                }
+            }
+            na += tot >> 16;
+            nc += tot & 0xFFFF;
         }
-        na += tot >> 16;
-        nc += tot & 0xFFFF;
+        if (tid == 0) xch[0] = nc > kStreamCand;
+        cl.sync();  // also: every CTA has summed the others' first histograms
+        over = false;  // some CTA's list of d0 overflowed: the finer digits come from the row
+        for (int r = 0; r < P; ++r) over |= cl.map_shared_rank(xch, r)[0] != 0;
     }
-    if (tid == 0) xch[0] = nc > kStreamCand;
-    cl.sync();  // also: every CTA has summed the others' first histograms
-    bool over = false;  // some CTA's list of d0 overflowed: the finer digits come from the row
-    for (int r = 0; r < P; ++r) over |= cl.map_shared_rank(xch, r)[0] != 0;
 
-    // ---- 3: two finer digits over the cluster's keys of d0
+    // ---- 3: the digits not yet pinned (the two finer ones after steps 1-2,
+    // all three over the sampled lists), over the cluster's lists
 #pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-        const int shift = pass == 0 ? 10 : 0;
-        const int nb = pass == 0 ? 2048 : 1024;
+    for (int pass = sampled ? 0 : 1; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int nb = pass == 2 ? 1024 : 2048;
         for (int i = tid; i < 2048; i += NT) h[i] = 0;
         __syncthreads();
         if (!over) {

@@ -211,6 +211,46 @@ def test_long_rows_all_equal_scores():
         assert np.array_equal(idx[t], np.arange(2048))
 
 
+def test_long_rows_sampled_threshold():
+    """Rows of 4 blocks (65,536 keys) or more per CTA of their cluster: each
+    CTA samples 1024 evenly spaced keys, lists the keys at or above the
+    sample's threshold digit in one pass and selects from the lists; the
+    selection falls back to two passes over the row when a list overflows or
+    the lists hold fewer than k keys.  Three rows of one launch (clusters of 8
+    CTAs): normal scores with a ragged last block (1,100,000 keys); equal
+    scores (every key listed: overflow); and 300 scores near 8 planted at
+    multiples of 128, where the evenly spaced sample of a 1,048,576-key row
+    lands, above normal scores (the sample's threshold passes 300 keys, fewer
+    than k).  Each row's selection is the oracle's."""
+    ctx = [1100000, 1048576, 1048576]
+    ctx_t = torch.tensor(ctx, dtype=torch.int32, device=DEV)
+    qs = torch.arange(len(ctx) + 1, dtype=torch.int32, device=DEV)
+    qp = torch.tensor([c - 1 for c in ctx], dtype=torch.int32, device=DEV)
+    base = torch.tensor(np.concatenate([[0], np.cumsum(ctx)[:-1]]), dtype=torch.int64, device=DEV)
+    seqs = dsa.Seqs(ctx_t, qs, qp, max_ctx=max(ctx), max_q_per_seq=1, num_rows=sum(ctx), seq_base=base)
+    k, Q, ld = 2048, len(ctx), P.ld_of(max(ctx))
+    g = torch.Generator().manual_seed(17)
+    sc = torch.full((Q, ld), float("nan"), dtype=torch.float32)
+    sc[0, : ctx[0]] = torch.randn(ctx[0], generator=g)
+    sc[1, : ctx[1]] = 0.25
+    v = torch.randn(ctx[2], generator=g)
+    planted = 128 * torch.randperm(ctx[2] // 128, generator=g)[:300]
+    v[planted] = 8.0 + torch.rand(300, generator=g)
+    sc[2, : ctx[2]] = v
+    idx = torch.empty(Q, k, dtype=torch.int32, device=DEV)
+    tlen = torch.empty(Q, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    dsa.dsa_topk(sc.to(DEV), ld, seqs, Q, k, idx, tlen, None, 0, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    idx, tlen = idx.cpu().numpy(), tlen.cpu().numpy()
+    oracle = __import__("oracle")
+    for t, n in enumerate(ctx):
+        ref, m = oracle.topk(sc[t, :n].double().numpy(), k)
+        assert tlen[t] == m == k
+        assert np.array_equal(idx[t], np.sort(ref[:m])), f"row {t}"
+
+
 @pytest.mark.parametrize("seed", [0, 1])
 def test_topk_rows_in_shared_memory(seed):
     """Rows of 16,385 to 32,768 keys (one CTA per row, the row in shared
